@@ -1,0 +1,60 @@
+"""The seeded input generator: determinism, distributions, layouts of the workloads."""
+import numpy as np
+import torch
+
+import synth
+
+
+def test_counter_based_determinism_and_prefix_stability():
+    a = synth.normal_f32(0, 5, 1000)
+    b = synth.normal_f32(0, 5, 10)
+    np.testing.assert_array_equal(a[:10], b)
+    assert not np.array_equal(synth.normal_f32(0, 6, 10), b)
+    assert not np.array_equal(synth.normal_f32(1, 5, 10), b)
+
+
+def test_normal_moments():
+    x = synth.normal_f32(0, 1, 400_000).astype(np.float64)
+    assert abs(x.mean()) < 0.01 and abs(x.std() - 1) < 0.01
+
+
+def test_bf16_patterns_are_round_to_nearest_even_of_fp32():
+    f = synth.normal_f32(3, 4, 50_000, 0.0, 0.02)
+    u = synth.normal_bf16(3, 4, 50_000, 0.0, 0.02)
+    ref = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(u, ref)
+
+
+def test_exponential_variates():
+    e = synth.exponential_f32(0, 0, 400_000).astype(np.float64)
+    assert e.min() > 0 and abs(e.mean() - 1) < 0.01 and abs(e.var() - 1) < 0.02
+
+
+def test_expo_layout_frames_are_a_prefix():
+    a = synth.expo(2, 0, 8)
+    b = synth.expo(2, 0, 3, first_frame=5)
+    assert a.shape == (8, 11, 30)
+    np.testing.assert_array_equal(a[5:], b)
+
+
+def test_prompt_construction():
+    d = synth.CONFIGS["tiny"]["dims"]
+    p = synth.prompt("tiny")
+    assert p.shape == (32, 5)
+    assert (p[:24, 0] < d["sem_begin"]).all() and (p[:24, 1:] == 0).all()
+    assert ((p[24:, 0] >= d["sem_begin"]) & (p[24:, 0] <= d["sem_end"])).all()
+    assert (p[24:, 1:] < d["codebook_size"]).all()
+    f = synth.prompt("frame")
+    assert f.shape == (512, 11) and (f[:384, 0] < 151678).all() and (f[384:, 0] >= 151678).all()
+    lens = synth.prompt_lengths("serving")
+    assert len(lens) == 32 and min(lens) >= 512 and max(lens) <= 4096
+
+
+def test_weight_table():
+    d = synth.CONFIGS["tiny"]["dims"]
+    specs = synth.weight_specs(d)
+    assert len(specs) == 3 + 9 * d["n_layer"] + 4 + 9 * d["fast_n_layer"]
+    assert specs[0][0] == "embeddings" and specs[3][0] == "layers.0.attention_norm"
+    assert specs[4][1] == ((4 + 2 * 2) * 64, 256)
+    w = synth.make_weights(d)
+    assert w[2].dtype == np.float32 and (w[2] == 1).all()
