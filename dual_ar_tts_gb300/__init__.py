@@ -1,0 +1,271 @@
+"""GB300 (sm_103a) Dual-AR frame decoder for S2-Pro — thin Python binding of ``libs2frame.so``.
+
+The functions named ``s2_*`` mirror the C ABI in ``include/s2frame.h`` one to one and only
+marshal arguments; every step of the decode runs in the library's CUDA kernels.  PyTorch is
+used for device memory and streams.  There is no CPU fallback: if the CUDA library is missing
+or no GPU is present, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libs2frame.so")
+
+S2_F32, S2_BF16, S2_F16 = 0, 1, 2
+S2_OK, S2_EINVAL, S2_ENOMEM, S2_ECAPACITY, S2_ECUDA, S2_ETIMEOUT, S2_ESTATE = range(7)
+STATUS_NAMES = {0: "S2_OK", 1: "S2_EINVAL", 2: "S2_ENOMEM", 3: "S2_ECAPACITY", 4: "S2_ECUDA", 5: "S2_ETIMEOUT",
+                6: "S2_ESTATE"}
+
+EXPORTS = ("s2_weight_count", "s2_weight_info", "s2_frame_workspace_bytes", "s2_frame_init", "s2_prefill",
+           "s2_decode_frames", "s2_fast_logits", "s2_sync_status", "s2_set_spin_limit", "s2_frame_free",
+           "s2_last_error")
+
+
+class s2_dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("dim", "n_layer", "n_head", "n_kv_head", "head_dim", "ffn", "vocab",
+                                            "sem_begin", "sem_end", "im_end", "n_codebooks", "codebook_size")] + \
+               [(n, ctypes.c_float) for n in ("sem_scale", "norm_eps", "rope_base")] + \
+               [(n, ctypes.c_int) for n in ("qk_norm", "rope_table_bf16", "fast_dim", "fast_n_layer", "fast_n_head",
+                                            "fast_n_kv_head", "fast_head_dim", "fast_ffn", "fast_window",
+                                            "has_fast_project_in", "weight_dtype", "kv_dtype")]
+
+
+class s2_sampling(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("top_p", ctypes.c_float), ("ras_temperature", ctypes.c_float),
+                ("ras_top_p", ctypes.c_float), ("top_k", ctypes.c_int), ("ras_window", ctypes.c_int),
+                ("min_tokens_before_end", ctypes.c_int), ("max_frames", ctypes.c_int)]
+
+
+class s2_debug_taps(ctypes.Structure):
+    _fields_ = [("main_logits", ctypes.c_void_p), ("fast_logits", ctypes.c_void_p), ("hidden", ctypes.c_void_p),
+                ("draws", ctypes.c_void_p)]
+
+
+class S2Error(RuntimeError):
+    def __init__(self, fn, code, msg):
+        super().__init__(f"{fn} -> {STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load the CUDA library (build it first with ``dual_ar_tts_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_size_t
+    P = ctypes.POINTER
+    sig = {
+        "s2_weight_count": (i32, [P(s2_dims)]),
+        "s2_weight_info": (i64, [P(s2_dims), i32, ctypes.c_char_p, i32]),
+        "s2_frame_workspace_bytes": (sz, [P(s2_dims), i32, i32]),
+        "s2_frame_init": (i32, [P(s2_dims), P(vp), i32, vp, sz, i32, i32, P(vp)]),
+        "s2_prefill": (i32, [vp, i32, P(i32), vp, P(i32), vp]),
+        "s2_decode_frames": (i32, [vp, i32, P(i32), i32, P(s2_sampling), vp, vp, vp, vp, P(s2_debug_taps), vp]),
+        "s2_fast_logits": (i32, [vp, i32, vp, vp, vp, vp]),
+        "s2_sync_status": (i32, [vp, vp]),
+        "s2_set_spin_limit": (i32, [vp, i64]),
+        "s2_frame_free": (i32, [vp]),
+        "s2_last_error": (ctypes.c_char_p, [vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(fn, rc, ctx=None):
+    if rc != S2_OK:
+        raise S2Error(fn, rc, load().s2_last_error(ctx).decode())
+    return rc
+
+
+def _ints(seq):
+    arr = (ctypes.c_int * len(seq))(*[int(v) for v in seq])
+    return arr
+
+
+# ------------------------------------------------------------------ the C ABI
+
+def make_dims(d: dict) -> s2_dims:
+    s = s2_dims()
+    for name, _ in s2_dims._fields_:
+        setattr(s, name, d[name])
+    return s
+
+
+def s2_weight_count(dims: s2_dims) -> int:
+    return load().s2_weight_count(ctypes.byref(dims))
+
+
+def s2_weight_info(dims: s2_dims, i: int):
+    buf = ctypes.create_string_buffer(128)
+    n = load().s2_weight_info(ctypes.byref(dims), i, buf, 128)
+    return buf.value.decode(), n
+
+
+def s2_frame_workspace_bytes(dims: s2_dims, max_streams: int, kv_slots: int) -> int:
+    return load().s2_frame_workspace_bytes(ctypes.byref(dims), max_streams, kv_slots)
+
+
+def s2_frame_init(dims: s2_dims, weight_ptrs, workspace_ptr: int, ws_bytes: int, max_streams: int, kv_slots: int):
+    n = len(weight_ptrs)
+    arr = (ctypes.c_void_p * n)(*[p if p else None for p in weight_ptrs])
+    out = ctypes.c_void_p()
+    rc = load().s2_frame_init(ctypes.byref(dims), arr, n, workspace_ptr, ws_bytes, max_streams, kv_slots,
+                              ctypes.byref(out))
+    _check("s2_frame_init", rc, None)
+    return out.value
+
+
+def s2_prefill(ctx, stream_ids, tokens_ptr: int, lengths, stream: int = 0):
+    rc = load().s2_prefill(ctx, len(stream_ids), _ints(stream_ids), tokens_ptr, _ints(lengths), stream)
+    return _check("s2_prefill", rc, ctx)
+
+
+def s2_decode_frames(ctx, stream_ids, n_frames: int, params, expo_ptr: int, forced_ptr: int | None, codes_ptr: int,
+                     n_out_ptr: int, taps: s2_debug_taps | None = None, stream: int = 0):
+    n = len(stream_ids)
+    arr = (s2_sampling * n)(*params)
+    rc = load().s2_decode_frames(ctx, n, _ints(stream_ids), n_frames, arr, expo_ptr, forced_ptr, codes_ptr, n_out_ptr,
+                                 ctypes.byref(taps) if taps is not None else None, stream)
+    return _check("s2_decode_frames", rc, ctx)
+
+
+def s2_fast_logits(ctx, n_frames: int, hidden_ptr: int, prefix_ptr: int, logits_ptr: int, stream: int = 0):
+    rc = load().s2_fast_logits(ctx, n_frames, hidden_ptr, prefix_ptr, logits_ptr, stream)
+    return _check("s2_fast_logits", rc, ctx)
+
+
+def s2_sync_status(ctx, stream: int = 0) -> int:
+    return load().s2_sync_status(ctx, stream)
+
+
+def s2_set_spin_limit(ctx, limit: int):
+    return _check("s2_set_spin_limit", load().s2_set_spin_limit(ctx, limit), ctx)
+
+
+def s2_frame_free(ctx):
+    return load().s2_frame_free(ctx)
+
+
+def s2_last_error(ctx=None) -> str:
+    return load().s2_last_error(ctx).decode()
+
+
+def make_sampling(s: dict) -> s2_sampling:
+    return s2_sampling(s["temperature"], s["top_p"], s["ras_temperature"], s["ras_top_p"], s["top_k"],
+                       s["ras_window"], s["min_tokens_before_end"], s.get("max_frames", 0))
+
+
+# ------------------------------------------------------- memory-owning helper
+
+class Decoder:
+    """Owns the device workspace (a torch tensor) and the weight tensors for one context."""
+
+    def __init__(self, d: dict, weights, max_streams: int = 1, kv_slots: int = 0, device: str = "cuda"):
+        import torch
+        if not torch.cuda.is_available():
+            raise RuntimeError("the frame decoder needs a CUDA GPU")
+        load()
+        self.d = d
+        self.dims = make_dims(d)
+        self.weights = weights          # torch device tensors (or None), table order
+        ptrs = [w.data_ptr() if w is not None else 0 for w in weights]
+        nbytes = s2_frame_workspace_bytes(self.dims, max_streams, kv_slots)
+        if nbytes == 0:
+            raise S2Error("s2_frame_workspace_bytes", S2_EINVAL, s2_last_error(None))
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.ctx = s2_frame_init(self.dims, ptrs, self.workspace.data_ptr(), nbytes, max_streams, kv_slots)
+        self.max_streams = max_streams
+        self.kv_slots = kv_slots
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            s2_frame_free(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def stream(self):
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+
+    def prefill(self, prompts, stream_ids=None):
+        """prompts: list of [T][NCB+1] int32 arrays/tensors (host or device)."""
+        import torch
+        ids = list(range(len(prompts))) if stream_ids is None else list(stream_ids)
+        toks = torch.cat([torch.as_tensor(p, dtype=torch.int32).reshape(-1) for p in prompts]).cuda()
+        lens = [int(torch.as_tensor(p).shape[0]) for p in prompts]
+        s2_prefill(self.ctx, ids, toks.data_ptr(), lens, self.stream())
+        self._keep = toks
+        return toks
+
+    def decode(self, n_frames, sampling, expo, forced=None, stream_ids=None, taps=False):
+        """expo: [n][n_frames][11][30] float32 (device tensor); forced: optional [n][n_frames][11] int32.
+        Returns dict of device tensors (codes, n_out and, with taps, the debug outputs)."""
+        import torch
+        n = expo.shape[0]
+        ids = list(range(n)) if stream_ids is None else list(stream_ids)
+        d = self.d
+        dev = expo.device
+        codes = torch.zeros((n, d["n_codebooks"] * n_frames), dtype=torch.int32, device=dev)
+        n_out = torch.zeros(n, dtype=torch.int32, device=dev)
+        out = dict(codes=codes, n_out=n_out)
+        t = None
+        if taps:
+            A = d["codebook_size"] + 1
+            out["main_logits"] = torch.full((n, n_frames, A), float("nan"), device=dev)
+            out["fast_logits"] = torch.full((n, n_frames, d["n_codebooks"] - 1, d["codebook_size"]), float("nan"),
+                                            device=dev)
+            out["hidden"] = torch.full((n, n_frames, d["dim"]), float("nan"), device=dev)
+            out["draws"] = torch.full((n, n_frames, 11), -2, dtype=torch.int32, device=dev)
+            t = s2_debug_taps(out["main_logits"].data_ptr(), out["fast_logits"].data_ptr(), out["hidden"].data_ptr(),
+                              out["draws"].data_ptr())
+        params = [make_sampling(sampling) for _ in range(n)] if isinstance(sampling, dict) else \
+            [make_sampling(s) for s in sampling]
+        s2_decode_frames(self.ctx, ids, n_frames, params, expo.data_ptr(),
+                         forced.data_ptr() if forced is not None else None, codes.data_ptr(), n_out.data_ptr(), t,
+                         self.stream())
+        return out
+
+    def fast_logits(self, hidden, prefix):
+        import torch
+        n = hidden.shape[0]
+        d = self.d
+        out = torch.empty((n, d["n_codebooks"] - 1, d["codebook_size"]), dtype=torch.float32, device=hidden.device)
+        s2_fast_logits(self.ctx, n, hidden.data_ptr(), prefix.data_ptr(), out.data_ptr(), self.stream())
+        return out
+
+    def sync_status(self) -> int:
+        return s2_sync_status(self.ctx, self.stream())
+
+
+def upload_weights(host_weights, device="cuda"):
+    """Host arrays (fp32, or uint16 bf16 patterns) -> torch device tensors (bf16 / fp32)."""
+    import numpy as np
+    import torch
+    out = []
+    for w in host_weights:
+        if w is None:
+            out.append(None)
+            continue
+        if w.dtype == np.uint16:
+            t = torch.from_numpy(w.view(np.int16)).to(device).view(torch.bfloat16)
+        else:
+            t = torch.from_numpy(np.ascontiguousarray(w, dtype=np.float32)).to(device)
+        out.append(t)
+    return out

@@ -1,0 +1,693 @@
+// C ABI of the frame decoder: context, workspace layout, phase programs, call drivers.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "s2_internal.h"
+
+using namespace s2;
+
+struct s2_ctx {
+  Dims d{};
+  const void *E = nullptr, *CE = nullptr, *norm = nullptr, *P = nullptr, *FE = nullptr, *fnorm = nullptr,
+             *FO = nullptr;
+  std::vector<LayerW> slow, fast;
+  unsigned char* ws = nullptr;
+  size_t ws_bytes = 0;
+  int max_streams = 0, kv_slots = 0, grid = 0, device = 0;
+  // workspace regions
+  Control* ctl = nullptr;
+  float2* rope = nullptr;
+  float2* rope_f = nullptr;
+  StreamState* st = nullptr;       // [max_streams + 1] (last: scratch state of the Fast-AR-alone path)
+  float* hidden = nullptr;         // [max_streams + 1][D]
+  float* logits = nullptr;         // [max_streams][A]
+  unsigned char* kc = nullptr;     // [L][max_streams][Hkv][slots][hd]
+  unsigned char* vc = nullptr;
+  int32_t* stage = nullptr;        // [max_streams][kMaxFramesPerCall][NCB]
+  float *x = nullptr, *qkv = nullptr, *o = nullptr, *g = nullptr;
+  float *fx = nullptr, *fqkv = nullptr, *fo = nullptr, *fg = nullptr, *fk = nullptr, *fv = nullptr;
+  float *flogits = nullptr, *part = nullptr, *pscratch = nullptr;
+  int32_t* fcode = nullptr;
+  float* hidden_src = nullptr;     // builder: hidden buffer feeding Fast-AR position 0
+  Phase* prog = nullptr;           // [max_streams][n_dec] then fast-only program
+  int n_dec = 0, n_fast = 0, prefill_chunk = 0;
+  std::vector<int> host_pos;
+  std::vector<char> host_prefilled;
+  std::string err;
+};
+
+namespace {
+
+std::string g_init_error = "no error";
+
+constexpr const char* kLayerNames[9] = {"attention_norm", "attention.wqkv", "attention.q_norm", "attention.k_norm",
+                                        "attention.wo", "ffn_norm", "feed_forward.w1", "feed_forward.w3",
+                                        "feed_forward.w2"};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int fail(s2_ctx* c, int code, const std::string& msg) {
+  if (c) c->err = msg;
+  else g_init_error = msg;
+  return code;
+}
+
+bool to_dims(const s2_dims* s, Dims& d, std::string& why) {
+  d.D = s->dim; d.L = s->n_layer; d.Hq = s->n_head; d.Hkv = s->n_kv_head; d.hd = s->head_dim; d.F = s->ffn;
+  d.V = s->vocab; d.sem_lo = s->sem_begin; d.sem_hi = s->sem_end; d.im_end = s->im_end; d.ncb = s->n_codebooks;
+  d.cbs = s->codebook_size; d.sem_scale = s->sem_scale; d.eps = s->norm_eps; d.rope_base = s->rope_base;
+  d.qk_norm = s->qk_norm; d.rope_bf16 = s->rope_table_bf16; d.Df = s->fast_dim; d.Lf = s->fast_n_layer;
+  d.Hqf = s->fast_n_head; d.Hkvf = s->fast_n_kv_head; d.hdf = s->fast_head_dim; d.Ff = s->fast_ffn;
+  d.Wf = s->fast_window; d.has_proj = s->has_fast_project_in; d.wdt = s->weight_dtype; d.kvdt = s->kv_dtype;
+  d.esz = d.wdt == S2_BF16 ? 2 : 4;
+  d.kvsz = d.kvdt == S2_F16 ? 2 : 4;
+  d.A = d.cbs + 1;
+  auto bad = [&](const char* m) { why = m; return false; };
+  if (d.wdt != S2_BF16 && d.wdt != S2_F32) return bad("weight_dtype must be S2_BF16 or S2_F32");
+  if (d.kvdt != S2_F16 && d.kvdt != S2_F32) return bad("kv_dtype must be S2_F16 or S2_F32");
+  const int al = d.wdt == S2_BF16 ? 8 : 4;
+  if (d.D <= 0 || d.D % al || d.Df <= 0 || d.Df % al) return bad("dim/fast_dim must be positive multiples of 16 bytes");
+  if (d.L < 0 || d.Lf <= 0) return bad("a fast decoder (fast_n_layer > 0) is required");
+  if (d.ncb < 2 || d.ncb > kMaxCodebooks) return bad("n_codebooks out of range (2..15)");
+  if (d.Wf < d.ncb || d.Wf > 16) return bad("fast_window must cover n_codebooks positions (and be <= 16)");
+  if (d.cbs <= 0 || d.cbs % al) return bad("codebook_size must be a positive multiple of 16 bytes of weights");
+  if (d.Hqf <= 0 || d.Hkvf <= 0 || d.Hqf % d.Hkvf || d.Hqf / d.Hkvf > 4) return bad("fast heads: n_head % n_kv_head == 0, ratio <= 4");
+  if (d.hdf != 64 && d.hdf != 128) return bad("fast_head_dim must be 64 or 128");
+  if (d.Ff <= 0 || d.Ff % al || (d.Hqf * d.hdf) % al) return bad("fast ffn / head sizes must be multiples of 16 bytes");
+  if (!d.has_proj && d.Df != d.D) return bad("without fast_project_in, fast_dim must equal dim");
+  if (!(d.sem_scale > 0.f) || !(d.eps > 0.f) || !(d.rope_base > 1.0)) return bad("sem_scale, norm_eps, rope_base must be positive");
+  if (d.qk_norm != 0 && d.qk_norm != 1) return bad("qk_norm must be 0 or 1");
+  if (d.L > 0) {
+    if (d.Hq <= 0 || d.Hkv <= 0 || d.Hq % d.Hkv || d.Hq / d.Hkv > 4 || d.Hkv > 64) return bad("heads: n_head % n_kv_head == 0, ratio <= 4, n_kv_head <= 64");
+    if (d.hd != 64 && d.hd != 128) return bad("head_dim must be 64 or 128");
+    if (d.F <= 0 || d.F % al || (d.Hq * d.hd) % al) return bad("ffn / head sizes must be multiples of 16 bytes");
+    if (d.sem_hi - d.sem_lo + 1 != d.cbs) return bad("the semantic range must hold codebook_size ids");
+    if (d.sem_lo < 0 || d.sem_hi >= d.V || d.im_end < 0 || d.im_end >= d.V) return bad("semantic range / im_end outside the vocabulary");
+    if (d.im_end >= d.sem_lo && d.im_end <= d.sem_hi) return bad("im_end must lie outside the semantic range");
+  }
+  const int64_t maxk = kStageBytes / d.esz;
+  if (d.D > maxk || d.F > maxk || d.Ff > maxk || d.Hq * d.hd > maxk || d.Hqf * d.hdf > maxk || d.Df > maxk)
+    return bad("a projection input is longer than one pipeline stage");
+  if (2LL * d.D * d.esz > kStageBytes || 2LL * d.Df * d.esz > kStageBytes) return bad("gate/up rows exceed one pipeline stage");
+  return true;
+}
+
+int layer_count(const Dims& d) { return 3 + 9 * d.L + 4 + 9 * d.Lf; }
+
+long long tensor_numel(const Dims& d, int i, std::string* name) {
+  auto setn = [&](const std::string& s) { if (name) *name = s; };
+  if (i < 0 || i >= layer_count(d)) return -1;
+  if (i == 0) { setn("embeddings"); return 1LL * d.V * d.D; }
+  if (i == 1) { setn("codebook_embeddings"); return 1LL * d.ncb * d.cbs * d.D; }
+  if (i == 2) { setn("norm"); return d.D; }
+  i -= 3;
+  auto layer = [&](int li, int k, const char* pre, int D, int Hq, int Hkv, int hd, int F) -> long long {
+    setn(std::string(pre) + std::to_string(li) + "." + kLayerNames[k]);
+    switch (k) {
+      case 0: case 5: return D;
+      case 1: return 1LL * (Hq + 2 * Hkv) * hd * D;
+      case 2: case 3: return hd;
+      case 4: return 1LL * D * Hq * hd;
+      case 6: case 7: return 1LL * F * D;
+      default: return 1LL * D * F;
+    }
+  };
+  if (i < 9 * d.L) return layer(i / 9, i % 9, "layers.", d.D, d.Hq, d.Hkv, d.hd, d.F);
+  i -= 9 * d.L;
+  if (i == 0) { setn("fast_project_in"); return 1LL * d.Df * d.D; }
+  if (i == 1) { setn("fast_embeddings"); return 1LL * d.cbs * d.Df; }
+  if (i == 2) { setn("fast_norm"); return d.Df; }
+  if (i == 3) { setn("fast_output"); return 1LL * d.cbs * d.Df; }
+  i -= 4;
+  return layer(i / 9, i % 9, "fast_layers.", d.Df, d.Hqf, d.Hkvf, d.hdf, d.Ff);
+}
+
+// Sequential carve of the workspace (base == nullptr: size only).
+struct Carver {
+  unsigned char* base;
+  size_t off = 0;
+  template <typename T>
+  T* take(size_t count) {
+    off = align_up(off, 256);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+int attn_items_max(const Dims& d, int grid, int slots) {
+  if (d.L == 0) return 1;
+  return d.Hkv * (grid / d.Hkv + slots / kAttnMaxChunk + 2);
+}
+
+void carve(s2_ctx* c, Carver& cv) {
+  const Dims& d = c->d;
+  const int B = c->max_streams;
+  const size_t slots = static_cast<size_t>(c->kv_slots);
+  const int QKV = (d.Hq + 2 * d.Hkv) * d.hd, QKVf = (d.Hqf + 2 * d.Hkvf) * d.hdf;
+  c->ctl = cv.take<Control>(1);
+  c->rope = cv.take<float2>(std::max<size_t>(1, slots * (d.hd / 2)));
+  c->rope_f = cv.take<float2>(static_cast<size_t>(d.Wf) * (d.hdf / 2));
+  c->st = cv.take<StreamState>(B + 1);
+  c->hidden = cv.take<float>(static_cast<size_t>(B + 1) * d.D);
+  c->logits = cv.take<float>(static_cast<size_t>(B) * d.A);
+  const size_t kv = static_cast<size_t>(d.L) * B * d.Hkv * slots * d.hd * d.kvsz;
+  c->kc = cv.take<unsigned char>(kv);
+  c->vc = cv.take<unsigned char>(kv);
+  c->stage = cv.take<int32_t>(static_cast<size_t>(B) * kMaxFramesPerCall * d.ncb);
+  c->x = cv.take<float>(d.D);
+  c->qkv = cv.take<float>(std::max(QKV, 1));
+  c->o = cv.take<float>(std::max(d.Hq * d.hd, 1));
+  c->g = cv.take<float>(std::max(d.F, 1));
+  c->fx = cv.take<float>(static_cast<size_t>(d.Wf) * d.Df);
+  c->fqkv = cv.take<float>(2 * static_cast<size_t>(QKVf));
+  c->fo = cv.take<float>(2 * static_cast<size_t>(d.Hqf) * d.hdf);
+  c->fg = cv.take<float>(2 * static_cast<size_t>(d.Ff));
+  c->fk = cv.take<float>(static_cast<size_t>(d.Lf) * d.Wf * d.Hkvf * d.hdf);
+  c->fv = cv.take<float>(static_cast<size_t>(d.Lf) * d.Wf * d.Hkvf * d.hdf);
+  c->flogits = cv.take<float>(d.cbs);
+  c->fcode = cv.take<int32_t>(16);
+  c->part = cv.take<float>(static_cast<size_t>(attn_items_max(d, c->grid, c->kv_slots)) * 4 * (d.hd + 2));
+  c->prefill_chunk = 512;
+  c->pscratch = d.L > 0 ? cv.take<float>(prefill_scratch_floats(d, c->prefill_chunk)) : nullptr;
+  c->n_dec = d.L > 0 ? 1 + (d.ncb - 1) * (5 * d.Lf + 2) + 5 * d.L + 1 : 0;
+  c->n_fast = 2 + (d.ncb - 1) * (5 * d.Lf + 2);
+  c->prog = cv.take<Phase>(static_cast<size_t>(B) * c->n_dec + c->n_fast);
+}
+
+// ------------------------------------------------------------ phase builders
+
+struct Builder {
+  s2_ctx* c;
+  std::vector<Phase>* out;
+  std::string err;
+
+  Phase gemv(int M, int K, int ncols, const void* w0, const void* w1, const void* normw, int epi) {
+    const Dims& d = c->d;
+    Phase p{};
+    p.op = OP_GEMV;
+    p.M = M;
+    p.K = K;
+    p.nmat = w1 ? 2 : 1;
+    p.ncols = ncols;
+    p.epi = epi;
+    p.w[0] = w0;
+    p.w[1] = w1;
+    p.normw = normw;
+    const int epc = 16 / d.esz;
+    const int nch = kXRegFloats / (epc * ncols);
+    const int nchunk = K / epc;
+    int Q = 1;
+    while ((nchunk + Q - 1) / Q > 32 * nch) Q *= 2;
+    if (Q > kConsumerWarps) err = "projection too long for the register-resident activation slices";
+    p.Q = Q;
+    const int rowb = K * d.esz * p.nmat;
+    p.rows_per_tile = std::max(1, kStageBytes / rowb);
+    return p;
+  }
+  void push(Phase p) {
+    const int g2 = c->grid - p.cta0;
+    if (p.op == OP_GEMV) {
+      const int rows = (p.M + g2 - 1) / g2;
+      if (static_cast<long long>(rows) * p.nmat * p.ncols * p.Q > kRedFloats) err = "too many rows per CTA for the partial-sum buffer";
+      if (p.last_row && p.nmat != 1) err = "last-row override needs one matrix";
+    }
+    out->push_back(p);
+  }
+  static GemvCol buf(const float* p, float* wb = nullptr) { return GemvCol{SRC_BUF, 0, p, wb}; }
+
+  // Fast-AR calls 1..NCB-1 (fast_only: without draws' side effects on the stream state)
+  void fast_calls() {
+    const Dims& d = c->d;
+    const int QKVf = (d.Hqf + 2 * d.Hkvf) * d.hdf;
+    const size_t kvl = static_cast<size_t>(d.Wf) * d.Hkvf * d.hdf;
+    const float scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d.hdf)));
+    for (int cb = 1; cb < d.ncb; ++cb) {
+      const int npos = cb == 1 ? 2 : 1, pos0 = cb == 1 ? 0 : cb;
+      for (int l = 0; l < d.Lf; ++l) {
+        const LayerW& w = c->fast[l];
+        Phase q = gemv(QKVf, d.Df, npos, w.wqkv, nullptr, w.an, EPI_STORE);
+        for (int j = 0; j < npos; ++j) {
+          const int p = pos0 + j;
+          float* xp = c->fx + static_cast<size_t>(p) * d.Df;
+          if (l == 0 && p >= 1) q.col[j] = GemvCol{SRC_FEROW, 0, c->fcode + (p - 1), xp};
+          else if (l == 0 && p == 0 && !d.has_proj) q.col[j] = buf(c->hidden_src, xp);
+          else q.col[j] = buf(xp);
+          q.y[j] = c->fqkv + static_cast<size_t>(j) * QKVf;
+        }
+        push(q);
+        Phase a{};
+        a.op = OP_ATTN_FAST;
+        a.layer = l;
+        a.npos = npos;
+        a.pos0 = pos0;
+        a.qkv = c->fqkv;
+        a.out = c->fo;
+        a.kc = c->fk + l * kvl;
+        a.vc = c->fv + l * kvl;
+        a.qn = w.qn;
+        a.kn = w.kn;
+        a.scale = scale;
+        push(a);
+        Phase o = gemv(d.Df, d.Hqf * d.hdf, npos, w.wo, nullptr, nullptr, EPI_ADD);
+        for (int j = 0; j < npos; ++j) {
+          o.col[j] = buf(c->fo + static_cast<size_t>(j) * d.Hqf * d.hdf);
+          o.y[j] = c->fx + static_cast<size_t>(pos0 + j) * d.Df;
+        }
+        push(o);
+        Phase u = gemv(d.Ff, d.Df, npos, w.w1, w.w3, w.fn, EPI_SWIGLU);
+        for (int j = 0; j < npos; ++j) {
+          u.col[j] = buf(c->fx + static_cast<size_t>(pos0 + j) * d.Df);
+          u.y[j] = c->fg + static_cast<size_t>(j) * d.Ff;
+        }
+        push(u);
+        Phase dn = gemv(d.Df, d.Ff, npos, w.w2, nullptr, nullptr, EPI_ADD);
+        for (int j = 0; j < npos; ++j) {
+          dn.col[j] = buf(c->fg + static_cast<size_t>(j) * d.Ff);
+          dn.y[j] = c->fx + static_cast<size_t>(pos0 + j) * d.Df;
+        }
+        push(dn);
+      }
+      Phase fo = gemv(d.cbs, d.Df, 1, c->FO, nullptr, c->fnorm, EPI_STORE);
+      fo.col[0] = buf(c->fx + static_cast<size_t>(cb) * d.Df);
+      fo.y[0] = c->flogits;
+      push(fo);
+      Phase s{};
+      s.op = OP_SAMPLE_FAST;
+      s.cb = cb;
+      push(s);
+    }
+  }
+};
+
+}  // namespace
+
+extern "C" {
+
+int s2_weight_count(const s2_dims* s) {
+  Dims d;
+  std::string why;
+  if (!s || !to_dims(s, d, why)) return -1;
+  return layer_count(d);
+}
+
+long long s2_weight_info(const s2_dims* s, int i, char* name, int len) {
+  Dims d;
+  std::string why, nm;
+  if (!s || !to_dims(s, d, why)) return -1;
+  const long long n = tensor_numel(d, i, &nm);
+  if (n >= 0 && name && len > 0) {
+    std::snprintf(name, static_cast<size_t>(len), "%s", nm.c_str());
+  }
+  return n;
+}
+
+size_t s2_frame_workspace_bytes(const s2_dims* s, int max_streams, int kv_slots) {
+  Dims d;
+  std::string why;
+  if (!s || !to_dims(s, d, why) || max_streams <= 0 || kv_slots < 0) return 0;
+  s2_ctx tmp;
+  tmp.d = d;
+  tmp.max_streams = max_streams;
+  tmp.kv_slots = d.L > 0 ? kv_slots : 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int grid = 0;
+  if (frame_kernel_grid(dev, &grid) != S2_OK) grid = 256;
+  tmp.grid = grid;
+  Carver cv{nullptr};
+  carve(&tmp, cv);
+  return align_up(cv.off, 256);
+}
+
+}  // extern "C"
+
+namespace {
+
+int build_programs(s2_ctx* c) {
+  const Dims& d = c->d;
+  std::vector<Phase> all;
+  Builder b{c, &all, {}};
+  for (int sid = 0; sid < c->max_streams && d.L > 0; ++sid) {
+    const size_t before = all.size();
+    float* hid = c->hidden + static_cast<size_t>(sid) * d.D;
+    float* lg = c->logits + static_cast<size_t>(sid) * d.A;
+    c->hidden_src = hid;
+    // 1. main draw on CTA 0 while the other CTAs project the hidden state into Fast-AR position 0
+    if (d.has_proj) {
+      Phase p = b.gemv(d.Df, d.D, 1, c->P, nullptr, nullptr, EPI_STORE);
+      p.merge_main = 1;
+      p.cta0 = 1;
+      p.col[0] = Builder::buf(hid);
+      p.y[0] = c->fx;
+      b.push(p);
+    } else {
+      Phase p{};
+      p.op = OP_SAMPLE_MAIN;
+      b.push(p);
+    }
+    // 2. nine Fast-AR calls with their draws
+    b.fast_calls();
+    // 3. Slow-AR step on [token, code_0..code_{NCB-1}]
+    const size_t kvl = static_cast<size_t>(c->max_streams) * d.Hkv * c->kv_slots * d.hd * d.kvsz;
+    const size_t kvs = static_cast<size_t>(sid) * d.Hkv * c->kv_slots * d.hd * d.kvsz;
+    const int QKV = (d.Hq + 2 * d.Hkv) * d.hd;
+    const float scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d.hd)));
+    for (int l = 0; l < d.L; ++l) {
+      const LayerW& w = c->slow[l];
+      Phase q = b.gemv(QKV, d.D, 1, w.wqkv, nullptr, w.an, EPI_STORE);
+      q.col[0] = l == 0 ? GemvCol{SRC_EMBED, 0, c->st[sid].vals, c->x} : Builder::buf(c->x);
+      q.y[0] = c->qkv;
+      b.push(q);
+      Phase a{};
+      a.op = OP_ATTN_SLOW;
+      a.layer = l;
+      a.qkv = c->qkv;
+      a.out = c->o;
+      a.kc = c->kc + l * kvl + kvs;
+      a.vc = c->vc + l * kvl + kvs;
+      a.qn = w.qn;
+      a.kn = w.kn;
+      a.scale = scale;
+      b.push(a);
+      Phase o = b.gemv(d.D, d.Hq * d.hd, 1, w.wo, nullptr, nullptr, EPI_ADD);
+      o.col[0] = Builder::buf(c->o);
+      o.y[0] = c->x;
+      b.push(o);
+      Phase u = b.gemv(d.F, d.D, 1, w.w1, w.w3, w.fn, EPI_SWIGLU);
+      u.col[0] = Builder::buf(c->x);
+      u.y[0] = c->g;
+      b.push(u);
+      Phase dn = b.gemv(d.D, d.F, 1, w.w2, nullptr, nullptr, EPI_ADD);
+      dn.col[0] = Builder::buf(c->g);
+      dn.y[0] = c->x;
+      b.push(dn);
+    }
+    // final norm + tied logits on the admissible ids (sem_begin..sem_end contiguous, im_end last)
+    Phase lo = b.gemv(d.A, d.D, 1, static_cast<const unsigned char*>(c->E) + static_cast<size_t>(d.sem_lo) * d.D * d.esz,
+                      nullptr, c->norm, EPI_STORE);
+    lo.last_row = static_cast<const unsigned char*>(c->E) + static_cast<size_t>(d.im_end) * d.D * d.esz;
+    lo.col[0] = Builder::buf(c->x);
+    lo.hid_out = hid;
+    lo.y[0] = lg;
+    lo.bump_pos = 1;
+    b.push(lo);
+    if (static_cast<int>(all.size() - before) != c->n_dec) return fail(c, S2_EINVAL, "internal: decode program length");
+  }
+  // Fast-AR-alone program
+  {
+    const size_t before = all.size();
+    float* hid = c->hidden + static_cast<size_t>(c->max_streams) * d.D;
+    c->hidden_src = hid;
+    Phase fi{};
+    fi.op = OP_FAST_IN;
+    b.push(fi);
+    if (d.has_proj) {
+      Phase p = b.gemv(d.Df, d.D, 1, c->P, nullptr, nullptr, EPI_STORE);
+      p.col[0] = Builder::buf(hid);
+      p.y[0] = c->fx;
+      b.push(p);
+    } else {
+      Phase p{};
+      p.op = OP_FAST_IN;  // harmless repeat keeps the program length fixed
+      b.push(p);
+    }
+    b.fast_calls();
+    if (static_cast<int>(all.size() - before) != c->n_fast) return fail(c, S2_EINVAL, "internal: fast program length");
+  }
+  if (!b.err.empty()) return fail(c, S2_EINVAL, b.err);
+  if (cudaMemcpy(c->prog, all.data(), all.size() * sizeof(Phase), cudaMemcpyHostToDevice) != cudaSuccess)
+    return fail(c, S2_ECUDA, "copying the phase programs failed");
+  return S2_OK;
+}
+
+CallParams base_params(s2_ctx* c) {
+  CallParams cp{};
+  cp.d = c->d;
+  cp.ctl = c->ctl;
+  cp.part = c->part;
+  cp.fcode = c->fcode;
+  cp.flogits = c->flogits;
+  cp.rope = c->rope;
+  cp.rope_f = c->rope_f;
+  cp.E = c->E;
+  cp.CE = c->CE;
+  cp.FE = c->FE;
+  cp.kv_slots = c->kv_slots;
+  return cp;
+}
+
+}  // namespace
+
+extern "C" {
+
+int s2_frame_init(const s2_dims* s, const void* const* weights, int n_weights, void* workspace, size_t ws_bytes,
+                  int max_streams, int kv_slots, s2_ctx** out) {
+  if (!out) return fail(nullptr, S2_EINVAL, "out is NULL");
+  *out = nullptr;
+  Dims d;
+  std::string why;
+  if (!s || !to_dims(s, d, why)) return fail(nullptr, S2_EINVAL, "bad dims: " + why);
+  if (max_streams <= 0 || max_streams > 1024) return fail(nullptr, S2_EINVAL, "max_streams must be in 1..1024");
+  if (d.L > 0 && kv_slots <= 0) return fail(nullptr, S2_EINVAL, "kv_slots must be positive");
+  if (!weights || n_weights != layer_count(d)) return fail(nullptr, S2_EINVAL, "weight table size does not match the dims");
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return fail(nullptr, S2_EINVAL, "workspace must be 256-byte aligned");
+  for (int i = 0; i < n_weights; ++i) {
+    const bool slow_part = i < 3 + 9 * d.L;
+    const bool optional = (d.L == 0 && i < 3) || (i == 3 + 9 * d.L && !d.has_proj);
+    if (!weights[i] && !optional) {
+      std::string nm;
+      tensor_numel(d, i, &nm);
+      return fail(nullptr, S2_EINVAL, "missing weight " + nm);
+    }
+    if (weights[i] && (reinterpret_cast<uintptr_t>(weights[i]) & 15u))
+      return fail(nullptr, S2_EINVAL, "weights must be 16-byte aligned");
+    (void)slow_part;
+  }
+  s2_ctx* c = new s2_ctx();
+  c->d = d;
+  c->max_streams = max_streams;
+  c->kv_slots = d.L > 0 ? kv_slots : 0;
+  cudaGetDevice(&c->device);
+  if (frame_kernel_grid(c->device, &c->grid) != S2_OK) {
+    delete c;
+    return fail(nullptr, S2_ECUDA, "the frame kernel cannot be resident on this device");
+  }
+  int i = 0;
+  c->E = weights[i++];
+  c->CE = weights[i++];
+  c->norm = weights[i++];
+  auto bind = [&](std::vector<LayerW>& v, int n) {
+    v.resize(n);
+    for (int l = 0; l < n; ++l) {
+      LayerW& w = v[l];
+      const void** f[9] = {&w.an, &w.wqkv, &w.qn, &w.kn, &w.wo, &w.fn, &w.w1, &w.w3, &w.w2};
+      for (int k = 0; k < 9; ++k) *f[k] = weights[i++];
+    }
+  };
+  bind(c->slow, d.L);
+  c->P = weights[i++];
+  c->FE = weights[i++];
+  c->fnorm = weights[i++];
+  c->FO = weights[i++];
+  bind(c->fast, d.Lf);
+  c->ws = static_cast<unsigned char*>(workspace);
+  c->ws_bytes = ws_bytes;
+  Carver cv{nullptr};
+  carve(c, cv);
+  if (align_up(cv.off, 256) > ws_bytes) {
+    delete c;
+    return fail(nullptr, S2_ENOMEM, "workspace too small: need " + std::to_string(align_up(cv.off, 256)) + " bytes");
+  }
+  Carver real{c->ws};
+  carve(c, real);
+  // control block, stream states, tables
+  Control ctl{};
+  ctl.spin_limit = 2000000;
+  if (cudaMemcpy(c->ctl, &ctl, sizeof(Control), cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemset(c->st, 0, sizeof(StreamState) * (max_streams + 1)) != cudaSuccess) {
+    delete c;
+    return fail(nullptr, S2_ECUDA, "initialising the workspace failed");
+  }
+  if (build_rope_tables(c->rope, c->kv_slots, d.hd, c->rope_f, d.Wf, d.hdf, d.rope_base, d.rope_bf16, nullptr) != S2_OK ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    delete c;
+    return fail(nullptr, S2_ECUDA, "building the RoPE tables failed");
+  }
+  const int rc = build_programs(c);
+  if (rc != S2_OK) {
+    g_init_error = c->err;
+    delete c;
+    return rc;
+  }
+  c->host_pos.assign(max_streams, 0);
+  c->host_prefilled.assign(max_streams, 0);
+  *out = c;
+  return S2_OK;
+}
+
+int s2_prefill(s2_ctx* c, int n, const int* ids, const int32_t* tokens, const int* lengths, CUstream_st* stream) {
+  if (!c) return fail(nullptr, S2_EINVAL, "ctx is NULL");
+  const Dims& d = c->d;
+  if (d.L == 0) return fail(c, S2_ESTATE, "this context has no Slow-AR (Fast-AR-alone shape)");
+  if (n <= 0 || !ids || !tokens || !lengths) return fail(c, S2_EINVAL, "bad prefill arguments");
+  size_t off = 0;
+  for (int k = 0; k < n; ++k) {
+    const int sid = ids[k], T = lengths[k];
+    if (sid < 0 || sid >= c->max_streams) return fail(c, S2_EINVAL, "stream id out of range");
+    if (T <= 0) return fail(c, S2_EINVAL, "prompt length must be positive");
+    if (T > c->kv_slots) return fail(c, S2_ECAPACITY, "prompt longer than the KV slots");
+  }
+  for (int k = 0; k < n; ++k) {
+    const int sid = ids[k], T = lengths[k];
+    PrefillArgs a{};
+    a.d = d;
+    a.E = c->E;
+    a.CE = c->CE;
+    a.norm = c->norm;
+    a.layers = c->slow.data();
+    a.tokens = tokens + off;
+    a.T = T;
+    a.chunk = c->prefill_chunk;
+    const size_t kvl = static_cast<size_t>(c->max_streams) * d.Hkv * c->kv_slots * d.hd * d.kvsz;
+    const size_t kvs = static_cast<size_t>(sid) * d.Hkv * c->kv_slots * d.hd * d.kvsz;
+    a.kc0 = c->kc + kvs;
+    a.vc0 = c->vc + kvs;
+    a.kv_layer_stride = kvl;
+    a.kv_slots = c->kv_slots;
+    a.rope = c->rope;
+    a.scratch = c->pscratch;
+    a.hidden = c->hidden + static_cast<size_t>(sid) * d.D;
+    a.logits = c->logits + static_cast<size_t>(sid) * d.A;
+    a.st = c->st + sid;
+    a.err = &c->ctl->error;
+    const int rc = run_prefill(a, stream);
+    if (rc != S2_OK) return fail(c, rc, std::string("prefill launch failed: ") + cudaGetErrorString(cudaGetLastError()));
+    off += static_cast<size_t>(T) * (d.ncb + 1);
+    c->host_pos[sid] = T;
+    c->host_prefilled[sid] = 1;
+  }
+  return S2_OK;
+}
+
+int s2_decode_frames(s2_ctx* c, int n, const int* ids, int n_frames, const s2_sampling* params, const float* expo,
+                     const int32_t* forced, int32_t* codes, int32_t* n_out, const s2_debug_taps* taps,
+                     CUstream_st* stream) {
+  if (!c) return fail(nullptr, S2_EINVAL, "ctx is NULL");
+  const Dims& d = c->d;
+  if (d.L == 0) return fail(c, S2_ESTATE, "this context has no Slow-AR (Fast-AR-alone shape)");
+  if (n <= 0 || !ids || !params || !expo || !codes || !n_out) return fail(c, S2_EINVAL, "bad decode arguments");
+  if (n_frames <= 0 || n_frames > kMaxFramesPerCall) return fail(c, S2_EINVAL, "n_frames must be in 1..8192");
+  for (int k = 0; k < n; ++k) {
+    const int sid = ids[k];
+    if (sid < 0 || sid >= c->max_streams) return fail(c, S2_EINVAL, "stream id out of range");
+    if (!c->host_prefilled[sid]) return fail(c, S2_ESTATE, "stream not prefilled");
+    if (c->host_pos[sid] + n_frames > c->kv_slots) return fail(c, S2_ECAPACITY, "decode would exceed the KV slots");
+    const s2_sampling& p = params[k];
+    if (p.top_k != kTopK) return fail(c, S2_EINVAL, "top_k must be 30");
+    if (!(p.temperature > 0.f) || !(p.ras_temperature > 0.f)) return fail(c, S2_EINVAL, "temperatures must be > 0");
+    if (!(p.top_p > 0.f && p.top_p <= 1.f) || !(p.ras_top_p > 0.f && p.ras_top_p <= 1.f))
+      return fail(c, S2_EINVAL, "top_p must be in (0, 1]");
+    if (p.ras_window < 1 || p.ras_window > kMaxWindow) return fail(c, S2_EINVAL, "ras_window must be in 1..16");
+    for (int j = 0; j < k; ++j)
+      if (ids[j] == sid) return fail(c, S2_EINVAL, "a stream appears twice");
+  }
+  for (int k = 0; k < n; ++k) {
+    const int sid = ids[k];
+    CallParams cp = base_params(c);
+    cp.n_frames = n_frames;
+    cp.fast_only = 0;
+    cp.n_phases = c->n_dec;
+    cp.stream = sid;
+    cp.prog = c->prog + static_cast<size_t>(sid) * c->n_dec;
+    cp.st = c->st + sid;
+    cp.hidden = c->hidden + static_cast<size_t>(sid) * d.D;
+    cp.logits = c->logits + static_cast<size_t>(sid) * d.A;
+    cp.stage = c->stage + static_cast<size_t>(sid) * kMaxFramesPerCall * d.ncb;
+    const size_t fo = static_cast<size_t>(k) * n_frames;
+    cp.expo = expo + fo * kDraws * kTopK;
+    cp.forced = forced ? forced + fo * kDraws : nullptr;
+    if (taps) {
+      cp.dbg_main = taps->main_logits ? taps->main_logits + fo * d.A : nullptr;
+      cp.dbg_fast = taps->fast_logits ? taps->fast_logits + fo * (d.ncb - 1) * d.cbs : nullptr;
+      cp.dbg_hidden = taps->hidden ? taps->hidden + fo * d.D : nullptr;
+      cp.dbg_draws = taps->draws ? taps->draws + fo * kDraws : nullptr;
+    }
+    const s2_sampling& p = params[k];
+    cp.temperature = p.temperature;
+    cp.top_p = p.top_p;
+    cp.ras_temperature = p.ras_temperature;
+    cp.ras_top_p = p.ras_top_p;
+    cp.ras_window = p.ras_window;
+    cp.min_tokens = p.min_tokens_before_end;
+    int rc = launch_frames(cp, c->grid, stream);
+    if (rc != S2_OK) return fail(c, rc, std::string("frame kernel launch failed: ") + cudaGetErrorString(cudaGetLastError()));
+    rc = compact_codes(cp.stage, codes + static_cast<size_t>(k) * d.ncb * n_frames, cp.st, n_frames, d.ncb, n_out + k,
+                       stream);
+    if (rc != S2_OK) return fail(c, rc, "code compaction launch failed");
+    c->host_pos[sid] += n_frames;
+  }
+  return S2_OK;
+}
+
+int s2_fast_logits(s2_ctx* c, int n_frames, const float* hidden, const int32_t* prefix, float* logits,
+                   CUstream_st* stream) {
+  if (!c) return fail(nullptr, S2_EINVAL, "ctx is NULL");
+  const Dims& d = c->d;
+  if (n_frames <= 0 || !hidden || !prefix || !logits) return fail(c, S2_EINVAL, "bad fast_logits arguments");
+  CallParams cp = base_params(c);
+  cp.n_frames = n_frames;
+  cp.fast_only = 1;
+  cp.n_phases = c->n_fast;
+  cp.prog = c->prog + static_cast<size_t>(c->max_streams) * c->n_dec;
+  cp.st = c->st + c->max_streams;
+  cp.hidden = c->hidden + static_cast<size_t>(c->max_streams) * d.D;
+  cp.fin_hidden = hidden;
+  cp.fin_prefix = prefix;
+  cp.fout = logits;
+  cp.temperature = 1.f;
+  cp.top_p = 1.f;
+  const int rc = launch_frames(cp, c->grid, stream);
+  if (rc != S2_OK) return fail(c, rc, std::string("frame kernel launch failed: ") + cudaGetErrorString(cudaGetLastError()));
+  return S2_OK;
+}
+
+int s2_sync_status(s2_ctx* c, CUstream_st* stream) {
+  if (!c) return fail(nullptr, S2_EINVAL, "ctx is NULL");
+  if (cudaStreamSynchronize(stream) != cudaSuccess)
+    return fail(c, S2_ECUDA, std::string("stream synchronisation failed: ") + cudaGetErrorString(cudaGetLastError()));
+  int e[2] = {0, 0};
+  if (cudaMemcpy(e, &c->ctl->error, sizeof(e), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return fail(c, S2_ECUDA, "reading the device status failed");
+  if (e[0] != 0) {
+    const int z[2] = {0, 0};
+    cudaMemcpy(&c->ctl->error, z, sizeof(z), cudaMemcpyHostToDevice);
+    return fail(c, e[0], e[0] == S2_ETIMEOUT ? "a device-side wait gave up (site " + std::to_string(e[1]) + ")"
+                                             : "an input id was out of range");
+  }
+  return S2_OK;
+}
+
+int s2_set_spin_limit(s2_ctx* c, long long limit) {
+  if (!c) return fail(nullptr, S2_EINVAL, "ctx is NULL");
+  if (limit < 0) return fail(c, S2_EINVAL, "limit must be >= 0");
+  const long long v = limit == 0 ? 2000000 : limit;
+  if (cudaMemcpy(&c->ctl->spin_limit, &v, sizeof(v), cudaMemcpyHostToDevice) != cudaSuccess)
+    return fail(c, S2_ECUDA, "setting the spin limit failed");
+  return S2_OK;
+}
+
+int s2_frame_free(s2_ctx* c) {
+  delete c;
+  return S2_OK;
+}
+
+const char* s2_last_error(const s2_ctx* c) { return c ? c->err.c_str() : g_init_error.c_str(); }
+
+}  // extern "C"

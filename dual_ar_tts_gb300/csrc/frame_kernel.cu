@@ -1,0 +1,1101 @@
+// Persistent frame kernel: runs whole Dual-AR frames (main draw, nine Fast-AR calls with their
+// draws, one Slow-AR step) for one stream in a single cooperative launch.
+//
+// Layout of a CTA (one per SM):
+//   warp 8      producer: streams the CTA's weight tiles of every GEMV phase, in program order,
+//               into a ring of shared-memory stages with 1-D bulk async copies (TMA engine).
+//               Weights never depend on activations, so it runs ahead across grid barriers,
+//               bounded only by ring capacity.
+//   warps 0..7  consumers: execute the phase program; a grid barrier (bounded spin on a global
+//               counter) separates dependent phases.
+// Every wait is bounded; a wait that gives up records S2_ETIMEOUT in the control block and the
+// whole grid leaves the kernel cleanly (no trap).
+//
+// The computations follow s2.cpp analysis ch.02 "Overall architecture and Dual-AR data flow"
+// §3.2-§3.4 (input embedding, 36-layer block, tied logits, feedback), ch.06 "Fast-AR codebook
+// decoding and the generation main loop" §1-§6 (Fast-AR window, causal mask offset 0, untied
+// output, sem_mask, min_tokens_before_end, RAS, clamp) and the Mizuoto "Fish Speech" engine
+// page (fp32 RMSNorm, adjacent-pair RoPE with a bf16 table, top-k 30, argmax(probs / -log u),
+// draw order).
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+#include "s2_internal.h"
+
+namespace s2 {
+
+constexpr int kMiscFloats = 5376;
+
+struct Smem {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  int abort_flag;   // consumers -> producer: stop streaming
+  int fail;         // a consumer wait gave up: leave at the next phase boundary
+  int sync_ok;
+  int flag;
+  float red[kRedFloats];
+  float misc[kMiscFloats];
+  alignas(128) unsigned char ring[kStages][kStageBytes];
+};
+
+// misc[] regions
+constexpr int kMiscQ = 0;                  // attention: q heads of this CTA [4][128]
+constexpr int kMiscKV = 512;               // new k, v [2][128]
+constexpr int kMiscWarp = 768;             // attention warp partials [8][4][130]
+constexpr int kMiscSS = 768 + 8 * 4 * 130; // GEMV sum-of-squares partials [16]
+constexpr int kMiscSamp = kMiscSS + 32;    // sampler: candidates, warp winners
+static_assert(kMiscSamp + 256 <= kMiscFloats, "misc layout");
+
+struct Pipe {
+  int stage;
+  uint32_t round;
+  __device__ void advance() {
+    if (++stage == kStages) {
+      stage = 0;
+      ++round;
+    }
+  }
+};
+
+// ------------------------------------------------------------------ helpers
+
+__device__ __forceinline__ void rows_of(const Phase& ph, int cta, int G, int& r0, int& nr) {
+  const int g2 = G - ph.cta0, i = cta - ph.cta0;
+  if (i < 0 || g2 <= 0) {
+    r0 = 0;
+    nr = 0;
+    return;
+  }
+  const int base = ph.M / g2, rem = ph.M % g2;
+  r0 = i * base + (i < rem ? i : rem);
+  nr = base + (i < rem ? 1 : 0);
+}
+
+__device__ __forceinline__ bool should_bail(const CallParams& cp, Smem& S) {
+  return *reinterpret_cast<volatile int*>(&S.fail) != 0 || ld_volatile_int(&cp.ctl->error) != 0;
+}
+
+// Bounded wait on an mbarrier phase; on give-up records the failure and returns false.
+__device__ bool wait_bar(const CallParams& cp, Smem& S, uint64_t* bar, uint32_t parity, int where,
+                         bool producer) {
+  if (mbar_test(bar, parity)) return true;
+  const long long t0 = clock_us();
+  const long long lim = cp.ctl->spin_limit;
+  while (!mbar_test(bar, parity)) {
+    if (producer ? (*reinterpret_cast<volatile int*>(&S.abort_flag) != 0) : should_bail(cp, S)) return false;
+    if (ld_volatile_int(&cp.ctl->error) != 0) return false;
+    if (clock_us() - t0 > lim) {
+      if (atomicCAS(&cp.ctl->error, 0, S2_ETIMEOUT) == 0) cp.ctl->error_where = where;
+      return false;
+    }
+  }
+  return true;
+}
+
+// Grid-wide barrier among the consumer threads of all CTAs.
+__device__ bool grid_sync(const CallParams& cp, Smem& S, unsigned& target) {
+  named_bar(1, kConsumers);
+  target += gridDim.x;
+  if (threadIdx.x == 0) {
+    int ok = !should_bail(cp, S);
+    if (ok) {
+      __threadfence();
+      red_release_add(&cp.ctl->gbar, 1u);
+      const long long lim = cp.ctl->spin_limit;
+      long long t0 = 0;
+      unsigned spins = 0;
+      while (ld_acquire(&cp.ctl->gbar) < target) {
+        if (ld_volatile_int(&cp.ctl->error) != 0) {
+          ok = 0;
+          break;
+        }
+        if ((++spins & 63u) == 0) {
+          const long long t = clock_us();
+          if (t0 == 0) t0 = t;
+          else if (t - t0 > lim) {
+            if (atomicCAS(&cp.ctl->error, 0, S2_ETIMEOUT) == 0) cp.ctl->error_where = 1;
+            ok = 0;
+            break;
+          }
+        }
+      }
+      __threadfence();
+    }
+    S.sync_ok = ok;
+    if (!ok) S.fail = 1;
+  }
+  named_bar(1, kConsumers);
+  return S.sync_ok != 0;
+}
+
+__device__ __forceinline__ void unpack16(const uint4& u, float* f, uint16_t) {
+  f[0] = bf16lo(u.x); f[1] = bf16hi(u.x); f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
+  f[4] = bf16lo(u.z); f[5] = bf16hi(u.z); f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
+}
+__device__ __forceinline__ void unpack16(const uint4& u, float* f, float) {
+  f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+  f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+}
+
+// =========================================================================
+// producer
+// =========================================================================
+
+__device__ void producer(const CallParams& cp, Smem& S) {
+  if ((threadIdx.x & 31) != 0) return;
+  const uint64_t pol = policy_evict_first();
+  Pipe pp{0, 0};
+  uint32_t fill_parity[kStages];
+  bool filled[kStages];
+  for (int s = 0; s < kStages; ++s) filled[s] = false;
+  bool stop = ld_volatile_int(&cp.st->done) != 0 && !cp.fast_only;
+  for (int f = 0; f < cp.n_frames && !stop; ++f) {
+    for (int p = 0; p < cp.n_phases && !stop; ++p) {
+      const Phase& ph = cp.prog[p];
+      if (ph.op != OP_GEMV) continue;
+      int r0, nr;
+      rows_of(ph, blockIdx.x, gridDim.x, r0, nr);
+      const int R = ph.rows_per_tile;
+      const uint32_t rowb = static_cast<uint32_t>(ph.K) * cp.d.esz;
+      for (int t = 0; t < nr; t += R) {
+        const int rr = min(R, nr - t);
+        if (!wait_bar(cp, S, &S.empty[pp.stage], (pp.round & 1u) ^ 1u, 2, true)) {
+          stop = true;
+          break;
+        }
+        const uint32_t bytes = rowb * rr * ph.nmat;
+        uint64_t* fb = &S.full[pp.stage];
+        mbar_arrive_expect_tx(fb, bytes);
+        unsigned char* dst = S.ring[pp.stage];
+        const int row = r0 + t;
+        for (int m = 0; m < ph.nmat; ++m) {
+          const unsigned char* src = static_cast<const unsigned char*>(ph.w[m]) + static_cast<size_t>(row) * rowb;
+          unsigned char* dm = dst + static_cast<size_t>(m) * rr * rowb;
+          if (ph.last_row != nullptr && row + rr == ph.M) {
+            if (rr > 1) bulk_g2s(dm, src, rowb * (rr - 1), fb, pol);
+            bulk_g2s(dm + static_cast<size_t>(rr - 1) * rowb, ph.last_row, rowb, fb, pol);
+          } else {
+            bulk_g2s(dm, src, rowb * rr, fb, pol);
+          }
+        }
+        fill_parity[pp.stage] = pp.round & 1u;
+        filled[pp.stage] = true;
+        pp.advance();
+      }
+    }
+  }
+  // Leave no copy in flight: wait for every stage whose last fill may not have landed.
+  for (int s = 0; s < kStages; ++s) {
+    if (!filled[s]) continue;
+    const long long t0 = clock_us();
+    while (!mbar_test(&S.full[s], fill_parity[s])) {
+      if (clock_us() - t0 > cp.ctl->spin_limit) {
+        if (atomicCAS(&cp.ctl->error, 0, S2_ETIMEOUT) == 0) cp.ctl->error_where = 3;
+        break;
+      }
+    }
+  }
+}
+
+// =========================================================================
+// GEMV phase:  y[c][r] = W[r,:] · xn[c]   (xn = RMSNorm(x)·normw, or x)
+// =========================================================================
+
+template <typename WT, int NC>
+__device__ void gemv_t(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe) {
+  constexpr int EPC = 16 / static_cast<int>(sizeof(WT));
+  constexpr int NCH = kXRegFloats / (EPC * NC);
+  const Dims& d = cp.d;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = ph.K, Q = ph.Q;
+  const int nchunk = K / EPC;
+  const int slice = (nchunk + Q - 1) / Q;
+  const int q = warp % Q, group = warp / Q, ngroups = kConsumerWarps / Q;
+  const int c_beg = q * slice, c_end = min(nchunk, c_beg + slice);
+  const bool writer = (blockIdx.x == 0) && (group == 0);
+  int r0, nr;
+  rows_of(ph, blockIdx.x, gridDim.x, r0, nr);
+
+  // ---- activation slices into registers
+  float xr[NC][NCH][EPC];
+  float ss[NC];
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    ss[c] = 0.f;
+    const GemvCol col = ph.col[c];
+    int tok = 0, codes[kMaxCodebooks];
+    float m = 0.f;
+    if (col.src == SRC_EMBED) {
+      const int* vals = static_cast<const int*>(col.p);
+      tok = ldcgi(vals);
+      m = (tok >= d.sem_lo && tok <= d.sem_hi) ? 1.f : 0.f;
+      for (int j = 0; j < d.ncb; ++j) codes[j] = ldcgi(vals + 1 + j);
+    } else if (col.src == SRC_FEROW) {
+      tok = ldcgi(static_cast<const int*>(col.p));
+    }
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      const int ch = c_beg + lane + 32 * i;
+      float* xv = xr[c][i];
+#pragma unroll
+      for (int j = 0; j < EPC; ++j) xv[j] = 0.f;
+      if (ch < c_end) {
+        const size_t e0 = static_cast<size_t>(ch) * EPC;
+        if (col.src == SRC_BUF) {
+          const float* xp = static_cast<const float*>(col.p) + e0;
+#pragma unroll
+          for (int j = 0; j < EPC; j += 4) {
+            float4 v = ldcg4(xp + j);
+            xv[j] = v.x; xv[j + 1] = v.y; xv[j + 2] = v.z; xv[j + 3] = v.w;
+          }
+        } else if (col.src == SRC_FEROW) {
+          const uint4 u = ldnc_u4(static_cast<const unsigned char*>(cp.FE) +
+                                  (static_cast<size_t>(tok) * K + e0) * sizeof(WT));
+          unpack16(u, xv, WT());
+        } else if (col.src == SRC_EMBED) {
+          float acc[EPC], er[EPC];
+#pragma unroll
+          for (int j = 0; j < EPC; ++j) acc[j] = 0.f;
+          for (int cb = 0; cb < d.ncb; ++cb) {
+            const size_t row = static_cast<size_t>(cb) * d.cbs + codes[cb];
+            const uint4 u = ldnc_u4(static_cast<const unsigned char*>(cp.CE) + (row * K + e0) * sizeof(WT));
+            float cv[EPC];
+            unpack16(u, cv, WT());
+#pragma unroll
+            for (int j = 0; j < EPC; ++j) acc[j] = __fadd_rn(acc[j], cv[j]);
+          }
+          const uint4 u = ldnc_u4(static_cast<const unsigned char*>(cp.E) + (static_cast<size_t>(tok) * K + e0) * sizeof(WT));
+          unpack16(u, er, WT());
+#pragma unroll
+          for (int j = 0; j < EPC; ++j) xv[j] = __fadd_rn(__fmul_rn(d.sem_scale, er[j]), __fmul_rn(m, acc[j]));
+        }
+        if (writer && col.wb != nullptr) {
+#pragma unroll
+          for (int j = 0; j < EPC; j += 4)
+            *reinterpret_cast<float4*>(col.wb + e0 + j) = make_float4(xv[j], xv[j + 1], xv[j + 2], xv[j + 3]);
+        }
+#pragma unroll
+        for (int j = 0; j < EPC; ++j) ss[c] += xv[j] * xv[j];
+      }
+    }
+  }
+
+  // ---- RMSNorm: every slice is held once by the warps of group 0
+  if (ph.normw != nullptr) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const float t = warp_sum(ss[c]);
+      if (group == 0 && lane == 0) S.misc[kMiscSS + q * NC + c] = t;
+    }
+  }
+  named_bar(1, kConsumers);
+  if (ph.normw != nullptr) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      float tot = 0.f;
+      for (int qq = 0; qq < Q; ++qq) tot += S.misc[kMiscSS + qq * NC + c];
+      const float r = 1.0f / sqrtf(tot / static_cast<float>(K) + d.eps);
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) {
+        const int ch = c_beg + lane + 32 * i;
+        if (ch < c_end) {
+          const size_t e0 = static_cast<size_t>(ch) * EPC;
+          float wv[EPC];
+          const uint4 u = ldnc_u4(static_cast<const unsigned char*>(ph.normw) + e0 * sizeof(WT));
+          unpack16(u, wv, WT());
+#pragma unroll
+          for (int j = 0; j < EPC; ++j) xr[c][i][j] = (xr[c][i][j] * r) * wv[j];
+          if (c == 0 && writer && ph.hid_out != nullptr) {
+#pragma unroll
+            for (int j = 0; j < EPC; j += 4)
+              *reinterpret_cast<float4*>(ph.hid_out + e0 + j) =
+                  make_float4(xr[0][i][j], xr[0][i][j + 1], xr[0][i][j + 2], xr[0][i][j + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  // ---- stream the CTA's row tiles
+  const int R = ph.rows_per_tile;
+  const int nmat = ph.nmat;
+  const size_t rowb = static_cast<size_t>(K) * sizeof(WT);
+  const int ntiles = (nr + R - 1) / R;
+  for (int t = 0; t < ntiles; ++t) {
+    const int rr = min(R, nr - t * R);
+    const bool ok = wait_bar(cp, S, &S.full[pipe.stage], pipe.round & 1u, 4, false);
+    if (!ok) S.fail = 1;
+    if (ok && (t % ngroups) == group) {
+      const unsigned char* base = S.ring[pipe.stage];
+      const int nv = rr * nmat;  // virtual rows: rr rows of matrix 0, then rr of matrix 1
+      for (int v0 = 0; v0 < nv; v0 += 4) {
+        float acc[4][NC];
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+#pragma unroll
+          for (int c = 0; c < NC; ++c) acc[v][c] = 0.f;
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+          const int ch = c_beg + lane + 32 * i;
+          if (ch < c_end) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              if (v0 + v < nv) {
+                const uint4 u = *reinterpret_cast<const uint4*>(base + (v0 + v) * rowb + static_cast<size_t>(ch) * 16);
+                float wf[EPC];
+                unpack16(u, wf, WT());
+#pragma unroll
+                for (int c = 0; c < NC; ++c)
+#pragma unroll
+                  for (int j = 0; j < EPC; ++j) acc[v][c] = fmaf(wf[j], xr[c][i][j], acc[v][c]);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+#pragma unroll
+          for (int c = 0; c < NC; ++c) acc[v][c] = warp_sum(acc[v][c]);
+        if (lane == 0) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            if (v0 + v < nv) {
+              const int mat = (v0 + v) / rr, rl = t * R + (v0 + v) % rr;
+#pragma unroll
+              for (int c = 0; c < NC; ++c) S.red[((rl * nmat + mat) * NC + c) * Q + q] = acc[v][c];
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[pipe.stage]);
+    pipe.advance();
+  }
+  named_bar(1, kConsumers);
+
+  // ---- epilogue: sum the slices in fixed order, apply the output rule
+  if (!S.fail) {
+    const int nout = nr * NC;
+    for (int idx = threadIdx.x; idx < nout; idx += kConsumers) {
+      const int rl = idx / NC, c = idx % NC;
+      float a = 0.f, b = 0.f;
+      for (int qq = 0; qq < Q; ++qq) a += S.red[((rl * nmat + 0) * NC + c) * Q + qq];
+      if (nmat == 2)
+        for (int qq = 0; qq < Q; ++qq) b += S.red[((rl * nmat + 1) * NC + c) * Q + qq];
+      float* y = ph.y[c] + r0 + rl;
+      if (ph.epi == EPI_STORE) {
+        *y = a;
+      } else if (ph.epi == EPI_ADD) {
+        *y = ldcg(y) + a;
+      } else {
+        *y = (a / (1.0f + expf(-a))) * b;
+      }
+    }
+  }
+}
+
+__device__ void gemv(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe) {
+  if (cp.d.wdt == S2_BF16) {
+    if (ph.ncols == 1) gemv_t<uint16_t, 1>(cp, ph, S, pipe);
+    else gemv_t<uint16_t, 2>(cp, ph, S, pipe);
+  } else {
+    if (ph.ncols == 1) gemv_t<float, 1>(cp, ph, S, pipe);
+    else gemv_t<float, 2>(cp, ph, S, pipe);
+  }
+}
+
+// =========================================================================
+// per-head RMSNorm + RoPE of one head vector held by a warp (lane holds DPL contiguous values)
+// =========================================================================
+
+template <int DPL>
+__device__ __forceinline__ void head_norm_rope(float (&v)[DPL], const void* nw, int esz, float eps, int hd,
+                                               bool norm, const float2* rope_row) {
+  const int lane = threadIdx.x & 31;
+  if (norm) {
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) s += v[j] * v[j];
+    s = warp_sum(s);
+    const float r = 1.0f / sqrtf(s / static_cast<float>(hd) + eps);
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) v[j] = (v[j] * r) * wload(nw, lane * DPL + j, esz);
+  }
+#pragma unroll
+  for (int j = 0; j < DPL; j += 2) {
+    const float2 cs = rope_row[(lane * DPL + j) >> 1];
+    const float a = v[j], b = v[j + 1];
+    v[j] = a * cs.x - b * cs.y;
+    v[j + 1] = a * cs.y + b * cs.x;
+  }
+}
+
+template <typename KT>
+__device__ __forceinline__ float kv_to_f(KT x);
+template <>
+__device__ __forceinline__ float kv_to_f<__half>(__half x) { return __half2float(x); }
+template <>
+__device__ __forceinline__ float kv_to_f<float>(float x) { return x; }
+template <typename KT>
+__device__ __forceinline__ KT f_to_kv(float x);
+template <>
+__device__ __forceinline__ __half f_to_kv<__half>(float x) { return __float2half_rn(x); }
+template <>
+__device__ __forceinline__ float f_to_kv<float>(float x) { return x; }
+
+// =========================================================================
+// Slow-AR attention: q/k norm + RoPE, KV store of the new slot, split-K decode attention
+// over slots 0..pos with a last-arriver combine per KV head.
+// =========================================================================
+
+template <typename KT, int HD>
+__device__ void attn_slow_t(const CallParams& cp, const Phase& ph, Smem& S) {
+  constexpr int DPL = HD / 32;
+  const Dims& d = cp.d;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rep = d.Hq / d.Hkv;
+  const int pos = ldcgi(&cp.st->pos);
+  const int n = pos + 1;
+  const int G = gridDim.x;
+  int ns = max(1, min(G / d.Hkv, (n + 31) / 32));
+  ns = max(ns, (n + kAttnMaxChunk - 1) / kAttnMaxChunk);
+  const int chunk = (n + ns - 1) / ns;
+  ns = (n + chunk - 1) / chunk;
+  const int nitems = d.Hkv * ns;
+  const float sc_mul = ph.scale;  // 1/sqrt(head_dim)
+  const size_t kvh = static_cast<size_t>(cp.kv_slots) * HD;  // elements per KV head
+  const KT* Kc = static_cast<const KT*>(ph.kc);
+  const KT* Vc = static_cast<const KT*>(ph.vc);
+  const float2* rope_row = cp.rope + static_cast<size_t>(pos) * (HD / 2);
+  float* qs = S.misc + kMiscQ;
+  float* knew = S.misc + kMiscKV;
+  float* vnew = S.misc + kMiscKV + 128;
+  float* wp = S.misc + kMiscWarp;
+
+  for (int item = blockIdx.x; item < nitems; item += G) {
+    const int g = item / ns, s = item % ns;
+    const int j0 = s * chunk, j1 = min(n, j0 + chunk);
+    const bool has_new = (j1 == n);
+    if (warp < rep) {
+      const int h = g * rep + warp;
+      float v[DPL];
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) v[j] = ldcg(ph.qkv + h * HD + lane * DPL + j);
+      head_norm_rope<DPL>(v, ph.qn, d.esz, d.eps, HD, d.qk_norm != 0, rope_row);
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) qs[warp * HD + lane * DPL + j] = v[j];
+    } else if (warp == rep && has_new) {
+      float k[DPL], v[DPL];
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) {
+        k[j] = ldcg(ph.qkv + (d.Hq + g) * HD + lane * DPL + j);
+        v[j] = ldcg(ph.qkv + (d.Hq + d.Hkv + g) * HD + lane * DPL + j);
+      }
+      head_norm_rope<DPL>(k, ph.kn, d.esz, d.eps, HD, d.qk_norm != 0, rope_row);
+      KT* kd = const_cast<KT*>(Kc) + g * kvh + static_cast<size_t>(pos) * HD + lane * DPL;
+      KT* vd = const_cast<KT*>(Vc) + g * kvh + static_cast<size_t>(pos) * HD + lane * DPL;
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) {
+        const KT kq = f_to_kv<KT>(k[j]), vq = f_to_kv<KT>(v[j]);
+        kd[j] = kq;
+        vd[j] = vq;
+        knew[lane * DPL + j] = kv_to_f<KT>(kq);
+        vnew[lane * DPL + j] = kv_to_f<KT>(vq);
+      }
+    }
+    named_bar(1, kConsumers);
+
+    // each warp: a contiguous sub-range of [j0, j1), lane-per-slot scores, online softmax
+    float mr[4], lr[4], acc[4][DPL];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      mr[r] = -INFINITY;
+      lr[r] = 0.f;
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) acc[r][j] = 0.f;
+    }
+    const int len = j1 - j0;
+    const int per = (len + kConsumerWarps - 1) / kConsumerWarps;
+    const int a0 = j0 + warp * per, a1 = min(j1, a0 + per);
+    for (int b0 = a0; b0 < a1; b0 += 32) {
+      const int j = b0 + lane;
+      const int nvalid = min(32, a1 - b0);
+      const bool valid = lane < nvalid;
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (valid) {
+        if (j == pos) {
+          for (int e = 0; e < HD; ++e) {
+            const float kv = knew[e];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+              if (r < rep) sc[r] = fmaf(qs[r * HD + e], kv, sc[r]);
+          }
+        } else {
+          const KT* kr = Kc + g * kvh + static_cast<size_t>(j) * HD;
+          constexpr int EPV = 16 / sizeof(KT);
+#pragma unroll 4
+          for (int e0 = 0; e0 < HD; e0 += EPV) {
+            const uint4 u = ldcg_u4(kr + e0);
+            float kf[EPV];
+            if constexpr (sizeof(KT) == 2) {
+              const __half2* h2 = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const float2 f2 = __half22float2(h2[t]);
+                kf[2 * t] = f2.x;
+                kf[2 * t + 1] = f2.y;
+              }
+            } else {
+              kf[0] = __uint_as_float(u.x); kf[1] = __uint_as_float(u.y);
+              kf[2] = __uint_as_float(u.z); kf[3] = __uint_as_float(u.w);
+            }
+#pragma unroll
+            for (int t = 0; t < EPV; ++t)
+#pragma unroll
+              for (int r = 0; r < 4; ++r)
+                if (r < rep) sc[r] = fmaf(qs[r * HD + e0 + t], kf[t], sc[r]);
+          }
+        }
+      }
+      float p[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        if (r >= rep) continue;
+        const float s_ = valid ? sc[r] * sc_mul : -INFINITY;
+        const float mb = warp_max(s_);
+        const float mnew = fmaxf(mr[r], mb);
+        const float alpha = expf(mr[r] - mnew);
+        p[r] = valid ? expf(s_ - mnew) : 0.f;
+        lr[r] = lr[r] * alpha + warp_sum(p[r]);
+#pragma unroll
+        for (int j2 = 0; j2 < DPL; ++j2) acc[r][j2] *= alpha;
+        mr[r] = mnew;
+      }
+      for (int jj = 0; jj < nvalid; ++jj) {
+        const int slot = b0 + jj;
+        float vv[DPL];
+        if (slot == pos) {
+#pragma unroll
+          for (int j2 = 0; j2 < DPL; ++j2) vv[j2] = vnew[lane * DPL + j2];
+        } else {
+          const KT* vr = Vc + g * kvh + static_cast<size_t>(slot) * HD + lane * DPL;
+          if constexpr (sizeof(KT) == 2) {
+            if constexpr (DPL == 4) {
+              const uint2 u = ldcg_u2(vr);
+              const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+              const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+              vv[0] = f0.x; vv[1] = f0.y; vv[2] = f1.x; vv[3] = f1.y;
+            } else {
+              const unsigned u = __ldcg(reinterpret_cast<const unsigned*>(vr));
+              const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&u));
+              vv[0] = f0.x; vv[1] = f0.y;
+            }
+          } else {
+#pragma unroll
+            for (int j2 = 0; j2 < DPL; ++j2) vv[j2] = ldcg(reinterpret_cast<const float*>(vr) + j2);
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          if (r >= rep) continue;
+          const float pj = __shfl_sync(0xffffffffu, p[r], jj);
+#pragma unroll
+          for (int j2 = 0; j2 < DPL; ++j2) acc[r][j2] = fmaf(pj, vv[j2], acc[r][j2]);
+        }
+      }
+    }
+    // warp partials -> smem
+    for (int r = 0; r < rep; ++r) {
+      float* o = wp + (warp * 4 + r) * (HD + 2);
+#pragma unroll
+      for (int j2 = 0; j2 < DPL; ++j2) o[lane * DPL + j2] = acc[r][j2];
+      if (lane == 0) {
+        o[HD] = mr[r];
+        o[HD + 1] = lr[r];
+      }
+    }
+    named_bar(1, kConsumers);
+    // CTA partial of this item -> global
+    float* part = cp.part + static_cast<size_t>(item) * 4 * (HD + 2);
+    for (int idx = threadIdx.x; idx < rep * HD; idx += kConsumers) {
+      const int r = idx / HD, e = idx % HD;
+      float M = -INFINITY;
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, wp[(w * 4 + r) * (HD + 2) + HD]);
+      float o = 0.f, l = 0.f;
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float* src = wp + (w * 4 + r) * (HD + 2);
+        const float sc2 = src[HD] == -INFINITY ? 0.f : expf(src[HD] - M);
+        o += src[e] * sc2;
+        l += src[HD + 1] * sc2;
+      }
+      part[r * (HD + 2) + e] = o;
+      if (e == 0) {
+        part[r * (HD + 2) + HD] = M;
+        part[r * (HD + 2) + HD + 1] = l;
+      }
+    }
+    __threadfence();
+    named_bar(1, kConsumers);
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const unsigned t = atomicAdd(&cp.ctl->tickets[g], 1u);
+      S.flag = (t == static_cast<unsigned>(ns - 1)) ? 1 : 0;
+      if (S.flag) {
+        __threadfence();
+        cp.ctl->tickets[g] = 0u;
+      }
+    }
+    named_bar(1, kConsumers);
+    if (S.flag) {
+      // last arriver for KV head g: combine the ns partials in split order
+      for (int idx = threadIdx.x; idx < rep * HD; idx += kConsumers) {
+        const int r = idx / HD, e = idx % HD;
+        float M = -INFINITY;
+        for (int s2i = 0; s2i < ns; ++s2i) {
+          const float* pp = cp.part + static_cast<size_t>(g * ns + s2i) * 4 * (HD + 2) + r * (HD + 2);
+          M = fmaxf(M, ldcg(pp + HD));
+        }
+        float o = 0.f, l = 0.f;
+        for (int s2i = 0; s2i < ns; ++s2i) {
+          const float* pp = cp.part + static_cast<size_t>(g * ns + s2i) * 4 * (HD + 2) + r * (HD + 2);
+          const float w = expf(ldcg(pp + HD) - M);
+          o += ldcg(pp + e) * w;
+          l += ldcg(pp + HD + 1) * w;
+        }
+        ph.out[(g * rep + r) * HD + e] = o / l;
+      }
+    }
+    named_bar(1, kConsumers);
+  }
+}
+
+__device__ void attn_slow(const CallParams& cp, const Phase& ph, Smem& S) {
+  if (cp.d.kvdt == S2_F16) {
+    if (cp.d.hd == 128) attn_slow_t<__half, 128>(cp, ph, S);
+    else attn_slow_t<__half, 64>(cp, ph, S);
+  } else {
+    if (cp.d.hd == 128) attn_slow_t<float, 128>(cp, ph, S);
+    else attn_slow_t<float, 64>(cp, ph, S);
+  }
+}
+
+// =========================================================================
+// Fast-AR attention over the frame's window (positions 0..pos0+npos-1), causal offset 0.
+// One warp per (new position, query head); the within-frame K/V (fp32) of earlier positions
+// come from the window cache, the new ones are recomputed by each warp that needs them.
+// =========================================================================
+
+template <int HD>
+__device__ void attn_fast_t(const CallParams& cp, const Phase& ph, Smem& S) {
+  constexpr int DPL = HD / 32;
+  const Dims& d = cp.d;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = d.Hqf, Hk = d.Hkvf, rep = H / Hk;
+  const int QKV = (H + 2 * Hk) * HD;
+  const int nitems = ph.npos * H;
+  const int G = gridDim.x;
+  const float sc_mul = ph.scale;
+  float* kc = static_cast<float*>(ph.kc);  // [Wf][Hk][HD]
+  float* vc = static_cast<float*>(ph.vc);
+  for (int item = blockIdx.x + G * warp; item < nitems; item += G * kConsumerWarps) {
+    const int jn = item / H, h = item % H, g = h / rep;
+    const int p = ph.pos0 + jn;
+    float q[DPL];
+    const float* qrow = ph.qkv + static_cast<size_t>(jn) * QKV;
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) q[j] = ldcg(qrow + h * HD + lane * DPL + j);
+    head_norm_rope<DPL>(q, ph.qn, d.esz, d.eps, HD, d.qk_norm != 0, cp.rope_f + static_cast<size_t>(p) * (HD / 2));
+    float sc[16];
+    float kk[16][DPL];  // keys of slots 0..p (p <= 10)
+    float vv[16][DPL];
+    for (int s = 0; s <= p; ++s) {
+      if (s >= ph.pos0) {
+        const float* r = ph.qkv + static_cast<size_t>(s - ph.pos0) * QKV;
+        float k[DPL], v[DPL];
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) {
+          k[j] = ldcg(r + (H + g) * HD + lane * DPL + j);
+          v[j] = ldcg(r + (H + Hk + g) * HD + lane * DPL + j);
+        }
+        head_norm_rope<DPL>(k, ph.kn, d.esz, d.eps, HD, d.qk_norm != 0, cp.rope_f + static_cast<size_t>(s) * (HD / 2));
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) {
+          kk[s][j] = k[j];
+          vv[s][j] = v[j];
+        }
+        if (s == p && (h % rep) == 0) {
+#pragma unroll
+          for (int j = 0; j < DPL; ++j) {
+            kc[(static_cast<size_t>(s) * Hk + g) * HD + lane * DPL + j] = k[j];
+            vc[(static_cast<size_t>(s) * Hk + g) * HD + lane * DPL + j] = v[j];
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) {
+          kk[s][j] = ldcg(kc + (static_cast<size_t>(s) * Hk + g) * HD + lane * DPL + j);
+          vv[s][j] = ldcg(vc + (static_cast<size_t>(s) * Hk + g) * HD + lane * DPL + j);
+        }
+      }
+      float dot = 0.f;
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) dot += q[j] * kk[s][j];
+      sc[s] = warp_sum(dot) * sc_mul;
+    }
+    float m = -INFINITY;
+    for (int s = 0; s <= p; ++s) m = fmaxf(m, sc[s]);
+    float l = 0.f;
+    for (int s = 0; s <= p; ++s) {
+      sc[s] = expf(sc[s] - m);
+      l += sc[s];
+    }
+    float o[DPL];
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) o[j] = 0.f;
+    for (int s = 0; s <= p; ++s) {
+      const float pr = sc[s] / l;
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) o[j] += pr * vv[s][j];
+    }
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) ph.out[static_cast<size_t>(jn) * (H * HD) + h * HD + lane * DPL + j] = o[j];
+  }
+}
+
+__device__ void attn_fast(const CallParams& cp, const Phase& ph, Smem& S) {
+  if (cp.d.hdf == 128) attn_fast_t<128>(cp, ph, S);
+  else attn_fast_t<64>(cp, ph, S);
+}
+
+// =========================================================================
+// sampler (CTA 0): top-30 by (value desc, id asc), softmax, top-p (keep rank r iff r == 0 or
+// Σ_{s<r} π_s < p), winner = argmax π_r / E_r (ties -> lower rank)
+// =========================================================================
+
+constexpr int kSampPer = 17;  // values per thread: 256 * 17 >= 4097
+
+// id of entry i of a logits vector: main (admissible) -> token id; fast -> code
+__device__ __forceinline__ int entry_id(const Dims& d, bool main, int i) {
+  return main ? (i < d.cbs ? d.sem_lo + i : d.im_end) : i;
+}
+
+__device__ __forceinline__ bool better(float za, int ia, float zb, int ib) {
+  return za > zb || (za == zb && ia < ib);
+}
+
+// Returns the drawn token (same value in every consumer thread); -1 if nothing is drawable.
+__device__ int draw(const CallParams& cp, Smem& S, const float* logits, int n, bool main, bool mask_end,
+                    float temperature, float top_p, const float* E) {
+  const Dims& d = cp.d;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float zv[kSampPer];
+  int iv[kSampPer];
+#pragma unroll
+  for (int k = 0; k < kSampPer; ++k) {
+    const int i = tid + k * kConsumers;
+    zv[k] = -INFINITY;
+    iv[k] = 0x7fffffff;
+    if (i < n) {
+      const int id = entry_id(d, main, i);
+      const float l = ldcg(logits + i);
+      if (!(mask_end && main && id == d.im_end) && isfinite(l)) {
+        zv[k] = l / temperature;
+        iv[k] = id;
+      }
+    }
+  }
+  float* cz = S.misc + kMiscSamp;                       // [32] candidate z
+  int* ci = reinterpret_cast<int*>(S.misc + kMiscSamp + 32);   // [32] candidate ids
+  float* wz = S.misc + kMiscSamp + 64;                  // [8] warp winners
+  int* wi = reinterpret_cast<int*>(S.misc + kMiscSamp + 72);
+  int* res = reinterpret_cast<int*>(S.misc + kMiscSamp + 80);
+  int kk = 0;
+  for (int r = 0; r < kTopK; ++r) {
+    float bz = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int k = 0; k < kSampPer; ++k)
+      if (better(zv[k], iv[k], bz, bi)) {
+        bz = zv[k];
+        bi = iv[k];
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float oz = __shfl_xor_sync(0xffffffffu, bz, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (better(oz, oi, bz, bi)) {
+        bz = oz;
+        bi = oi;
+      }
+    }
+    if (lane == 0) {
+      wz[warp] = bz;
+      wi[warp] = bi;
+    }
+    named_bar(1, kConsumers);
+    float gz = wz[0];
+    int gi = wi[0];
+    for (int w = 1; w < kConsumerWarps; ++w)
+      if (better(wz[w], wi[w], gz, gi)) {
+        gz = wz[w];
+        gi = wi[w];
+      }
+    if (gi == 0x7fffffff || gz == -INFINITY) {
+      named_bar(1, kConsumers);
+      break;
+    }
+    if (tid == 0) {
+      cz[r] = gz;
+      ci[r] = gi;
+    }
+#pragma unroll
+    for (int k = 0; k < kSampPer; ++k)
+      if (iv[k] == gi) {
+        zv[k] = -INFINITY;
+        iv[k] = 0x7fffffff;
+      }
+    kk = r + 1;
+    named_bar(1, kConsumers);
+  }
+  if (tid == 0) {
+    int tok = -1;
+    if (kk > 0) {
+      float pi[kTopK];
+      const float zmax = cz[0];
+      float sum = 0.f;
+      for (int r = 0; r < kk; ++r) {
+        pi[r] = expf(cz[r] - zmax);
+        sum += pi[r];
+      }
+      for (int r = 0; r < kk; ++r) pi[r] = pi[r] / sum;
+      float cum = 0.f;
+      int kept = 0;
+      for (int r = 0; r < kk; ++r) {
+        if (r == 0 || cum < top_p) kept = r + 1;
+        else break;
+        cum += pi[r];
+      }
+      int best = 0;
+      float bq = pi[0] / ldcg(E);
+      for (int r = 1; r < kept; ++r) {
+        const float qv = pi[r] / ldcg(E + r);
+        if (qv > bq) {
+          best = r;
+          bq = qv;
+        }
+      }
+      tok = ci[best];
+    }
+    *res = tok;
+  }
+  named_bar(1, kConsumers);
+  const int out = *res;
+  named_bar(1, kConsumers);
+  return out;
+}
+
+// caller-supplied ids (forced draws, Fast-AR-alone prefixes) are checked before any use as an index
+__device__ __forceinline__ int checked_id(const CallParams& cp, int v, int hi) {
+  if (v < 0 || v >= hi) {
+    atomicCAS(&cp.ctl->error, 0, S2_EINVAL);
+    return 0;
+  }
+  return v;
+}
+
+__device__ void copy_vec(float* dst, const float* src, int n) {
+  for (int i = threadIdx.x; i < n; i += kConsumers) dst[i] = ldcg(src + i);
+}
+
+// main draw, repetition-aware redraw, clamp, stop (CTA 0)
+__device__ void sample_main(const CallParams& cp, Smem& S, int f) {
+  const Dims& d = cp.d;
+  StreamState* st = cp.st;
+  const int fd = ldcgi(&st->frames_done);
+  if (cp.dbg_main) copy_vec(cp.dbg_main + static_cast<size_t>(f) * d.A, cp.logits, d.A);
+  if (cp.dbg_hidden) copy_vec(cp.dbg_hidden + static_cast<size_t>(f) * d.D, cp.hidden, d.D);
+  const float* E = cp.expo + static_cast<size_t>(f) * kDraws * kTopK;
+  const bool block_end = fd < cp.min_tokens;
+  int d0 = draw(cp, S, cp.logits, d.A, true, block_end, cp.temperature, cp.top_p, E);
+  if (threadIdx.x == 0) {
+    if (cp.dbg_draws) cp.dbg_draws[f * kDraws + 0] = d0;
+    if (cp.forced) {
+      d0 = cp.forced[f * kDraws + 0];
+      if (d0 < 0 || d0 >= d.V) {
+        atomicCAS(&cp.ctl->error, 0, S2_EINVAL);
+        d0 = d.im_end;  // an invalid forced token ends the stream
+      }
+    }
+    S.flag = d0;
+  }
+  named_bar(1, kConsumers);
+  d0 = S.flag;
+  named_bar(1, kConsumers);
+  if (d0 == d.im_end || d0 < 0) {
+    if (threadIdx.x == 0) {
+      st->done = 1;
+      st->n_out = f;
+      if (cp.dbg_draws)
+        for (int k = 1; k < kDraws; ++k) cp.dbg_draws[f * kDraws + k] = -1;
+    }
+    return;
+  }
+  int d1 = draw(cp, S, cp.logits, d.A, true, block_end, cp.ras_temperature, cp.ras_top_p, E + kTopK);
+  if (threadIdx.x == 0) {
+    if (cp.dbg_draws) cp.dbg_draws[f * kDraws + 1] = d1;
+    if (cp.forced) d1 = checked_id(cp, cp.forced[f * kDraws + 1], d.V);
+    if (d1 < 0) d1 = d0;
+    const int wl = st->wlen;
+    bool seen = false;
+    for (int i = 0; i < wl; ++i) seen |= (st->window[i] == d0);
+    const bool trig = seen && d0 >= d.sem_lo && d0 <= d.sem_hi;
+    const int tok = trig ? d1 : d0;
+    int code0 = tok - d.sem_lo;
+    code0 = code0 < 0 ? 0 : (code0 > d.cbs - 1 ? d.cbs - 1 : code0);
+    st->vals[0] = tok;
+    st->vals[1] = code0;
+    cp.fcode[0] = code0;
+    cp.stage[static_cast<size_t>(f) * d.ncb + 0] = code0;
+    if (wl < cp.ras_window) {
+      st->window[wl] = tok;
+      st->wlen = wl + 1;
+    } else {
+      for (int i = 1; i < wl; ++i) st->window[i - 1] = st->window[i];
+      st->window[wl - 1] = tok;
+    }
+    st->frames_done = fd + 1;
+  }
+}
+
+// one Fast-AR draw (CTA 0), codebook c = 1..NCB-1
+__device__ void sample_fast(const CallParams& cp, Smem& S, int f, int c) {
+  const Dims& d = cp.d;
+  if (cp.fast_only) {
+    copy_vec(cp.fout + (static_cast<size_t>(f) * (d.ncb - 1) + (c - 1)) * d.cbs, cp.flogits, d.cbs);
+    if (threadIdx.x == 0 && c < d.ncb - 1) cp.fcode[c] = checked_id(cp, cp.fin_prefix[f * (d.ncb - 1) + c], d.cbs);
+    return;
+  }
+  if (cp.dbg_fast) copy_vec(cp.dbg_fast + (static_cast<size_t>(f) * (d.ncb - 1) + (c - 1)) * d.cbs, cp.flogits, d.cbs);
+  const float* E = cp.expo + static_cast<size_t>(f) * kDraws * kTopK + (1 + c) * kTopK;
+  int dc = draw(cp, S, cp.flogits, d.cbs, false, false, cp.temperature, cp.top_p, E);
+  if (threadIdx.x == 0) {
+    if (cp.dbg_draws) cp.dbg_draws[f * kDraws + 1 + c] = dc;
+    if (cp.forced) dc = checked_id(cp, cp.forced[f * kDraws + 1 + c], d.cbs);
+    if (dc < 0) dc = 0;  // nothing drawable: the remaining codes are 0 (ch.06 §5.2)
+    cp.fcode[c] = dc;
+    cp.st->vals[1 + c] = dc;
+    cp.stage[static_cast<size_t>(f) * d.ncb + c] = dc;
+    if (c == d.ncb - 1) cp.st->n_out = f + 1;
+  }
+}
+
+// Fast-AR-alone mode: the frame's hidden and first prefix code (CTA 0)
+__device__ void fast_in(const CallParams& cp, int f) {
+  const Dims& d = cp.d;
+  for (int i = threadIdx.x; i < d.D; i += kConsumers) cp.hidden[i] = cp.fin_hidden[static_cast<size_t>(f) * d.D + i];
+  if (threadIdx.x == 0) cp.fcode[0] = checked_id(cp, cp.fin_prefix[f * (d.ncb - 1)], d.cbs);
+}
+
+// =========================================================================
+// consumers
+// =========================================================================
+
+__device__ void consumers(const CallParams& cp, Smem& S) {
+  Pipe pipe{0, 0};
+  unsigned target = 0;
+  const bool cta0 = blockIdx.x == 0;
+  if (!cp.fast_only && ldcgi(&cp.st->done) != 0) {
+    if (cta0 && threadIdx.x == 0) cp.st->n_out = 0;
+    return;
+  }
+  if (cta0 && threadIdx.x == 0) cp.st->n_out = 0;
+  for (int f = 0; f < cp.n_frames; ++f) {
+    for (int p = 0; p < cp.n_phases; ++p) {
+      const Phase& ph = cp.prog[p];
+      switch (ph.op) {
+        case OP_GEMV:
+          if (ph.merge_main && cta0) sample_main(cp, S, f);
+          else gemv(cp, ph, S, pipe);
+          break;
+        case OP_ATTN_SLOW:
+          attn_slow(cp, ph, S);
+          break;
+        case OP_ATTN_FAST:
+          attn_fast(cp, ph, S);
+          break;
+        case OP_SAMPLE_FAST:
+          if (cta0) sample_fast(cp, S, f, ph.cb);
+          break;
+        case OP_SAMPLE_MAIN:
+          if (cta0) sample_main(cp, S, f);
+          break;
+        case OP_FAST_IN:
+          if (cta0) fast_in(cp, f);
+          break;
+        default:
+          break;
+      }
+      if (ph.bump_pos && cta0 && threadIdx.x == 0) {
+        cp.st->pos = cp.st->pos + 1;  // the Slow-AR step's last phase: its slot is now filled
+      }
+      if (!grid_sync(cp, S, target)) return;
+      if ((ph.op == OP_SAMPLE_MAIN || ph.merge_main) && ldcgi(&cp.st->done) != 0) return;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) frame_kernel(const CallParams cp) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], kConsumerWarps);
+    }
+    S.abort_flag = 0;
+    S.fail = 0;
+    S.sync_ok = 1;
+    S.flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x >= kConsumers) {
+    producer(cp, S);
+  } else {
+    consumers(cp, S);
+    named_bar(1, kConsumers);
+    if (threadIdx.x == 0) {
+      __threadfence_block();
+      *reinterpret_cast<volatile int*>(&S.abort_flag) = 1;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+int frame_kernel_grid(int device, int* grid_out) {
+  const int smem = static_cast<int>(sizeof(Smem));
+  if (cudaFuncSetAttribute(frame_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return S2_ECUDA;
+  int per_sm = 0, sms = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, frame_kernel, kThreads, smem) != cudaSuccess)
+    return S2_ECUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return S2_ECUDA;
+  if (per_sm < 1) return S2_ECUDA;
+  *grid_out = sms;  // one CTA per SM
+  return S2_OK;
+}
+
+int launch_frames(const CallParams& cp, int grid, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(&cp.ctl->gbar, 0, sizeof(unsigned), s) != cudaSuccess) return S2_ECUDA;
+  void* args[] = {const_cast<CallParams*>(&cp)};
+  const cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(frame_kernel), dim3(grid),
+                                                    dim3(kThreads), args, sizeof(Smem), s);
+  return e == cudaSuccess ? S2_OK : S2_ECUDA;
+}
+
+size_t frame_kernel_smem() { return sizeof(Smem); }
+
+}  // namespace s2

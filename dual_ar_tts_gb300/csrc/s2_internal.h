@@ -1,0 +1,187 @@
+// Internal definitions of the frame engine shared by its translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/s2frame.h"
+
+namespace s2 {
+
+// ---------------------------------------------------------------- constants
+
+constexpr int kTopK = 30;              // fixed top-k (Mizuoto "Fish Speech" page)
+constexpr int kDraws = 11;             // main, redraw, codebooks 1..9
+constexpr int kMaxCodebooks = 15;      // vals[] holds NCB+1 <= 16 ids
+constexpr int kMaxWindow = 16;         // RAS window capacity (ras_window <= 10 used)
+constexpr int kMaxFramesPerCall = 8192;
+
+// persistent frame kernel geometry
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = 32 * kConsumerWarps;
+constexpr int kThreads = kConsumers + 32;      // + one producer warp
+constexpr int kStages = 9;                     // weight ring depth
+constexpr int kStageBytes = 20480;             // one tile: 4 rows of 2560 bf16, 1 row of 9728 bf16
+constexpr int kRedFloats = 4096;               // per-CTA partial sums (GEMV row × slice)
+constexpr int kXRegFloats = 80;                // activation slice per lane held in registers
+constexpr int kAttnMaxChunk = 2048;            // slots per split-K attention item
+
+enum Op : int {
+  OP_GEMV = 1,       // y = W·normed(x) with epilogue; may carry a main draw on CTA 0
+  OP_ATTN_SLOW,      // q/k norm + RoPE + KV store of the new slot + split-K attention + combine
+  OP_ATTN_FAST,      // Fast-AR attention over the within-frame window
+  OP_SAMPLE_FAST,    // one Fast-AR draw (CTA 0)
+  OP_FAST_IN,        // Fast-AR-alone mode: load the frame's hidden and prefix (CTA 0)
+  OP_SAMPLE_MAIN,    // main draw + redraw + RAS + clamp (CTA 0) when not merged into a GEMV
+};
+
+enum Src : int { SRC_NONE = 0, SRC_BUF, SRC_EMBED, SRC_FEROW };
+enum Epi : int { EPI_STORE = 0, EPI_ADD, EPI_SWIGLU };
+
+// --------------------------------------------------------------- the model
+
+struct Dims {
+  int D, L, Hq, Hkv, hd, F, V;
+  int sem_lo, sem_hi, im_end, ncb, cbs;
+  float sem_scale, eps;
+  double rope_base;
+  int qk_norm, rope_bf16;
+  int Df, Lf, Hqf, Hkvf, hdf, Ff, Wf, has_proj;
+  int wdt;       // S2_F32 / S2_BF16
+  int kvdt;      // S2_F32 / S2_F16
+  int esz;       // weight element bytes
+  int kvsz;      // KV element bytes
+  int A;         // admissible logits = cbs + 1
+};
+
+struct LayerW {
+  const void *an, *wqkv, *qn, *kn, *wo, *fn, *w1, *w3, *w2;
+};
+
+// ------------------------------------------------------- device-side state
+
+struct StreamState {
+  int pos;           // KV slots filled
+  int frames_done;   // frames emitted since prefill
+  int done;          // im_end drawn
+  int prefilled;
+  int wlen;          // RAS window length
+  int n_out;         // frames emitted by the current call
+  int status;
+  int pad0;
+  int window[kMaxWindow];  // oldest first
+  int vals[16];            // next Slow-AR input: [token, code_0..code_{NCB-1}]
+};
+
+struct Control {
+  unsigned gbar;            // grid barrier counter (reset before each launch)
+  int error;                // device-detected failure (S2_ETIMEOUT) of any launch
+  int error_where;          // which wait gave up
+  int pad;
+  long long spin_limit;     // wait bound in ~1 µs units
+  unsigned tickets[64];     // split-K attention: arrivals per KV head
+};
+
+// ------------------------------------------------------------ the program
+
+struct GemvCol {
+  int src;            // Src
+  int pad;
+  const void* p;      // SRC_BUF: float[K]; SRC_EMBED: int[NCB+1]; SRC_FEROW: int* code
+  float* wb;          // nullable: CTA 0 writes the raw (pre-norm) column here
+};
+
+struct Phase {
+  int op;
+  int merge_main;     // OP_GEMV: CTA 0 performs the main draw instead of GEMV rows
+  int cta0;           // first CTA doing GEMV rows
+  int M, K, nmat, ncols, epi, rows_per_tile, Q;
+  const void* w[2];   // row-major [M][K]; w[1] is the gate partner for EPI_SWIGLU
+  const void* last_row;  // nullable: source of row M-1 (admissible logits: im_end row)
+  const void* normw;     // nullable RMSNorm weight [K]
+  float* hid_out;        // nullable: CTA 0 writes normalised column 0 here
+  GemvCol col[2];
+  float* y[2];           // per-column output [M]
+  // attention
+  int layer, npos, pos0, cb;
+  int bump_pos;          // CTA 0 advances the stream position after this phase
+  float scale;           // attention: 1/sqrt(head_dim)
+  const float* qkv;      // [npos][QKV]
+  float* out;            // [npos][Hq*hd]
+  void* kc;              // Slow: K cache of this layer/stream [Hkv][slots][hd]; Fast: [W][Hkv][hd] fp32
+  void* vc;
+  const void* qn;
+  const void* kn;
+};
+
+struct CallParams {
+  int n_frames;
+  int fast_only;
+  int n_phases;
+  int stream;
+  const Phase* prog;
+  StreamState* st;
+  float* hidden;          // [D] normalised Slow-AR hidden of the stream
+  float* logits;          // [A] admissible Slow-AR logits of the stream
+  int32_t* stage;         // [n_frames][NCB] emitted codes
+  const float* expo;      // [n_frames][11][30]
+  const int32_t* forced;  // [n_frames][11] or null
+  float* dbg_main;        // [n_frames][A] or null
+  float* dbg_fast;        // [n_frames][NCB-1][CBS] or null
+  float* dbg_hidden;      // [n_frames][D] or null
+  int32_t* dbg_draws;     // [n_frames][11] or null
+  // Fast-AR alone
+  const float* fin_hidden;    // [n_frames][D]
+  const int32_t* fin_prefix;  // [n_frames][NCB-1]
+  float* fout;                // [n_frames][NCB-1][CBS]
+  // sampling
+  float temperature, top_p, ras_temperature, ras_top_p;
+  int ras_window, min_tokens;
+  // scratch
+  float* part;            // split-K partials
+  int32_t* fcode;         // [NCB] Fast-AR codes of the frame
+  float* flogits;         // [CBS]
+  const float2* rope;     // Slow-AR table [slots][hd/2]
+  const float2* rope_f;   // Fast-AR table [Wf][hdf/2]
+  Control* ctl;
+  Dims d;
+  // weights for sampling / inputs
+  const void* E;
+  const void* CE;
+  const void* FE;
+  int kv_slots;
+};
+
+// host entry points between translation units
+int launch_frames(const CallParams& cp, int grid, void* stream);
+int frame_kernel_grid(int device, int* grid_out);
+size_t frame_kernel_smem();
+int build_rope_tables(float2* slow, int slots, int hd, float2* fast, int wf, int hdf, double base, int bf16,
+                      void* stream);
+int compact_codes(const int32_t* stage, int32_t* codes, const StreamState* st, int n_frames, int ncb,
+                  int32_t* n_out, void* stream);
+
+struct PrefillArgs {
+  Dims d;
+  const void* E;
+  const void* CE;
+  const void* norm;
+  const LayerW* layers;   // host array [L]
+  const int32_t* tokens;  // device [T][NCB+1]
+  int T;
+  int chunk;
+  void* kc0;              // K cache of layer 0 for this stream; layer stride = kv_layer_stride bytes
+  void* vc0;
+  size_t kv_layer_stride;
+  int kv_slots;
+  const float2* rope;
+  float* scratch;         // chunk * per-position floats
+  float* hidden;          // [D]
+  float* logits;          // [A]
+  StreamState* st;
+  int* err;               // device word receiving S2_EINVAL on an out-of-range id
+};
+int run_prefill(const PrefillArgs& a, void* stream);
+size_t prefill_scratch_floats(const Dims& d, int chunk);
+
+}  // namespace s2

@@ -1,0 +1,158 @@
+/*
+ * s2frame.h — C ABI of the GB300 (sm_103a) Dual-AR frame decoder for S2-Pro.
+ *
+ * One frame of the method, per stream (s2.cpp analysis ch.02 "Overall architecture and
+ * Dual-AR data flow" §3.2-§3.5 and ch.06 "Fast-AR codebook decoding and the generation
+ * main loop" §5.1):
+ *   1. draw the main token from the Slow-AR logits + sem_mask (top-k 30 / top-p, draw =
+ *      argmax(probs / E), E an exponential variate), redraw at (1.0, 0.9) when it repeats a
+ *      token of the last 10 (RAS, ch.06 §6); stop on im_end;
+ *   2. sem_code = clamp(token - sem_begin, 0, codebook_size - 1);
+ *   3. nine Fast-AR calls (4-layer transformer over [fast_project_in·hidden ; fast_embeddings
+ *      of the codes so far], positions from 0, causal, untied fast_output) each followed by a
+ *      draw, giving codes 1..9 (ch.06 §1-§4);
+ *   4. one Slow-AR step on [token, code_0..code_9] (36-layer GQA transformer with fp16 KV
+ *      cache, q/k RMSNorm, RoPE base 1e6, SwiGLU, tied logits), producing the next logits and
+ *      the normalised hidden state (ch.02 §3.2, §3.4).
+ *
+ * Conventions
+ *  - Every call is asynchronous on the caller's CUDA stream; results are valid once that
+ *    stream has been synchronised.  Calls on one context must be ordered (one stream, or
+ *    synchronised between streams): they share the context's scratch memory.
+ *  - "device" pointers are CUDA device memory (e.g. torch tensors); "host" pointers are
+ *    ordinary host memory read before the call returns.
+ *  - The library allocates no device memory: all of it (KV cache, per-stream state,
+ *    scratch) lives in the caller's workspace.  It keeps only a small host-side object.
+ *  - Return values are S2_* status codes; no C++ exception crosses this boundary.  A
+ *    message for the last failure is available from s2_last_error().
+ *  - Problems detected on the device (a grid barrier or pipeline wait that gave up) are
+ *    recorded in device memory and reported by s2_sync_status(); they never trap.
+ */
+#ifndef S2FRAME_H
+#define S2FRAME_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* a cudaStream_t; NULL means the legacy default stream */
+typedef struct s2_ctx s2_ctx;
+
+enum { S2_F32 = 0, S2_BF16 = 1, S2_F16 = 2 };
+
+enum {
+  S2_OK = 0,
+  S2_EINVAL = 1,     /* bad argument or shape */
+  S2_ENOMEM = 2,     /* workspace too small */
+  S2_ECAPACITY = 3,  /* a stream would exceed its KV slots */
+  S2_ECUDA = 4,      /* a CUDA runtime call failed */
+  S2_ETIMEOUT = 5,   /* a device-side wait gave up (see s2_sync_status) */
+  S2_ESTATE = 6      /* call not valid in the stream's state (e.g. not prefilled) */
+};
+
+/* Model shape (ch.02 §2 dims table; ch.04 "Model loading and GGUF" §2.2 hyper-parameters). */
+typedef struct s2_dims {
+  int dim, n_layer, n_head, n_kv_head, head_dim, ffn, vocab;
+  int sem_begin, sem_end, im_end, n_codebooks, codebook_size;
+  float sem_scale, norm_eps, rope_base;
+  int qk_norm;          /* per-head RMSNorm of q and k before RoPE (must be 1 or 0) */
+  int rope_table_bf16;  /* round the RoPE cos/sin table to bf16 */
+  int fast_dim, fast_n_layer, fast_n_head, fast_n_kv_head, fast_head_dim, fast_ffn, fast_window,
+      has_fast_project_in;
+  int weight_dtype;     /* S2_F32 or S2_BF16: every weight tensor has this type */
+  int kv_dtype;         /* S2_F32 or S2_F16: Slow-AR KV cache element type */
+} s2_dims;
+
+/* Sampler settings of one stream ([ch.06 §5.3, §6]; Mizuoto "Fish Speech" engine page:
+ * top-k is fixed at 30). */
+typedef struct s2_sampling {
+  float temperature, top_p;          /* main and Fast-AR draws; temperature > 0, 0 < top_p <= 1 */
+  float ras_temperature, ras_top_p;  /* repetition-aware redraw (1.0, 0.9 upstream) */
+  int top_k;                         /* must be 30 */
+  int ras_window;                    /* 1..10 recent tokens compared */
+  int min_tokens_before_end;         /* im_end is masked while frames_done < this */
+  int max_frames;                    /* informational; n_frames of each call bounds the loop */
+} s2_sampling;
+
+/* Optional per-frame debug outputs of s2_decode_frames (any member may be NULL). */
+typedef struct s2_debug_taps {
+  float* main_logits;   /* device [n][n_frames][codebook_size+1]: Slow-AR logits on the admissible
+                           ids (sem_begin..sem_end, then im_end) used for the frame's main draw */
+  float* fast_logits;   /* device [n][n_frames][n_codebooks-1][codebook_size] */
+  float* hidden;        /* device [n][n_frames][dim]: normalised Slow-AR hidden given to Fast-AR */
+  int32_t* draws;       /* device [n][n_frames][11]: the library's own outcome of each draw (main,
+                           redraw, codebooks 1..9) before any forcing; -1 where not drawn */
+} s2_debug_taps;
+
+/* Weight table.  Order: embeddings [vocab][dim], codebook_embeddings [n_codebooks*codebook_size]
+ * [dim], norm [dim]; per Slow-AR layer 9 tensors: attention_norm [dim], attention.wqkv
+ * [(n_head+2*n_kv_head)*head_dim][dim] (rows q | k | v, head-major), attention.q_norm [head_dim],
+ * attention.k_norm [head_dim], attention.wo [dim][n_head*head_dim], ffn_norm [dim],
+ * feed_forward.w1 [ffn][dim], feed_forward.w3 [ffn][dim], feed_forward.w2 [dim][ffn]; then
+ * fast_project_in [fast_dim][dim], fast_embeddings [codebook_size][fast_dim], fast_norm
+ * [fast_dim], fast_output [codebook_size][fast_dim]; then 9 per Fast-AR layer as above with the
+ * fast_* sizes.  Names follow the GGUF names of ch.04 §3.  All row-major. */
+int s2_weight_count(const s2_dims* d);
+/* Writes the i-th name (NUL-terminated, truncated to len) and returns its element count, or -1. */
+long long s2_weight_info(const s2_dims* d, int i, char* name, int len);
+
+/* Device bytes s2_frame_init needs for `max_streams` streams of `kv_slots` KV positions each. */
+size_t s2_frame_workspace_bytes(const s2_dims* d, int max_streams, int kv_slots);
+
+/* Validate the shape, bind the weight table (device pointers, caller-owned, must outlive the
+ * context; entries of an absent part may be NULL: the Slow-AR tensors when n_layer == 0,
+ * fast_project_in when has_fast_project_in == 0) and lay out the workspace (device, caller-owned,
+ * >= s2_frame_workspace_bytes, 256-byte aligned).  Synchronous (builds tables on the device of
+ * the current CUDA context).  Fast-AR entry checks of ch.06 §1 are enforced here: a fast decoder
+ * must exist, and fast_window must cover n_codebooks positions. */
+int s2_frame_init(const s2_dims* d, const void* const* weights, int n_weights, void* workspace,
+                  size_t ws_bytes, int max_streams, int kv_slots, s2_ctx** out);
+
+/* Prefill n streams (ids host [n]) with their prompts: tokens device int32, the streams'
+ * [len][n_codebooks+1] matrices (column-major token layout of ch.02 §3.1: row 0 text/semantic
+ * id, rows 1.. codes) concatenated in order; lengths host [n].  Resets each stream, writes KV
+ * slots 0..len-1 and keeps the logits and normalised hidden of the last position. */
+int s2_prefill(s2_ctx* ctx, int n, const int* stream_ids, const int32_t* tokens, const int* lengths,
+               struct CUstream_st* stream);
+
+/* Decode up to n_frames frames for each of n prefilled streams (ids host [n]).
+ *   params  host [n] sampler settings
+ *   expo    device [n][n_frames][11][30] exponential variates E = -ln u (draw order: main,
+ *           redraw, codebooks 1..9; index = rank within the top 30)
+ *   forced  device [n][n_frames][11] or NULL: replaces the outcome of each draw (teacher forcing)
+ *   codes   device [n][n_codebooks*n_frames]: stream i's block holds codes[cb*n_out_i + f]
+ *           (ch.06 §8 layout, compacted to the frames actually produced)
+ *   n_out   device [n]: frames produced (< n_frames when im_end was drawn)
+ *   taps    host struct or NULL: debug outputs (see s2_debug_taps)
+ * Streams resume where the previous call left them (KV, position, RAS window, logits). */
+int s2_decode_frames(s2_ctx* ctx, int n, const int* stream_ids, int n_frames, const s2_sampling* params,
+                     const float* expo, const int32_t* forced, int32_t* codes, int32_t* n_out,
+                     const s2_debug_taps* taps, struct CUstream_st* stream);
+
+/* Fast-AR alone, teacher-forced (ch.06 §1-§4): for each of n_frames frames, hidden device
+ * [n_frames][dim] and prefix device [n_frames][n_codebooks-1] (code_0..code_{NCB-2}); writes
+ * logits device [n_frames][n_codebooks-1][codebook_size], window w = 2..n_codebooks. */
+int s2_fast_logits(s2_ctx* ctx, int n_frames, const float* hidden, const int32_t* prefix, float* logits,
+                   struct CUstream_st* stream);
+
+/* Synchronise `stream` and report device-side failures of earlier calls (S2_ETIMEOUT) or
+ * S2_OK; clears the recorded failure. */
+int s2_sync_status(s2_ctx* ctx, struct CUstream_st* stream);
+
+/* Testing hook: bound on device-side spin waits, in units of ~1 µs (0 restores the default of
+ * about two seconds).  Lets a test make a wait give up without any fault. */
+int s2_set_spin_limit(s2_ctx* ctx, long long limit);
+
+int s2_frame_free(s2_ctx* ctx);
+
+/* Message of the last failure on this context (or of the last failed s2_frame_init when ctx is
+ * NULL); never NULL. */
+const char* s2_last_error(const s2_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* S2FRAME_H */

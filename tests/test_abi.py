@@ -1,0 +1,85 @@
+"""The C-ABI library builds, loads without a GPU, exports every entry point the header declares,
+and its host-side logic (weight table, workspace sizing, argument checks) agrees with the
+generator's weight table."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "s2frame.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dual_ar_tts_gb300 import build
+    build.build()
+    import dual_ar_tts_gb300 as pkg
+    return pkg.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(s2_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declarations_are_exported(lib):
+    names = _declared()
+    assert "s2_decode_frames" in names and "s2_frame_init" in names
+    so = os.path.join(ROOT, "dual_ar_tts_gb300", "libs2frame.so")
+    syms = subprocess.run(["nm", "-D", "--defined-only", so], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (s2_\w+)", syms))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert hasattr(lib, n)
+    import dual_ar_tts_gb300 as pkg
+    assert set(pkg.EXPORTS) == set(names)
+
+
+@pytest.mark.parametrize("cfg", ["tiny", "frame", "fast"])
+def test_weight_table_matches_generator(lib, cfg):
+    import dual_ar_tts_gb300 as pkg
+    d = synth.CONFIGS[cfg]["dims"]
+    dims = pkg.make_dims(d)
+    specs = synth.weight_specs(d)
+    assert pkg.s2_weight_count(dims) == len(specs)
+    for i, (name, shape, _) in enumerate(specs):
+        nm, n = pkg.s2_weight_info(dims, i)
+        assert nm == name
+        assert n == int(__import__("numpy").prod(shape))
+    assert pkg.s2_weight_info(dims, len(specs))[1] == -1
+
+
+def test_workspace_sizing_and_bad_dims(lib):
+    import dual_ar_tts_gb300 as pkg
+    d = synth.CONFIGS["frame"]["dims"]
+    one = pkg.s2_frame_workspace_bytes(pkg.make_dims(d), 1, 32768)
+    kv = 2 * 36 * 8 * 32768 * 128 * 2
+    assert kv < one < kv + 2 ** 30
+    assert pkg.s2_frame_workspace_bytes(pkg.make_dims(d), 2, 32768) > one + kv // 2
+    bad = dict(d, head_dim=96)
+    assert pkg.s2_frame_workspace_bytes(pkg.make_dims(bad), 1, 16) == 0
+    bad = dict(d, fast_n_layer=0)                  # no fast decoder (ch.06 §1 entry check)
+    assert pkg.s2_weight_count(pkg.make_dims(bad)) == -1
+    bad = dict(d, fast_window=9)                   # window must hold the 10 codebook positions
+    assert pkg.s2_weight_count(pkg.make_dims(bad)) == -1
+
+
+def test_init_rejects_bad_arguments_without_touching_a_gpu(lib):
+    import dual_ar_tts_gb300 as pkg
+    d = synth.CONFIGS["tiny"]["dims"]
+    dims = pkg.make_dims(d)
+    n = pkg.s2_weight_count(dims)
+    out = ctypes.c_void_p()
+    arr = (ctypes.c_void_p * (n - 1))()
+    rc = lib.s2_frame_init(ctypes.byref(dims), arr, n - 1, ctypes.c_void_p(256), 1 << 20, 1, 64, ctypes.byref(out))
+    assert rc == pkg.S2_EINVAL and "weight table" in pkg.s2_last_error(None)
+    arr = (ctypes.c_void_p * n)(*([256] * n))
+    rc = lib.s2_frame_init(ctypes.byref(dims), arr, n, ctypes.c_void_p(8), 1 << 20, 1, 64, ctypes.byref(out))
+    assert rc == pkg.S2_EINVAL and "aligned" in pkg.s2_last_error(None)
