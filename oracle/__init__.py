@@ -267,6 +267,9 @@ def compact(frames_codes, d):
     return out
 
 
+N_DRAW_SLOTS = 11   # per-frame draw slots: main, redraw, codebooks 1..9 (unused slots -1)
+
+
 def run_frames(sess: Session, logits, hidden, n_frames, s, expo, forced=None, window=None, frame0=0,
                trace=True):
     """Frame loop of ch.06 §5.1 from a state (logits, hidden) left by prefill or a step.
@@ -298,7 +301,7 @@ def run_frames(sess: Session, logits, hidden, n_frames, s, expo, forced=None, wi
             d0 = int(forced[fi][0])
         if d0 == d["im_end"]:
             out["stopped"] = True
-            out["draws"].append(draws + [-1] * (10))
+            out["draws"].append(draws + [-1] * (N_DRAW_SLOTS - len(draws)))
             out["diags"].append(diags)
             break
         d1, g1 = draw(lp, s["ras_temperature"], s["ras_top_p"], s["top_k"], e[1])
@@ -321,7 +324,7 @@ def run_frames(sess: Session, logits, hidden, n_frames, s, expo, forced=None, wi
                 fl_all.append(fl)
         out["codes"].append(codes)
         out["tokens"].append(token)
-        out["draws"].append(draws)
+        out["draws"].append(draws + [-1] * (N_DRAW_SLOTS - len(draws)))
         out["diags"].append(diags)
         if trace:
             out["fast_logits"].append(np.stack(fl_all))

@@ -57,7 +57,7 @@ def test_tiny_early_stop_and_resume():
     ref, out, dec = _run(d, w, n, s, synth.prompt("tiny"), expo)
     assert ref["stopped"]
     compare_frames(ref, out, d, s, TOL)
-    assert int(out["n_out"][0]) == len(ref["codes"]) == 3
+    assert int(out["n_out"][0]) == len(ref["codes"]) < n
     out2 = dec.decode(2, s, torch.from_numpy(synth.expo(6, 0, 2)).cuda()[None], taps=False)
     assert dec.sync_status() == 0
     assert int(out2["n_out"][0]) == 0
