@@ -23,6 +23,7 @@ import math
 import os
 import subprocess
 import threading
+import zlib
 
 import numpy as np
 
@@ -200,7 +201,8 @@ def make_weights(d: dict, seed: int = 0, std: float = 0.02, norm_jitter: float =
     if skip_slow is None:
         skip_slow = d["n_layer"] == 0
     out = []
-    for idx, (name, shape, is_norm) in enumerate(weight_specs(d)):
+    for name, shape, is_norm in weight_specs(d):
+        idx = tensor_stream(name)
         if skip_slow and name in ("embeddings", "codebook_embeddings", "norm"):
             out.append(None)
             continue
@@ -215,6 +217,13 @@ def make_weights(d: dict, seed: int = 0, std: float = 0.02, norm_jitter: float =
             arr = normal_f32(seed, idx, n, mean, s) if s > 0 else np.full(n, mean, np.float32)
         out.append(arr.reshape(shape))
     return out
+
+
+def tensor_stream(name: str) -> int:
+    """Generator stream of a weight tensor, keyed by its name (so a tensor has the same values in
+    every workload that contains it, e.g. the Fast-AR weights of the full model and of the
+    Fast-AR-alone workload)."""
+    return zlib.crc32(name.encode())
 
 
 def _const_bf16(n, v):

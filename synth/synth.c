@@ -13,7 +13,8 @@
  * a single value.
  *
  *   uniform01(b)   = ((b >> 11) + 0.5) · 2^-53        in (0, 1), never 0 or 1
- *   normal(i)      = sqrt(-2 ln u(2i)) · cos(2π u(2i+1))   (Box–Muller, double)
+ *   normal(2j), normal(2j+1) = r·cos(t), r·sin(t) with r = sqrt(-2 ln u(2j)),
+ *                  t = 2π u(2j+1)                       (Box–Muller, double)
  *   exponential(i) = -ln u(i)                          (inverse CDF, double)
  *   integer(i)     = lo + (b mod (hi - lo + 1))
  *
@@ -53,24 +54,40 @@ static inline uint16_t f32_to_bf16_rne(float f) {
   return (uint16_t)(u >> 16);
 }
 
-static inline double normal_at(uint64_t key, uint64_t i) {
-  double a = u01(draw_bits(key, 2 * i));
-  double b = u01(draw_bits(key, 2 * i + 1));
-  return sqrt(-2.0 * log(a)) * cos(6.283185307179586476925286766559 * b);
+/* Box–Muller pair j: (r cos t, r sin t) with r = sqrt(-2 ln u(2j)), t = 2π u(2j+1);
+ * element 2j takes the cosine branch and element 2j+1 the sine branch. */
+static inline void normal_pair(uint64_t key, uint64_t j, double* z0, double* z1) {
+  double a = u01(draw_bits(key, 2 * j));
+  double b = u01(draw_bits(key, 2 * j + 1));
+  double r = sqrt(-2.0 * log(a)), t = 6.283185307179586476925286766559 * b;
+  *z0 = r * cos(t);
+  *z1 = r * sin(t);
 }
 
 /* n values of mean + std·N(0,1) as fp32. */
 void synth_normal_f32(uint64_t seed, uint64_t stream, int64_t n, double mean, double std, float* out) {
   uint64_t key = stream_key(seed, stream);
+  int64_t pairs = (n + 1) / 2;
 #pragma omp parallel for schedule(static)
-  for (int64_t i = 0; i < n; ++i) out[i] = (float)(mean + std * normal_at(key, (uint64_t)i));
+  for (int64_t j = 0; j < pairs; ++j) {
+    double z0, z1;
+    normal_pair(key, (uint64_t)j, &z0, &z1);
+    out[2 * j] = (float)(mean + std * z0);
+    if (2 * j + 1 < n) out[2 * j + 1] = (float)(mean + std * z1);
+  }
 }
 
 /* n values of mean + std·N(0,1), rounded fp64 -> fp32 -> bf16 (raw 16-bit patterns). */
 void synth_normal_bf16(uint64_t seed, uint64_t stream, int64_t n, double mean, double std, uint16_t* out) {
   uint64_t key = stream_key(seed, stream);
+  int64_t pairs = (n + 1) / 2;
 #pragma omp parallel for schedule(static)
-  for (int64_t i = 0; i < n; ++i) out[i] = f32_to_bf16_rne((float)(mean + std * normal_at(key, (uint64_t)i)));
+  for (int64_t j = 0; j < pairs; ++j) {
+    double z0, z1;
+    normal_pair(key, (uint64_t)j, &z0, &z1);
+    out[2 * j] = f32_to_bf16_rne((float)(mean + std * z0));
+    if (2 * j + 1 < n) out[2 * j + 1] = f32_to_bf16_rne((float)(mean + std * z1));
+  }
 }
 
 /* n standard exponential variates -ln(u), u uniform in (0,1), as fp32. */
