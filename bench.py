@@ -285,7 +285,7 @@ def main():
                 "frac_of_measured": achieved / pk, "parts_gb": {k: v / 1e9 for k, v in parts.items()}},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk, "unit": "GB/s", "frac": achieved / pk,
                      "traffic": None, "kernel": "frame_kernel", "peak_kind": pk_kind},
-        "e2e": {"value": world * K / e2e_max, "unit": "frames/s", "h2d_bytes_per_step": int(expo_h[0, 0].numel() * 4),
+        "e2e": {"value": world * K / e2e_max, "unit": "frames/s", "h2d_bytes_per_step": int(expo_h[0].numel() * 4),
                 "d2h_bytes_per_step": int(d["n_codebooks"] * 4)},
         "gpu_launches": 2,
         "clocks": clk.summary(),

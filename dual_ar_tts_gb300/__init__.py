@@ -19,8 +19,8 @@ STATUS_NAMES = {0: "S2_OK", 1: "S2_EINVAL", 2: "S2_ENOMEM", 3: "S2_ECAPACITY", 4
                 6: "S2_ESTATE"}
 
 EXPORTS = ("s2_weight_count", "s2_weight_info", "s2_frame_workspace_bytes", "s2_frame_init", "s2_prefill",
-           "s2_decode_frames", "s2_fast_logits", "s2_sync_status", "s2_set_spin_limit", "s2_frame_free",
-           "s2_last_error")
+           "s2_decode_frames", "s2_fast_logits", "s2_sync_status", "s2_set_spin_limit", "s2_set_trace",
+           "s2_phase_count", "s2_frame_free", "s2_last_error")
 
 
 class s2_dims(ctypes.Structure):
@@ -72,6 +72,8 @@ def load(path: str = LIB_PATH):
         "s2_fast_logits": (i32, [vp, i32, vp, vp, vp, vp]),
         "s2_sync_status": (i32, [vp, vp]),
         "s2_set_spin_limit": (i32, [vp, i64]),
+        "s2_set_trace": (i32, [vp, vp, i32]),
+        "s2_phase_count": (i32, [vp, i32]),
         "s2_frame_free": (i32, [vp]),
         "s2_last_error": (ctypes.c_char_p, [vp]),
     }
@@ -152,6 +154,14 @@ def s2_sync_status(ctx, stream: int = 0) -> int:
 
 def s2_set_spin_limit(ctx, limit: int):
     return _check("s2_set_spin_limit", load().s2_set_spin_limit(ctx, limit), ctx)
+
+
+def s2_set_trace(ctx, buf_ptr: int | None, capacity: int):
+    return _check("s2_set_trace", load().s2_set_trace(ctx, buf_ptr, capacity), ctx)
+
+
+def s2_phase_count(ctx, fast_only: bool = False) -> int:
+    return load().s2_phase_count(ctx, int(bool(fast_only)))
 
 
 def s2_frame_free(ctx):

@@ -37,6 +37,8 @@ struct s2_ctx {
   float* hidden_src = nullptr;     // builder: hidden buffer feeding Fast-AR position 0
   Phase* prog = nullptr;           // [max_streams][n_dec] then fast-only program
   int n_dec = 0, n_fast = 0, prefill_chunk = 0;
+  unsigned long long* trace = nullptr;  // caller-owned device buffer (tracing hook)
+  int trace_cap = 0;
   std::vector<int> host_pos;
   std::vector<char> host_prefilled;
   std::string err;
@@ -440,6 +442,8 @@ CallParams base_params(s2_ctx* c) {
   cp.CE = c->CE;
   cp.FE = c->FE;
   cp.kv_slots = c->kv_slots;
+  cp.trace = c->trace;
+  cp.trace_cap = c->trace_cap;
   return cp;
 }
 
@@ -681,6 +685,19 @@ int s2_set_spin_limit(s2_ctx* c, long long limit) {
   if (cudaMemcpy(&c->ctl->spin_limit, &v, sizeof(v), cudaMemcpyHostToDevice) != cudaSuccess)
     return fail(c, S2_ECUDA, "setting the spin limit failed");
   return S2_OK;
+}
+
+int s2_set_trace(s2_ctx* c, unsigned long long* buf, int capacity) {
+  if (!c) return fail(nullptr, S2_EINVAL, "ctx is NULL");
+  if ((buf == nullptr) != (capacity == 0) || capacity < 0) return fail(c, S2_EINVAL, "bad trace buffer");
+  c->trace = buf;
+  c->trace_cap = capacity;
+  return S2_OK;
+}
+
+int s2_phase_count(const s2_ctx* c, int fast_only) {
+  if (!c) return -1;
+  return fast_only ? c->n_fast : c->n_dec;
 }
 
 int s2_frame_free(s2_ctx* c) {

@@ -182,6 +182,10 @@ __device__ void producer(const CallParams& cp, Smem& S) {
         filled[pp.stage] = true;
         pp.advance();
       }
+      if (cp.trace != nullptr && blockIdx.x == 0) {
+        const int k = f * cp.n_phases + p;
+        if (k < cp.trace_cap) cp.trace[cp.trace_cap + k] = globaltimer_ns();
+      }
     }
   }
   // Leave no copy in flight: wait for every stage whose last fill may not have landed.
@@ -1040,6 +1044,10 @@ __device__ void consumers(const CallParams& cp, Smem& S) {
         cp.st->pos = cp.st->pos + 1;  // the Slow-AR step's last phase: its slot is now filled
       }
       if (!grid_sync(cp, S, target)) return;
+      if (cp.trace != nullptr && cta0 && threadIdx.x == 0) {
+        const int k = f * cp.n_phases + p;
+        if (k < cp.trace_cap) cp.trace[k] = globaltimer_ns();
+      }
       if ((ph.op == OP_SAMPLE_MAIN || ph.merge_main) && ldcgi(&cp.st->done) != 0) return;
     }
   }

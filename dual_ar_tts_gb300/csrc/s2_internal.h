@@ -144,6 +144,8 @@ struct CallParams {
   const float2* rope;     // Slow-AR table [slots][hd/2]
   const float2* rope_f;   // Fast-AR table [Wf][hdf/2]
   Control* ctl;
+  unsigned long long* trace;  // nullable: [frame][phase] consumer exit time, then producer issue-done time
+  int trace_cap;              // entries per half
   Dims d;
   // weights for sampling / inputs
   const void* E;

@@ -146,6 +146,15 @@ int s2_sync_status(s2_ctx* ctx, struct CUstream_st* stream);
  * about two seconds).  Lets a test make a wait give up without any fault. */
 int s2_set_spin_limit(s2_ctx* ctx, long long limit);
 
+/* Tracing hook: when buf (device, 2*capacity entries) is set, later decode / Fast-AR calls record,
+ * for frame f and program phase p (index k = f*phase_count + p < capacity), the globaltimer (ns)
+ * at which the first CTA's consumers leave phase p (buf[k]) and at which its weight producer has
+ * issued all of phase p's tiles (buf[capacity + k]).  buf = NULL, capacity = 0 turns it off. */
+int s2_set_trace(s2_ctx* ctx, unsigned long long* buf, int capacity);
+
+/* Number of phases of one frame's program (fast_only: the Fast-AR-alone program), or -1. */
+int s2_phase_count(const s2_ctx* ctx, int fast_only);
+
 int s2_frame_free(s2_ctx* ctx);
 
 /* Message of the last failure on this context (or of the last failed s2_frame_init when ctx is
