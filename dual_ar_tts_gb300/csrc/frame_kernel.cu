@@ -76,20 +76,30 @@ __device__ __forceinline__ bool should_bail(const CallParams& cp, Smem& S) {
 }
 
 // Bounded wait on an mbarrier phase; on give-up records the failure and returns false.
+// try_wait suspends in hardware until the phase completes or a short time limit passes; the
+// abort/failure flags (shared memory) are polled every 16 tries, the global error word and the
+// clock every 256 tries, so the common case reacts to the completion without any global load.
 __device__ bool wait_bar(const CallParams& cp, Smem& S, uint64_t* bar, uint32_t parity, int where,
                          bool producer) {
   if (mbar_test(bar, parity)) return true;
-  const long long t0 = clock_us();
-  const long long lim = cp.ctl->spin_limit;
-  while (!mbar_test(bar, parity)) {
-    if (producer ? (*reinterpret_cast<volatile int*>(&S.abort_flag) != 0) : should_bail(cp, S)) return false;
-    if (ld_volatile_int(&cp.ctl->error) != 0) return false;
-    if (clock_us() - t0 > lim) {
-      if (atomicCAS(&cp.ctl->error, 0, S2_ETIMEOUT) == 0) cp.ctl->error_where = where;
-      return false;
+  long long t0 = -1;
+  for (unsigned it = 1;; ++it) {
+    if (mbar_test(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (producer ? (*reinterpret_cast<volatile int*>(&S.abort_flag) != 0)
+                   : (*reinterpret_cast<volatile int*>(&S.fail) != 0))
+        return false;
+      if ((it & 255u) == 0) {
+        if (ld_volatile_int(&cp.ctl->error) != 0) return false;
+        const long long t = clock_us();
+        if (t0 < 0) t0 = t;
+        else if (t - t0 > cp.ctl->spin_limit) {
+          if (atomicCAS(&cp.ctl->error, 0, S2_ETIMEOUT) == 0) cp.ctl->error_where = where;
+          return false;
+        }
+      }
     }
   }
-  return true;
 }
 
 // Grid-wide barrier among the consumer threads of all CTAs.
@@ -105,11 +115,11 @@ __device__ bool grid_sync(const CallParams& cp, Smem& S, unsigned& target) {
       long long t0 = 0;
       unsigned spins = 0;
       while (ld_acquire(&cp.ctl->gbar) < target) {
-        if (ld_volatile_int(&cp.ctl->error) != 0) {
-          ok = 0;
-          break;
-        }
         if ((++spins & 63u) == 0) {
+          if (ld_volatile_int(&cp.ctl->error) != 0) {
+            ok = 0;
+            break;
+          }
           const long long t = clock_us();
           if (t0 == 0) t0 = t;
           else if (t - t0 > lim) {
@@ -784,92 +794,232 @@ __device__ __forceinline__ int entry_id(const Dims& d, bool main, int i) {
   return main ? (i < d.cbs ? d.sem_lo + i : d.im_end) : i;
 }
 
-__device__ __forceinline__ bool better(float za, int ia, float zb, int ib) {
-  return za > zb || (za == zb && ia < ib);
+// total order of candidates: larger value first, equal values -> lower id first
+__device__ __forceinline__ bool better_k(uint32_t ka, int ia, uint32_t kb, int ib) {
+  return ka > kb || (ka == kb && ia < ib);
 }
 
-// Returns the drawn token (same value in every consumer thread); -1 if nothing is drawable.
+// order-preserving map of a float to an unsigned key (finite values map above 0x007fffff)
+__device__ __forceinline__ uint32_t fkey(float z) {
+  const uint32_t u = __float_as_uint(z);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// warp-aggregated histogram update: lanes with the same bin add once (bin 256 = no update)
+__device__ __forceinline__ void hist_add(int* hist, int bin, int lane) {
+  const unsigned m = __match_any_sync(0xffffffffu, bin);
+  if (bin < 256 && lane == __ffs(m) - 1) atomicAdd(&hist[bin], __popc(m));
+}
+
+// Sampler scratch (sampling phases never overlap attention / GEMV phases on a CTA).
+struct SampScratch {
+  int hist[256];
+  int nvalid;
+  uint32_t prefix;
+  int rem, n_gt, n_eq, result;
+  int pad[2];
+  uint32_t ck[64];
+  int cid[64];
+  float cz[64];
+  int tie_id[64];
+};
+static_assert(sizeof(SampScratch) <= kMiscWarp * sizeof(float) + 8 * 4 * 130 * sizeof(float), "sampler scratch");
+
+// One draw: the top-30 candidates by (value desc, id asc) are found with a 4-pass 8-bit radix
+// select of the 30th largest key, gathered, sorted by one warp; then, in one thread and in rank
+// order exactly as the method states: softmax over the 30, keep rank r iff r == 0 or
+// Σ_{s<r} π_s < top_p, winner = argmax π_r / E_r (ties -> lower rank).
+// Returns the drawn id in every consumer thread; -1 if nothing is drawable.
 __device__ int draw(const CallParams& cp, Smem& S, const float* logits, int n, bool main, bool mask_end,
                     float temperature, float top_p, const float* E) {
   const Dims& d = cp.d;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  SampScratch& W = *reinterpret_cast<SampScratch*>(S.misc);
+  uint32_t key[kSampPer];
   float zv[kSampPer];
-  int iv[kSampPer];
+  int nv = 0;
 #pragma unroll
   for (int k = 0; k < kSampPer; ++k) {
     const int i = tid + k * kConsumers;
-    zv[k] = -INFINITY;
-    iv[k] = 0x7fffffff;
+    key[k] = 0u;
+    zv[k] = 0.f;
     if (i < n) {
       const int id = entry_id(d, main, i);
       const float l = ldcg(logits + i);
       if (!(mask_end && main && id == d.im_end) && isfinite(l)) {
         zv[k] = l / temperature;
-        iv[k] = id;
+        key[k] = fkey(zv[k]);
+        ++nv;
       }
     }
   }
-  float* cz = S.misc + kMiscSamp;                       // [32] candidate z
-  int* ci = reinterpret_cast<int*>(S.misc + kMiscSamp + 32);   // [32] candidate ids
-  float* wz = S.misc + kMiscSamp + 64;                  // [8] warp winners
-  int* wi = reinterpret_cast<int*>(S.misc + kMiscSamp + 72);
-  int* res = reinterpret_cast<int*>(S.misc + kMiscSamp + 80);
-  int kk = 0;
-  for (int r = 0; r < kTopK; ++r) {
-    float bz = -INFINITY;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int k = 0; k < kSampPer; ++k)
-      if (better(zv[k], iv[k], bz, bi)) {
-        bz = zv[k];
-        bi = iv[k];
-      }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float oz = __shfl_xor_sync(0xffffffffu, bz, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (better(oz, oi, bz, bi)) {
-        bz = oz;
-        bi = oi;
-      }
-    }
-    if (lane == 0) {
-      wz[warp] = bz;
-      wi[warp] = bi;
-    }
-    named_bar(1, kConsumers);
-    float gz = wz[0];
-    int gi = wi[0];
-    for (int w = 1; w < kConsumerWarps; ++w)
-      if (better(wz[w], wi[w], gz, gi)) {
-        gz = wz[w];
-        gi = wi[w];
-      }
-    if (gi == 0x7fffffff || gz == -INFINITY) {
-      named_bar(1, kConsumers);
-      break;
-    }
-    if (tid == 0) {
-      cz[r] = gz;
-      ci[r] = gi;
-    }
-#pragma unroll
-    for (int k = 0; k < kSampPer; ++k)
-      if (iv[k] == gi) {
-        zv[k] = -INFINITY;
-        iv[k] = 0x7fffffff;
-      }
-    kk = r + 1;
-    named_bar(1, kConsumers);
-  }
+  W.hist[tid] = 0;
   if (tid == 0) {
-    int tok = -1;
-    if (kk > 0) {
+    W.nvalid = 0;
+    W.prefix = 0;
+    W.n_gt = 0;
+    W.n_eq = 0;
+  }
+  named_bar(1, kConsumers);
+  if (nv) atomicAdd(&W.nvalid, nv);
+#pragma unroll
+  for (int k = 0; k < kSampPer; ++k) hist_add(W.hist, key[k] ? static_cast<int>(key[k] >> 24) : 256, lane);
+  named_bar(1, kConsumers);
+  const int kk = min(kTopK, W.nvalid);
+  if (kk == 0) {
+    named_bar(1, kConsumers);
+    return -1;
+  }
+  if (tid == 0) W.rem = kk;
+  named_bar(1, kConsumers);
+  // ---- radix select of the kk-th largest key, 8 bits per pass from the top
+  for (int pass = 0; pass < 4; ++pass) {
+    if (warp == 0) {
+      int c[8], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = W.hist[255 - 8 * lane - j];
+        sum += c[j];
+      }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const int excl = incl - sum;
+      const int rem = W.rem;
+      const unsigned b = __ballot_sync(0xffffffffu, excl < rem && incl >= rem);
+      if (lane == __ffs(b) - 1) {
+        int cum = excl;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (cum + c[j] >= rem) {
+            W.prefix = (W.prefix << 8) | static_cast<uint32_t>(255 - 8 * lane - j);
+            W.rem = rem - cum;
+            break;
+          }
+          cum += c[j];
+        }
+      }
+    }
+    named_bar(1, kConsumers);
+    if (pass == 3) break;
+    W.hist[tid] = 0;
+    named_bar(1, kConsumers);
+    const uint32_t pre = W.prefix;
+    const int hs = 24 - 8 * pass;  // the prefix covers bits [hs, 32)
+#pragma unroll
+    for (int k = 0; k < kSampPer; ++k)
+      hist_add(W.hist, (key[k] && (key[k] >> hs) == pre) ? static_cast<int>((key[k] >> (hs - 8)) & 255u) : 256,
+               lane);
+    named_bar(1, kConsumers);
+  }
+  const uint32_t T = W.prefix;
+  const int rem = W.rem;  // how many entries equal to T are among the top kk
+  // ---- gather: all keys above T, and the entries tied at T
+#pragma unroll
+  for (int k = 0; k < kSampPer; ++k) {
+    if (!key[k]) continue;
+    const int id = entry_id(d, main, tid + k * kConsumers);
+    if (key[k] > T) {
+      const int slot = atomicAdd(&W.n_gt, 1);
+      W.ck[slot] = key[k];
+      W.cid[slot] = id;
+      W.cz[slot] = zv[k];
+    } else if (key[k] == T) {
+      const int slot = atomicAdd(&W.n_eq, 1);
+      if (slot < 64) W.tie_id[slot] = id;
+      if (slot == 0) W.cz[63] = zv[k];  // every tied entry has this value
+    }
+  }
+  named_bar(1, kConsumers);
+  const int n_gt = W.n_gt;
+  const float tz = W.cz[63];
+  if (W.n_eq <= 64) {
+    // warp 0: the rem lowest ids among the ties (bitonic sort of up to 64 ids, two per lane)
+    if (warp == 0) {
+      int a = lane < W.n_eq ? W.tie_id[lane] : 0x7fffffff;
+      int b = lane + 32 < W.n_eq ? W.tie_id[lane + 32] : 0x7fffffff;
+      if (b < a) { const int t = a; a = b; b = t; }
+      // sort the 32 pairwise minima and the 32 maxima separately is not enough: full 64-sort
+      for (int size = 2; size <= 64; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          if (stride == 32) {
+            // partner of element lane is lane+32 in the same lane: a <-> b
+            const bool asc = true;
+            if (asc ? (b < a) : (a < b)) { const int t = a; a = b; b = t; }
+            continue;
+          }
+          const int pa = __shfl_xor_sync(0xffffffffu, a, stride);
+          const int pb = __shfl_xor_sync(0xffffffffu, b, stride);
+          const bool lower = (lane & stride) == 0;
+          const bool asc_a = (lane & size) == 0;               // element index = lane
+          const bool asc_b = ((lane + 32) & size) == 0;        // element index = lane + 32
+          a = (lower == asc_a) ? min(a, pa) : max(a, pa);
+          b = (lower == asc_b) ? min(b, pb) : max(b, pb);
+        }
+      }
+      if (lane < rem) {
+        W.ck[n_gt + lane] = T;
+        W.cid[n_gt + lane] = a;
+        W.cz[n_gt + lane] = tz;
+      }
+    }
+  } else {
+    // many equal values: take the rem lowest tied ids one by one
+    int last = -1;
+    for (int r = 0; r < rem; ++r) {
+      int best = 0x7fffffff;
+#pragma unroll
+      for (int k = 0; k < kSampPer; ++k) {
+        const int id = entry_id(d, main, tid + k * kConsumers);
+        if (key[k] == T && id > last && id < best) best = id;
+      }
+      for (int o = 16; o > 0; o >>= 1) best = min(best, __shfl_xor_sync(0xffffffffu, best, o));
+      if (lane == 0) W.hist[warp] = best;
+      named_bar(1, kConsumers);
+      int m = W.hist[0];
+      for (int w = 1; w < kConsumerWarps; ++w) m = min(m, W.hist[w]);
+      if (tid == 0) {
+        W.ck[n_gt + r] = T;
+        W.cid[n_gt + r] = m;
+        W.cz[n_gt + r] = tz;
+      }
+      last = m;
+      named_bar(1, kConsumers);
+    }
+  }
+  named_bar(1, kConsumers);
+  // ---- warp 0: sort the kk candidates by (value desc, id asc), then the draw in rank order
+  if (warp == 0) {
+    uint32_t kq = lane < kk ? W.ck[lane] : 0u;
+    int iq = lane < kk ? W.cid[lane] : (0x7fffffff - lane);
+    float zq = lane < kk ? W.cz[lane] : 0.f;
+    for (int size = 2; size <= 32; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const uint32_t pk = __shfl_xor_sync(0xffffffffu, kq, stride);
+        const int pi = __shfl_xor_sync(0xffffffffu, iq, stride);
+        const float pz = __shfl_xor_sync(0xffffffffu, zq, stride);
+        const bool lower = (lane & stride) == 0;
+        const bool asc = (lane & size) == 0;  // "ascending" = best first
+        const bool other_first = better_k(pk, pi, kq, iq);
+        if ((lower == asc) == other_first) {
+          kq = pk;
+          iq = pi;
+          zq = pz;
+        }
+      }
+    }
+    W.cz[lane] = zq;
+    W.cid[lane] = iq;
+    __syncwarp();
+    if (lane == 0) {
       float pi[kTopK];
-      const float zmax = cz[0];
+      const float zmax = W.cz[0];
       float sum = 0.f;
       for (int r = 0; r < kk; ++r) {
-        pi[r] = expf(cz[r] - zmax);
+        pi[r] = expf(W.cz[r] - zmax);
         sum += pi[r];
       }
       for (int r = 0; r < kk; ++r) pi[r] = pi[r] / sum;
@@ -889,12 +1039,11 @@ __device__ int draw(const CallParams& cp, Smem& S, const float* logits, int n, b
           bq = qv;
         }
       }
-      tok = ci[best];
+      W.result = W.cid[best];
     }
-    *res = tok;
   }
   named_bar(1, kConsumers);
-  const int out = *res;
+  const int out = W.result;
   named_bar(1, kConsumers);
   return out;
 }
