@@ -203,21 +203,31 @@ struct Builder {
     p.w[1] = w1;
     p.normw = normw;
     const int epc = 16 / d.esz;
-    const int nch = kXRegFloats / (epc * ncols);
     const int nchunk = K / epc;
-    int Q = 1;
-    while ((nchunk + Q - 1) / Q > 32 * nch) Q *= 2;
-    if (Q > kConsumerWarps) err = "projection too long for the register-resident activation slices";
+    // every consumer warp takes a 1/8 K-slice of every row (all warps on every tile)
+    const int Q = kConsumerWarps;
+    if ((nchunk + Q - 1) / Q > 32 * kGemvChunksPerLane) err = "projection too long for the register-resident activation slices";
     p.Q = Q;
     const int rowb = K * d.esz * p.nmat;
     p.rows_per_tile = std::max(1, kStageBytes / rowb);
+    if (d.wdt == S2_BF16) {
+      // 8-row tiles of Kt columns: Kt a multiple of 16 dividing K, 8 padded rows within a stage
+      const int kmax = (kStageBytes / kTileRows - kTileRowPad) / 2;
+      int nkt = (K + kmax - 1) / kmax;
+      while (nkt <= K / 16 && (K % nkt != 0 || (K / nkt) % 16 != 0)) ++nkt;
+      if (nkt > K / 16) err = "no K tiling of a projection fits the pipeline stage";
+      p.Kt = K / nkt;
+      if (2LL * 2 * ncols * K > kXsBytes) err = "projection input does not fit the shared activation buffer";
+      if (K * d.esz > kStageBytes) err = "norm vector exceeds one pipeline stage";
+    }
     return p;
   }
   void push(Phase p) {
     const int g2 = c->grid - p.cta0;
     if (p.op == OP_GEMV) {
       const int rows = (p.M + g2 - 1) / g2;
-      if (static_cast<long long>(rows) * p.nmat * p.ncols * p.Q > kRedFloats) err = "too many rows per CTA for the partial-sum buffer";
+      if (static_cast<long long>(rows) * p.nmat * p.ncols * kConsumerWarps > kRedFloats)
+        err = "too many rows per CTA for the partial-sum buffer";
       if (p.last_row && p.nmat != 1) err = "last-row override needs one matrix";
     }
     out->push_back(p);

@@ -24,7 +24,7 @@
 
 namespace s2 {
 
-constexpr int kMiscFloats = 5376;
+constexpr int kMiscFloats = 64;
 
 struct Smem {
   uint64_t full[kStages];
@@ -33,18 +33,21 @@ struct Smem {
   int fail;         // a consumer wait gave up: leave at the next phase boundary
   int sync_ok;
   int flag;
-  float red[kRedFloats];
-  float misc[kMiscFloats];
+  Phase ph[2];      // consumers: the current phase descriptor and the prefetched next one
+  Phase pph[2];     // producer: the same, walked ahead of the consumers
+  float red[kRedFloats];             // GEMV partial sums
+  float misc[kMiscFloats];           // GEMV sum-of-squares partials
+  alignas(16) unsigned char xs[kXsBytes];  // GEMV activations | attention scratch | sampler scratch
   alignas(128) unsigned char ring[kStages][kStageBytes];
 };
 
 // misc[] regions
-constexpr int kMiscQ = 0;                  // attention: q heads of this CTA [4][128]
-constexpr int kMiscKV = 512;               // new k, v [2][128]
-constexpr int kMiscWarp = 768;             // attention warp partials [8][4][130]
-constexpr int kMiscSS = 768 + 8 * 4 * 130; // GEMV sum-of-squares partials [16]
-constexpr int kMiscSamp = kMiscSS + 32;    // sampler: candidates, warp winners
-static_assert(kMiscSamp + 256 <= kMiscFloats, "misc layout");
+constexpr int kMiscSS = 0;                 // GEMV sum-of-squares partials [16]
+// xs regions while an attention phase runs (floats)
+constexpr int kXsQ = 0;                    // q heads of this CTA [4][128]
+constexpr int kXsKV = 512;                 // new k, v [2][128]
+constexpr int kXsWarp = 768;               // warp partials [8][4][130]
+static_assert((kXsWarp + 8 * 4 * 130) * 4 <= kXsBytes, "attention scratch");
 
 struct Pipe {
   int stage;
@@ -79,9 +82,8 @@ __device__ __forceinline__ bool should_bail(const CallParams& cp, Smem& S) {
 // try_wait suspends in hardware until the phase completes or a short time limit passes; the
 // abort/failure flags (shared memory) are polled every 16 tries, the global error word and the
 // clock every 256 tries, so the common case reacts to the completion without any global load.
-__device__ bool wait_bar(const CallParams& cp, Smem& S, uint64_t* bar, uint32_t parity, int where,
-                         bool producer) {
-  if (mbar_test(bar, parity)) return true;
+__device__ __noinline__ bool wait_bar_slow(const CallParams& cp, Smem& S, uint64_t* bar, uint32_t parity, int where,
+                                           bool producer) {
   long long t0 = -1;
   for (unsigned it = 1;; ++it) {
     if (mbar_test(bar, parity)) return true;
@@ -100,6 +102,12 @@ __device__ bool wait_bar(const CallParams& cp, Smem& S, uint64_t* bar, uint32_t 
       }
     }
   }
+}
+
+__device__ __forceinline__ bool wait_bar(const CallParams& cp, Smem& S, uint64_t* bar, uint32_t parity, int where,
+                                         bool producer) {
+  if (mbar_test(bar, parity)) return true;
+  return wait_bar_slow(cp, S, bar, parity, where, producer);
 }
 
 // Grid-wide barrier among the consumer threads of all CTAs.
@@ -152,52 +160,109 @@ __device__ __forceinline__ void unpack16(const uint4& u, float* f, float) {
 // =========================================================================
 
 __device__ void producer(const CallParams& cp, Smem& S) {
-  if ((threadIdx.x & 31) != 0) return;
+  // The whole warp walks the program: lanes fetch the next phase descriptor (one 16-byte load
+  // each) while lane 0 issues the current phase's tile copies.
+  const int lane = threadIdx.x & 31;
+  constexpr int NQ = static_cast<int>(sizeof(Phase) / 16);
   const uint64_t pol = policy_evict_first();
   Pipe pp{0, 0};
   uint32_t fill_parity[kStages];
   bool filled[kStages];
   for (int s = 0; s < kStages; ++s) filled[s] = false;
-  bool stop = ld_volatile_int(&cp.st->done) != 0 && !cp.fast_only;
+  int stop = (ld_volatile_int(&cp.st->done) != 0 && !cp.fast_only) ? 1 : 0;
+  if (lane < NQ) reinterpret_cast<uint4*>(&S.pph[0])[lane] = __ldg(reinterpret_cast<const uint4*>(cp.prog) + lane);
+  __syncwarp();
+  int k = 0;
   for (int f = 0; f < cp.n_frames && !stop; ++f) {
-    for (int p = 0; p < cp.n_phases && !stop; ++p) {
-      const Phase& ph = cp.prog[p];
-      if (ph.op != OP_GEMV) continue;
-      int r0, nr;
-      rows_of(ph, blockIdx.x, gridDim.x, r0, nr);
-      const int R = ph.rows_per_tile;
-      const uint32_t rowb = static_cast<uint32_t>(ph.K) * cp.d.esz;
-      for (int t = 0; t < nr; t += R) {
-        const int rr = min(R, nr - t);
-        if (!wait_bar(cp, S, &S.empty[pp.stage], (pp.round & 1u) ^ 1u, 2, true)) {
-          stop = true;
-          break;
-        }
-        const uint32_t bytes = rowb * rr * ph.nmat;
-        uint64_t* fb = &S.full[pp.stage];
-        mbar_arrive_expect_tx(fb, bytes);
-        unsigned char* dst = S.ring[pp.stage];
-        const int row = r0 + t;
-        for (int m = 0; m < ph.nmat; ++m) {
-          const unsigned char* src = static_cast<const unsigned char*>(ph.w[m]) + static_cast<size_t>(row) * rowb;
-          unsigned char* dm = dst + static_cast<size_t>(m) * rr * rowb;
-          if (ph.last_row != nullptr && row + rr == ph.M) {
-            if (rr > 1) bulk_g2s(dm, src, rowb * (rr - 1), fb, pol);
-            bulk_g2s(dm + static_cast<size_t>(rr - 1) * rowb, ph.last_row, rowb, fb, pol);
-          } else {
-            bulk_g2s(dm, src, rowb * rr, fb, pol);
+    for (int p = 0; p < cp.n_phases && !stop; ++p, ++k) {
+      const Phase& ph = S.pph[k & 1];
+      const int np = (p + 1 == cp.n_phases) ? 0 : p + 1;
+      const bool has_next = (p + 1 < cp.n_phases) || (f + 1 < cp.n_frames);
+      uint4 nx = make_uint4(0u, 0u, 0u, 0u);
+      if (lane < NQ && has_next) nx = __ldg(reinterpret_cast<const uint4*>(cp.prog + np) + lane);
+      if (lane == 0 && ph.op == OP_GEMV) {
+        int r0, nr;
+        rows_of(ph, blockIdx.x, gridDim.x, r0, nr);
+        const int R = ph.rows_per_tile;
+        const uint32_t rowb = static_cast<uint32_t>(ph.K) * cp.d.esz;
+        if (ph.normw != nullptr && !(ph.merge_main && blockIdx.x == 0)) {
+          // the RMSNorm weight vector travels through the ring ahead of the phase's row tiles
+          if (!wait_bar(cp, S, &S.empty[pp.stage], (pp.round & 1u) ^ 1u, 2, true)) stop = 1;
+          if (!stop) {
+            mbar_arrive_expect_tx(&S.full[pp.stage], rowb);
+            bulk_g2s(S.ring[pp.stage], ph.normw, rowb, &S.full[pp.stage], pol);
+            fill_parity[pp.stage] = pp.round & 1u;
+            filled[pp.stage] = true;
+            pp.advance();
           }
         }
-        fill_parity[pp.stage] = pp.round & 1u;
-        filled[pp.stage] = true;
-        pp.advance();
+        if (cp.d.esz == 2) {
+          // bf16: tiles of 8 rows x Kt columns; one copy per row segment, rows padded by 16 bytes
+          const int Kt = ph.Kt, nkt = ph.K / Kt;
+          const uint32_t segb = static_cast<uint32_t>(Kt) * 2u, pitch = segb + kTileRowPad;
+          for (int b = 0; b < nr && !stop; b += kTileRows) {
+            const int rows = min(kTileRows, nr - b);
+            for (int m = 0; m < ph.nmat && !stop; ++m) {
+              for (int kt = 0; kt < nkt; ++kt) {
+                if (!wait_bar(cp, S, &S.empty[pp.stage], (pp.round & 1u) ^ 1u, 2, true)) {
+                  stop = 1;
+                  break;
+                }
+                uint64_t* fb = &S.full[pp.stage];
+                mbar_arrive_expect_tx(fb, segb * rows);
+                unsigned char* dst = S.ring[pp.stage];
+                for (int i = 0; i < rows; ++i) {
+                  const int row = r0 + b + i;
+                  const unsigned char* src =
+                      (ph.last_row != nullptr && row == ph.M - 1)
+                          ? static_cast<const unsigned char*>(ph.last_row) + static_cast<size_t>(kt) * segb
+                          : static_cast<const unsigned char*>(ph.w[m]) + static_cast<size_t>(row) * rowb +
+                                static_cast<size_t>(kt) * segb;
+                  bulk_g2s(dst + static_cast<size_t>(i) * pitch, src, segb, fb, pol);
+                }
+                fill_parity[pp.stage] = pp.round & 1u;
+                filled[pp.stage] = true;
+                pp.advance();
+              }
+            }
+          }
+        }
+        for (int t = 0; t < nr && !stop && cp.d.esz != 2; t += R) {
+          const int rr = min(R, nr - t);
+          if (!wait_bar(cp, S, &S.empty[pp.stage], (pp.round & 1u) ^ 1u, 2, true)) {
+            stop = 1;
+            break;
+          }
+          const uint32_t bytes = rowb * rr * ph.nmat;
+          uint64_t* fb = &S.full[pp.stage];
+          mbar_arrive_expect_tx(fb, bytes);
+          unsigned char* dst = S.ring[pp.stage];
+          const int row = r0 + t;
+          for (int m = 0; m < ph.nmat; ++m) {
+            const unsigned char* src = static_cast<const unsigned char*>(ph.w[m]) + static_cast<size_t>(row) * rowb;
+            unsigned char* dm = dst + static_cast<size_t>(m) * rr * rowb;
+            if (ph.last_row != nullptr && row + rr == ph.M) {
+              if (rr > 1) bulk_g2s(dm, src, rowb * (rr - 1), fb, pol);
+              bulk_g2s(dm + static_cast<size_t>(rr - 1) * rowb, ph.last_row, rowb, fb, pol);
+            } else {
+              bulk_g2s(dm, src, rowb * rr, fb, pol);
+            }
+          }
+          fill_parity[pp.stage] = pp.round & 1u;
+          filled[pp.stage] = true;
+          pp.advance();
+        }
+        if (cp.trace != nullptr && blockIdx.x == 0) {
+          const int kk = f * cp.n_phases + p;
+          if (kk < cp.trace_cap) cp.trace[cp.trace_cap + kk] = globaltimer_ns();
+        }
       }
-      if (cp.trace != nullptr && blockIdx.x == 0) {
-        const int k = f * cp.n_phases + p;
-        if (k < cp.trace_cap) cp.trace[cp.trace_cap + k] = globaltimer_ns();
-      }
+      stop = __shfl_sync(0xffffffffu, stop, 0);
+      if (lane < NQ && has_next) reinterpret_cast<uint4*>(&S.pph[(k + 1) & 1])[lane] = nx;
+      __syncwarp();
     }
   }
+  if (lane != 0) return;
   // Leave no copy in flight: wait for every stage whose last fill may not have landed.
   for (int s = 0; s < kStages; ++s) {
     if (!filled[s]) continue;
@@ -216,94 +281,134 @@ __device__ void producer(const CallParams& cp, Smem& S) {
 // =========================================================================
 
 template <typename WT, int NC>
-__device__ void gemv_t(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe) {
+__device__ __noinline__ void gemv_t(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe) {
   constexpr int EPC = 16 / static_cast<int>(sizeof(WT));
-  constexpr int NCH = kXRegFloats / (EPC * NC);
+  constexpr int NCH = kGemvChunksPerLane;  // every warp holds a 1/8 K-slice: <= 5 chunks per lane
   const Dims& d = cp.d;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int K = ph.K, Q = ph.Q;
   const int nchunk = K / EPC;
   const int slice = (nchunk + Q - 1) / Q;
-  const int q = warp % Q, group = warp / Q, ngroups = kConsumerWarps / Q;
+  const int q = warp % Q, group = warp / Q;
   const int c_beg = q * slice, c_end = min(nchunk, c_beg + slice);
   const bool writer = (blockIdx.x == 0) && (group == 0);
+  const bool has_norm = ph.normw != nullptr;
   int r0, nr;
   rows_of(ph, blockIdx.x, gridDim.x, r0, nr);
+  // the residual rows of an accumulate phase are final since an earlier phase: request them now
+  float yres = 0.f;
+  if (ph.epi == EPI_ADD && tid < nr * NC) yres = ldcg(ph.y[tid % NC] + r0 + tid / NC);
 
-  // ---- activation slices into registers
-  float xr[NC][NCH][EPC];
-  float ss[NC];
+  // ---- resolve each column's source: fp32 global vector, weight row (bf16/fp32), or the
+  // Slow-AR input embedding, which is summed here into shared memory first
+  const float* xf[NC];
+  const unsigned char* xw[NC];
+  bool staged = false;
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
-    ss[c] = 0.f;
     const GemvCol col = ph.col[c];
-    int tok = 0, codes[kMaxCodebooks];
-    float m = 0.f;
-    if (col.src == SRC_EMBED) {
-      const int* vals = static_cast<const int*>(col.p);
-      tok = ldcgi(vals);
-      m = (tok >= d.sem_lo && tok <= d.sem_hi) ? 1.f : 0.f;
-      for (int j = 0; j < d.ncb; ++j) codes[j] = ldcgi(vals + 1 + j);
+    xf[c] = nullptr;
+    xw[c] = nullptr;
+    if (col.src == SRC_BUF) {
+      xf[c] = static_cast<const float*>(col.p);
     } else if (col.src == SRC_FEROW) {
-      tok = ldcgi(static_cast<const int*>(col.p));
+      const int code = ldcgi(static_cast<const int*>(col.p));
+      xw[c] = static_cast<const unsigned char*>(cp.FE) + static_cast<size_t>(code) * K * sizeof(WT);
+    } else {
+      // x = sem_scale·E[r0] + m·Σ_cb CE[cb·CBS + code_cb], m = [r0 semantic]   (ch.02 §3.2)
+      const int* vals = static_cast<const int*>(col.p);
+      const int tok = ldcgi(vals);
+      const float m = (tok >= d.sem_lo && tok <= d.sem_hi) ? 1.f : 0.f;
+      float* xs = S.red + c * K;
+      for (int e = tid; e < K; e += kConsumers) {
+        float acc = 0.f;
+        for (int cb = 0; cb < d.ncb; ++cb) {
+          const size_t row = static_cast<size_t>(cb) * d.cbs + ldcgi(vals + 1 + cb);
+          acc = __fadd_rn(acc, wload(cp.CE, row * K + e, sizeof(WT)));
+        }
+        xs[e] = __fadd_rn(__fmul_rn(d.sem_scale, wload(cp.E, static_cast<size_t>(tok) * K + e, sizeof(WT))),
+                          __fmul_rn(m, acc));
+      }
+      xf[c] = xs;
+      staged = true;
     }
+  }
+  if (staged) named_bar(1, kConsumers);
+
+  // ---- activation slices into registers (all loads issued before any store)
+  float xr[NC][NCH][EPC];
 #pragma unroll
-    for (int i = 0; i < NCH; ++i) {
-      const int ch = c_beg + lane + 32 * i;
-      float* xv = xr[c][i];
+  for (int c = 0; c < NC; ++c) {
 #pragma unroll
-      for (int j = 0; j < EPC; ++j) xv[j] = 0.f;
-      if (ch < c_end) {
-        const size_t e0 = static_cast<size_t>(ch) * EPC;
-        if (col.src == SRC_BUF) {
-          const float* xp = static_cast<const float*>(col.p) + e0;
+    for (int i = 0; i < NCH; ++i)
+#pragma unroll
+      for (int j = 0; j < EPC; ++j) xr[c][i][j] = 0.f;
+    if (xw[c] != nullptr) {
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) {
+        const int ch = c_beg + lane + 32 * i;
+        if (ch < c_end) unpack16(ldnc_u4(xw[c] + static_cast<size_t>(ch) * 16), xr[c][i], WT());
+      }
+    } else if (staged) {
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) {
+        const int ch = c_beg + lane + 32 * i;
+        if (ch < c_end)
 #pragma unroll
           for (int j = 0; j < EPC; j += 4) {
-            float4 v = ldcg4(xp + j);
-            xv[j] = v.x; xv[j + 1] = v.y; xv[j + 2] = v.z; xv[j + 3] = v.w;
+            const float4 v = *reinterpret_cast<const float4*>(xf[c] + ch * EPC + j);
+            xr[c][i][j] = v.x; xr[c][i][j + 1] = v.y; xr[c][i][j + 2] = v.z; xr[c][i][j + 3] = v.w;
           }
-        } else if (col.src == SRC_FEROW) {
-          const uint4 u = ldnc_u4(static_cast<const unsigned char*>(cp.FE) +
-                                  (static_cast<size_t>(tok) * K + e0) * sizeof(WT));
-          unpack16(u, xv, WT());
-        } else if (col.src == SRC_EMBED) {
-          float acc[EPC], er[EPC];
+      }
+    } else {
 #pragma unroll
-          for (int j = 0; j < EPC; ++j) acc[j] = 0.f;
-          for (int cb = 0; cb < d.ncb; ++cb) {
-            const size_t row = static_cast<size_t>(cb) * d.cbs + codes[cb];
-            const uint4 u = ldnc_u4(static_cast<const unsigned char*>(cp.CE) + (row * K + e0) * sizeof(WT));
-            float cv[EPC];
-            unpack16(u, cv, WT());
+      for (int i = 0; i < NCH; ++i) {
+        const int ch = c_beg + lane + 32 * i;
+        if (ch < c_end)
 #pragma unroll
-            for (int j = 0; j < EPC; ++j) acc[j] = __fadd_rn(acc[j], cv[j]);
+          for (int j = 0; j < EPC; j += 4) {
+            const float4 v = ldcg4(xf[c] + ch * EPC + j);
+            xr[c][i][j] = v.x; xr[c][i][j + 1] = v.y; xr[c][i][j + 2] = v.z; xr[c][i][j + 3] = v.w;
           }
-          const uint4 u = ldnc_u4(static_cast<const unsigned char*>(cp.E) + (static_cast<size_t>(tok) * K + e0) * sizeof(WT));
-          unpack16(u, er, WT());
+      }
+    }
+  }
+  // raw (pre-norm) column written back for the residual stream (one CTA, one copy of each slice)
+  if (writer) {
 #pragma unroll
-          for (int j = 0; j < EPC; ++j) xv[j] = __fadd_rn(__fmul_rn(d.sem_scale, er[j]), __fmul_rn(m, acc[j]));
-        }
-        if (writer && col.wb != nullptr) {
+    for (int c = 0; c < NC; ++c) {
+      float* wb = ph.col[c].wb;
+      if (wb == nullptr) continue;
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) {
+        const int ch = c_beg + lane + 32 * i;
+        if (ch < c_end)
 #pragma unroll
           for (int j = 0; j < EPC; j += 4)
-            *reinterpret_cast<float4*>(col.wb + e0 + j) = make_float4(xv[j], xv[j + 1], xv[j + 2], xv[j + 3]);
-        }
-#pragma unroll
-        for (int j = 0; j < EPC; ++j) ss[c] += xv[j] * xv[j];
+            *reinterpret_cast<float4*>(wb + ch * EPC + j) = make_float4(xr[c][i][j], xr[c][i][j + 1], xr[c][i][j + 2], xr[c][i][j + 3]);
       }
     }
   }
 
-  // ---- RMSNorm: every slice is held once by the warps of group 0
-  if (ph.normw != nullptr) {
+  // ---- RMSNorm (fp32): each slice is held once by the warps of group 0
+  if (has_norm) {
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
-      const float t = warp_sum(ss[c]);
-      if (group == 0 && lane == 0) S.misc[kMiscSS + q * NC + c] = t;
+      float ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < NCH; ++i)
+#pragma unroll
+        for (int j = 0; j < EPC; ++j) ss += xr[c][i][j] * xr[c][i][j];
+      ss = warp_sum(ss);
+      if (group == 0 && lane == 0) S.misc[kMiscSS + q * NC + c] = ss;
     }
   }
   named_bar(1, kConsumers);
-  if (ph.normw != nullptr) {
+  if (has_norm) {
+    // the norm weights are the phase's first ring stage
+    const bool ok = wait_bar(cp, S, &S.full[pipe.stage], pipe.round & 1u, 5, false);
+    if (!ok) S.fail = 1;
+    const unsigned char* nws = S.ring[pipe.stage];
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
       float tot = 0.f;
@@ -313,24 +418,31 @@ __device__ void gemv_t(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pip
       for (int i = 0; i < NCH; ++i) {
         const int ch = c_beg + lane + 32 * i;
         if (ch < c_end) {
-          const size_t e0 = static_cast<size_t>(ch) * EPC;
           float wv[EPC];
-          const uint4 u = ldnc_u4(static_cast<const unsigned char*>(ph.normw) + e0 * sizeof(WT));
-          unpack16(u, wv, WT());
+          unpack16(*reinterpret_cast<const uint4*>(nws + static_cast<size_t>(ch) * 16), wv, WT());
 #pragma unroll
           for (int j = 0; j < EPC; ++j) xr[c][i][j] = (xr[c][i][j] * r) * wv[j];
-          if (c == 0 && writer && ph.hid_out != nullptr) {
-#pragma unroll
-            for (int j = 0; j < EPC; j += 4)
-              *reinterpret_cast<float4*>(ph.hid_out + e0 + j) =
-                  make_float4(xr[0][i][j], xr[0][i][j + 1], xr[0][i][j + 2], xr[0][i][j + 3]);
-          }
         }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[pipe.stage]);
+    pipe.advance();
+    if (writer && ph.hid_out != nullptr) {
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) {
+        const int ch = c_beg + lane + 32 * i;
+        if (ch < c_end)
+#pragma unroll
+          for (int j = 0; j < EPC; j += 4)
+            *reinterpret_cast<float4*>(ph.hid_out + ch * EPC + j) =
+                make_float4(xr[0][i][j], xr[0][i][j + 1], xr[0][i][j + 2], xr[0][i][j + 3]);
       }
     }
   }
 
-  // ---- stream the CTA's row tiles
+  // ---- stream the CTA's row tiles: all eight warps work on every tile, each on its K-slice of
+  // every row, four rows at a time (independent accumulation chains)
   const int R = ph.rows_per_tile;
   const int nmat = ph.nmat;
   const size_t rowb = static_cast<size_t>(K) * sizeof(WT);
@@ -339,9 +451,11 @@ __device__ void gemv_t(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pip
     const int rr = min(R, nr - t * R);
     const bool ok = wait_bar(cp, S, &S.full[pipe.stage], pipe.round & 1u, 4, false);
     if (!ok) S.fail = 1;
-    if (ok && (t % ngroups) == group) {
-      const unsigned char* base = S.ring[pipe.stage];
+    if (ok) {
+      const uint32_t base = smem_u32(S.ring[pipe.stage]) + static_cast<uint32_t>(c_beg + lane) * 16u;
+      const uint32_t red = smem_u32(S.red);
       const int nv = rr * nmat;  // virtual rows: rr rows of matrix 0, then rr of matrix 1
+#pragma unroll 1
       for (int v0 = 0; v0 < nv; v0 += 4) {
         float acc[4][NC];
 #pragma unroll
@@ -350,14 +464,12 @@ __device__ void gemv_t(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pip
           for (int c = 0; c < NC; ++c) acc[v][c] = 0.f;
 #pragma unroll
         for (int i = 0; i < NCH; ++i) {
-          const int ch = c_beg + lane + 32 * i;
-          if (ch < c_end) {
+          if (c_beg + lane + 32 * i < c_end) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               if (v0 + v < nv) {
-                const uint4 u = *reinterpret_cast<const uint4*>(base + (v0 + v) * rowb + static_cast<size_t>(ch) * 16);
                 float wf[EPC];
-                unpack16(u, wf, WT());
+                unpack16(lds128(base + static_cast<uint32_t>((v0 + v) * rowb) + i * 512u), wf, WT());
 #pragma unroll
                 for (int c = 0; c < NC; ++c)
 #pragma unroll
@@ -376,7 +488,7 @@ __device__ void gemv_t(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pip
             if (v0 + v < nv) {
               const int mat = (v0 + v) / rr, rl = t * R + (v0 + v) % rr;
 #pragma unroll
-              for (int c = 0; c < NC; ++c) S.red[((rl * nmat + mat) * NC + c) * Q + q] = acc[v][c];
+              for (int c = 0; c < NC; ++c) sts32f(red + 4u * (((rl * nmat + mat) * NC + c) * Q + q), acc[v][c]);
             }
           }
         }
@@ -391,7 +503,7 @@ __device__ void gemv_t(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pip
   // ---- epilogue: sum the slices in fixed order, apply the output rule
   if (!S.fail) {
     const int nout = nr * NC;
-    for (int idx = threadIdx.x; idx < nout; idx += kConsumers) {
+    for (int idx = tid; idx < nout; idx += kConsumers) {
       const int rl = idx / NC, c = idx % NC;
       float a = 0.f, b = 0.f;
       for (int qq = 0; qq < Q; ++qq) a += S.red[((rl * nmat + 0) * NC + c) * Q + qq];
@@ -401,7 +513,7 @@ __device__ void gemv_t(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pip
       if (ph.epi == EPI_STORE) {
         *y = a;
       } else if (ph.epi == EPI_ADD) {
-        *y = ldcg(y) + a;
+        *y = (idx == tid ? yres : ldcg(y)) + a;
       } else {
         *y = (a / (1.0f + expf(-a))) * b;
       }
@@ -409,10 +521,224 @@ __device__ void gemv_t(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pip
   }
 }
 
+// =========================================================================
+// GEMV phase, bf16 weights, on the tensor cores (mma.sync m16n8k16, fp32 accumulate), in
+// transposed form: D[16 x 8] += X^T[16 x 16] · W^T[16 x 8], where the 8 columns of W^T are 8
+// weight rows (an 8-row tile, ldmatrix from shared memory) and the rows of X^T are the
+// activation columns split into bf16 hi and lo parts (x = hi + lo to ~2^-17 relative), so each
+// output is Σ_k w·hi + Σ_k w·lo.  Each warp owns every 8th 16-wide k step of a tile; the eight
+// warps' partial sums are added in a fixed order.
+// =========================================================================
+
+template <int NC>
+__device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe) {
+  const Dims& d = cp.d;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int K = ph.K, Kt = ph.Kt, nkt = K / Kt;
+  const bool has_norm = ph.normw != nullptr;
+  int r0, nr;
+  rows_of(ph, blockIdx.x, gridDim.x, r0, nr);
+  float yres = 0.f;
+  if (ph.epi == EPI_ADD && tid < nr * NC) yres = ldcg(ph.y[tid % NC] + r0 + tid / NC);
+
+  // ---- activation columns into registers: thread tid holds elements 4·(tid + 256 j) .. +3
+  constexpr int GMAX = 10;  // float4 groups per thread per column (K <= 10240)
+  const int ng = K / 4;
+  float4 xv[NC][GMAX];
+  float ss[NC];
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    ss[c] = 0.f;
+    const GemvCol col = ph.col[c];
+    const int* vals = static_cast<const int*>(col.p);
+    int tok = 0, code = 0;
+    float msem = 0.f;
+    if (col.src == SRC_EMBED) {
+      tok = ldcgi(vals);
+      msem = (tok >= d.sem_lo && tok <= d.sem_hi) ? 1.f : 0.f;
+    } else if (col.src == SRC_FEROW) {
+      code = ldcgi(vals);
+    }
+#pragma unroll
+    for (int j = 0; j < GMAX; ++j) {
+      const int g = tid + kConsumers * j;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (g < ng) {
+        const int e = 4 * g;
+        if (col.src == SRC_BUF) {
+          v = ldcg4(static_cast<const float*>(col.p) + e);
+        } else if (col.src == SRC_FEROW) {
+          const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const unsigned char*>(cp.FE) +
+                                                               (static_cast<size_t>(code) * K + e) * 2));
+          v = make_float4(bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y));
+        } else {
+          // x = sem_scale·E[r0] + m·Σ_cb CE[cb·CBS + code_cb]   (ch.02 §3.2)
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int cb = 0; cb < d.ncb; ++cb) {
+            const size_t row = static_cast<size_t>(cb) * d.cbs + ldcgi(vals + 1 + cb);
+            const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const unsigned char*>(cp.CE) + (row * K + e) * 2));
+            acc[0] = __fadd_rn(acc[0], bf16lo(u.x));
+            acc[1] = __fadd_rn(acc[1], bf16hi(u.x));
+            acc[2] = __fadd_rn(acc[2], bf16lo(u.y));
+            acc[3] = __fadd_rn(acc[3], bf16hi(u.y));
+          }
+          const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const unsigned char*>(cp.E) +
+                                                               (static_cast<size_t>(tok) * K + e) * 2));
+          v.x = __fadd_rn(__fmul_rn(d.sem_scale, bf16lo(u.x)), __fmul_rn(msem, acc[0]));
+          v.y = __fadd_rn(__fmul_rn(d.sem_scale, bf16hi(u.x)), __fmul_rn(msem, acc[1]));
+          v.z = __fadd_rn(__fmul_rn(d.sem_scale, bf16lo(u.y)), __fmul_rn(msem, acc[2]));
+          v.w = __fadd_rn(__fmul_rn(d.sem_scale, bf16hi(u.y)), __fmul_rn(msem, acc[3]));
+        }
+      }
+      xv[c][j] = v;
+      ss[c] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+  }
+  if (blockIdx.x == 0) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      float* wb = ph.col[c].wb;
+      if (wb == nullptr) continue;
+#pragma unroll
+      for (int j = 0; j < GMAX; ++j) {
+        const int g = tid + kConsumers * j;
+        if (g < ng) *reinterpret_cast<float4*>(wb + 4 * g) = xv[c][j];
+      }
+    }
+  }
+  // ---- RMSNorm in fp32 (block reduction of the sum of squares)
+  if (has_norm) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const float t = warp_sum(ss[c]);
+      if (lane == 0) S.misc[kMiscSS + warp * NC + c] = t;
+    }
+  }
+  named_bar(1, kConsumers);
+  if (has_norm) {
+    const bool ok = wait_bar(cp, S, &S.full[pipe.stage], pipe.round & 1u, 5, false);
+    if (!ok) S.fail = 1;
+    const uint32_t nws = smem_u32(S.ring[pipe.stage]);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      float tot = 0.f;
+      for (int w = 0; w < kConsumerWarps; ++w) tot += S.misc[kMiscSS + w * NC + c];
+      const float r = 1.0f / sqrtf(tot / static_cast<float>(K) + d.eps);
+#pragma unroll
+      for (int j = 0; j < GMAX; ++j) {
+        const int g = tid + kConsumers * j;
+        if (g < ng) {
+          const uint32_t w01 = lds32(nws + 8u * g), w23 = lds32(nws + 8u * g + 4u);
+          float4& v = xv[c][j];
+          v.x = (v.x * r) * bf16lo(w01);
+          v.y = (v.y * r) * bf16hi(w01);
+          v.z = (v.z * r) * bf16lo(w23);
+          v.w = (v.w * r) * bf16hi(w23);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[pipe.stage]);
+    pipe.advance();
+    if (blockIdx.x == 0 && ph.hid_out != nullptr) {
+#pragma unroll
+      for (int j = 0; j < GMAX; ++j) {
+        const int g = tid + kConsumers * j;
+        if (g < ng) *reinterpret_cast<float4*>(ph.hid_out + 4 * g) = xv[0][j];
+      }
+    }
+  }
+  // ---- split into bf16 hi and lo rows: xs[2c][k] = hi, xs[2c+1][k] = lo
+  const uint32_t xsb = smem_u32(S.xs);
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+#pragma unroll
+    for (int j = 0; j < GMAX; ++j) {
+      const int g = tid + kConsumers * j;
+      if (g < ng) {
+        const float4 v = xv[c][j];
+        const float h0 = round_bf16(v.x), h1 = round_bf16(v.y), h2 = round_bf16(v.z), h3 = round_bf16(v.w);
+        const uint32_t hi01 = pack_bf16x2(h0, h1), hi23 = pack_bf16x2(h2, h3);
+        const uint32_t lo01 = pack_bf16x2(v.x - h0, v.y - h1), lo23 = pack_bf16x2(v.z - h2, v.w - h3);
+        const uint32_t ahi = xsb + 2u * static_cast<uint32_t>((2 * c) * K + 4 * g);
+        const uint32_t alo = xsb + 2u * static_cast<uint32_t>((2 * c + 1) * K + 4 * g);
+        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(ahi), "r"(hi01), "r"(hi23) : "memory");
+        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(alo), "r"(lo01), "r"(lo23) : "memory");
+      }
+    }
+  }
+  named_bar(1, kConsumers);
+
+  // ---- tiles: 8-row blocks, each matrix, each K tile; D accumulates over the K tiles
+  const int nmat = ph.nmat;
+  const uint32_t pitch = static_cast<uint32_t>(Kt) * 2u + kTileRowPad;
+  const int nsteps = Kt / 16;
+  const int am = lane >> 2;  // A row held by this lane (x column 2c = hi, 2c+1 = lo)
+  const bool a_live = lane < 8 * NC;
+  const uint32_t a_row = xsb + 2u * static_cast<uint32_t>(am * K + 2 * (lane & 3));
+  const uint32_t b_off = static_cast<uint32_t>(lane & 7) * pitch + static_cast<uint32_t>((lane >> 3) & 1) * 16u;
+  const uint32_t red = smem_u32(S.red);
+  for (int b = 0; b < nr; b += kTileRows) {
+    const int rows = min(kTileRows, nr - b);
+    for (int m = 0; m < nmat; ++m) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int kt = 0; kt < nkt; ++kt) {
+        const bool ok = wait_bar(cp, S, &S.full[pipe.stage], pipe.round & 1u, 4, false);
+        if (!ok) S.fail = 1;
+        if (ok) {
+          const uint32_t tb = smem_u32(S.ring[pipe.stage]) + b_off;
+          const uint32_t ab = a_row + 2u * static_cast<uint32_t>(kt * Kt);
+#pragma unroll 2
+          for (int st = warp; st < nsteps; st += kConsumerWarps) {
+            const uint32_t a0 = a_live ? lds32(ab + 32u * st) : 0u;
+            const uint32_t a2 = a_live ? lds32(ab + 32u * st + 16u) : 0u;
+            uint32_t b0, b1;
+            ldmatrix_x2(tb + 32u * st, b0, b1);
+            mma_bf16_16816(acc, a0, 0u, a2, 0u, b0, b1);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[pipe.stage]);
+        pipe.advance();
+      }
+      // rows 2c (hi) and 2c+1 (lo) of D: lanes 8c..8c+3 and 8c+4..8c+7, columns n = 2(lane&3), +1
+      const float o0 = __shfl_down_sync(0xffffffffu, acc[0], 4);
+      const float o1 = __shfl_down_sync(0xffffffffu, acc[1], 4);
+      if (a_live && (lane & 4) == 0) {
+        const int c = lane >> 3, n0 = 2 * (lane & 3);
+        if (n0 < rows) sts32f(red + 4u * ((((b + n0) * nmat + m) * NC + c) * kConsumerWarps + warp), acc[0] + o0);
+        if (n0 + 1 < rows)
+          sts32f(red + 4u * ((((b + n0 + 1) * nmat + m) * NC + c) * kConsumerWarps + warp), acc[1] + o1);
+      }
+    }
+  }
+  named_bar(1, kConsumers);
+
+  // ---- epilogue: add the warps' partials in a fixed order, apply the output rule
+  if (!S.fail) {
+    const int nout = nr * NC;
+    for (int idx = tid; idx < nout; idx += kConsumers) {
+      const int rl = idx / NC, c = idx % NC;
+      float a = 0.f, bb = 0.f;
+      for (int w = 0; w < kConsumerWarps; ++w) a += S.red[((rl * nmat + 0) * NC + c) * kConsumerWarps + w];
+      if (nmat == 2)
+        for (int w = 0; w < kConsumerWarps; ++w) bb += S.red[((rl * nmat + 1) * NC + c) * kConsumerWarps + w];
+      float* y = ph.y[c] + r0 + rl;
+      if (ph.epi == EPI_STORE) {
+        *y = a;
+      } else if (ph.epi == EPI_ADD) {
+        *y = (idx == tid ? yres : ldcg(y)) + a;
+      } else {
+        *y = (a / (1.0f + expf(-a))) * bb;
+      }
+    }
+  }
+}
+
 __device__ void gemv(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe) {
   if (cp.d.wdt == S2_BF16) {
-    if (ph.ncols == 1) gemv_t<uint16_t, 1>(cp, ph, S, pipe);
-    else gemv_t<uint16_t, 2>(cp, ph, S, pipe);
+    if (ph.ncols == 1) gemv_mma<1>(cp, ph, S, pipe);
+    else gemv_mma<2>(cp, ph, S, pipe);
   } else {
     if (ph.ncols == 1) gemv_t<float, 1>(cp, ph, S, pipe);
     else gemv_t<float, 2>(cp, ph, S, pipe);
@@ -464,7 +790,7 @@ __device__ __forceinline__ float f_to_kv<float>(float x) { return x; }
 // =========================================================================
 
 template <typename KT, int HD>
-__device__ void attn_slow_t(const CallParams& cp, const Phase& ph, Smem& S) {
+__device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, Smem& S) {
   constexpr int DPL = HD / 32;
   const Dims& d = cp.d;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -482,10 +808,11 @@ __device__ void attn_slow_t(const CallParams& cp, const Phase& ph, Smem& S) {
   const KT* Kc = static_cast<const KT*>(ph.kc);
   const KT* Vc = static_cast<const KT*>(ph.vc);
   const float2* rope_row = cp.rope + static_cast<size_t>(pos) * (HD / 2);
-  float* qs = S.misc + kMiscQ;
-  float* knew = S.misc + kMiscKV;
-  float* vnew = S.misc + kMiscKV + 128;
-  float* wp = S.misc + kMiscWarp;
+  float* xsf = reinterpret_cast<float*>(S.xs);
+  float* qs = xsf + kXsQ;
+  float* knew = xsf + kXsKV;
+  float* vnew = xsf + kXsKV + 128;
+  float* wp = xsf + kXsWarp;
 
   for (int item = blockIdx.x; item < nitems; item += G) {
     const int g = item / ns, s = item % ns;
@@ -539,6 +866,7 @@ __device__ void attn_slow_t(const CallParams& cp, const Phase& ph, Smem& S) {
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
       if (valid) {
         if (j == pos) {
+#pragma unroll 1
           for (int e = 0; e < HD; ++e) {
             const float kv = knew[e];
 #pragma unroll
@@ -701,7 +1029,7 @@ __device__ void attn_slow(const CallParams& cp, const Phase& ph, Smem& S) {
 // =========================================================================
 
 template <int HD>
-__device__ void attn_fast_t(const CallParams& cp, const Phase& ph, Smem& S) {
+__device__ __noinline__ void attn_fast_t(const CallParams& cp, const Phase& ph, Smem& S) {
   constexpr int DPL = HD / 32;
   const Dims& d = cp.d;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -804,6 +1132,9 @@ __device__ __forceinline__ uint32_t fkey(float z) {
   const uint32_t u = __float_as_uint(z);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+__device__ __forceinline__ float fval(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
 
 // warp-aggregated histogram update: lanes with the same bin add once (bin 256 = no update)
 __device__ __forceinline__ void hist_add(int* hist, int bin, int lane) {
@@ -823,47 +1154,49 @@ struct SampScratch {
   float cz[64];
   int tie_id[64];
 };
-static_assert(sizeof(SampScratch) <= kMiscWarp * sizeof(float) + 8 * 4 * 130 * sizeof(float), "sampler scratch");
+constexpr int kSampKeys = 1024;  // sampler keys [kSampPer][kConsumers] after the scratch (4-byte units)
+static_assert(sizeof(SampScratch) <= kSampKeys * 4, "sampler scratch");
+static_assert((kSampKeys + 17 * kConsumers) * 4 <= kXsBytes, "sampler keys");
 
 // One draw: the top-30 candidates by (value desc, id asc) are found with a 4-pass 8-bit radix
 // select of the 30th largest key, gathered, sorted by one warp; then, in one thread and in rank
 // order exactly as the method states: softmax over the 30, keep rank r iff r == 0 or
 // Σ_{s<r} π_s < top_p, winner = argmax π_r / E_r (ties -> lower rank).
 // Returns the drawn id in every consumer thread; -1 if nothing is drawable.
-__device__ int draw(const CallParams& cp, Smem& S, const float* logits, int n, bool main, bool mask_end,
-                    float temperature, float top_p, const float* E) {
+// Keys live in shared memory (kSampPer per thread, [k][thread]) so that the loops stay compact.
+__device__ __noinline__ int draw(const CallParams& cp, Smem& S, const float* logits, int n, bool main, bool mask_end,
+                                 float temperature, float top_p, const float* E) {
   const Dims& d = cp.d;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  SampScratch& W = *reinterpret_cast<SampScratch*>(S.misc);
-  uint32_t key[kSampPer];
-  float zv[kSampPer];
+  SampScratch& W = *reinterpret_cast<SampScratch*>(S.xs);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(S.xs) + kSampKeys;
   int nv = 0;
-#pragma unroll
   for (int k = 0; k < kSampPer; ++k) {
     const int i = tid + k * kConsumers;
-    key[k] = 0u;
-    zv[k] = 0.f;
+    uint32_t key = 0u;
     if (i < n) {
       const int id = entry_id(d, main, i);
       const float l = ldcg(logits + i);
       if (!(mask_end && main && id == d.im_end) && isfinite(l)) {
-        zv[k] = l / temperature;
-        key[k] = fkey(zv[k]);
+        key = fkey(l / temperature);
         ++nv;
       }
     }
+    keys[k * kConsumers + tid] = key;
   }
   W.hist[tid] = 0;
   if (tid == 0) {
     W.nvalid = 0;
-    W.prefix = 0;
+    W.prefix = 0u;
     W.n_gt = 0;
     W.n_eq = 0;
   }
   named_bar(1, kConsumers);
   if (nv) atomicAdd(&W.nvalid, nv);
-#pragma unroll
-  for (int k = 0; k < kSampPer; ++k) hist_add(W.hist, key[k] ? static_cast<int>(key[k] >> 24) : 256, lane);
+  for (int k = 0; k < kSampPer; ++k) {
+    const uint32_t key = keys[k * kConsumers + tid];
+    hist_add(W.hist, key ? static_cast<int>(key >> 24) : 256, lane);
+  }
   named_bar(1, kConsumers);
   const int kk = min(kTopK, W.nvalid);
   if (kk == 0) {
@@ -892,7 +1225,6 @@ __device__ int draw(const CallParams& cp, Smem& S, const float* logits, int n, b
       const unsigned b = __ballot_sync(0xffffffffu, excl < rem && incl >= rem);
       if (lane == __ffs(b) - 1) {
         int cum = excl;
-#pragma unroll
         for (int j = 0; j < 8; ++j) {
           if (cum + c[j] >= rem) {
             W.prefix = (W.prefix << 8) | static_cast<uint32_t>(255 - 8 * lane - j);
@@ -909,53 +1241,46 @@ __device__ int draw(const CallParams& cp, Smem& S, const float* logits, int n, b
     named_bar(1, kConsumers);
     const uint32_t pre = W.prefix;
     const int hs = 24 - 8 * pass;  // the prefix covers bits [hs, 32)
-#pragma unroll
-    for (int k = 0; k < kSampPer; ++k)
-      hist_add(W.hist, (key[k] && (key[k] >> hs) == pre) ? static_cast<int>((key[k] >> (hs - 8)) & 255u) : 256,
-               lane);
+    for (int k = 0; k < kSampPer; ++k) {
+      const uint32_t key = keys[k * kConsumers + tid];
+      hist_add(W.hist, (key && (key >> hs) == pre) ? static_cast<int>((key >> (hs - 8)) & 255u) : 256, lane);
+    }
     named_bar(1, kConsumers);
   }
   const uint32_t T = W.prefix;
   const int rem = W.rem;  // how many entries equal to T are among the top kk
   // ---- gather: all keys above T, and the entries tied at T
-#pragma unroll
   for (int k = 0; k < kSampPer; ++k) {
-    if (!key[k]) continue;
+    const uint32_t key = keys[k * kConsumers + tid];
+    if (!key || key < T) continue;
     const int id = entry_id(d, main, tid + k * kConsumers);
-    if (key[k] > T) {
+    if (key > T) {
       const int slot = atomicAdd(&W.n_gt, 1);
-      W.ck[slot] = key[k];
+      W.ck[slot] = key;
       W.cid[slot] = id;
-      W.cz[slot] = zv[k];
-    } else if (key[k] == T) {
+    } else {
       const int slot = atomicAdd(&W.n_eq, 1);
       if (slot < 64) W.tie_id[slot] = id;
-      if (slot == 0) W.cz[63] = zv[k];  // every tied entry has this value
     }
   }
   named_bar(1, kConsumers);
   const int n_gt = W.n_gt;
-  const float tz = W.cz[63];
   if (W.n_eq <= 64) {
     // warp 0: the rem lowest ids among the ties (bitonic sort of up to 64 ids, two per lane)
     if (warp == 0) {
       int a = lane < W.n_eq ? W.tie_id[lane] : 0x7fffffff;
       int b = lane + 32 < W.n_eq ? W.tie_id[lane + 32] : 0x7fffffff;
-      if (b < a) { const int t = a; a = b; b = t; }
-      // sort the 32 pairwise minima and the 32 maxima separately is not enough: full 64-sort
       for (int size = 2; size <= 64; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
           if (stride == 32) {
-            // partner of element lane is lane+32 in the same lane: a <-> b
-            const bool asc = true;
-            if (asc ? (b < a) : (a < b)) { const int t = a; a = b; b = t; }
+            if (b < a) { const int t = a; a = b; b = t; }
             continue;
           }
           const int pa = __shfl_xor_sync(0xffffffffu, a, stride);
           const int pb = __shfl_xor_sync(0xffffffffu, b, stride);
           const bool lower = (lane & stride) == 0;
-          const bool asc_a = (lane & size) == 0;               // element index = lane
-          const bool asc_b = ((lane + 32) & size) == 0;        // element index = lane + 32
+          const bool asc_a = (lane & size) == 0;
+          const bool asc_b = ((lane + 32) & size) == 0;
           a = (lower == asc_a) ? min(a, pa) : max(a, pa);
           b = (lower == asc_b) ? min(b, pb) : max(b, pb);
         }
@@ -963,7 +1288,6 @@ __device__ int draw(const CallParams& cp, Smem& S, const float* logits, int n, b
       if (lane < rem) {
         W.ck[n_gt + lane] = T;
         W.cid[n_gt + lane] = a;
-        W.cz[n_gt + lane] = tz;
       }
     }
   } else {
@@ -971,10 +1295,9 @@ __device__ int draw(const CallParams& cp, Smem& S, const float* logits, int n, b
     int last = -1;
     for (int r = 0; r < rem; ++r) {
       int best = 0x7fffffff;
-#pragma unroll
       for (int k = 0; k < kSampPer; ++k) {
         const int id = entry_id(d, main, tid + k * kConsumers);
-        if (key[k] == T && id > last && id < best) best = id;
+        if (keys[k * kConsumers + tid] == T && id > last && id < best) best = id;
       }
       for (int o = 16; o > 0; o >>= 1) best = min(best, __shfl_xor_sync(0xffffffffu, best, o));
       if (lane == 0) W.hist[warp] = best;
@@ -984,7 +1307,6 @@ __device__ int draw(const CallParams& cp, Smem& S, const float* logits, int n, b
       if (tid == 0) {
         W.ck[n_gt + r] = T;
         W.cid[n_gt + r] = m;
-        W.cz[n_gt + r] = tz;
       }
       last = m;
       named_bar(1, kConsumers);
@@ -995,23 +1317,20 @@ __device__ int draw(const CallParams& cp, Smem& S, const float* logits, int n, b
   if (warp == 0) {
     uint32_t kq = lane < kk ? W.ck[lane] : 0u;
     int iq = lane < kk ? W.cid[lane] : (0x7fffffff - lane);
-    float zq = lane < kk ? W.cz[lane] : 0.f;
     for (int size = 2; size <= 32; size <<= 1) {
       for (int stride = size >> 1; stride > 0; stride >>= 1) {
         const uint32_t pk = __shfl_xor_sync(0xffffffffu, kq, stride);
         const int pi = __shfl_xor_sync(0xffffffffu, iq, stride);
-        const float pz = __shfl_xor_sync(0xffffffffu, zq, stride);
         const bool lower = (lane & stride) == 0;
         const bool asc = (lane & size) == 0;  // "ascending" = best first
         const bool other_first = better_k(pk, pi, kq, iq);
         if ((lower == asc) == other_first) {
           kq = pk;
           iq = pi;
-          zq = pz;
         }
       }
     }
-    W.cz[lane] = zq;
+    W.cz[lane] = fval(kq);
     W.cid[lane] = iq;
     __syncwarp();
     if (lane == 0) {
@@ -1062,7 +1381,7 @@ __device__ void copy_vec(float* dst, const float* src, int n) {
 }
 
 // main draw, repetition-aware redraw, clamp, stop (CTA 0)
-__device__ void sample_main(const CallParams& cp, Smem& S, int f) {
+__device__ __noinline__ void sample_main(const CallParams& cp, Smem& S, int f) {
   const Dims& d = cp.d;
   StreamState* st = cp.st;
   const int fd = ldcgi(&st->frames_done);
@@ -1122,7 +1441,7 @@ __device__ void sample_main(const CallParams& cp, Smem& S, int f) {
 }
 
 // one Fast-AR draw (CTA 0), codebook c = 1..NCB-1
-__device__ void sample_fast(const CallParams& cp, Smem& S, int f, int c) {
+__device__ __noinline__ void sample_fast(const CallParams& cp, Smem& S, int f, int c) {
   const Dims& d = cp.d;
   if (cp.fast_only) {
     copy_vec(cp.fout + (static_cast<size_t>(f) * (d.ncb - 1) + (c - 1)) * d.cbs, cp.flogits, d.cbs);
@@ -1158,14 +1477,25 @@ __device__ void consumers(const CallParams& cp, Smem& S) {
   Pipe pipe{0, 0};
   unsigned target = 0;
   const bool cta0 = blockIdx.x == 0;
+  const int tid = threadIdx.x;
+  constexpr int NQ = static_cast<int>(sizeof(Phase) / 16);
   if (!cp.fast_only && ldcgi(&cp.st->done) != 0) {
-    if (cta0 && threadIdx.x == 0) cp.st->n_out = 0;
+    if (cta0 && tid == 0) cp.st->n_out = 0;
     return;
   }
-  if (cta0 && threadIdx.x == 0) cp.st->n_out = 0;
+  if (cta0 && tid == 0) cp.st->n_out = 0;
+  // phase descriptors live in shared memory; the next one is fetched while the current one runs
+  if (tid < NQ) reinterpret_cast<uint4*>(&S.ph[0])[tid] = __ldg(reinterpret_cast<const uint4*>(cp.prog) + tid);
+  named_bar(1, kConsumers);
+  int k = 0;
   for (int f = 0; f < cp.n_frames; ++f) {
-    for (int p = 0; p < cp.n_phases; ++p) {
-      const Phase& ph = cp.prog[p];
+    for (int p = 0; p < cp.n_phases; ++p, ++k) {
+      const Phase& ph = S.ph[k & 1];
+      int np = p + 1;
+      if (np == cp.n_phases) np = 0;
+      const bool has_next = (p + 1 < cp.n_phases) || (f + 1 < cp.n_frames);
+      uint4 nx = make_uint4(0u, 0u, 0u, 0u);
+      if (tid < NQ && has_next) nx = __ldg(reinterpret_cast<const uint4*>(cp.prog + np) + tid);
       switch (ph.op) {
         case OP_GEMV:
           if (ph.merge_main && cta0) sample_main(cp, S, f);
@@ -1189,13 +1519,14 @@ __device__ void consumers(const CallParams& cp, Smem& S) {
         default:
           break;
       }
-      if (ph.bump_pos && cta0 && threadIdx.x == 0) {
+      if (ph.bump_pos && cta0 && tid == 0) {
         cp.st->pos = cp.st->pos + 1;  // the Slow-AR step's last phase: its slot is now filled
       }
+      if (tid < NQ && has_next) reinterpret_cast<uint4*>(&S.ph[(k + 1) & 1])[tid] = nx;
       if (!grid_sync(cp, S, target)) return;
-      if (cp.trace != nullptr && cta0 && threadIdx.x == 0) {
-        const int k = f * cp.n_phases + p;
-        if (k < cp.trace_cap) cp.trace[k] = globaltimer_ns();
+      if (cp.trace != nullptr && cta0 && tid == 0) {
+        const int kk = f * cp.n_phases + p;
+        if (kk < cp.trace_cap) cp.trace[kk] = globaltimer_ns();
       }
       if ((ph.op == OP_SAMPLE_MAIN || ph.merge_main) && ldcgi(&cp.st->done) != 0) return;
     }

@@ -20,10 +20,14 @@ constexpr int kMaxFramesPerCall = 8192;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumers + 32;      // + one producer warp
-constexpr int kStages = 9;                     // weight ring depth
-constexpr int kStageBytes = 20480;             // one tile: 4 rows of 2560 bf16, 1 row of 9728 bf16
-constexpr int kRedFloats = 4096;               // per-CTA partial sums (GEMV row × slice)
+constexpr int kStages = 6;                     // weight ring depth
+constexpr int kStageBytes = 20608;             // one tile: 8 row segments of <= 1280 bf16 (+16 B pad each)
+constexpr int kTileRows = 8;                   // rows per bf16 weight tile (the MMA n dimension)
+constexpr int kTileRowPad = 16;                // bytes added to each tile row (bank-conflict-free ldmatrix)
+constexpr int kXsBytes = 77824;                // shared activations: bf16 hi/lo of <= 2 columns x 9728
+constexpr int kRedFloats = 2048;               // per-CTA partial sums (GEMV row × K-slice)
 constexpr int kXRegFloats = 80;                // activation slice per lane held in registers
+constexpr int kGemvChunksPerLane = 5;          // 16-byte chunks per lane: K-slices of 1/8 of <= 10240 bf16
 constexpr int kAttnMaxChunk = 2048;            // slots per split-K attention item
 
 enum Op : int {
@@ -91,11 +95,12 @@ struct GemvCol {
   float* wb;          // nullable: CTA 0 writes the raw (pre-norm) column here
 };
 
-struct Phase {
+struct alignas(16) Phase {
   int op;
   int merge_main;     // OP_GEMV: CTA 0 performs the main draw instead of GEMV rows
   int cta0;           // first CTA doing GEMV rows
   int M, K, nmat, ncols, epi, rows_per_tile, Q;
+  int Kt;                // bf16 weights: columns per tile (K = nkt * Kt)
   const void* w[2];   // row-major [M][K]; w[1] is the gate partner for EPI_SWIGLU
   const void* last_row;  // nullable: source of row M-1 (admissible logits: im_end row)
   const void* normw;     // nullable RMSNorm weight [K]
