@@ -143,6 +143,18 @@ struct Carver {
   }
 };
 
+// A 2-column bf16 projection stages 2 x 2 x K bf16 activations in shared memory; the Fast-AR
+// down projection of the first call (two positions) is split when that does not fit.
+bool split_fast_down(const Dims& d, int npos) {
+  return npos == 2 && d.wdt == S2_BF16 && 2LL * 2 * 2 * d.Ff > kXsBytes;
+}
+
+int fast_call_phases(const Dims& d) {
+  int n = 0;
+  for (int cb = 1; cb < d.ncb; ++cb) n += d.Lf * (5 + (split_fast_down(d, cb == 1 ? 2 : 1) ? 1 : 0)) + 2;
+  return n;
+}
+
 int attn_items_max(const Dims& d, int grid, int slots) {
   if (d.L == 0) return 1;
   return d.Hkv * (grid / d.Hkv + slots / kAttnMaxChunk + 2);
@@ -178,8 +190,8 @@ void carve(s2_ctx* c, Carver& cv) {
   c->part = cv.take<float>(static_cast<size_t>(attn_items_max(d, c->grid, c->kv_slots)) * 4 * (d.hd + 2));
   c->prefill_chunk = 512;
   c->pscratch = d.L > 0 ? cv.take<float>(prefill_scratch_floats(d, c->prefill_chunk)) : nullptr;
-  c->n_dec = d.L > 0 ? 1 + (d.ncb - 1) * (5 * d.Lf + 2) + 5 * d.L + 1 : 0;
-  c->n_fast = 2 + (d.ncb - 1) * (5 * d.Lf + 2);
+  c->n_dec = d.L > 0 ? 1 + fast_call_phases(d) + 5 * d.L + 1 : 0;
+  c->n_fast = 2 + fast_call_phases(d);
   c->prog = cv.take<Phase>(static_cast<size_t>(B) * c->n_dec + c->n_fast);
 }
 
@@ -233,6 +245,7 @@ struct Builder {
     out->push_back(p);
   }
   static GemvCol buf(const float* p, float* wb = nullptr) { return GemvCol{SRC_BUF, 0, p, wb}; }
+  bool split_down(int npos) const { return split_fast_down(c->d, npos); }
 
   // Fast-AR calls 1..NCB-1 (fast_only: without draws' side effects on the stream state)
   void fast_calls() {
@@ -279,12 +292,22 @@ struct Builder {
           u.y[j] = c->fg + static_cast<size_t>(j) * d.Ff;
         }
         push(u);
-        Phase dn = gemv(d.Df, d.Ff, npos, w.w2, nullptr, nullptr, EPI_ADD);
-        for (int j = 0; j < npos; ++j) {
-          dn.col[j] = buf(c->fg + static_cast<size_t>(j) * d.Ff);
-          dn.y[j] = c->fx + static_cast<size_t>(pos0 + j) * d.Df;
+        if (split_down(npos)) {
+          // two positions whose activations exceed the shared buffer: one phase per position
+          for (int j = 0; j < npos; ++j) {
+            Phase dn = gemv(d.Df, d.Ff, 1, w.w2, nullptr, nullptr, EPI_ADD);
+            dn.col[0] = buf(c->fg + static_cast<size_t>(j) * d.Ff);
+            dn.y[0] = c->fx + static_cast<size_t>(pos0 + j) * d.Df;
+            push(dn);
+          }
+        } else {
+          Phase dn = gemv(d.Df, d.Ff, npos, w.w2, nullptr, nullptr, EPI_ADD);
+          for (int j = 0; j < npos; ++j) {
+            dn.col[j] = buf(c->fg + static_cast<size_t>(j) * d.Ff);
+            dn.y[j] = c->fx + static_cast<size_t>(pos0 + j) * d.Df;
+          }
+          push(dn);
         }
-        push(dn);
       }
       Phase fo = gemv(d.cbs, d.Df, 1, c->FO, nullptr, c->fnorm, EPI_STORE);
       fo.col[0] = buf(c->fx + static_cast<size_t>(cb) * d.Df);

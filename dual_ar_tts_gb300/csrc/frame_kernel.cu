@@ -117,7 +117,8 @@ __device__ bool grid_sync(const CallParams& cp, Smem& S, unsigned& target) {
   if (threadIdx.x == 0) {
     int ok = !should_bail(cp, S);
     if (ok) {
-      __threadfence();
+      // release: this CTA's writes (ordered before by the named barrier) become visible with the
+      // arrival; acquire on the spin makes every other CTA's writes visible after it
       red_release_add(&cp.ctl->gbar, 1u);
       const long long lim = cp.ctl->spin_limit;
       long long t0 = 0;
@@ -137,7 +138,6 @@ __device__ bool grid_sync(const CallParams& cp, Smem& S, unsigned& target) {
           }
         }
       }
-      __threadfence();
     }
     S.sync_ok = ok;
     if (!ok) S.fail = 1;
@@ -159,16 +159,35 @@ __device__ __forceinline__ void unpack16(const uint4& u, float* f, float) {
 // producer
 // =========================================================================
 
+// K split of an 8-row (or shorter) bf16 tile: the fewest K tiles such that `rows` padded row
+// segments fit one stage (Kt a multiple of 16 dividing K).  Producer and consumers agree on it.
+__device__ __forceinline__ int tile_kt(int K, int rows) {
+  for (int n = 1; n <= K / 16; ++n) {
+    if (K % n != 0 || (K / n) % 16 != 0) continue;
+    if (rows * ((K / n) * 2 + kTileRowPad) <= kStageBytes) return K / n;
+  }
+  return 16;
+}
+
+// Producer warp: walks the program ahead of the consumers and fills the ring with each GEMV
+// phase's weights (the RMSNorm vector first, then the row tiles).  Lane 0 waits for a free stage
+// and posts the byte count; the tile's row segments are then issued by separate lanes.
+__device__ bool producer_acquire(const CallParams& cp, Smem& S, Pipe& pp, uint32_t bytes) {
+  const int lane = threadIdx.x & 31;
+  int ok = 1;
+  if (lane == 0) {
+    ok = wait_bar(cp, S, &S.empty[pp.stage], (pp.round & 1u) ^ 1u, 2, true) ? 1 : 0;
+    if (ok) mbar_arrive_expect_tx(&S.full[pp.stage], bytes);
+  }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 __device__ void producer(const CallParams& cp, Smem& S) {
-  // The whole warp walks the program: lanes fetch the next phase descriptor (one 16-byte load
-  // each) while lane 0 issues the current phase's tile copies.
   const int lane = threadIdx.x & 31;
   constexpr int NQ = static_cast<int>(sizeof(Phase) / 16);
   const uint64_t pol = policy_evict_first();
   Pipe pp{0, 0};
-  uint32_t fill_parity[kStages];
-  bool filled[kStages];
-  for (int s = 0; s < kStages; ++s) filled[s] = false;
+  unsigned long long issued = 0;  // stages filled so far (all lanes keep the same count)
   int stop = (ld_volatile_int(&cp.st->done) != 0 && !cp.fast_only) ? 1 : 0;
   if (lane < NQ) reinterpret_cast<uint4*>(&S.pph[0])[lane] = __ldg(reinterpret_cast<const uint4*>(cp.prog) + lane);
   __syncwarp();
@@ -180,79 +199,70 @@ __device__ void producer(const CallParams& cp, Smem& S) {
       const bool has_next = (p + 1 < cp.n_phases) || (f + 1 < cp.n_frames);
       uint4 nx = make_uint4(0u, 0u, 0u, 0u);
       if (lane < NQ && has_next) nx = __ldg(reinterpret_cast<const uint4*>(cp.prog + np) + lane);
-      if (lane == 0 && ph.op == OP_GEMV) {
+      if (ph.op == OP_GEMV && !(ph.merge_main && blockIdx.x == 0)) {
         int r0, nr;
         rows_of(ph, blockIdx.x, gridDim.x, r0, nr);
-        const int R = ph.rows_per_tile;
         const uint32_t rowb = static_cast<uint32_t>(ph.K) * cp.d.esz;
-        if (ph.normw != nullptr && !(ph.merge_main && blockIdx.x == 0)) {
+        if (ph.normw != nullptr) {
           // the RMSNorm weight vector travels through the ring ahead of the phase's row tiles
-          if (!wait_bar(cp, S, &S.empty[pp.stage], (pp.round & 1u) ^ 1u, 2, true)) stop = 1;
-          if (!stop) {
-            mbar_arrive_expect_tx(&S.full[pp.stage], rowb);
-            bulk_g2s(S.ring[pp.stage], ph.normw, rowb, &S.full[pp.stage], pol);
-            fill_parity[pp.stage] = pp.round & 1u;
-            filled[pp.stage] = true;
+          if (!producer_acquire(cp, S, pp, rowb)) {
+            stop = 1;
+          } else {
+            if (lane == 0) bulk_g2s(S.ring[pp.stage], ph.normw, rowb, &S.full[pp.stage], pol);
             pp.advance();
+            ++issued;
           }
         }
         if (cp.d.esz == 2) {
-          // bf16: tiles of 8 rows x Kt columns; one copy per row segment, rows padded by 16 bytes
-          const int Kt = ph.Kt, nkt = ph.K / Kt;
-          const uint32_t segb = static_cast<uint32_t>(Kt) * 2u, pitch = segb + kTileRowPad;
+          // bf16: tiles of <= 8 rows x Kt columns, row segments padded by 16 bytes, one lane per row
           for (int b = 0; b < nr && !stop; b += kTileRows) {
             const int rows = min(kTileRows, nr - b);
+            const int Kt = tile_kt(ph.K, rows), nkt = ph.K / Kt;
+            const uint32_t segb = static_cast<uint32_t>(Kt) * 2u, pitch = segb + kTileRowPad;
+            const int row = r0 + b + lane;
             for (int m = 0; m < ph.nmat && !stop; ++m) {
+              const unsigned char* rsrc =
+                  (ph.last_row != nullptr && row == ph.M - 1)
+                      ? static_cast<const unsigned char*>(ph.last_row)
+                      : static_cast<const unsigned char*>(ph.w[m]) + static_cast<size_t>(row) * rowb;
               for (int kt = 0; kt < nkt; ++kt) {
-                if (!wait_bar(cp, S, &S.empty[pp.stage], (pp.round & 1u) ^ 1u, 2, true)) {
+                if (!producer_acquire(cp, S, pp, segb * rows)) {
                   stop = 1;
                   break;
                 }
-                uint64_t* fb = &S.full[pp.stage];
-                mbar_arrive_expect_tx(fb, segb * rows);
-                unsigned char* dst = S.ring[pp.stage];
-                for (int i = 0; i < rows; ++i) {
-                  const int row = r0 + b + i;
-                  const unsigned char* src =
-                      (ph.last_row != nullptr && row == ph.M - 1)
-                          ? static_cast<const unsigned char*>(ph.last_row) + static_cast<size_t>(kt) * segb
-                          : static_cast<const unsigned char*>(ph.w[m]) + static_cast<size_t>(row) * rowb +
-                                static_cast<size_t>(kt) * segb;
-                  bulk_g2s(dst + static_cast<size_t>(i) * pitch, src, segb, fb, pol);
-                }
-                fill_parity[pp.stage] = pp.round & 1u;
-                filled[pp.stage] = true;
+                if (lane < rows)
+                  bulk_g2s(S.ring[pp.stage] + lane * pitch, rsrc + static_cast<size_t>(kt) * segb, segb,
+                           &S.full[pp.stage], pol);
                 pp.advance();
+                ++issued;
               }
             }
           }
-        }
-        for (int t = 0; t < nr && !stop && cp.d.esz != 2; t += R) {
-          const int rr = min(R, nr - t);
-          if (!wait_bar(cp, S, &S.empty[pp.stage], (pp.round & 1u) ^ 1u, 2, true)) {
-            stop = 1;
-            break;
-          }
-          const uint32_t bytes = rowb * rr * ph.nmat;
-          uint64_t* fb = &S.full[pp.stage];
-          mbar_arrive_expect_tx(fb, bytes);
-          unsigned char* dst = S.ring[pp.stage];
-          const int row = r0 + t;
-          for (int m = 0; m < ph.nmat; ++m) {
-            const unsigned char* src = static_cast<const unsigned char*>(ph.w[m]) + static_cast<size_t>(row) * rowb;
-            unsigned char* dm = dst + static_cast<size_t>(m) * rr * rowb;
-            if (ph.last_row != nullptr && row + rr == ph.M) {
-              if (rr > 1) bulk_g2s(dm, src, rowb * (rr - 1), fb, pol);
-              bulk_g2s(dm + static_cast<size_t>(rr - 1) * rowb, ph.last_row, rowb, fb, pol);
-            } else {
-              bulk_g2s(dm, src, rowb * rr, fb, pol);
+        } else {
+          // fp32: tiles of whole rows, one copy
+          const int R = ph.rows_per_tile;
+          for (int t = 0; t < nr && !stop; t += R) {
+            const int rr = min(R, nr - t);
+            if (!producer_acquire(cp, S, pp, rowb * rr * ph.nmat)) {
+              stop = 1;
+              break;
             }
+            if (lane < ph.nmat) {
+              const unsigned char* src =
+                  static_cast<const unsigned char*>(ph.w[lane]) + static_cast<size_t>(r0 + t) * rowb;
+              unsigned char* dm = S.ring[pp.stage] + static_cast<size_t>(lane) * rr * rowb;
+              if (ph.last_row != nullptr && r0 + t + rr == ph.M) {
+                if (rr > 1) bulk_g2s(dm, src, rowb * (rr - 1), &S.full[pp.stage], pol);
+                bulk_g2s(dm + static_cast<size_t>(rr - 1) * rowb, ph.last_row, rowb, &S.full[pp.stage], pol);
+              } else {
+                bulk_g2s(dm, src, rowb * rr, &S.full[pp.stage], pol);
+              }
+            }
+            pp.advance();
+            ++issued;
           }
-          fill_parity[pp.stage] = pp.round & 1u;
-          filled[pp.stage] = true;
-          pp.advance();
         }
-        if (cp.trace != nullptr && blockIdx.x == 0) {
+        if (lane == 0 && cp.trace != nullptr && blockIdx.x == 0) {
           const int kk = f * cp.n_phases + p;
           if (kk < cp.trace_cap) cp.trace[cp.trace_cap + kk] = globaltimer_ns();
         }
@@ -263,11 +273,13 @@ __device__ void producer(const CallParams& cp, Smem& S) {
     }
   }
   if (lane != 0) return;
-  // Leave no copy in flight: wait for every stage whose last fill may not have landed.
-  for (int s = 0; s < kStages; ++s) {
-    if (!filled[s]) continue;
+  // Leave no copy in flight: the last fill of each stage must have landed before the CTA exits.
+  for (unsigned long long back = 1; back <= kStages && back <= issued; ++back) {
+    const unsigned long long t = issued - back;
+    const int s = static_cast<int>(t % kStages);
+    const uint32_t par = static_cast<uint32_t>((t / kStages) & 1u);
     const long long t0 = clock_us();
-    while (!mbar_test(&S.full[s], fill_parity[s])) {
+    while (!mbar_test(&S.full[s], par)) {
       if (clock_us() - t0 > cp.ctl->spin_limit) {
         if (atomicCAS(&cp.ctl->error, 0, S2_ETIMEOUT) == 0) cp.ctl->error_where = 3;
         break;
@@ -534,7 +546,7 @@ template <int NC>
 __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe) {
   const Dims& d = cp.d;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int K = ph.K, Kt = ph.Kt, nkt = K / Kt;
+  const int K = ph.K;
   const bool has_norm = ph.normw != nullptr;
   int r0, nr;
   rows_of(ph, blockIdx.x, gridDim.x, r0, nr);
@@ -671,36 +683,54 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
 
   // ---- tiles: 8-row blocks, each matrix, each K tile; D accumulates over the K tiles
   const int nmat = ph.nmat;
-  const uint32_t pitch = static_cast<uint32_t>(Kt) * 2u + kTileRowPad;
-  const int nsteps = Kt / 16;
   const int am = lane >> 2;  // A row held by this lane (x column 2c = hi, 2c+1 = lo)
   const bool a_live = lane < 8 * NC;
   const uint32_t a_row = xsb + 2u * static_cast<uint32_t>(am * K + 2 * (lane & 3));
-  const uint32_t b_off = static_cast<uint32_t>(lane & 7) * pitch + static_cast<uint32_t>((lane >> 3) & 1) * 16u;
   const uint32_t red = smem_u32(S.red);
   for (int b = 0; b < nr; b += kTileRows) {
     const int rows = min(kTileRows, nr - b);
+    const int Kt = tile_kt(K, rows), nkt = K / Kt;
+    const uint32_t pitch = static_cast<uint32_t>(Kt) * 2u + kTileRowPad;
+    const int nsteps = Kt / 16;
+    // ldmatrix.x4 rows: matrices 0,1 = k step s (k, k+8), matrices 2,3 = k step s + 8; rows past the
+    // block's last one repeat it (their outputs are discarded)
+    const uint32_t b_off2 = static_cast<uint32_t>(min(lane & 7, rows - 1)) * pitch +
+                            static_cast<uint32_t>((lane >> 3) & 1) * 16u;
+    const uint32_t b_off = b_off2 + static_cast<uint32_t>((lane >> 4) & 1) * 256u;
     for (int m = 0; m < nmat; ++m) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
       for (int kt = 0; kt < nkt; ++kt) {
         const bool ok = wait_bar(cp, S, &S.full[pipe.stage], pipe.round & 1u, 4, false);
         if (!ok) S.fail = 1;
         if (ok) {
-          const uint32_t tb = smem_u32(S.ring[pipe.stage]) + b_off;
+          const uint32_t tb = smem_u32(S.ring[pipe.stage]);
           const uint32_t ab = a_row + 2u * static_cast<uint32_t>(kt * Kt);
-#pragma unroll 2
-          for (int st = warp; st < nsteps; st += kConsumerWarps) {
+          // steps s and s + 8 per iteration: two independent accumulation chains
+          for (int st = warp; st < nsteps; st += 2 * kConsumerWarps) {
+            const bool two = st + kConsumerWarps < nsteps;
+            uint32_t b0, b1, b2, b3;
+            if (two) {
+              ldmatrix_x4(tb + b_off + 32u * st, b0, b1, b2, b3);
+            } else {
+              ldmatrix_x2(tb + b_off2 + 32u * st, b0, b1);
+              b2 = b3 = 0u;
+            }
             const uint32_t a0 = a_live ? lds32(ab + 32u * st) : 0u;
             const uint32_t a2 = a_live ? lds32(ab + 32u * st + 16u) : 0u;
-            uint32_t b0, b1;
-            ldmatrix_x2(tb + 32u * st, b0, b1);
             mma_bf16_16816(acc, a0, 0u, a2, 0u, b0, b1);
+            if (two) {
+              const uint32_t c0 = a_live ? lds32(ab + 32u * (st + kConsumerWarps)) : 0u;
+              const uint32_t c2 = a_live ? lds32(ab + 32u * (st + kConsumerWarps) + 16u) : 0u;
+              mma_bf16_16816(acc2, c0, 0u, c2, 0u, b2, b3);
+            }
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[pipe.stage]);
         pipe.advance();
       }
+      acc[0] += acc2[0];
+      acc[1] += acc2[1];
       // rows 2c (hi) and 2c+1 (lo) of D: lanes 8c..8c+3 and 8c+4..8c+7, columns n = 2(lane&3), +1
       const float o0 = __shfl_down_sync(0xffffffffu, acc[0], 4);
       const float o1 = __shfl_down_sync(0xffffffffu, acc[1], 4);
