@@ -35,6 +35,9 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-frames", type=int, default=2, help="frames in the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--slow-layers", type=int, default=None,
+                    help="profiling captures only: Slow-AR layer count (S2-Pro widths kept); the bench line "
+                         "then describes that smaller model")
     return ap.parse_args()
 
 
@@ -211,6 +214,10 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     d = synth.CONFIGS["frame"]["dims"]
+    workload = WORKLOAD
+    if args.slow_layers is not None:
+        d = dict(d, n_layer=args.slow_layers)
+        workload = WORKLOAD.replace("36+4 layers", f"{args.slow_layers}+4 layers (profiling case)")
     s = synth.sampling("frame", min_tokens_before_end=args.warmup + args.steps + 1)
     t_setup = time.perf_counter()
     host_w = synth.make_weights(d, 0)
@@ -277,7 +284,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": t_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded random weights of the S2-Pro shape, synthetic prompt/variates)",
-        "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": PROMPT_LEN,
+        "config": {"workload": workload, "global_batch": world, "seq_len": PROMPT_LEN,
                    "parallelism": f"replicas{world}" if world > 1 else "none",
                    "frames_per_call": K, "l2": "inputs larger than L2 (9.1 GB of weights streamed per frame)"},
         "per_stream_fps": K / (dev_ms / 1000.0),
@@ -291,7 +298,7 @@ def main():
         "clocks": clk.summary(),
         "setup_s": setup_s,
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and args.slow_layers is None:
         try:
             v, cores, sample = cpu_oracle_sample(d, host_w, args.cpu_frames, s)
             line["cpu_baseline"] = {"value": v, "unit": "frames/s", "cores": cores, "kind": "oracle", "sample": sample}
