@@ -20,7 +20,7 @@ STATUS_NAMES = {0: "S2_OK", 1: "S2_EINVAL", 2: "S2_ENOMEM", 3: "S2_ECAPACITY", 4
 
 EXPORTS = ("s2_weight_count", "s2_weight_info", "s2_frame_workspace_bytes", "s2_frame_init", "s2_prefill",
            "s2_decode_frames", "s2_fast_logits", "s2_sync_status", "s2_set_spin_limit", "s2_set_trace",
-           "s2_phase_count", "s2_frame_free", "s2_last_error")
+           "s2_phase_count", "s2_frame_free", "s2_last_error", "s2_fast_logits_static")
 
 
 class s2_dims(ctypes.Structure):
@@ -76,6 +76,7 @@ def load(path: str = LIB_PATH):
         "s2_phase_count": (i32, [vp, i32]),
         "s2_frame_free": (i32, [vp]),
         "s2_last_error": (ctypes.c_char_p, [vp]),
+        "s2_fast_logits_static": (i32, [P(s2_dims), P(vp), i32, i32, vp, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -170,6 +171,16 @@ def s2_frame_free(ctx):
 
 def s2_last_error(ctx=None) -> str:
     return load().s2_last_error(ctx).decode()
+
+
+def s2_fast_logits_static(dims: s2_dims, weight_ptrs, n_frames: int, hidden_ptr: int, prefix_ptr: int,
+                          logits_ptr: int, status_ptr: int | None = None, stream: int = 0):
+    """Fast-AR alone on the library's static scratch: no context, no workspace, no allocation.
+    The caller passes every input and output (device pointers)."""
+    arr = (ctypes.c_void_p * len(weight_ptrs))(*[p if p else None for p in weight_ptrs])
+    rc = load().s2_fast_logits_static(ctypes.byref(dims), arr, len(weight_ptrs), n_frames, hidden_ptr, prefix_ptr,
+                                      logits_ptr, status_ptr, stream)
+    return _check("s2_fast_logits_static", rc)
 
 
 def make_sampling(s: dict) -> s2_sampling:

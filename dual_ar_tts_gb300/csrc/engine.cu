@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -741,3 +742,250 @@ int s2_frame_free(s2_ctx* c) {
 const char* s2_last_error(const s2_ctx* c) { return c ? c->err.c_str() : g_init_error.c_str(); }
 
 }  // extern "C"
+
+// ============================================ Fast-AR alone on static scratch (no allocation)
+//
+// s2_fast_logits_static serves callers that may not allocate device memory (a host application
+// whose pool already holds the device memory, or a latency-critical thread that must not block
+// in cudaMalloc/cudaFree).  Its scratch is a file-scope device array that is part of this
+// library; every call on a device shares it.
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = S2_STATIC_SCRATCH_BYTES;
+constexpr int kStaticMaxPhases = 1024;
+constexpr int kStaticMaxDevices = 64;
+constexpr int kStaticMaxFrames = 1 << 20;
+
+// In host code this name is only a stand-in for the symbol: the device address of each device's
+// copy comes from cudaGetSymbolAddress, made once per device with that device current.
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+struct StaticDevice {
+  unsigned char* scratch = nullptr;  // device address of g_static_scratch on this device
+  int grid = 0;                      // frame kernel grid (one CTA per SM)
+};
+
+std::mutex g_static_mu;                       // serialises the host side of the calls
+StaticDevice g_static_dev[kStaticMaxDevices];
+Phase g_static_prog[kStaticMaxPhases];        // host copy of the program being uploaded
+
+struct StaticFastLayout {
+  Control* ctl;
+  float2* rope_f;
+  StreamState* st;
+  float *hidden, *fx, *fqkv, *fo, *fg, *fk, *fv, *flogits;
+  int32_t* fcode;
+  Phase* prog;
+};
+
+// Scratch of the Fast-AR-alone program: the context's Fast-AR buffers, carved from the array.
+size_t carve_static_fast(const Dims& d, int n_phases, unsigned char* base, StaticFastLayout& s) {
+  Carver cv{base};
+  const int QKVf = (d.Hqf + 2 * d.Hkvf) * d.hdf;
+  s.ctl = cv.take<Control>(1);
+  s.rope_f = cv.take<float2>(static_cast<size_t>(d.Wf) * (d.hdf / 2));
+  s.st = cv.take<StreamState>(1);
+  s.hidden = cv.take<float>(d.D);
+  s.fx = cv.take<float>(static_cast<size_t>(d.Wf) * d.Df);
+  s.fqkv = cv.take<float>(2 * static_cast<size_t>(QKVf));
+  s.fo = cv.take<float>(2 * static_cast<size_t>(d.Hqf) * d.hdf);
+  s.fg = cv.take<float>(2 * static_cast<size_t>(d.Ff));
+  s.fk = cv.take<float>(static_cast<size_t>(d.Lf) * d.Wf * d.Hkvf * d.hdf);
+  s.fv = cv.take<float>(static_cast<size_t>(d.Lf) * d.Wf * d.Hkvf * d.hdf);
+  s.flogits = cv.take<float>(d.cbs);
+  s.fcode = cv.take<int32_t>(16);
+  s.prog = cv.take<Phase>(static_cast<size_t>(n_phases));
+  return align_up(cv.off, 256);
+}
+
+// The Fast-AR-alone program (the same phases as a context's) over the static layout, written to
+// `out` (host, kStaticMaxPhases entries).  wt is the s2_frame_init weight table.
+int build_static_fast_program(const Dims& d, int grid, const void* const* wt, const StaticFastLayout& s,
+                              Phase* out, int* n_out, std::string& why) {
+  s2_ctx shape;  // the phase helper reads only the shape
+  shape.d = d;
+  shape.grid = grid;
+  Builder b{&shape, nullptr, {}};
+  int n = 0;
+  auto push = [&](const Phase& p) {
+    if (p.op == OP_GEMV) {
+      const int g2 = grid - p.cta0;
+      const int rows = (p.M + g2 - 1) / g2;
+      if (static_cast<long long>(rows) * p.nmat * p.ncols * kConsumerWarps > kRedFloats)
+        b.err = "too many rows per CTA for the partial-sum buffer";
+    }
+    if (n < kStaticMaxPhases) out[n] = p;
+    ++n;
+  };
+  const int base = 3 + 9 * d.L;
+  const void* P = wt[base];
+  const void* fnorm = wt[base + 2];
+  const void* FO = wt[base + 3];
+  auto fw = [&](int l, int k) { return wt[base + 4 + 9 * l + k]; };  // an wqkv qn kn wo fn w1 w3 w2
+  Phase fi{};
+  fi.op = OP_FAST_IN;
+  push(fi);
+  if (d.has_proj) {
+    Phase p = b.gemv(d.Df, d.D, 1, P, nullptr, nullptr, EPI_STORE);
+    p.col[0] = Builder::buf(s.hidden);
+    p.y[0] = s.fx;
+    push(p);
+  } else {
+    push(fi);  // keeps the program length of a context's Fast-AR-alone program
+  }
+  const int QKVf = (d.Hqf + 2 * d.Hkvf) * d.hdf;
+  const size_t kvl = static_cast<size_t>(d.Wf) * d.Hkvf * d.hdf;
+  const float scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d.hdf)));
+  for (int cb = 1; cb < d.ncb; ++cb) {
+    const int npos = cb == 1 ? 2 : 1, pos0 = cb == 1 ? 0 : cb;
+    for (int l = 0; l < d.Lf; ++l) {
+      Phase q = b.gemv(QKVf, d.Df, npos, fw(l, 1), nullptr, fw(l, 0), EPI_STORE);
+      for (int j = 0; j < npos; ++j) {
+        const int p = pos0 + j;
+        float* xp = s.fx + static_cast<size_t>(p) * d.Df;
+        if (l == 0 && p >= 1) q.col[j] = GemvCol{SRC_FEROW, 0, s.fcode + (p - 1), xp};
+        else if (l == 0 && p == 0 && !d.has_proj) q.col[j] = Builder::buf(s.hidden, xp);
+        else q.col[j] = Builder::buf(xp);
+        q.y[j] = s.fqkv + static_cast<size_t>(j) * QKVf;
+      }
+      push(q);
+      Phase a{};
+      a.op = OP_ATTN_FAST;
+      a.layer = l;
+      a.npos = npos;
+      a.pos0 = pos0;
+      a.qkv = s.fqkv;
+      a.out = s.fo;
+      a.kc = s.fk + l * kvl;
+      a.vc = s.fv + l * kvl;
+      a.qn = fw(l, 2);
+      a.kn = fw(l, 3);
+      a.scale = scale;
+      push(a);
+      Phase o = b.gemv(d.Df, d.Hqf * d.hdf, npos, fw(l, 4), nullptr, nullptr, EPI_ADD);
+      for (int j = 0; j < npos; ++j) {
+        o.col[j] = Builder::buf(s.fo + static_cast<size_t>(j) * d.Hqf * d.hdf);
+        o.y[j] = s.fx + static_cast<size_t>(pos0 + j) * d.Df;
+      }
+      push(o);
+      Phase u = b.gemv(d.Ff, d.Df, npos, fw(l, 6), fw(l, 7), fw(l, 5), EPI_SWIGLU);
+      for (int j = 0; j < npos; ++j) {
+        u.col[j] = Builder::buf(s.fx + static_cast<size_t>(pos0 + j) * d.Df);
+        u.y[j] = s.fg + static_cast<size_t>(j) * d.Ff;
+      }
+      push(u);
+      const int ndown = split_fast_down(d, npos) ? npos : 1;  // one phase per position when split
+      for (int t = 0; t < ndown; ++t) {
+        const int nc = ndown == 1 ? npos : 1;
+        Phase dn = b.gemv(d.Df, d.Ff, nc, fw(l, 8), nullptr, nullptr, EPI_ADD);
+        for (int j = 0; j < nc; ++j) {
+          const int jj = ndown == 1 ? j : t;
+          dn.col[j] = Builder::buf(s.fg + static_cast<size_t>(jj) * d.Ff);
+          dn.y[j] = s.fx + static_cast<size_t>(pos0 + jj) * d.Df;
+        }
+        push(dn);
+      }
+    }
+    Phase fo = b.gemv(d.cbs, d.Df, 1, FO, nullptr, fnorm, EPI_STORE);
+    fo.col[0] = Builder::buf(s.fx + static_cast<size_t>(cb) * d.Df);
+    fo.y[0] = s.flogits;
+    push(fo);
+    Phase sf{};
+    sf.op = OP_SAMPLE_FAST;
+    sf.cb = cb;
+    push(sf);
+  }
+  if (!b.err.empty()) {
+    why = b.err;
+    return S2_EINVAL;
+  }
+  if (n > kStaticMaxPhases) {
+    why = "the Fast-AR program has " + std::to_string(n) + " phases; the static path holds at most " +
+          std::to_string(kStaticMaxPhases);
+    return S2_ENOMEM;
+  }
+  *n_out = n;
+  return S2_OK;
+}
+
+int static_fail(int code, const std::string& msg) { return fail(nullptr, code, "s2_fast_logits_static: " + msg); }
+
+}  // namespace
+
+extern "C" int s2_fast_logits_static(const s2_dims* s, const void* const* weights, int n_weights, int n_frames,
+                                     const float* hidden, const int32_t* prefix, float* logits, int32_t* status,
+                                     CUstream_st* stream) {
+  Dims d;
+  std::string why;
+  if (!s || !to_dims(s, d, why)) return static_fail(S2_EINVAL, "bad dims: " + why);
+  if (!weights || n_weights != layer_count(d)) return static_fail(S2_EINVAL, "weight table size does not match the dims");
+  if (n_frames <= 0 || n_frames > kStaticMaxFrames) return static_fail(S2_EINVAL, "n_frames must be in 1..1048576");
+  if (!hidden || !prefix || !logits) return static_fail(S2_EINVAL, "hidden, prefix and logits are required");
+  const int base = 3 + 9 * d.L;
+  for (int i = base; i < n_weights; ++i) {
+    if (i == base && !d.has_proj) continue;
+    if (!weights[i]) return static_fail(S2_EINVAL, "a Fast-AR weight is NULL");
+    if (reinterpret_cast<uintptr_t>(weights[i]) & 15u) return static_fail(S2_EINVAL, "weights must be 16-byte aligned");
+  }
+  const int n_phases = 2 + fast_call_phases(d);
+  StaticFastLayout probe{};
+  const size_t need = carve_static_fast(d, n_phases, nullptr, probe);
+  if (need > kStaticScratchBytes)
+    return static_fail(S2_ENOMEM, "this Fast-AR shape needs " + std::to_string(need) +
+                                      " bytes of scratch; the static array holds " + std::to_string(kStaticScratchBytes));
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return static_fail(S2_ECUDA, "no current CUDA device");
+  if (dev < 0 || dev >= kStaticMaxDevices) return static_fail(S2_EINVAL, "device ordinal above 63");
+  StaticDevice& sd = g_static_dev[dev];
+  if (sd.scratch == nullptr) {
+    // set-up, once per device (this device is current)
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+    if (e != cudaSuccess) return static_fail(S2_ECUDA, std::string("cudaGetSymbolAddress failed: ") + cudaGetErrorString(e));
+    int grid = 0;
+    if (frame_kernel_grid(dev, &grid) != S2_OK) return static_fail(S2_ECUDA, "the frame kernel cannot be resident on this device");
+    sd.grid = grid;
+    sd.scratch = static_cast<unsigned char*>(ptr);
+  }
+  StaticFastLayout sl{};
+  carve_static_fast(d, n_phases, sd.scratch, sl);
+  int n_built = 0;
+  int rc = build_static_fast_program(d, sd.grid, weights, sl, g_static_prog, &n_built, why);
+  if (rc != S2_OK) return static_fail(rc, why);
+  if (n_built != n_phases) return static_fail(S2_EINVAL, "internal: Fast-AR program length");
+  cudaStream_t cs = stream;
+  // what must start from zero (the array keeps the previous call's contents): control block, stream state
+  Control ctl{};
+  ctl.spin_limit = 2000000;
+  if (cudaMemcpyAsync(sl.ctl, &ctl, sizeof(Control), cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+      cudaMemsetAsync(sl.st, 0, sizeof(StreamState), cs) != cudaSuccess ||
+      cudaMemcpyAsync(sl.prog, g_static_prog, sizeof(Phase) * n_phases, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+    return static_fail(S2_ECUDA, "initialising the static scratch failed");
+  if (build_rope_tables(nullptr, 0, d.hd, sl.rope_f, d.Wf, d.hdf, d.rope_base, d.rope_bf16, cs) != S2_OK)
+    return static_fail(S2_ECUDA, "building the RoPE table failed");
+  CallParams cp{};
+  cp.d = d;
+  cp.ctl = sl.ctl;
+  cp.fcode = sl.fcode;
+  cp.flogits = sl.flogits;
+  cp.rope_f = sl.rope_f;
+  cp.FE = weights[base + 1];
+  cp.n_frames = n_frames;
+  cp.fast_only = 1;
+  cp.n_phases = n_phases;
+  cp.prog = sl.prog;
+  cp.st = sl.st;
+  cp.hidden = sl.hidden;
+  cp.fin_hidden = hidden;
+  cp.fin_prefix = prefix;
+  cp.fout = logits;
+  cp.temperature = 1.f;
+  cp.top_p = 1.f;
+  rc = launch_frames(cp, sd.grid, cs);
+  if (rc != S2_OK) return static_fail(rc, std::string("frame kernel launch failed: ") + cudaGetErrorString(cudaGetLastError()));
+  if (status && cudaMemcpyAsync(status, &sl.ctl->error, 2 * sizeof(int32_t), cudaMemcpyDeviceToDevice, cs) != cudaSuccess)
+    return static_fail(S2_ECUDA, "copying the status failed");
+  return S2_OK;
+}

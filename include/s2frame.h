@@ -157,9 +157,51 @@ int s2_phase_count(const s2_ctx* ctx, int fast_only);
 
 int s2_frame_free(s2_ctx* ctx);
 
-/* Message of the last failure on this context (or of the last failed s2_frame_init when ctx is
- * NULL); never NULL. */
+/* Message of the last failure on this context (or, when ctx is NULL, of the last failed
+ * s2_frame_init or s2_fast_logits_static); never NULL. */
 const char* s2_last_error(const s2_ctx* ctx);
+
+/* ---------------------------------------------------------------------------------------------
+ * Fast-AR alone without a context or workspace: for callers that cannot allocate device memory.
+ *
+ * The pages describing the method have no counterpart of this call; it is a service of this
+ * library only.  Some callers may not call cudaMalloc: a host application whose own memory pool
+ * has already reserved the device memory (an allocation outside the pool fails or escapes its
+ * accounting), or a latency-critical thread, such as an audio callback, that must not block in
+ * cudaMalloc/cudaFree (they can synchronise the whole device).  Such a caller cannot provide the
+ * workspace s2_frame_init needs.  This call computes what s2_fast_logits computes, with the same
+ * kernel and the same phases, but its scratch (Fast-AR activations, within-frame K/V, RoPE table,
+ * control block and phase program: about 0.8 MB at S2-Pro shapes) is a file-scope device array of
+ * S2_STATIC_SCRATCH_BYTES that belongs to the library: every GPU on which the library's device code
+ * is loaded holds it until the process exits.
+ *
+ *   d, weights, n_weights  the shape and the weight table of s2_frame_init (device pointers, 16-byte
+ *                          aligned); only the Fast-AR part and fast_project_in are read, the other
+ *                          entries may be NULL
+ *   hidden   device [n_frames][dim] fp32; prefix device [n_frames][n_codebooks-1] int32
+ *   logits   device [n_frames][n_codebooks-1][codebook_size] fp32 (output), windows 2..n_codebooks
+ *   status   device int32 [2] or NULL (output): the device-detected result of this call, {S2_OK,
+ *            S2_ETIMEOUT (a wait gave up) or S2_EINVAL (a prefix code outside 0..codebook_size-1),
+ *            site}, written on `stream` after the kernel
+ *
+ * Allocates nothing: it calls no cudaMalloc, cudaFree or other allocating routine (the message of a
+ * failed call is the one exception, on the host).  The caller owns every input and output.
+ * Limits: the shape's scratch must fit S2_STATIC_SCRATCH_BYTES and its program 1024 phases, else
+ * S2_ENOMEM and nothing is launched; n_frames in 1..1048576 (frames run one after another in the
+ * same scratch, so their number does not grow it).
+ * Set-up: the first call on a device (the current one) looks up the array's device address and
+ * configures the kernel on that device; make that first call before any stream capture.
+ * Sharing: all calls on a device use the one array, which keeps the previous call's contents; each
+ * call re-initialises what must start from zero (control block, state, program, RoPE table) before
+ * its kernel.  Calls whose GPU work overlaps (different streams, or host threads without ordering)
+ * race on the array and give undefined results: issue them on one stream or synchronise between them.
+ * The host side of concurrent calls is serialised.
+ * Errors (nothing launched): S2_EINVAL bad shape, pointer, alignment, count or device ordinal (> 63);
+ * S2_ENOMEM above the limits; S2_ECUDA set-up, copy or launch failed.  Message: s2_last_error(NULL). */
+#define S2_STATIC_SCRATCH_BYTES ((size_t)2 << 20)
+int s2_fast_logits_static(const s2_dims* d, const void* const* weights, int n_weights, int n_frames,
+                          const float* hidden, const int32_t* prefix, float* logits, int32_t* status,
+                          struct CUstream_st* stream);
 
 #ifdef __cplusplus
 }
