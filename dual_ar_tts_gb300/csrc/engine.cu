@@ -144,10 +144,10 @@ struct Carver {
   }
 };
 
-// A 2-column bf16 projection stages 2 x 2 x K bf16 activations in shared memory; the Fast-AR
+// A 2-column bf16 projection stages 2 x 2 padded rows of K bf16 activations in shared memory; the Fast-AR
 // down projection of the first call (two positions) is split when that does not fit.
 bool split_fast_down(const Dims& d, int npos) {
-  return npos == 2 && d.wdt == S2_BF16 && 2LL * 2 * 2 * d.Ff > kXsBytes;
+  return npos == 2 && d.wdt == S2_BF16 && 2LL * 2 * (2LL * d.Ff + kTileRowPad) > kXsBytes;
 }
 
 int fast_call_phases(const Dims& d) {
@@ -230,7 +230,7 @@ struct Builder {
       while (nkt <= K / 16 && (K % nkt != 0 || (K / nkt) % 16 != 0)) ++nkt;
       if (nkt > K / 16) err = "no K tiling of a projection fits the pipeline stage";
       p.Kt = K / nkt;
-      if (2LL * 2 * ncols * K > kXsBytes) err = "projection input does not fit the shared activation buffer";
+      if (2LL * ncols * (2LL * K + kTileRowPad) > kXsBytes) err = "projection input does not fit the shared activation buffer";
       if (K * d.esz > kStageBytes) err = "norm vector exceeds one pipeline stage";
     }
     return p;

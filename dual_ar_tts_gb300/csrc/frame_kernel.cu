@@ -660,8 +660,10 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
       }
     }
   }
-  // ---- split into bf16 hi and lo rows: xs[2c][k] = hi, xs[2c+1][k] = lo
+  // ---- split into bf16 hi and lo rows: xs row 2c = hi, row 2c+1 = lo (rows padded by 16 bytes so
+  // the rows of one ldmatrix sit in different banks)
   const uint32_t xsb = smem_u32(S.xs);
+  const uint32_t xpitch = 2u * static_cast<uint32_t>(K) + kTileRowPad;
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
 #pragma unroll
@@ -672,8 +674,8 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
         const float h0 = round_bf16(v.x), h1 = round_bf16(v.y), h2 = round_bf16(v.z), h3 = round_bf16(v.w);
         const uint32_t hi01 = pack_bf16x2(h0, h1), hi23 = pack_bf16x2(h2, h3);
         const uint32_t lo01 = pack_bf16x2(v.x - h0, v.y - h1), lo23 = pack_bf16x2(v.z - h2, v.w - h3);
-        const uint32_t ahi = xsb + 2u * static_cast<uint32_t>((2 * c) * K + 4 * g);
-        const uint32_t alo = xsb + 2u * static_cast<uint32_t>((2 * c + 1) * K + 4 * g);
+        const uint32_t ahi = xsb + static_cast<uint32_t>(2 * c) * xpitch + 8u * static_cast<uint32_t>(g);
+        const uint32_t alo = ahi + xpitch;
         asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(ahi), "r"(hi01), "r"(hi23) : "memory");
         asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(alo), "r"(lo01), "r"(lo23) : "memory");
       }
@@ -681,64 +683,83 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
   }
   named_bar(1, kConsumers);
 
-  // ---- tiles: 8-row blocks, each matrix, each K tile; D accumulates over the K tiles
+  // ---- tiles: 8-row blocks, each matrix, each K tile; D accumulates over the K tiles.
+  // A (activations) and B (weights) both come from shared memory by ldmatrix: per iteration one
+  // x4 load of each covers k steps s and s + 8; four accumulation chains.
   const int nmat = ph.nmat;
-  const int am = lane >> 2;  // A row held by this lane (x column 2c = hi, 2c+1 = lo)
   const bool a_live = lane < 8 * NC;
-  const uint32_t a_row = xsb + 2u * static_cast<uint32_t>(am * K + 2 * (lane & 3));
+  // ldmatrix row addresses for A: matrix row r is activation row r (rows >= 2·NC repeat live rows;
+  // their products land in D rows that are discarded); matrices: k 0-7 / 8-15 of step s, then s + 8
+  const uint32_t a_ld0 = order_after(xsb) + static_cast<uint32_t>((lane & 7) % (2 * NC)) * xpitch +
+                         static_cast<uint32_t>((lane >> 3) & 1) * 16u;
+  const uint32_t a_ld = a_ld0 + static_cast<uint32_t>((lane >> 4) & 1) * 256u;
   const uint32_t red = smem_u32(S.red);
+  // a block of 8 rows has at most kIters iterations per warp; shorter blocks can have longer K
+  // tiles, which the outer loop covers
+  constexpr int kIters = ((kStageBytes / kTileRows - kTileRowPad) / 32 + 2 * kConsumerWarps - 1) / (2 * kConsumerWarps);
   for (int b = 0; b < nr; b += kTileRows) {
     const int rows = min(kTileRows, nr - b);
     const int Kt = tile_kt(K, rows), nkt = K / Kt;
     const uint32_t pitch = static_cast<uint32_t>(Kt) * 2u + kTileRowPad;
     const int nsteps = Kt / 16;
-    // ldmatrix.x4 rows: matrices 0,1 = k step s (k, k+8), matrices 2,3 = k step s + 8; rows past the
-    // block's last one repeat it (their outputs are discarded)
+    // ldmatrix.x4 rows for B: matrices 0,1 = k step s (k, k+8), matrices 2,3 = k step s + 8; rows
+    // past the block's last one repeat it (their outputs are discarded)
     const uint32_t b_off2 = static_cast<uint32_t>(min(lane & 7, rows - 1)) * pitch +
                             static_cast<uint32_t>((lane >> 3) & 1) * 16u;
     const uint32_t b_off = b_off2 + static_cast<uint32_t>((lane >> 4) & 1) * 256u;
     for (int m = 0; m < nmat; ++m) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc2[4] = {0.f, 0.f, 0.f, 0.f}, acc3[4] = {0.f, 0.f, 0.f, 0.f};
       for (int kt = 0; kt < nkt; ++kt) {
         const bool ok = wait_bar(cp, S, &S.full[pipe.stage], pipe.round & 1u, 4, false);
         if (!ok) S.fail = 1;
         if (ok) {
-          const uint32_t tb = smem_u32(S.ring[pipe.stage]);
-          const uint32_t ab = a_row + 2u * static_cast<uint32_t>(kt * Kt);
-          // steps s and s + 8 per iteration: two independent accumulation chains
-          for (int st = warp; st < nsteps; st += 2 * kConsumerWarps) {
-            const bool two = st + kConsumerWarps < nsteps;
-            uint32_t b0, b1, b2, b3;
-            if (two) {
-              ldmatrix_x4(tb + b_off + 32u * st, b0, b1, b2, b3);
-            } else {
-              ldmatrix_x2(tb + b_off2 + 32u * st, b0, b1);
-              b2 = b3 = 0u;
-            }
-            const uint32_t a0 = a_live ? lds32(ab + 32u * st) : 0u;
-            const uint32_t a2 = a_live ? lds32(ab + 32u * st + 16u) : 0u;
-            mma_bf16_16816(acc, a0, 0u, a2, 0u, b0, b1);
-            if (two) {
-              const uint32_t c0 = a_live ? lds32(ab + 32u * (st + kConsumerWarps)) : 0u;
-              const uint32_t c2 = a_live ? lds32(ab + 32u * (st + kConsumerWarps) + 16u) : 0u;
-              mma_bf16_16816(acc2, c0, 0u, c2, 0u, b2, b3);
+          const uint32_t tb = order_after(smem_u32(S.ring[pipe.stage]));
+          const uint32_t ak = 2u * static_cast<uint32_t>(kt * Kt);
+          for (int st0 = warp; st0 < nsteps; st0 += 2 * kConsumerWarps * kIters) {
+#pragma unroll
+            for (int i = 0; i < kIters; ++i) {
+              const int st = st0 + 2 * kConsumerWarps * i;
+              if (st < nsteps) {
+                uint32_t b0, b1, b2 = 0u, b3 = 0u, a0, a2, c0 = 0u, c2 = 0u;
+                const bool two = st + kConsumerWarps < nsteps;
+                if (two) {
+                  ldmatrix_x4(tb + b_off + 32u * st, b0, b1, b2, b3);
+                  ldmatrix_x4(a_ld + ak + 32u * st, a0, a2, c0, c2);
+                } else {
+                  ldmatrix_x2(tb + b_off2 + 32u * st, b0, b1);
+                  ldmatrix_x2(a_ld0 + ak + 32u * st, a0, a2);
+                }
+                if (!a_live) a0 = a2 = c0 = c2 = 0u;
+                if (i & 1) {
+                  mma_bf16_16816(acc2, a0, 0u, a2, 0u, b0, b1);
+                  if (two) mma_bf16_16816(acc3, c0, 0u, c2, 0u, b2, b3);
+                } else {
+                  mma_bf16_16816(acc0, a0, 0u, a2, 0u, b0, b1);
+                  if (two) mma_bf16_16816(acc1, c0, 0u, c2, 0u, b2, b3);
+                }
+              }
             }
           }
         }
+        hold(acc0);
+        hold(acc1);
+        hold(acc2);
+        hold(acc3);
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[pipe.stage]);
         pipe.advance();
       }
-      acc[0] += acc2[0];
-      acc[1] += acc2[1];
+      const float s0 = (acc0[0] + acc1[0]) + (acc2[0] + acc3[0]);
+      const float s1 = (acc0[1] + acc1[1]) + (acc2[1] + acc3[1]);
       // rows 2c (hi) and 2c+1 (lo) of D: lanes 8c..8c+3 and 8c+4..8c+7, columns n = 2(lane&3), +1
-      const float o0 = __shfl_down_sync(0xffffffffu, acc[0], 4);
-      const float o1 = __shfl_down_sync(0xffffffffu, acc[1], 4);
+      const float o0 = __shfl_down_sync(0xffffffffu, s0, 4);
+      const float o1 = __shfl_down_sync(0xffffffffu, s1, 4);
       if (a_live && (lane & 4) == 0) {
         const int c = lane >> 3, n0 = 2 * (lane & 3);
-        if (n0 < rows) sts32f(red + 4u * ((((b + n0) * nmat + m) * NC + c) * kConsumerWarps + warp), acc[0] + o0);
+        if (n0 < rows) sts32f(red + 4u * ((((b + n0) * nmat + m) * NC + c) * kConsumerWarps + warp), s0 + o0);
         if (n0 + 1 < rows)
-          sts32f(red + 4u * ((((b + n0 + 1) * nmat + m) * NC + c) * kConsumerWarps + warp), acc[1] + o1);
+          sts32f(red + 4u * ((((b + n0 + 1) * nmat + m) * NC + c) * kConsumerWarps + warp), s1 + o1);
       }
     }
   }

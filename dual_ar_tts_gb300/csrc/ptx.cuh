@@ -103,24 +103,40 @@ __device__ __forceinline__ uint32_t lds32(uint32_t a) {
   return v;
 }
 
+// The shared-memory matrix loads and the MMA below are plain (non-volatile) asm, so the compiler
+// may schedule them freely within a tile.  Their ordering against the pipeline waits is made
+// explicit instead: the tile's base address passes through order_after() once the wait has
+// returned (every load depends on it), and hold() pins the accumulators before the stage is
+// released (every load has been consumed by then).
+
 // four 8x8 b16 matrices; lane i supplies the row address of row (i % 8) of matrix (i / 8)
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
+  asm("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+      : "r"(addr));
 }
 __device__ __forceinline__ void ldmatrix_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+  asm("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
 }
 
 // D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col)
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// a copy of v that the compiler cannot compute before the preceding volatile asm (e.g. a wait)
+__device__ __forceinline__ uint32_t order_after(uint32_t v) {
+  uint32_t r;
+  asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v));
+  return r;
+}
+// forces the four values to be final before any later volatile asm (e.g. a barrier arrive)
+__device__ __forceinline__ void hold(float (&d)[4]) {
+  asm volatile("" : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3]));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

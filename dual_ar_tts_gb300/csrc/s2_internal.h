@@ -20,11 +20,11 @@ constexpr int kMaxFramesPerCall = 8192;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumers + 32;      // + one producer warp
-constexpr int kStages = 8;                     // weight ring depth
-constexpr int kStageBytes = 20608;             // one tile: 8 row segments of <= 1280 bf16 (+16 B pad each)
+constexpr int kStages = 4;                     // weight ring depth
+constexpr int kStageBytes = 41088;             // one tile: 8 row segments of <= 2560 bf16 (+16 B pad each)
 constexpr int kTileRows = 8;                   // rows per bf16 weight tile (the MMA n dimension)
 constexpr int kTileRowPad = 16;                // bytes added to each tile row (bank-conflict-free ldmatrix)
-constexpr int kXsBytes = 40960;                // shared activations: bf16 hi/lo of 1 column x <= 10240 (2 x <= 5120)
+constexpr int kXsBytes = 40960;                // shared activations: padded bf16 hi/lo rows of 1 column x <= 10232 (2 x <= 5112)
 constexpr int kRedFloats = 2048;               // per-CTA partial sums (GEMV row × K-slice)
 constexpr int kXRegFloats = 80;                // activation slice per lane held in registers
 constexpr int kGemvChunksPerLane = 5;          // 16-byte chunks per lane: K-slices of 1/8 of <= 10240 bf16
