@@ -11,8 +11,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libs2frame.so")
 BUILD = os.path.join(HERE, "_build")
-SOURCES = ["frame_kernel.cu", "prefill.cu", "engine.cu"]
-HEADERS = ["s2_internal.h", "ptx.cuh", os.path.join("..", "..", "include", "s2frame.h")]
+SOURCES = ["fk_bf16_h128.cu", "fk_bf16_h64.cu", "fk_f32_h128.cu", "fk_f32_h64.cu", "frame_launch.cu", "prefill.cu",
+           "engine.cu"]
+HEADERS = ["s2_internal.h", "ptx.cuh", "frame_kernel.cuh", os.path.join("..", "..", "include", "s2frame.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]

@@ -74,6 +74,7 @@ bool to_dims(const s2_dims* s, Dims& d, std::string& why) {
   auto bad = [&](const char* m) { why = m; return false; };
   if (d.wdt != S2_BF16 && d.wdt != S2_F32) return bad("weight_dtype must be S2_BF16 or S2_F32");
   if (d.kvdt != S2_F16 && d.kvdt != S2_F32) return bad("kv_dtype must be S2_F16 or S2_F32");
+  if ((d.wdt == S2_BF16) != (d.kvdt == S2_F16)) return bad("bf16 weights go with an S2_F16 KV cache, fp32 weights with S2_F32");
   const int al = d.wdt == S2_BF16 ? 8 : 4;
   if (d.D <= 0 || d.D % al || d.Df <= 0 || d.Df % al) return bad("dim/fast_dim must be positive multiples of 16 bytes");
   if (d.L < 0 || d.Lf <= 0) return bad("a fast decoder (fast_n_layer > 0) is required");
@@ -89,6 +90,7 @@ bool to_dims(const s2_dims* s, Dims& d, std::string& why) {
   if (d.L > 0) {
     if (d.Hq <= 0 || d.Hkv <= 0 || d.Hq % d.Hkv || d.Hq / d.Hkv > 4 || d.Hkv > 64) return bad("heads: n_head % n_kv_head == 0, ratio <= 4, n_kv_head <= 64");
     if (d.hd != 64 && d.hd != 128) return bad("head_dim must be 64 or 128");
+    if (d.hd != d.hdf) return bad("head_dim and fast_head_dim must be equal");
     if (d.F <= 0 || d.F % al || (d.Hq * d.hd) % al) return bad("ffn / head sizes must be multiples of 16 bytes");
     if (d.sem_hi - d.sem_lo + 1 != d.cbs) return bad("the semantic range must hold codebook_size ids");
     if (d.sem_lo < 0 || d.sem_hi >= d.V || d.im_end < 0 || d.im_end >= d.V) return bad("semantic range / im_end outside the vocabulary");

@@ -17,12 +17,27 @@
 // output, sem_mask, min_tokens_before_end, RAS, clamp) and the Mizuoto "Fish Speech" engine
 // page (fp32 RMSNorm, adjacent-pair RoPE with a bf16 table, top-k 30, argmax(probs / -log u),
 // draw order).
+#pragma once
 #include <cuda_runtime.h>
+
+#include <type_traits>
 
 #include "ptx.cuh"
 #include "s2_internal.h"
 
 namespace s2 {
+// Internal linkage: every kernel instance unit compiles its own copy of the device code.
+namespace {
+
+// Compile-time configuration of one frame kernel: bf16 weights with an fp16 Slow-AR KV cache on
+// the tensor cores, or fp32 weights with an fp32 cache on the CUDA cores; HD = head_dim of both
+// transformers.  Each configuration is its own kernel, so that a kernel holds only the code it runs.
+template <bool BF16, int HD>
+struct Cfg {
+  static constexpr bool bf16 = BF16;
+  static constexpr int hd = HD;
+  using KT = typename std::conditional<BF16, __half, float>::type;
+};
 
 constexpr int kMiscFloats = 64;
 
@@ -35,6 +50,8 @@ struct Smem {
   int flag;
   Phase ph[2];      // consumers: the current phase descriptor and the prefetched next one
   Phase pph[2];     // producer: the same, walked ahead of the consumers
+  alignas(16) CallParams cp;         // the launch's parameters (shared, so that callees taking them by
+                                     // reference do not need a per-thread local copy)
   float red[kRedFloats];             // GEMV partial sums
   float misc[kMiscFloats];           // GEMV sum-of-squares partials
   alignas(16) unsigned char xs[kXsBytes];  // GEMV activations | attention scratch | sampler scratch
@@ -43,11 +60,13 @@ struct Smem {
 
 // misc[] regions
 constexpr int kMiscSS = 0;                 // GEMV sum-of-squares partials [16]
-// xs regions while an attention phase runs (floats)
+// xs regions while a Slow-AR attention phase runs (floats)
 constexpr int kXsQ = 0;                    // q heads of this CTA [4][128]
 constexpr int kXsKV = 512;                 // new k, v [2][128]
-constexpr int kXsWarp = 768;               // warp partials [8][4][130]
-static_assert((kXsWarp + 8 * 4 * 130) * 4 <= kXsBytes, "attention scratch");
+constexpr int kXsSc = 768;                 // scores / probabilities [2 rounds][4][256]
+constexpr int kXsStat = kXsSc + 2048;      // per head: alpha [4], m [4], l [4]; then the splits' (m, l) [4][32][2]
+constexpr int kXsRed = kXsStat + 16 + 4 * kAttnMaxSplits * 2;  // warp partial outputs [8][4][128]
+static_assert((kXsRed + 8 * 4 * 128) * 4 <= kXsBytes, "attention scratch");
 
 struct Pipe {
   int stage;
@@ -155,6 +174,17 @@ __device__ __forceinline__ void unpack16(const uint4& u, float* f, float) {
   f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
 }
 
+// Split of the Slow-AR attention over n slots: ns splits of `chunk` slots per KV head, at most one
+// item per CTA.
+__device__ __forceinline__ void attn_split(int n, int G, int Hkv, int& ns, int& chunk) {
+  ns = max(1, min(min(kAttnMaxSplits, max(1, G / Hkv)), (n + kAttnItemSlots - 1) / kAttnItemSlots));
+  chunk = (n + ns - 1) / ns;
+  ns = (n + chunk - 1) / chunk;
+}
+__device__ __forceinline__ const float* attn_part_ml(const CallParams& cp, int G) {
+  return cp.part + static_cast<size_t>(cp.d.Hkv) * max(1, G / cp.d.Hkv) * 4 * cp.d.hd;
+}
+
 // =========================================================================
 // producer
 // =========================================================================
@@ -182,6 +212,7 @@ __device__ bool producer_acquire(const CallParams& cp, Smem& S, Pipe& pp, uint32
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+template <class C>
 __device__ void producer(const CallParams& cp, Smem& S) {
   const int lane = threadIdx.x & 31;
   constexpr int NQ = static_cast<int>(sizeof(Phase) / 16);
@@ -213,7 +244,7 @@ __device__ void producer(const CallParams& cp, Smem& S) {
             ++issued;
           }
         }
-        if (cp.d.esz == 2) {
+        if constexpr (C::bf16) {
           // bf16: tiles of <= 8 rows x Kt columns, row segments padded by 16 bytes, one lane per row
           for (int b = 0; b < nr && !stop; b += kTileRows) {
             const int rows = min(kTileRows, nr - b);
@@ -554,7 +585,7 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
   if (ph.epi == EPI_ADD && tid < nr * NC) yres = ldcg(ph.y[tid % NC] + r0 + tid / NC);
 
   // ---- activation columns into registers: thread tid holds elements 4·(tid + 256 j) .. +3
-  constexpr int GMAX = 10;  // float4 groups per thread per column (K <= 10240)
+  constexpr int GMAX = 10 / NC;  // float4 groups per thread per column (NC·K <= 10240)
   const int ng = K / 4;
   float4 xv[NC][GMAX];
   float ss[NC];
@@ -786,8 +817,9 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
   }
 }
 
+template <class C>
 __device__ void gemv(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe) {
-  if (cp.d.wdt == S2_BF16) {
+  if constexpr (C::bf16) {
     if (ph.ncols == 1) gemv_mma<1>(cp, ph, S, pipe);
     else gemv_mma<2>(cp, ph, S, pipe);
   } else {
@@ -835,24 +867,51 @@ __device__ __forceinline__ __half f_to_kv<__half>(float x) { return __float2half
 template <>
 __device__ __forceinline__ float f_to_kv<float>(float x) { return x; }
 
+// one 16-byte chunk of a K/V row to fp32
+template <typename KT>
+__device__ __forceinline__ void unpack_kv(const uint4& u, float (&f)[16 / sizeof(KT)]) {
+  if constexpr (sizeof(KT) == 2) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&w[t]));
+      f[2 * t] = f2.x;
+      f[2 * t + 1] = f2.y;
+    }
+  } else {
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
+  }
+}
+
+
 // =========================================================================
-// Slow-AR attention: q/k norm + RoPE, KV store of the new slot, split-K decode attention
-// over slots 0..pos with a last-arriver combine per KV head.
+// Slow-AR attention: q/k norm + RoPE, KV store of the new slot, split-K decode attention over
+// slots 0..pos.  Item = (KV head, split); each writes its unnormalised output with its running
+// max and denominator, and the last split of a KV head to finish combines them.
+// Thread layout: 16-byte chunk c of a K/V row x slot group sg; each thread loads its chunk of
+// SPT slots of a round (K before q is ready, V while the round's softmax runs).
 // =========================================================================
 
 template <typename KT, int HD>
 __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, Smem& S) {
+  constexpr int EPC = 16 / static_cast<int>(sizeof(KT));  // elements per 16-byte chunk
+  constexpr int CPR = HD / EPC;                            // chunks per row: 8, 16 or 32
+  constexpr int NG = kConsumers / CPR;                     // slot groups
+  constexpr int SPT = 8;                                   // slots per thread per round
+  constexpr int RS = NG * SPT;                             // slots per round
   constexpr int DPL = HD / 32;
+  static_assert(RS <= 256, "score buffer");
   const Dims& d = cp.d;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rep = d.Hq / d.Hkv;
   const int pos = ldcgi(&cp.st->pos);
   const int n = pos + 1;
   const int G = gridDim.x;
-  int ns = max(1, min(G / d.Hkv, (n + 31) / 32));
-  ns = max(ns, (n + kAttnMaxChunk - 1) / kAttnMaxChunk);
-  const int chunk = (n + ns - 1) / ns;
-  ns = (n + chunk - 1) / chunk;
+  int ns, chunk;
+  attn_split(n, G, d.Hkv, ns, chunk);
   const int nitems = d.Hkv * ns;
   const float sc_mul = ph.scale;  // 1/sqrt(head_dim)
   const size_t kvh = static_cast<size_t>(cp.kv_slots) * HD;  // elements per KV head
@@ -863,174 +922,192 @@ __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, 
   float* qs = xsf + kXsQ;
   float* knew = xsf + kXsKV;
   float* vnew = xsf + kXsKV + 128;
-  float* wp = xsf + kXsWarp;
+  float* scs = xsf + kXsSc;
+  float* stat = xsf + kXsStat;
+  float* wred = xsf + kXsRed;
+  float* pml = const_cast<float*>(attn_part_ml(cp, G));
+  const int c = tid % CPR, sg = tid / CPR;
 
   for (int item = blockIdx.x; item < nitems; item += G) {
     const int g = item / ns, s = item % ns;
     const int j0 = s * chunk, j1 = min(n, j0 + chunk);
     const bool has_new = (j1 == n);
-    if (warp < rep) {
-      const int h = g * rep + warp;
-      float v[DPL];
+    const KT* Kg = Kc + g * kvh + c * EPC;
+    const KT* Vg = Vc + g * kvh + c * EPC;
+    float acc[4][EPC], qv[4][EPC];
 #pragma unroll
-      for (int j = 0; j < DPL; ++j) v[j] = ldcg(ph.qkv + h * HD + lane * DPL + j);
-      head_norm_rope<DPL>(v, ph.qn, d.esz, d.eps, HD, d.qk_norm != 0, rope_row);
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int j = 0; j < DPL; ++j) qs[warp * HD + lane * DPL + j] = v[j];
-    } else if (warp == rep && has_new) {
-      float k[DPL], v[DPL];
+      for (int e = 0; e < EPC; ++e) acc[r][e] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;  // warps r < rep, all lanes
+    int buf = 0;
+    for (int b0 = j0; b0 < j1; b0 += RS, buf ^= 1) {
+      // ---- this round's K chunks (the new slot comes from shared memory instead)
+      uint4 kr[SPT], vr[SPT];
 #pragma unroll
-      for (int j = 0; j < DPL; ++j) {
-        k[j] = ldcg(ph.qkv + (d.Hq + g) * HD + lane * DPL + j);
-        v[j] = ldcg(ph.qkv + (d.Hq + d.Hkv + g) * HD + lane * DPL + j);
+      for (int i = 0; i < SPT; ++i) {
+        const int slot = b0 + sg + NG * i;
+        kr[i] = (slot < j1 && slot != pos) ? ldcg_u4(Kg + static_cast<size_t>(slot) * HD) : make_uint4(0u, 0u, 0u, 0u);
       }
-      head_norm_rope<DPL>(k, ph.kn, d.esz, d.eps, HD, d.qk_norm != 0, rope_row);
-      KT* kd = const_cast<KT*>(Kc) + g * kvh + static_cast<size_t>(pos) * HD + lane * DPL;
-      KT* vd = const_cast<KT*>(Vc) + g * kvh + static_cast<size_t>(pos) * HD + lane * DPL;
+      if (b0 == j0) {
+        // ---- q heads of this KV head; the new slot's k (normed, rotated) and v, stored in the cache
+        if (warp < rep) {
+          const int h = g * rep + warp;
+          float v[DPL];
 #pragma unroll
-      for (int j = 0; j < DPL; ++j) {
-        const KT kq = f_to_kv<KT>(k[j]), vq = f_to_kv<KT>(v[j]);
-        kd[j] = kq;
-        vd[j] = vq;
-        knew[lane * DPL + j] = kv_to_f<KT>(kq);
-        vnew[lane * DPL + j] = kv_to_f<KT>(vq);
-      }
-    }
-    named_bar(1, kConsumers);
-
-    // each warp: a contiguous sub-range of [j0, j1), lane-per-slot scores, online softmax
-    float mr[4], lr[4], acc[4][DPL];
+          for (int j = 0; j < DPL; ++j) v[j] = ldcg(ph.qkv + h * HD + lane * DPL + j);
+          head_norm_rope<DPL>(v, ph.qn, d.esz, d.eps, HD, d.qk_norm != 0, rope_row);
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      mr[r] = -INFINITY;
-      lr[r] = 0.f;
+          for (int j = 0; j < DPL; ++j) qs[warp * HD + lane * DPL + j] = v[j];
+        } else if (warp == rep && has_new) {
+          float k[DPL], v[DPL];
 #pragma unroll
-      for (int j = 0; j < DPL; ++j) acc[r][j] = 0.f;
-    }
-    const int len = j1 - j0;
-    const int per = (len + kConsumerWarps - 1) / kConsumerWarps;
-    const int a0 = j0 + warp * per, a1 = min(j1, a0 + per);
-    for (int b0 = a0; b0 < a1; b0 += 32) {
-      const int j = b0 + lane;
-      const int nvalid = min(32, a1 - b0);
-      const bool valid = lane < nvalid;
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
-      if (valid) {
-        if (j == pos) {
-#pragma unroll 1
-          for (int e = 0; e < HD; ++e) {
-            const float kv = knew[e];
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-              if (r < rep) sc[r] = fmaf(qs[r * HD + e], kv, sc[r]);
+          for (int j = 0; j < DPL; ++j) {
+            k[j] = ldcg(ph.qkv + (d.Hq + g) * HD + lane * DPL + j);
+            v[j] = ldcg(ph.qkv + (d.Hq + d.Hkv + g) * HD + lane * DPL + j);
           }
-        } else {
-          const KT* kr = Kc + g * kvh + static_cast<size_t>(j) * HD;
-          constexpr int EPV = 16 / sizeof(KT);
-#pragma unroll 4
-          for (int e0 = 0; e0 < HD; e0 += EPV) {
-            const uint4 u = ldcg_u4(kr + e0);
-            float kf[EPV];
-            if constexpr (sizeof(KT) == 2) {
-              const __half2* h2 = reinterpret_cast<const __half2*>(&u);
+          head_norm_rope<DPL>(k, ph.kn, d.esz, d.eps, HD, d.qk_norm != 0, rope_row);
+          KT* kd = const_cast<KT*>(Kc) + g * kvh + static_cast<size_t>(pos) * HD + lane * DPL;
+          KT* vd = const_cast<KT*>(Vc) + g * kvh + static_cast<size_t>(pos) * HD + lane * DPL;
 #pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                const float2 f2 = __half22float2(h2[t]);
-                kf[2 * t] = f2.x;
-                kf[2 * t + 1] = f2.y;
-              }
-            } else {
-              kf[0] = __uint_as_float(u.x); kf[1] = __uint_as_float(u.y);
-              kf[2] = __uint_as_float(u.z); kf[3] = __uint_as_float(u.w);
-            }
-#pragma unroll
-            for (int t = 0; t < EPV; ++t)
-#pragma unroll
-              for (int r = 0; r < 4; ++r)
-                if (r < rep) sc[r] = fmaf(qs[r * HD + e0 + t], kf[t], sc[r]);
+          for (int j = 0; j < DPL; ++j) {
+            const KT kq = f_to_kv<KT>(k[j]), vq = f_to_kv<KT>(v[j]);
+            kd[j] = kq;
+            vd[j] = vq;
+            knew[lane * DPL + j] = kv_to_f<KT>(kq);
+            vnew[lane * DPL + j] = kv_to_f<KT>(vq);
           }
         }
-      }
-      float p[4];
+        named_bar(1, kConsumers);
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        if (r >= rep) continue;
-        const float s_ = valid ? sc[r] * sc_mul : -INFINITY;
-        const float mb = warp_max(s_);
-        const float mnew = fmaxf(mr[r], mb);
-        const float alpha = expf(mr[r] - mnew);
-        p[r] = valid ? expf(s_ - mnew) : 0.f;
-        lr[r] = lr[r] * alpha + warp_sum(p[r]);
+        for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int j2 = 0; j2 < DPL; ++j2) acc[r][j2] *= alpha;
-        mr[r] = mnew;
+          for (int e = 0; e < EPC; ++e) qv[r][e] = r < rep ? qs[r * HD + c * EPC + e] : 0.f;
       }
-      for (int jj = 0; jj < nvalid; ++jj) {
-        const int slot = b0 + jj;
-        float vv[DPL];
+      // ---- scores of this thread's slots: chunk dot products, summed over the row's CPR lanes
+      float* scb = scs + buf * 1024;
+#pragma unroll
+      for (int i = 0; i < SPT; ++i) {
+        const int slot = b0 + sg + NG * i;
+        float kf[EPC];
         if (slot == pos) {
 #pragma unroll
-          for (int j2 = 0; j2 < DPL; ++j2) vv[j2] = vnew[lane * DPL + j2];
+          for (int e = 0; e < EPC; ++e) kf[e] = knew[c * EPC + e];
         } else {
-          const KT* vr = Vc + g * kvh + static_cast<size_t>(slot) * HD + lane * DPL;
-          if constexpr (sizeof(KT) == 2) {
-            if constexpr (DPL == 4) {
-              const uint2 u = ldcg_u2(vr);
-              const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-              const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-              vv[0] = f0.x; vv[1] = f0.y; vv[2] = f1.x; vv[3] = f1.y;
-            } else {
-              const unsigned u = __ldcg(reinterpret_cast<const unsigned*>(vr));
-              const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&u));
-              vv[0] = f0.x; vv[1] = f0.y;
-            }
-          } else {
-#pragma unroll
-            for (int j2 = 0; j2 < DPL; ++j2) vv[j2] = ldcg(reinterpret_cast<const float*>(vr) + j2);
-          }
+          unpack_kv<KT>(kr[i], kf);
         }
+        float dot[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          if (r >= rep) continue;
-          const float pj = __shfl_sync(0xffffffffu, p[r], jj);
+          dot[r] = 0.f;
 #pragma unroll
-          for (int j2 = 0; j2 < DPL; ++j2) acc[r][j2] = fmaf(pj, vv[j2], acc[r][j2]);
+          for (int e = 0; e < EPC; ++e) dot[r] = fmaf(qv[r][e], kf[e], dot[r]);
+        }
+#pragma unroll
+        for (int off = CPR / 2; off >= 1; off >>= 1)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], off);
+        if (c == 0 && slot < j1) {
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+            if (r < rep) scb[r * 256 + sg + NG * i] = dot[r] * sc_mul;
+        }
+      }
+      // ---- V chunks: in flight while the softmax runs
+#pragma unroll
+      for (int i = 0; i < SPT; ++i) {
+        const int slot = b0 + sg + NG * i;
+        vr[i] = (slot < j1 && slot != pos) ? ldcg_u4(Vg + static_cast<size_t>(slot) * HD) : make_uint4(0u, 0u, 0u, 0u);
+      }
+      named_bar(1, kConsumers);
+      // ---- online softmax of the round (warp r: head r)
+      const int L = min(RS, j1 - b0);
+      if (warp < rep) {
+        float* row = scb + warp * 256;
+        float mx = -INFINITY;
+        for (int j = lane; j < L; j += 32) mx = fmaxf(mx, row[j]);
+        mx = warp_max(mx);
+        const float mnew = fmaxf(m_run, mx);
+        const float alpha = expf(m_run - mnew);
+        float sum = 0.f;
+        for (int j = lane; j < L; j += 32) {
+          const float p = expf(row[j] - mnew);
+          row[j] = p;
+          sum += p;
+        }
+        sum = warp_sum(sum);
+        l_run = l_run * alpha + sum;
+        m_run = mnew;
+        if (lane == 0) stat[warp] = alpha;
+      }
+      named_bar(1, kConsumers);
+      // ---- P·V
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float a = r < rep ? stat[r] : 0.f;
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) acc[r][e] *= a;
+      }
+#pragma unroll
+      for (int i = 0; i < SPT; ++i) {
+        const int slot = b0 + sg + NG * i;
+        if (slot < j1) {
+          float vf[EPC];
+          if (slot == pos) {
+#pragma unroll
+            for (int e = 0; e < EPC; ++e) vf[e] = vnew[c * EPC + e];
+          } else {
+            unpack_kv<KT>(vr[i], vf);
+          }
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const float p = r < rep ? scb[r * 256 + sg + NG * i] : 0.f;
+#pragma unroll
+            for (int e = 0; e < EPC; ++e) acc[r][e] = fmaf(p, vf[e], acc[r][e]);
+          }
         }
       }
     }
-    // warp partials -> smem
-    for (int r = 0; r < rep; ++r) {
-      float* o = wp + (warp * 4 + r) * (HD + 2);
+    // ---- sum the slot groups: within the warp by shuffles, then across warps in shared memory
 #pragma unroll
-      for (int j2 = 0; j2 < DPL; ++j2) o[lane * DPL + j2] = acc[r][j2];
-      if (lane == 0) {
-        o[HD] = mr[r];
-        o[HD + 1] = lr[r];
-      }
+    for (int off = CPR; off < 32; off <<= 1)
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) acc[r][e] += __shfl_xor_sync(0xffffffffu, acc[r][e], off);
+    if (lane < CPR) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        if (r < rep)
+#pragma unroll
+          for (int e = 0; e < EPC; ++e) wred[(warp * 4 + r) * HD + c * EPC + e] = acc[r][e];
+    }
+    if (warp < rep && lane == 0) {
+      stat[4 + warp] = m_run;
+      stat[8 + warp] = l_run;
     }
     named_bar(1, kConsumers);
-    // CTA partial of this item -> global
-    float* part = cp.part + static_cast<size_t>(item) * 4 * (HD + 2);
-    for (int idx = threadIdx.x; idx < rep * HD; idx += kConsumers) {
+    for (int idx = tid; idx < rep * HD; idx += kConsumers) {
       const int r = idx / HD, e = idx % HD;
-      float M = -INFINITY;
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, wp[(w * 4 + r) * (HD + 2) + HD]);
-      float o = 0.f, l = 0.f;
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float* src = wp + (w * 4 + r) * (HD + 2);
-        const float sc2 = src[HD] == -INFINITY ? 0.f : expf(src[HD] - M);
-        o += src[e] * sc2;
-        l += src[HD + 1] * sc2;
-      }
-      part[r * (HD + 2) + e] = o;
-      if (e == 0) {
-        part[r * (HD + 2) + HD] = M;
-        part[r * (HD + 2) + HD + 1] = l;
-      }
+      float o = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) o += wred[(w * 4 + r) * HD + e];
+      if (ns == 1) ph.out[(g * rep + r) * HD + e] = o / stat[8 + r];
+      else cp.part[(static_cast<size_t>(item) * 4 + r) * HD + e] = o;
     }
+    if (ns == 1) {
+      named_bar(1, kConsumers);
+      continue;
+    }
+    if (tid < rep) {
+      pml[(static_cast<size_t>(item) * 4 + tid) * 2] = stat[4 + tid];
+      pml[(static_cast<size_t>(item) * 4 + tid) * 2 + 1] = stat[8 + tid];
+    }
+    // ---- the last split of this KV head to arrive combines all of them:
+    //   o = Σ_s e^{m_s - M} o_s / Σ_s e^{m_s - M} l_s
     __threadfence();
     named_bar(1, kConsumers);
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
       __threadfence();
       const unsigned t = atomicAdd(&cp.ctl->tickets[g], 1u);
       S.flag = (t == static_cast<unsigned>(ns - 1)) ? 1 : 0;
@@ -1041,36 +1118,56 @@ __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, 
     }
     named_bar(1, kConsumers);
     if (S.flag) {
-      // last arriver for KV head g: combine the ns partials in split order
-      for (int idx = threadIdx.x; idx < rep * HD; idx += kConsumers) {
-        const int r = idx / HD, e = idx % HD;
-        float M = -INFINITY;
-        for (int s2i = 0; s2i < ns; ++s2i) {
-          const float* pp = cp.part + static_cast<size_t>(g * ns + s2i) * 4 * (HD + 2) + r * (HD + 2);
-          M = fmaxf(M, ldcg(pp + HD));
+      constexpr int NSM = 8;  // splits whose partials are requested before the weights are known
+      float* mls = stat + 16;
+      for (int i = tid; i < rep * ns; i += kConsumers) {
+        const int r = i / ns, s2 = i % ns;
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(pml + (static_cast<size_t>(g * ns + s2) * 4 + r) * 2));
+        mls[2 * i] = ml.x;
+        mls[2 * i + 1] = ml.y;
+      }
+      float ov[2][NSM];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int idx = tid + kConsumers * j, r = idx / HD, e = idx % HD;
+#pragma unroll
+        for (int s2 = 0; s2 < NSM; ++s2)
+          ov[j][s2] = (idx < rep * HD && s2 < ns) ? ldcg(cp.part + (static_cast<size_t>(g * ns + s2) * 4 + r) * HD + e) : 0.f;
+      }
+      named_bar(1, kConsumers);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int idx = tid + kConsumers * j;
+        if (idx < rep * HD) {
+          const int r = idx / HD, e = idx % HD;
+          const float* mr = mls + 2 * r * ns;
+          float M = -INFINITY;
+          for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, mr[2 * s2]);
+          float o = 0.f, l = 0.f;
+#pragma unroll
+          for (int s2 = 0; s2 < NSM; ++s2) {
+            if (s2 < ns) {
+              const float w = expf(mr[2 * s2] - M);
+              o += w * ov[j][s2];
+              l += w * mr[2 * s2 + 1];
+            }
+          }
+          for (int s2 = NSM; s2 < ns; ++s2) {
+            const float w = expf(mr[2 * s2] - M);
+            o += w * ldcg(cp.part + (static_cast<size_t>(g * ns + s2) * 4 + r) * HD + e);
+            l += w * mr[2 * s2 + 1];
+          }
+          ph.out[(g * rep + r) * HD + e] = o / l;
         }
-        float o = 0.f, l = 0.f;
-        for (int s2i = 0; s2i < ns; ++s2i) {
-          const float* pp = cp.part + static_cast<size_t>(g * ns + s2i) * 4 * (HD + 2) + r * (HD + 2);
-          const float w = expf(ldcg(pp + HD) - M);
-          o += ldcg(pp + e) * w;
-          l += ldcg(pp + HD + 1) * w;
-        }
-        ph.out[(g * rep + r) * HD + e] = o / l;
       }
     }
     named_bar(1, kConsumers);
   }
 }
 
+template <class C>
 __device__ void attn_slow(const CallParams& cp, const Phase& ph, Smem& S) {
-  if (cp.d.kvdt == S2_F16) {
-    if (cp.d.hd == 128) attn_slow_t<__half, 128>(cp, ph, S);
-    else attn_slow_t<__half, 64>(cp, ph, S);
-  } else {
-    if (cp.d.hd == 128) attn_slow_t<float, 128>(cp, ph, S);
-    else attn_slow_t<float, 64>(cp, ph, S);
-  }
+  attn_slow_t<typename C::KT, C::hd>(cp, ph, S);
 }
 
 // =========================================================================
@@ -1156,9 +1253,9 @@ __device__ __noinline__ void attn_fast_t(const CallParams& cp, const Phase& ph, 
   }
 }
 
+template <class C>
 __device__ void attn_fast(const CallParams& cp, const Phase& ph, Smem& S) {
-  if (cp.d.hdf == 128) attn_fast_t<128>(cp, ph, S);
-  else attn_fast_t<64>(cp, ph, S);
+  attn_fast_t<C::hd>(cp, ph, S);
 }
 
 // =========================================================================
@@ -1524,6 +1621,7 @@ __device__ void fast_in(const CallParams& cp, int f) {
 // consumers
 // =========================================================================
 
+template <class C>
 __device__ void consumers(const CallParams& cp, Smem& S) {
   Pipe pipe{0, 0};
   unsigned target = 0;
@@ -1550,13 +1648,13 @@ __device__ void consumers(const CallParams& cp, Smem& S) {
       switch (ph.op) {
         case OP_GEMV:
           if (ph.merge_main && cta0) sample_main(cp, S, f);
-          else gemv(cp, ph, S, pipe);
+          else gemv<C>(cp, ph, S, pipe);
           break;
         case OP_ATTN_SLOW:
-          attn_slow(cp, ph, S);
+          attn_slow<C>(cp, ph, S);
           break;
         case OP_ATTN_FAST:
-          attn_fast(cp, ph, S);
+          attn_fast<C>(cp, ph, S);
           break;
         case OP_SAMPLE_FAST:
           if (cta0) sample_fast(cp, S, f, ph.cb);
@@ -1584,9 +1682,14 @@ __device__ void consumers(const CallParams& cp, Smem& S) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) frame_kernel(const CallParams cp) {
+template <class C>
+__global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constant__ CallParams params) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+  static_assert(sizeof(CallParams) % 16 == 0, "parameter copy");
+  for (int i = threadIdx.x; i < static_cast<int>(sizeof(CallParams) / 16); i += kThreads)
+    reinterpret_cast<uint4*>(&S.cp)[i] = reinterpret_cast<const uint4*>(&params)[i];
+  const CallParams& cp = S.cp;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&S.full[s], 1);
@@ -1600,9 +1703,9 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const CallParams cp)
   }
   __syncthreads();
   if (threadIdx.x >= kConsumers) {
-    producer(cp, S);
+    producer<C>(cp, S);
   } else {
-    consumers(cp, S);
+    consumers<C>(cp, S);
     named_bar(1, kConsumers);
     if (threadIdx.x == 0) {
       __threadfence_block();
@@ -1611,30 +1714,5 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const CallParams cp)
   }
 }
 
-// ------------------------------------------------------------------ host side
-
-int frame_kernel_grid(int device, int* grid_out) {
-  const int smem = static_cast<int>(sizeof(Smem));
-  if (cudaFuncSetAttribute(frame_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return S2_ECUDA;
-  int per_sm = 0, sms = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, frame_kernel, kThreads, smem) != cudaSuccess)
-    return S2_ECUDA;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return S2_ECUDA;
-  if (per_sm < 1) return S2_ECUDA;
-  *grid_out = sms;  // one CTA per SM
-  return S2_OK;
-}
-
-int launch_frames(const CallParams& cp, int grid, void* stream) {
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(&cp.ctl->gbar, 0, sizeof(unsigned), s) != cudaSuccess) return S2_ECUDA;
-  void* args[] = {const_cast<CallParams*>(&cp)};
-  const cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(frame_kernel), dim3(grid),
-                                                    dim3(kThreads), args, sizeof(Smem), s);
-  return e == cudaSuccess ? S2_OK : S2_ECUDA;
-}
-
-size_t frame_kernel_smem() { return sizeof(Smem); }
-
+}  // namespace
 }  // namespace s2

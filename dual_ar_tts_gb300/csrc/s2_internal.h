@@ -28,7 +28,9 @@ constexpr int kXsBytes = 40960;                // shared activations: padded bf1
 constexpr int kRedFloats = 2048;               // per-CTA partial sums (GEMV row × K-slice)
 constexpr int kXRegFloats = 80;                // activation slice per lane held in registers
 constexpr int kGemvChunksPerLane = 5;          // 16-byte chunks per lane: K-slices of 1/8 of <= 10240 bf16
-constexpr int kAttnMaxChunk = 2048;            // slots per split-K attention item
+constexpr int kAttnMaxChunk = 2048;            // workspace sizing of the split-K partials
+constexpr int kAttnItemSlots = 128;            // target slots per Slow-AR attention split
+constexpr int kAttnMaxSplits = 32;             // splits per KV head at most
 
 enum Op : int {
   OP_GEMV = 1,       // y = W·normed(x) with epilogue; may carry a main draw on CTA 0
@@ -119,7 +121,7 @@ struct alignas(16) Phase {
   const void* kn;
 };
 
-struct CallParams {
+struct alignas(16) CallParams {
   int n_frames;
   int fast_only;
   int n_phases;
@@ -143,7 +145,7 @@ struct CallParams {
   float temperature, top_p, ras_temperature, ras_top_p;
   int ras_window, min_tokens;
   // scratch
-  float* part;            // split-K partials
+  float* part;            // Slow-AR attention split-K partials: o [items][4][hd], then (m, l) [items][4]
   int32_t* fcode;         // [NCB] Fast-AR codes of the frame
   float* flogits;         // [CBS]
   const float2* rope;     // Slow-AR table [slots][hd/2]

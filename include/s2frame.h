@@ -63,7 +63,8 @@ typedef struct s2_dims {
   int fast_dim, fast_n_layer, fast_n_head, fast_n_kv_head, fast_head_dim, fast_ffn, fast_window,
       has_fast_project_in;
   int weight_dtype;     /* S2_F32 or S2_BF16: every weight tensor has this type */
-  int kv_dtype;         /* S2_F32 or S2_F16: Slow-AR KV cache element type */
+  int kv_dtype;         /* Slow-AR KV cache element type: S2_F16 with bf16 weights, S2_F32 with fp32
+                           weights (the supported pairs); head_dim == fast_head_dim, 64 or 128 */
 } s2_dims;
 
 /* Sampler settings of one stream ([ch.06 §5.3, §6]; Mizuoto "Fish Speech" engine page:
