@@ -1299,8 +1299,9 @@ struct SampScratch {
   int pad[2];
   uint32_t ck[64];
   int cid[64];
-  float cz[64];
   int tie_id[64];
+  float ce[32];   // e^{z_r - z_0} of the sorted candidates
+  float cE[32];   // the draw's exponential variate of rank r
 };
 constexpr int kSampKeys = 1024;  // sampler keys [kSampPer][kConsumers] after the scratch (4-byte units)
 static_assert(sizeof(SampScratch) <= kSampKeys * 4, "sampler scratch");
@@ -1478,36 +1479,45 @@ __device__ __noinline__ int draw(const CallParams& cp, Smem& S, const float* log
         }
       }
     }
-    W.cz[lane] = fval(kq);
+    // rank r = lane: its exponential and variate are computed / fetched in parallel; the sums,
+    // whose rounding depends on the order, run in rank order in lane 0
+    const float z = fval(kq);
+    const float zmax = __shfl_sync(0xffffffffu, z, 0);
+    const float e = lane < kk ? expf(z - zmax) : 0.f;
+    const float ev = lane < kk ? ldcg(E + lane) : 1.f;
+    W.ce[lane] = e;
     W.cid[lane] = iq;
     __syncwarp();
+    float sum = 0.f;
+    if (lane == 0)
+      for (int r = 0; r < kk; ++r) sum += W.ce[r];
+    sum = __shfl_sync(0xffffffffu, sum, 0);
+    const float pi = e / sum;
+    W.ce[lane] = pi;
+    __syncwarp();
+    int kept = 0;
     if (lane == 0) {
-      float pi[kTopK];
-      const float zmax = W.cz[0];
-      float sum = 0.f;
-      for (int r = 0; r < kk; ++r) {
-        pi[r] = expf(W.cz[r] - zmax);
-        sum += pi[r];
-      }
-      for (int r = 0; r < kk; ++r) pi[r] = pi[r] / sum;
       float cum = 0.f;
-      int kept = 0;
       for (int r = 0; r < kk; ++r) {
         if (r == 0 || cum < top_p) kept = r + 1;
         else break;
-        cum += pi[r];
+        cum += W.ce[r];
       }
-      int best = 0;
-      float bq = pi[0] / ldcg(E);
-      for (int r = 1; r < kept; ++r) {
-        const float qv = pi[r] / ldcg(E + r);
-        if (qv > bq) {
-          best = r;
-          bq = qv;
-        }
-      }
-      W.result = W.cid[best];
     }
+    kept = __shfl_sync(0xffffffffu, kept, 0);
+    // winner = argmax_{r < kept} π_r / E_r, ties -> lower rank
+    float q = lane < kept ? pi / ev : -INFINITY;
+    int rq = lane;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float q2 = __shfl_xor_sync(0xffffffffu, q, o);
+      const int r2 = __shfl_xor_sync(0xffffffffu, rq, o);
+      if (q2 > q || (q2 == q && r2 < rq)) {
+        q = q2;
+        rq = r2;
+      }
+    }
+    if (lane == 0) W.result = W.cid[rq];
   }
   named_bar(1, kConsumers);
   const int out = W.result;
