@@ -1284,227 +1284,258 @@ __device__ __forceinline__ float fval(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// warp-aggregated histogram update: lanes with the same bin add once (bin 256 = no update)
-__device__ __forceinline__ void hist_add(int* hist, int bin, int lane) {
-  const unsigned m = __match_any_sync(0xffffffffu, bin);
-  if (bin < 256 && lane == __ffs(m) - 1) atomicAdd(&hist[bin], __popc(m));
+// Sampler scratch (sampling phases never overlap attention / GEMV phases on a CTA).
+constexpr int kSampHist = 4096;  // first-level histogram: the top 12 bits of a key
+struct SampScratch {
+  int nvalid, cut, rem, nA, nB, result, pad[2];
+  int wsum[kConsumerWarps];
+  uint32_t aK[32];  // candidates above the boundary bin (fewer than 30)
+  int aI[32];
+  uint32_t bK[64];  // candidates in the boundary bin
+  int bI[64];
+  uint32_t cK[32];  // the final candidates in rank order
+  int cI[32];
+  int hist[kSampHist];
+  uint32_t keys[kSampPer * kConsumers];  // [k][thread]
+};
+static_assert(sizeof(SampScratch) <= kXsBytes, "sampler scratch");
+
+// bitonic sort of 32 (key, id) pairs across a warp, one per lane: best (larger key, then lower
+// id) first
+__device__ __forceinline__ void warp_sort32(uint32_t& k, int& id) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll 1
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint32_t pk = __shfl_xor_sync(0xffffffffu, k, stride);
+      const int pi = __shfl_xor_sync(0xffffffffu, id, stride);
+      const bool lower = (lane & stride) == 0;
+      const bool asc = (lane & size) == 0;  // "ascending" = best first
+      if ((lower == asc) == better_k(pk, pi, k, id)) {
+        k = pk;
+        id = pi;
+      }
+    }
+  }
 }
 
-// Sampler scratch (sampling phases never overlap attention / GEMV phases on a CTA).
-struct SampScratch {
-  int hist[256];
-  int nvalid;
-  uint32_t prefix;
-  int rem, n_gt, n_eq, result;
-  int pad[2];
-  uint32_t ck[64];
-  int cid[64];
-  int tie_id[64];
-  float ce[32];   // e^{z_r - z_0} of the sorted candidates
-  float cE[32];   // the draw's exponential variate of rank r
-};
-constexpr int kSampKeys = 1024;  // sampler keys [kSampPer][kConsumers] after the scratch (4-byte units)
-static_assert(sizeof(SampScratch) <= kSampKeys * 4, "sampler scratch");
-static_assert((kSampKeys + 17 * kConsumers) * 4 <= kXsBytes, "sampler keys");
-
-// One draw: the top-30 candidates by (value desc, id asc) are found with a 4-pass 8-bit radix
-// select of the 30th largest key, gathered, sorted by one warp; then, in one thread and in rank
-// order exactly as the method states: softmax over the 30, keep rank r iff r == 0 or
-// Σ_{s<r} π_s < top_p, winner = argmax π_r / E_r (ties -> lower rank).
-// Returns the drawn id in every consumer thread; -1 if nothing is drawable.
-// Keys live in shared memory (kSampPer per thread, [k][thread]) so that the loops stay compact.
+// One draw: the top-30 candidates by (value desc, id asc), then, in rank order exactly as the
+// method states: softmax over them, keep rank r iff r == 0 or Σ_{s<r} π_s < top_p, winner =
+// argmax π_r / E_r (ties -> lower rank).  Returns the drawn id in every consumer thread; -1 if
+// nothing is drawable.
+// Selection: order-preserving 32-bit keys of z = logit / T (kSampPer per thread, in shared
+// memory so that the loops stay compact).  A 4096-bin histogram of the top 12 bits locates the
+// bin holding the 30th key; while that bin holds more than 64 keys it is refined by the next 10
+// bits (at most twice).  Keys above the boundary and the boundary bin's keys are then sorted by
+// two warps.
 __device__ __noinline__ int draw(const CallParams& cp, Smem& S, const float* logits, int n, bool main, bool mask_end,
                                  float temperature, float top_p, const float* E) {
   const Dims& d = cp.d;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   SampScratch& W = *reinterpret_cast<SampScratch*>(S.xs);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(S.xs) + kSampKeys;
+  // the rank-r variate, needed at the end, is requested first
+  const float ev = (warp == 0 && lane < kTopK) ? ldcg(E + lane) : 1.f;
   int nv = 0;
+#pragma unroll 1
   for (int k = 0; k < kSampPer; ++k) {
     const int i = tid + k * kConsumers;
     uint32_t key = 0u;
     if (i < n) {
-      const int id = entry_id(d, main, i);
       const float l = ldcg(logits + i);
-      if (!(mask_end && main && id == d.im_end) && isfinite(l)) {
+      if (!(mask_end && main && entry_id(d, main, i) == d.im_end) && isfinite(l)) {
         key = fkey(l / temperature);
         ++nv;
       }
     }
-    keys[k * kConsumers + tid] = key;
+    W.keys[k * kConsumers + tid] = key;
   }
-  W.hist[tid] = 0;
+#pragma unroll 1
+  for (int b = tid; b < kSampHist; b += kConsumers) W.hist[b] = 0;
+  nv = warp_sum_i(nv);
+  if (lane == 0) W.wsum[warp] = nv;
   if (tid == 0) {
-    W.nvalid = 0;
-    W.prefix = 0u;
-    W.n_gt = 0;
-    W.n_eq = 0;
+    W.nA = 0;
+    W.nB = 0;
   }
   named_bar(1, kConsumers);
-  if (nv) atomicAdd(&W.nvalid, nv);
-  for (int k = 0; k < kSampPer; ++k) {
-    const uint32_t key = keys[k * kConsumers + tid];
-    hist_add(W.hist, key ? static_cast<int>(key >> 24) : 256, lane);
-  }
-  named_bar(1, kConsumers);
-  const int kk = min(kTopK, W.nvalid);
-  if (kk == 0) {
-    named_bar(1, kConsumers);
-    return -1;
-  }
-  if (tid == 0) W.rem = kk;
-  named_bar(1, kConsumers);
-  // ---- radix select of the kk-th largest key, 8 bits per pass from the top
-  for (int pass = 0; pass < 4; ++pass) {
-    if (warp == 0) {
-      int c[8], sum = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = W.hist[255 - 8 * lane - j];
-        sum += c[j];
-      }
-      int incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const int excl = incl - sum;
-      const int rem = W.rem;
-      const unsigned b = __ballot_sync(0xffffffffu, excl < rem && incl >= rem);
-      if (lane == __ffs(b) - 1) {
-        int cum = excl;
-        for (int j = 0; j < 8; ++j) {
-          if (cum + c[j] >= rem) {
-            W.prefix = (W.prefix << 8) | static_cast<uint32_t>(255 - 8 * lane - j);
-            W.rem = rem - cum;
-            break;
-          }
-          cum += c[j];
-        }
-      }
-    }
-    named_bar(1, kConsumers);
-    if (pass == 3) break;
-    W.hist[tid] = 0;
-    named_bar(1, kConsumers);
-    const uint32_t pre = W.prefix;
-    const int hs = 24 - 8 * pass;  // the prefix covers bits [hs, 32)
+  int nvalid = 0;
+#pragma unroll 1
+  for (int w = 0; w < kConsumerWarps; ++w) nvalid += W.wsum[w];
+  if (nvalid == 0) return -1;  // uniform: every thread saw the same count
+  const int kk = min(kTopK, nvalid);
+
+  // ---- locate the kk-th largest key: prefix `pre` of its top (32 - shift) bits, `need` of the
+  // keys with that prefix belong to the top kk
+  uint32_t pre = 0u;
+  int shift = 32, need = kk, n_eq = 0;
+#pragma unroll 1
+  for (int level = 0; level < 3; ++level) {
+    const int width = level == 0 ? 12 : 10;
+    const uint32_t prev = pre;
+    shift -= width;
+    const uint32_t mask = (1u << width) - 1u;
+#pragma unroll 1
     for (int k = 0; k < kSampPer; ++k) {
-      const uint32_t key = keys[k * kConsumers + tid];
-      hist_add(W.hist, (key && (key >> hs) == pre) ? static_cast<int>((key >> (hs - 8)) & 255u) : 256, lane);
+      const uint32_t key = W.keys[k * kConsumers + tid];
+      if (key && (level == 0 || (key >> (shift + width)) == prev)) atomicAdd(&W.hist[(key >> shift) & mask], 1);
     }
     named_bar(1, kConsumers);
+    // bins from the top: thread t owns bins nb-1-t*per .. nb-per-t*per
+    const int nb = 1 << width, per = nb / kConsumers;
+    int c = 0;
+#pragma unroll 1
+    for (int j = 0; j < per; ++j) c += W.hist[nb - 1 - tid * per - j];
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) W.wsum[warp] = incl;
+    named_bar(1, kConsumers);
+    int before = incl - c;
+#pragma unroll 1
+    for (int w = 0; w < warp; ++w) before += W.wsum[w];
+    if (before < need && before + c >= need) {
+      int cum = before;
+#pragma unroll 1
+      for (int j = 0; j < per; ++j) {
+        const int bin = nb - 1 - tid * per - j;
+        const int h = W.hist[bin];
+        if (cum + h >= need) {
+          W.cut = bin;
+          W.rem = need - cum;
+          break;
+        }
+        cum += h;
+      }
+    }
+    named_bar(1, kConsumers);
+    const int cut = W.cut;
+    need = W.rem;
+    n_eq = W.hist[cut];
+    pre = (prev << width) | static_cast<uint32_t>(cut);
+    if (n_eq <= 64 || level == 2) break;
+    named_bar(1, kConsumers);  // everyone has read the histogram
+#pragma unroll 1
+    for (int b = tid; b < 1024; b += kConsumers) W.hist[b] = 0;
+    named_bar(1, kConsumers);
   }
-  const uint32_t T = W.prefix;
-  const int rem = W.rem;  // how many entries equal to T are among the top kk
-  // ---- gather: all keys above T, and the entries tied at T
+
+  // ---- gather: keys above the boundary prefix (all in the top kk) and keys at it
+#pragma unroll 1
   for (int k = 0; k < kSampPer; ++k) {
-    const uint32_t key = keys[k * kConsumers + tid];
-    if (!key || key < T) continue;
+    const uint32_t key = W.keys[k * kConsumers + tid];
+    if (!key) continue;
+    const uint32_t hi = key >> shift;
+    if (hi < pre) continue;
     const int id = entry_id(d, main, tid + k * kConsumers);
-    if (key > T) {
-      const int slot = atomicAdd(&W.n_gt, 1);
-      W.ck[slot] = key;
-      W.cid[slot] = id;
+    if (hi > pre) {
+      const int slot = atomicAdd(&W.nA, 1);
+      W.aK[slot] = key;
+      W.aI[slot] = id;
     } else {
-      const int slot = atomicAdd(&W.n_eq, 1);
-      if (slot < 64) W.tie_id[slot] = id;
+      const int slot = atomicAdd(&W.nB, 1);
+      if (slot < 64) {
+        W.bK[slot] = key;
+        W.bI[slot] = id;
+      }
     }
   }
   named_bar(1, kConsumers);
-  const int n_gt = W.n_gt;
-  if (W.n_eq <= 64) {
-    // warp 0: the rem lowest ids among the ties (bitonic sort of up to 64 ids, two per lane)
-    if (warp == 0) {
-      int a = lane < W.n_eq ? W.tie_id[lane] : 0x7fffffff;
-      int b = lane + 32 < W.n_eq ? W.tie_id[lane + 32] : 0x7fffffff;
-      for (int size = 2; size <= 64; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-          if (stride == 32) {
-            if (b < a) { const int t = a; a = b; b = t; }
-            continue;
+  const int nA = W.nA;  // == kk - need
+  if (warp == 0) {
+    uint32_t k0 = lane < nA ? W.aK[lane] : 0u;
+    int i0 = lane < nA ? W.aI[lane] : (0x7fffffff - lane);
+    warp_sort32(k0, i0);
+    if (lane < nA) {
+      W.cK[lane] = k0;
+      W.cI[lane] = i0;
+    }
+  } else if (warp == 1 && n_eq <= 64) {
+    // boundary bin: bitonic sort of up to 64 pairs, two per lane (lane, lane + 32)
+    uint32_t ka = lane < n_eq ? W.bK[lane] : 0u, kb = lane + 32 < n_eq ? W.bK[lane + 32] : 0u;
+    int ia = lane < n_eq ? W.bI[lane] : (0x7fffffff - lane), ib = lane + 32 < n_eq ? W.bI[lane + 32] : (0x7fffffdf - lane);
+#pragma unroll 1
+    for (int size = 2; size <= 64; size <<= 1) {
+#pragma unroll 1
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        if (stride == 32) {
+          if (better_k(kb, ib, ka, ia)) {
+            const uint32_t tk = ka; ka = kb; kb = tk;
+            const int ti = ia; ia = ib; ib = ti;
           }
-          const int pa = __shfl_xor_sync(0xffffffffu, a, stride);
-          const int pb = __shfl_xor_sync(0xffffffffu, b, stride);
-          const bool lower = (lane & stride) == 0;
-          const bool asc_a = (lane & size) == 0;
-          const bool asc_b = ((lane + 32) & size) == 0;
-          a = (lower == asc_a) ? min(a, pa) : max(a, pa);
-          b = (lower == asc_b) ? min(b, pb) : max(b, pb);
+          continue;
+        }
+        const uint32_t pka = __shfl_xor_sync(0xffffffffu, ka, stride), pkb = __shfl_xor_sync(0xffffffffu, kb, stride);
+        const int pia = __shfl_xor_sync(0xffffffffu, ia, stride), pib = __shfl_xor_sync(0xffffffffu, ib, stride);
+        const bool lower = (lane & stride) == 0;
+        if ((lower == ((lane & size) == 0)) == better_k(pka, pia, ka, ia)) {
+          ka = pka;
+          ia = pia;
+        }
+        if ((lower == (((lane + 32) & size) == 0)) == better_k(pkb, pib, kb, ib)) {
+          kb = pkb;
+          ib = pib;
         }
       }
-      if (lane < rem) {
-        W.ck[n_gt + lane] = T;
-        W.cid[n_gt + lane] = a;
-      }
     }
-  } else {
-    // many equal values: take the rem lowest tied ids one by one
+    if (lane < need) {
+      W.cK[nA + lane] = ka;
+      W.cI[nA + lane] = ia;
+    }
+    if (lane + 32 < need) {
+      W.cK[nA + lane + 32] = kb;
+      W.cI[nA + lane + 32] = ib;
+    }
+  }
+  if (n_eq > 64) {
+    // more than 64 equal keys at full resolution: the `need` lowest ids among them, one by one
     int last = -1;
-    for (int r = 0; r < rem; ++r) {
+#pragma unroll 1
+    for (int r = 0; r < need; ++r) {
       int best = 0x7fffffff;
+#pragma unroll 1
       for (int k = 0; k < kSampPer; ++k) {
         const int id = entry_id(d, main, tid + k * kConsumers);
-        if (keys[k * kConsumers + tid] == T && id > last && id < best) best = id;
+        const uint32_t key = W.keys[k * kConsumers + tid];
+        if (key && (key >> shift) == pre && id > last && id < best) best = id;
       }
-      for (int o = 16; o > 0; o >>= 1) best = min(best, __shfl_xor_sync(0xffffffffu, best, o));
-      if (lane == 0) W.hist[warp] = best;
+      best = warp_min_i(best);
+      if (lane == 0) W.wsum[warp] = best;
       named_bar(1, kConsumers);
-      int m = W.hist[0];
-      for (int w = 1; w < kConsumerWarps; ++w) m = min(m, W.hist[w]);
+      int m = W.wsum[0];
+#pragma unroll 1
+      for (int w = 1; w < kConsumerWarps; ++w) m = min(m, W.wsum[w]);
       if (tid == 0) {
-        W.ck[n_gt + r] = T;
-        W.cid[n_gt + r] = m;
+        W.cK[nA + r] = pre << shift;
+        W.cI[nA + r] = m;
       }
       last = m;
       named_bar(1, kConsumers);
     }
   }
   named_bar(1, kConsumers);
-  // ---- warp 0: sort the kk candidates by (value desc, id asc), then the draw in rank order
+  // ---- warp 0: the draw over the kk candidates, rank r = lane.  The sums, whose rounding depends
+  // on the order, are taken in rank order (every lane runs the same sequence over shuffled values)
   if (warp == 0) {
-    uint32_t kq = lane < kk ? W.ck[lane] : 0u;
-    int iq = lane < kk ? W.cid[lane] : (0x7fffffff - lane);
-    for (int size = 2; size <= 32; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        const uint32_t pk = __shfl_xor_sync(0xffffffffu, kq, stride);
-        const int pi = __shfl_xor_sync(0xffffffffu, iq, stride);
-        const bool lower = (lane & stride) == 0;
-        const bool asc = (lane & size) == 0;  // "ascending" = best first
-        const bool other_first = better_k(pk, pi, kq, iq);
-        if ((lower == asc) == other_first) {
-          kq = pk;
-          iq = pi;
-        }
-      }
-    }
-    // rank r = lane: its exponential and variate are computed / fetched in parallel; the sums,
-    // whose rounding depends on the order, run in rank order in lane 0
-    const float z = fval(kq);
+    const float z = lane < kk ? fval(W.cK[lane]) : 0.f;
     const float zmax = __shfl_sync(0xffffffffu, z, 0);
     const float e = lane < kk ? expf(z - zmax) : 0.f;
-    const float ev = lane < kk ? ldcg(E + lane) : 1.f;
-    W.ce[lane] = e;
-    W.cid[lane] = iq;
-    __syncwarp();
     float sum = 0.f;
-    if (lane == 0)
-      for (int r = 0; r < kk; ++r) sum += W.ce[r];
-    sum = __shfl_sync(0xffffffffu, sum, 0);
+#pragma unroll 1
+    for (int r = 0; r < kk; ++r) sum += __shfl_sync(0xffffffffu, e, r);
     const float pi = e / sum;
-    W.ce[lane] = pi;
-    __syncwarp();
+    float cum = 0.f;
     int kept = 0;
-    if (lane == 0) {
-      float cum = 0.f;
-      for (int r = 0; r < kk; ++r) {
-        if (r == 0 || cum < top_p) kept = r + 1;
-        else break;
-        cum += W.ce[r];
-      }
+#pragma unroll 1
+    for (int r = 0; r < kk; ++r) {
+      const float pr = __shfl_sync(0xffffffffu, pi, r);
+      if (r == 0 || cum < top_p) kept = r + 1;
+      else break;
+      cum += pr;
     }
-    kept = __shfl_sync(0xffffffffu, kept, 0);
     // winner = argmax_{r < kept} π_r / E_r, ties -> lower rank
     float q = lane < kept ? pi / ev : -INFINITY;
     int rq = lane;
@@ -1517,7 +1548,7 @@ __device__ __noinline__ int draw(const CallParams& cp, Smem& S, const float* log
         rq = r2;
       }
     }
-    if (lane == 0) W.result = W.cid[rq];
+    if (lane == 0) W.result = W.cI[rq];
   }
   named_bar(1, kConsumers);
   const int out = W.result;
