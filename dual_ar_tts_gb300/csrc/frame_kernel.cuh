@@ -1296,7 +1296,7 @@ struct SampScratch {
   uint32_t cK[32];  // the final candidates in rank order
   int cI[32];
   int hist[kSampHist];
-  uint32_t keys[kSampPer * kConsumers];  // [k][thread]
+  alignas(16) uint32_t keys[kSampPer * kConsumers];  // by entry index: the logits, then their keys
 };
 static_assert(sizeof(SampScratch) <= kXsBytes, "sampler scratch");
 
@@ -1304,9 +1304,9 @@ static_assert(sizeof(SampScratch) <= kXsBytes, "sampler scratch");
 // id) first
 __device__ __forceinline__ void warp_sort32(uint32_t& k, int& id) {
   const int lane = threadIdx.x & 31;
-#pragma unroll 1
+#pragma unroll
   for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll 1
+#pragma unroll
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       const uint32_t pk = __shfl_xor_sync(0xffffffffu, k, stride);
       const int pi = __shfl_xor_sync(0xffffffffu, id, stride);
@@ -1334,21 +1334,28 @@ __device__ __noinline__ int draw(const CallParams& cp, Smem& S, const float* log
   const Dims& d = cp.d;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   SampScratch& W = *reinterpret_cast<SampScratch*>(S.xs);
-  // the rank-r variate, needed at the end, is requested first
+  // the rank-r variate, needed at the end, is requested first; the logits come into shared
+  // memory in one batch of 16-byte copies (n4 full chunks, then the remaining entries)
   const float ev = (warp == 0 && lane < kTopK) ? ldcg(E + lane) : 1.f;
+  const int n4 = n / 4;
+#pragma unroll 1
+  for (int c = tid; c < n4; c += kConsumers) cp_async16(&W.keys[4 * c], logits + 4 * c);
+  if (tid < n - 4 * n4) W.keys[4 * n4 + tid] = __float_as_uint(ldcg(logits + 4 * n4 + tid));
+  cp_async_wait_all();
+  named_bar(1, kConsumers);
   int nv = 0;
 #pragma unroll 1
   for (int k = 0; k < kSampPer; ++k) {
     const int i = tid + k * kConsumers;
     uint32_t key = 0u;
     if (i < n) {
-      const float l = ldcg(logits + i);
+      const float l = __uint_as_float(W.keys[i]);
       if (!(mask_end && main && entry_id(d, main, i) == d.im_end) && isfinite(l)) {
         key = fkey(l / temperature);
         ++nv;
       }
     }
-    W.keys[k * kConsumers + tid] = key;
+    W.keys[i] = key;
   }
 #pragma unroll 1
   for (int b = tid; b < kSampHist; b += kConsumers) W.hist[b] = 0;
@@ -1375,7 +1382,7 @@ __device__ __noinline__ int draw(const CallParams& cp, Smem& S, const float* log
     const uint32_t prev = pre;
     shift -= width;
     const uint32_t mask = (1u << width) - 1u;
-#pragma unroll 1
+#pragma unroll
     for (int k = 0; k < kSampPer; ++k) {
       const uint32_t key = W.keys[k * kConsumers + tid];
       if (key && (level == 0 || (key >> (shift + width)) == prev)) atomicAdd(&W.hist[(key >> shift) & mask], 1);
@@ -1384,7 +1391,7 @@ __device__ __noinline__ int draw(const CallParams& cp, Smem& S, const float* log
     // bins from the top: thread t owns bins nb-1-t*per .. nb-per-t*per
     const int nb = 1 << width, per = nb / kConsumers;
     int c = 0;
-#pragma unroll 1
+#pragma unroll 4
     for (int j = 0; j < per; ++j) c += W.hist[nb - 1 - tid * per - j];
     int incl = c;
 #pragma unroll
@@ -1424,7 +1431,7 @@ __device__ __noinline__ int draw(const CallParams& cp, Smem& S, const float* log
   }
 
   // ---- gather: keys above the boundary prefix (all in the top kk) and keys at it
-#pragma unroll 1
+#pragma unroll
   for (int k = 0; k < kSampPer; ++k) {
     const uint32_t key = W.keys[k * kConsumers + tid];
     if (!key) continue;
@@ -1457,9 +1464,9 @@ __device__ __noinline__ int draw(const CallParams& cp, Smem& S, const float* log
     // boundary bin: bitonic sort of up to 64 pairs, two per lane (lane, lane + 32)
     uint32_t ka = lane < n_eq ? W.bK[lane] : 0u, kb = lane + 32 < n_eq ? W.bK[lane + 32] : 0u;
     int ia = lane < n_eq ? W.bI[lane] : (0x7fffffff - lane), ib = lane + 32 < n_eq ? W.bI[lane + 32] : (0x7fffffdf - lane);
-#pragma unroll 1
+#pragma unroll
     for (int size = 2; size <= 64; size <<= 1) {
-#pragma unroll 1
+#pragma unroll
       for (int stride = size >> 1; stride > 0; stride >>= 1) {
         if (stride == 32) {
           if (better_k(kb, ib, ka, ia)) {
@@ -1524,17 +1531,23 @@ __device__ __noinline__ int draw(const CallParams& cp, Smem& S, const float* log
     const float zmax = __shfl_sync(0xffffffffu, z, 0);
     const float e = lane < kk ? expf(z - zmax) : 0.f;
     float sum = 0.f;
-#pragma unroll 1
-    for (int r = 0; r < kk; ++r) sum += __shfl_sync(0xffffffffu, e, r);
+#pragma unroll
+    for (int r = 0; r < kTopK; ++r) {
+      const float er = __shfl_sync(0xffffffffu, e, r);
+      if (r < kk) sum += er;
+    }
     const float pi = e / sum;
     float cum = 0.f;
     int kept = 0;
-#pragma unroll 1
-    for (int r = 0; r < kk; ++r) {
+    bool open = true;
+#pragma unroll
+    for (int r = 0; r < kTopK; ++r) {
       const float pr = __shfl_sync(0xffffffffu, pi, r);
-      if (r == 0 || cum < top_p) kept = r + 1;
-      else break;
-      cum += pr;
+      if (r < kk && open) {
+        if (r == 0 || cum < top_p) kept = r + 1;
+        else open = false;
+        cum += pr;
+      }
     }
     // winner = argmax_{r < kept} π_r / E_r, ties -> lower rank
     float q = lane < kept ? pi / ev : -INFINITY;
