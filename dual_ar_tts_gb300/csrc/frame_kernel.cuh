@@ -1304,9 +1304,9 @@ static_assert(sizeof(SampScratch) <= kXsBytes, "sampler scratch");
 // id) first
 __device__ __forceinline__ void warp_sort32(uint32_t& k, int& id) {
   const int lane = threadIdx.x & 31;
-#pragma unroll
+#pragma unroll 1
   for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
+#pragma unroll 1
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       const uint32_t pk = __shfl_xor_sync(0xffffffffu, k, stride);
       const int pi = __shfl_xor_sync(0xffffffffu, id, stride);
@@ -1382,7 +1382,7 @@ __device__ __noinline__ int draw(const CallParams& cp, Smem& S, const float* log
     const uint32_t prev = pre;
     shift -= width;
     const uint32_t mask = (1u << width) - 1u;
-#pragma unroll
+#pragma unroll 1
     for (int k = 0; k < kSampPer; ++k) {
       const uint32_t key = W.keys[k * kConsumers + tid];
       if (key && (level == 0 || (key >> (shift + width)) == prev)) atomicAdd(&W.hist[(key >> shift) & mask], 1);
@@ -1431,7 +1431,7 @@ __device__ __noinline__ int draw(const CallParams& cp, Smem& S, const float* log
   }
 
   // ---- gather: keys above the boundary prefix (all in the top kk) and keys at it
-#pragma unroll
+#pragma unroll 1
   for (int k = 0; k < kSampPer; ++k) {
     const uint32_t key = W.keys[k * kConsumers + tid];
     if (!key) continue;
@@ -1464,9 +1464,9 @@ __device__ __noinline__ int draw(const CallParams& cp, Smem& S, const float* log
     // boundary bin: bitonic sort of up to 64 pairs, two per lane (lane, lane + 32)
     uint32_t ka = lane < n_eq ? W.bK[lane] : 0u, kb = lane + 32 < n_eq ? W.bK[lane + 32] : 0u;
     int ia = lane < n_eq ? W.bI[lane] : (0x7fffffff - lane), ib = lane + 32 < n_eq ? W.bI[lane + 32] : (0x7fffffdf - lane);
-#pragma unroll
+#pragma unroll 1
     for (int size = 2; size <= 64; size <<= 1) {
-#pragma unroll
+#pragma unroll 1
       for (int stride = size >> 1; stride > 0; stride >>= 1) {
         if (stride == 32) {
           if (better_k(kb, ib, ka, ia)) {
@@ -1616,29 +1616,38 @@ __device__ __noinline__ void sample_main(const CallParams& cp, Smem& S, int f) {
     return;
   }
   int d1 = draw(cp, S, cp.logits, d.A, true, block_end, cp.ras_temperature, cp.ras_top_p, E + kTopK);
-  if (threadIdx.x == 0) {
-    if (cp.dbg_draws) cp.dbg_draws[f * kDraws + 1] = d1;
-    if (cp.forced) d1 = checked_id(cp, cp.forced[f * kDraws + 1], d.V);
-    if (d1 < 0) d1 = d0;
-    const int wl = st->wlen;
-    bool seen = false;
-    for (int i = 0; i < wl; ++i) seen |= (st->window[i] == d0);
+  if (threadIdx.x < 32) {
+    // warp 0: the RAS window is read, tested and shifted by its lanes at once (lane i: entry i)
+    const int lane = threadIdx.x;
+    if (lane == 0) {
+      if (cp.dbg_draws) cp.dbg_draws[f * kDraws + 1] = d1;
+      if (cp.forced) d1 = checked_id(cp, cp.forced[f * kDraws + 1], d.V);
+      if (d1 < 0) d1 = d0;
+    }
+    d1 = __shfl_sync(0xffffffffu, d1, 0);
+    const int wl = ldcgi(&st->wlen);
+    const int wv = lane < wl ? ldcgi(&st->window[lane]) : -1;
+    const bool seen = __any_sync(0xffffffffu, lane < wl && wv == d0);
     const bool trig = seen && d0 >= d.sem_lo && d0 <= d.sem_hi;
     const int tok = trig ? d1 : d0;
-    int code0 = tok - d.sem_lo;
-    code0 = code0 < 0 ? 0 : (code0 > d.cbs - 1 ? d.cbs - 1 : code0);
-    st->vals[0] = tok;
-    st->vals[1] = code0;
-    cp.fcode[0] = code0;
-    cp.stage[static_cast<size_t>(f) * d.ncb + 0] = code0;
     if (wl < cp.ras_window) {
-      st->window[wl] = tok;
-      st->wlen = wl + 1;
+      if (lane == 0) {
+        st->window[wl] = tok;
+        st->wlen = wl + 1;
+      }
     } else {
-      for (int i = 1; i < wl; ++i) st->window[i - 1] = st->window[i];
-      st->window[wl - 1] = tok;
+      if (lane >= 1 && lane < wl) st->window[lane - 1] = wv;
+      if (lane == 0) st->window[wl - 1] = tok;
     }
-    st->frames_done = fd + 1;
+    if (lane == 0) {
+      int code0 = tok - d.sem_lo;
+      code0 = code0 < 0 ? 0 : (code0 > d.cbs - 1 ? d.cbs - 1 : code0);
+      st->vals[0] = tok;
+      st->vals[1] = code0;
+      cp.fcode[0] = code0;
+      cp.stage[static_cast<size_t>(f) * d.ncb + 0] = code0;
+      st->frames_done = fd + 1;
+    }
   }
 }
 
