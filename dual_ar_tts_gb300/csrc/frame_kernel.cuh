@@ -573,6 +573,40 @@ __device__ __noinline__ void gemv_t(const CallParams& cp, const Phase& ph, Smem&
 // warps' partial sums are added in a fixed order.
 // =========================================================================
 
+// The k steps of one tile for a warp, with the step count fixed at compile time so that the loads
+// of later steps are issued ahead of the MMAs of earlier ones: Q iterations over the step pairs
+// (st, st + 8), st = warp + 16 i, then with TAIL one more single step st = warp + 16 Q.
+// (nsteps = 16 Q, or 16 Q + 8 with TAIL.)  Four accumulation chains.
+template <int Q, bool TAIL>
+__device__ __forceinline__ void tile_steps(uint32_t tb, uint32_t b_off, uint32_t b_off2, uint32_t a_ld, uint32_t a_ld0,
+                                           uint32_t ak, int warp, bool a_live, float (&acc0)[4], float (&acc1)[4],
+                                           float (&acc2)[4], float (&acc3)[4]) {
+#pragma unroll
+  for (int i = 0; i < Q; ++i) {
+    const uint32_t st = static_cast<uint32_t>(warp + 2 * kConsumerWarps * i);
+    uint32_t b0, b1, b2, b3, a0, a2, c0, c2;
+    ldmatrix_x4(tb + b_off + 32u * st, b0, b1, b2, b3);
+    ldmatrix_x4(a_ld + ak + 32u * st, a0, a2, c0, c2);
+    if (!a_live) a0 = a2 = c0 = c2 = 0u;
+    if (i & 1) {
+      mma_bf16_16816(acc2, a0, 0u, a2, 0u, b0, b1);
+      mma_bf16_16816(acc3, c0, 0u, c2, 0u, b2, b3);
+    } else {
+      mma_bf16_16816(acc0, a0, 0u, a2, 0u, b0, b1);
+      mma_bf16_16816(acc1, c0, 0u, c2, 0u, b2, b3);
+    }
+  }
+  if constexpr (TAIL) {
+    const uint32_t st = static_cast<uint32_t>(warp + 2 * kConsumerWarps * Q);
+    uint32_t b0, b1, a0, a2;
+    ldmatrix_x2(tb + b_off2 + 32u * st, b0, b1);
+    ldmatrix_x2(a_ld0 + ak + 32u * st, a0, a2);
+    if (!a_live) a0 = a2 = 0u;
+    if (Q & 1) mma_bf16_16816(acc2, a0, 0u, a2, 0u, b0, b1);
+    else mma_bf16_16816(acc0, a0, 0u, a2, 0u, b0, b1);
+  }
+}
+
 template <int NC>
 __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe) {
   const Dims& d = cp.d;
@@ -747,6 +781,14 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
         if (ok) {
           const uint32_t tb = order_after(smem_u32(S.ring[pipe.stage]));
           const uint32_t ak = 2u * static_cast<uint32_t>(kt * Kt);
+          // the K tiles of the S2-Pro projections (2560, 2432, 2048 columns) have fixed step counts
+          if (nsteps == 160) {
+            tile_steps<10, false>(tb, b_off, b_off2, a_ld, a_ld0, ak, warp, a_live, acc0, acc1, acc2, acc3);
+          } else if (nsteps == 152) {
+            tile_steps<9, true>(tb, b_off, b_off2, a_ld, a_ld0, ak, warp, a_live, acc0, acc1, acc2, acc3);
+          } else if (nsteps == 128) {
+            tile_steps<8, false>(tb, b_off, b_off2, a_ld, a_ld0, ak, warp, a_live, acc0, acc1, acc2, acc3);
+          } else
           for (int st0 = warp; st0 < nsteps; st0 += 2 * kConsumerWarps * kIters) {
 #pragma unroll
             for (int i = 0; i < kIters; ++i) {
