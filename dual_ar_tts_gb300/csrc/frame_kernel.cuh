@@ -608,6 +608,11 @@ __device__ __forceinline__ void tile_steps(uint32_t tb, uint32_t b_off, uint32_t
 }
 
 template <int NC>
+__device__ __noinline__ void gemv_tiles(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe, float yres);
+
+// GEMV prologue for activations of at most GM·1024 elements per column: the columns into registers
+// (GM float4 groups per thread), RMSNorm, the bf16 hi/lo split into shared memory; then the tiles.
+template <int NC, int GM>
 __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe) {
   const Dims& d = cp.d;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -619,37 +624,44 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
   if (ph.epi == EPI_ADD && tid < nr * NC) yres = ldcg(ph.y[tid % NC] + r0 + tid / NC);
 
   // ---- activation columns into registers: thread tid holds elements 4·(tid + 256 j) .. +3
-  constexpr int GMAX = 10 / NC;  // float4 groups per thread per column (NC·K <= 10240)
+  static_assert(GM * 4 * kConsumers * NC <= 10240, "activation registers");
   const int ng = K / 4;
-  float4 xv[NC][GMAX];
+  float4 xv[NC][GM];
   float ss[NC];
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
-    ss[c] = 0.f;
     const GemvCol col = ph.col[c];
     const int* vals = static_cast<const int*>(col.p);
-    int tok = 0, code = 0;
-    float msem = 0.f;
-    if (col.src == SRC_EMBED) {
-      tok = ldcgi(vals);
-      msem = (tok >= d.sem_lo && tok <= d.sem_hi) ? 1.f : 0.f;
-    } else if (col.src == SRC_FEROW) {
-      code = ldcgi(vals);
-    }
+    if (col.src == SRC_BUF) {
+      const float* src = static_cast<const float*>(col.p);
 #pragma unroll
-    for (int j = 0; j < GMAX; ++j) {
-      const int g = tid + kConsumers * j;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (g < ng) {
-        const int e = 4 * g;
-        if (col.src == SRC_BUF) {
-          v = ldcg4(static_cast<const float*>(col.p) + e);
-        } else if (col.src == SRC_FEROW) {
-          const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const unsigned char*>(cp.FE) +
-                                                               (static_cast<size_t>(code) * K + e) * 2));
+      for (int j = 0; j < GM; ++j) {
+        const int g = tid + kConsumers * j;
+        xv[c][j] = g < ng ? ldcg4(src + 4 * g) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    } else if (col.src == SRC_FEROW) {
+      const int code = ldcgi(vals);
+      const unsigned char* row = static_cast<const unsigned char*>(cp.FE) + static_cast<size_t>(code) * K * 2;
+#pragma unroll
+      for (int j = 0; j < GM; ++j) {
+        const int g = tid + kConsumers * j;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (g < ng) {
+          const uint2 u = __ldg(reinterpret_cast<const uint2*>(row + static_cast<size_t>(g) * 8));
           v = make_float4(bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y));
-        } else {
-          // x = sem_scale·E[r0] + m·Σ_cb CE[cb·CBS + code_cb]   (ch.02 §3.2)
+        }
+        xv[c][j] = v;
+      }
+    } else {
+      // x = sem_scale·E[r0] + m·Σ_cb CE[cb·CBS + code_cb]   (ch.02 §3.2)
+      const int tok = ldcgi(vals);
+      const float msem = (tok >= d.sem_lo && tok <= d.sem_hi) ? 1.f : 0.f;
+#pragma unroll
+      for (int j = 0; j < GM; ++j) {
+        const int g = tid + kConsumers * j;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (g < ng) {
+          const int e = 4 * g;
           float acc[4] = {0.f, 0.f, 0.f, 0.f};
           for (int cb = 0; cb < d.ncb; ++cb) {
             const size_t row = static_cast<size_t>(cb) * d.cbs + ldcgi(vals + 1 + cb);
@@ -666,8 +678,13 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
           v.z = __fadd_rn(__fmul_rn(d.sem_scale, bf16lo(u.y)), __fmul_rn(msem, acc[2]));
           v.w = __fadd_rn(__fmul_rn(d.sem_scale, bf16hi(u.y)), __fmul_rn(msem, acc[3]));
         }
+        xv[c][j] = v;
       }
-      xv[c][j] = v;
+    }
+    ss[c] = 0.f;
+#pragma unroll
+    for (int j = 0; j < GM; ++j) {
+      const float4 v = xv[c][j];
       ss[c] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
     }
   }
@@ -677,7 +694,7 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
       float* wb = ph.col[c].wb;
       if (wb == nullptr) continue;
 #pragma unroll
-      for (int j = 0; j < GMAX; ++j) {
+      for (int j = 0; j < GM; ++j) {
         const int g = tid + kConsumers * j;
         if (g < ng) *reinterpret_cast<float4*>(wb + 4 * g) = xv[c][j];
       }
@@ -702,7 +719,7 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
       for (int w = 0; w < kConsumerWarps; ++w) tot += S.misc[kMiscSS + w * NC + c];
       const float r = 1.0f / sqrtf(tot / static_cast<float>(K) + d.eps);
 #pragma unroll
-      for (int j = 0; j < GMAX; ++j) {
+      for (int j = 0; j < GM; ++j) {
         const int g = tid + kConsumers * j;
         if (g < ng) {
           const uint32_t w01 = lds32(nws + 8u * g), w23 = lds32(nws + 8u * g + 4u);
@@ -719,7 +736,7 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
     pipe.advance();
     if (blockIdx.x == 0 && ph.hid_out != nullptr) {
 #pragma unroll
-      for (int j = 0; j < GMAX; ++j) {
+      for (int j = 0; j < GM; ++j) {
         const int g = tid + kConsumers * j;
         if (g < ng) *reinterpret_cast<float4*>(ph.hid_out + 4 * g) = xv[0][j];
       }
@@ -732,7 +749,7 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
 #pragma unroll
-    for (int j = 0; j < GMAX; ++j) {
+    for (int j = 0; j < GM; ++j) {
       const int g = tid + kConsumers * j;
       if (g < ng) {
         const float4 v = xv[c][j];
@@ -748,6 +765,17 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
   }
   named_bar(1, kConsumers);
 
+  gemv_tiles<NC>(cp, ph, S, pipe, yres);
+}
+
+template <int NC>
+__device__ __noinline__ void gemv_tiles(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe, float yres) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int K = ph.K;
+  int r0, nr;
+  rows_of(ph, blockIdx.x, gridDim.x, r0, nr);
+  const uint32_t xsb = smem_u32(S.xs);
+  const uint32_t xpitch = 2u * static_cast<uint32_t>(K) + kTileRowPad;
   // ---- tiles: 8-row blocks, each matrix, each K tile; D accumulates over the K tiles.
   // A (activations) and B (weights) both come from shared memory by ldmatrix: per iteration one
   // x4 load of each covers k steps s and s + 8; four accumulation chains.
@@ -862,8 +890,15 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
 template <class C>
 __device__ void gemv(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe) {
   if constexpr (C::bf16) {
-    if (ph.ncols == 1) gemv_mma<1>(cp, ph, S, pipe);
-    else gemv_mma<2>(cp, ph, S, pipe);
+    // the activation length selects how many float4 groups each thread holds (K <= GM·1024)
+    if (ph.ncols == 1) {
+      if (ph.K <= 3072) gemv_mma<1, 3>(cp, ph, S, pipe);
+      else if (ph.K <= 4096) gemv_mma<1, 4>(cp, ph, S, pipe);
+      else gemv_mma<1, 10>(cp, ph, S, pipe);
+    } else {
+      if (ph.K <= 3072) gemv_mma<2, 3>(cp, ph, S, pipe);
+      else gemv_mma<2, 5>(cp, ph, S, pipe);
+    }
   } else {
     if (ph.ncols == 1) gemv_t<float, 1>(cp, ph, S, pipe);
     else gemv_t<float, 2>(cp, ph, S, pipe);
