@@ -60,13 +60,14 @@ struct Smem {
 
 // misc[] regions
 constexpr int kMiscSS = 0;                 // GEMV sum-of-squares partials [16]
-// xs regions while a Slow-AR attention phase runs (floats)
-constexpr int kXsQ = 0;                    // q heads of this CTA [4][128]
-constexpr int kXsKV = 512;                 // new k, v [2][128]
-constexpr int kXsSc = 768;                 // scores / probabilities [2 rounds][4][256]
-constexpr int kXsStat = kXsSc + 2048;      // per head: alpha [4], m [4], l [4]; then the splits' (m, l) [4][32][2]
-constexpr int kXsRed = kXsStat + 16 + 4 * kAttnMaxSplits * 2;  // warp partial outputs [8][4][128]
-static_assert((kXsRed + 8 * 4 * 128) * 4 <= kXsBytes, "attention scratch");
+// xs regions while a Slow-AR attention phase runs: K/V staging [2 rounds][RS slots][head_dim]
+// (8 KB per buffer and operand), then fp32 scratch (float offsets)
+constexpr int kXsStageBytes = 8192;                 // one round of K (or V) rows
+constexpr int kXsQ = 4 * kXsStageBytes / 4;         // q heads of this CTA [4][128]
+constexpr int kXsKV = kXsQ + 512;                   // new k, v [2][128] (fp32, as stored)
+constexpr int kXsSc = kXsKV + 256;                  // scores / probabilities [4][64]
+constexpr int kXsStat = kXsSc + 256;                // per head: alpha [4], m [4], l [4]; splits' (m, l) [4][32][2]
+static_assert((kXsStat + 16 + 4 * kAttnMaxSplits * 2) * 4 <= kXsBytes, "attention scratch");
 
 struct Pipe {
   int stage;
@@ -968,19 +969,21 @@ __device__ __forceinline__ void unpack_kv(const uint4& u, float (&f)[16 / sizeof
 // Slow-AR attention: q/k norm + RoPE, KV store of the new slot, split-K decode attention over
 // slots 0..pos.  Item = (KV head, split); each writes its unnormalised output with its running
 // max and denominator, and the last split of a KV head to finish combines them.
-// Thread layout: 16-byte chunk c of a K/V row x slot group sg; each thread loads its chunk of
-// SPT slots of a round (K before q is ready, V while the round's softmax runs).
+// Rounds of RS slots: the K and V rows of the next round are copied into shared memory
+// (cp.async, double-buffered) while the current one is processed.  Scores: TPS threads per slot,
+// each a 32-byte part of the row; P·V: each thread owns fixed (head, element) outputs.
 // =========================================================================
 
 template <typename KT, int HD>
 __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, Smem& S) {
-  constexpr int EPC = 16 / static_cast<int>(sizeof(KT));  // elements per 16-byte chunk
-  constexpr int CPR = HD / EPC;                            // chunks per row: 8, 16 or 32
-  constexpr int NG = kConsumers / CPR;                     // slot groups
-  constexpr int SPT = 8;                                   // slots per thread per round
-  constexpr int RS = NG * SPT;                             // slots per round
+  constexpr int RB = HD * static_cast<int>(sizeof(KT));  // bytes per K/V row
+  constexpr int RS = kXsStageBytes / RB;                 // slots per round (16, 32 or 64)
+  constexpr int TPS = kConsumers / RS;                   // threads per slot in the scores
+  constexpr int EPS = HD / TPS;                          // elements per thread in the scores
+  constexpr int CPS = RB / 16;                           // 16-byte chunks per row
+  constexpr int OPT = 4 * HD / kConsumers;               // outputs per thread in P·V
   constexpr int DPL = HD / 32;
-  static_assert(RS <= 256, "score buffer");
+  static_assert(RS <= 64 && EPS * static_cast<int>(sizeof(KT)) == 32, "attention round layout");
   const Dims& d = cp.d;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rep = d.Hq / d.Hkv;
@@ -995,182 +998,158 @@ __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, 
   const KT* Kc = static_cast<const KT*>(ph.kc);
   const KT* Vc = static_cast<const KT*>(ph.vc);
   const float2* rope_row = cp.rope + static_cast<size_t>(pos) * (HD / 2);
+  KT* kst = reinterpret_cast<KT*>(S.xs);                        // [2][RS][HD]
+  KT* vst = reinterpret_cast<KT*>(S.xs + 2 * kXsStageBytes);    // [2][RS][HD]
   float* xsf = reinterpret_cast<float*>(S.xs);
   float* qs = xsf + kXsQ;
   float* knew = xsf + kXsKV;
   float* vnew = xsf + kXsKV + 128;
-  float* scs = xsf + kXsSc;
+  float* ps = xsf + kXsSc;
   float* stat = xsf + kXsStat;
-  float* wred = xsf + kXsRed;
   float* pml = const_cast<float*>(attn_part_ml(cp, G));
-  const int c = tid % CPR, sg = tid / CPR;
+  const int ss = tid / TPS, sp = tid % TPS;  // scores: slot, part
+  const int oe = tid % HD, oh = tid / HD;    // P·V: element, first head (then + kConsumers / HD)
 
   for (int item = blockIdx.x; item < nitems; item += G) {
     const int g = item / ns, s = item % ns;
     const int j0 = s * chunk, j1 = min(n, j0 + chunk);
     const bool has_new = (j1 == n);
-    const KT* Kg = Kc + g * kvh + c * EPC;
-    const KT* Vg = Vc + g * kvh + c * EPC;
-    float acc[4][EPC], qv[4][EPC];
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-      for (int e = 0; e < EPC; ++e) acc[r][e] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;  // warps r < rep, all lanes
-    int buf = 0;
-    for (int b0 = j0; b0 < j1; b0 += RS, buf ^= 1) {
-      // ---- this round's K chunks (the new slot comes from shared memory instead)
-      uint4 kr[SPT], vr[SPT];
-#pragma unroll
-      for (int i = 0; i < SPT; ++i) {
-        const int slot = b0 + sg + NG * i;
-        kr[i] = (slot < j1 && slot != pos) ? ldcg_u4(Kg + static_cast<size_t>(slot) * HD) : make_uint4(0u, 0u, 0u, 0u);
-      }
-      if (b0 == j0) {
-        // ---- q heads of this KV head; the new slot's k (normed, rotated) and v, stored in the cache
-        if (warp < rep) {
-          const int h = g * rep + warp;
-          float v[DPL];
-#pragma unroll
-          for (int j = 0; j < DPL; ++j) v[j] = ldcg(ph.qkv + h * HD + lane * DPL + j);
-          head_norm_rope<DPL>(v, ph.qn, d.esz, d.eps, HD, d.qk_norm != 0, rope_row);
-#pragma unroll
-          for (int j = 0; j < DPL; ++j) qs[warp * HD + lane * DPL + j] = v[j];
-        } else if (warp == rep && has_new) {
-          float k[DPL], v[DPL];
-#pragma unroll
-          for (int j = 0; j < DPL; ++j) {
-            k[j] = ldcg(ph.qkv + (d.Hq + g) * HD + lane * DPL + j);
-            v[j] = ldcg(ph.qkv + (d.Hq + d.Hkv + g) * HD + lane * DPL + j);
-          }
-          head_norm_rope<DPL>(k, ph.kn, d.esz, d.eps, HD, d.qk_norm != 0, rope_row);
-          KT* kd = const_cast<KT*>(Kc) + g * kvh + static_cast<size_t>(pos) * HD + lane * DPL;
-          KT* vd = const_cast<KT*>(Vc) + g * kvh + static_cast<size_t>(pos) * HD + lane * DPL;
-#pragma unroll
-          for (int j = 0; j < DPL; ++j) {
-            const KT kq = f_to_kv<KT>(k[j]), vq = f_to_kv<KT>(v[j]);
-            kd[j] = kq;
-            vd[j] = vq;
-            knew[lane * DPL + j] = kv_to_f<KT>(kq);
-            vnew[lane * DPL + j] = kv_to_f<KT>(vq);
-          }
-        }
-        named_bar(1, kConsumers);
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-          for (int e = 0; e < EPC; ++e) qv[r][e] = r < rep ? qs[r * HD + c * EPC + e] : 0.f;
-      }
-      // ---- scores of this thread's slots: chunk dot products, summed over the row's CPR lanes
-      float* scb = scs + buf * 1024;
-#pragma unroll
-      for (int i = 0; i < SPT; ++i) {
-        const int slot = b0 + sg + NG * i;
-        float kf[EPC];
-        if (slot == pos) {
-#pragma unroll
-          for (int e = 0; e < EPC; ++e) kf[e] = knew[c * EPC + e];
-        } else {
-          unpack_kv<KT>(kr[i], kf);
-        }
-        float dot[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          dot[r] = 0.f;
-#pragma unroll
-          for (int e = 0; e < EPC; ++e) dot[r] = fmaf(qv[r][e], kf[e], dot[r]);
-        }
-#pragma unroll
-        for (int off = CPR / 2; off >= 1; off >>= 1)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], off);
-        if (c == 0 && slot < j1) {
-#pragma unroll
-          for (int r = 0; r < 4; ++r)
-            if (r < rep) scb[r * 256 + sg + NG * i] = dot[r] * sc_mul;
+    const int nrounds = (j1 - j0 + RS - 1) / RS;
+    const KT* Kg = Kc + g * kvh;
+    const KT* Vg = Vc + g * kvh;
+    // K and V rows of round r into buffer r & 1 (the new slot is filled from shared memory)
+    auto issue = [&](int r) {
+      const int b0 = j0 + r * RS;
+      for (int i = tid; i < RS * CPS; i += kConsumers) {
+        const int sl = i / CPS, ch = i % CPS, slot = b0 + sl;
+        if (slot < j1 && slot != pos) {
+          const size_t off = static_cast<size_t>(slot) * HD + ch * (16 / sizeof(KT));
+          const size_t so = (static_cast<size_t>(r & 1) * RS + sl) * HD + ch * (16 / sizeof(KT));
+          cp_async16(kst + so, Kg + off);
+          cp_async16(vst + so, Vg + off);
         }
       }
-      // ---- V chunks: in flight while the softmax runs
+      cp_async_commit();
+    };
+    issue(0);
+    // ---- q heads of this KV head; the new slot's k (normed, rotated) and v, stored in the cache
+    if (warp < rep) {
+      const int h = g * rep + warp;
+      float v[DPL];
 #pragma unroll
-      for (int i = 0; i < SPT; ++i) {
-        const int slot = b0 + sg + NG * i;
-        vr[i] = (slot < j1 && slot != pos) ? ldcg_u4(Vg + static_cast<size_t>(slot) * HD) : make_uint4(0u, 0u, 0u, 0u);
+      for (int j = 0; j < DPL; ++j) v[j] = ldcg(ph.qkv + h * HD + lane * DPL + j);
+      head_norm_rope<DPL>(v, ph.qn, d.esz, d.eps, HD, d.qk_norm != 0, rope_row);
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) qs[warp * HD + lane * DPL + j] = v[j];
+    } else if (warp == rep && has_new) {
+      float k[DPL], v[DPL];
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) {
+        k[j] = ldcg(ph.qkv + (d.Hq + g) * HD + lane * DPL + j);
+        v[j] = ldcg(ph.qkv + (d.Hq + d.Hkv + g) * HD + lane * DPL + j);
+      }
+      head_norm_rope<DPL>(k, ph.kn, d.esz, d.eps, HD, d.qk_norm != 0, rope_row);
+      KT* kd = const_cast<KT*>(Kc) + g * kvh + static_cast<size_t>(pos) * HD + lane * DPL;
+      KT* vd = const_cast<KT*>(Vc) + g * kvh + static_cast<size_t>(pos) * HD + lane * DPL;
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) {
+        const KT kq = f_to_kv<KT>(k[j]), vq = f_to_kv<KT>(v[j]);
+        kd[j] = kq;
+        vd[j] = vq;
+        knew[lane * DPL + j] = kv_to_f<KT>(kq);
+        vnew[lane * DPL + j] = kv_to_f<KT>(vq);
+      }
+    }
+    float acc[OPT];
+#pragma unroll
+    for (int j = 0; j < OPT; ++j) acc[j] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;  // warps r < rep
+#pragma unroll 1
+    for (int r = 0; r < nrounds; ++r) {
+      named_bar(1, kConsumers);  // round r - 1 is fully consumed: its buffer may be refilled
+      if (r + 1 < nrounds) {
+        issue(r + 1);
+        cp_async_wait_group<1>();
+      } else {
+        cp_async_wait_group<0>();
+      }
+      const int b0 = j0 + r * RS, L = min(RS, j1 - b0);
+      const int buf = r & 1;
+      if (pos >= b0 && pos < b0 + L && tid < HD) {
+        const size_t so = (static_cast<size_t>(buf) * RS + (pos - b0)) * HD + tid;
+        kst[so] = f_to_kv<KT>(knew[tid]);
+        vst[so] = f_to_kv<KT>(vnew[tid]);
       }
       named_bar(1, kConsumers);
-      // ---- online softmax of the round (warp r: head r)
-      const int L = min(RS, j1 - b0);
-      if (warp < rep) {
-        float* row = scb + warp * 256;
-        float mx = -INFINITY;
-        for (int j = lane; j < L; j += 32) mx = fmaxf(mx, row[j]);
-        mx = warp_max(mx);
-        const float mnew = fmaxf(m_run, mx);
-        const float alpha = expf(m_run - mnew);
-        float sum = 0.f;
-        for (int j = lane; j < L; j += 32) {
-          const float p = expf(row[j] - mnew);
-          row[j] = p;
-          sum += p;
+      // ---- scores: slot ss, elements sp·EPS .. +EPS of each of the rep q heads
+      {
+        float kf[EPS];
+        const uint4* kr = reinterpret_cast<const uint4*>(kst + (static_cast<size_t>(buf) * RS + ss) * HD + sp * EPS);
+        unpack_kv<KT>(kr[0], *reinterpret_cast<float(*)[16 / sizeof(KT)]>(&kf[0]));
+        unpack_kv<KT>(kr[1], *reinterpret_cast<float(*)[16 / sizeof(KT)]>(&kf[16 / sizeof(KT)]));
+        float dot[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          if (h < rep) {
+            const float* q = qs + h * HD + sp * EPS;
+#pragma unroll
+            for (int e = 0; e < EPS; ++e) dot[h] = fmaf(q[e], kf[e], dot[h]);
+          }
         }
-        sum = warp_sum(sum);
-        l_run = l_run * alpha + sum;
+#pragma unroll
+        for (int off = TPS / 2; off >= 1; off >>= 1)
+#pragma unroll
+          for (int h = 0; h < 4; ++h) dot[h] += __shfl_xor_sync(0xffffffffu, dot[h], off);
+        if (sp == 0)
+#pragma unroll
+          for (int h = 0; h < 4; ++h)
+            if (h < rep) ps[h * 64 + ss] = ss < L ? dot[h] * sc_mul : -INFINITY;
+      }
+      named_bar(1, kConsumers);
+      // ---- online softmax of the round (warp h: head h)
+      if (warp < rep) {
+        float* row = ps + warp * 64;
+        const float v0 = lane < RS ? row[lane] : -INFINITY;
+        const float v1 = lane + 32 < RS ? row[lane + 32] : -INFINITY;
+        const float mnew = fmaxf(m_run, warp_max(fmaxf(v0, v1)));
+        const float alpha = expf(m_run - mnew);
+        const float p0 = expf(v0 - mnew), p1 = expf(v1 - mnew);
+        if (lane < RS) row[lane] = p0;
+        if (lane + 32 < RS) row[lane + 32] = p1;
+        l_run = l_run * alpha + warp_sum(p0 + p1);
         m_run = mnew;
         if (lane == 0) stat[warp] = alpha;
       }
       named_bar(1, kConsumers);
-      // ---- P·V
+      // ---- P·V: outputs (head oh + j·(kConsumers / HD), element oe)
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const float a = r < rep ? stat[r] : 0.f;
-#pragma unroll
-        for (int e = 0; e < EPC; ++e) acc[r][e] *= a;
+      for (int j = 0; j < OPT; ++j) {
+        const int h = oh + j * (kConsumers / HD);
+        acc[j] *= h < rep ? stat[h] : 0.f;
       }
+      const KT* vr = vst + static_cast<size_t>(buf) * RS * HD + oe;
+#pragma unroll 4
+      for (int sl = 0; sl < L; ++sl) {
+        const float v = kv_to_f<KT>(vr[static_cast<size_t>(sl) * HD]);
 #pragma unroll
-      for (int i = 0; i < SPT; ++i) {
-        const int slot = b0 + sg + NG * i;
-        if (slot < j1) {
-          float vf[EPC];
-          if (slot == pos) {
-#pragma unroll
-            for (int e = 0; e < EPC; ++e) vf[e] = vnew[c * EPC + e];
-          } else {
-            unpack_kv<KT>(vr[i], vf);
-          }
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const float p = r < rep ? scb[r * 256 + sg + NG * i] : 0.f;
-#pragma unroll
-            for (int e = 0; e < EPC; ++e) acc[r][e] = fmaf(p, vf[e], acc[r][e]);
-          }
+        for (int j = 0; j < OPT; ++j) {
+          const int h = oh + j * (kConsumers / HD);
+          if (h < rep) acc[j] = fmaf(ps[h * 64 + sl], v, acc[j]);
         }
       }
-    }
-    // ---- sum the slot groups: within the warp by shuffles, then across warps in shared memory
-#pragma unroll
-    for (int off = CPR; off < 32; off <<= 1)
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int e = 0; e < EPC; ++e) acc[r][e] += __shfl_xor_sync(0xffffffffu, acc[r][e], off);
-    if (lane < CPR) {
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-        if (r < rep)
-#pragma unroll
-          for (int e = 0; e < EPC; ++e) wred[(warp * 4 + r) * HD + c * EPC + e] = acc[r][e];
     }
     if (warp < rep && lane == 0) {
       stat[4 + warp] = m_run;
       stat[8 + warp] = l_run;
     }
     named_bar(1, kConsumers);
-    for (int idx = tid; idx < rep * HD; idx += kConsumers) {
-      const int r = idx / HD, e = idx % HD;
-      float o = 0.f;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) o += wred[(w * 4 + r) * HD + e];
-      if (ns == 1) ph.out[(g * rep + r) * HD + e] = o / stat[8 + r];
-      else cp.part[(static_cast<size_t>(item) * 4 + r) * HD + e] = o;
+    for (int j = 0; j < OPT; ++j) {
+      const int h = oh + j * (kConsumers / HD);
+      if (h < rep) {
+        if (ns == 1) ph.out[(g * rep + h) * HD + oe] = acc[j] / stat[8 + h];
+        else cp.part[(static_cast<size_t>(item) * 4 + h) * HD + oe] = acc[j];
+      }
     }
     if (ns == 1) {
       named_bar(1, kConsumers);
@@ -1195,47 +1174,30 @@ __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, 
     }
     named_bar(1, kConsumers);
     if (S.flag) {
-      constexpr int NSM = 8;  // splits whose partials are requested before the weights are known
       float* mls = stat + 16;
+#pragma unroll 1
       for (int i = tid; i < rep * ns; i += kConsumers) {
         const int r = i / ns, s2 = i % ns;
         const float2 ml = __ldcg(reinterpret_cast<const float2*>(pml + (static_cast<size_t>(g * ns + s2) * 4 + r) * 2));
         mls[2 * i] = ml.x;
         mls[2 * i + 1] = ml.y;
       }
-      float ov[2][NSM];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int idx = tid + kConsumers * j, r = idx / HD, e = idx % HD;
-#pragma unroll
-        for (int s2 = 0; s2 < NSM; ++s2)
-          ov[j][s2] = (idx < rep * HD && s2 < ns) ? ldcg(cp.part + (static_cast<size_t>(g * ns + s2) * 4 + r) * HD + e) : 0.f;
-      }
       named_bar(1, kConsumers);
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int idx = tid + kConsumers * j;
-        if (idx < rep * HD) {
-          const int r = idx / HD, e = idx % HD;
-          const float* mr = mls + 2 * r * ns;
-          float M = -INFINITY;
-          for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, mr[2 * s2]);
-          float o = 0.f, l = 0.f;
-#pragma unroll
-          for (int s2 = 0; s2 < NSM; ++s2) {
-            if (s2 < ns) {
-              const float w = expf(mr[2 * s2] - M);
-              o += w * ov[j][s2];
-              l += w * mr[2 * s2 + 1];
-            }
-          }
-          for (int s2 = NSM; s2 < ns; ++s2) {
-            const float w = expf(mr[2 * s2] - M);
-            o += w * ldcg(cp.part + (static_cast<size_t>(g * ns + s2) * 4 + r) * HD + e);
-            l += w * mr[2 * s2 + 1];
-          }
-          ph.out[(g * rep + r) * HD + e] = o / l;
+#pragma unroll 1
+      for (int idx = tid; idx < rep * HD; idx += kConsumers) {
+        const int r = idx / HD, e = idx % HD;
+        const float* mr = mls + 2 * r * ns;
+        float M = -INFINITY;
+#pragma unroll 1
+        for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, mr[2 * s2]);
+        float o = 0.f, l = 0.f;
+#pragma unroll 4
+        for (int s2 = 0; s2 < ns; ++s2) {
+          const float w = expf(mr[2 * s2] - M);
+          o += w * ldcg(cp.part + (static_cast<size_t>(g * ns + s2) * 4 + r) * HD + e);
+          l += w * mr[2 * s2 + 1];
         }
+        ph.out[(g * rep + r) * HD + e] = o / l;
       }
     }
     named_bar(1, kConsumers);
