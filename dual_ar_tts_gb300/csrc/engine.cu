@@ -33,6 +33,8 @@ struct s2_ctx {
   int32_t* stage = nullptr;        // [max_streams][kMaxFramesPerCall][NCB]
   float *x = nullptr, *qkv = nullptr, *o = nullptr, *g = nullptr;
   float *fx = nullptr, *fqkv = nullptr, *fo = nullptr, *fg = nullptr, *fk = nullptr, *fv = nullptr;
+  // bf16 hi / lo rows of projection inputs (bf16 models): attention outputs and SwiGLU outputs
+  uint16_t *op = nullptr, *gp = nullptr, *fop = nullptr, *fgp = nullptr;
   float *flogits = nullptr, *part = nullptr, *pscratch = nullptr;
   int32_t* fcode = nullptr;
   float* hidden_src = nullptr;     // builder: hidden buffer feeding Fast-AR position 0
@@ -186,6 +188,10 @@ void carve(s2_ctx* c, Carver& cv) {
   c->fqkv = cv.take<float>(2 * static_cast<size_t>(QKVf));
   c->fo = cv.take<float>(2 * static_cast<size_t>(d.Hqf) * d.hdf);
   c->fg = cv.take<float>(2 * static_cast<size_t>(d.Ff));
+  c->op = cv.take<uint16_t>(2 * static_cast<size_t>(std::max(d.Hq * d.hd, 1)));
+  c->gp = cv.take<uint16_t>(2 * static_cast<size_t>(std::max(d.F, 1)));
+  c->fop = cv.take<uint16_t>(4 * static_cast<size_t>(d.Hqf) * d.hdf);
+  c->fgp = cv.take<uint16_t>(4 * static_cast<size_t>(d.Ff));
   c->fk = cv.take<float>(static_cast<size_t>(d.Lf) * d.Wf * d.Hkvf * d.hdf);
   c->fv = cv.take<float>(static_cast<size_t>(d.Lf) * d.Wf * d.Hkvf * d.hdf);
   c->flogits = cv.take<float>(d.cbs);
@@ -239,6 +245,7 @@ struct Builder {
   }
   void push(Phase p) {
     const int g2 = c->grid - p.cta0;
+    if (p.op == OP_GEMV && p.col[0].src == SRC_PLANES && p.normw != nullptr) err = "internal: normalised planes input";
     if (p.op == OP_GEMV) {
       const int rows = (p.M + g2 - 1) / g2;
       if (static_cast<long long>(rows) * p.nmat * p.ncols * kConsumerWarps > kRedFloats)
@@ -248,6 +255,9 @@ struct Builder {
     out->push_back(p);
   }
   static GemvCol buf(const float* p, float* wb = nullptr) { return GemvCol{SRC_BUF, 0, p, wb}; }
+  static GemvCol planes(const uint16_t* p) { return GemvCol{SRC_PLANES, 0, p, nullptr}; }
+  // bf16 models pass attention and SwiGLU outputs to the next projection as hi / lo planes
+  bool use_planes() const { return c->d.wdt == S2_BF16; }
   bool split_down(int npos) const { return split_fast_down(c->d, npos); }
 
   // Fast-AR calls 1..NCB-1 (fast_only: without draws' side effects on the stream state)
@@ -277,6 +287,7 @@ struct Builder {
         a.pos0 = pos0;
         a.qkv = c->fqkv;
         a.out = c->fo;
+        if (use_planes()) a.outp = c->fop;
         a.kc = c->fk + l * kvl;
         a.vc = c->fv + l * kvl;
         a.qn = w.qn;
@@ -285,28 +296,32 @@ struct Builder {
         push(a);
         Phase o = gemv(d.Df, d.Hqf * d.hdf, npos, w.wo, nullptr, nullptr, EPI_ADD);
         for (int j = 0; j < npos; ++j) {
-          o.col[j] = buf(c->fo + static_cast<size_t>(j) * d.Hqf * d.hdf);
+          o.col[j] = use_planes() ? planes(c->fop + static_cast<size_t>(j) * 2 * d.Hqf * d.hdf)
+                                  : buf(c->fo + static_cast<size_t>(j) * d.Hqf * d.hdf);
           o.y[j] = c->fx + static_cast<size_t>(pos0 + j) * d.Df;
         }
         push(o);
         Phase u = gemv(d.Ff, d.Df, npos, w.w1, w.w3, w.fn, EPI_SWIGLU);
         for (int j = 0; j < npos; ++j) {
           u.col[j] = buf(c->fx + static_cast<size_t>(pos0 + j) * d.Df);
-          u.y[j] = c->fg + static_cast<size_t>(j) * d.Ff;
+          if (use_planes()) u.yp[j] = c->fgp + static_cast<size_t>(j) * 2 * d.Ff;
+          else u.y[j] = c->fg + static_cast<size_t>(j) * d.Ff;
         }
         push(u);
         if (split_down(npos)) {
           // two positions whose activations exceed the shared buffer: one phase per position
           for (int j = 0; j < npos; ++j) {
             Phase dn = gemv(d.Df, d.Ff, 1, w.w2, nullptr, nullptr, EPI_ADD);
-            dn.col[0] = buf(c->fg + static_cast<size_t>(j) * d.Ff);
+            dn.col[0] = use_planes() ? planes(c->fgp + static_cast<size_t>(j) * 2 * d.Ff)
+                                     : buf(c->fg + static_cast<size_t>(j) * d.Ff);
             dn.y[0] = c->fx + static_cast<size_t>(pos0 + j) * d.Df;
             push(dn);
           }
         } else {
           Phase dn = gemv(d.Df, d.Ff, npos, w.w2, nullptr, nullptr, EPI_ADD);
           for (int j = 0; j < npos; ++j) {
-            dn.col[j] = buf(c->fg + static_cast<size_t>(j) * d.Ff);
+            dn.col[j] = use_planes() ? planes(c->fgp + static_cast<size_t>(j) * 2 * d.Ff)
+                                     : buf(c->fg + static_cast<size_t>(j) * d.Ff);
             dn.y[j] = c->fx + static_cast<size_t>(pos0 + j) * d.Df;
           }
           push(dn);
@@ -408,6 +423,7 @@ int build_programs(s2_ctx* c) {
       a.layer = l;
       a.qkv = c->qkv;
       a.out = c->o;
+      if (b.use_planes()) a.outp = c->op;
       a.kc = c->kc + l * kvl + kvs;
       a.vc = c->vc + l * kvl + kvs;
       a.qn = w.qn;
@@ -415,15 +431,16 @@ int build_programs(s2_ctx* c) {
       a.scale = scale;
       b.push(a);
       Phase o = b.gemv(d.D, d.Hq * d.hd, 1, w.wo, nullptr, nullptr, EPI_ADD);
-      o.col[0] = Builder::buf(c->o);
+      o.col[0] = b.use_planes() ? Builder::planes(c->op) : Builder::buf(c->o);
       o.y[0] = c->x;
       b.push(o);
       Phase u = b.gemv(d.F, d.D, 1, w.w1, w.w3, w.fn, EPI_SWIGLU);
       u.col[0] = Builder::buf(c->x);
-      u.y[0] = c->g;
+      if (b.use_planes()) u.yp[0] = c->gp;
+      else u.y[0] = c->g;
       b.push(u);
       Phase dn = b.gemv(d.D, d.F, 1, w.w2, nullptr, nullptr, EPI_ADD);
-      dn.col[0] = Builder::buf(c->g);
+      dn.col[0] = b.use_planes() ? Builder::planes(c->gp) : Builder::buf(c->g);
       dn.y[0] = c->x;
       b.push(dn);
     }
@@ -777,6 +794,7 @@ struct StaticFastLayout {
   float2* rope_f;
   StreamState* st;
   float *hidden, *fx, *fqkv, *fo, *fg, *fk, *fv, *flogits;
+  uint16_t *fop, *fgp;
   int32_t* fcode;
   Phase* prog;
 };
@@ -796,6 +814,8 @@ size_t carve_static_fast(const Dims& d, int n_phases, unsigned char* base, Stati
   s.fk = cv.take<float>(static_cast<size_t>(d.Lf) * d.Wf * d.Hkvf * d.hdf);
   s.fv = cv.take<float>(static_cast<size_t>(d.Lf) * d.Wf * d.Hkvf * d.hdf);
   s.flogits = cv.take<float>(d.cbs);
+  s.fop = cv.take<uint16_t>(4 * static_cast<size_t>(d.Hqf) * d.hdf);
+  s.fgp = cv.take<uint16_t>(4 * static_cast<size_t>(d.Ff));
   s.fcode = cv.take<int32_t>(16);
   s.prog = cv.take<Phase>(static_cast<size_t>(n_phases));
   return align_up(cv.off, 256);
@@ -859,6 +879,7 @@ int build_static_fast_program(const Dims& d, int grid, const void* const* wt, co
       a.pos0 = pos0;
       a.qkv = s.fqkv;
       a.out = s.fo;
+      if (b.use_planes()) a.outp = s.fop;
       a.kc = s.fk + l * kvl;
       a.vc = s.fv + l * kvl;
       a.qn = fw(l, 2);
@@ -867,14 +888,16 @@ int build_static_fast_program(const Dims& d, int grid, const void* const* wt, co
       push(a);
       Phase o = b.gemv(d.Df, d.Hqf * d.hdf, npos, fw(l, 4), nullptr, nullptr, EPI_ADD);
       for (int j = 0; j < npos; ++j) {
-        o.col[j] = Builder::buf(s.fo + static_cast<size_t>(j) * d.Hqf * d.hdf);
+        o.col[j] = b.use_planes() ? Builder::planes(s.fop + static_cast<size_t>(j) * 2 * d.Hqf * d.hdf)
+                                  : Builder::buf(s.fo + static_cast<size_t>(j) * d.Hqf * d.hdf);
         o.y[j] = s.fx + static_cast<size_t>(pos0 + j) * d.Df;
       }
       push(o);
       Phase u = b.gemv(d.Ff, d.Df, npos, fw(l, 6), fw(l, 7), fw(l, 5), EPI_SWIGLU);
       for (int j = 0; j < npos; ++j) {
         u.col[j] = Builder::buf(s.fx + static_cast<size_t>(pos0 + j) * d.Df);
-        u.y[j] = s.fg + static_cast<size_t>(j) * d.Ff;
+        if (b.use_planes()) u.yp[j] = s.fgp + static_cast<size_t>(j) * 2 * d.Ff;
+        else u.y[j] = s.fg + static_cast<size_t>(j) * d.Ff;
       }
       push(u);
       const int ndown = split_fast_down(d, npos) ? npos : 1;  // one phase per position when split
@@ -883,7 +906,8 @@ int build_static_fast_program(const Dims& d, int grid, const void* const* wt, co
         Phase dn = b.gemv(d.Df, d.Ff, nc, fw(l, 8), nullptr, nullptr, EPI_ADD);
         for (int j = 0; j < nc; ++j) {
           const int jj = ndown == 1 ? j : t;
-          dn.col[j] = Builder::buf(s.fg + static_cast<size_t>(jj) * d.Ff);
+          dn.col[j] = b.use_planes() ? Builder::planes(s.fgp + static_cast<size_t>(jj) * 2 * d.Ff)
+                                     : Builder::buf(s.fg + static_cast<size_t>(jj) * d.Ff);
           dn.y[j] = s.fx + static_cast<size_t>(pos0 + jj) * d.Df;
         }
         push(dn);

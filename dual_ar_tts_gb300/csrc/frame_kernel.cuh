@@ -44,6 +44,7 @@ constexpr int kMiscFloats = 64;
 struct Smem {
   uint64_t full[kStages];
   uint64_t empty[kStages];
+  uint64_t xsbar;   // bulk copies of a GEMV's activation planes into xs
   int abort_flag;   // consumers -> producer: stop streaming
   int fail;         // a consumer wait gave up: leave at the next phase boundary
   int sync_ok;
@@ -72,6 +73,7 @@ static_assert((kXsStat + 16 + 4 * kAttnMaxSplits * 2) * 4 <= kXsBytes, "attentio
 struct Pipe {
   int stage;
   uint32_t round;
+  uint32_t xs_uses;  // completed uses of the xs barrier (its phase parity)
   __device__ void advance() {
     if (++stage == kStages) {
       stage = 0;
@@ -175,6 +177,14 @@ __device__ __forceinline__ void unpack16(const uint4& u, float* f, float) {
   f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
 }
 
+// v as bf16 hi (row 0, index i) and lo (row 1 at offset n): hi + lo = v to ~2^-17 relative
+__device__ __forceinline__ void store_planes(uint16_t* planes, int n, int i, float v) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+  planes[i] = __bfloat16_as_ushort(hi);
+  planes[n + i] = __bfloat16_as_ushort(lo);
+}
+
 // Split of the Slow-AR attention over n slots: ns splits of `chunk` slots per KV head, at most one
 // item per CTA.
 __device__ __forceinline__ void attn_split(int n, int G, int Hkv, int& ns, int& chunk) {
@@ -218,7 +228,7 @@ __device__ void producer(const CallParams& cp, Smem& S) {
   const int lane = threadIdx.x & 31;
   constexpr int NQ = static_cast<int>(sizeof(Phase) / 16);
   const uint64_t pol = policy_evict_first();
-  Pipe pp{0, 0};
+  Pipe pp{0, 0, 0};
   unsigned long long issued = 0;  // stages filled so far (all lanes keep the same count)
   int stop = (ld_volatile_int(&cp.st->done) != 0 && !cp.fast_only) ? 1 : 0;
   if (lane < NQ) reinterpret_cast<uint4*>(&S.pph[0])[lane] = __ldg(reinterpret_cast<const uint4*>(cp.prog) + lane);
@@ -876,21 +886,58 @@ __device__ __noinline__ void gemv_tiles(const CallParams& cp, const Phase& ph, S
       for (int w = 0; w < kConsumerWarps; ++w) a += S.red[((rl * nmat + 0) * NC + c) * kConsumerWarps + w];
       if (nmat == 2)
         for (int w = 0; w < kConsumerWarps; ++w) bb += S.red[((rl * nmat + 1) * NC + c) * kConsumerWarps + w];
-      float* y = ph.y[c] + r0 + rl;
+      float v;
       if (ph.epi == EPI_STORE) {
-        *y = a;
+        v = a;
       } else if (ph.epi == EPI_ADD) {
-        *y = (idx == tid ? yres : ldcg(y)) + a;
+        v = (idx == tid ? yres : ldcg(ph.y[c] + r0 + rl)) + a;
       } else {
-        *y = (a / (1.0f + expf(-a))) * bb;
+        v = (a / (1.0f + expf(-a))) * bb;
       }
+      if (ph.y[c] != nullptr) ph.y[c][r0 + rl] = v;
+      if (ph.yp[c] != nullptr) store_planes(ph.yp[c], ph.M, r0 + rl, v);
     }
   }
+}
+
+// The activation comes as bf16 hi / lo rows written by the producing phase: one bulk copy per row
+// into xs, then the tiles (no normalisation on this path).
+template <int NC>
+__device__ __noinline__ void gemv_planes(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe) {
+  const int tid = threadIdx.x;
+  const int K = ph.K;
+  int r0, nr;
+  rows_of(ph, blockIdx.x, gridDim.x, r0, nr);
+  float yres = 0.f;
+  if (ph.epi == EPI_ADD && tid < nr * NC) yres = ldcg(ph.y[tid % NC] + r0 + tid / NC);
+  const uint32_t xpitch = 2u * static_cast<uint32_t>(K) + kTileRowPad;
+  if (tid == 0) {
+    // the previous users of xs (generic-proxy accesses, ordered before by the phase barrier) come
+    // before these async-proxy writes
+    fence_proxy_async_smem();
+    const uint32_t rowb = 2u * static_cast<uint32_t>(K);
+    mbar_arrive_expect_tx(&S.xsbar, 2u * NC * rowb);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const uint16_t* pl = static_cast<const uint16_t*>(ph.col[c].p);
+      bulk_g2s_plain(S.xs + (2 * c) * xpitch, pl, rowb, &S.xsbar);
+      bulk_g2s_plain(S.xs + (2 * c + 1) * xpitch, pl + K, rowb, &S.xsbar);
+    }
+  }
+  const bool ok = wait_bar(cp, S, &S.xsbar, pipe.xs_uses & 1u, 6, false);
+  if (!ok) S.fail = 1;
+  ++pipe.xs_uses;
+  gemv_tiles<NC>(cp, ph, S, pipe, yres);
 }
 
 template <class C>
 __device__ void gemv(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe) {
   if constexpr (C::bf16) {
+    if (ph.col[0].src == SRC_PLANES) {
+      if (ph.ncols == 1) gemv_planes<1>(cp, ph, S, pipe);
+      else gemv_planes<2>(cp, ph, S, pipe);
+      return;
+    }
     // the activation length selects how many float4 groups each thread holds (K <= GM·1024)
     if (ph.ncols == 1) {
       if (ph.K <= 3072) gemv_mma<1, 3>(cp, ph, S, pipe);
@@ -1147,8 +1194,13 @@ __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, 
     for (int j = 0; j < OPT; ++j) {
       const int h = oh + j * (kConsumers / HD);
       if (h < rep) {
-        if (ns == 1) ph.out[(g * rep + h) * HD + oe] = acc[j] / stat[8 + h];
-        else cp.part[(static_cast<size_t>(item) * 4 + h) * HD + oe] = acc[j];
+        if (ns == 1) {
+          const float o = acc[j] / stat[8 + h];
+          ph.out[(g * rep + h) * HD + oe] = o;
+          if (ph.outp != nullptr) store_planes(ph.outp, d.Hq * HD, (g * rep + h) * HD + oe, o);
+        } else {
+          cp.part[(static_cast<size_t>(item) * 4 + h) * HD + oe] = acc[j];
+        }
       }
     }
     if (ns == 1) {
@@ -1198,6 +1250,7 @@ __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, 
           l += w * mr[2 * s2 + 1];
         }
         ph.out[(g * rep + r) * HD + e] = o / l;
+        if (ph.outp != nullptr) store_planes(ph.outp, d.Hq * HD, (g * rep + r) * HD + e, o / l);
       }
     }
     named_bar(1, kConsumers);
@@ -1289,6 +1342,10 @@ __device__ __noinline__ void attn_fast_t(const CallParams& cp, const Phase& ph, 
     }
 #pragma unroll
     for (int j = 0; j < DPL; ++j) ph.out[static_cast<size_t>(jn) * (H * HD) + h * HD + lane * DPL + j] = o[j];
+    if (ph.outp != nullptr)
+#pragma unroll
+      for (int j = 0; j < DPL; ++j)
+        store_planes(ph.outp + static_cast<size_t>(jn) * 2 * (H * HD), H * HD, h * HD + lane * DPL + j, o[j]);
   }
 }
 
@@ -1725,7 +1782,7 @@ __device__ void fast_in(const CallParams& cp, int f) {
 
 template <class C>
 __device__ void consumers(const CallParams& cp, Smem& S) {
-  Pipe pipe{0, 0};
+  Pipe pipe{0, 0, 0};
   unsigned target = 0;
   const bool cta0 = blockIdx.x == 0;
   const int tid = threadIdx.x;
@@ -1797,6 +1854,7 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constan
       mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], kConsumerWarps);
     }
+    mbar_init(&S.xsbar, 1);
     S.abort_flag = 0;
     S.fail = 0;
     S.sync_ok = 1;

@@ -41,7 +41,9 @@ enum Op : int {
   OP_SAMPLE_MAIN,    // main draw + redraw + RAS + clamp (CTA 0) when not merged into a GEMV
 };
 
-enum Src : int { SRC_NONE = 0, SRC_BUF, SRC_EMBED, SRC_FEROW };
+// GEMV column sources: an fp32 vector, the Slow-AR input embedding, a fast_embeddings row, or
+// bf16 hi / lo rows (K each, hi + lo = the fp32 value to ~2^-17) written by the producing phase
+enum Src : int { SRC_NONE = 0, SRC_BUF, SRC_EMBED, SRC_FEROW, SRC_PLANES };
 enum Epi : int { EPI_STORE = 0, EPI_ADD, EPI_SWIGLU };
 
 // --------------------------------------------------------------- the model
@@ -108,13 +110,15 @@ struct alignas(16) Phase {
   const void* normw;     // nullable RMSNorm weight [K]
   float* hid_out;        // nullable: CTA 0 writes normalised column 0 here
   GemvCol col[2];
-  float* y[2];           // per-column output [M]
+  float* y[2];           // per-column output [M] (nullable when only planes are wanted)
+  uint16_t* yp[2];       // nullable: per-column output as bf16 hi [M] then lo [M] rows
   // attention
   int layer, npos, pos0, cb;
   int bump_pos;          // CTA 0 advances the stream position after this phase
   float scale;           // attention: 1/sqrt(head_dim)
   const float* qkv;      // [npos][QKV]
   float* out;            // [npos][Hq*hd]
+  uint16_t* outp;        // nullable: the output as bf16 hi / lo rows, [npos][2][Hq*hd]
   void* kc;              // Slow: K cache of this layer/stream [Hkv][slots][hd]; Fast: [W][Hkv][hd] fp32
   void* vc;
   const void* qn;
