@@ -57,6 +57,29 @@ constexpr const char* kLayerNames[9] = {"attention_norm", "attention.wqkv", "att
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Every activation-plane pointer of a program lies, with its whole extent, inside
+// [base, base + bytes): the device reads and writes them without further checks.
+bool planes_inside(const Phase* prog, size_t n, const void* base, size_t bytes, std::string& why) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(base), hi = lo + bytes;
+  auto in = [&](const void* q, size_t m) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(q);
+    return a >= lo && a + m <= hi;
+  };
+  for (size_t i = 0; i < n; ++i) {
+    const Phase& p = prog[i];
+    if (p.op == OP_GEMV) {
+      for (int c = 0; c < p.ncols; ++c) {
+        if (p.col[c].src == SRC_PLANES && !in(p.col[c].p, 4ull * p.K)) return (why = "planes input outside the workspace", false);
+        if (p.yp[c] != nullptr && !in(p.yp[c], 4ull * p.M)) return (why = "planes output outside the workspace", false);
+      }
+    }
+    if ((p.op == OP_ATTN_SLOW || p.op == OP_ATTN_FAST) && p.outp != nullptr &&
+        !in(p.outp, 4ull * static_cast<size_t>(p.npos > 0 ? p.npos : 1)))
+      return (why = "attention planes outside the workspace", false);
+  }
+  return true;
+}
+
 int fail(s2_ctx* c, int code, const std::string& msg) {
   if (c) c->err = msg;
   else g_init_error = msg;
@@ -245,6 +268,8 @@ struct Builder {
   }
   void push(Phase p) {
     const int g2 = c->grid - p.cta0;
+    if (p.op == OP_GEMV && p.ncols == 2 && (p.col[0].src == SRC_PLANES) != (p.col[1].src == SRC_PLANES))
+      err = "internal: a phase mixes planes and other activation sources";
     if (p.op == OP_GEMV && p.col[0].src == SRC_PLANES && p.normw != nullptr) err = "internal: normalised planes input";
     if (p.op == OP_GEMV) {
       const int rows = (p.M + g2 - 1) / g2;
@@ -477,6 +502,8 @@ int build_programs(s2_ctx* c) {
     if (static_cast<int>(all.size() - before) != c->n_fast) return fail(c, S2_EINVAL, "internal: fast program length");
   }
   if (!b.err.empty()) return fail(c, S2_EINVAL, b.err);
+  std::string why;
+  if (!planes_inside(all.data(), all.size(), c->ws, c->ws_bytes, why)) return fail(c, S2_EINVAL, "internal: " + why);
   if (cudaMemcpy(c->prog, all.data(), all.size() * sizeof(Phase), cudaMemcpyHostToDevice) != cudaSuccess)
     return fail(c, S2_ECUDA, "copying the phase programs failed");
   return S2_OK;
@@ -831,6 +858,8 @@ int build_static_fast_program(const Dims& d, int grid, const void* const* wt, co
   Builder b{&shape, nullptr, {}};
   int n = 0;
   auto push = [&](const Phase& p) {
+    if (p.op == OP_GEMV && p.ncols == 2 && (p.col[0].src == SRC_PLANES) != (p.col[1].src == SRC_PLANES))
+      b.err = "internal: a phase mixes planes and other activation sources";
     if (p.op == OP_GEMV) {
       const int g2 = grid - p.cta0;
       const int rows = (p.M + g2 - 1) / g2;
@@ -981,6 +1010,8 @@ extern "C" int s2_fast_logits_static(const s2_dims* s, const void* const* weight
   int rc = build_static_fast_program(d, sd.grid, weights, sl, g_static_prog, &n_built, why);
   if (rc != S2_OK) return static_fail(rc, why);
   if (n_built != n_phases) return static_fail(S2_EINVAL, "internal: Fast-AR program length");
+  if (!planes_inside(g_static_prog, static_cast<size_t>(n_built), sd.scratch, kStaticScratchBytes, why))
+    return static_fail(S2_EINVAL, "internal: " + why);
   cudaStream_t cs = stream;
   // what must start from zero (the array keeps the previous call's contents): control block, stream state
   Control ctl{};
