@@ -96,10 +96,6 @@ __device__ __forceinline__ void rows_of(const Phase& ph, int cta, int G, int& r0
   nr = base + (i < rem ? 1 : 0);
 }
 
-__device__ __forceinline__ bool should_bail(const CallParams& cp, Smem& S) {
-  return *reinterpret_cast<volatile int*>(&S.fail) != 0 || ld_volatile_int(&cp.ctl->error) != 0;
-}
-
 // Bounded wait on an mbarrier phase; on give-up records the failure and returns false.
 // try_wait suspends in hardware until the phase completes or a short time limit passes; the
 // abort/failure flags (shared memory) are polled every 16 tries, the global error word and the
@@ -137,23 +133,24 @@ __device__ bool grid_sync(const CallParams& cp, Smem& S, unsigned& target) {
   named_bar(1, kConsumers);
   target += gridDim.x;
   if (threadIdx.x == 0) {
-    int ok = !should_bail(cp, S);
+    // a failed CTA leaves at once (its failure is already in the global error word); the global
+    // error word itself is read only while waiting, off the path of the arrival
+    int ok = *reinterpret_cast<volatile int*>(&S.fail) == 0;
     if (ok) {
       // release: this CTA's writes (ordered before by the named barrier) become visible with the
       // arrival; acquire on the spin makes every other CTA's writes visible after it
       red_release_add(&cp.ctl->gbar, 1u);
       const long long lim = cp.ctl->spin_limit;
-      long long t0 = 0;
+      const long long t0 = clock_us();
       unsigned spins = 0;
+      // the clock every 8 polls, the global error word every 64
       while (ld_acquire(&cp.ctl->gbar) < target) {
-        if ((++spins & 63u) == 0) {
-          if (ld_volatile_int(&cp.ctl->error) != 0) {
+        if ((++spins & 7u) == 0) {
+          if ((spins & 63u) == 0 && ld_volatile_int(&cp.ctl->error) != 0) {
             ok = 0;
             break;
           }
-          const long long t = clock_us();
-          if (t0 == 0) t0 = t;
-          else if (t - t0 > lim) {
+          if (clock_us() - t0 > lim) {
             if (atomicCAS(&cp.ctl->error, 0, S2_ETIMEOUT) == 0) cp.ctl->error_where = 1;
             ok = 0;
             break;
@@ -194,6 +191,20 @@ __device__ __forceinline__ void attn_split(int n, int G, int Hkv, int& ns, int& 
 }
 __device__ __forceinline__ const float* attn_part_ml(const CallParams& cp, int G) {
   return cp.part + static_cast<size_t>(cp.d.Hkv) * max(1, G / cp.d.Hkv) * 4 * cp.d.hd;
+}
+
+// Wait for bulk copies into this CTA's shared memory to land before it may leave the kernel.
+// The bound is fixed (about two seconds, not the adjustable wait bound): copies complete within
+// microseconds unless the memory system has failed.
+constexpr long long kDrainLimitUs = 2000000;
+__device__ __noinline__ void drain_copies(const CallParams& cp, uint64_t* bar, uint32_t parity, int where) {
+  const long long t0 = clock_us();
+  while (!mbar_test(bar, parity)) {
+    if (clock_us() - t0 > kDrainLimitUs) {
+      if (atomicCAS(&cp.ctl->error, 0, S2_ETIMEOUT) == 0) cp.ctl->error_where = where;
+      break;
+    }
+  }
 }
 
 // =========================================================================
@@ -318,15 +329,7 @@ __device__ void producer(const CallParams& cp, Smem& S) {
   // Leave no copy in flight: the last fill of each stage must have landed before the CTA exits.
   for (unsigned long long back = 1; back <= kStages && back <= issued; ++back) {
     const unsigned long long t = issued - back;
-    const int s = static_cast<int>(t % kStages);
-    const uint32_t par = static_cast<uint32_t>((t / kStages) & 1u);
-    const long long t0 = clock_us();
-    while (!mbar_test(&S.full[s], par)) {
-      if (clock_us() - t0 > cp.ctl->spin_limit) {
-        if (atomicCAS(&cp.ctl->error, 0, S2_ETIMEOUT) == 0) cp.ctl->error_where = 3;
-        break;
-      }
-    }
+    drain_copies(cp, &S.full[static_cast<int>(t % kStages)], static_cast<uint32_t>((t / kStages) & 1u), 3);
   }
 }
 
@@ -925,7 +928,10 @@ __device__ __noinline__ void gemv_planes(const CallParams& cp, const Phase& ph, 
     }
   }
   const bool ok = wait_bar(cp, S, &S.xsbar, pipe.xs_uses & 1u, 6, false);
-  if (!ok) S.fail = 1;
+  if (!ok) {
+    S.fail = 1;
+    if (tid == 0) drain_copies(cp, &S.xsbar, pipe.xs_uses & 1u, 7);  // this CTA's own copies
+  }
   ++pipe.xs_uses;
   gemv_tiles<NC>(cp, ph, S, pipe, yres);
 }
