@@ -20,7 +20,7 @@ STATUS_NAMES = {0: "S2_OK", 1: "S2_EINVAL", 2: "S2_ENOMEM", 3: "S2_ECAPACITY", 4
 
 EXPORTS = ("s2_weight_count", "s2_weight_info", "s2_frame_workspace_bytes", "s2_frame_init", "s2_prefill",
            "s2_decode_frames", "s2_fast_logits", "s2_sync_status", "s2_set_spin_limit", "s2_set_trace",
-           "s2_phase_count", "s2_frame_free", "s2_last_error", "s2_fast_logits_static")
+           "s2_phase_count", "s2_frame_free", "s2_last_error", "s2_fast_logits_static", "s2_stream_import")
 
 
 class s2_dims(ctypes.Structure):
@@ -77,6 +77,7 @@ def load(path: str = LIB_PATH):
         "s2_frame_free": (i32, [vp]),
         "s2_last_error": (ctypes.c_char_p, [vp]),
         "s2_fast_logits_static": (i32, [P(s2_dims), P(vp), i32, i32, vp, vp, vp, vp, vp]),
+        "s2_stream_import": (i32, [vp, i32, i32, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -133,6 +134,11 @@ def s2_frame_init(dims: s2_dims, weight_ptrs, workspace_ptr: int, ws_bytes: int,
 def s2_prefill(ctx, stream_ids, tokens_ptr: int, lengths, stream: int = 0):
     rc = load().s2_prefill(ctx, len(stream_ids), _ints(stream_ids), tokens_ptr, _ints(lengths), stream)
     return _check("s2_prefill", rc, ctx)
+
+
+def s2_stream_import(ctx, stream_id: int, n_pos: int, k_ptr: int, v_ptr: int, x_last_ptr: int, stream: int = 0):
+    rc = load().s2_stream_import(ctx, stream_id, n_pos, k_ptr, v_ptr, x_last_ptr, stream)
+    return _check("s2_stream_import", rc, ctx)
 
 
 def s2_decode_frames(ctx, stream_ids, n_frames: int, params, expo_ptr: int, forced_ptr: int | None, codes_ptr: int,
@@ -234,6 +240,11 @@ class Decoder:
         s2_prefill(self.ctx, ids, toks.data_ptr(), lens, self.stream())
         self._keep = toks
         return toks
+
+    def import_stream(self, stream_id, k, v, x_last):
+        """k, v: device tensors [n_layer][n_kv_head][n_pos][head_dim] of the KV dtype; x_last: [dim] fp32."""
+        n_pos = int(k.shape[2])
+        s2_stream_import(self.ctx, stream_id, n_pos, k.data_ptr(), v.data_ptr(), x_last.data_ptr(), self.stream())
 
     def decode(self, n_frames, sampling, expo, forced=None, stream_ids=None, taps=False):
         """expo: [n][n_frames][11][30] float32 (device tensor); forced: optional [n][n_frames][11] int32.

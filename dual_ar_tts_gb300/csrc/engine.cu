@@ -56,6 +56,9 @@ constexpr const char* kLayerNames[9] = {"attention_norm", "attention.wqkv", "att
                                         "feed_forward.w2"};
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+// floats between the admissible-logit rows of consecutive streams: rows start on 256-byte
+// boundaries (the sampler copies a row into shared memory in 16-byte pieces)
+size_t logits_stride(const Dims& d) { return align_up(static_cast<size_t>(d.A), 64); }
 
 // Every activation-plane pointer of a program lies, with its whole extent, inside
 // [base, base + bytes): the device reads and writes them without further checks.
@@ -198,7 +201,7 @@ void carve(s2_ctx* c, Carver& cv) {
   c->rope_f = cv.take<float2>(static_cast<size_t>(d.Wf) * (d.hdf / 2));
   c->st = cv.take<StreamState>(B + 1);
   c->hidden = cv.take<float>(static_cast<size_t>(B + 1) * d.D);
-  c->logits = cv.take<float>(static_cast<size_t>(B) * d.A);
+  c->logits = cv.take<float>(static_cast<size_t>(B) * logits_stride(d));
   const size_t kv = static_cast<size_t>(d.L) * B * d.Hkv * slots * d.hd * d.kvsz;
   c->kc = cv.take<unsigned char>(kv);
   c->vc = cv.take<unsigned char>(kv);
@@ -415,7 +418,7 @@ int build_programs(s2_ctx* c) {
   for (int sid = 0; sid < c->max_streams && d.L > 0; ++sid) {
     const size_t before = all.size();
     float* hid = c->hidden + static_cast<size_t>(sid) * d.D;
-    float* lg = c->logits + static_cast<size_t>(sid) * d.A;
+    float* lg = c->logits + static_cast<size_t>(sid) * logits_stride(d);
     c->hidden_src = hid;
     // 1. main draw on CTA 0 while the other CTAs project the hidden state into Fast-AR position 0
     if (d.has_proj) {
@@ -648,7 +651,7 @@ int s2_prefill(s2_ctx* c, int n, const int* ids, const int32_t* tokens, const in
     a.rope = c->rope;
     a.scratch = c->pscratch;
     a.hidden = c->hidden + static_cast<size_t>(sid) * d.D;
-    a.logits = c->logits + static_cast<size_t>(sid) * d.A;
+    a.logits = c->logits + static_cast<size_t>(sid) * logits_stride(d);
     a.st = c->st + sid;
     a.err = &c->ctl->error;
     const int rc = run_prefill(a, stream);
@@ -657,6 +660,41 @@ int s2_prefill(s2_ctx* c, int n, const int* ids, const int32_t* tokens, const in
     c->host_pos[sid] = T;
     c->host_prefilled[sid] = 1;
   }
+  return S2_OK;
+}
+
+int s2_stream_import(s2_ctx* c, int sid, int n_pos, const void* k, const void* v, const float* x_last,
+                     CUstream_st* stream) {
+  if (!c) return fail(nullptr, S2_EINVAL, "ctx is NULL");
+  const Dims& d = c->d;
+  if (d.L == 0) return fail(c, S2_ESTATE, "this context has no Slow-AR (Fast-AR-alone shape)");
+  if (sid < 0 || sid >= c->max_streams) return fail(c, S2_EINVAL, "stream id out of range");
+  if (n_pos <= 0) return fail(c, S2_EINVAL, "n_pos must be positive");
+  if (n_pos > c->kv_slots) return fail(c, S2_ECAPACITY, "n_pos exceeds the KV slots");
+  if (!k || !v || !x_last) return fail(c, S2_EINVAL, "null import pointer");
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) % d.kvsz != 0 ||
+      reinterpret_cast<uintptr_t>(x_last) % 4 != 0)
+    return fail(c, S2_EINVAL, "import pointers are not aligned to their element size");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // cache layout: [layer][stream][KV head][slot][head_dim]; source: [layer][KV head][n_pos][head_dim]
+  const size_t row = static_cast<size_t>(n_pos) * d.hd * d.kvsz;
+  const size_t dpitch = static_cast<size_t>(c->kv_slots) * d.hd * d.kvsz;
+  const size_t layer_dst = static_cast<size_t>(c->max_streams) * d.Hkv * dpitch;
+  const size_t stream_dst = static_cast<size_t>(sid) * d.Hkv * dpitch;
+  const size_t layer_src = static_cast<size_t>(d.Hkv) * row;
+  for (int l = 0; l < d.L; ++l) {
+    const size_t dst = l * layer_dst + stream_dst;
+    if (cudaMemcpy2DAsync(c->kc + dst, dpitch, static_cast<const unsigned char*>(k) + l * layer_src, row, row,
+                          d.Hkv, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+        cudaMemcpy2DAsync(c->vc + dst, dpitch, static_cast<const unsigned char*>(v) + l * layer_src, row, row,
+                          d.Hkv, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return fail(c, S2_ECUDA, std::string("KV import copy failed: ") + cudaGetErrorString(cudaGetLastError()));
+  }
+  const int rc = run_head(d, x_last, c->norm, c->E, c->hidden + static_cast<size_t>(sid) * d.D,
+                          c->logits + static_cast<size_t>(sid) * logits_stride(d), c->st + sid, n_pos, stream);
+  if (rc != S2_OK) return fail(c, rc, std::string("import head launch failed: ") + cudaGetErrorString(cudaGetLastError()));
+  c->host_pos[sid] = n_pos;
+  c->host_prefilled[sid] = 1;
   return S2_OK;
 }
 
@@ -692,7 +730,7 @@ int s2_decode_frames(s2_ctx* c, int n, const int* ids, int n_frames, const s2_sa
     cp.prog = c->prog + static_cast<size_t>(sid) * c->n_dec;
     cp.st = c->st + sid;
     cp.hidden = c->hidden + static_cast<size_t>(sid) * d.D;
-    cp.logits = c->logits + static_cast<size_t>(sid) * d.A;
+    cp.logits = c->logits + static_cast<size_t>(sid) * logits_stride(d);
     cp.stage = c->stage + static_cast<size_t>(sid) * kMaxFramesPerCall * d.ncb;
     const size_t fo = static_cast<size_t>(k) * n_frames;
     cp.expo = expo + fo * kDraws * kTopK;
@@ -710,6 +748,10 @@ int s2_decode_frames(s2_ctx* c, int n, const int* ids, int n_frames, const s2_sa
     cp.ras_top_p = p.ras_top_p;
     cp.ras_window = p.ras_window;
     cp.min_tokens = p.min_tokens_before_end;
+    // the kernel copies these with 16-byte (bulk or cp.async) copies
+    if ((reinterpret_cast<uintptr_t>(cp.logits) | reinterpret_cast<uintptr_t>(cp.hidden) |
+         reinterpret_cast<uintptr_t>(cp.flogits)) % 16 != 0)
+      return fail(c, S2_EINVAL, "internal: a per-stream buffer is not 16-byte aligned");
     int rc = launch_frames(cp, c->grid, stream);
     if (rc != S2_OK) return fail(c, rc, std::string("frame kernel launch failed: ") + cudaGetErrorString(cudaGetLastError()));
     rc = compact_codes(cp.stage, codes + static_cast<size_t>(k) * d.ncb * n_frames, cp.st, n_frames, d.ncb, n_out + k,

@@ -403,6 +403,15 @@ int run_prefill(const PrefillArgs& a, void* stream) {
   return d.hd == 128 ? prefill_t<float, float, 128>(a, s, err) : prefill_t<float, float, 64>(a, s, err);
 }
 
+int run_head(const Dims& d, const float* x, const void* norm, const void* E, float* hidden, float* logits,
+             StreamState* st, int pos, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int blocks = (d.A + 7) / 8;
+  k_final<<<blocks, 256, d.D * sizeof(float), s>>>(x, d, norm, E, hidden, logits);
+  k_state_reset<<<1, 32, 0, s>>>(st, pos);
+  return cudaGetLastError() == cudaSuccess ? S2_OK : S2_ECUDA;
+}
+
 int build_rope_tables(float2* slow, int slots, int hd, float2* fast, int wf, int hdf, double base, int bf16,
                       void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -195,6 +195,9 @@ struct PrefillArgs {
   int* err;               // device word receiving S2_EINVAL on an out-of-range id
 };
 int run_prefill(const PrefillArgs& a, void* stream);
+// final norm + admissible logits of a residual x [D], then the stream reset to position pos
+int run_head(const Dims& d, const float* x, const void* norm, const void* E, float* hidden, float* logits,
+             StreamState* st, int pos, void* stream);
 size_t prefill_scratch_floats(const Dims& d, int chunk);
 
 }  // namespace s2

@@ -119,6 +119,21 @@ int s2_frame_init(const s2_dims* d, const void* const* weights, int n_weights, v
 int s2_prefill(s2_ctx* ctx, int n, const int* stream_ids, const int32_t* tokens, const int* lengths,
                struct CUstream_st* stream);
 
+/* Load one stream's decode state from caller memory instead of running s2_prefill (restoring a
+ * saved stream).  The pages have no counterpart: their state after a prompt is the KV cache of
+ * the Slow-AR (ch.02 §1: one fp16 slot per position and layer) plus the last position's output,
+ * which is what this call takes.
+ *   k, v    device [n_layer][n_kv_head][n_pos][head_dim] in the context's KV dtype (fp16 or
+ *           fp32); position t of KV head g of layer l at ((l*n_kv_head + g)*n_pos + t)*head_dim
+ *   x_last  device [dim] fp32: the Slow-AR residual of position n_pos-1 before the final norm
+ * The call copies K/V into slots 0..n_pos-1 of the stream, computes the normalised hidden and
+ * the admissible logits from x_last as s2_prefill does for its last position, and resets the
+ * stream (window empty, no frames emitted).  The caller's buffers may be reused once the call's
+ * work on `stream` has completed.  Errors: S2_EINVAL (bad id, n_pos <= 0, null or unaligned
+ * pointer), S2_ECAPACITY (n_pos > kv_slots), S2_ESTATE (no Slow-AR), S2_ECUDA. */
+int s2_stream_import(s2_ctx* ctx, int stream_id, int n_pos, const void* k, const void* v, const float* x_last,
+                     struct CUstream_st* stream);
+
 /* Decode up to n_frames frames for each of n prefilled streams (ids host [n]).
  *   params  host [n] sampler settings
  *   expo    device [n][n_frames][11][30] exponential variates E = -ln u (draw order: main,

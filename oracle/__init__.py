@@ -81,6 +81,8 @@ def _load():
                 "or_fast_forward": (i32, [vp, vp, vp, i32, vp, vp]),
                 "or_kv_io": (i32, [vp, i32, i32, i32, vp, vp, i32]),
                 "or_draw": (i32, [vp, vp, i32, f32, f32, i32, vp, vp]),
+                "or_kv_set_f16": (i32, [vp, i32, i32, vp, vp]),
+                "or_head": (i32, [vp, vp, vp, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -132,11 +134,11 @@ def attention(q, K, V, n=None):
 
 
 def draw(logits, temperature, top_p, top_k, E, ids=None):
-    """Returns (token, diag[6]); see ``or_draw`` in s2_oracle.c."""
+    """Returns (token, diag[7]); see ``or_draw`` in s2_oracle.c."""
     lg = _f32(logits)
     e = _f32(E)
     assert e.size >= top_k
-    diag = np.zeros(6, np.float32)
+    diag = np.zeros(7, np.float32)
     idv = None if ids is None else _i32(ids)
     tok = _load().or_draw(lg.ctypes.data, None if idv is None else idv.ctypes.data, lg.size, float(temperature),
                           float(top_p), int(top_k), e.ctypes.data, diag.ctypes.data)
@@ -220,6 +222,30 @@ class Session:
         if _load().or_kv_io(self._h, layer, s0, n, k.ctypes.data, v.ctypes.data, 0):
             raise ValueError("kv range")
         return k, v
+
+    def set_kv_f16(self, layer, k16, v16):
+        """Slots 0..n-1 of one layer from fp16 bit patterns (uint16) in [kv_head][n][head_dim] order."""
+        k16 = np.ascontiguousarray(k16, dtype=np.uint16)
+        v16 = np.ascontiguousarray(v16, dtype=np.uint16)
+        if _load().or_kv_set_f16(self._h, layer, k16.shape[1], k16.ctypes.data, v16.ctypes.data):
+            raise ValueError("kv range")
+
+    def head(self, x_last):
+        """Final norm + tied logits of a residual: (logits over the vocabulary, normalised hidden)."""
+        x = _f32(x_last)
+        logits = np.empty(self.d["vocab"], np.float32)
+        hidden = np.empty(self.d["dim"], np.float32)
+        _load().or_head(self._h, x.ctypes.data, logits.ctypes.data, hidden.ctypes.data)
+        return logits, hidden
+
+    def import_state(self, k16, v16, x_last):
+        """Stream state without a prompt: K/V fp16 [L][kv_head][n][head_dim] into slots 0..n-1,
+        position n, and the head's outputs on x_last (what a prefill of n positions leaves)."""
+        n = k16.shape[2]
+        for l in range(self.d["n_layer"]):
+            self.set_kv_f16(l, k16[l], v16[l])
+        self.set_pos(n)
+        return self.head(x_last)
 
     def set_kv(self, layer, s0, k, v):
         k, v = _f32(k), _f32(v)

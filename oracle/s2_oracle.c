@@ -457,6 +457,37 @@ int or_kv_io(or_sess* s, int layer, int s0, int n, float* k, float* v, int write
   return 0;
 }
 
+/* KV slots [0, n) of one layer from fp16 bit patterns in [kv_head][n][head_dim] order, widened
+ * exactly to fp32 (the cache precision of ch.02 §1); the stream's other slots are untouched. */
+int or_kv_set_f16(or_sess* s, int layer, int n, const uint16_t* k, const uint16_t* v) {
+  const or_dims* d = &s->d;
+  if (layer < 0 || layer >= d->n_layer || n < 0 || n > s->slots) return -1;
+  size_t per_layer = (size_t)d->n_kv_head * s->slots * d->head_dim;
+#pragma omp parallel for schedule(static)
+  for (int g = 0; g < d->n_kv_head; ++g)
+    for (int t = 0; t < n; ++t) {
+      float* kc = s->kc + layer * per_layer + ((size_t)g * s->slots + t) * d->head_dim;
+      float* vc = s->vc + layer * per_layer + ((size_t)g * s->slots + t) * d->head_dim;
+      const uint16_t* ki = k + ((size_t)g * n + t) * d->head_dim;
+      const uint16_t* vi = v + ((size_t)g * n + t) * d->head_dim;
+      for (int e = 0; e < d->head_dim; ++e) {
+        _Float16 a, b;
+        memcpy(&a, ki + e, 2);
+        memcpy(&b, vi + e, 2);
+        kc[e] = (float)a;
+        vc[e] = (float)b;
+      }
+    }
+  return 0;
+}
+
+/* The Slow-AR head on a given residual (ch.02 §3.2: final RMSNorm, then logits against the
+ * tied embedding table over the whole vocabulary). */
+int or_head(const or_sess* s, const float* xlast, float* logits, float* hidden) {
+  head(s, xlast, logits, hidden);
+  return 0;
+}
+
 int or_set_pos(or_sess* s, int pos) {
   if (pos < 0 || pos > s->slots) return -1;
   s->pos = pos;
@@ -486,10 +517,11 @@ static int cand_cmp(const void* a, const void* b) {
  *   rank r is kept iff r == 0 or Σ_{s<r} π_s < top_p
  *   return the kept candidate maximising π_r / E_r (E = -log u, given); ties -> lower rank
  * `ids` (nullable) gives the token id of each logit (default: its index).
- * `diag` (nullable, 6 floats) receives, for margin checks: [0] z of rank k-1 minus z of rank k
+ * `diag` (nullable, 7 floats) receives, for margin checks: [0] z of rank k-1 minus z of rank k
  * (the top-k cut; +inf if fewer), [1] smallest |Σ_{s<r} π_s - top_p| over ranks 1..k-1,
  * [2] best score, [3] runner-up score (score = log π_r - log E_r), [4] max |logit| over finite
- * entries, [5] rank of the winner. */
+ * entries, [5] rank of the winner, [6] smallest z gap between the winner and its neighbouring
+ * ranks (+inf if it has none). */
 int or_draw(const float* logits, const int32_t* ids, int n, float temperature, float top_p, int top_k,
             const float* E, float* diag) {
   if (top_k < 1 || top_k > 64 || n <= 0) return -1;
@@ -549,6 +581,12 @@ int or_draw(const float* logits, const int32_t* ids, int n, float temperature, f
     diag[3] = second;
     diag[4] = amax;
     diag[5] = (float)best;
+    /* the variates belong to ranks: the winner's token is unambiguous only while its z is apart
+     * from the z of the neighbouring ranks */
+    float rg = INFINITY;
+    if (best > 0) rg = c[best - 1].z - c[best].z;
+    if (best + 1 < k && c[best].z - c[best + 1].z < rg) rg = c[best].z - c[best + 1].z;
+    diag[6] = rg;
   }
   free(c);
   return tok;

@@ -57,10 +57,11 @@ def _load():
                                       ctypes.c_double, ctypes.c_void_p)
             lib.synth_normal_f32.argtypes = [u64, u64, i64, dbl, dbl, vp]
             lib.synth_normal_bf16.argtypes = [u64, u64, i64, dbl, dbl, vp]
+            lib.synth_normal_f16.argtypes = [u64, u64, i64, dbl, dbl, vp]
             lib.synth_exponential_f32.argtypes = [u64, u64, i64, vp]
             lib.synth_uniform_f64.argtypes = [u64, u64, i64, vp]
             lib.synth_uniform_int.argtypes = [u64, u64, i64, i32, i32, vp]
-            for f in (lib.synth_normal_f32, lib.synth_normal_bf16, lib.synth_exponential_f32,
+            for f in (lib.synth_normal_f32, lib.synth_normal_bf16, lib.synth_normal_f16, lib.synth_exponential_f32,
                       lib.synth_uniform_f64, lib.synth_uniform_int):
                 f.restype = None
             _lib = lib
@@ -81,6 +82,13 @@ def normal_bf16(seed: int, stream: int, n: int, mean: float = 0.0, std: float = 
     """bf16 bit patterns (uint16)."""
     out = np.empty(n, np.uint16)
     _load().synth_normal_bf16(seed, stream, n, mean, std, out.ctypes.data)
+    return out
+
+
+def normal_f16(seed: int, stream: int, n: int, mean: float = 0.0, std: float = 1.0) -> np.ndarray:
+    """fp16 bit patterns (uint16)."""
+    out = np.empty(n, np.uint16)
+    _load().synth_normal_f16(seed, stream, n, mean, std, out.ctypes.data)
     return out
 
 
@@ -298,6 +306,29 @@ def expo(seed: int, stream: int, n_frames: int, first_frame: int = 0) -> np.ndar
     per = N_DRAWS * TOP_K
     full = exponential_f32(seed, 2_000_000 + stream, (first_frame + n_frames) * per)
     return full[first_frame * per:].reshape(n_frames, N_DRAWS, TOP_K)
+
+
+def kv_state(seed: int, stream: int, d: dict, n_pos: int):
+    """Synthetic decode state of one stream, standing in for a prefilled prompt of n_pos positions
+    (used where an fp32 CPU prefill of the prompt would take too long).
+
+    K and V ~ N(0, 1) as fp16 bit patterns [n_layer][n_kv_head][n_pos][head_dim] (the scale of
+    normalised keys and of values projected from a normalised residual with N(0, 0.02) weights),
+    and the last residual x ~ N(0, 1) fp32 [dim].  Values of (layer, head) come from their own
+    generator stream indexed by slot * head_dim + element, so a shorter state is a prefix of a
+    longer one under the same seed and stream.
+    """
+    L, H, hd = d["n_layer"], d["n_kv_head"], d["head_dim"]
+    base = 4_000_000 + 4096 * stream
+    k = np.empty((L, H, n_pos, hd), np.uint16)
+    v = np.empty_like(k)
+    for l in range(L):
+        for g in range(H):
+            j = 2 * (l * H + g)
+            k[l, g] = normal_f16(seed, base + j, n_pos * hd).reshape(n_pos, hd)
+            v[l, g] = normal_f16(seed, base + j + 1, n_pos * hd).reshape(n_pos, hd)
+    x = normal_f32(seed, base + 4095, d["dim"])
+    return k, v, x
 
 
 def fast_inputs(seed: int, n_frames: int, d: dict):

@@ -18,7 +18,8 @@
  *   exponential(i) = -ln u(i)                          (inverse CDF, double)
  *   integer(i)     = lo + (b mod (hi - lo + 1))
  *
- * bf16 outputs are the fp32 value rounded to nearest-even on its top 16 bits.
+ * bf16 outputs are the fp32 value rounded to nearest-even on its top 16 bits; fp16 outputs are
+ * the double rounded to nearest-even binary16 (subnormals kept, overflow to infinity).
  */
 #include <math.h>
 #include <stddef.h>
@@ -87,6 +88,41 @@ void synth_normal_bf16(uint64_t seed, uint64_t stream, int64_t n, double mean, d
     normal_pair(key, (uint64_t)j, &z0, &z1);
     out[2 * j] = f32_to_bf16_rne((float)(mean + std * z0));
     if (2 * j + 1 < n) out[2 * j + 1] = f32_to_bf16_rne((float)(mean + std * z1));
+  }
+}
+
+/* double -> IEEE binary16 bits, round to nearest even.  Scaling by a power of two is exact, so
+ * rint() (default rounding mode: nearest even) does the only rounding. */
+static inline uint16_t f64_to_f16_rne(double x) {
+  uint16_t sign = signbit(x) ? 0x8000u : 0u;
+  double a = fabs(x);
+  if (a == 0.0) return sign;
+  int e2;
+  (void)frexp(a, &e2);               /* a = m * 2^e2, m in [0.5, 1) */
+  int e = e2 - 1;                    /* a in [2^e, 2^(e+1)) */
+  if (e < -14) {                     /* subnormal range: steps of 2^-24 */
+    double q = rint(ldexp(a, 24));   /* q = 1024 lands on the smallest normal, bits 0x0400 */
+    return (uint16_t)(sign | (uint16_t)q);
+  }
+  double q = rint(ldexp(a, 10 - e)); /* in [1024, 2048] */
+  if (q >= 2048.0) {
+    q = 1024.0;
+    e += 1;
+  }
+  if (e > 15) return (uint16_t)(sign | 0x7c00u);
+  return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)(q - 1024.0));
+}
+
+/* n values of mean + std·N(0,1), rounded fp64 -> fp16 (raw 16-bit patterns). */
+void synth_normal_f16(uint64_t seed, uint64_t stream, int64_t n, double mean, double std, uint16_t* out) {
+  uint64_t key = stream_key(seed, stream);
+  int64_t pairs = (n + 1) / 2;
+#pragma omp parallel for schedule(static)
+  for (int64_t j = 0; j < pairs; ++j) {
+    double z0, z1;
+    normal_pair(key, (uint64_t)j, &z0, &z1);
+    out[2 * j] = f64_to_f16_rne(mean + std * z0);
+    if (2 * j + 1 < n) out[2 * j + 1] = f64_to_f16_rne(mean + std * z1);
   }
 }
 

@@ -25,3 +25,18 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def s2pro():
+    """S2-Pro-shaped synthetic weights (seed 0): dims, host arrays, device tensors, names."""
+    import torch
+    import synth
+    import dual_ar_tts_gb300 as pkg
+    d = synth.CONFIGS["frame"]["dims"]
+    host = synth.make_weights(d, 0)
+    dev = pkg.upload_weights(host)
+    names = [n for n, _, _ in synth.weight_specs(d)]
+    yield d, host, dev, names
+    del dev
+    torch.cuda.empty_cache()

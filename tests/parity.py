@@ -16,7 +16,10 @@ def draw_is_pinned(diag, eps_logit, temperature):
     decisions: the top-k cut, the top-p cut and the winner (diag from oracle.draw)."""
     eta = eps_logit / temperature            # perturbation of z = logit / T
     topk_gap, p_gap, best, second = float(diag[0]), float(diag[1]), float(diag[2]), float(diag[3])
-    return topk_gap > 2 * eta and p_gap > 3 * eta and (best - second) > 4 * eta
+    # the variates are indexed by rank, so the winning rank must hold the same token on both
+    # sides: its z is apart from the neighbouring ranks' by more than two perturbations
+    rank_gap = float(diag[6])
+    return topk_gap > 2 * eta and p_gap > 3 * eta and (best - second) > 4 * eta and rank_gap > 2 * eta
 
 
 def compare_frames(ref, out, d, s, tol, stream=0, check_draws=True):

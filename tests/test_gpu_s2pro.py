@@ -20,18 +20,6 @@ pytestmark = pytest.mark.gpu
 TOL = 2e-2
 
 
-@pytest.fixture(scope="module")
-def s2pro():
-    import dual_ar_tts_gb300 as pkg
-    d = synth.CONFIGS["frame"]["dims"]
-    host = synth.make_weights(d, 0)
-    dev = pkg.upload_weights(host)
-    names = [n for n, _, _ in synth.weight_specs(d)]
-    yield d, host, dev, names
-    del dev
-    torch.cuda.empty_cache()
-
-
 def _subset(names_full, tensors, d_sub):
     by = dict(zip(names_full, tensors))
     return [None if (d_sub["n_layer"] == 0 and n in ("embeddings", "codebook_embeddings", "norm")) else by[n]

@@ -491,3 +491,70 @@ def test_fp16_kv_cache_rounds_on_store():
     k16, v16 = b.kv(0, 0, 32)
     np.testing.assert_array_equal(k16, k32.astype(np.float16).astype(np.float32))
     np.testing.assert_array_equal(v16, v32.astype(np.float16).astype(np.float32))
+
+
+# ------------------------------------------------ stream state without a prompt
+
+def test_kv_set_f16_widens_bit_patterns_exactly():
+    d16 = dict(TINY, kv_dtype=synth.F16)
+    s = oracle.Session(d16, _tiny_weights(), 8)
+    H, hd = d16["n_kv_head"], d16["head_dim"]
+    pats = np.array([0x3C00, 0xC000, 0x0001, 0x7BFF, 0x8000, 0x3555, 0x0400, 0xFBFF], np.uint16)
+    want = np.array([1.0, -2.0, 2.0 ** -24, 65504.0, -0.0, 0.333251953125, 2.0 ** -14, -65504.0], np.float32)
+    k = np.tile(pats, H * 2 * hd // len(pats)).reshape(H, 2, hd)
+    v = k[:, ::-1].copy()
+    s.set_kv_f16(1, k, v)
+    kk, vv = s.kv(1, 0, 2)                      # [slot][head][hd]
+    np.testing.assert_array_equal(kk, np.tile(want, H * 2 * hd // len(want)).reshape(H, 2, hd).transpose(1, 0, 2))
+    np.testing.assert_array_equal(vv[0], kk[1])
+
+
+def test_head_closed_form_and_brute_force():
+    d = TINY
+    w = _tiny_weights(jitter=0.1)
+    s = oracle.Session(d, w, 8)
+    normw = w[2].astype(np.float64)
+    lg, h = s.head(np.full(d["dim"], -3.0, np.float32))
+    np.testing.assert_allclose(h, -normw, rtol=1e-6)          # x = a·1: RMSNorm gives sign(a)·w
+    x = synth.normal_f32(5, 5, d["dim"])
+    lg, h = s.head(x)
+    xd = x.astype(np.float64)
+    np.testing.assert_allclose(h, xd / np.sqrt(np.mean(xd ** 2) + 1e-6) * normw, rtol=2e-5, atol=1e-6)
+    np.testing.assert_allclose(lg, w[0].astype(np.float64) @ h.astype(np.float64), rtol=1e-4, atol=1e-5)
+    lg2, h2 = s.head(x * 7.0)                    # scale invariance of the final norm
+    np.testing.assert_allclose(h2, h, rtol=1e-5, atol=1e-6)
+
+
+def test_imported_state_steps_like_the_prefilled_one():
+    # a stream restored from another stream's fp16 KV and position continues identically
+    d16 = dict(TINY, kv_dtype=synth.F16)
+    w = _tiny_weights(jitter=0.1)
+    p = synth.prompt("tiny")
+    a = oracle.Session(d16, w, 40)
+    a.prefill(p)
+    b = oracle.Session(d16, w, 40)
+    L, H, hd, n = d16["n_layer"], d16["n_kv_head"], d16["head_dim"], len(p)
+    for l in range(L):
+        k, v = a.kv(l, 0, n)                     # [slot][head][hd], fp16 values
+        k16 = k.astype(np.float16).view(np.uint16).transpose(1, 0, 2)
+        v16 = v.astype(np.float16).view(np.uint16).transpose(1, 0, 2)
+        b.set_kv_f16(l, k16, v16)
+    b.set_pos(n)
+    vals = p[-1].copy()
+    vals[0] = d16["sem_begin"] + 3
+    la, ha = a.step(vals)
+    lb, hb = b.step(vals)
+    np.testing.assert_array_equal(la, lb)
+    np.testing.assert_array_equal(ha, hb)
+
+
+def test_draw_diag_reports_the_winner_rank_gap():
+    # three candidates with z = 3, 2.5, 2.4 (T = 1); variates make rank 1 win
+    lg = np.array([3.0, 2.5, 2.4, -5.0], np.float32)
+    E = np.full(30, 100.0, np.float32)
+    E[1] = 1e-3
+    tok, diag = oracle.draw(lg, 1.0, 1.0, 30, E)
+    assert tok == 1 and int(diag[5]) == 1
+    assert abs(float(diag[6]) - 0.1) < 1e-6        # min(3 - 2.5, 2.5 - 2.4)
+    tok, diag = oracle.draw(np.array([3.0], np.float32), 1.0, 1.0, 30, E)
+    assert np.isinf(diag[6])
