@@ -1,0 +1,1243 @@
+// Batched frame decode: one decode call advances B independent streams together, and every weight
+// matrix is read from HBM once per step for the whole batch (the frame loop of s2.cpp analysis
+// ch.06 §5.1 run for B streams at once; the projections of ch.02 §3.2 as skinny GEMMs).
+//
+// One frame is a fixed sequence of kernels, captured once per call as a CUDA graph and replayed
+// for every frame (kernels read the frame index from device memory):
+//
+//   main draws (one CTA per stream) -> fast_project_in -> Fast-AR calls 1..9 (4 layers each, then
+//   fast_output and the draw) -> Slow-AR step (36 layers, final norm, admissible tied logits)
+//
+// Projections run on the 5th-generation tensor cores (k_bgemv): y[c] = W·a_c for the NC columns
+// of the batch.  Tiles of 128 weight rows × 64 K come in by TMA (128-byte swizzle); the
+// activations are bf16 hi/lo "planes" (row 2c = hi, row 2c+1 = lo, hi + lo = the fp32 value to
+// ~2^-17), the MMA's N dimension; one thread issues tcgen05.mma into a TMEM accumulator and four
+// warps read it back.  K is split across CTAs so that every SM streams weights; the partial sums
+// are reduced in a fixed order by the consumer kernel (deterministic results).  The consumer
+// kernels fuse what follows a projection: residual add + RMSNorm + planes for the next
+// projection, SwiGLU, q/k norm + RoPE + KV store + attention, the draws.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "ptx.cuh"
+#include "s2_internal.h"
+#include "sampler.cuh"
+#include "tc05.cuh"
+
+namespace s2 {
+namespace {
+
+constexpr int kTileM = 128;                 // weight rows per MMA tile (the MMA's M)
+constexpr int kAtom = 64;                   // K elements per pipeline stage (one 128-byte row)
+constexpr int kABytes = kTileM * kAtom * 2;  // one weight tile
+constexpr int kGemvThreads = 192;           // 4 epilogue warps, 1 TMA warp, 1 MMA warp
+constexpr int kMaxGemvStages = 8;
+constexpr int kGemvSmemBudget = 200 * 1024;
+constexpr int kPrepThreads = 256;
+constexpr int kAttnTile = 32;               // KV slots per staged tile (Slow-AR attention)
+constexpr int kAttnChunk = 128;             // target slots per Slow-AR attention item
+constexpr int kMaxSplitsAttn = 32;          // items per (stream, KV head) at most
+
+enum ColMode : int { CM_RESID = 0, CM_STORE, CM_FEROW, CM_EMBED, CM_HIDDEN };
+
+// per-stream settings of a call (device copy)
+struct BStream {
+  int sid, min_tokens, ras_window, pad;
+  float T, top_p, ras_T, ras_top_p;
+  const float* expo;       // [n_frames][11][30]
+  const int32_t* forced;   // [n_frames][11] or null
+  float* dbg_main;         // [n_frames][A] or null
+  float* dbg_fast;         // [n_frames][NCB-1][CBS] or null
+  float* dbg_hidden;       // [n_frames][D] or null
+  int32_t* dbg_draws;      // [n_frames][11] or null
+};
+
+// everything a batched kernel may touch (passed by value)
+struct BEnv {
+  Dims d;
+  int nb;
+  int max_streams, kv_slots, lstride;
+  StreamState* st;
+  const BStream* bs;
+  int* bctl;               // [0] frame index within the call
+  float* hidden;           // [max_streams][D]
+  float* logits;           // [max_streams][lstride]
+  int32_t* stage;          // [max_streams][kMaxFramesPerCall][NCB]
+  Control* ctl;
+  unsigned char* kc;
+  unsigned char* vc;
+  const float2* rope;
+  const float2* rope_f;
+  const void* E;
+  const void* CE;
+  const void* FE;
+  uint16_t* pX;            // planes [rows][ldX]
+  uint16_t* pO;
+  uint16_t* pH;
+  int ldX, ldO, ldH;
+  float* part;             // split-K partials
+  float* bx;               // [max_streams][D]       Slow-AR residual
+  float* bfx;              // [max_streams][2][Df]   Fast-AR residual rows of the call's new positions
+  float* bfk;              // [max_streams][Lf][Wf][Hkvf][hdf]
+  float* bfv;
+  float* apart;            // attention split partials
+  float* bflog;            // [max_streams][CBS]
+  int32_t* bfcode;         // [max_streams][16]
+};
+
+__device__ __forceinline__ int frame_index(const BEnv& e) { return ldcgi(e.bctl); }
+__device__ __forceinline__ bool stream_done(const BEnv& e, int sid) { return ldcgi(&e.st[sid].done) != 0; }
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Control* ctl) {
+  const long long lim = ctl->spin_limit;
+  const long long t0 = clock_us();
+  for (unsigned i = 1;; ++i) {
+    if (mbar_test(bar, parity)) return true;
+    if ((i & 255u) == 0 && clock_us() - t0 > lim) break;
+  }
+  if (atomicCAS(&ctl->error, 0, S2_ETIMEOUT) == 0) ctl->error_where = 10;
+  return false;
+}
+
+__device__ __forceinline__ void store_hilo(uint16_t* planes, int ld, int col, int k, float v) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+  planes[static_cast<size_t>(2 * col) * ld + k] = __bfloat16_as_ushort(hi);
+  planes[static_cast<size_t>(2 * col + 1) * ld + k] = __bfloat16_as_ushort(lo);
+}
+
+// deterministic block sum (fixed order) for 256 threads
+__device__ __forceinline__ float block_sum256(float v, float* red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int i = 0; i < kPrepThreads / 32; ++i) t += red[i];
+  return t;
+}
+
+// =========================================================================================
+// projection: part[((z*splits + split)*NC + c)*M + m] = Σ_{k in split} W_z[row0 + m][k]·a_c[k]
+// =========================================================================================
+
+struct GemvBars {
+  uint64_t full[kMaxGemvStages], empty[kMaxGemvStages], acc;
+  uint32_t taddr;
+};
+
+__global__ void __launch_bounds__(kGemvThreads, 1)
+    k_bgemv(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+            const __grid_constant__ CUtensorMap tmB, int M, int row0, int N, int NC, int atoms_total, int atoms_per,
+            int nstages, float* part, Control* ctl) {
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  const int sbytes = kABytes + N * 128;
+  GemvBars& S = *reinterpret_cast<GemvBars*>(sm + nstages * sbytes);
+  const int tile = blockIdx.x, split = blockIdx.y, z = blockIdx.z, splits = gridDim.y;
+  const int a0 = split * atoms_per, a1 = min(a0 + atoms_per, atoms_total);
+  const int na = a1 - a0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const CUtensorMap* tA = z == 0 ? &tmA : &tmA2;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < nstages; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 1);
+    }
+    mbar_init(&S.acc, 1);
+    fence_barrier_init();
+  }
+  const uint32_t ncols = N <= 32 ? 32u : (N <= 64 ? 64u : (N <= 128 ? 128u : 256u));
+  if (warp == 0) {
+    tmem_alloc(&S.taddr, ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tacc = S.taddr;
+  if (warp == 4) {
+    if (lane == 0) {
+      prefetch_tmap(tA);
+      prefetch_tmap(&tmB);
+      const uint64_t pol = policy_evict_first();
+      for (int i = 0; i < na; ++i) {
+        const int s = i % nstages;
+        if (i >= nstages && !wait_bar(&S.empty[s], ((i / nstages) & 1) ^ 1, ctl)) break;
+        unsigned char* A = sm + s * sbytes;
+        mbar_arrive_expect_tx(&S.full[s], sbytes);
+        tma_load_2d(A, tA, (a0 + i) * kAtom, row0 + tile * kTileM, &S.full[s], pol);
+        tma_load_2d(A + kABytes, &tmB, (a0 + i) * kAtom, 0, &S.full[s], pol);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kTileM, N);
+      int i = 0;
+      for (; i < na; ++i) {
+        const int s = i % nstages;
+        if (!wait_bar(&S.full[s], (i / nstages) & 1, ctl)) break;
+        tc_fence_after();
+        const uint32_t A = smem_u32(sm + s * sbytes);
+        const uint32_t B = A + kABytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma(tacc, desc_sw128(A + kk * 32), desc_sw128(B + kk * 32), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&S.empty[s]);
+      }
+      tc_commit(&S.acc);
+    }
+  } else {
+    const bool ok = __all_sync(0xffffffffu, wait_bar(&S.acc, 0, ctl));
+    if (ok) {
+      tc_fence_after();
+      const int row = tile * kTileM + warp * 32 + lane;
+      float* out = part + (static_cast<size_t>(z) * splits + split) * NC * M;
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        float v[16];
+        tmem_ld16(tacc + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int c = c0 / 2 + j;
+          if (c < NC && row < M) out[static_cast<size_t>(c) * M + row] = v[2 * j] + v[2 * j + 1];
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tacc, ncols);
+}
+
+// =========================================================================================
+// column preparation: the fp32 input row of each column (residual add of split partials, a
+// fast_embeddings row, the Slow-AR input embedding, or the hidden state), stored, RMS-normalised
+// with a norm weight, and written as hi/lo planes for the next projection
+// =========================================================================================
+
+struct ColPrep {
+  int npos;               // columns per stream
+  int mode[2];            // ColMode of position j
+  int K;                  // row length
+  const float* part;      // partials [splits][part_nc][K] (CM_RESID, CM_STORE)
+  int splits;
+  int part_nc;            // columns of the partials
+  int part_by_stream;     // partial column = stream b (else = this column c)
+  float* x;               // residual rows: stream b, position j at x + b*xb + j*K
+  int xb;
+  const void* normw;      // RMSNorm weight (bf16 or fp32 per d.esz); null: no norm
+  int last_only;          // planes only for position npos-1, at column b
+  int code_idx;           // CM_FEROW: which code of the frame (bfcode[b][code_idx])
+  float* hid_out;         // optional: the normalised row (by stream id, stride D)
+};
+
+__global__ void __launch_bounds__(kPrepThreads) k_colprep(const BEnv e, const ColPrep p) {
+  __shared__ float red[kPrepThreads / 32];
+  constexpr int kMaxPer = 12;  // K <= 12 * 256 (checked on the host)
+  const Dims& d = e.d;
+  const int c = blockIdx.x, b = c / p.npos, j = c % p.npos;
+  const int sid = e.bs[b].sid;
+  if (stream_done(e, sid)) return;
+  const int K = p.K, tid = threadIdx.x;
+  const int mode = p.mode[j];
+  const int pcol = p.part_by_stream ? b : c;
+  float v[kMaxPer];
+  float ss = 0.f;
+  int code = 0, tok = 0;
+  float msem = 0.f;
+  if (mode == CM_FEROW) code = ldcgi(&e.bfcode[b * 16 + p.code_idx]);
+  if (mode == CM_EMBED) {
+    tok = ldcgi(&e.st[sid].vals[0]);
+    msem = (tok >= d.sem_lo && tok <= d.sem_hi) ? 1.f : 0.f;
+  }
+  float* xr = p.x ? p.x + static_cast<size_t>(b) * p.xb + static_cast<size_t>(j) * K : nullptr;
+#pragma unroll
+  for (int i = 0; i < kMaxPer; ++i) {
+    const int k = tid + i * kPrepThreads;
+    float a = 0.f;
+    if (k < K) {
+      if (mode == CM_RESID || mode == CM_STORE) {
+        a = mode == CM_RESID ? ldcg(xr + k) : 0.f;
+        for (int s = 0; s < p.splits; ++s) a += ldcg(p.part + (static_cast<size_t>(s) * p.part_nc + pcol) * K + k);
+      } else if (mode == CM_FEROW) {
+        a = wload(e.FE, static_cast<size_t>(code) * K + k, d.esz);
+      } else if (mode == CM_EMBED) {
+        // x = sem_scale·E[r0] + m·Σ_cb CE[cb·CBS + code_cb]   (ch.02 §3.2)
+        float acc = 0.f;
+        for (int cb = 0; cb < d.ncb; ++cb) {
+          const size_t row = static_cast<size_t>(cb) * d.cbs + ldcgi(&e.st[sid].vals[1 + cb]);
+          acc = __fadd_rn(acc, wload(e.CE, row * K + k, d.esz));
+        }
+        a = __fadd_rn(__fmul_rn(d.sem_scale, wload(e.E, static_cast<size_t>(tok) * K + k, d.esz)), __fmul_rn(msem, acc));
+      } else {  // CM_HIDDEN
+        a = ldcg(e.hidden + static_cast<size_t>(sid) * d.D + k);
+      }
+      if (xr) xr[k] = a;
+      ss += a * a;
+    }
+    v[i] = a;
+  }
+  float r = 1.f;
+  if (p.normw) r = 1.0f / sqrtf(block_sum256(ss, red) / static_cast<float>(K) + d.eps);
+  const bool planes = !p.last_only || j == p.npos - 1;
+  const int pc = p.last_only ? b : c;
+#pragma unroll
+  for (int i = 0; i < kMaxPer; ++i) {
+    const int k = tid + i * kPrepThreads;
+    if (k < K) {
+      const float n = p.normw ? (v[i] * r) * wload(p.normw, k, d.esz) : v[i];
+      if (planes) store_hilo(e.pX, e.ldX, pc, k, n);
+      if (p.hid_out) p.hid_out[static_cast<size_t>(sid) * d.D + k] = n;
+    }
+  }
+}
+
+// SwiGLU of the two projections (partials of W1 then W3, one split): planes of silu(g)·u
+__global__ void __launch_bounds__(256) k_swiglu(const BEnv e, const float* part, int M, int NC) {
+  const int c = blockIdx.y;
+  const int sid = e.bs[c / (NC / e.nb)].sid;
+  if (stream_done(e, sid)) return;
+  for (int m = blockIdx.x * blockDim.x + threadIdx.x; m < M; m += gridDim.x * blockDim.x) {
+    const float a = ldcg(part + static_cast<size_t>(c) * M + m);
+    const float u = ldcg(part + (static_cast<size_t>(NC) + c) * M + m);
+    store_hilo(e.pH, e.ldH, c, m, (a / (1.0f + expf(-a))) * u);
+  }
+}
+
+// =========================================================================================
+// attention
+// =========================================================================================
+
+template <typename KT>
+__device__ __forceinline__ float kvf(KT x);
+template <>
+__device__ __forceinline__ float kvf<__half>(__half x) { return __half2float(x); }
+template <>
+__device__ __forceinline__ float kvf<float>(float x) { return x; }
+template <typename KT>
+__device__ __forceinline__ KT tokv(float x);
+template <>
+__device__ __forceinline__ __half tokv<__half>(float x) { return __float2half_rn(x); }
+template <>
+__device__ __forceinline__ float tokv<float>(float x) { return x; }
+
+// per-head RMSNorm (weight [hd]) then RoPE on adjacent pairs, in place on v[0..HD) by 128 threads
+// of one head group (helpers run by the whole CTA with head h = thread / (HD/2) pairs)
+template <int HD>
+__device__ void norm_rope_heads(float* v, int nheads, const void* nw, bool norm, int esz, float eps,
+                                const float2* rope_row, float* red) {
+  // v: [nheads][HD] in shared memory; thread t handles pair (h, i) for t < nheads*HD/2
+  const int tid = threadIdx.x;
+  constexpr int P = HD / 2;
+  __syncthreads();
+  if (norm) {
+    // sum of squares per head: one warp per head
+    const int w = tid >> 5, lane = tid & 31;
+    for (int h = w; h < nheads; h += blockDim.x >> 5) {
+      float s = 0.f;
+      for (int i = lane; i < HD; i += 32) s += v[h * HD + i] * v[h * HD + i];
+      s = warp_sum(s);
+      if (lane == 0) red[h] = 1.0f / sqrtf(s / static_cast<float>(HD) + eps);
+    }
+    __syncthreads();
+  }
+  for (int t = tid; t < nheads * P; t += blockDim.x) {
+    const int h = t / P, i = t % P;
+    float a = v[h * HD + 2 * i], bb = v[h * HD + 2 * i + 1];
+    if (norm) {
+      a = (a * red[h]) * wload(nw, 2 * i, esz);
+      bb = (bb * red[h]) * wload(nw, 2 * i + 1, esz);
+    }
+    const float2 cs = rope_row[i];
+    v[h * HD + 2 * i] = a * cs.x - bb * cs.y;
+    v[h * HD + 2 * i + 1] = a * cs.y + bb * cs.x;
+  }
+  __syncthreads();
+}
+
+// Slow-AR: item (stream b, KV head g, split s) over its range of slots; the item whose range
+// holds the new slot normalises, rotates and stores the new K/V first.
+template <int HD, typename KT>
+__global__ void __launch_bounds__(256) k_attn_slow(const BEnv e, int layer, const void* qn, const void* kn,
+                                                   const float* part, int splits, int ns, float scale) {
+  constexpr int G = 4;  // query heads per KV head
+  __shared__ float q[G][HD];
+  __shared__ float kn_new[HD], vn_new[HD];
+  __shared__ __align__(16) KT ks[2][kAttnTile][HD];
+  __shared__ __align__(16) KT vs[2][kAttnTile][HD];
+  __shared__ float sc[G][kAttnTile];
+  __shared__ float corr[G], mrun[G], lrun[G], red[8];
+  const Dims& d = e.d;
+  const int it = blockIdx.x;
+  const int s = it % ns, g = (it / ns) % d.Hkv, b = it / (ns * d.Hkv);
+  const int sid = e.bs[b].sid;
+  float* outp = e.apart + static_cast<size_t>(it) * G * (HD + 2);
+  const int tid = threadIdx.x;
+  if (stream_done(e, sid)) return;
+  const int pos = ldcgi(&e.st[sid].pos);
+  const int n = pos + 1;
+  // the stream's own split count (a function of its context only, so that a stream's result does
+  // not depend on the other streams of the batch); items beyond it stay empty
+  const int nsb = min(ns, (n + kAttnChunk - 1) / kAttnChunk);
+  const int chunk = (n + nsb - 1) / nsb;
+  const int s0 = s * chunk, s1 = s < nsb ? min(n, s0 + chunk) : s0;
+  if (s0 >= s1) {
+    if (tid < G) {
+      outp[G * HD + tid] = -INFINITY;
+      outp[G * HD + G + tid] = 0.f;
+    }
+    return;
+  }
+  const int QKV = (d.Hq + 2 * d.Hkv) * HD;
+  const int NC = e.nb;
+  auto col = [&](int r) {
+    float a = 0.f;
+    for (int sp = 0; sp < splits; ++sp) a += ldcg(part + (static_cast<size_t>(sp) * NC + b) * QKV + r);
+    return a;
+  };
+  for (int t = tid; t < G * HD; t += blockDim.x) q[t / HD][t % HD] = col((g * G) * HD + t);
+  const bool has_new = pos >= s0 && pos < s1;
+  if (has_new)
+    for (int t = tid; t < HD; t += blockDim.x) {
+      kn_new[t] = col(d.Hq * HD + g * HD + t);
+      vn_new[t] = col((d.Hq + d.Hkv) * HD + g * HD + t);
+    }
+  const float2* rrow = e.rope + static_cast<size_t>(pos) * (HD / 2);
+  norm_rope_heads<HD>(&q[0][0], G, qn, d.qk_norm != 0, d.esz, d.eps, rrow, red);
+  const size_t slots = static_cast<size_t>(e.kv_slots);
+  const size_t base = ((static_cast<size_t>(layer) * e.max_streams + sid) * d.Hkv + g) * slots * HD;
+  KT* Kc = reinterpret_cast<KT*>(e.kc) + base;
+  KT* Vc = reinterpret_cast<KT*>(e.vc) + base;
+  if (has_new) {
+    norm_rope_heads<HD>(kn_new, 1, kn, d.qk_norm != 0, d.esz, d.eps, rrow, red);
+    for (int t = tid; t < HD; t += blockDim.x) {
+      const KT kq = tokv<KT>(kn_new[t]), vq = tokv<KT>(vn_new[t]);
+      Kc[static_cast<size_t>(pos) * HD + t] = kq;
+      Vc[static_cast<size_t>(pos) * HD + t] = vq;
+      kn_new[t] = kvf<KT>(kq);
+      vn_new[t] = kvf<KT>(vq);
+    }
+  }
+  for (int t = tid; t < G * HD; t += blockDim.x) q[t / HD][t % HD] *= scale;
+  if (tid < G) {
+    mrun[tid] = -INFINITY;
+    lrun[tid] = 0.f;
+  }
+  // P·V: thread t owns head t / 64 and HD / 64 consecutive output elements
+  constexpr int EPT = HD / 64;
+  const int oh = tid >> 6, oe = (tid & 63) * EPT;
+  float o[EPT];
+#pragma unroll
+  for (int i = 0; i < EPT; ++i) o[i] = 0.f;
+  constexpr int CPR = HD * static_cast<int>(sizeof(KT)) / 16;  // 16-byte chunks per row
+  auto stage = [&](int buf, int t0) {
+    const int rows = min(kAttnTile, s1 - t0);
+    for (int i = tid; i < rows * CPR; i += blockDim.x) {
+      const int r = i / CPR, cc = i % CPR;
+      cp_async16(reinterpret_cast<unsigned char*>(&ks[buf][r][0]) + cc * 16,
+                 reinterpret_cast<const unsigned char*>(Kc + static_cast<size_t>(t0 + r) * HD) + cc * 16);
+      cp_async16(reinterpret_cast<unsigned char*>(&vs[buf][r][0]) + cc * 16,
+                 reinterpret_cast<const unsigned char*>(Vc + static_cast<size_t>(t0 + r) * HD) + cc * 16);
+    }
+    cp_async_commit();
+  };
+  __syncthreads();
+  stage(0, s0);
+  int buf = 0;
+  for (int t0 = s0; t0 < s1; t0 += kAttnTile, buf ^= 1) {
+    const int rows = min(kAttnTile, s1 - t0);
+    if (t0 + kAttnTile < s1) {
+      stage(buf ^ 1, t0 + kAttnTile);
+      cp_async_wait_group<1>();
+    } else {
+      cp_async_wait_group<0>();
+    }
+    __syncthreads();
+    // scores: pair (head, slot) by two adjacent threads, one half of the head dimension each
+    {
+      const int pr = tid >> 1, half = tid & 1;
+      const int h = pr >> 5, sl = pr & 31;
+      float a = 0.f;
+      if (sl < rows) {
+        const bool fresh = has_new && t0 + sl == pos;
+#pragma unroll 8
+        for (int i = 0; i < HD / 2; ++i) {
+          const int k = half * (HD / 2) + i;
+          a = fmaf(q[h][k], fresh ? kn_new[k] : kvf<KT>(ks[buf][sl][k]), a);
+        }
+      }
+      a += __shfl_xor_sync(0xffffffffu, a, 1);
+      if (half == 0) sc[h][sl] = sl < rows ? a : -INFINITY;
+    }
+    __syncthreads();
+    // online softmax: warp h updates head h's running max and sum
+    if (tid < 32 * G) {
+      const int h = tid >> 5, lane = tid & 31;
+      const float v = sc[h][lane];
+      const float mo = mrun[h];
+      const float mn = fmaxf(mo, warp_max(v));
+      const float pv = v == -INFINITY ? 0.f : expf(v - mn);
+      const float ps = warp_sum(pv);
+      sc[h][lane] = pv;
+      if (lane == 0) {
+        const float cf = mo == -INFINITY ? 0.f : expf(mo - mn);
+        corr[h] = cf;
+        lrun[h] = lrun[h] * cf + ps;
+        mrun[h] = mn;
+      }
+    }
+    __syncthreads();
+    {
+      const float cf = corr[oh];
+#pragma unroll
+      for (int i = 0; i < EPT; ++i) o[i] *= cf;
+      for (int sl = 0; sl < rows; ++sl) {
+        const float pv = sc[oh][sl];
+        const bool fresh = has_new && t0 + sl == pos;
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) o[i] = fmaf(pv, fresh ? vn_new[oe + i] : kvf<KT>(vs[buf][sl][oe + i]), o[i]);
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < EPT; ++i) outp[oh * HD + oe + i] = o[i];
+  if (tid < G) {
+    outp[G * HD + tid] = mrun[tid];
+    outp[G * HD + G + tid] = lrun[tid];
+  }
+}
+
+// combine the splits of each (stream, KV head): o = Σ_s e^{m_s - M} o_s / Σ_s e^{m_s - M} l_s,
+// written as the planes of the out-projection input (query head h at columns h*HD..)
+template <int HD>
+__global__ void __launch_bounds__(256) k_attn_comb(const BEnv e, int ns) {
+  constexpr int G = 4;
+  const Dims& d = e.d;
+  const int b = blockIdx.x / d.Hkv, g = blockIdx.x % d.Hkv;
+  if (stream_done(e, e.bs[b].sid)) return;
+  const float* base = e.apart + static_cast<size_t>(blockIdx.x) * ns * G * (HD + 2);
+  for (int t = threadIdx.x; t < G * HD; t += blockDim.x) {
+    const int h = t / HD;
+    float M = -INFINITY;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, ldcg(base + static_cast<size_t>(s) * G * (HD + 2) + G * HD + h));
+    float num = 0.f, den = 0.f;
+    for (int s = 0; s < ns; ++s) {
+      const float* ps = base + static_cast<size_t>(s) * G * (HD + 2);
+      const float m = ldcg(ps + G * HD + h);
+      if (m == -INFINITY) continue;
+      const float w = expf(m - M);
+      num = fmaf(w, ldcg(ps + t), num);
+      den = fmaf(w, ldcg(ps + G * HD + G + h), den);
+    }
+    store_hilo(e.pO, e.ldO, b, (g * G + h) * HD + (t % HD), num / den);
+  }
+}
+
+// Fast-AR: per (stream, KV head), the call's new positions in order: q/k norm, RoPE at the
+// position, K/V into the stream's window, attention over positions 0..p (ch.06 §1-§4).
+template <int HD>
+__global__ void __launch_bounds__(256) k_attn_fast(const BEnv e, int layer, const void* qn, const void* kn,
+                                                   const float* part, int splits, int npos, int pos0, float scale) {
+  constexpr int G = 4;
+  constexpr int WMAX = 16;
+  __shared__ float q[G][HD];
+  __shared__ float kv[2][HD];
+  __shared__ float sc[G][WMAX];
+  __shared__ float red[8];
+  const Dims& d = e.d;
+  const int b = blockIdx.x / d.Hkvf, g = blockIdx.x % d.Hkvf;
+  const int sid = e.bs[b].sid;
+  if (stream_done(e, sid)) return;
+  const int tid = threadIdx.x;
+  const int QKV = (d.Hqf + 2 * d.Hkvf) * HD;
+  const int NC = e.nb * npos;
+  const size_t wl = static_cast<size_t>(d.Wf) * d.Hkvf * HD;  // one layer of the window
+  float* Kw = e.bfk + (static_cast<size_t>(b) * d.Lf + layer) * wl;
+  float* Vw = e.bfv + (static_cast<size_t>(b) * d.Lf + layer) * wl;
+  for (int j = 0; j < npos; ++j) {
+    const int c = b * npos + j, p = pos0 + j;
+    auto col = [&](int r) {
+      float a = 0.f;
+      for (int sp = 0; sp < splits; ++sp) a += ldcg(part + (static_cast<size_t>(sp) * NC + c) * QKV + r);
+      return a;
+    };
+    __syncthreads();
+    for (int t = tid; t < G * HD; t += blockDim.x) q[t / HD][t % HD] = col((g * G) * HD + t);
+    for (int t = tid; t < HD; t += blockDim.x) {
+      kv[0][t] = col(d.Hqf * HD + g * HD + t);
+      kv[1][t] = col((d.Hqf + d.Hkvf) * HD + g * HD + t);
+    }
+    const float2* rrow = e.rope_f + static_cast<size_t>(p) * (HD / 2);
+    norm_rope_heads<HD>(&q[0][0], G, qn, d.qk_norm != 0, d.esz, d.eps, rrow, red);
+    norm_rope_heads<HD>(&kv[0][0], 1, kn, d.qk_norm != 0, d.esz, d.eps, rrow, red);
+    for (int t = tid; t < HD; t += blockDim.x) {
+      Kw[(static_cast<size_t>(p) * d.Hkvf + g) * HD + t] = kv[0][t];
+      Vw[(static_cast<size_t>(p) * d.Hkvf + g) * HD + t] = kv[1][t];
+    }
+    __threadfence_block();
+    __syncthreads();
+    // scores of the G heads over positions 0..p: one warp per (head, position)
+    const int w = tid >> 5, lane = tid & 31;
+    for (int hp = w; hp < G * (p + 1); hp += blockDim.x >> 5) {
+      const int h = hp / (p + 1), t = hp % (p + 1);
+      const float* kr = Kw + (static_cast<size_t>(t) * d.Hkvf + g) * HD;
+      float a = 0.f;
+      for (int k = lane; k < HD; k += 32) a = fmaf(q[h][k], t == p ? kv[0][k] : kr[k], a);
+      a = warp_sum(a);
+      if (lane == 0) sc[h][t] = a * scale;
+    }
+    __syncthreads();
+    if (tid < G) {
+      float m = -INFINITY;
+      for (int t = 0; t <= p; ++t) m = fmaxf(m, sc[tid][t]);
+      float l = 0.f;
+      for (int t = 0; t <= p; ++t) {
+        sc[tid][t] = expf(sc[tid][t] - m);
+        l += sc[tid][t];
+      }
+      red[tid] = 1.0f / l;
+    }
+    __syncthreads();
+    for (int t2 = tid; t2 < G * HD; t2 += blockDim.x) {
+      const int h = t2 / HD, k = t2 % HD;
+      float a = 0.f;
+      for (int t = 0; t <= p; ++t) a = fmaf(sc[h][t], t == p ? kv[1][k] : Vw[(static_cast<size_t>(t) * d.Hkvf + g) * HD + k], a);
+      store_hilo(e.pO, e.ldO, c, (g * G + h) * HD + k, a * red[h]);
+    }
+  }
+}
+
+// =========================================================================================
+// draws and bookkeeping (one CTA of 256 threads per stream)
+// =========================================================================================
+
+__device__ void copy_row(float* dst, const float* src, int n) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = ldcg(src + i);
+}
+
+__device__ __forceinline__ int checked(const BEnv& e, int v, int hi) {
+  if (v < 0 || v >= hi) {
+    atomicCAS(&e.ctl->error, 0, S2_EINVAL);
+    return 0;
+  }
+  return v;
+}
+
+// main draw, repetition-aware redraw, clamp, stop (ch.06 §5, §6); then the planes of the stream's
+// hidden state for fast_project_in
+__global__ void __launch_bounds__(kConsumers) k_samp_main(const BEnv e) {
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  SampScratch& W = *reinterpret_cast<SampScratch*>(smraw);
+  __shared__ int flag;
+  const Dims& d = e.d;
+  const int b = blockIdx.x;
+  const BStream& bs = e.bs[b];
+  const int sid = bs.sid;
+  StreamState* st = e.st + sid;
+  if (stream_done(e, sid)) return;
+  const int f = frame_index(e);
+  const float* lg = e.logits + static_cast<size_t>(sid) * e.lstride;
+  const float* hid = e.hidden + static_cast<size_t>(sid) * d.D;
+  if (bs.dbg_main) copy_row(bs.dbg_main + static_cast<size_t>(f) * d.A, lg, d.A);
+  if (bs.dbg_hidden) copy_row(bs.dbg_hidden + static_cast<size_t>(f) * d.D, hid, d.D);
+  const int fd = ldcgi(&st->frames_done);
+  const float* E = bs.expo + static_cast<size_t>(f) * kDraws * kTopK;
+  const bool block_end = fd < bs.min_tokens;
+  int d0 = draw(d, W, lg, d.A, true, block_end, bs.T, bs.top_p, E);
+  if (threadIdx.x == 0) {
+    if (bs.dbg_draws) bs.dbg_draws[f * kDraws + 0] = d0;
+    if (bs.forced) {
+      d0 = bs.forced[f * kDraws + 0];
+      if (d0 < 0 || d0 >= d.V) {
+        atomicCAS(&e.ctl->error, 0, S2_EINVAL);
+        d0 = d.im_end;
+      }
+    }
+    flag = d0;
+  }
+  __syncthreads();
+  d0 = flag;
+  __syncthreads();
+  if (d0 == d.im_end || d0 < 0) {
+    if (threadIdx.x == 0) {
+      st->done = 1;
+      st->n_out = f;
+      if (bs.dbg_draws)
+        for (int k = 1; k < kDraws; ++k) bs.dbg_draws[f * kDraws + k] = -1;
+    }
+    return;
+  }
+  int d1 = draw(d, W, lg, d.A, true, block_end, bs.ras_T, bs.ras_top_p, E + kTopK);
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    if (lane == 0) {
+      if (bs.dbg_draws) bs.dbg_draws[f * kDraws + 1] = d1;
+      if (bs.forced) d1 = checked(e, bs.forced[f * kDraws + 1], d.V);
+      if (d1 < 0) d1 = d0;
+    }
+    d1 = __shfl_sync(0xffffffffu, d1, 0);
+    const int wl = ldcgi(&st->wlen);
+    const int wv = lane < wl ? ldcgi(&st->window[lane]) : -1;
+    const bool seen = __any_sync(0xffffffffu, lane < wl && wv == d0);
+    const bool trig = seen && d0 >= d.sem_lo && d0 <= d.sem_hi;
+    const int tok = trig ? d1 : d0;
+    if (wl < bs.ras_window) {
+      if (lane == 0) {
+        st->window[wl] = tok;
+        st->wlen = wl + 1;
+      }
+    } else {
+      if (lane >= 1 && lane < wl) st->window[lane - 1] = wv;
+      if (lane == 0) st->window[wl - 1] = tok;
+    }
+    if (lane == 0) {
+      int code0 = tok - d.sem_lo;
+      code0 = code0 < 0 ? 0 : (code0 > d.cbs - 1 ? d.cbs - 1 : code0);
+      st->vals[0] = tok;
+      st->vals[1] = code0;
+      e.bfcode[b * 16 + 0] = code0;
+      e.stage[(static_cast<size_t>(sid) * kMaxFramesPerCall + f) * d.ncb + 0] = code0;
+      st->frames_done = fd + 1;
+    }
+  }
+  for (int k = threadIdx.x; k < d.D; k += blockDim.x) store_hilo(e.pX, e.ldX, b, k, ldcg(hid + k));
+}
+
+// one Fast-AR draw (codebook cb) from the summed fast_output partials; then the next call's new
+// input row (fast_embeddings[code], normalised with the first Fast-AR layer's attention norm),
+// or after the last codebook the Slow-AR input embedding of the frame (normalised likewise)
+__global__ void __launch_bounds__(kConsumers) k_samp_fast(const BEnv e, int cb, const float* part, int splits,
+                                                          const void* an_fast0, const void* an_slow0) {
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  SampScratch& W = *reinterpret_cast<SampScratch*>(smraw);
+  __shared__ int flag;
+  __shared__ float red[kPrepThreads / 32];
+  const Dims& d = e.d;
+  const int b = blockIdx.x;
+  const BStream& bs = e.bs[b];
+  const int sid = bs.sid;
+  StreamState* st = e.st + sid;
+  if (stream_done(e, sid)) return;
+  const int f = frame_index(e);
+  float* fl = e.bflog + static_cast<size_t>(b) * d.cbs;
+  const int NC = e.nb;
+  for (int i = threadIdx.x; i < d.cbs; i += blockDim.x) {
+    float a = 0.f;
+    for (int s = 0; s < splits; ++s) a += ldcg(part + (static_cast<size_t>(s) * NC + b) * d.cbs + i);
+    fl[i] = a;
+  }
+  __threadfence_block();
+  __syncthreads();
+  if (bs.dbg_fast) copy_row(bs.dbg_fast + (static_cast<size_t>(f) * (d.ncb - 1) + (cb - 1)) * d.cbs, fl, d.cbs);
+  const float* E = bs.expo + static_cast<size_t>(f) * kDraws * kTopK + (1 + cb) * kTopK;
+  int dc = draw(d, W, fl, d.cbs, false, false, bs.T, bs.top_p, E);
+  if (threadIdx.x == 0) {
+    if (bs.dbg_draws) bs.dbg_draws[f * kDraws + 1 + cb] = dc;
+    if (bs.forced) dc = checked(e, bs.forced[f * kDraws + 1 + cb], d.cbs);
+    if (dc < 0) dc = 0;
+    e.bfcode[b * 16 + cb] = dc;
+    st->vals[1 + cb] = dc;
+    e.stage[(static_cast<size_t>(sid) * kMaxFramesPerCall + f) * d.ncb + cb] = dc;
+    if (cb == d.ncb - 1) st->n_out = f + 1;
+    flag = dc;
+  }
+  __syncthreads();
+  dc = flag;
+  // next input row, normalised, as planes at column b
+  const bool slow = cb == d.ncb - 1;
+  const int K = slow ? d.D : d.Df;
+  const void* nw = slow ? an_slow0 : an_fast0;
+  float* xr = slow ? e.bx + static_cast<size_t>(b) * d.D : e.bfx + static_cast<size_t>(b) * 2 * d.Df;
+  int tok = 0;
+  float msem = 0.f;
+  if (slow) {
+    tok = ldcgi(&st->vals[0]);
+    msem = (tok >= d.sem_lo && tok <= d.sem_hi) ? 1.f : 0.f;
+  }
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    float a;
+    if (slow) {
+      float acc = 0.f;
+      for (int c2 = 0; c2 < d.ncb; ++c2) {
+        const int code = c2 == cb ? dc : ldcgi(&st->vals[1 + c2]);
+        acc = __fadd_rn(acc, wload(e.CE, (static_cast<size_t>(c2) * d.cbs + code) * K + k, d.esz));
+      }
+      a = __fadd_rn(__fmul_rn(d.sem_scale, wload(e.E, static_cast<size_t>(tok) * K + k, d.esz)), __fmul_rn(msem, acc));
+    } else {
+      a = wload(e.FE, static_cast<size_t>(dc) * K + k, d.esz);
+    }
+    xr[k] = a;
+    ss += a * a;
+  }
+  const float r = 1.0f / sqrtf(block_sum256(ss, red) / static_cast<float>(K) + d.eps);
+  for (int k = threadIdx.x; k < K; k += blockDim.x) store_hilo(e.pX, e.ldX, b, k, (ldcg(xr + k) * r) * wload(nw, k, d.esz));
+}
+
+// admissible Slow-AR logits of the step: the semantic rows from the partials, im_end by one dot
+// product with the normalised hidden state; then the stream position advances
+__global__ void __launch_bounds__(256) k_logits_fin(const BEnv e, const float* part, int splits) {
+  __shared__ float red[8];
+  const Dims& d = e.d;
+  const int b = blockIdx.x;
+  const int sid = e.bs[b].sid;
+  if (stream_done(e, sid)) return;
+  float* lg = e.logits + static_cast<size_t>(sid) * e.lstride;
+  const int NC = e.nb;
+  for (int i = threadIdx.x; i < d.cbs; i += blockDim.x) {
+    float a = 0.f;
+    for (int s = 0; s < splits; ++s) a += ldcg(part + (static_cast<size_t>(s) * NC + b) * d.cbs + i);
+    lg[i] = a;
+  }
+  const float* h = e.hidden + static_cast<size_t>(sid) * d.D;
+  float a = 0.f;
+  for (int k = threadIdx.x; k < d.D; k += blockDim.x)
+    a = fmaf(wload(e.E, static_cast<size_t>(d.im_end) * d.D + k, d.esz), ldcg(h + k), a);
+  a = block_sum256(a, red);
+  if (threadIdx.x == 0) {
+    lg[d.cbs] = a;
+    e.st[sid].pos = ldcgi(&e.st[sid].pos) + 1;
+  }
+}
+
+__global__ void k_call_start(const BEnv e) {
+  const int b = threadIdx.x;
+  if (b < e.nb) e.st[e.bs[b].sid].n_out = 0;
+  if (b == 0) e.bctl[0] = 0;
+}
+
+__global__ void k_frame_end(const BEnv e) {
+  if (threadIdx.x == 0) e.bctl[0] = e.bctl[0] + 1;
+}
+
+}  // namespace
+
+// =========================================================================================
+// host side
+// =========================================================================================
+
+namespace {
+
+constexpr int kPrepMaxK = 12 * kPrepThreads;
+
+int round16(int v) { return (v + 15) / 16 * 16; }
+
+struct GemvPlan {
+  int tiles, splits, per, atoms, nmat, M, K;
+};
+
+GemvPlan plan_gemv(int M, int K, int nmat, int sms, bool whole_k) {
+  GemvPlan g{};
+  g.M = M;
+  g.K = K;
+  g.nmat = nmat;
+  g.atoms = K / kAtom;
+  g.tiles = (M + kTileM - 1) / kTileM;
+  int splits = whole_k ? 1 : std::max(1, std::min(g.atoms, sms / std::max(1, g.tiles * nmat)));
+  g.per = (g.atoms + splits - 1) / splits;
+  g.splits = (g.atoms + g.per - 1) / g.per;
+  return g;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over rows of `inner` elements (row pitch ld elements), box {64, box_rows},
+// 128-byte swizzle
+bool encode_map(CUtensorMap* m, const void* base, int inner, long long rows, int ld, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kAtom), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// items per (stream, KV head) in the grid: enough for the longest context of the call
+int attn_splits(int max_ctx) {
+  return std::max(1, std::min(kMaxSplitsAttn, (max_ctx + kAttnChunk - 1) / kAttnChunk));
+}
+
+}  // namespace
+
+struct Batch {
+  BatchModel m;
+  std::map<const void*, CUtensorMap> wmaps;
+  std::map<std::tuple<const void*, int, int>, CUtensorMap> pmaps;
+  BatchSizes sz{};
+  std::vector<BStream> host_bs;
+  cudaStream_t cap = nullptr;   // private stream the frame is captured on
+};
+
+bool batch_supported(const Dims& d, int max_streams, std::string* why) {
+  auto no = [&](const char* w) {
+    if (why) *why = w;
+    return false;
+  };
+  if (d.wdt != S2_BF16 || d.kvdt != S2_F16) return no("batched decode needs bf16 weights and an fp16 KV cache");
+  if (d.L == 0) return no("no Slow-AR");
+  if (max_streams < 2 || max_streams > 64) return no("batched decode serves 2..64 streams per context");
+  if (d.hd != 128 && d.hd != 64) return no("head_dim must be 64 or 128");
+  if (d.Hq != 4 * d.Hkv || d.Hqf != 4 * d.Hkvf) return no("batched attention assumes 4 query heads per KV head");
+  const int ks[6] = {d.D, d.Df, d.F, d.Ff, d.Hq * d.hd, d.Hqf * d.hdf};
+  for (int k : ks)
+    if (k % kAtom != 0) return no("projection lengths must be multiples of 64");
+  if (d.D > kPrepMaxK || d.Df > kPrepMaxK) return no("model width above the column-preparation limit");
+  if (d.Wf > 16) return no("Fast-AR window above 16");
+  return true;
+}
+
+BatchSizes batch_sizes(const Dims& d, int max_streams, int sms) {
+  BatchSizes z{};
+  const int ncmax = 2 * max_streams;
+  z.planes_rows = static_cast<size_t>(round16(2 * ncmax));
+  z.ldX = std::max(d.D, d.Df);
+  z.ldO = std::max(d.Hq * d.hd, d.Hqf * d.hdf);
+  z.ldH = std::max(d.F, d.Ff);
+  const int QKV = (d.Hq + 2 * d.Hkv) * d.hd, QKVf = (d.Hqf + 2 * d.Hkvf) * d.hdf;
+  size_t mx = 0;
+  auto acc = [&](int M, int K, int nmat, bool whole, int nc) {
+    const GemvPlan g = plan_gemv(M, K, nmat, sms, whole);
+    mx = std::max(mx, static_cast<size_t>(g.nmat) * g.splits * nc * M);
+  };
+  acc(QKV, d.D, 1, false, max_streams);
+  acc(d.D, d.Hq * d.hd, 1, false, max_streams);
+  acc(d.F, d.D, 2, true, max_streams);
+  acc(d.D, d.F, 1, false, max_streams);
+  acc(d.cbs, d.D, 1, false, max_streams);
+  acc(d.Df, d.D, 1, false, max_streams);
+  acc(d.cbs, d.Df, 1, false, max_streams);
+  acc(QKVf, d.Df, 1, false, ncmax);
+  acc(d.Df, d.Hqf * d.hdf, 1, false, ncmax);
+  acc(d.Ff, d.Df, 2, true, ncmax);
+  acc(d.Df, d.Ff, 1, false, ncmax);
+  z.part_floats = mx;
+  z.apart_floats = static_cast<size_t>(max_streams) * d.Hkv * kMaxSplitsAttn * 4 * (d.hd + 2);
+  return z;
+}
+
+size_t batch_stream_bytes(int max_streams) { return sizeof(BStream) * static_cast<size_t>(max_streams); }
+
+Batch* batch_create(const BatchModel& m, std::string* err) {
+  if (!encode_fn()) {
+    *err = "cuTensorMapEncodeTiled is not available from the driver";
+    return nullptr;
+  }
+  Batch* b = new Batch();
+  b->m = m;
+  b->sz = batch_sizes(m.d, m.max_streams, m.sms);
+  const Dims& d = m.d;
+  auto add = [&](const void* w, int rows, int cols) {
+    CUtensorMap t;
+    if (!encode_map(&t, w, cols, rows, cols, kTileM)) return false;
+    b->wmaps[w] = t;
+    return true;
+  };
+  bool ok = add(m.E, d.V, d.D) && add(m.FO, d.cbs, d.Df) && (!m.P || add(m.P, d.Df, d.D));
+  const int QKV = (d.Hq + 2 * d.Hkv) * d.hd, QKVf = (d.Hqf + 2 * d.Hkvf) * d.hdf;
+  for (int l = 0; l < d.L && ok; ++l) {
+    const LayerW& w = m.slow[l];
+    ok = add(w.wqkv, QKV, d.D) && add(w.wo, d.D, d.Hq * d.hd) && add(w.w1, d.F, d.D) && add(w.w3, d.F, d.D) &&
+         add(w.w2, d.D, d.F);
+  }
+  for (int l = 0; l < d.Lf && ok; ++l) {
+    const LayerW& w = m.fast[l];
+    ok = add(w.wqkv, QKVf, d.Df) && add(w.wo, d.Df, d.Hqf * d.hdf) && add(w.w1, d.Ff, d.Df) &&
+         add(w.w3, d.Ff, d.Df) && add(w.w2, d.Df, d.Ff);
+  }
+  if (!ok) {
+    *err = "encoding a weight tensor map failed";
+    delete b;
+    return nullptr;
+  }
+  if (cudaStreamCreateWithFlags(&b->cap, cudaStreamNonBlocking) != cudaSuccess) {
+    *err = "creating the capture stream failed";
+    delete b;
+    return nullptr;
+  }
+  const int gsmem = kGemvSmemBudget + 1024 + static_cast<int>(sizeof(GemvBars));
+  if (cudaFuncSetAttribute(k_bgemv, cudaFuncAttributeMaxDynamicSharedMemorySize, gsmem) != cudaSuccess) {
+    *err = "setting the projection kernel's shared memory failed";
+    delete b;
+    return nullptr;
+  }
+  return b;
+}
+
+void batch_destroy(Batch* b) {
+  if (b && b->cap) cudaStreamDestroy(b->cap);
+  delete b;
+}
+
+namespace {
+
+struct Frame {
+  Batch* b;
+  BEnv e;
+  cudaStream_t s;
+  int nb;
+  int ns;
+  bool ok = true;
+
+  const CUtensorMap& planes(uint16_t* buf, int N, int K, int ld) {
+    auto key = std::make_tuple(static_cast<const void*>(buf), N, K);
+    auto it = b->pmaps.find(key);
+    if (it != b->pmaps.end()) return it->second;
+    CUtensorMap t;
+    if (!encode_map(&t, buf, K, N, ld, N)) ok = false;
+    return b->pmaps[key] = t;
+  }
+
+  // projection of NC columns; returns the plan (partials layout)
+  GemvPlan gemv(const void* w0, const void* w1, int M, int K, int row0, uint16_t* pl, int ld, int NC, bool whole_k) {
+    const GemvPlan g = plan_gemv(M, K, w1 ? 2 : 1, b->m.sms, whole_k);
+    const int N = round16(2 * NC);
+    const CUtensorMap& ta = b->wmaps.at(w0);
+    const CUtensorMap& ta2 = w1 ? b->wmaps.at(w1) : ta;
+    const CUtensorMap& tb = planes(pl, N, K, ld);
+    const int sbytes = kABytes + N * 128;
+    const int nst = std::min(kMaxGemvStages, kGemvSmemBudget / sbytes);
+    const int smem = nst * sbytes + 1024 + static_cast<int>(sizeof(GemvBars));
+    dim3 grid(g.tiles, g.splits, g.nmat);
+    k_bgemv<<<grid, kGemvThreads, smem, s>>>(ta, ta2, tb, M, row0, N, NC, g.atoms, g.per, nst, e.part, e.ctl);
+    return g;
+  }
+
+  void colprep(const ColPrep& p, int NC) { k_colprep<<<NC, kPrepThreads, 0, s>>>(e, p); }
+
+  void run() {
+    const Dims& d = e.d;
+    const BatchModel& m = b->m;
+    const size_t samp = sizeof(SampScratch);
+    k_samp_main<<<nb, kConsumers, samp, s>>>(e);
+    // Fast-AR call 1: positions 0 (projected hidden) and 1 (fast_embeddings[code_0])
+    {
+      ColPrep p{};
+      p.npos = 2;
+      p.K = d.Df;
+      p.x = e.bfx;
+      p.xb = 2 * d.Df;
+      p.normw = m.fast[0].an;
+      p.code_idx = 0;
+      p.mode[1] = CM_FEROW;
+      if (m.P) {
+        const GemvPlan g = gemv(m.P, nullptr, d.Df, d.D, 0, e.pX, e.ldX, nb, false);
+        p.mode[0] = CM_STORE;
+        p.part = e.part;
+        p.splits = g.splits;
+        p.part_nc = nb;
+        p.part_by_stream = 1;
+      } else {
+        p.mode[0] = CM_HIDDEN;
+      }
+      colprep(p, 2 * nb);
+    }
+    const float fscale = 1.0f / std::sqrt(static_cast<float>(d.hdf));
+    const int QKVf = (d.Hqf + 2 * d.Hkvf) * d.hdf;
+    for (int cb = 1; cb < d.ncb; ++cb) {
+      const int npos = cb == 1 ? 2 : 1, pos0 = cb == 1 ? 0 : cb, NC = nb * npos;
+      for (int l = 0; l < d.Lf; ++l) {
+        const LayerW& w = m.fast[l];
+        GemvPlan g = gemv(w.wqkv, nullptr, QKVf, d.Df, 0, e.pX, e.ldX, NC, false);
+        if (d.hdf == 128)
+          k_attn_fast<128><<<nb * d.Hkvf, 256, 0, s>>>(e, l, w.qn, w.kn, e.part, g.splits, npos, pos0, fscale);
+        else
+          k_attn_fast<64><<<nb * d.Hkvf, 256, 0, s>>>(e, l, w.qn, w.kn, e.part, g.splits, npos, pos0, fscale);
+        g = gemv(w.wo, nullptr, d.Df, d.Hqf * d.hdf, 0, e.pO, e.ldO, NC, false);
+        ColPrep p{};
+        p.npos = npos;
+        p.mode[0] = p.mode[1] = CM_RESID;
+        p.K = d.Df;
+        p.part = e.part;
+        p.splits = g.splits;
+        p.part_nc = NC;
+        p.x = e.bfx;
+        p.xb = 2 * d.Df;
+        p.normw = w.fn;
+        colprep(p, NC);
+        gemv(w.w1, w.w3, d.Ff, d.Df, 0, e.pX, e.ldX, NC, true);
+        k_swiglu<<<dim3((d.Ff + 255) / 256, NC), 256, 0, s>>>(e, e.part, d.Ff, NC);
+        g = gemv(w.w2, nullptr, d.Df, d.Ff, 0, e.pH, e.ldH, NC, false);
+        p.splits = g.splits;
+        const bool last = l == d.Lf - 1;
+        p.normw = last ? m.fnorm : m.fast[l + 1].an;
+        p.last_only = last ? 1 : 0;
+        colprep(p, NC);
+      }
+      const GemvPlan g = gemv(m.FO, nullptr, d.cbs, d.Df, 0, e.pX, e.ldX, nb, false);
+      k_samp_fast<<<nb, kConsumers, samp, s>>>(e, cb, e.part, g.splits, m.fast[0].an, m.slow[0].an);
+    }
+    // Slow-AR step
+    const float sscale = 1.0f / std::sqrt(static_cast<float>(d.hd));
+    const int QKV = (d.Hq + 2 * d.Hkv) * d.hd;
+    for (int l = 0; l < d.L; ++l) {
+      const LayerW& w = m.slow[l];
+      GemvPlan g = gemv(w.wqkv, nullptr, QKV, d.D, 0, e.pX, e.ldX, nb, false);
+      if (d.hd == 128) {
+        k_attn_slow<128, __half><<<nb * d.Hkv * ns, 256, 0, s>>>(e, l, w.qn, w.kn, e.part, g.splits, ns, sscale);
+        k_attn_comb<128><<<nb * d.Hkv, 256, 0, s>>>(e, ns);
+      } else {
+        k_attn_slow<64, __half><<<nb * d.Hkv * ns, 256, 0, s>>>(e, l, w.qn, w.kn, e.part, g.splits, ns, sscale);
+        k_attn_comb<64><<<nb * d.Hkv, 256, 0, s>>>(e, ns);
+      }
+      g = gemv(w.wo, nullptr, d.D, d.Hq * d.hd, 0, e.pO, e.ldO, nb, false);
+      ColPrep p{};
+      p.npos = 1;
+      p.mode[0] = p.mode[1] = CM_RESID;
+      p.K = d.D;
+      p.part = e.part;
+      p.splits = g.splits;
+      p.part_nc = nb;
+      p.x = e.bx;
+      p.xb = d.D;
+      p.normw = w.fn;
+      colprep(p, nb);
+      gemv(w.w1, w.w3, d.F, d.D, 0, e.pX, e.ldX, nb, true);
+      k_swiglu<<<dim3((d.F + 255) / 256, nb), 256, 0, s>>>(e, e.part, d.F, nb);
+      g = gemv(w.w2, nullptr, d.D, d.F, 0, e.pH, e.ldH, nb, false);
+      p.splits = g.splits;
+      const bool last = l == d.L - 1;
+      p.normw = last ? m.norm : m.slow[l + 1].an;
+      p.hid_out = last ? e.hidden : nullptr;
+      colprep(p, nb);
+    }
+    const GemvPlan g = gemv(m.E, nullptr, d.cbs, d.D, d.sem_lo, e.pX, e.ldX, nb, false);
+    k_logits_fin<<<nb, 256, 0, s>>>(e, e.part, g.splits);
+    k_frame_end<<<1, 32, 0, s>>>(e);
+  }
+};
+
+}  // namespace
+
+int batch_decode(Batch* b, int n, const int* ids, int n_frames, const s2_sampling* params, const float* expo,
+                 const int32_t* forced, const s2_debug_taps* taps, int max_ctx, void* stream, std::string* err) {
+  const BatchModel& m = b->m;
+  const Dims& d = m.d;
+  if (n < 1 || n > m.max_streams) {
+    *err = "batched decode: stream count out of range";
+    return S2_EINVAL;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  b->host_bs.assign(n, BStream{});
+  for (int k = 0; k < n; ++k) {
+    BStream& t = b->host_bs[k];
+    const size_t fo = static_cast<size_t>(k) * n_frames;
+    const s2_sampling& p = params[k];
+    t.sid = ids[k];
+    t.min_tokens = p.min_tokens_before_end;
+    t.ras_window = p.ras_window;
+    t.T = p.temperature;
+    t.top_p = p.top_p;
+    t.ras_T = p.ras_temperature;
+    t.ras_top_p = p.ras_top_p;
+    t.expo = expo + fo * kDraws * kTopK;
+    t.forced = forced ? forced + fo * kDraws : nullptr;
+    if (taps) {
+      t.dbg_main = taps->main_logits ? taps->main_logits + fo * d.A : nullptr;
+      t.dbg_fast = taps->fast_logits ? taps->fast_logits + fo * (d.ncb - 1) * d.cbs : nullptr;
+      t.dbg_hidden = taps->hidden ? taps->hidden + fo * d.D : nullptr;
+      t.dbg_draws = taps->draws ? taps->draws + fo * kDraws : nullptr;
+    }
+  }
+  if (cudaMemcpyAsync(m.bstreams, b->host_bs.data(), sizeof(BStream) * n, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    *err = "copying the call settings failed";
+    return S2_ECUDA;
+  }
+  Frame fr{};
+  fr.b = b;
+  fr.s = b->cap;
+  fr.nb = n;
+  fr.ns = attn_splits(max_ctx);
+  BEnv& e = fr.e;
+  e.d = d;
+  e.nb = n;
+  e.max_streams = m.max_streams;
+  e.kv_slots = m.kv_slots;
+  e.lstride = m.lstride;
+  e.st = m.st;
+  e.bs = static_cast<const BStream*>(m.bstreams);
+  e.bctl = m.bctl;
+  e.hidden = m.hidden;
+  e.logits = m.logits;
+  e.stage = m.stage;
+  e.ctl = m.ctl;
+  e.kc = m.kc;
+  e.vc = m.vc;
+  e.rope = m.rope;
+  e.rope_f = m.rope_f;
+  e.E = m.E;
+  e.CE = m.CE;
+  e.FE = m.FE;
+  e.pX = m.pX;
+  e.pO = m.pO;
+  e.pH = m.pH;
+  e.ldX = b->sz.ldX;
+  e.ldO = b->sz.ldO;
+  e.ldH = b->sz.ldH;
+  e.part = m.part;
+  e.bx = m.bx;
+  e.bfx = m.bfx;
+  e.bfk = m.bfk;
+  e.bfv = m.bfv;
+  e.apart = m.apart;
+  e.bflog = m.bflog;
+  e.bfcode = m.bfcode;
+  k_call_start<<<1, 64, 0, s>>>(e);
+  if (cudaGetLastError() != cudaSuccess) {
+    *err = "batched call start failed";
+    return S2_ECUDA;
+  }
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  if (cudaStreamBeginCapture(b->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    *err = "graph capture could not begin";
+    return S2_ECUDA;
+  }
+  fr.run();
+  const cudaError_t ce = cudaStreamEndCapture(b->cap, &graph);
+  if (ce != cudaSuccess || !fr.ok) {
+    if (graph) cudaGraphDestroy(graph);
+    *err = std::string("capturing the frame failed: ") + (fr.ok ? cudaGetErrorString(ce) : "tensor map encoding");
+    return S2_ECUDA;
+  }
+  if (cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) {
+    cudaGraphDestroy(graph);
+    *err = "instantiating the frame graph failed";
+    return S2_ECUDA;
+  }
+  cudaError_t le = cudaSuccess;
+  for (int f = 0; f < n_frames && le == cudaSuccess; ++f) le = cudaGraphLaunch(exec, s);
+  cudaGraphExecDestroy(exec);
+  cudaGraphDestroy(graph);
+  if (le != cudaSuccess) {
+    *err = std::string("launching the frame graph failed: ") + cudaGetErrorString(le);
+    return S2_ECUDA;
+  }
+  return S2_OK;
+}
+
+}  // namespace s2

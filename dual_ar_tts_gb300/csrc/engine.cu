@@ -45,6 +45,11 @@ struct s2_ctx {
   std::vector<int> host_pos;
   std::vector<char> host_prefilled;
   std::string err;
+  // batched decode (bf16 models serving several streams)
+  bool batched = false;
+  int sms = 0;
+  BatchModel bm{};
+  Batch* batch = nullptr;
 };
 
 namespace {
@@ -191,6 +196,18 @@ int attn_items_max(const Dims& d, int grid, int slots) {
   return d.Hkv * (grid / d.Hkv + slots / kAttnMaxChunk + 2);
 }
 
+// bf16 contexts serving several streams also carry the batched-decode buffers
+void setup_batched(s2_ctx* c) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms <= 0) {
+    cudaGetLastError();
+    sms = 152;
+  }
+  c->sms = sms;
+  c->batched = batch_supported(c->d, c->max_streams, nullptr);
+}
+
 void carve(s2_ctx* c, Carver& cv) {
   const Dims& d = c->d;
   const int B = c->max_streams;
@@ -228,6 +245,24 @@ void carve(s2_ctx* c, Carver& cv) {
   c->n_dec = d.L > 0 ? 1 + fast_call_phases(d) + 5 * d.L + 1 : 0;
   c->n_fast = 2 + fast_call_phases(d);
   c->prog = cv.take<Phase>(static_cast<size_t>(B) * c->n_dec + c->n_fast);
+  if (c->batched) {
+    const BatchSizes z = batch_sizes(d, B, c->sms);
+    BatchModel& m = c->bm;
+    m.pX = cv.take<uint16_t>(z.planes_rows * z.ldX);
+    m.pO = cv.take<uint16_t>(z.planes_rows * z.ldO);
+    m.pH = cv.take<uint16_t>(z.planes_rows * z.ldH);
+    m.part = cv.take<float>(z.part_floats);
+    m.bx = cv.take<float>(static_cast<size_t>(B) * d.D);
+    m.bfx = cv.take<float>(static_cast<size_t>(B) * 2 * d.Df);
+    const size_t fw = static_cast<size_t>(B) * d.Lf * d.Wf * d.Hkvf * d.hdf;
+    m.bfk = cv.take<float>(fw);
+    m.bfv = cv.take<float>(fw);
+    m.apart = cv.take<float>(z.apart_floats);
+    m.bflog = cv.take<float>(static_cast<size_t>(B) * d.cbs);
+    m.bfcode = cv.take<int32_t>(static_cast<size_t>(B) * 16);
+    m.bctl = cv.take<int>(16);
+    m.bstreams = cv.take<unsigned char>(batch_stream_bytes(B));
+  }
 }
 
 // ------------------------------------------------------------ phase builders
@@ -402,6 +437,7 @@ size_t s2_frame_workspace_bytes(const s2_dims* s, int max_streams, int kv_slots)
   int grid = 0;
   if (frame_kernel_grid(dev, &grid) != S2_OK) grid = 256;
   tmp.grid = grid;
+  setup_batched(&tmp);
   Carver cv{nullptr};
   carve(&tmp, cv);
   return align_up(cv.off, 256);
@@ -586,6 +622,7 @@ int s2_frame_init(const s2_dims* s, const void* const* weights, int n_weights, v
   bind(c->fast, d.Lf);
   c->ws = static_cast<unsigned char*>(workspace);
   c->ws_bytes = ws_bytes;
+  setup_batched(c);
   Carver cv{nullptr};
   carve(c, cv);
   if (align_up(cv.off, 256) > ws_bytes) {
@@ -615,6 +652,39 @@ int s2_frame_init(const s2_dims* s, const void* const* weights, int n_weights, v
   }
   c->host_pos.assign(max_streams, 0);
   c->host_prefilled.assign(max_streams, 0);
+  if (c->batched) {
+    BatchModel& m = c->bm;
+    m.d = d;
+    m.E = c->E;
+    m.CE = c->CE;
+    m.FE = c->FE;
+    m.P = d.has_proj ? c->P : nullptr;
+    m.FO = c->FO;
+    m.norm = c->norm;
+    m.fnorm = c->fnorm;
+    m.slow = c->slow.data();
+    m.fast = c->fast.data();
+    m.max_streams = max_streams;
+    m.kv_slots = c->kv_slots;
+    m.lstride = static_cast<int>(logits_stride(d));
+    m.sms = c->sms;
+    m.st = c->st;
+    m.hidden = c->hidden;
+    m.logits = c->logits;
+    m.stage = c->stage;
+    m.ctl = c->ctl;
+    m.kc = c->kc;
+    m.vc = c->vc;
+    m.rope = c->rope;
+    m.rope_f = c->rope_f;
+    std::string why;
+    c->batch = batch_create(m, &why);
+    if (!c->batch) {
+      g_init_error = "batched decode setup failed: " + why;
+      delete c;
+      return S2_ECUDA;
+    }
+  }
   *out = c;
   return S2_OK;
 }
@@ -720,6 +790,22 @@ int s2_decode_frames(s2_ctx* c, int n, const int* ids, int n_frames, const s2_sa
     for (int j = 0; j < k; ++j)
       if (ids[j] == sid) return fail(c, S2_EINVAL, "a stream appears twice");
   }
+  if (c->batch && n >= 2) {
+    int max_ctx = 0;
+    for (int k = 0; k < n; ++k) max_ctx = std::max(max_ctx, c->host_pos[ids[k]] + n_frames);
+    std::string why;
+    int rc = batch_decode(c->batch, n, ids, n_frames, params, expo, forced, taps, max_ctx, stream, &why);
+    if (rc != S2_OK) return fail(c, rc, why);
+    for (int k = 0; k < n; ++k) {
+      const int sid = ids[k];
+      rc = compact_codes(c->stage + static_cast<size_t>(sid) * kMaxFramesPerCall * d.ncb,
+                         codes + static_cast<size_t>(k) * d.ncb * n_frames, c->st + sid, n_frames, d.ncb, n_out + k,
+                         stream);
+      if (rc != S2_OK) return fail(c, rc, "code compaction launch failed");
+      c->host_pos[sid] += n_frames;
+    }
+    return S2_OK;
+  }
   for (int k = 0; k < n; ++k) {
     const int sid = ids[k];
     CallParams cp = base_params(c);
@@ -823,6 +909,7 @@ int s2_phase_count(const s2_ctx* c, int fast_only) {
 }
 
 int s2_frame_free(s2_ctx* c) {
+  if (c && c->batch) batch_destroy(c->batch);
   delete c;
   return S2_OK;
 }

@@ -24,6 +24,7 @@
 
 #include "ptx.cuh"
 #include "s2_internal.h"
+#include "sampler.cuh"
 
 namespace s2 {
 // Internal linkage: every kernel instance unit compiles its own copy of the device code.
@@ -58,6 +59,7 @@ struct Smem {
   alignas(16) unsigned char xs[kXsBytes];  // GEMV activations | attention scratch | sampler scratch
   alignas(128) unsigned char ring[kStages][kStageBytes];
 };
+static_assert(sizeof(SampScratch) <= kXsBytes, "sampler scratch");
 
 // misc[] regions
 constexpr int kMiscSS = 0;                 // GEMV sum-of-squares partials [16]
@@ -1360,317 +1362,6 @@ __device__ void attn_fast(const CallParams& cp, const Phase& ph, Smem& S) {
   attn_fast_t<C::hd>(cp, ph, S);
 }
 
-// =========================================================================
-// sampler (CTA 0): top-30 by (value desc, id asc), softmax, top-p (keep rank r iff r == 0 or
-// Σ_{s<r} π_s < p), winner = argmax π_r / E_r (ties -> lower rank)
-// =========================================================================
-
-constexpr int kSampPer = 17;  // values per thread: 256 * 17 >= 4097
-
-// id of entry i of a logits vector: main (admissible) -> token id; fast -> code
-__device__ __forceinline__ int entry_id(const Dims& d, bool main, int i) {
-  return main ? (i < d.cbs ? d.sem_lo + i : d.im_end) : i;
-}
-
-// total order of candidates: larger value first, equal values -> lower id first
-__device__ __forceinline__ bool better_k(uint32_t ka, int ia, uint32_t kb, int ib) {
-  return ka > kb || (ka == kb && ia < ib);
-}
-
-// order-preserving map of a float to an unsigned key (finite values map above 0x007fffff)
-__device__ __forceinline__ uint32_t fkey(float z) {
-  const uint32_t u = __float_as_uint(z);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float fval(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
-// Sampler scratch (sampling phases never overlap attention / GEMV phases on a CTA).
-constexpr int kSampHist = 4096;  // first-level histogram: the top 12 bits of a key
-struct SampScratch {
-  int nvalid, cut, rem, nA, nB, result, pad[2];
-  int wsum[kConsumerWarps];
-  uint32_t aK[32];  // candidates above the boundary bin (fewer than 30)
-  int aI[32];
-  uint32_t bK[64];  // candidates in the boundary bin
-  int bI[64];
-  uint32_t cK[32];  // the final candidates in rank order
-  int cI[32];
-  int hist[kSampHist];
-  alignas(16) uint32_t keys[kSampPer * kConsumers];  // by entry index: the logits, then their keys
-};
-static_assert(sizeof(SampScratch) <= kXsBytes, "sampler scratch");
-
-// bitonic sort of 32 (key, id) pairs across a warp, one per lane: best (larger key, then lower
-// id) first
-__device__ __forceinline__ void warp_sort32(uint32_t& k, int& id) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll 1
-  for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll 1
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const uint32_t pk = __shfl_xor_sync(0xffffffffu, k, stride);
-      const int pi = __shfl_xor_sync(0xffffffffu, id, stride);
-      const bool lower = (lane & stride) == 0;
-      const bool asc = (lane & size) == 0;  // "ascending" = best first
-      if ((lower == asc) == better_k(pk, pi, k, id)) {
-        k = pk;
-        id = pi;
-      }
-    }
-  }
-}
-
-// One draw: the top-30 candidates by (value desc, id asc), then, in rank order exactly as the
-// method states: softmax over them, keep rank r iff r == 0 or Σ_{s<r} π_s < top_p, winner =
-// argmax π_r / E_r (ties -> lower rank).  Returns the drawn id in every consumer thread; -1 if
-// nothing is drawable.
-// Selection: order-preserving 32-bit keys of z = logit / T (kSampPer per thread, in shared
-// memory so that the loops stay compact).  A 4096-bin histogram of the top 12 bits locates the
-// bin holding the 30th key; while that bin holds more than 64 keys it is refined by the next 10
-// bits (at most twice).  Keys above the boundary and the boundary bin's keys are then sorted by
-// two warps.
-__device__ __noinline__ int draw(const CallParams& cp, Smem& S, const float* logits, int n, bool main, bool mask_end,
-                                 float temperature, float top_p, const float* E) {
-  const Dims& d = cp.d;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  SampScratch& W = *reinterpret_cast<SampScratch*>(S.xs);
-  // the rank-r variate, needed at the end, is requested first; the logits come into shared
-  // memory in one batch of 16-byte copies (n4 full chunks, then the remaining entries)
-  const float ev = (warp == 0 && lane < kTopK) ? ldcg(E + lane) : 1.f;
-  const int n4 = n / 4;
-#pragma unroll 1
-  for (int c = tid; c < n4; c += kConsumers) cp_async16(&W.keys[4 * c], logits + 4 * c);
-  if (tid < n - 4 * n4) W.keys[4 * n4 + tid] = __float_as_uint(ldcg(logits + 4 * n4 + tid));
-  cp_async_wait_all();
-  named_bar(1, kConsumers);
-  int nv = 0;
-#pragma unroll 1
-  for (int k = 0; k < kSampPer; ++k) {
-    const int i = tid + k * kConsumers;
-    uint32_t key = 0u;
-    if (i < n) {
-      const float l = __uint_as_float(W.keys[i]);
-      if (!(mask_end && main && entry_id(d, main, i) == d.im_end) && isfinite(l)) {
-        key = fkey(l / temperature);
-        ++nv;
-      }
-    }
-    W.keys[i] = key;
-  }
-#pragma unroll 1
-  for (int b = tid; b < kSampHist; b += kConsumers) W.hist[b] = 0;
-  nv = warp_sum_i(nv);
-  if (lane == 0) W.wsum[warp] = nv;
-  if (tid == 0) {
-    W.nA = 0;
-    W.nB = 0;
-  }
-  named_bar(1, kConsumers);
-  int nvalid = 0;
-#pragma unroll 1
-  for (int w = 0; w < kConsumerWarps; ++w) nvalid += W.wsum[w];
-  if (nvalid == 0) return -1;  // uniform: every thread saw the same count
-  const int kk = min(kTopK, nvalid);
-
-  // ---- locate the kk-th largest key: prefix `pre` of its top (32 - shift) bits, `need` of the
-  // keys with that prefix belong to the top kk
-  uint32_t pre = 0u;
-  int shift = 32, need = kk, n_eq = 0;
-#pragma unroll 1
-  for (int level = 0; level < 3; ++level) {
-    const int width = level == 0 ? 12 : 10;
-    const uint32_t prev = pre;
-    shift -= width;
-    const uint32_t mask = (1u << width) - 1u;
-#pragma unroll 1
-    for (int k = 0; k < kSampPer; ++k) {
-      const uint32_t key = W.keys[k * kConsumers + tid];
-      if (key && (level == 0 || (key >> (shift + width)) == prev)) atomicAdd(&W.hist[(key >> shift) & mask], 1);
-    }
-    named_bar(1, kConsumers);
-    // bins from the top: thread t owns bins nb-1-t*per .. nb-per-t*per
-    const int nb = 1 << width, per = nb / kConsumers;
-    int c = 0;
-#pragma unroll 4
-    for (int j = 0; j < per; ++j) c += W.hist[nb - 1 - tid * per - j];
-    int incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    if (lane == 31) W.wsum[warp] = incl;
-    named_bar(1, kConsumers);
-    int before = incl - c;
-#pragma unroll 1
-    for (int w = 0; w < warp; ++w) before += W.wsum[w];
-    if (before < need && before + c >= need) {
-      int cum = before;
-#pragma unroll 1
-      for (int j = 0; j < per; ++j) {
-        const int bin = nb - 1 - tid * per - j;
-        const int h = W.hist[bin];
-        if (cum + h >= need) {
-          W.cut = bin;
-          W.rem = need - cum;
-          break;
-        }
-        cum += h;
-      }
-    }
-    named_bar(1, kConsumers);
-    const int cut = W.cut;
-    need = W.rem;
-    n_eq = W.hist[cut];
-    pre = (prev << width) | static_cast<uint32_t>(cut);
-    if (n_eq <= 64 || level == 2) break;
-    named_bar(1, kConsumers);  // everyone has read the histogram
-#pragma unroll 1
-    for (int b = tid; b < 1024; b += kConsumers) W.hist[b] = 0;
-    named_bar(1, kConsumers);
-  }
-
-  // ---- gather: keys above the boundary prefix (all in the top kk) and keys at it
-#pragma unroll 1
-  for (int k = 0; k < kSampPer; ++k) {
-    const uint32_t key = W.keys[k * kConsumers + tid];
-    if (!key) continue;
-    const uint32_t hi = key >> shift;
-    if (hi < pre) continue;
-    const int id = entry_id(d, main, tid + k * kConsumers);
-    if (hi > pre) {
-      const int slot = atomicAdd(&W.nA, 1);
-      W.aK[slot] = key;
-      W.aI[slot] = id;
-    } else {
-      const int slot = atomicAdd(&W.nB, 1);
-      if (slot < 64) {
-        W.bK[slot] = key;
-        W.bI[slot] = id;
-      }
-    }
-  }
-  named_bar(1, kConsumers);
-  const int nA = W.nA;  // == kk - need
-  if (warp == 0) {
-    uint32_t k0 = lane < nA ? W.aK[lane] : 0u;
-    int i0 = lane < nA ? W.aI[lane] : (0x7fffffff - lane);
-    warp_sort32(k0, i0);
-    if (lane < nA) {
-      W.cK[lane] = k0;
-      W.cI[lane] = i0;
-    }
-  } else if (warp == 1 && n_eq <= 64) {
-    // boundary bin: bitonic sort of up to 64 pairs, two per lane (lane, lane + 32)
-    uint32_t ka = lane < n_eq ? W.bK[lane] : 0u, kb = lane + 32 < n_eq ? W.bK[lane + 32] : 0u;
-    int ia = lane < n_eq ? W.bI[lane] : (0x7fffffff - lane), ib = lane + 32 < n_eq ? W.bI[lane + 32] : (0x7fffffdf - lane);
-#pragma unroll 1
-    for (int size = 2; size <= 64; size <<= 1) {
-#pragma unroll 1
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        if (stride == 32) {
-          if (better_k(kb, ib, ka, ia)) {
-            const uint32_t tk = ka; ka = kb; kb = tk;
-            const int ti = ia; ia = ib; ib = ti;
-          }
-          continue;
-        }
-        const uint32_t pka = __shfl_xor_sync(0xffffffffu, ka, stride), pkb = __shfl_xor_sync(0xffffffffu, kb, stride);
-        const int pia = __shfl_xor_sync(0xffffffffu, ia, stride), pib = __shfl_xor_sync(0xffffffffu, ib, stride);
-        const bool lower = (lane & stride) == 0;
-        if ((lower == ((lane & size) == 0)) == better_k(pka, pia, ka, ia)) {
-          ka = pka;
-          ia = pia;
-        }
-        if ((lower == (((lane + 32) & size) == 0)) == better_k(pkb, pib, kb, ib)) {
-          kb = pkb;
-          ib = pib;
-        }
-      }
-    }
-    if (lane < need) {
-      W.cK[nA + lane] = ka;
-      W.cI[nA + lane] = ia;
-    }
-    if (lane + 32 < need) {
-      W.cK[nA + lane + 32] = kb;
-      W.cI[nA + lane + 32] = ib;
-    }
-  }
-  if (n_eq > 64) {
-    // more than 64 equal keys at full resolution: the `need` lowest ids among them, one by one
-    int last = -1;
-#pragma unroll 1
-    for (int r = 0; r < need; ++r) {
-      int best = 0x7fffffff;
-#pragma unroll 1
-      for (int k = 0; k < kSampPer; ++k) {
-        const int id = entry_id(d, main, tid + k * kConsumers);
-        const uint32_t key = W.keys[k * kConsumers + tid];
-        if (key && (key >> shift) == pre && id > last && id < best) best = id;
-      }
-      best = warp_min_i(best);
-      if (lane == 0) W.wsum[warp] = best;
-      named_bar(1, kConsumers);
-      int m = W.wsum[0];
-#pragma unroll 1
-      for (int w = 1; w < kConsumerWarps; ++w) m = min(m, W.wsum[w]);
-      if (tid == 0) {
-        W.cK[nA + r] = pre << shift;
-        W.cI[nA + r] = m;
-      }
-      last = m;
-      named_bar(1, kConsumers);
-    }
-  }
-  named_bar(1, kConsumers);
-  // ---- warp 0: the draw over the kk candidates, rank r = lane.  The sums, whose rounding depends
-  // on the order, are taken in rank order (every lane runs the same sequence over shuffled values)
-  if (warp == 0) {
-    const float z = lane < kk ? fval(W.cK[lane]) : 0.f;
-    const float zmax = __shfl_sync(0xffffffffu, z, 0);
-    const float e = lane < kk ? expf(z - zmax) : 0.f;
-    float sum = 0.f;
-#pragma unroll
-    for (int r = 0; r < kTopK; ++r) {
-      const float er = __shfl_sync(0xffffffffu, e, r);
-      if (r < kk) sum += er;
-    }
-    const float pi = e / sum;
-    float cum = 0.f;
-    int kept = 0;
-    bool open = true;
-#pragma unroll
-    for (int r = 0; r < kTopK; ++r) {
-      const float pr = __shfl_sync(0xffffffffu, pi, r);
-      if (r < kk && open) {
-        if (r == 0 || cum < top_p) kept = r + 1;
-        else open = false;
-        cum += pr;
-      }
-    }
-    // winner = argmax_{r < kept} π_r / E_r, ties -> lower rank
-    float q = lane < kept ? pi / ev : -INFINITY;
-    int rq = lane;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float q2 = __shfl_xor_sync(0xffffffffu, q, o);
-      const int r2 = __shfl_xor_sync(0xffffffffu, rq, o);
-      if (q2 > q || (q2 == q && r2 < rq)) {
-        q = q2;
-        rq = r2;
-      }
-    }
-    if (lane == 0) W.result = W.cI[rq];
-  }
-  named_bar(1, kConsumers);
-  const int out = W.result;
-  named_bar(1, kConsumers);
-  return out;
-}
-
 // caller-supplied ids (forced draws, Fast-AR-alone prefixes) are checked before any use as an index
 __device__ __forceinline__ int checked_id(const CallParams& cp, int v, int hi) {
   if (v < 0 || v >= hi) {
@@ -1693,7 +1384,7 @@ __device__ __noinline__ void sample_main(const CallParams& cp, Smem& S, int f) {
   if (cp.dbg_hidden) copy_vec(cp.dbg_hidden + static_cast<size_t>(f) * d.D, cp.hidden, d.D);
   const float* E = cp.expo + static_cast<size_t>(f) * kDraws * kTopK;
   const bool block_end = fd < cp.min_tokens;
-  int d0 = draw(cp, S, cp.logits, d.A, true, block_end, cp.temperature, cp.top_p, E);
+  int d0 = draw(cp.d, *reinterpret_cast<SampScratch*>(S.xs), cp.logits, d.A, true, block_end, cp.temperature, cp.top_p, E);
   if (threadIdx.x == 0) {
     if (cp.dbg_draws) cp.dbg_draws[f * kDraws + 0] = d0;
     if (cp.forced) {
@@ -1717,7 +1408,7 @@ __device__ __noinline__ void sample_main(const CallParams& cp, Smem& S, int f) {
     }
     return;
   }
-  int d1 = draw(cp, S, cp.logits, d.A, true, block_end, cp.ras_temperature, cp.ras_top_p, E + kTopK);
+  int d1 = draw(cp.d, *reinterpret_cast<SampScratch*>(S.xs), cp.logits, d.A, true, block_end, cp.ras_temperature, cp.ras_top_p, E + kTopK);
   if (threadIdx.x < 32) {
     // warp 0: the RAS window is read, tested and shifted by its lanes at once (lane i: entry i)
     const int lane = threadIdx.x;
@@ -1763,7 +1454,7 @@ __device__ __noinline__ void sample_fast(const CallParams& cp, Smem& S, int f, i
   }
   if (cp.dbg_fast) copy_vec(cp.dbg_fast + (static_cast<size_t>(f) * (d.ncb - 1) + (c - 1)) * d.cbs, cp.flogits, d.cbs);
   const float* E = cp.expo + static_cast<size_t>(f) * kDraws * kTopK + (1 + c) * kTopK;
-  int dc = draw(cp, S, cp.flogits, d.cbs, false, false, cp.temperature, cp.top_p, E);
+  int dc = draw(cp.d, *reinterpret_cast<SampScratch*>(S.xs), cp.flogits, d.cbs, false, false, cp.temperature, cp.top_p, E);
   if (threadIdx.x == 0) {
     if (cp.dbg_draws) cp.dbg_draws[f * kDraws + 1 + c] = dc;
     if (cp.forced) dc = checked_id(cp, cp.forced[f * kDraws + 1 + c], d.cbs);

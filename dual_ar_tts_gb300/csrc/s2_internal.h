@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <string>
 
 #include "../../include/s2frame.h"
 
@@ -199,5 +200,48 @@ int run_prefill(const PrefillArgs& a, void* stream);
 int run_head(const Dims& d, const float* x, const void* norm, const void* E, float* hidden, float* logits,
              StreamState* st, int pos, void* stream);
 size_t prefill_scratch_floats(const Dims& d, int chunk);
+
+// ------------------------------------------------------------- batched decode
+// Several streams decoded together, every weight read once per step for the whole batch (bf16
+// weights; see batch.cu).  The engine carves the buffers below from the workspace.
+
+struct BatchSizes {
+  size_t planes_rows;      // rows of each planes buffer (hi/lo of up to 2 * max_streams columns)
+  int ldX, ldO, ldH;       // planes row lengths: projection inputs, attention outputs, SwiGLU outputs
+  size_t part_floats;      // split-K partials
+  size_t apart_floats;     // attention split partials
+};
+
+struct BatchModel {
+  Dims d;
+  const void *E, *CE, *FE, *P, *FO, *norm, *fnorm;
+  const LayerW* slow;      // [L]
+  const LayerW* fast;      // [Lf]
+  int max_streams, kv_slots, lstride, sms;
+  StreamState* st;
+  float* hidden;
+  float* logits;
+  int32_t* stage;
+  Control* ctl;
+  unsigned char* kc;
+  unsigned char* vc;
+  const float2* rope;
+  const float2* rope_f;
+  uint16_t *pX, *pO, *pH;
+  float *part, *bx, *bfx, *bfk, *bfv, *apart, *bflog;
+  int32_t* bfcode;
+  int* bctl;
+  void* bstreams;          // device array of per-stream call settings
+};
+
+bool batch_supported(const Dims& d, int max_streams, std::string* why);
+BatchSizes batch_sizes(const Dims& d, int max_streams, int sms);
+size_t batch_stream_bytes(int max_streams);
+struct Batch;
+Batch* batch_create(const BatchModel& m, std::string* err);
+void batch_destroy(Batch* b);
+// streams ids[0..n), n_frames frames; expo/forced/taps laid out as for s2_decode_frames
+int batch_decode(Batch* b, int n, const int* ids, int n_frames, const s2_sampling* params, const float* expo,
+                 const int32_t* forced, const s2_debug_taps* taps, int max_ctx, void* stream, std::string* err);
 
 }  // namespace s2

@@ -259,6 +259,18 @@ def _prompt(d, seed, stream, n_text, n_ref):
     return p
 
 
+def make_prompt(d: dict, seed: int, stream: int, n_text: int, n_ref: int) -> np.ndarray:
+    """A prompt of the given text / reference split for any model shape (same recipe as the
+    workloads' prompts)."""
+    return _prompt(d, seed, stream, n_text, n_ref)
+
+
+#: a small bf16 model with four query heads per KV head (the grouping of S2-Pro), for quick
+#: checks of the batched decode path
+MINI = dict(_TINY, n_head=4, n_kv_head=1, ffn=512, fast_n_head=4, fast_n_kv_head=1, fast_ffn=512,
+            weight_dtype=BF16, kv_dtype=F16)
+
+
 def prompt_lengths(cfg: str):
     c = CONFIGS[cfg]
     if cfg == "tiny":

@@ -134,3 +134,31 @@ def test_import_rejects_bad_arguments(s2pro):
         dec.import_stream(2, k[:, :, :8].contiguous(), k[:, :, :8].contiguous(), x)
     assert e.value.code == pkg.S2_EINVAL
     dec.close()
+
+
+def test_mini_batched_prefill_and_frames_match_oracle():
+    # three streams of a small bf16 model (4 query heads per KV head) from real prompts of
+    # different lengths, decoded together, teacher-forced with the oracle's draws
+    import dual_ar_tts_gb300 as pkg
+    d = synth.MINI
+    host = synth.make_weights(d, 7, norm_jitter=0.1)
+    dev = pkg.upload_weights(host)
+    prompts = [synth.make_prompt(d, 7, i, 20 + 3 * i, 6 + i) for i in range(3)]
+    s = synth.sampling("tiny")
+    n_frames = 6
+    expo = np.stack([synth.expo(7, i, n_frames) for i in range(3)])
+    refs, forced = [], np.zeros((3, n_frames, 11), np.int32)
+    for i, p in enumerate(prompts):
+        sess = oracle.Session(d, host, len(p) + n_frames + 1)
+        ref = oracle.generate(sess, p, n_frames, s, expo[i])
+        forced[i, :len(ref["draws"])] = np.asarray(ref["draws"], np.int32)
+        refs.append(ref)
+        sess.close()
+    dec = pkg.Decoder(d, dev, max_streams=4, kv_slots=64)
+    dec.prefill(prompts)
+    out = dec.decode(n_frames, s, torch.from_numpy(expo).cuda(), torch.from_numpy(forced).cuda(), taps=True)
+    assert dec.sync_status() == pkg.S2_OK, pkg.s2_last_error(dec.ctx)
+    for i in range(3):
+        st = compare_frames(refs[i], out, d, s, TOL, stream=i)
+        print(f"mini stream {i}:", st)
+    dec.close()
