@@ -41,6 +41,9 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-frames", type=int, default=2, help="frames in the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batched", default="serving", choices=["serving", "longctx", "none"],
+                    help="also measure the aggregate of a batched workload (reported under 'batched')")
+    ap.add_argument("--batched-steps", type=int, default=16)
     ap.add_argument("--slow-layers", type=int, default=None,
                     help="profiling captures only: Slow-AR layer count (S2-Pro widths kept); the bench line "
                          "then describes that smaller model")
@@ -157,6 +160,63 @@ def max_over_ranks(v, world):
     t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def batched_measure(pkg, d, dev_w, cfg_name, steps, warmup, peak, local):
+    """Aggregate frames/s of a batched workload: every stream of the workload decoded in one call
+    (weights read once per step for the whole batch).  Each stream's decode state (its context's
+    fp16 K/V, its last residual) is imported from seeded device-side random values: the KV
+    contents do not change the work of a decode step, and a prefill of these contexts is not part
+    of the timed step.  Returns the dict reported under 'batched'."""
+    import numpy as np
+    import torch
+    import synth
+    cfg = synth.CONFIGS[cfg_name]
+    n, slots, seed = cfg["streams"], cfg["kv_slots"], cfg["input_seed"]
+    lengths = synth.prompt_lengths(cfg_name)
+    kmax = max(lengths)
+    dec = pkg.Decoder(d, dev_w, max_streams=n, kv_slots=slots)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    shape = (d["n_layer"], d["n_kv_head"], kmax, d["head_dim"])
+    k = torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).half()
+    v = torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).half()
+    for i, L in enumerate(lengths):
+        x = torch.randn(d["dim"], generator=g, device="cuda", dtype=torch.float32)
+        dec.import_stream(i, k[:, :, :L].contiguous(), v[:, :, :L].contiguous(), x)
+    del k, v
+    s = synth.sampling(cfg_name, min_tokens_before_end=warmup + steps + 1)
+    ex = np.stack([synth.expo(seed, i, warmup + steps) for i in range(n)])
+    expo_w = torch.from_numpy(np.ascontiguousarray(ex[:, :warmup])).cuda()
+    expo_t = torch.from_numpy(np.ascontiguousarray(ex[:, warmup:])).cuda()
+    dec.decode(warmup, s, expo_w)
+    torch.cuda.synchronize()
+    assert dec.sync_status() == pkg.S2_OK, pkg.s2_last_error(dec.ctx)
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        out = dec.decode(steps, s, expo_t)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    assert dec.sync_status() == pkg.S2_OK, pkg.s2_last_error(dec.ctx)
+    assert (out["n_out"].cpu().numpy() == steps).all()
+    dec.close()
+    w_bytes, parts = frame_bytes(d, 0)
+    w_bytes -= parts["kv"]
+    kv_slot = d["n_layer"] * d["n_kv_head"] * d["head_dim"] * 2 * 2
+    ctx_avg = [L + warmup + (steps - 1) / 2.0 for L in lengths]
+    step_bytes = w_bytes + sum(kv_slot * (c + 1) for c in ctx_avg)
+    t = ms / 1000.0
+    achieved = step_bytes * steps / t / 1e9
+    return {"workload": f"{cfg_name}: {n} streams, contexts {min(lengths)}..{kmax}, bf16 weights, fp16 KV "
+                        f"(decode state imported, see docstring)",
+            "streams": n, "frames_per_stream": steps, "warmup": warmup,
+            "value": n * steps / t, "unit": "frames/s (aggregate)", "per_stream_fps": steps / t,
+            "ms_per_step": ms / steps, "algorithmic_gb_per_step": step_bytes / 1e9,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak},
+            "clocks": clk.summary()}
 
 
 def cpu_oracle_sample(d, host_w, n_frames, s):
@@ -306,6 +366,10 @@ def main():
         "clocks": clk.summary(),
         "setup_s": setup_s,
     }
+    if args.batched != "none" and args.slow_layers is None:
+        dec.close()
+        torch.cuda.empty_cache()
+        line["batched"] = batched_measure(pkg, d, dev_w, args.batched, args.batched_steps, args.warmup, pk, local)
     if rank == 0 and not args.no_cpu_baseline and args.slow_layers is None:
         try:
             v, cores, sample = cpu_oracle_sample(d, host_w, args.cpu_frames, s)

@@ -42,9 +42,12 @@ constexpr int kABytes = kTileM * kAtom * 2;  // one weight tile
 constexpr int kGemvThreads = 192;           // 4 epilogue warps, 1 TMA warp, 1 MMA warp
 constexpr int kMaxGemvStages = 8;
 constexpr int kGemvSmemBudget = 200 * 1024;
-constexpr int kPrepThreads = 256;
+constexpr int kPrepThreads = 1024;                // column preparation: one CTA per column
+constexpr int kPrepPer = 3;                       // row elements per thread
+constexpr int kPrepMaxK = kPrepPer * kPrepThreads;  // longest row a column-preparation CTA holds
 constexpr int kAttnTile = 32;               // KV slots per staged tile (Slow-AR attention)
-constexpr int kAttnChunk = 128;             // target slots per Slow-AR attention item
+constexpr int kAttnChunk = 256;             // target slots per Slow-AR attention item
+constexpr int kAttnStages = 4;              // K/V tiles in flight per item
 constexpr int kMaxSplitsAttn = 32;          // items per (stream, KV head) at most
 
 enum ColMode : int { CM_RESID = 0, CM_STORE, CM_FEROW, CM_EMBED, CM_HIDDEN };
@@ -115,8 +118,9 @@ __device__ __forceinline__ void store_hilo(uint16_t* planes, int ld, int col, in
   planes[static_cast<size_t>(2 * col + 1) * ld + k] = __bfloat16_as_ushort(lo);
 }
 
-// deterministic block sum (fixed order) for 256 threads
-__device__ __forceinline__ float block_sum256(float v, float* red) {
+// deterministic block sum (fixed order) over the NT threads of the block; red holds NT / 32 floats
+template <int NT>
+__device__ __forceinline__ float block_sum(float v, float* red) {
   v = warp_sum(v);
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __syncthreads();
@@ -124,7 +128,7 @@ __device__ __forceinline__ float block_sum256(float v, float* red) {
   __syncthreads();
   float t = 0.f;
 #pragma unroll
-  for (int i = 0; i < kPrepThreads / 32; ++i) t += red[i];
+  for (int i = 0; i < NT / 32; ++i) t += red[i];
   return t;
 }
 
@@ -150,6 +154,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   const int na = a1 - a0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const CUtensorMap* tA = z == 0 ? &tmA : &tmA2;
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < nstages; ++s) {
       mbar_init(&S.full[s], 1);
@@ -172,9 +177,19 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       prefetch_tmap(tA);
       prefetch_tmap(&tmB);
       const uint64_t pol = policy_evict_first();
-      for (int i = 0; i < na; ++i) {
+      // the weights do not depend on earlier kernels: the first stages' weight tiles are requested
+      // before waiting for the grid that produces the activations
+      const int pre = min(nstages, na);
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&S.full[i], sbytes);
+        tma_load_2d(sm + i * sbytes, tA, (a0 + i) * kAtom, row0 + tile * kTileM, &S.full[i], pol);
+      }
+      pdl_wait();
+      for (int i = 0; i < pre; ++i)
+        tma_load_2d(sm + i * sbytes + kABytes, &tmB, (a0 + i) * kAtom, 0, &S.full[i], pol);
+      for (int i = pre; i < na; ++i) {
         const int s = i % nstages;
-        if (i >= nstages && !wait_bar(&S.empty[s], ((i / nstages) & 1) ^ 1, ctl)) break;
+        if (!wait_bar(&S.empty[s], ((i / nstages) & 1) ^ 1, ctl)) break;
         unsigned char* A = sm + s * sbytes;
         mbar_arrive_expect_tx(&S.full[s], sbytes);
         tma_load_2d(A, tA, (a0 + i) * kAtom, row0 + tile * kTileM, &S.full[s], pol);
@@ -200,6 +215,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     }
   } else {
     const bool ok = __all_sync(0xffffffffu, wait_bar(&S.acc, 0, ctl));
+    pdl_wait();  // the partials buffer may still be read by the previous grid until it completes
     if (ok) {
       tc_fence_after();
       const int row = tile * kTileM + warp * 32 + lane;
@@ -243,8 +259,10 @@ struct ColPrep {
 };
 
 __global__ void __launch_bounds__(kPrepThreads) k_colprep(const BEnv e, const ColPrep p) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[kPrepThreads / 32];
-  constexpr int kMaxPer = 12;  // K <= 12 * 256 (checked on the host)
+  constexpr int kMaxPer = kPrepPer;  // K <= kPrepMaxK (checked on the host)
   const Dims& d = e.d;
   const int c = blockIdx.x, b = c / p.npos, j = c % p.npos;
   const int sid = e.bs[b].sid;
@@ -253,6 +271,8 @@ __global__ void __launch_bounds__(kPrepThreads) k_colprep(const BEnv e, const Co
   const int mode = p.mode[j];
   const int pcol = p.part_by_stream ? b : c;
   float v[kMaxPer];
+#pragma unroll
+  for (int i = 0; i < kMaxPer; ++i) v[i] = 0.f;
   float ss = 0.f;
   int code = 0, tok = 0;
   float msem = 0.f;
@@ -262,14 +282,28 @@ __global__ void __launch_bounds__(kPrepThreads) k_colprep(const BEnv e, const Co
     msem = (tok >= d.sem_lo && tok <= d.sem_hi) ? 1.f : 0.f;
   }
   float* xr = p.x ? p.x + static_cast<size_t>(b) * p.xb + static_cast<size_t>(j) * K : nullptr;
+  // gather every input first (no stores in between, so the loads overlap), then store
+  if (mode == CM_RESID || mode == CM_STORE) {
+#pragma unroll
+    for (int i = 0; i < kMaxPer; ++i) {
+      const int k = tid + i * kPrepThreads;
+      v[i] = (mode == CM_RESID && k < K) ? __ldcg(xr + k) : 0.f;
+    }
+    for (int s = 0; s < p.splits; ++s) {
+      const float* ps = p.part + (static_cast<size_t>(s) * p.part_nc + pcol) * K;
+#pragma unroll
+      for (int i = 0; i < kMaxPer; ++i) {
+        const int k = tid + i * kPrepThreads;
+        if (k < K) v[i] += __ldcg(ps + k);
+      }
+    }
+  }
 #pragma unroll
   for (int i = 0; i < kMaxPer; ++i) {
     const int k = tid + i * kPrepThreads;
-    float a = 0.f;
+    float a = v[i];
     if (k < K) {
       if (mode == CM_RESID || mode == CM_STORE) {
-        a = mode == CM_RESID ? ldcg(xr + k) : 0.f;
-        for (int s = 0; s < p.splits; ++s) a += ldcg(p.part + (static_cast<size_t>(s) * p.part_nc + pcol) * K + k);
       } else if (mode == CM_FEROW) {
         a = wload(e.FE, static_cast<size_t>(code) * K + k, d.esz);
       } else if (mode == CM_EMBED) {
@@ -281,15 +315,21 @@ __global__ void __launch_bounds__(kPrepThreads) k_colprep(const BEnv e, const Co
         }
         a = __fadd_rn(__fmul_rn(d.sem_scale, wload(e.E, static_cast<size_t>(tok) * K + k, d.esz)), __fmul_rn(msem, acc));
       } else {  // CM_HIDDEN
-        a = ldcg(e.hidden + static_cast<size_t>(sid) * d.D + k);
+        a = __ldcg(e.hidden + static_cast<size_t>(sid) * d.D + k);
       }
-      if (xr) xr[k] = a;
-      ss += a * a;
     }
     v[i] = a;
   }
+#pragma unroll
+  for (int i = 0; i < kMaxPer; ++i) {
+    const int k = tid + i * kPrepThreads;
+    if (k < K) {
+      if (xr) xr[k] = v[i];
+      ss += v[i] * v[i];
+    }
+  }
   float r = 1.f;
-  if (p.normw) r = 1.0f / sqrtf(block_sum256(ss, red) / static_cast<float>(K) + d.eps);
+  if (p.normw) r = 1.0f / sqrtf(block_sum<kPrepThreads>(ss, red) / static_cast<float>(K) + d.eps);
   const bool planes = !p.last_only || j == p.npos - 1;
   const int pc = p.last_only ? b : c;
 #pragma unroll
@@ -305,6 +345,8 @@ __global__ void __launch_bounds__(kPrepThreads) k_colprep(const BEnv e, const Co
 
 // SwiGLU of the two projections (partials of W1 then W3, one split): planes of silu(g)·u
 __global__ void __launch_bounds__(256) k_swiglu(const BEnv e, const float* part, int M, int NC) {
+  pdl_wait();
+  pdl_trigger();
   const int c = blockIdx.y;
   const int sid = e.bs[c / (NC / e.nb)].sid;
   if (stream_done(e, sid)) return;
@@ -367,23 +409,35 @@ __device__ void norm_rope_heads(float* v, int nheads, const void* nw, bool norm,
 }
 
 // Slow-AR: item (stream b, KV head g, split s) over its range of slots; the item whose range
-// holds the new slot normalises, rotates and stores the new K/V first.
+// holds the new slot normalises, rotates and stores the new K/V first.  Each warp owns every
+// eighth group of 4 slots of the range and runs its own cp.async pipeline (kAttnStages groups in
+// flight), its own online softmax and P·V for the 4 query heads, so the slot loop needs no
+// block-wide barrier; the 8 warps' partial results are combined at the end.
+// Scores: lane = (slot of the group, 16-element chunk of the head dimension), the query chunk in
+// registers, reduced over the 8 chunk lanes by shuffles.  P·V: lane = HD/32 output elements of
+// every head.
 template <int HD, typename KT>
-__global__ void __launch_bounds__(256) k_attn_slow(const BEnv e, int layer, const void* qn, const void* kn,
-                                                   const float* part, int splits, int ns, float scale) {
-  constexpr int G = 4;  // query heads per KV head
-  __shared__ float q[G][HD];
+__global__ void __launch_bounds__(256, 2) k_attn_slow(const BEnv e, int layer, const void* qn, const void* kn,
+                                                      const float* __restrict__ part, int splits, int ns, float scale) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int G = 4;                 // query heads per KV head
+  constexpr int CH = HD / 8;           // score chunk per lane
+  constexpr int OE = HD / 32;          // P·V outputs per lane and head
+  constexpr int ROWB = HD * 2;         // bytes of one fp16 row
+  constexpr int QB = 4 * ROWB;         // bytes of the K (or V) rows of one 4-slot group
+  static_assert(sizeof(KT) == 2 && CH % 8 == 0 && OE % 2 == 0, "fp16 cache");
+  __shared__ __align__(16) float q[G][HD];
   __shared__ float kn_new[HD], vn_new[HD];
-  __shared__ __align__(16) KT ks[2][kAttnTile][HD];
-  __shared__ __align__(16) KT vs[2][kAttnTile][HD];
-  __shared__ float sc[G][kAttnTile];
-  __shared__ float corr[G], mrun[G], lrun[G], red[8];
+  __shared__ float wm[8][G], wl[8][G];
+  __shared__ float red[8];
+  extern __shared__ __align__(1024) unsigned char smraw[];
   const Dims& d = e.d;
   const int it = blockIdx.x;
   const int s = it % ns, g = (it / ns) % d.Hkv, b = it / (ns * d.Hkv);
   const int sid = e.bs[b].sid;
   float* outp = e.apart + static_cast<size_t>(it) * G * (HD + 2);
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (stream_done(e, sid)) return;
   const int pos = ldcgi(&e.st[sid].pos);
   const int n = pos + 1;
@@ -401,121 +455,191 @@ __global__ void __launch_bounds__(256) k_attn_slow(const BEnv e, int layer, cons
   }
   const int QKV = (d.Hq + 2 * d.Hkv) * HD;
   const int NC = e.nb;
-  auto col = [&](int r) {
-    float a = 0.f;
-    for (int sp = 0; sp < splits; ++sp) a += ldcg(part + (static_cast<size_t>(sp) * NC + b) * QKV + r);
-    return a;
-  };
-  for (int t = tid; t < G * HD; t += blockDim.x) q[t / HD][t % HD] = col((g * G) * HD + t);
   const bool has_new = pos >= s0 && pos < s1;
-  if (has_new)
-    for (int t = tid; t < HD; t += blockDim.x) {
-      kn_new[t] = col(d.Hq * HD + g * HD + t);
-      vn_new[t] = col((d.Hq + d.Hkv) * HD + g * HD + t);
-    }
-  const float2* rrow = e.rope + static_cast<size_t>(pos) * (HD / 2);
-  norm_rope_heads<HD>(&q[0][0], G, qn, d.qk_norm != 0, d.esz, d.eps, rrow, red);
   const size_t slots = static_cast<size_t>(e.kv_slots);
   const size_t base = ((static_cast<size_t>(layer) * e.max_streams + sid) * d.Hkv + g) * slots * HD;
   KT* Kc = reinterpret_cast<KT*>(e.kc) + base;
   KT* Vc = reinterpret_cast<KT*>(e.vc) + base;
+  // this warp's 4-slot groups: qi = warp, warp + 8, ...
+  const int nq = (s1 - s0 + 3) / 4;
+  const int nstep = nq > warp ? (nq - warp + 7) / 8 : 0;
+  unsigned char* wst = smraw + static_cast<size_t>(warp) * kAttnStages * 2 * QB;
+  auto stage = [&](int t) {
+    if (t < nstep) {
+      const int q0 = s0 + 4 * (warp + 8 * t);
+      const int rows = min(4, s1 - q0);
+      unsigned char* dk = wst + (t % kAttnStages) * 2 * QB;
+      for (int c = lane; c < rows * (ROWB / 16); c += 32) {
+        const int r = c / (ROWB / 16), cc = c % (ROWB / 16);
+        cp_async16(dk + r * ROWB + cc * 16, reinterpret_cast<const unsigned char*>(Kc + static_cast<size_t>(q0 + r) * HD) + cc * 16);
+        cp_async16(dk + QB + r * ROWB + cc * 16,
+                   reinterpret_cast<const unsigned char*>(Vc + static_cast<size_t>(q0 + r) * HD) + cc * 16);
+      }
+    }
+    cp_async_commit();
+  };
+  // the old slots do not depend on this step: their copies start before the prologue
+  for (int t = 0; t < kAttnStages - 1; ++t) stage(t);
+  // q of the G heads (and the new k, v) from the split partials: all loads first
+  {
+    constexpr int PER = G * HD / 256;
+    float a[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) a[u] = 0.f;
+    for (int sp = 0; sp < splits; ++sp) {
+      const float* pp = part + (static_cast<size_t>(sp) * NC + b) * QKV + (g * G) * HD;
+#pragma unroll
+      for (int u = 0; u < PER; ++u) a[u] += __ldcg(pp + tid + u * 256);
+    }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) (&q[0][0])[tid + u * 256] = a[u];
+    if (has_new && tid < HD) {
+      float kk = 0.f, vv = 0.f;
+      for (int sp = 0; sp < splits; ++sp) {
+        const float* pp = part + (static_cast<size_t>(sp) * NC + b) * QKV;
+        kk += __ldcg(pp + d.Hq * HD + g * HD + tid);
+        vv += __ldcg(pp + (d.Hq + d.Hkv) * HD + g * HD + tid);
+      }
+      kn_new[tid] = kk;
+      vn_new[tid] = vv;
+    }
+  }
+  const float2* rrow = e.rope + static_cast<size_t>(pos) * (HD / 2);
+  norm_rope_heads<HD>(&q[0][0], G, qn, d.qk_norm != 0, d.esz, d.eps, rrow, red);
   if (has_new) {
     norm_rope_heads<HD>(kn_new, 1, kn, d.qk_norm != 0, d.esz, d.eps, rrow, red);
-    for (int t = tid; t < HD; t += blockDim.x) {
+    for (int t = tid; t < HD; t += 256) {
       const KT kq = tokv<KT>(kn_new[t]), vq = tokv<KT>(vn_new[t]);
       Kc[static_cast<size_t>(pos) * HD + t] = kq;
       Vc[static_cast<size_t>(pos) * HD + t] = vq;
       kn_new[t] = kvf<KT>(kq);
       vn_new[t] = kvf<KT>(vq);
     }
-  }
-  for (int t = tid; t < G * HD; t += blockDim.x) q[t / HD][t % HD] *= scale;
-  if (tid < G) {
-    mrun[tid] = -INFINITY;
-    lrun[tid] = 0.f;
-  }
-  // P·V: thread t owns head t / 64 and HD / 64 consecutive output elements
-  constexpr int EPT = HD / 64;
-  const int oh = tid >> 6, oe = (tid & 63) * EPT;
-  float o[EPT];
-#pragma unroll
-  for (int i = 0; i < EPT; ++i) o[i] = 0.f;
-  constexpr int CPR = HD * static_cast<int>(sizeof(KT)) / 16;  // 16-byte chunks per row
-  auto stage = [&](int buf, int t0) {
-    const int rows = min(kAttnTile, s1 - t0);
-    for (int i = tid; i < rows * CPR; i += blockDim.x) {
-      const int r = i / CPR, cc = i % CPR;
-      cp_async16(reinterpret_cast<unsigned char*>(&ks[buf][r][0]) + cc * 16,
-                 reinterpret_cast<const unsigned char*>(Kc + static_cast<size_t>(t0 + r) * HD) + cc * 16);
-      cp_async16(reinterpret_cast<unsigned char*>(&vs[buf][r][0]) + cc * 16,
-                 reinterpret_cast<const unsigned char*>(Vc + static_cast<size_t>(t0 + r) * HD) + cc * 16);
-    }
-    cp_async_commit();
-  };
-  __syncthreads();
-  stage(0, s0);
-  int buf = 0;
-  for (int t0 = s0; t0 < s1; t0 += kAttnTile, buf ^= 1) {
-    const int rows = min(kAttnTile, s1 - t0);
-    if (t0 + kAttnTile < s1) {
-      stage(buf ^ 1, t0 + kAttnTile);
-      cp_async_wait_group<1>();
-    } else {
-      cp_async_wait_group<0>();
-    }
     __syncthreads();
-    // scores: pair (head, slot) by two adjacent threads, one half of the head dimension each
-    {
-      const int pr = tid >> 1, half = tid & 1;
-      const int h = pr >> 5, sl = pr & 31;
-      float a = 0.f;
-      if (sl < rows) {
-        const bool fresh = has_new && t0 + sl == pos;
-#pragma unroll 8
-        for (int i = 0; i < HD / 2; ++i) {
-          const int k = half * (HD / 2) + i;
-          a = fmaf(q[h][k], fresh ? kn_new[k] : kvf<KT>(ks[buf][sl][k]), a);
+  }
+  const int sl = lane >> 3, kc = lane & 7;
+  float qr[G][CH];
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int u = 0; u < CH; ++u) qr[h][u] = q[h][kc * CH + u] * scale;
+  float o[G][OE];
+  float mw[G], lw[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    mw[h] = -INFINITY;
+    lw[h] = 0.f;
+#pragma unroll
+    for (int u = 0; u < OE; ++u) o[h][u] = 0.f;
+  }
+  for (int t = 0; t < nstep; ++t) {
+    stage(t + kAttnStages - 1);
+    cp_async_wait_group<kAttnStages - 1>();
+    __syncwarp();
+    const int q0 = s0 + 4 * (warp + 8 * t);
+    unsigned char* dk = wst + (t % kAttnStages) * 2 * QB;
+    if (has_new && pos >= q0 && pos < q0 + 4) {
+      // the copy of the new slot may predate its store: use the values computed here
+      KT* kr = reinterpret_cast<KT*>(dk + (pos - q0) * ROWB);
+      KT* vr = reinterpret_cast<KT*>(dk + QB + (pos - q0) * ROWB);
+      for (int u = lane; u < HD; u += 32) {
+        kr[u] = tokv<KT>(kn_new[u]);
+        vr[u] = tokv<KT>(vn_new[u]);
+      }
+      __syncwarp();
+    }
+    const bool valid = q0 + sl < s1;
+    float sc[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) sc[h] = 0.f;
+    if (valid) {
+      const uint4* kr = reinterpret_cast<const uint4*>(dk + sl * ROWB + kc * CH * 2);
+#pragma unroll
+      for (int w = 0; w < CH / 8; ++w) {
+        const uint4 u4 = kr[w];
+        const uint32_t wd[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const float2 kv = __half22float2(*reinterpret_cast<const __half2*>(&wd[x]));
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            sc[h] = fmaf(qr[h][w * 8 + 2 * x], kv.x, sc[h]);
+            sc[h] = fmaf(qr[h][w * 8 + 2 * x + 1], kv.y, sc[h]);
+          }
         }
       }
-      a += __shfl_xor_sync(0xffffffffu, a, 1);
-      if (half == 0) sc[h][sl] = sl < rows ? a : -INFINITY;
     }
-    __syncthreads();
-    // online softmax: warp h updates head h's running max and sum
-    if (tid < 32 * G) {
-      const int h = tid >> 5, lane = tid & 31;
-      const float v = sc[h][lane];
-      const float mo = mrun[h];
-      const float mn = fmaxf(mo, warp_max(v));
-      const float pv = v == -INFINITY ? 0.f : expf(v - mn);
-      const float ps = warp_sum(pv);
-      sc[h][lane] = pv;
-      if (lane == 0) {
-        const float cf = mo == -INFINITY ? 0.f : expf(mo - mn);
-        corr[h] = cf;
-        lrun[h] = lrun[h] * cf + ps;
-        mrun[h] = mn;
+    float pr[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float v = sc[h];
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v = valid ? v : -INFINITY;
+      float mq = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+      mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, 16));
+      const float mn = fmaxf(mw[h], mq);
+      const float p = valid ? expf(v - mn) : 0.f;
+      const float cf = mw[h] == -INFINITY ? 0.f : expf(mw[h] - mn);
+      float ps = p + __shfl_xor_sync(0xffffffffu, p, 8);
+      ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+      lw[h] = lw[h] * cf + ps;
+      mw[h] = mn;
+#pragma unroll
+      for (int u = 0; u < OE; ++u) o[h][u] *= cf;
+      pr[h] = p;
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      if (q0 + r >= s1) break;
+      const KT* vr = reinterpret_cast<const KT*>(dk + QB + r * ROWB) + lane * OE;
+      float vv[OE];
+#pragma unroll
+      for (int u = 0; u < OE; u += 2) {
+        const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(vr + u));
+        vv[u] = f2.x;
+        vv[u + 1] = f2.y;
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float ph = __shfl_sync(0xffffffffu, pr[h], r * 8);
+#pragma unroll
+        for (int u = 0; u < OE; ++u) o[h][u] = fmaf(ph, vv[u], o[h][u]);
       }
     }
-    __syncthreads();
-    {
-      const float cf = corr[oh];
-#pragma unroll
-      for (int i = 0; i < EPT; ++i) o[i] *= cf;
-      for (int sl = 0; sl < rows; ++sl) {
-        const float pv = sc[oh][sl];
-        const bool fresh = has_new && t0 + sl == pos;
-#pragma unroll
-        for (int i = 0; i < EPT; ++i) o[i] = fmaf(pv, fresh ? vn_new[oe + i] : kvf<KT>(vs[buf][sl][oe + i]), o[i]);
-      }
-    }
-    __syncthreads();
+    __syncwarp();
   }
+  cp_async_wait_group<0>();
+  __syncwarp();
+  // the warp's partial result into its own staging area, then the 8 warps combined
+  float* ow = reinterpret_cast<float*>(wst);
 #pragma unroll
-  for (int i = 0; i < EPT; ++i) outp[oh * HD + oe + i] = o[i];
-  if (tid < G) {
-    outp[G * HD + tid] = mrun[tid];
-    outp[G * HD + G + tid] = lrun[tid];
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int u = 0; u < OE; ++u) ow[h * HD + lane * OE + u] = o[h][u];
+  if (lane < G) {
+    wm[warp][lane] = mw[lane];
+    wl[warp][lane] = lw[lane];
+  }
+  __syncthreads();
+  for (int t2 = tid; t2 < G * HD; t2 += 256) {
+    const int h = t2 / HD;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) M = fmaxf(M, wm[w][h]);
+    float acc = 0.f, l = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const float cw = wm[w][h] == -INFINITY ? 0.f : expf(wm[w][h] - M);
+      acc = fmaf(cw, reinterpret_cast<const float*>(smraw + static_cast<size_t>(w) * kAttnStages * 2 * QB)[t2], acc);
+      l = fmaf(cw, wl[w][h], l);
+    }
+    outp[t2] = acc;
+    if (t2 % HD == 0) {
+      outp[G * HD + h] = M;
+      outp[G * HD + G + h] = l;
+    }
   }
 }
 
@@ -523,37 +647,65 @@ __global__ void __launch_bounds__(256) k_attn_slow(const BEnv e, int layer, cons
 // written as the planes of the out-projection input (query head h at columns h*HD..)
 template <int HD>
 __global__ void __launch_bounds__(256) k_attn_comb(const BEnv e, int ns) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int G = 4;
+  constexpr int EPT = G * HD / 256;
+  __shared__ float wgt[kMaxSplitsAttn][G];
+  __shared__ float inv[G];
   const Dims& d = e.d;
   const int b = blockIdx.x / d.Hkv, g = blockIdx.x % d.Hkv;
   if (stream_done(e, e.bs[b].sid)) return;
   const float* base = e.apart + static_cast<size_t>(blockIdx.x) * ns * G * (HD + 2);
-  for (int t = threadIdx.x; t < G * HD; t += blockDim.x) {
-    const int h = t / HD;
+  const int tid = threadIdx.x;
+  if (tid < G) {
+    // weights e^{m_s - M} per split of head tid, and 1 / Σ_s e^{m_s - M} l_s
     float M = -INFINITY;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, ldcg(base + static_cast<size_t>(s) * G * (HD + 2) + G * HD + h));
-    float num = 0.f, den = 0.f;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(base + static_cast<size_t>(s) * G * (HD + 2) + G * HD + tid));
+    float den = 0.f;
     for (int s = 0; s < ns; ++s) {
       const float* ps = base + static_cast<size_t>(s) * G * (HD + 2);
-      const float m = ldcg(ps + G * HD + h);
-      if (m == -INFINITY) continue;
-      const float w = expf(m - M);
-      num = fmaf(w, ldcg(ps + t), num);
-      den = fmaf(w, ldcg(ps + G * HD + G + h), den);
+      const float m = __ldcg(ps + G * HD + tid);
+      const float w = m == -INFINITY ? 0.f : expf(m - M);
+      wgt[s][tid] = w;
+      den = fmaf(w, __ldcg(ps + G * HD + G + tid), den);
     }
-    store_hilo(e.pO, e.ldO, b, (g * G + h) * HD + (t % HD), num / den);
+    inv[tid] = 1.0f / den;
+  }
+  __syncthreads();
+  float num[EPT];
+#pragma unroll
+  for (int u = 0; u < EPT; ++u) num[u] = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float* ps = base + static_cast<size_t>(s) * G * (HD + 2);
+#pragma unroll
+    for (int u = 0; u < EPT; ++u) {
+      const int t = tid + u * 256;
+      const float w = wgt[s][t / HD];
+      if (w != 0.f) num[u] = fmaf(w, __ldcg(ps + t), num[u]);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < EPT; ++u) {
+    const int t = tid + u * 256, h = t / HD;
+    store_hilo(e.pO, e.ldO, b, (g * G + h) * HD + (t % HD), num[u] * inv[h]);
   }
 }
 
 // Fast-AR: per (stream, KV head), the call's new positions in order: q/k norm, RoPE at the
-// position, K/V into the stream's window, attention over positions 0..p (ch.06 §1-§4).
+// position, K/V into the stream's window, attention over positions 0..p (ch.06 §1-§4).  The
+// window's earlier rows are staged in shared memory once.
 template <int HD>
 __global__ void __launch_bounds__(256) k_attn_fast(const BEnv e, int layer, const void* qn, const void* kn,
-                                                   const float* part, int splits, int npos, int pos0, float scale) {
+                                                   const float* __restrict__ part, int splits, int npos, int pos0,
+                                                   float scale) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int G = 4;
   constexpr int WMAX = 16;
-  __shared__ float q[G][HD];
-  __shared__ float kv[2][HD];
+  __shared__ __align__(16) float q[G][HD];
+  __shared__ __align__(16) float kw[WMAX][HD];
+  __shared__ __align__(16) float vw[WMAX][HD];
   __shared__ float sc[G][WMAX];
   __shared__ float red[8];
   const Dims& d = e.d;
@@ -566,37 +718,56 @@ __global__ void __launch_bounds__(256) k_attn_fast(const BEnv e, int layer, cons
   const size_t wl = static_cast<size_t>(d.Wf) * d.Hkvf * HD;  // one layer of the window
   float* Kw = e.bfk + (static_cast<size_t>(b) * d.Lf + layer) * wl;
   float* Vw = e.bfv + (static_cast<size_t>(b) * d.Lf + layer) * wl;
+  for (int t = tid; t < pos0 * HD; t += 256) {
+    const int r = t / HD, k = t % HD;
+    kw[r][k] = __ldcg(Kw + (static_cast<size_t>(r) * d.Hkvf + g) * HD + k);
+    vw[r][k] = __ldcg(Vw + (static_cast<size_t>(r) * d.Hkvf + g) * HD + k);
+  }
   for (int j = 0; j < npos; ++j) {
     const int c = b * npos + j, p = pos0 + j;
-    auto col = [&](int r) {
-      float a = 0.f;
-      for (int sp = 0; sp < splits; ++sp) a += ldcg(part + (static_cast<size_t>(sp) * NC + c) * QKV + r);
-      return a;
-    };
-    __syncthreads();
-    for (int t = tid; t < G * HD; t += blockDim.x) q[t / HD][t % HD] = col((g * G) * HD + t);
-    for (int t = tid; t < HD; t += blockDim.x) {
-      kv[0][t] = col(d.Hqf * HD + g * HD + t);
-      kv[1][t] = col((d.Hqf + d.Hkvf) * HD + g * HD + t);
+    {
+      // q of the G heads, then k and v: loads first
+      constexpr int PER = G * HD / 256;
+      float a[PER];
+      float kk = 0.f, vv = 0.f;
+#pragma unroll
+      for (int u = 0; u < PER; ++u) a[u] = 0.f;
+      for (int sp = 0; sp < splits; ++sp) {
+        const float* pp = part + (static_cast<size_t>(sp) * NC + c) * QKV;
+#pragma unroll
+        for (int u = 0; u < PER; ++u) a[u] += __ldcg(pp + (g * G) * HD + tid + u * 256);
+        if (tid < HD) {
+          kk += __ldcg(pp + d.Hqf * HD + g * HD + tid);
+          vv += __ldcg(pp + (d.Hqf + d.Hkvf) * HD + g * HD + tid);
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int u = 0; u < PER; ++u) (&q[0][0])[tid + u * 256] = a[u];
+      if (tid < HD) {
+        kw[p][tid] = kk;
+        vw[p][tid] = vv;
+      }
     }
     const float2* rrow = e.rope_f + static_cast<size_t>(p) * (HD / 2);
     norm_rope_heads<HD>(&q[0][0], G, qn, d.qk_norm != 0, d.esz, d.eps, rrow, red);
-    norm_rope_heads<HD>(&kv[0][0], 1, kn, d.qk_norm != 0, d.esz, d.eps, rrow, red);
-    for (int t = tid; t < HD; t += blockDim.x) {
-      Kw[(static_cast<size_t>(p) * d.Hkvf + g) * HD + t] = kv[0][t];
-      Vw[(static_cast<size_t>(p) * d.Hkvf + g) * HD + t] = kv[1][t];
+    norm_rope_heads<HD>(&kw[p][0], 1, kn, d.qk_norm != 0, d.esz, d.eps, rrow, red);
+    if (tid < HD) {
+      Kw[(static_cast<size_t>(p) * d.Hkvf + g) * HD + tid] = kw[p][tid];
+      Vw[(static_cast<size_t>(p) * d.Hkvf + g) * HD + tid] = vw[p][tid];
     }
-    __threadfence_block();
-    __syncthreads();
-    // scores of the G heads over positions 0..p: one warp per (head, position)
-    const int w = tid >> 5, lane = tid & 31;
-    for (int hp = w; hp < G * (p + 1); hp += blockDim.x >> 5) {
-      const int h = hp / (p + 1), t = hp % (p + 1);
-      const float* kr = Kw + (static_cast<size_t>(t) * d.Hkvf + g) * HD;
+    // scores: 4 threads per (head, position), a quarter of the head dimension each
+    {
+      const int pr = tid >> 2, qtr = tid & 3;
+      const int h = pr / WMAX, t = pr % WMAX;
       float a = 0.f;
-      for (int k = lane; k < HD; k += 32) a = fmaf(q[h][k], t == p ? kv[0][k] : kr[k], a);
-      a = warp_sum(a);
-      if (lane == 0) sc[h][t] = a * scale;
+      if (t <= p) {
+#pragma unroll 8
+        for (int k = qtr * (HD / 4); k < (qtr + 1) * (HD / 4); ++k) a = fmaf(q[h][k], kw[t][k], a);
+      }
+      a += __shfl_xor_sync(0xffffffffu, a, 1);
+      a += __shfl_xor_sync(0xffffffffu, a, 2);
+      if (qtr == 0 && h < G) sc[h][t] = t <= p ? a * scale : -INFINITY;
     }
     __syncthreads();
     if (tid < G) {
@@ -610,10 +781,10 @@ __global__ void __launch_bounds__(256) k_attn_fast(const BEnv e, int layer, cons
       red[tid] = 1.0f / l;
     }
     __syncthreads();
-    for (int t2 = tid; t2 < G * HD; t2 += blockDim.x) {
+    for (int t2 = tid; t2 < G * HD; t2 += 256) {
       const int h = t2 / HD, k = t2 % HD;
       float a = 0.f;
-      for (int t = 0; t <= p; ++t) a = fmaf(sc[h][t], t == p ? kv[1][k] : Vw[(static_cast<size_t>(t) * d.Hkvf + g) * HD + k], a);
+      for (int t = 0; t <= p; ++t) a = fmaf(sc[h][t], vw[t][k], a);
       store_hilo(e.pO, e.ldO, c, (g * G + h) * HD + k, a * red[h]);
     }
   }
@@ -622,6 +793,27 @@ __global__ void __launch_bounds__(256) k_attn_fast(const BEnv e, int layer, cons
 // =========================================================================================
 // draws and bookkeeping (one CTA of 256 threads per stream)
 // =========================================================================================
+
+// dst[i] = Σ_s part[s][col][i] for i < n (n <= 16 * blockDim.x), loads batched per thread
+__device__ void sum_partials(float* dst, const float* __restrict__ part, int splits, int NC, int col, int n) {
+  constexpr int R = 16;
+  float a[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) a[r] = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    const float* ps = part + (static_cast<size_t>(s) * NC + col) * n;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int i = threadIdx.x + r * blockDim.x;
+      if (i < n) a[r] += __ldcg(ps + i);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int i = threadIdx.x + r * blockDim.x;
+    if (i < n) dst[i] = a[r];
+  }
+}
 
 __device__ void copy_row(float* dst, const float* src, int n) {
   for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = ldcg(src + i);
@@ -638,6 +830,8 @@ __device__ __forceinline__ int checked(const BEnv& e, int v, int hi) {
 // main draw, repetition-aware redraw, clamp, stop (ch.06 §5, §6); then the planes of the stream's
 // hidden state for fast_project_in
 __global__ void __launch_bounds__(kConsumers) k_samp_main(const BEnv e) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(1024) unsigned char smraw[];
   SampScratch& W = *reinterpret_cast<SampScratch*>(smraw);
   __shared__ int flag;
@@ -720,10 +914,12 @@ __global__ void __launch_bounds__(kConsumers) k_samp_main(const BEnv e) {
 // or after the last codebook the Slow-AR input embedding of the frame (normalised likewise)
 __global__ void __launch_bounds__(kConsumers) k_samp_fast(const BEnv e, int cb, const float* part, int splits,
                                                           const void* an_fast0, const void* an_slow0) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(1024) unsigned char smraw[];
   SampScratch& W = *reinterpret_cast<SampScratch*>(smraw);
   __shared__ int flag;
-  __shared__ float red[kPrepThreads / 32];
+  __shared__ float red[kConsumers / 32];
   const Dims& d = e.d;
   const int b = blockIdx.x;
   const BStream& bs = e.bs[b];
@@ -733,11 +929,7 @@ __global__ void __launch_bounds__(kConsumers) k_samp_fast(const BEnv e, int cb, 
   const int f = frame_index(e);
   float* fl = e.bflog + static_cast<size_t>(b) * d.cbs;
   const int NC = e.nb;
-  for (int i = threadIdx.x; i < d.cbs; i += blockDim.x) {
-    float a = 0.f;
-    for (int s = 0; s < splits; ++s) a += ldcg(part + (static_cast<size_t>(s) * NC + b) * d.cbs + i);
-    fl[i] = a;
-  }
+  sum_partials(fl, part, splits, NC, b, d.cbs);
   __threadfence_block();
   __syncthreads();
   if (bs.dbg_fast) copy_row(bs.dbg_fast + (static_cast<size_t>(f) * (d.ncb - 1) + (cb - 1)) * d.cbs, fl, d.cbs);
@@ -766,29 +958,56 @@ __global__ void __launch_bounds__(kConsumers) k_samp_fast(const BEnv e, int cb, 
     tok = ldcgi(&st->vals[0]);
     msem = (tok >= d.sem_lo && tok <= d.sem_hi) ? 1.f : 0.f;
   }
-  float ss = 0.f;
-  for (int k = threadIdx.x; k < K; k += blockDim.x) {
-    float a;
-    if (slow) {
-      float acc = 0.f;
-      for (int c2 = 0; c2 < d.ncb; ++c2) {
-        const int code = c2 == cb ? dc : ldcgi(&st->vals[1 + c2]);
-        acc = __fadd_rn(acc, wload(e.CE, (static_cast<size_t>(c2) * d.cbs + code) * K + k, d.esz));
+  // the row in registers (K <= 12 * 256): codebook-outer accumulation keeps the loads in flight
+  constexpr int RP = (kPrepMaxK + kConsumers - 1) / kConsumers;
+  float v[RP];
+#pragma unroll
+  for (int i = 0; i < RP; ++i) v[i] = 0.f;
+  if (slow) {
+    for (int c2 = 0; c2 < d.ncb; ++c2) {
+      const int code = c2 == cb ? dc : ldcgi(&st->vals[1 + c2]);
+      const size_t row = (static_cast<size_t>(c2) * d.cbs + code) * K;
+#pragma unroll
+      for (int i = 0; i < RP; ++i) {
+        const int k = threadIdx.x + i * kConsumers;
+        if (k < K) v[i] = __fadd_rn(v[i], wload(e.CE, row + k, d.esz));
       }
-      a = __fadd_rn(__fmul_rn(d.sem_scale, wload(e.E, static_cast<size_t>(tok) * K + k, d.esz)), __fmul_rn(msem, acc));
-    } else {
-      a = wload(e.FE, static_cast<size_t>(dc) * K + k, d.esz);
     }
-    xr[k] = a;
-    ss += a * a;
+#pragma unroll
+    for (int i = 0; i < RP; ++i) {
+      const int k = threadIdx.x + i * kConsumers;
+      if (k < K)
+        v[i] = __fadd_rn(__fmul_rn(d.sem_scale, wload(e.E, static_cast<size_t>(tok) * K + k, d.esz)), __fmul_rn(msem, v[i]));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < RP; ++i) {
+      const int k = threadIdx.x + i * kConsumers;
+      if (k < K) v[i] = wload(e.FE, static_cast<size_t>(dc) * K + k, d.esz);
+    }
   }
-  const float r = 1.0f / sqrtf(block_sum256(ss, red) / static_cast<float>(K) + d.eps);
-  for (int k = threadIdx.x; k < K; k += blockDim.x) store_hilo(e.pX, e.ldX, b, k, (ldcg(xr + k) * r) * wload(nw, k, d.esz));
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < RP; ++i) {
+    const int k = threadIdx.x + i * kConsumers;
+    if (k < K) {
+      xr[k] = v[i];
+      ss += v[i] * v[i];
+    }
+  }
+  const float r = 1.0f / sqrtf(block_sum<kConsumers>(ss, red) / static_cast<float>(K) + d.eps);
+#pragma unroll
+  for (int i = 0; i < RP; ++i) {
+    const int k = threadIdx.x + i * kConsumers;
+    if (k < K) store_hilo(e.pX, e.ldX, b, k, (v[i] * r) * wload(nw, k, d.esz));
+  }
 }
 
 // admissible Slow-AR logits of the step: the semantic rows from the partials, im_end by one dot
 // product with the normalised hidden state; then the stream position advances
 __global__ void __launch_bounds__(256) k_logits_fin(const BEnv e, const float* part, int splits) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[8];
   const Dims& d = e.d;
   const int b = blockIdx.x;
@@ -796,16 +1015,12 @@ __global__ void __launch_bounds__(256) k_logits_fin(const BEnv e, const float* p
   if (stream_done(e, sid)) return;
   float* lg = e.logits + static_cast<size_t>(sid) * e.lstride;
   const int NC = e.nb;
-  for (int i = threadIdx.x; i < d.cbs; i += blockDim.x) {
-    float a = 0.f;
-    for (int s = 0; s < splits; ++s) a += ldcg(part + (static_cast<size_t>(s) * NC + b) * d.cbs + i);
-    lg[i] = a;
-  }
+  sum_partials(lg, part, splits, NC, b, d.cbs);
   const float* h = e.hidden + static_cast<size_t>(sid) * d.D;
   float a = 0.f;
   for (int k = threadIdx.x; k < d.D; k += blockDim.x)
     a = fmaf(wload(e.E, static_cast<size_t>(d.im_end) * d.D + k, d.esz), ldcg(h + k), a);
-  a = block_sum256(a, red);
+  a = block_sum<256>(a, red);
   if (threadIdx.x == 0) {
     lg[d.cbs] = a;
     e.st[sid].pos = ldcgi(&e.st[sid].pos) + 1;
@@ -813,12 +1028,16 @@ __global__ void __launch_bounds__(256) k_logits_fin(const BEnv e, const float* p
 }
 
 __global__ void k_call_start(const BEnv e) {
+  pdl_wait();
+  pdl_trigger();
   const int b = threadIdx.x;
   if (b < e.nb) e.st[e.bs[b].sid].n_out = 0;
   if (b == 0) e.bctl[0] = 0;
 }
 
 __global__ void k_frame_end(const BEnv e) {
+  pdl_wait();
+  pdl_trigger();
   if (threadIdx.x == 0) e.bctl[0] = e.bctl[0] + 1;
 }
 
@@ -830,9 +1049,10 @@ __global__ void k_frame_end(const BEnv e) {
 
 namespace {
 
-constexpr int kPrepMaxK = 12 * kPrepThreads;
-
 int round16(int v) { return (v + 15) / 16 * 16; }
+
+// dynamic shared memory of the Slow-AR attention: per warp, kAttnStages groups of 4 K and 4 V rows
+constexpr int attn_smem(int hd) { return 8 * kAttnStages * 2 * 4 * hd * 2; }
 
 struct GemvPlan {
   int tiles, splits, per, atoms, nmat, M, K;
@@ -979,6 +1199,14 @@ Batch* batch_create(const BatchModel& m, std::string* err) {
     delete b;
     return nullptr;
   }
+  if (cudaFuncSetAttribute(k_attn_slow<128, __half>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem(128)) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(k_attn_slow<64, __half>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem(64)) !=
+          cudaSuccess) {
+    *err = "setting the attention kernel's shared memory failed";
+    delete b;
+    return nullptr;
+  }
   const int gsmem = kGemvSmemBudget + 1024 + static_cast<int>(sizeof(GemvBars));
   if (cudaFuncSetAttribute(k_bgemv, cudaFuncAttributeMaxDynamicSharedMemorySize, gsmem) != cudaSuccess) {
     *err = "setting the projection kernel's shared memory failed";
@@ -1003,6 +1231,23 @@ struct Frame {
   int ns;
   bool ok = true;
 
+  // every kernel of the frame may start while its predecessor finishes (programmatic dependent
+  // launch): each one waits for its predecessor's results in pdl_wait before using them
+  template <typename... Exp, typename... Act>
+  void launch(void (*k)(Exp...), dim3 grid, dim3 block, size_t smem, Act&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k, std::forward<Act>(args)...) != cudaSuccess) ok = false;
+  }
+
   const CUtensorMap& planes(uint16_t* buf, int N, int K, int ld) {
     auto key = std::make_tuple(static_cast<const void*>(buf), N, K);
     auto it = b->pmaps.find(key);
@@ -1023,17 +1268,17 @@ struct Frame {
     const int nst = std::min(kMaxGemvStages, kGemvSmemBudget / sbytes);
     const int smem = nst * sbytes + 1024 + static_cast<int>(sizeof(GemvBars));
     dim3 grid(g.tiles, g.splits, g.nmat);
-    k_bgemv<<<grid, kGemvThreads, smem, s>>>(ta, ta2, tb, M, row0, N, NC, g.atoms, g.per, nst, e.part, e.ctl);
+    launch(k_bgemv, grid, kGemvThreads, smem, ta, ta2, tb, M, row0, N, NC, g.atoms, g.per, nst, e.part, e.ctl);
     return g;
   }
 
-  void colprep(const ColPrep& p, int NC) { k_colprep<<<NC, kPrepThreads, 0, s>>>(e, p); }
+  void colprep(const ColPrep& p, int NC) { launch(k_colprep, NC, kPrepThreads, 0, e, p); }
 
   void run() {
     const Dims& d = e.d;
     const BatchModel& m = b->m;
     const size_t samp = sizeof(SampScratch);
-    k_samp_main<<<nb, kConsumers, samp, s>>>(e);
+    launch(k_samp_main, nb, kConsumers, samp, e);
     // Fast-AR call 1: positions 0 (projected hidden) and 1 (fast_embeddings[code_0])
     {
       ColPrep p{};
@@ -1064,9 +1309,9 @@ struct Frame {
         const LayerW& w = m.fast[l];
         GemvPlan g = gemv(w.wqkv, nullptr, QKVf, d.Df, 0, e.pX, e.ldX, NC, false);
         if (d.hdf == 128)
-          k_attn_fast<128><<<nb * d.Hkvf, 256, 0, s>>>(e, l, w.qn, w.kn, e.part, g.splits, npos, pos0, fscale);
+          launch(k_attn_fast<128>, nb * d.Hkvf, 256, 0, e, l, w.qn, w.kn, e.part, g.splits, npos, pos0, fscale);
         else
-          k_attn_fast<64><<<nb * d.Hkvf, 256, 0, s>>>(e, l, w.qn, w.kn, e.part, g.splits, npos, pos0, fscale);
+          launch(k_attn_fast<64>, nb * d.Hkvf, 256, 0, e, l, w.qn, w.kn, e.part, g.splits, npos, pos0, fscale);
         g = gemv(w.wo, nullptr, d.Df, d.Hqf * d.hdf, 0, e.pO, e.ldO, NC, false);
         ColPrep p{};
         p.npos = npos;
@@ -1080,7 +1325,7 @@ struct Frame {
         p.normw = w.fn;
         colprep(p, NC);
         gemv(w.w1, w.w3, d.Ff, d.Df, 0, e.pX, e.ldX, NC, true);
-        k_swiglu<<<dim3((d.Ff + 255) / 256, NC), 256, 0, s>>>(e, e.part, d.Ff, NC);
+        launch(k_swiglu, dim3((d.Ff + 255) / 256, NC), 256, 0, e, e.part, d.Ff, NC);
         g = gemv(w.w2, nullptr, d.Df, d.Ff, 0, e.pH, e.ldH, NC, false);
         p.splits = g.splits;
         const bool last = l == d.Lf - 1;
@@ -1089,7 +1334,7 @@ struct Frame {
         colprep(p, NC);
       }
       const GemvPlan g = gemv(m.FO, nullptr, d.cbs, d.Df, 0, e.pX, e.ldX, nb, false);
-      k_samp_fast<<<nb, kConsumers, samp, s>>>(e, cb, e.part, g.splits, m.fast[0].an, m.slow[0].an);
+      launch(k_samp_fast, nb, kConsumers, samp, e, cb, e.part, g.splits, m.fast[0].an, m.slow[0].an);
     }
     // Slow-AR step
     const float sscale = 1.0f / std::sqrt(static_cast<float>(d.hd));
@@ -1098,11 +1343,13 @@ struct Frame {
       const LayerW& w = m.slow[l];
       GemvPlan g = gemv(w.wqkv, nullptr, QKV, d.D, 0, e.pX, e.ldX, nb, false);
       if (d.hd == 128) {
-        k_attn_slow<128, __half><<<nb * d.Hkv * ns, 256, 0, s>>>(e, l, w.qn, w.kn, e.part, g.splits, ns, sscale);
-        k_attn_comb<128><<<nb * d.Hkv, 256, 0, s>>>(e, ns);
+        launch(k_attn_slow<128, __half>, nb * d.Hkv * ns, 256, attn_smem(128), e, l, w.qn, w.kn, e.part, g.splits, ns,
+                                                                             sscale);
+        launch(k_attn_comb<128>, nb * d.Hkv, 256, 0, e, ns);
       } else {
-        k_attn_slow<64, __half><<<nb * d.Hkv * ns, 256, 0, s>>>(e, l, w.qn, w.kn, e.part, g.splits, ns, sscale);
-        k_attn_comb<64><<<nb * d.Hkv, 256, 0, s>>>(e, ns);
+        launch(k_attn_slow<64, __half>, nb * d.Hkv * ns, 256, attn_smem(64), e, l, w.qn, w.kn, e.part, g.splits, ns,
+                                                                           sscale);
+        launch(k_attn_comb<64>, nb * d.Hkv, 256, 0, e, ns);
       }
       g = gemv(w.wo, nullptr, d.D, d.Hq * d.hd, 0, e.pO, e.ldO, nb, false);
       ColPrep p{};
@@ -1117,7 +1364,7 @@ struct Frame {
       p.normw = w.fn;
       colprep(p, nb);
       gemv(w.w1, w.w3, d.F, d.D, 0, e.pX, e.ldX, nb, true);
-      k_swiglu<<<dim3((d.F + 255) / 256, nb), 256, 0, s>>>(e, e.part, d.F, nb);
+      launch(k_swiglu, dim3((d.F + 255) / 256, nb), 256, 0, e, e.part, d.F, nb);
       g = gemv(w.w2, nullptr, d.D, d.F, 0, e.pH, e.ldH, nb, false);
       p.splits = g.splits;
       const bool last = l == d.L - 1;
@@ -1126,8 +1373,8 @@ struct Frame {
       colprep(p, nb);
     }
     const GemvPlan g = gemv(m.E, nullptr, d.cbs, d.D, d.sem_lo, e.pX, e.ldX, nb, false);
-    k_logits_fin<<<nb, 256, 0, s>>>(e, e.part, g.splits);
-    k_frame_end<<<1, 32, 0, s>>>(e);
+    launch(k_logits_fin, nb, 256, 0, e, e.part, g.splits);
+    launch(k_frame_end, 1, 32, 0, e);
   }
 };
 

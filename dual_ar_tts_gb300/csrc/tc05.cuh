@@ -36,6 +36,14 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+// ------------------------------------------------------------------ dependent launches
+
+// Wait until the grids this one depends on (programmatic stream serialisation) have completed and
+// their memory operations are visible; a no-op without such a dependency.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next grid of the stream to be scheduled (it still waits for this grid in pdl_wait).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ tensor memory
 
 // Whole warp: allocate `ncols` TMEM columns (a power of two >= 32); the base address goes to
