@@ -47,7 +47,7 @@ constexpr int kPrepPer = 3;                       // row elements per thread
 constexpr int kPrepMaxK = kPrepPer * kPrepThreads;  // longest row a column-preparation CTA holds
 constexpr int kAttnTile = 32;               // KV slots per staged tile (Slow-AR attention)
 constexpr int kAttnChunk = 256;             // target slots per Slow-AR attention item
-constexpr int kAttnStages = 4;              // K/V tiles in flight per item
+constexpr int kAttnStages = 3;              // K/V slot groups in flight per warp
 constexpr int kMaxSplitsAttn = 32;          // items per (stream, KV head) at most
 
 enum ColMode : int { CM_RESID = 0, CM_STORE, CM_FEROW, CM_EMBED, CM_HIDDEN };
@@ -408,28 +408,62 @@ __device__ void norm_rope_heads(float* v, int nheads, const void* nw, bool norm,
   __syncthreads();
 }
 
+// tensor-core fragments (mma.sync m16n8k16, fp16 inputs, fp32 accumulation)
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  // rows 8..15 of A are zero (a1 = a3 = 0)
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+// x split as fp16 hi (part 0) or the fp16 remainder x - hi (part 1)
+__device__ __forceinline__ float h_part(float x, int part) {
+  const float hi = __half2float(__float2half_rn(x));
+  return part == 0 ? hi : x - hi;
+}
+
 // Slow-AR: item (stream b, KV head g, split s) over its range of slots; the item whose range
-// holds the new slot normalises, rotates and stores the new K/V first.  Each warp owns every
-// eighth group of 4 slots of the range and runs its own cp.async pipeline (kAttnStages groups in
-// flight), its own online softmax and P·V for the 4 query heads, so the slot loop needs no
-// block-wide barrier; the 8 warps' partial results are combined at the end.
-// Scores: lane = (slot of the group, 16-element chunk of the head dimension), the query chunk in
-// registers, reduced over the 8 chunk lanes by shuffles.  P·V: lane = HD/32 output elements of
-// every head.
+// holds the new slot normalises, rotates and stores the new K/V first.  Each of the 4 warps owns
+// every fourth group of 16 slots of the range and runs its own cp.async pipeline, online softmax
+// and P·V, so the slot loop needs no block-wide barrier; the warps' results are combined at the
+// end.  Scores and P·V run on the tensor cores (mma.sync, fp16 inputs, fp32 accumulation):
+//   S = [q_hi; q_lo] · K^T   rows 0-3 / 4-7 of A = fp16 hi / remainder of the 4 scaled query
+//                            heads (q = hi + lo to ~2^-22), B = the fp16 K rows (ldmatrix)
+//   O += [p_hi; p_lo] · V    A = the probabilities (hi / remainder) taken from the score
+//                            accumulators' registers, B = the fp16 V rows (ldmatrix.trans)
+// and the hi and lo rows are added at the end, so the result carries fp32 precision.
 template <int HD, typename KT>
-__global__ void __launch_bounds__(256, 2) k_attn_slow(const BEnv e, int layer, const void* qn, const void* kn,
+__global__ void __launch_bounds__(128, 2) k_attn_slow(const BEnv e, int layer, const void* qn, const void* kn,
                                                       const float* __restrict__ part, int splits, int ns, float scale) {
   pdl_wait();
   pdl_trigger();
   constexpr int G = 4;                 // query heads per KV head
-  constexpr int CH = HD / 8;           // score chunk per lane
-  constexpr int OE = HD / 32;          // P·V outputs per lane and head
-  constexpr int ROWB = HD * 2;         // bytes of one fp16 row
-  constexpr int QB = 4 * ROWB;         // bytes of the K (or V) rows of one 4-slot group
-  static_assert(sizeof(KT) == 2 && CH % 8 == 0 && OE % 2 == 0, "fp16 cache");
+  constexpr int NW = 4;                // warps
+  constexpr int SG = 16;               // slots per warp step
+  constexpr int RB = HD * 2 + 16;      // padded row bytes (conflict-free ldmatrix)
+  constexpr int STB = SG * RB;         // K (or V) bytes of one step
+  constexpr int KS = HD / 16;          // k-steps of the scores
+  constexpr int NB = HD / 8;           // n-blocks of the output
+  static_assert(sizeof(KT) == 2, "fp16 cache");
   __shared__ __align__(16) float q[G][HD];
   __shared__ float kn_new[HD], vn_new[HD];
-  __shared__ float wm[8][G], wl[8][G];
+  __shared__ float wm[NW][G], wl[NW][G];
   __shared__ float red[8];
   extern __shared__ __align__(1024) unsigned char smraw[];
   const Dims& d = e.d;
@@ -460,19 +494,20 @@ __global__ void __launch_bounds__(256, 2) k_attn_slow(const BEnv e, int layer, c
   const size_t base = ((static_cast<size_t>(layer) * e.max_streams + sid) * d.Hkv + g) * slots * HD;
   KT* Kc = reinterpret_cast<KT*>(e.kc) + base;
   KT* Vc = reinterpret_cast<KT*>(e.vc) + base;
-  // this warp's 4-slot groups: qi = warp, warp + 8, ...
-  const int nq = (s1 - s0 + 3) / 4;
-  const int nstep = nq > warp ? (nq - warp + 7) / 8 : 0;
-  unsigned char* wst = smraw + static_cast<size_t>(warp) * kAttnStages * 2 * QB;
+  // this warp's 16-slot groups: warp, warp + 4, ...
+  const int ngrp = (s1 - s0 + SG - 1) / SG;
+  const int nstep = ngrp > warp ? (ngrp - warp + NW - 1) / NW : 0;
+  unsigned char* wst = smraw + static_cast<size_t>(warp) * kAttnStages * 2 * STB;
   auto stage = [&](int t) {
     if (t < nstep) {
-      const int q0 = s0 + 4 * (warp + 8 * t);
-      const int rows = min(4, s1 - q0);
-      unsigned char* dk = wst + (t % kAttnStages) * 2 * QB;
-      for (int c = lane; c < rows * (ROWB / 16); c += 32) {
-        const int r = c / (ROWB / 16), cc = c % (ROWB / 16);
-        cp_async16(dk + r * ROWB + cc * 16, reinterpret_cast<const unsigned char*>(Kc + static_cast<size_t>(q0 + r) * HD) + cc * 16);
-        cp_async16(dk + QB + r * ROWB + cc * 16,
+      const int q0 = s0 + SG * (warp + NW * t);
+      const int rows = min(SG, s1 - q0);
+      unsigned char* dk = wst + (t % kAttnStages) * 2 * STB;
+      constexpr int CPR = HD * 2 / 16;
+      for (int c = lane; c < rows * CPR; c += 32) {
+        const int r = c / CPR, cc = c % CPR;
+        cp_async16(dk + r * RB + cc * 16, reinterpret_cast<const unsigned char*>(Kc + static_cast<size_t>(q0 + r) * HD) + cc * 16);
+        cp_async16(dk + STB + r * RB + cc * 16,
                    reinterpret_cast<const unsigned char*>(Vc + static_cast<size_t>(q0 + r) * HD) + cc * 16);
       }
     }
@@ -482,33 +517,34 @@ __global__ void __launch_bounds__(256, 2) k_attn_slow(const BEnv e, int layer, c
   for (int t = 0; t < kAttnStages - 1; ++t) stage(t);
   // q of the G heads (and the new k, v) from the split partials: all loads first
   {
-    constexpr int PER = G * HD / 256;
+    constexpr int PER = G * HD / 128;
     float a[PER];
 #pragma unroll
     for (int u = 0; u < PER; ++u) a[u] = 0.f;
     for (int sp = 0; sp < splits; ++sp) {
       const float* pp = part + (static_cast<size_t>(sp) * NC + b) * QKV + (g * G) * HD;
 #pragma unroll
-      for (int u = 0; u < PER; ++u) a[u] += __ldcg(pp + tid + u * 256);
+      for (int u = 0; u < PER; ++u) a[u] += __ldcg(pp + tid + u * 128);
     }
 #pragma unroll
-    for (int u = 0; u < PER; ++u) (&q[0][0])[tid + u * 256] = a[u];
-    if (has_new && tid < HD) {
-      float kk = 0.f, vv = 0.f;
-      for (int sp = 0; sp < splits; ++sp) {
-        const float* pp = part + (static_cast<size_t>(sp) * NC + b) * QKV;
-        kk += __ldcg(pp + d.Hq * HD + g * HD + tid);
-        vv += __ldcg(pp + (d.Hq + d.Hkv) * HD + g * HD + tid);
+    for (int u = 0; u < PER; ++u) (&q[0][0])[tid + u * 128] = a[u];
+    if (has_new)
+      for (int t = tid; t < HD; t += 128) {
+        float kk = 0.f, vv = 0.f;
+        for (int sp = 0; sp < splits; ++sp) {
+          const float* pp = part + (static_cast<size_t>(sp) * NC + b) * QKV;
+          kk += __ldcg(pp + d.Hq * HD + g * HD + t);
+          vv += __ldcg(pp + (d.Hq + d.Hkv) * HD + g * HD + t);
+        }
+        kn_new[t] = kk;
+        vn_new[t] = vv;
       }
-      kn_new[tid] = kk;
-      vn_new[tid] = vv;
-    }
   }
   const float2* rrow = e.rope + static_cast<size_t>(pos) * (HD / 2);
   norm_rope_heads<HD>(&q[0][0], G, qn, d.qk_norm != 0, d.esz, d.eps, rrow, red);
   if (has_new) {
     norm_rope_heads<HD>(kn_new, 1, kn, d.qk_norm != 0, d.esz, d.eps, rrow, red);
-    for (int t = tid; t < HD; t += 256) {
+    for (int t = tid; t < HD; t += 128) {
       const KT kq = tokv<KT>(kn_new[t]), vq = tokv<KT>(vn_new[t]);
       Kc[static_cast<size_t>(pos) * HD + t] = kq;
       Vc[static_cast<size_t>(pos) * HD + t] = vq;
@@ -517,122 +553,128 @@ __global__ void __launch_bounds__(256, 2) k_attn_slow(const BEnv e, int layer, c
     }
     __syncthreads();
   }
-  const int sl = lane >> 3, kc = lane & 7;
-  float qr[G][CH];
+  // A fragments of the scaled queries: row gq = lane/4 (< 8: head gq & 3, hi or remainder part)
+  const int gq = lane >> 2, tq = lane & 3, hq = gq & 3, partq = gq >> 2;
+  uint32_t qa[KS][2];
 #pragma unroll
-  for (int h = 0; h < G; ++h)
-#pragma unroll
-    for (int u = 0; u < CH; ++u) qr[h][u] = q[h][kc * CH + u] * scale;
-  float o[G][OE];
-  float mw[G], lw[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    mw[h] = -INFINITY;
-    lw[h] = 0.f;
-#pragma unroll
-    for (int u = 0; u < OE; ++u) o[h][u] = 0.f;
+  for (int ks = 0; ks < KS; ++ks) {
+    const int e0 = 16 * ks + 2 * tq;
+    qa[ks][0] = pack_h2(h_part(q[hq][e0] * scale, partq), h_part(q[hq][e0 + 1] * scale, partq));
+    qa[ks][1] = pack_h2(h_part(q[hq][e0 + 8] * scale, partq), h_part(q[hq][e0 + 9] * scale, partq));
   }
+  float o[NB][4];
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb) o[nb][0] = o[nb][1] = o[nb][2] = o[nb][3] = 0.f;
+  float m_run = -INFINITY, l_run = 0.f;  // of head hq
+  const int lr = lane & 7, lm = lane >> 3;  // ldmatrix: row within a matrix, matrix index
   for (int t = 0; t < nstep; ++t) {
     stage(t + kAttnStages - 1);
     cp_async_wait_group<kAttnStages - 1>();
     __syncwarp();
-    const int q0 = s0 + 4 * (warp + 8 * t);
-    unsigned char* dk = wst + (t % kAttnStages) * 2 * QB;
-    if (has_new && pos >= q0 && pos < q0 + 4) {
+    const int q0 = s0 + SG * (warp + NW * t);
+    const int rows = min(SG, s1 - q0);
+    unsigned char* dk = wst + (t % kAttnStages) * 2 * STB;
+    unsigned char* dv = dk + STB;
+    if (has_new && pos >= q0 && pos < q0 + SG) {
       // the copy of the new slot may predate its store: use the values computed here
-      KT* kr = reinterpret_cast<KT*>(dk + (pos - q0) * ROWB);
-      KT* vr = reinterpret_cast<KT*>(dk + QB + (pos - q0) * ROWB);
+      KT* kr = reinterpret_cast<KT*>(dk + (pos - q0) * RB);
+      KT* vr = reinterpret_cast<KT*>(dv + (pos - q0) * RB);
       for (int u = lane; u < HD; u += 32) {
         kr[u] = tokv<KT>(kn_new[u]);
         vr[u] = tokv<KT>(vn_new[u]);
       }
-      __syncwarp();
     }
-    const bool valid = q0 + sl < s1;
-    float sc[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) sc[h] = 0.f;
-    if (valid) {
-      const uint4* kr = reinterpret_cast<const uint4*>(dk + sl * ROWB + kc * CH * 2);
-#pragma unroll
-      for (int w = 0; w < CH / 8; ++w) {
-        const uint4 u4 = kr[w];
-        const uint32_t wd[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const float2 kv = __half22float2(*reinterpret_cast<const __half2*>(&wd[x]));
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            sc[h] = fmaf(qr[h][w * 8 + 2 * x], kv.x, sc[h]);
-            sc[h] = fmaf(qr[h][w * 8 + 2 * x + 1], kv.y, sc[h]);
-          }
-        }
+    if (rows < SG) {
+      // rows past the range: zero V (their probability is 0, and 0 * stale data must stay 0)
+      for (int c = lane; c < (SG - rows) * (HD / 2); c += 32) {
+        const int r = rows + c / (HD / 2), cc = c % (HD / 2);
+        reinterpret_cast<uint32_t*>(dv + r * RB)[cc] = 0u;
+        reinterpret_cast<uint32_t*>(dk + r * RB)[cc] = 0u;
       }
     }
-    float pr[G];
+    __syncwarp();
+    // scores of the two 8-slot blocks
+    float sc[2][4];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float v = sc[h];
-      v += __shfl_xor_sync(0xffffffffu, v, 1);
-      v += __shfl_xor_sync(0xffffffffu, v, 2);
-      v += __shfl_xor_sync(0xffffffffu, v, 4);
-      v = valid ? v : -INFINITY;
-      float mq = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-      mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, 16));
-      const float mn = fmaxf(mw[h], mq);
-      const float p = valid ? expf(v - mn) : 0.f;
-      const float cf = mw[h] == -INFINITY ? 0.f : expf(mw[h] - mn);
-      float ps = p + __shfl_xor_sync(0xffffffffu, p, 8);
-      ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-      lw[h] = lw[h] * cf + ps;
-      mw[h] = mn;
+    for (int blk = 0; blk < 2; ++blk) {
+      sc[blk][0] = sc[blk][1] = sc[blk][2] = sc[blk][3] = 0.f;
 #pragma unroll
-      for (int u = 0; u < OE; ++u) o[h][u] *= cf;
-      pr[h] = p;
+      for (int ks = 0; ks < KS; ks += 2) {
+        uint32_t bf[4];
+        // matrices: (slots blk*8.., e 16ks), (.., 16ks+8), (.., 16ks+16), (.., 16ks+24)
+        ldsm_x4(smem_u32(dk + (blk * 8 + lr) * RB + (16 * ks + 8 * lm) * 2), bf);
+        mma_f16(sc[blk], qa[ks][0], qa[ks][1], bf[0], bf[1]);
+        mma_f16(sc[blk], qa[ks + 1][0], qa[ks + 1][1], bf[2], bf[3]);
+      }
     }
+    // full scores (hi + remainder rows), masked; lane holds head hq, slots blk*8 + 2tq + {0,1}
+    float v[4];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      if (q0 + r >= s1) break;
-      const KT* vr = reinterpret_cast<const KT*>(dk + QB + r * ROWB) + lane * OE;
-      float vv[OE];
+    for (int blk = 0; blk < 2; ++blk)
 #pragma unroll
-      for (int u = 0; u < OE; u += 2) {
-        const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(vr + u));
-        vv[u] = f2.x;
-        vv[u + 1] = f2.y;
+      for (int c = 0; c < 2; ++c) {
+        const float x = sc[blk][c] + __shfl_xor_sync(0xffffffffu, sc[blk][c], 16);
+        v[blk * 2 + c] = (blk * 8 + 2 * tq + c < rows) ? x : -INFINITY;
       }
+    float mt = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+    const float mn = fmaxf(m_run, mt);
+    const float cf = m_run == -INFINITY ? 0.f : expf(m_run - mn);
+    float pv[4], ps = 0.f;
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float ph = __shfl_sync(0xffffffffu, pr[h], r * 8);
+    for (int u = 0; u < 4; ++u) {
+      pv[u] = v[u] == -INFINITY ? 0.f : expf(v[u] - mn);
+      ps += pv[u];
+    }
+    ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+    ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+    l_run = l_run * cf + ps;
+    m_run = mn;
 #pragma unroll
-        for (int u = 0; u < OE; ++u) o[h][u] = fmaf(ph, vv[u], o[h][u]);
-      }
+    for (int nb = 0; nb < NB; ++nb) {
+      o[nb][0] *= cf;
+      o[nb][1] *= cf;
+    }
+    // P as the A operand: row gq = head hq, hi (gq < 4) or remainder; k = slot of the group
+    const uint32_t pa0 = pack_h2(h_part(pv[0], partq), h_part(pv[1], partq));
+    const uint32_t pa2 = pack_h2(h_part(pv[2], partq), h_part(pv[3], partq));
+#pragma unroll
+    for (int nbp = 0; nbp < NB / 2; ++nbp) {
+      uint32_t bf[4];
+      // matrices: (slots 0-7, e 16nbp), (slots 8-15, e 16nbp), (slots 0-7, e 16nbp+8), (slots 8-15, ..)
+      ldsm_x4_t(smem_u32(dv + ((lm & 1) * 8 + lr) * RB + (16 * nbp + 8 * (lm >> 1)) * 2), bf);
+      mma_f16(o[2 * nbp], pa0, pa2, bf[0], bf[1]);
+      mma_f16(o[2 * nbp + 1], pa0, pa2, bf[2], bf[3]);
     }
     __syncwarp();
   }
   cp_async_wait_group<0>();
   __syncwarp();
-  // the warp's partial result into its own staging area, then the 8 warps combined
+  // the warp's result (hi + remainder rows added) into its own staging area, then combined
   float* ow = reinterpret_cast<float*>(wst);
 #pragma unroll
-  for (int h = 0; h < G; ++h)
+  for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-    for (int u = 0; u < OE; ++u) ow[h * HD + lane * OE + u] = o[h][u];
-  if (lane < G) {
-    wm[warp][lane] = mw[lane];
-    wl[warp][lane] = lw[lane];
+    for (int c = 0; c < 2; ++c) {
+      const float x = o[nb][c] + __shfl_xor_sync(0xffffffffu, o[nb][c], 16);
+      if (partq == 0) ow[hq * HD + nb * 8 + 2 * tq + c] = x;
+    }
+  if (lane < 16 && (lane & 3) == 0) {
+    wm[warp][hq] = m_run;
+    wl[warp][hq] = l_run;
   }
   __syncthreads();
-  for (int t2 = tid; t2 < G * HD; t2 += 256) {
+  for (int t2 = tid; t2 < G * HD; t2 += 128) {
     const int h = t2 / HD;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) M = fmaxf(M, wm[w][h]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, wm[w][h]);
     float acc = 0.f, l = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
+    for (int w = 0; w < NW; ++w) {
       const float cw = wm[w][h] == -INFINITY ? 0.f : expf(wm[w][h] - M);
-      acc = fmaf(cw, reinterpret_cast<const float*>(smraw + static_cast<size_t>(w) * kAttnStages * 2 * QB)[t2], acc);
+      acc = fmaf(cw, reinterpret_cast<const float*>(smraw + static_cast<size_t>(w) * kAttnStages * 2 * STB)[t2], acc);
       l = fmaf(cw, wl[w][h], l);
     }
     outp[t2] = acc;
@@ -1051,8 +1093,9 @@ namespace {
 
 int round16(int v) { return (v + 15) / 16 * 16; }
 
-// dynamic shared memory of the Slow-AR attention: per warp, kAttnStages groups of 4 K and 4 V rows
-constexpr int attn_smem(int hd) { return 8 * kAttnStages * 2 * 4 * hd * 2; }
+// dynamic shared memory of the Slow-AR attention: per warp, kAttnStages groups of 16 K and 16 V
+// rows (padded)
+constexpr int attn_smem(int hd) { return 4 * kAttnStages * 2 * 16 * (hd * 2 + 16); }
 
 struct GemvPlan {
   int tiles, splits, per, atoms, nmat, M, K;
@@ -1343,11 +1386,11 @@ struct Frame {
       const LayerW& w = m.slow[l];
       GemvPlan g = gemv(w.wqkv, nullptr, QKV, d.D, 0, e.pX, e.ldX, nb, false);
       if (d.hd == 128) {
-        launch(k_attn_slow<128, __half>, nb * d.Hkv * ns, 256, attn_smem(128), e, l, w.qn, w.kn, e.part, g.splits, ns,
+        launch(k_attn_slow<128, __half>, nb * d.Hkv * ns, 128, attn_smem(128), e, l, w.qn, w.kn, e.part, g.splits, ns,
                                                                              sscale);
         launch(k_attn_comb<128>, nb * d.Hkv, 256, 0, e, ns);
       } else {
-        launch(k_attn_slow<64, __half>, nb * d.Hkv * ns, 256, attn_smem(64), e, l, w.qn, w.kn, e.part, g.splits, ns,
+        launch(k_attn_slow<64, __half>, nb * d.Hkv * ns, 128, attn_smem(64), e, l, w.qn, w.kn, e.part, g.splits, ns,
                                                                            sscale);
         launch(k_attn_comb<64>, nb * d.Hkv, 256, 0, e, ns);
       }
