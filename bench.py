@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--batched", default="serving", choices=["serving", "longctx", "none"],
                     help="also measure the aggregate of a batched workload (reported under 'batched')")
     ap.add_argument("--batched-steps", type=int, default=16)
+    ap.add_argument("--batched-streams", type=int, default=None,
+                    help="profiling captures only: the first N streams of the batched workload")
     ap.add_argument("--slow-layers", type=int, default=None,
                     help="profiling captures only: Slow-AR layer count (S2-Pro widths kept); the bench line "
                          "then describes that smaller model")
@@ -162,7 +164,7 @@ def max_over_ranks(v, world):
     return float(t.item())
 
 
-def batched_measure(pkg, d, dev_w, cfg_name, steps, warmup, peak, local):
+def batched_measure(pkg, d, dev_w, cfg_name, steps, warmup, peak, local, n_streams=None):
     """Aggregate frames/s of a batched workload: every stream of the workload decoded in one call
     (weights read once per step for the whole batch).  Each stream's decode state (its context's
     fp16 K/V, its last residual) is imported from seeded device-side random values: the KV
@@ -174,6 +176,9 @@ def batched_measure(pkg, d, dev_w, cfg_name, steps, warmup, peak, local):
     cfg = synth.CONFIGS[cfg_name]
     n, slots, seed = cfg["streams"], cfg["kv_slots"], cfg["input_seed"]
     lengths = synth.prompt_lengths(cfg_name)
+    if n_streams:
+        n = min(n, n_streams)
+        lengths = lengths[:n]
     kmax = max(lengths)
     dec = pkg.Decoder(d, dev_w, max_streams=n, kv_slots=slots)
     g = torch.Generator(device="cuda")
@@ -366,10 +371,11 @@ def main():
         "clocks": clk.summary(),
         "setup_s": setup_s,
     }
-    if args.batched != "none" and args.slow_layers is None:
+    if args.batched != "none":
         dec.close()
         torch.cuda.empty_cache()
-        line["batched"] = batched_measure(pkg, d, dev_w, args.batched, args.batched_steps, args.warmup, pk, local)
+        line["batched"] = batched_measure(pkg, d, dev_w, args.batched, args.batched_steps, args.warmup, pk, local,
+                                          args.batched_streams)
     if rank == 0 and not args.no_cpu_baseline and args.slow_layers is None:
         try:
             v, cores, sample = cpu_oracle_sample(d, host_w, args.cpu_frames, s)

@@ -41,12 +41,13 @@ constexpr int kAtom = 64;                   // K elements per pipeline stage (on
 constexpr int kABytes = kTileM * kAtom * 2;  // one weight tile
 constexpr int kGemvThreads = 192;           // 4 epilogue warps, 1 TMA warp, 1 MMA warp
 constexpr int kMaxGemvStages = 8;
-constexpr int kGemvSmemBudget = 200 * 1024;
+constexpr int kGemvSmemBudget = 100 * 1024;  // two CTAs per SM
+constexpr int kGemvCtasPerSm = 2;
 constexpr int kPrepThreads = 1024;                // column preparation: one CTA per column
 constexpr int kPrepPer = 3;                       // row elements per thread
 constexpr int kPrepMaxK = kPrepPer * kPrepThreads;  // longest row a column-preparation CTA holds
 constexpr int kAttnTile = 32;               // KV slots per staged tile (Slow-AR attention)
-constexpr int kAttnChunk = 256;             // target slots per Slow-AR attention item
+constexpr int kAttnChunk = 1024;            // target slots per Slow-AR attention item
 constexpr int kAttnStages = 3;              // K/V slot groups in flight per warp
 constexpr int kMaxSplitsAttn = 32;          // items per (stream, KV head) at most
 
@@ -141,7 +142,7 @@ struct GemvBars {
   uint32_t taddr;
 };
 
-__global__ void __launch_bounds__(kGemvThreads, 1)
+__global__ void __launch_bounds__(kGemvThreads, kGemvCtasPerSm)
     k_bgemv(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
             const __grid_constant__ CUtensorMap tmB, int M, int row0, int N, int NC, int atoms_total, int atoms_per,
             int nstages, float* part, Control* ctl) {
@@ -343,16 +344,20 @@ __global__ void __launch_bounds__(kPrepThreads) k_colprep(const BEnv e, const Co
   }
 }
 
-// SwiGLU of the two projections (partials of W1 then W3, one split): planes of silu(g)·u
-__global__ void __launch_bounds__(256) k_swiglu(const BEnv e, const float* part, int M, int NC) {
+// SwiGLU of the two projections (split partials of W1, then of W3): planes of silu(g)·u
+__global__ void __launch_bounds__(256) k_swiglu(const BEnv e, const float* __restrict__ part, int M, int NC,
+                                                int splits) {
   pdl_wait();
   pdl_trigger();
   const int c = blockIdx.y;
   const int sid = e.bs[c / (NC / e.nb)].sid;
   if (stream_done(e, sid)) return;
   for (int m = blockIdx.x * blockDim.x + threadIdx.x; m < M; m += gridDim.x * blockDim.x) {
-    const float a = ldcg(part + static_cast<size_t>(c) * M + m);
-    const float u = ldcg(part + (static_cast<size_t>(NC) + c) * M + m);
+    float a = 0.f, u = 0.f;
+    for (int s = 0; s < splits; ++s) {
+      a += __ldcg(part + (static_cast<size_t>(s) * NC + c) * M + m);
+      u += __ldcg(part + (static_cast<size_t>(splits + s) * NC + c) * M + m);
+    }
     store_hilo(e.pH, e.ldH, c, m, (a / (1.0f + expf(-a))) * u);
   }
 }
@@ -1184,19 +1189,19 @@ BatchSizes batch_sizes(const Dims& d, int max_streams, int sms) {
   const int QKV = (d.Hq + 2 * d.Hkv) * d.hd, QKVf = (d.Hqf + 2 * d.Hkvf) * d.hdf;
   size_t mx = 0;
   auto acc = [&](int M, int K, int nmat, bool whole, int nc) {
-    const GemvPlan g = plan_gemv(M, K, nmat, sms, whole);
+    const GemvPlan g = plan_gemv(M, K, nmat, kGemvCtasPerSm * sms, whole);
     mx = std::max(mx, static_cast<size_t>(g.nmat) * g.splits * nc * M);
   };
   acc(QKV, d.D, 1, false, max_streams);
   acc(d.D, d.Hq * d.hd, 1, false, max_streams);
-  acc(d.F, d.D, 2, true, max_streams);
+  acc(d.F, d.D, 2, false, max_streams);
   acc(d.D, d.F, 1, false, max_streams);
   acc(d.cbs, d.D, 1, false, max_streams);
   acc(d.Df, d.D, 1, false, max_streams);
   acc(d.cbs, d.Df, 1, false, max_streams);
   acc(QKVf, d.Df, 1, false, ncmax);
   acc(d.Df, d.Hqf * d.hdf, 1, false, ncmax);
-  acc(d.Ff, d.Df, 2, true, ncmax);
+  acc(d.Ff, d.Df, 2, false, ncmax);
   acc(d.Df, d.Ff, 1, false, ncmax);
   z.part_floats = mx;
   z.apart_floats = static_cast<size_t>(max_streams) * d.Hkv * kMaxSplitsAttn * 4 * (d.hd + 2);
@@ -1302,7 +1307,7 @@ struct Frame {
 
   // projection of NC columns; returns the plan (partials layout)
   GemvPlan gemv(const void* w0, const void* w1, int M, int K, int row0, uint16_t* pl, int ld, int NC, bool whole_k) {
-    const GemvPlan g = plan_gemv(M, K, w1 ? 2 : 1, b->m.sms, whole_k);
+    const GemvPlan g = plan_gemv(M, K, w1 ? 2 : 1, kGemvCtasPerSm * b->m.sms, whole_k);
     const int N = round16(2 * NC);
     const CUtensorMap& ta = b->wmaps.at(w0);
     const CUtensorMap& ta2 = w1 ? b->wmaps.at(w1) : ta;
@@ -1367,8 +1372,8 @@ struct Frame {
         p.xb = 2 * d.Df;
         p.normw = w.fn;
         colprep(p, NC);
-        gemv(w.w1, w.w3, d.Ff, d.Df, 0, e.pX, e.ldX, NC, true);
-        launch(k_swiglu, dim3((d.Ff + 255) / 256, NC), 256, 0, e, e.part, d.Ff, NC);
+        g = gemv(w.w1, w.w3, d.Ff, d.Df, 0, e.pX, e.ldX, NC, false);
+        launch(k_swiglu, dim3((d.Ff + 255) / 256, NC), 256, 0, e, e.part, d.Ff, NC, g.splits);
         g = gemv(w.w2, nullptr, d.Df, d.Ff, 0, e.pH, e.ldH, NC, false);
         p.splits = g.splits;
         const bool last = l == d.Lf - 1;
@@ -1406,8 +1411,8 @@ struct Frame {
       p.xb = d.D;
       p.normw = w.fn;
       colprep(p, nb);
-      gemv(w.w1, w.w3, d.F, d.D, 0, e.pX, e.ldX, nb, true);
-      launch(k_swiglu, dim3((d.F + 255) / 256, nb), 256, 0, e, e.part, d.F, nb);
+      g = gemv(w.w1, w.w3, d.F, d.D, 0, e.pX, e.ldX, nb, false);
+      launch(k_swiglu, dim3((d.F + 255) / 256, nb), 256, 0, e, e.part, d.F, nb, g.splits);
       g = gemv(w.w2, nullptr, d.D, d.F, 0, e.pH, e.ldH, nb, false);
       p.splits = g.splits;
       const bool last = l == d.L - 1;
