@@ -43,6 +43,7 @@ constexpr int kGemvThreads = 192;           // 4 epilogue warps, 1 TMA warp, 1 M
 constexpr int kMaxGemvStages = 8;
 constexpr int kGemvSmemBudget = 100 * 1024;  // two CTAs per SM
 constexpr int kGemvCtasPerSm = 2;
+constexpr int kSamplerSplits = 4;             // split-K of projections summed by one CTA per stream
 constexpr int kPrepThreads = 1024;                // column preparation: one CTA per column
 constexpr int kPrepPer = 3;                       // row elements per thread
 constexpr int kPrepMaxK = kPrepPer * kPrepThreads;  // longest row a column-preparation CTA holds
@@ -290,13 +291,22 @@ __global__ void __launch_bounds__(kPrepThreads) k_colprep(const BEnv e, const Co
       const int k = tid + i * kPrepThreads;
       v[i] = (mode == CM_RESID && k < K) ? __ldcg(xr + k) : 0.f;
     }
-    for (int s = 0; s < p.splits; ++s) {
-      const float* ps = p.part + (static_cast<size_t>(s) * p.part_nc + pcol) * K;
+    // four splits per round: their loads are issued together (the sums keep split order)
+    const size_t sstride = static_cast<size_t>(p.part_nc) * K;
+    const float* pc = p.part + static_cast<size_t>(pcol) * K;
+    for (int s = 0; s < p.splits; s += 4) {
+      float t[4][kMaxPer];
 #pragma unroll
-      for (int i = 0; i < kMaxPer; ++i) {
-        const int k = tid + i * kPrepThreads;
-        if (k < K) v[i] += __ldcg(ps + k);
-      }
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int i = 0; i < kMaxPer; ++i) {
+          const int k = tid + i * kPrepThreads;
+          t[j][i] = (s + j < p.splits && k < K) ? __ldcg(pc + (s + j) * sstride + k) : 0.f;
+        }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int i = 0; i < kMaxPer; ++i) v[i] += t[j][i];
     }
   }
 #pragma unroll
@@ -526,6 +536,7 @@ __global__ void __launch_bounds__(128, 2) k_attn_slow(const BEnv e, int layer, c
     float a[PER];
 #pragma unroll
     for (int u = 0; u < PER; ++u) a[u] = 0.f;
+#pragma unroll 4
     for (int sp = 0; sp < splits; ++sp) {
       const float* pp = part + (static_cast<size_t>(sp) * NC + b) * QKV + (g * G) * HD;
 #pragma unroll
@@ -536,7 +547,8 @@ __global__ void __launch_bounds__(128, 2) k_attn_slow(const BEnv e, int layer, c
     if (has_new)
       for (int t = tid; t < HD; t += 128) {
         float kk = 0.f, vv = 0.f;
-        for (int sp = 0; sp < splits; ++sp) {
+    #pragma unroll 4
+    for (int sp = 0; sp < splits; ++sp) {
           const float* pp = part + (static_cast<size_t>(sp) * NC + b) * QKV;
           kk += __ldcg(pp + d.Hq * HD + g * HD + t);
           vv += __ldcg(pp + (d.Hq + d.Hkv) * HD + g * HD + t);
@@ -779,7 +791,8 @@ __global__ void __launch_bounds__(256) k_attn_fast(const BEnv e, int layer, cons
       float kk = 0.f, vv = 0.f;
 #pragma unroll
       for (int u = 0; u < PER; ++u) a[u] = 0.f;
-      for (int sp = 0; sp < splits; ++sp) {
+  #pragma unroll 4
+    for (int sp = 0; sp < splits; ++sp) {
         const float* pp = part + (static_cast<size_t>(sp) * NC + c) * QKV;
 #pragma unroll
         for (int u = 0; u < PER; ++u) a[u] += __ldcg(pp + (g * G) * HD + tid + u * 256);
@@ -847,13 +860,19 @@ __device__ void sum_partials(float* dst, const float* __restrict__ part, int spl
   float a[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) a[r] = 0.f;
-  for (int s = 0; s < splits; ++s) {
+  for (int s = 0; s < splits; s += 2) {
     const float* ps = part + (static_cast<size_t>(s) * NC + col) * n;
+    const float* ps2 = ps + static_cast<size_t>(NC) * n;
+    const bool two = s + 1 < splits;
+    float t0[R], t1[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int i = threadIdx.x + r * blockDim.x;
-      if (i < n) a[r] += __ldcg(ps + i);
+      t0[r] = i < n ? __ldcg(ps + i) : 0.f;
+      t1[r] = (two && i < n) ? __ldcg(ps2 + i) : 0.f;
     }
+#pragma unroll
+    for (int r = 0; r < R; ++r) a[r] = (a[r] + t0[r]) + t1[r];
   }
 #pragma unroll
   for (int r = 0; r < R; ++r) {
@@ -1011,9 +1030,15 @@ __global__ void __launch_bounds__(kConsumers) k_samp_fast(const BEnv e, int cb, 
 #pragma unroll
   for (int i = 0; i < RP; ++i) v[i] = 0.f;
   if (slow) {
-    for (int c2 = 0; c2 < d.ncb; ++c2) {
-      const int code = c2 == cb ? dc : ldcgi(&st->vals[1 + c2]);
-      const size_t row = (static_cast<size_t>(c2) * d.cbs + code) * K;
+    // the frame's codes (this CTA drew them: its bfcode row), then every codebook row's loads
+    // issued together; the sum keeps codebook order
+    int codes[kMaxCodebooks];
+#pragma unroll
+    for (int c2 = 0; c2 < kMaxCodebooks; ++c2) codes[c2] = c2 < d.ncb ? (c2 == cb ? dc : e.bfcode[b * 16 + c2]) : 0;
+#pragma unroll
+    for (int c2 = 0; c2 < kMaxCodebooks; ++c2) {
+      if (c2 >= d.ncb) break;
+      const size_t row = (static_cast<size_t>(c2) * d.cbs + codes[c2]) * K;
 #pragma unroll
       for (int i = 0; i < RP; ++i) {
         const int k = threadIdx.x + i * kConsumers;
@@ -1106,14 +1131,14 @@ struct GemvPlan {
   int tiles, splits, per, atoms, nmat, M, K;
 };
 
-GemvPlan plan_gemv(int M, int K, int nmat, int sms, bool whole_k) {
+GemvPlan plan_gemv(int M, int K, int nmat, int sms, bool whole_k, int max_splits = 1 << 30) {
   GemvPlan g{};
   g.M = M;
   g.K = K;
   g.nmat = nmat;
   g.atoms = K / kAtom;
   g.tiles = (M + kTileM - 1) / kTileM;
-  int splits = whole_k ? 1 : std::max(1, std::min(g.atoms, sms / std::max(1, g.tiles * nmat)));
+  int splits = whole_k ? 1 : std::max(1, std::min(std::min(g.atoms, max_splits), sms / std::max(1, g.tiles * nmat)));
   g.per = (g.atoms + splits - 1) / splits;
   g.splits = (g.atoms + g.per - 1) / g.per;
   return g;
@@ -1306,8 +1331,9 @@ struct Frame {
   }
 
   // projection of NC columns; returns the plan (partials layout)
-  GemvPlan gemv(const void* w0, const void* w1, int M, int K, int row0, uint16_t* pl, int ld, int NC, bool whole_k) {
-    const GemvPlan g = plan_gemv(M, K, w1 ? 2 : 1, kGemvCtasPerSm * b->m.sms, whole_k);
+  GemvPlan gemv(const void* w0, const void* w1, int M, int K, int row0, uint16_t* pl, int ld, int NC, bool whole_k,
+               int max_splits = 1 << 30) {
+    const GemvPlan g = plan_gemv(M, K, w1 ? 2 : 1, kGemvCtasPerSm * b->m.sms, whole_k, max_splits);
     const int N = round16(2 * NC);
     const CUtensorMap& ta = b->wmaps.at(w0);
     const CUtensorMap& ta2 = w1 ? b->wmaps.at(w1) : ta;
@@ -1381,7 +1407,8 @@ struct Frame {
         p.last_only = last ? 1 : 0;
         colprep(p, NC);
       }
-      const GemvPlan g = gemv(m.FO, nullptr, d.cbs, d.Df, 0, e.pX, e.ldX, nb, false);
+      // its partials are summed by one CTA per stream: few splits
+      const GemvPlan g = gemv(m.FO, nullptr, d.cbs, d.Df, 0, e.pX, e.ldX, nb, false, kSamplerSplits);
       launch(k_samp_fast, nb, kConsumers, samp, e, cb, e.part, g.splits, m.fast[0].an, m.slow[0].an);
     }
     // Slow-AR step
@@ -1420,7 +1447,7 @@ struct Frame {
       p.hid_out = last ? e.hidden : nullptr;
       colprep(p, nb);
     }
-    const GemvPlan g = gemv(m.E, nullptr, d.cbs, d.D, d.sem_lo, e.pX, e.ldX, nb, false);
+    const GemvPlan g = gemv(m.E, nullptr, d.cbs, d.D, d.sem_lo, e.pX, e.ldX, nb, false, kSamplerSplits);
     launch(k_logits_fin, nb, 256, 0, e, e.part, g.splits);
     launch(k_frame_end, 1, 32, 0, e);
   }
