@@ -44,6 +44,7 @@ constexpr int kMaxGemvStages = 8;
 constexpr int kGemvSmemBudget = 100 * 1024;  // two CTAs per SM
 constexpr int kGemvCtasPerSm = 2;
 constexpr int kSamplerSplits = 4;             // split-K of projections summed by one CTA per stream
+constexpr int kPrefillCols = 128;             // prompt positions per projection launch (N = 256)
 constexpr int kPrepThreads = 1024;                // column preparation: one CTA per column
 constexpr int kPrepPer = 3;                       // row elements per thread
 constexpr int kPrepMaxK = kPrepPer * kPrepThreads;  // longest row a column-preparation CTA holds
@@ -1193,7 +1194,7 @@ bool batch_supported(const Dims& d, int max_streams, std::string* why) {
   };
   if (d.wdt != S2_BF16 || d.kvdt != S2_F16) return no("batched decode needs bf16 weights and an fp16 KV cache");
   if (d.L == 0) return no("no Slow-AR");
-  if (max_streams < 2 || max_streams > 64) return no("batched decode serves 2..64 streams per context");
+  if (max_streams < 1 || max_streams > 64) return no("batched decode serves up to 64 streams per context");
   if (d.hd != 128 && d.hd != 64) return no("head_dim must be 64 or 128");
   if (d.Hq != 4 * d.Hkv || d.Hqf != 4 * d.Hkvf) return no("batched attention assumes 4 query heads per KV head");
   const int ks[6] = {d.D, d.Df, d.F, d.Ff, d.Hq * d.hd, d.Hqf * d.hdf};
@@ -1287,6 +1288,44 @@ Batch* batch_create(const BatchModel& m, std::string* err) {
     return nullptr;
   }
   return b;
+}
+
+int batch_prefill_proj(Batch* b, const void* w0, const void* w1, int M, int K, const uint16_t* planes, int ld, int NC,
+                       float* part, void* stream) {
+  if (NC < 1 || NC > kPrefillCols || K % kAtom != 0) return -1;
+  const GemvPlan g = plan_gemv(M, K, w1 ? 2 : 1, kGemvCtasPerSm * b->m.sms, false);
+  const int N = round16(2 * NC);
+  auto wa = b->wmaps.find(w0);
+  auto wb = b->wmaps.find(w1 ? w1 : w0);
+  if (wa == b->wmaps.end() || wb == b->wmaps.end()) return -1;
+  auto key = std::make_tuple(static_cast<const void*>(planes), N, K);
+  auto it = b->pmaps.find(key);
+  if (it == b->pmaps.end()) {
+    CUtensorMap t;
+    if (!encode_map(&t, planes, K, N, ld, N)) return -1;
+    it = b->pmaps.emplace(key, t).first;
+  }
+  const int sbytes = kABytes + N * 128;
+  const int nst = std::min(kMaxGemvStages, kGemvSmemBudget / sbytes);
+  const int smem = nst * sbytes + 1024 + static_cast<int>(sizeof(GemvBars));
+  dim3 grid(g.tiles, g.splits, g.nmat);
+  k_bgemv<<<grid, kGemvThreads, smem, static_cast<cudaStream_t>(stream)>>>(
+      wa->second, wb->second, it->second, M, 0, N, NC, g.atoms, g.per, nst, part, b->m.ctl);
+  return cudaGetLastError() == cudaSuccess ? g.splits : -1;
+}
+
+size_t batch_prefill_part_floats(const Dims& d, int sms) {
+  const int QKV = (d.Hq + 2 * d.Hkv) * d.hd;
+  size_t mx = 0;
+  auto acc = [&](int M, int K, int nmat) {
+    const GemvPlan g = plan_gemv(M, K, nmat, kGemvCtasPerSm * sms, false);
+    mx = std::max(mx, static_cast<size_t>(g.nmat) * g.splits * kPrefillCols * M);
+  };
+  acc(QKV, d.D, 1);
+  acc(d.D, d.Hq * d.hd, 1);
+  acc(d.F, d.D, 2);
+  acc(d.D, d.F, 1);
+  return mx;
 }
 
 void batch_destroy(Batch* b) {

@@ -50,6 +50,9 @@ struct s2_ctx {
   int sms = 0;
   BatchModel bm{};
   Batch* batch = nullptr;
+  uint16_t* pf_planes = nullptr;   // prompt projections: planes [256][pf_ld]
+  int pf_ld = 0;
+  float* pf_part = nullptr;
 };
 
 namespace {
@@ -262,6 +265,10 @@ void carve(s2_ctx* c, Carver& cv) {
     m.bfcode = cv.take<int32_t>(static_cast<size_t>(B) * 16);
     m.bctl = cv.take<int>(16);
     m.bstreams = cv.take<unsigned char>(batch_stream_bytes(B));
+    // prompt projections on the tensor cores: planes of up to 128 positions and their partials
+    c->pf_ld = std::max(std::max(d.D, d.Hq * d.hd), d.F);
+    c->pf_planes = cv.take<uint16_t>(static_cast<size_t>(2 * kPrefillChunkTC) * c->pf_ld);
+    c->pf_part = cv.take<float>(batch_prefill_part_floats(d, c->sms));
   }
 }
 
@@ -724,6 +731,10 @@ int s2_prefill(s2_ctx* c, int n, const int* ids, const int32_t* tokens, const in
     a.logits = c->logits + static_cast<size_t>(sid) * logits_stride(d);
     a.st = c->st + sid;
     a.err = &c->ctl->error;
+    a.tc = c->batch;
+    a.tc_planes = c->pf_planes;
+    a.tc_ld = c->pf_ld;
+    a.tc_part = c->pf_part;
     const int rc = run_prefill(a, stream);
     if (rc != S2_OK) return fail(c, rc, std::string("prefill launch failed: ") + cudaGetErrorString(cudaGetLastError()));
     off += static_cast<size_t>(T) * (d.ncb + 1);

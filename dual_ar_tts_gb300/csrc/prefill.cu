@@ -331,6 +331,54 @@ __global__ void k_compact(const int32_t* stage, int32_t* codes, const StreamStat
   if (threadIdx.x == 0) *n_out = n;
 }
 
+// tensor-core prompt projections: the rows of a chunk as bf16 hi / lo planes (rows 2t, 2t+1) of
+// RMSNorm(x_t)·w, or of x_t itself when w is null
+__global__ void __launch_bounds__(kBlk) k_pf_planes(const float* X, int ldx, int K, const void* w, int esz, float eps,
+                                                    uint16_t* P, int ldp) {
+  __shared__ float sh[32];
+  const int t = blockIdx.x;
+  const float* x = X + static_cast<size_t>(t) * ldx;
+  float r = 1.f;
+  if (w) {
+    float s = 0.f;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) s += x[k] * x[k];
+    r = 1.0f / sqrtf(block_sum(s, sh) / static_cast<float>(K) + eps);
+  }
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    const float n = w ? (x[k] * r) * wload(w, k, esz) : x[k];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(n);
+    P[static_cast<size_t>(2 * t) * ldp + k] = __bfloat16_as_ushort(hi);
+    P[static_cast<size_t>(2 * t + 1) * ldp + k] = __bfloat16_as_ushort(__float2bfloat16_rn(n - __bfloat162float(hi)));
+  }
+}
+
+// Y[t][m] = (add ? Y[t][m] : 0) + Σ_s part[(s*NC + t)*M + m], splits summed in order
+__global__ void k_pf_reduce(const float* __restrict__ part, int splits, int NC, int M, float* Y, int ldy, int add) {
+  const int t = blockIdx.y;
+  for (int m = blockIdx.x * blockDim.x + threadIdx.x; m < M; m += gridDim.x * blockDim.x) {
+    float a = 0.f;
+    for (int s = 0; s < splits; ++s) a += __ldcg(part + (static_cast<size_t>(s) * NC + t) * M + m);
+    float* y = Y + static_cast<size_t>(t) * ldy + m;
+    *y = add ? *y + a : a;
+  }
+}
+
+// planes of silu(Σ W1 partials)·(Σ W3 partials) (ch.02 §3.2 SwiGLU)
+__global__ void k_pf_swiglu(const float* __restrict__ part, int splits, int NC, int M, uint16_t* P, int ldp) {
+  const int t = blockIdx.y;
+  for (int m = blockIdx.x * blockDim.x + threadIdx.x; m < M; m += gridDim.x * blockDim.x) {
+    float a = 0.f, u = 0.f;
+    for (int s = 0; s < splits; ++s) {
+      a += __ldcg(part + (static_cast<size_t>(s) * NC + t) * M + m);
+      u += __ldcg(part + (static_cast<size_t>(splits + s) * NC + t) * M + m);
+    }
+    const float h = (a / (1.0f + expf(-a))) * u;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(h);
+    P[static_cast<size_t>(2 * t) * ldp + m] = __bfloat16_as_ushort(hi);
+    P[static_cast<size_t>(2 * t + 1) * ldp + m] = __bfloat16_as_ushort(__float2bfloat16_rn(h - __bfloat162float(hi)));
+  }
+}
+
 template <typename WT>
 void gemm(const float* A, const void* W, float* Y, int T, int M, int K, int add, cudaStream_t s) {
   dim3 grid((M + 63) / 64, (T + 63) / 64);
@@ -357,15 +405,38 @@ static int prefill_t(const PrefillArgs& a, cudaStream_t s, int* err) {
   float* Ab = O + static_cast<size_t>(a.chunk) * d.Hq * HD;
   float* Bb = Ab + static_cast<size_t>(a.chunk) * d.F;
   const float scale = static_cast<float>(1.0 / sqrt(static_cast<double>(HD)));
-  for (int c0 = 0; c0 < a.T; c0 += a.chunk) {
-    const int Tc = std::min(a.chunk, a.T - c0);
+  const bool tc = a.tc != nullptr && sizeof(WT) == 2;
+  const int chunk = tc ? std::min(a.chunk, kPrefillChunkTC) : a.chunk;
+  // projection y[t] = W·in[t] of the chunk: tensor cores (planes + split partials) or the fp32 tiles
+  auto proj = [&](const float* in, int ldin, const void* normw, const void* W, const void* W3, float* out, int M, int K,
+                  int Tc, int add) -> bool {
+    if (!tc) {
+      if (W3) return false;
+      gemm<WT>(in, W, out, Tc, M, K, add, s);
+      return true;
+    }
+    k_pf_planes<<<Tc, kBlk, 0, s>>>(in, ldin, K, normw, d.esz, d.eps, a.tc_planes, a.tc_ld);
+    const int sp = batch_prefill_proj(a.tc, W, W3, M, K, a.tc_planes, a.tc_ld, Tc, a.tc_part, s);
+    if (sp <= 0) return false;
+    if (W3)
+      k_pf_swiglu<<<dim3((M + 255) / 256, Tc), 256, 0, s>>>(a.tc_part, sp, Tc, M, a.tc_planes, a.tc_ld);
+    else
+      k_pf_reduce<<<dim3((M + 255) / 256, Tc), 256, 0, s>>>(a.tc_part, sp, Tc, M, out, M, add);
+    return true;
+  };
+  for (int c0 = 0; c0 < a.T; c0 += chunk) {
+    const int Tc = std::min(chunk, a.T - c0);
     k_embed<<<Tc, kBlk, 0, s>>>(a.tokens + static_cast<size_t>(c0) * C, Tc, d, a.E, a.CE, X, err);
     for (int l = 0; l < d.L; ++l) {
       const LayerW& w = a.layers[l];
       KT* Kc = reinterpret_cast<KT*>(static_cast<unsigned char*>(a.kc0) + l * a.kv_layer_stride);
       KT* Vc = reinterpret_cast<KT*>(static_cast<unsigned char*>(a.vc0) + l * a.kv_layer_stride);
-      k_rmsnorm<<<Tc, kBlk, 0, s>>>(X, d.D, w.an, d.esz, d.eps, H);
-      gemm<WT>(H, w.wqkv, QKV, Tc, QD, d.D, 0, s);
+      if (tc) {
+        if (!proj(X, d.D, w.an, w.wqkv, nullptr, QKV, QD, d.D, Tc, 0)) return S2_ECUDA;
+      } else {
+        k_rmsnorm<<<Tc, kBlk, 0, s>>>(X, d.D, w.an, d.esz, d.eps, H);
+        gemm<WT>(H, w.wqkv, QKV, Tc, QD, d.D, 0, s);
+      }
       {
         const int items = Tc * (d.Hq + d.Hkv);
         k_qk_rope_kv<KT, HD><<<(items + 7) / 8, 256, 0, s>>>(QKV, Tc, c0, d, w.qn, w.kn, a.rope, Kc, Vc, a.kv_slots);
@@ -374,12 +445,22 @@ static int prefill_t(const PrefillArgs& a, cudaStream_t s, int* err) {
         const int items = Tc * d.Hkv;
         k_attn_prefill<KT, HD><<<(items + 7) / 8, 256, 0, s>>>(QKV, Tc, c0, d, Kc, Vc, a.kv_slots, scale, O);
       }
-      gemm<WT>(O, w.wo, X, Tc, d.D, d.Hq * HD, 1, s);
-      k_rmsnorm<<<Tc, kBlk, 0, s>>>(X, d.D, w.fn, d.esz, d.eps, H);
-      gemm<WT>(H, w.w1, Ab, Tc, d.F, d.D, 0, s);
-      gemm<WT>(H, w.w3, Bb, Tc, d.F, d.D, 0, s);
-      k_swiglu<<<1024, 256, 0, s>>>(Ab, Bb, static_cast<size_t>(Tc) * d.F);
-      gemm<WT>(Ab, w.w2, X, Tc, d.D, d.F, 1, s);
+      if (tc) {
+        // out-projection + residual; RMSNorm + gate/up (SwiGLU planes); down-projection + residual
+        if (!proj(O, d.Hq * HD, nullptr, w.wo, nullptr, X, d.D, d.Hq * HD, Tc, 1) ||
+            !proj(X, d.D, w.fn, w.w1, w.w3, nullptr, d.F, d.D, Tc, 0))
+          return S2_ECUDA;
+        const int sp = batch_prefill_proj(a.tc, w.w2, nullptr, d.D, d.F, a.tc_planes, a.tc_ld, Tc, a.tc_part, s);
+        if (sp <= 0) return S2_ECUDA;
+        k_pf_reduce<<<dim3((d.D + 255) / 256, Tc), 256, 0, s>>>(a.tc_part, sp, Tc, d.D, X, d.D, 1);
+      } else {
+        gemm<WT>(O, w.wo, X, Tc, d.D, d.Hq * HD, 1, s);
+        k_rmsnorm<<<Tc, kBlk, 0, s>>>(X, d.D, w.fn, d.esz, d.eps, H);
+        gemm<WT>(H, w.w1, Ab, Tc, d.F, d.D, 0, s);
+        gemm<WT>(H, w.w3, Bb, Tc, d.F, d.D, 0, s);
+        k_swiglu<<<1024, 256, 0, s>>>(Ab, Bb, static_cast<size_t>(Tc) * d.F);
+        gemm<WT>(Ab, w.w2, X, Tc, d.D, d.F, 1, s);
+      }
     }
     if (c0 + Tc == a.T) {
       const int blocks = (d.A + 7) / 8;

@@ -175,6 +175,7 @@ int build_rope_tables(float2* slow, int slots, int hd, float2* fast, int wf, int
 int compact_codes(const int32_t* stage, int32_t* codes, const StreamState* st, int n_frames, int ncb,
                   int32_t* n_out, void* stream);
 
+struct Batch;
 struct PrefillArgs {
   Dims d;
   const void* E;
@@ -194,6 +195,11 @@ struct PrefillArgs {
   float* logits;          // [A]
   StreamState* st;
   int* err;               // device word receiving S2_EINVAL on an out-of-range id
+  // tensor-core projections (bf16 models): the projection kernel, planes and partials
+  Batch* tc;
+  uint16_t* tc_planes;    // [256][tc_ld]
+  int tc_ld;
+  float* tc_part;
 };
 int run_prefill(const PrefillArgs& a, void* stream);
 // final norm + admissible logits of a residual x [D], then the stream reset to position pos
@@ -240,6 +246,13 @@ size_t batch_stream_bytes(int max_streams);
 struct Batch;
 Batch* batch_create(const BatchModel& m, std::string* err);
 void batch_destroy(Batch* b);
+// Prompt projections on the same tensor-core kernel: columns = up to 128 prompt positions given
+// as hi / lo planes [2*NC rows][ld]; writes split partials part[(z*splits + s)*NC + c][M]
+// and returns the split count (-1 on error).
+int batch_prefill_proj(Batch* b, const void* w0, const void* w1, int M, int K, const uint16_t* planes, int ld, int NC,
+                       float* part, void* stream);
+size_t batch_prefill_part_floats(const Dims& d, int sms);
+constexpr int kPrefillChunkTC = 128;
 // streams ids[0..n), n_frames frames; expo/forced/taps laid out as for s2_decode_frames
 int batch_decode(Batch* b, int n, const int* ids, int n_frames, const s2_sampling* params, const float* expo,
                  const int32_t* forced, const s2_debug_taps* taps, int max_ctx, void* stream, std::string* err);
