@@ -444,6 +444,12 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a2,
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ void mma_f16x(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -701,6 +707,175 @@ __global__ void __launch_bounds__(128, 2) k_attn_slow(const BEnv e, int layer, c
       outp[G * HD + G + h] = l;
     }
   }
+}
+
+// Prompt attention on the tensor cores (FlashAttention-style, causal, GQA with 4 query heads per
+// KV head).  CTA = (block of 8 prompt positions, KV head); warp w owns positions 2w, 2w+1 of the
+// block as one m16 tile: rows r < 8 -> first position, r >= 8 -> second; (r & 7) >> 2 selects the
+// fp16 hi part / remainder of the scaled query and r & 3 the query head.  K/V tiles of 32 slots
+// are staged by the CTA (cp.async, double-buffered, padded rows); scores and P·V use mma.sync
+// fp16 -> fp32 as in the decode attention, with the hi and lo rows added at the end.
+// QKV: [Tc][QD] with q normalised and rotated; K/V of slots < pos0 + Tc already in the cache.
+template <int HD>
+__global__ void __launch_bounds__(128) k_attn_prefill_tc(const float* __restrict__ QKV, int Tc, int pos0, int Hq, int Hkv,
+                                                         const __half* __restrict__ Kc, const __half* __restrict__ Vc,
+                                                         int slots, float scale, float* __restrict__ O) {
+  constexpr int G = 4, TS = 32;
+  constexpr int RB = HD * 2 + 16;
+  constexpr int KS = HD / 16, NB = HD / 8;
+  __shared__ __align__(16) unsigned char kv[2][2][TS * RB];  // [buffer][K, V]
+  const int g = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int t0 = blockIdx.x * 8 + 2 * warp;  // the warp's first position (chunk-local)
+  const int QD = (Hq + 2 * Hkv) * HD;
+  const int gq = lane >> 2, tq = lane & 3, hq = gq & 3, partq = gq >> 2;
+  // A fragments of the warp's queries: row gq -> position t0, row gq + 8 -> position t0 + 1
+  uint32_t qa[KS][4];
+  {
+    const int tA = min(t0, Tc - 1), tB = min(t0 + 1, Tc - 1);
+    const float* qA = QKV + static_cast<size_t>(tA) * QD + (g * G + hq) * HD;
+    const float* qB = QKV + static_cast<size_t>(tB) * QD + (g * G + hq) * HD;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const int e0 = 16 * ks + 2 * tq;
+      qa[ks][0] = pack_h2(h_part(qA[e0] * scale, partq), h_part(qA[e0 + 1] * scale, partq));
+      qa[ks][1] = pack_h2(h_part(qB[e0] * scale, partq), h_part(qB[e0 + 1] * scale, partq));
+      qa[ks][2] = pack_h2(h_part(qA[e0 + 8] * scale, partq), h_part(qA[e0 + 9] * scale, partq));
+      qa[ks][3] = pack_h2(h_part(qB[e0 + 8] * scale, partq), h_part(qB[e0 + 9] * scale, partq));
+    }
+  }
+  const int pA = pos0 + t0, pB = pos0 + t0 + 1;       // causal limits of the two rows
+  const int last = min(pos0 + blockIdx.x * 8 + 7, pos0 + Tc - 1);  // the block's last position
+  const int ntiles = (last + 1 + TS - 1) / TS;
+  const __half* Kh = Kc + static_cast<size_t>(g) * slots * HD;
+  const __half* Vh = Vc + static_cast<size_t>(g) * slots * HD;
+  auto stage = [&](int buf, int tt) {
+    const int s0 = tt * TS, rows = min(TS, last + 1 - s0);
+    constexpr int CPR = HD * 2 / 16;
+    for (int c = tid; c < rows * CPR; c += 128) {
+      const int r = c / CPR, cc = c % CPR;
+      cp_async16(&kv[buf][0][r * RB + cc * 16], reinterpret_cast<const unsigned char*>(Kh + static_cast<size_t>(s0 + r) * HD) + cc * 16);
+      cp_async16(&kv[buf][1][r * RB + cc * 16], reinterpret_cast<const unsigned char*>(Vh + static_cast<size_t>(s0 + r) * HD) + cc * 16);
+    }
+    // rows past the block's last position: zero (masked scores, zero probabilities)
+    for (int c = tid; c < (TS - rows) * (HD / 2); c += 128) {
+      const int r = rows + c / (HD / 2), cc = c % (HD / 2);
+      reinterpret_cast<uint32_t*>(&kv[buf][0][r * RB])[cc] = 0u;
+      reinterpret_cast<uint32_t*>(&kv[buf][1][r * RB])[cc] = 0u;
+    }
+    cp_async_commit();
+  };
+  float o[NB][4];
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb) o[nb][0] = o[nb][1] = o[nb][2] = o[nb][3] = 0.f;
+  float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+  const int lr = lane & 7, lm = lane >> 3;
+  stage(0, 0);
+  for (int tt = 0; tt < ntiles; ++tt) {
+    const int buf = tt & 1;
+    if (tt + 1 < ntiles) {
+      stage(buf ^ 1, tt + 1);
+      cp_async_wait_group<1>();
+    } else {
+      cp_async_wait_group<0>();
+    }
+    __syncthreads();
+    const unsigned char* dk = kv[buf][0];
+    const unsigned char* dv = kv[buf][1];
+    // scores of the 4 8-slot blocks
+    float sc[4][4];
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk) {
+      sc[blk][0] = sc[blk][1] = sc[blk][2] = sc[blk][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ks += 2) {
+        uint32_t bf[4];
+        ldsm_x4(smem_u32(dk + (blk * 8 + lr) * RB + (16 * ks + 8 * lm) * 2), bf);
+        mma_f16x(sc[blk], qa[ks], bf[0], bf[1]);
+        mma_f16x(sc[blk], qa[ks + 1], bf[2], bf[3]);
+      }
+    }
+    const int s0 = tt * TS;
+    float vA[8], vB[8];
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int slot = s0 + blk * 8 + 2 * tq + c;
+        const float xa = sc[blk][c] + __shfl_xor_sync(0xffffffffu, sc[blk][c], 16);
+        const float xb = sc[blk][2 + c] + __shfl_xor_sync(0xffffffffu, sc[blk][2 + c], 16);
+        vA[blk * 2 + c] = slot <= pA ? xa : -INFINITY;
+        vB[blk * 2 + c] = slot <= pB ? xb : -INFINITY;
+      }
+    float mtA = -INFINITY, mtB = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      mtA = fmaxf(mtA, vA[u]);
+      mtB = fmaxf(mtB, vB[u]);
+    }
+    mtA = fmaxf(mtA, __shfl_xor_sync(0xffffffffu, mtA, 1));
+    mtA = fmaxf(mtA, __shfl_xor_sync(0xffffffffu, mtA, 2));
+    mtB = fmaxf(mtB, __shfl_xor_sync(0xffffffffu, mtB, 1));
+    mtB = fmaxf(mtB, __shfl_xor_sync(0xffffffffu, mtB, 2));
+    const float mnA = fmaxf(mA, mtA), mnB = fmaxf(mB, mtB);
+    const float cfA = mA == -INFINITY ? 0.f : expf(mA - mnA);
+    const float cfB = mB == -INFINITY ? 0.f : expf(mB - mnB);
+    float psA = 0.f, psB = 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      vA[u] = vA[u] == -INFINITY ? 0.f : expf(vA[u] - mnA);
+      vB[u] = vB[u] == -INFINITY ? 0.f : expf(vB[u] - mnB);
+      psA += vA[u];
+      psB += vB[u];
+    }
+    psA += __shfl_xor_sync(0xffffffffu, psA, 1);
+    psA += __shfl_xor_sync(0xffffffffu, psA, 2);
+    psB += __shfl_xor_sync(0xffffffffu, psB, 1);
+    psB += __shfl_xor_sync(0xffffffffu, psB, 2);
+    // a row that has seen no slot yet keeps m = -inf (its probabilities are 0)
+    lA = lA * cfA + psA;
+    lB = lB * cfB + psB;
+    mA = mnA;
+    mB = mnB;
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      o[nb][0] *= cfA;
+      o[nb][1] *= cfA;
+      o[nb][2] *= cfB;
+      o[nb][3] *= cfB;
+    }
+    // P·V over the two 16-slot halves of the tile
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      uint32_t pa[4];
+      pa[0] = pack_h2(h_part(vA[4 * j + 0], partq), h_part(vA[4 * j + 1], partq));
+      pa[1] = pack_h2(h_part(vB[4 * j + 0], partq), h_part(vB[4 * j + 1], partq));
+      pa[2] = pack_h2(h_part(vA[4 * j + 2], partq), h_part(vA[4 * j + 3], partq));
+      pa[3] = pack_h2(h_part(vB[4 * j + 2], partq), h_part(vB[4 * j + 3], partq));
+#pragma unroll
+      for (int nbp = 0; nbp < NB / 2; ++nbp) {
+        uint32_t bf[4];
+        ldsm_x4_t(smem_u32(dv + (16 * j + (lm & 1) * 8 + lr) * RB + (16 * nbp + 8 * (lm >> 1)) * 2), bf);
+        mma_f16x(o[2 * nbp], pa, bf[0], bf[1]);
+        mma_f16x(o[2 * nbp + 1], pa, bf[2], bf[3]);
+      }
+    }
+    __syncthreads();
+  }
+  // hi + remainder rows, normalised; lanes of the hi part write
+  const float iA = 1.0f / lA, iB = 1.0f / lB;
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const float xa = o[nb][c] + __shfl_xor_sync(0xffffffffu, o[nb][c], 16);
+      const float xb = o[nb][2 + c] + __shfl_xor_sync(0xffffffffu, o[nb][2 + c], 16);
+      if (partq == 0) {
+        const int e = nb * 8 + 2 * tq + c;
+        if (t0 < Tc) O[static_cast<size_t>(t0) * Hq * HD + (g * G + hq) * HD + e] = xa * iA;
+        if (t0 + 1 < Tc) O[static_cast<size_t>(t0 + 1) * Hq * HD + (g * G + hq) * HD + e] = xb * iB;
+      }
+    }
 }
 
 // combine the splits of each (stream, KV head): o = Σ_s e^{m_s - M} o_s / Σ_s e^{m_s - M} l_s,
@@ -1312,6 +1487,20 @@ int batch_prefill_proj(Batch* b, const void* w0, const void* w1, int M, int K, c
   k_bgemv<<<grid, kGemvThreads, smem, static_cast<cudaStream_t>(stream)>>>(
       wa->second, wb->second, it->second, M, 0, N, NC, g.atoms, g.per, nst, part, b->m.ctl);
   return cudaGetLastError() == cudaSuccess ? g.splits : -1;
+}
+
+int batch_prefill_attn(const float* QKV, int Tc, int pos0, const Dims& d, const void* Kc, const void* Vc, int slots,
+                       float scale, float* O, void* stream) {
+  if (d.kvdt != S2_F16 || d.Hq != 4 * d.Hkv || (d.hd != 128 && d.hd != 64)) return -1;
+  dim3 grid((Tc + 7) / 8, d.Hkv);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d.hd == 128)
+    k_attn_prefill_tc<128><<<grid, 128, 0, s>>>(QKV, Tc, pos0, d.Hq, d.Hkv, static_cast<const __half*>(Kc),
+                                                 static_cast<const __half*>(Vc), slots, scale, O);
+  else
+    k_attn_prefill_tc<64><<<grid, 128, 0, s>>>(QKV, Tc, pos0, d.Hq, d.Hkv, static_cast<const __half*>(Kc),
+                                                static_cast<const __half*>(Vc), slots, scale, O);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
 size_t batch_prefill_part_floats(const Dims& d, int sms) {

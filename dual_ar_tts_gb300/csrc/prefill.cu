@@ -441,7 +441,7 @@ static int prefill_t(const PrefillArgs& a, cudaStream_t s, int* err) {
         const int items = Tc * (d.Hq + d.Hkv);
         k_qk_rope_kv<KT, HD><<<(items + 7) / 8, 256, 0, s>>>(QKV, Tc, c0, d, w.qn, w.kn, a.rope, Kc, Vc, a.kv_slots);
       }
-      {
+      if (!(tc && sizeof(KT) == 2 && batch_prefill_attn(QKV, Tc, c0, d, Kc, Vc, a.kv_slots, scale, O, s) == 0)) {
         const int items = Tc * d.Hkv;
         k_attn_prefill<KT, HD><<<(items + 7) / 8, 256, 0, s>>>(QKV, Tc, c0, d, Kc, Vc, a.kv_slots, scale, O);
       }

@@ -252,6 +252,10 @@ void batch_destroy(Batch* b);
 int batch_prefill_proj(Batch* b, const void* w0, const void* w1, int M, int K, const uint16_t* planes, int ld, int NC,
                        float* part, void* stream);
 size_t batch_prefill_part_floats(const Dims& d, int sms);
+// Prompt attention of a chunk (positions pos0..pos0+Tc-1, causal) on the tensor cores; K/V of this
+// stream's layer [Hkv][slots][hd] fp16 already hold every slot up to pos0+Tc-1.  0 or -1.
+int batch_prefill_attn(const float* QKV, int Tc, int pos0, const Dims& d, const void* Kc, const void* Vc, int slots,
+                       float scale, float* O, void* stream);
 constexpr int kPrefillChunkTC = 128;
 // streams ids[0..n), n_frames frames; expo/forced/taps laid out as for s2_decode_frames
 int batch_decode(Batch* b, int n, const int* ids, int n_frames, const s2_sampling* params, const float* expo,
