@@ -20,7 +20,8 @@ STATUS_NAMES = {0: "S2_OK", 1: "S2_EINVAL", 2: "S2_ENOMEM", 3: "S2_ECAPACITY", 4
 
 EXPORTS = ("s2_weight_count", "s2_weight_info", "s2_frame_workspace_bytes", "s2_frame_init", "s2_prefill",
            "s2_decode_frames", "s2_fast_logits", "s2_sync_status", "s2_set_spin_limit", "s2_set_trace",
-           "s2_phase_count", "s2_frame_free", "s2_last_error", "s2_fast_logits_static", "s2_stream_import")
+           "s2_phase_count", "s2_frame_free", "s2_last_error", "s2_fast_logits_static", "s2_stream_import",
+           "s2_stop_stream", "s2_stream_progress")
 
 
 class s2_dims(ctypes.Structure):
@@ -78,6 +79,8 @@ def load(path: str = LIB_PATH):
         "s2_last_error": (ctypes.c_char_p, [vp]),
         "s2_fast_logits_static": (i32, [P(s2_dims), P(vp), i32, i32, vp, vp, vp, vp, vp]),
         "s2_stream_import": (i32, [vp, i32, i32, vp, vp, vp, vp]),
+        "s2_stop_stream": (i32, [vp, i32, vp]),
+        "s2_stream_progress": (i32, [vp, i32, P(i32), vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -139,6 +142,15 @@ def s2_prefill(ctx, stream_ids, tokens_ptr: int, lengths, stream: int = 0):
 def s2_stream_import(ctx, stream_id: int, n_pos: int, k_ptr: int, v_ptr: int, x_last_ptr: int, stream: int = 0):
     rc = load().s2_stream_import(ctx, stream_id, n_pos, k_ptr, v_ptr, x_last_ptr, stream)
     return _check("s2_stream_import", rc, ctx)
+
+
+def s2_stop_stream(ctx, stream_id: int, side_stream: int = 0):
+    return _check("s2_stop_stream", load().s2_stop_stream(ctx, stream_id, side_stream), ctx)
+
+
+def s2_stream_progress(ctx, stream_ids, out_ptr: int, side_stream: int = 0):
+    rc = load().s2_stream_progress(ctx, len(stream_ids), _ints(stream_ids), out_ptr, side_stream)
+    return _check("s2_stream_progress", rc, ctx)
 
 
 def s2_decode_frames(ctx, stream_ids, n_frames: int, params, expo_ptr: int, forced_ptr: int | None, codes_ptr: int,
@@ -241,6 +253,24 @@ class Decoder:
         self._keep = toks
         return toks
 
+    def stop(self, stream_id, side_stream=None):
+        """Ask a stream to stop at its next frame boundary (takes effect during a running decode
+        when side_stream is a non-blocking stream other than the decode's)."""
+        import torch
+        side = side_stream if side_stream is not None else torch.cuda.Stream()
+        s2_stop_stream(self.ctx, stream_id, side.cuda_stream)
+        side.synchronize()
+
+    def progress(self, stream_ids, side_stream=None):
+        """Frames emitted so far by the running (or last) decode call, per stream id."""
+        import numpy as np
+        import torch
+        side = side_stream if side_stream is not None else torch.cuda.Stream()
+        out = np.zeros(len(stream_ids), np.int32)
+        s2_stream_progress(self.ctx, list(stream_ids), out.ctypes.data, side.cuda_stream)
+        side.synchronize()
+        return out
+
     def import_stream(self, stream_id, k, v, x_last):
         """k, v: device tensors [n_layer][n_kv_head][n_pos][head_dim] of the KV dtype; x_last: [dim] fp32."""
         n_pos = int(k.shape[2])
@@ -301,3 +331,44 @@ def upload_weights(host_weights, device="cuda"):
             t = torch.from_numpy(np.ascontiguousarray(w, dtype=np.float32)).to(device)
         out.append(t)
     return out
+
+
+def serve(decoder, requests, slots, frames_per_call, sampling, expo_fn):
+    """Continuous batching over the decoder's stream slots.
+
+    requests: list of (prompt [T][NCB+1] int32, n_frames).  A request holds a slot from its prefill
+    until it has produced n_frames frames or stopped (im_end); its slot then takes the next waiting
+    request.  The active slots are decoded together (one weight read per step) in calls of at most
+    frames_per_call frames, cut so that no request overshoots.  expo_fn(request, first_frame, n)
+    returns that request's exponential variates [n][11][30] (float32), so a request sees the same
+    variates whatever the batch around it.  Returns, per request, its codes [NCB][frames] (int32).
+    """
+    import collections
+    import numpy as np
+    import torch
+    ncb = decoder.d["n_codebooks"]
+    waiting = collections.deque(range(len(requests)))
+    active = {}
+    results = [None] * len(requests)
+    while waiting or active:
+        for slot in range(slots):
+            if slot not in active and waiting:
+                r = waiting.popleft()
+                decoder.prefill([requests[r][0]], stream_ids=[slot])
+                active[slot] = [r, 0, []]
+        ids = sorted(active)
+        n = min(frames_per_call, min(requests[active[k][0]][1] - active[k][1] for k in ids))
+        expo = torch.from_numpy(np.stack([expo_fn(active[k][0], active[k][1], n) for k in ids])).cuda()
+        out = decoder.decode(n, sampling, expo, stream_ids=ids)
+        n_out = out["n_out"].cpu().numpy()
+        codes = out["codes"].cpu().numpy()
+        for j, k in enumerate(ids):
+            r, done, chunks = active[k]
+            no = int(n_out[j])
+            chunks.append(codes[j, :ncb * no].reshape(ncb, no))
+            done += no
+            active[k][1] = done
+            if no < n or done >= requests[r][1]:
+                results[r] = np.concatenate(chunks, axis=1)
+                del active[k]
+    return results

@@ -1091,6 +1091,17 @@ __global__ void __launch_bounds__(kConsumers) k_samp_main(const BEnv e) {
   const int fd = ldcgi(&st->frames_done);
   const float* E = bs.expo + static_cast<size_t>(f) * kDraws * kTopK;
   const bool block_end = fd < bs.min_tokens;
+  // a stop request (s2_stop_stream) ends the stream at this frame boundary, like im_end
+  if (threadIdx.x == 0) flag = ld_volatile_int(&st->stop_req);
+  __syncthreads();
+  if (flag) {
+    if (threadIdx.x == 0) {
+      st->done = 1;
+      st->n_out = f;
+    }
+    return;
+  }
+  __syncthreads();
   int d0 = draw(d, W, lg, d.A, true, block_end, bs.T, bs.top_p, E);
   if (threadIdx.x == 0) {
     if (bs.dbg_draws) bs.dbg_draws[f * kDraws + 0] = d0;
@@ -1346,10 +1357,6 @@ bool encode_map(CUtensorMap* m, const void* base, int inner, long long rows, int
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// items per (stream, KV head) in the grid: enough for the longest context of the call
-int attn_splits(int max_ctx) {
-  return std::max(1, std::min(kMaxSplitsAttn, (max_ctx + kAttnChunk - 1) / kAttnChunk));
-}
 
 }  // namespace
 
@@ -1360,6 +1367,9 @@ struct Batch {
   BatchSizes sz{};
   std::vector<BStream> host_bs;
   cudaStream_t cap = nullptr;   // private stream the frame is captured on
+  // instantiated frame graphs by batch size: the per-call settings live in device memory, so a
+  // graph serves every later call with the same number of streams
+  std::map<int, cudaGraphExec_t> graphs;
 };
 
 bool batch_supported(const Dims& d, int max_streams, std::string* why) {
@@ -1518,7 +1528,9 @@ size_t batch_prefill_part_floats(const Dims& d, int sms) {
 }
 
 void batch_destroy(Batch* b) {
-  if (b && b->cap) cudaStreamDestroy(b->cap);
+  if (!b) return;
+  for (auto& kv : b->graphs) cudaGraphExecDestroy(kv.second);
+  if (b->cap) cudaStreamDestroy(b->cap);
   delete b;
 }
 
@@ -1721,7 +1733,10 @@ int batch_decode(Batch* b, int n, const int* ids, int n_frames, const s2_samplin
   fr.b = b;
   fr.s = b->cap;
   fr.nb = n;
-  fr.ns = attn_splits(max_ctx);
+  (void)max_ctx;
+  // attention items per (stream, KV head): enough for the longest context the KV slots allow, so
+  // that one graph per stream count serves every call; each stream uses its context's share
+  fr.ns = std::max(1, std::min(kMaxSplitsAttn, (m.kv_slots + kAttnChunk - 1) / kAttnChunk));
   BEnv& e = fr.e;
   e.d = d;
   e.nb = n;
@@ -1761,28 +1776,33 @@ int batch_decode(Batch* b, int n, const int* ids, int n_frames, const s2_samplin
     *err = "batched call start failed";
     return S2_ECUDA;
   }
-  cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
-  if (cudaStreamBeginCapture(b->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
-    *err = "graph capture could not begin";
-    return S2_ECUDA;
-  }
-  fr.run();
-  const cudaError_t ce = cudaStreamEndCapture(b->cap, &graph);
-  if (ce != cudaSuccess || !fr.ok) {
-    if (graph) cudaGraphDestroy(graph);
-    *err = std::string("capturing the frame failed: ") + (fr.ok ? cudaGetErrorString(ce) : "tensor map encoding");
-    return S2_ECUDA;
-  }
-  if (cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) {
+  auto cached = b->graphs.find(n);
+  if (cached != b->graphs.end()) {
+    exec = cached->second;
+  } else {
+    cudaGraph_t graph = nullptr;
+    if (cudaStreamBeginCapture(b->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+      *err = "graph capture could not begin";
+      return S2_ECUDA;
+    }
+    fr.run();
+    const cudaError_t ce = cudaStreamEndCapture(b->cap, &graph);
+    if (ce != cudaSuccess || !fr.ok) {
+      if (graph) cudaGraphDestroy(graph);
+      *err = std::string("capturing the frame failed: ") + (fr.ok ? cudaGetErrorString(ce) : "launch or tensor map");
+      return S2_ECUDA;
+    }
+    const cudaError_t ie = cudaGraphInstantiate(&exec, graph, 0);
     cudaGraphDestroy(graph);
-    *err = "instantiating the frame graph failed";
-    return S2_ECUDA;
+    if (ie != cudaSuccess) {
+      *err = "instantiating the frame graph failed";
+      return S2_ECUDA;
+    }
+    b->graphs[n] = exec;
   }
   cudaError_t le = cudaSuccess;
   for (int f = 0; f < n_frames && le == cudaSuccess; ++f) le = cudaGraphLaunch(exec, s);
-  cudaGraphExecDestroy(exec);
-  cudaGraphDestroy(graph);
   if (le != cudaSuccess) {
     *err = std::string("launching the frame graph failed: ") + cudaGetErrorString(le);
     return S2_ECUDA;

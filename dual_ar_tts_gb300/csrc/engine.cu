@@ -859,6 +859,28 @@ int s2_decode_frames(s2_ctx* c, int n, const int* ids, int n_frames, const s2_sa
   return S2_OK;
 }
 
+int s2_stop_stream(s2_ctx* c, int sid, CUstream_st* side) {
+  if (!c) return fail(nullptr, S2_EINVAL, "ctx is NULL");
+  if (sid < 0 || sid >= c->max_streams) return fail(c, S2_EINVAL, "stream id out of range");
+  static const int one = 1;
+  if (cudaMemcpyAsync(&c->st[sid].stop_req, &one, sizeof(int), cudaMemcpyHostToDevice,
+                      reinterpret_cast<cudaStream_t>(side)) != cudaSuccess)
+    return fail(c, S2_ECUDA, std::string("stop request copy failed: ") + cudaGetErrorString(cudaGetLastError()));
+  return S2_OK;
+}
+
+int s2_stream_progress(s2_ctx* c, int n, const int* ids, int32_t* out, CUstream_st* side) {
+  if (!c) return fail(nullptr, S2_EINVAL, "ctx is NULL");
+  if (n <= 0 || !ids || !out) return fail(c, S2_EINVAL, "bad progress arguments");
+  for (int k = 0; k < n; ++k) {
+    if (ids[k] < 0 || ids[k] >= c->max_streams) return fail(c, S2_EINVAL, "stream id out of range");
+    if (cudaMemcpyAsync(out + k, &c->st[ids[k]].n_out, sizeof(int32_t), cudaMemcpyDeviceToHost,
+                        reinterpret_cast<cudaStream_t>(side)) != cudaSuccess)
+      return fail(c, S2_ECUDA, std::string("progress copy failed: ") + cudaGetErrorString(cudaGetLastError()));
+  }
+  return S2_OK;
+}
+
 int s2_fast_logits(s2_ctx* c, int n_frames, const float* hidden, const int32_t* prefix, float* logits,
                    CUstream_st* stream) {
   if (!c) return fail(nullptr, S2_EINVAL, "ctx is NULL");

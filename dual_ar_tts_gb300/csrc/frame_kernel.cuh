@@ -1384,6 +1384,18 @@ __device__ __noinline__ void sample_main(const CallParams& cp, Smem& S, int f) {
   if (cp.dbg_hidden) copy_vec(cp.dbg_hidden + static_cast<size_t>(f) * d.D, cp.hidden, d.D);
   const float* E = cp.expo + static_cast<size_t>(f) * kDraws * kTopK;
   const bool block_end = fd < cp.min_tokens;
+  // a stop request (s2_stop_stream) ends the stream at this frame boundary, like im_end
+  if (threadIdx.x == 0) S.flag = ld_volatile_int(&st->stop_req);
+  named_bar(1, kConsumers);
+  const int stop = S.flag;
+  named_bar(1, kConsumers);
+  if (stop) {
+    if (threadIdx.x == 0) {
+      st->done = 1;
+      st->n_out = f;
+    }
+    return;
+  }
   int d0 = draw(cp.d, *reinterpret_cast<SampScratch*>(S.xs), cp.logits, d.A, true, block_end, cp.temperature, cp.top_p, E);
   if (threadIdx.x == 0) {
     if (cp.dbg_draws) cp.dbg_draws[f * kDraws + 0] = d0;

@@ -301,6 +301,7 @@ __global__ void k_state_reset(StreamState* st, int T) {
   st->wlen = 0;
   st->n_out = 0;
   st->status = 0;
+  st->stop_req = 0;
 }
 
 // cos/sin of pos·θ_i, θ_i = base^(-2i/hd), formed in fp64, rounded to fp32 (then bf16)

@@ -77,7 +77,7 @@ struct StreamState {
   int wlen;          // RAS window length
   int n_out;         // frames emitted by the current call
   int status;
-  int pad0;
+  int stop_req;      // set by s2_stop_stream: stop at the next frame boundary
   int window[kMaxWindow];  // oldest first
   int vals[16];            // next Slow-AR input: [token, code_0..code_{NCB-1}]
 };

@@ -143,10 +143,27 @@ int s2_stream_import(s2_ctx* ctx, int stream_id, int n_pos, const void* k, const
  *           (ch.06 §8 layout, compacted to the frames actually produced)
  *   n_out   device [n]: frames produced (< n_frames when im_end was drawn)
  *   taps    host struct or NULL: debug outputs (see s2_debug_taps)
- * Streams resume where the previous call left them (KV, position, RAS window, logits). */
+ * Streams resume where the previous call left them (KV, position, RAS window, logits).  Calls
+ * with two or more streams on a bf16 context decode them together (one weight read per step);
+ * the frame's kernel sequence is kept per stream count, so later calls with the same count
+ * start without setup (continuous batching: re-form the batch between short calls). */
 int s2_decode_frames(s2_ctx* ctx, int n, const int* stream_ids, int n_frames, const s2_sampling* params,
                      const float* expo, const int32_t* forced, int32_t* codes, int32_t* n_out,
                      const s2_debug_taps* taps, struct CUstream_st* stream);
+
+/* Frame-level control while a decode call runs (ch.06 §7: a per-frame callback may cancel the
+ * generation).  Both calls only enqueue a small copy on `side_stream`, which should be a
+ * non-blocking stream other than the one running s2_decode_frames, so that the copy takes effect
+ * (or is read) while that call is still running:
+ *   s2_stop_stream      asks stream_id to stop at its next frame boundary; the frame is not
+ *                       emitted, n_out of the running call counts the frames before it, and the
+ *                       stream stays stopped until it is prefilled or imported again.
+ *   s2_stream_progress  copies, for each of n stream ids (host array), the frames emitted so far
+ *                       by the running (or last) call into out (host memory, int32 [n]; valid
+ *                       once side_stream has completed the copy).
+ * Errors: S2_EINVAL (bad id or pointer), S2_ECUDA. */
+int s2_stop_stream(s2_ctx* ctx, int stream_id, struct CUstream_st* side_stream);
+int s2_stream_progress(s2_ctx* ctx, int n, const int* stream_ids, int32_t* out, struct CUstream_st* side_stream);
 
 /* Fast-AR alone, teacher-forced (ch.06 §1-§4): for each of n_frames frames, hidden device
  * [n_frames][dim] and prefix device [n_frames][n_codebooks-1] (code_0..code_{NCB-2}); writes

@@ -162,3 +162,59 @@ def test_mini_batched_prefill_and_frames_match_oracle():
         st = compare_frames(refs[i], out, d, s, TOL, stream=i)
         print(f"mini stream {i}:", st)
     dec.close()
+
+
+def _mini(pkg):
+    d = synth.MINI
+    host = synth.make_weights(d, 7, norm_jitter=0.1)
+    return d, host, pkg.upload_weights(host)
+
+
+def test_stop_request_and_progress():
+    # frame-level cancel (ch.06 §7): a stop request ends a stream at its next frame boundary; the
+    # others continue; progress reports the frames emitted; a new prefill clears the request
+    import dual_ar_tts_gb300 as pkg
+    d, host, dev = _mini(pkg)
+    s = synth.sampling("tiny", min_tokens_before_end=100)
+    prompts = [synth.make_prompt(d, 7, i, 20, 6) for i in range(3)]
+    for n in (3, 1):  # batched kernels, then the single-stream kernel
+        dec = pkg.Decoder(d, dev, max_streams=4, kv_slots=64)
+        dec.prefill(prompts[:n])
+        ex = lambda f0, k: torch.from_numpy(np.stack([synth.expo(7, i, k, f0) for i in range(n)])).cuda()
+        out = dec.decode(2, s, ex(0, 2))
+        assert dec.sync_status() == pkg.S2_OK
+        dec.stop(n - 1)
+        out = dec.decode(3, s, ex(2, 3))
+        assert dec.sync_status() == pkg.S2_OK
+        got = out["n_out"].cpu().numpy().tolist()
+        assert got == [3] * (n - 1) + [0], got
+        assert dec.progress(list(range(n))).tolist() == got
+        dec.prefill([prompts[n - 1]], stream_ids=[n - 1])
+        out = dec.decode(2, s, ex(0, 2)[n - 1:n], stream_ids=[n - 1])
+        assert dec.sync_status() == pkg.S2_OK and int(out["n_out"][0]) == 2
+        dec.close()
+
+
+def test_continuous_batching_matches_each_request_decoded_alone():
+    # five requests through two slots, decoded in short calls with slots refilled as requests
+    # finish; each request's codes equal those of the same request decoded beside a fixed partner
+    import dual_ar_tts_gb300 as pkg
+    d, host, dev = _mini(pkg)
+    s = synth.sampling("tiny", min_tokens_before_end=100)
+    lengths = [5, 9, 3, 7, 6]
+    reqs = [(synth.make_prompt(d, 7, i, 18 + 2 * i, 5 + i), lengths[i]) for i in range(5)]
+    expo_fn = lambda r, f0, n: synth.expo(70 + r, 0, n, f0)
+    dec = pkg.Decoder(d, dev, max_streams=2, kv_slots=64)
+    got = pkg.serve(dec, reqs, slots=2, frames_per_call=2, sampling=s, expo_fn=expo_fn)
+    assert dec.sync_status() == pkg.S2_OK
+    dec.close()
+    partner = synth.make_prompt(d, 7, 9, 16, 4)
+    for r, (prompt, n) in enumerate(reqs):
+        ref = pkg.Decoder(d, dev, max_streams=2, kv_slots=64)
+        ref.prefill([prompt, partner])
+        ex = torch.from_numpy(np.stack([expo_fn(r, 0, n), synth.expo(99, 0, n)])).cuda()
+        out = ref.decode(n, s, ex)
+        assert ref.sync_status() == pkg.S2_OK
+        want = out["codes"][0].cpu().numpy().reshape(d["n_codebooks"], n)
+        assert got[r].shape == want.shape and np.array_equal(got[r], want), r
+        ref.close()
