@@ -353,6 +353,24 @@ def main():
     e2e_max = max_over_ranks(e2e_s, world)
     assert int(nout_h[0]) == K
 
+    # codec front on the frames just produced: latent = Σ_cb quantizer_cb[code] (synthetic codebooks)
+    qs = synth.codec_quantizers(11, d["n_codebooks"], d["codebook_size"])
+    dq = [torch.from_numpy(q.view(np.int16)).cuda() for q in qs]
+    lat = torch.empty((K, synth.CODEC_DIM), device="cuda")
+    codes_d = o2["codes"][0].contiguous()
+    args_q = [t.data_ptr() for t in dq]
+    for _ in range(3):
+        pkg.s2_codec_latent(d["n_codebooks"], d["codebook_size"], synth.CODEC_DIM, args_q, K, codes_d.data_ptr(),
+                            lat.data_ptr())
+    ce0, ce1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ce0.record()
+    for _ in range(10):
+        pkg.s2_codec_latent(d["n_codebooks"], d["codebook_size"], synth.CODEC_DIM, args_q, K, codes_d.data_ptr(),
+                            lat.data_ptr())
+    ce1.record()
+    torch.cuda.synchronize()
+    codec_us = ce0.elapsed_time(ce1) * 100.0
+    codec_bytes = K * synth.CODEC_DIM * (2 * d["n_codebooks"] + 4)
     pk, pk_kind = peaks()
     ctx_avg = PROMPT_LEN + args.warmup + (K - 1) / 2.0
     fb, parts = frame_bytes(d, ctx_avg)
@@ -376,6 +394,8 @@ def main():
                 "d2h_bytes_per_step": int(d["n_codebooks"] * 4)},
         "prefill": {"positions": len(prompt), "ms": prefill_ms, "positions_per_s": len(prompt) / (prefill_ms / 1000.0),
                     "projections": "tcgen05" if d["weight_dtype"] == synth.BF16 else "fp32 tiles"},
+        "codec_latent": {"frames": K, "us": codec_us, "frames_per_s": K / (codec_us / 1e6),
+                         "gb_s": codec_bytes / (codec_us * 1e3)},
         "gpu_launches": 2,
         "clocks": clk.summary(),
         "setup_s": setup_s,

@@ -21,7 +21,7 @@ STATUS_NAMES = {0: "S2_OK", 1: "S2_EINVAL", 2: "S2_ENOMEM", 3: "S2_ECAPACITY", 4
 EXPORTS = ("s2_weight_count", "s2_weight_info", "s2_frame_workspace_bytes", "s2_frame_init", "s2_prefill",
            "s2_decode_frames", "s2_fast_logits", "s2_sync_status", "s2_set_spin_limit", "s2_set_trace",
            "s2_phase_count", "s2_frame_free", "s2_last_error", "s2_fast_logits_static", "s2_stream_import",
-           "s2_stop_stream", "s2_stream_progress")
+           "s2_stop_stream", "s2_stream_progress", "s2_codec_latent")
 
 
 class s2_dims(ctypes.Structure):
@@ -80,6 +80,7 @@ def load(path: str = LIB_PATH):
         "s2_fast_logits_static": (i32, [P(s2_dims), P(vp), i32, i32, vp, vp, vp, vp, vp]),
         "s2_stream_import": (i32, [vp, i32, i32, vp, vp, vp, vp]),
         "s2_stop_stream": (i32, [vp, i32, vp]),
+        "s2_codec_latent": (i32, [i32, i32, i32, P(vp), i32, vp, vp, vp, vp]),
         "s2_stream_progress": (i32, [vp, i32, P(i32), vp, vp]),
     }
     for name, (res, args) in sig.items():
@@ -151,6 +152,15 @@ def s2_stop_stream(ctx, stream_id: int, side_stream: int = 0):
 def s2_stream_progress(ctx, stream_ids, out_ptr: int, side_stream: int = 0):
     rc = load().s2_stream_progress(ctx, len(stream_ids), _ints(stream_ids), out_ptr, side_stream)
     return _check("s2_stream_progress", rc, ctx)
+
+
+def s2_codec_latent(n_codebooks: int, codebook_size: int, dim: int, quantizer_ptrs, n_frames: int, codes_ptr: int,
+                    latent_ptr: int, status_ptr: int | None = None, stream: int = 0):
+    """Codec latent = Σ_cb quantizer_cb[code] per frame (device pointers; see s2frame.h)."""
+    arr = (ctypes.c_void_p * len(quantizer_ptrs))(*quantizer_ptrs)
+    rc = load().s2_codec_latent(n_codebooks, codebook_size, dim, arr, n_frames, codes_ptr, latent_ptr, status_ptr,
+                                stream)
+    return _check("s2_codec_latent", rc)
 
 
 def s2_decode_frames(ctx, stream_ids, n_frames: int, params, expo_ptr: int, forced_ptr: int | None, codes_ptr: int,

@@ -236,6 +236,22 @@ int s2_fast_logits_static(const s2_dims* d, const void* const* weights, int n_we
                           const float* hidden, const int32_t* prefix, float* logits, int32_t* status,
                           struct CUstream_st* stream);
 
+/* Codec quantizer decode, lookup-and-sum part (ch.02 §3.5: the 10 x T codes go through the
+ * semantic VQ, quantizers.0, plus the sum of the residual VQs, quantizers.i, level by level):
+ *   latent[f][e] = Σ_{cb = 0..n_codebooks-1} quantizer_cb[codes[cb * n_frames + f]][e]
+ * summed in codebook order in fp32.  The upsampling that follows on the pages and the waveform
+ * decoder are not part of this call.  Stateless; allocates nothing.
+ *   quantizers  host array [n_codebooks] of device pointers, each bf16 [codebook_size][dim],
+ *               16-byte aligned
+ *   codes       device int32 [n_codebooks * n_frames] (the layout s2_decode_frames emits)
+ *   latent      device fp32 [n_frames][dim]
+ *   status      device int32 or NULL: S2_EINVAL is written there when a code is out of range
+ *               (that codebook's term is left out of the frame)
+ * Errors (nothing launched): S2_EINVAL bad counts (n_codebooks 1..16, dim a multiple of 8),
+ * pointers or alignment; S2_ECUDA launch failed. */
+int s2_codec_latent(int n_codebooks, int codebook_size, int dim, const void* const* quantizers, int n_frames,
+                    const int32_t* codes, float* latent, int32_t* status, struct CUstream_st* stream);
+
 #ifdef __cplusplus
 }
 #endif

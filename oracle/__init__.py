@@ -253,6 +253,21 @@ class Session:
             raise ValueError("kv range")
 
 
+# ------------------------------------------------------------ codec front
+
+def codec_latent(quantizers, codes, n_frames):
+    """Codec quantizer decode, lookup-and-sum part (ch.02 §3.5: semantic VQ quantizers.0 plus the
+    residual VQs quantizers.i, added level by level): latent[f] = Σ_cb Q_cb[codes[cb*n_frames + f]],
+    the bf16 codebook rows widened exactly to fp32 and added in codebook order.  The upsampling and
+    the waveform decoder that follow on the page are not part of it."""
+    out = None
+    for cb, q in enumerate(quantizers):
+        rows = np.asarray(codes[cb * n_frames:(cb + 1) * n_frames], np.int64)
+        widened = (np.asarray(q, np.uint16)[rows].astype(np.uint32) << 16).view(np.float32)
+        out = widened.copy() if out is None else (out + widened).astype(np.float32)
+    return out
+
+
 # ------------------------------------------------------------ generation loop
 
 def admissible_ids(d):

@@ -343,6 +343,16 @@ def kv_state(seed: int, stream: int, d: dict, n_pos: int):
     return k, v, x
 
 
+#: codec quantizer shape (the pages give none): one codebook per code row, 1024-wide latent
+CODEC_DIM = 1024
+
+
+def codec_quantizers(seed: int, n_codebooks: int, codebook_size: int, dim: int = CODEC_DIM):
+    """Synthetic codec VQ codebooks (semantic, then residual), bf16 N(0, 1) [codebook_size][dim]."""
+    return [normal_bf16(seed, 6_000_000 + cb, codebook_size * dim).reshape(codebook_size, dim)
+            for cb in range(n_codebooks)]
+
+
 def fast_inputs(seed: int, n_frames: int, d: dict):
     """Fast-AR-alone inputs: hidden ~ N(0,1)^D per frame, prefix codes uniform in [0, CBS)."""
     hid = normal_f32(seed, 3_000_000, n_frames * d["dim"]).reshape(n_frames, d["dim"])

@@ -83,3 +83,15 @@ def test_init_rejects_bad_arguments_without_touching_a_gpu(lib):
     arr = (ctypes.c_void_p * n)(*([256] * n))
     rc = lib.s2_frame_init(ctypes.byref(dims), arr, n, ctypes.c_void_p(8), 1 << 20, 1, 64, ctypes.byref(out))
     assert rc == pkg.S2_EINVAL and "aligned" in pkg.s2_last_error(None)
+
+
+def test_codec_latent_rejects_bad_arguments_before_any_cuda_call():
+    import ctypes
+    import dual_ar_tts_gb300 as pkg
+    lib = pkg.load()
+    arr = (ctypes.c_void_p * 2)(16, 32)
+    assert lib.s2_codec_latent(2, 64, 12, arr, 4, 16, 16, None, None) == pkg.S2_EINVAL   # dim not a multiple of 8
+    assert lib.s2_codec_latent(0, 64, 16, arr, 4, 16, 16, None, None) == pkg.S2_EINVAL   # no codebook
+    assert lib.s2_codec_latent(2, 64, 16, arr, 0, 16, 16, None, None) == pkg.S2_EINVAL   # no frame
+    bad = (ctypes.c_void_p * 2)(16, 40)                                                  # unaligned quantizer
+    assert lib.s2_codec_latent(2, 64, 16, bad, 4, 16, 16, None, None) == pkg.S2_EINVAL

@@ -558,3 +558,30 @@ def test_draw_diag_reports_the_winner_rank_gap():
     assert abs(float(diag[6]) - 0.1) < 1e-6        # min(3 - 2.5, 2.5 - 2.4)
     tok, diag = oracle.draw(np.array([3.0], np.float32), 1.0, 1.0, 30, E)
     assert np.isinf(diag[6])
+
+
+# ------------------------------------------------------------ codec front
+
+def test_codec_latent_constant_rows_sum_closed_form():
+    ncb, cbs, dim, n = 4, 64, 16, 5
+    qs = [np.full((cbs, dim), np.float32(cb + 1)).view(np.uint32) >> 16 for cb in range(ncb)]
+    qs = [q.astype(np.uint16) for q in qs]
+    codes = synth.uniform_int(1, 2, ncb * n, 0, cbs - 1)
+    lat = oracle.codec_latent(qs, codes, n)
+    np.testing.assert_array_equal(lat, np.full((n, dim), ncb * (ncb + 1) / 2, np.float32))
+
+
+def test_codec_latent_reads_codes_by_codebook_row():
+    # codebook cb holds its row index in element cb: latent[f][cb] must be code(cb, f), read from
+    # codes[cb * n_frames + f]
+    ncb, cbs, dim, n = 4, 64, 8, 6
+    qs = []
+    for cb in range(ncb):
+        q = np.zeros((cbs, dim), np.float32)
+        q[:, cb] = np.arange(cbs, dtype=np.float32)
+        qs.append((q.view(np.uint32) >> 16).astype(np.uint16))
+    codes = synth.uniform_int(3, 4, ncb * n, 0, cbs - 1)
+    lat = oracle.codec_latent(qs, codes, n)
+    for cb in range(ncb):
+        np.testing.assert_array_equal(lat[:, cb], codes[cb * n:(cb + 1) * n].astype(np.float32))
+    np.testing.assert_array_equal(lat[:, ncb:], 0)
