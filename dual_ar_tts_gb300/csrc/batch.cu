@@ -292,20 +292,21 @@ __global__ void __launch_bounds__(kPrepThreads) k_colprep(const BEnv e, const Co
       const int k = tid + i * kPrepThreads;
       v[i] = (mode == CM_RESID && k < K) ? __ldcg(xr + k) : 0.f;
     }
-    // four splits per round: their loads are issued together (the sums keep split order)
+    // eight splits per round: their loads are issued together (the sums keep split order)
+    constexpr int SR = 8;
     const size_t sstride = static_cast<size_t>(p.part_nc) * K;
     const float* pc = p.part + static_cast<size_t>(pcol) * K;
-    for (int s = 0; s < p.splits; s += 4) {
-      float t[4][kMaxPer];
+    for (int s = 0; s < p.splits; s += SR) {
+      float t[SR][kMaxPer];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
+      for (int j = 0; j < SR; ++j)
 #pragma unroll
         for (int i = 0; i < kMaxPer; ++i) {
           const int k = tid + i * kPrepThreads;
           t[j][i] = (s + j < p.splits && k < K) ? __ldcg(pc + (s + j) * sstride + k) : 0.f;
         }
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
+      for (int j = 0; j < SR; ++j)
 #pragma unroll
         for (int i = 0; i < kMaxPer; ++i) v[i] += t[j][i];
     }
@@ -1036,19 +1037,19 @@ __device__ void sum_partials(float* dst, const float* __restrict__ part, int spl
   float a[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) a[r] = 0.f;
-  for (int s = 0; s < splits; s += 2) {
-    const float* ps = part + (static_cast<size_t>(s) * NC + col) * n;
-    const float* ps2 = ps + static_cast<size_t>(NC) * n;
-    const bool two = s + 1 < splits;
-    float t0[R], t1[R];
+  for (int s = 0; s < splits; s += 4) {
+    float t[4][R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int i = threadIdx.x + r * blockDim.x;
-      t0[r] = i < n ? __ldcg(ps + i) : 0.f;
-      t1[r] = (two && i < n) ? __ldcg(ps2 + i) : 0.f;
+    for (int j = 0; j < 4; ++j) {
+      const float* ps = part + (static_cast<size_t>(s + j) * NC + col) * n;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int i = threadIdx.x + r * blockDim.x;
+        t[j][r] = (s + j < splits && i < n) ? __ldcg(ps + i) : 0.f;
+      }
     }
 #pragma unroll
-    for (int r = 0; r < R; ++r) a[r] = (a[r] + t0[r]) + t1[r];
+    for (int r = 0; r < R; ++r) a[r] = (((a[r] + t[0][r]) + t[1][r]) + t[2][r]) + t[3][r];
   }
 #pragma unroll
   for (int r = 0; r < R; ++r) {
@@ -1183,7 +1184,8 @@ __global__ void __launch_bounds__(kConsumers) k_samp_fast(const BEnv e, int cb, 
   float* fl = e.bflog + static_cast<size_t>(b) * d.cbs;
   const int NC = e.nb;
   sum_partials(fl, part, splits, NC, b, d.cbs);
-  __threadfence_block();
+  // the draw copies the row into shared memory through L2 (cp.async): make the stores visible there
+  __threadfence();
   __syncthreads();
   if (bs.dbg_fast) copy_row(bs.dbg_fast + (static_cast<size_t>(f) * (d.ncb - 1) + (cb - 1)) * d.cbs, fl, d.cbs);
   const float* E = bs.expo + static_cast<size_t>(f) * kDraws * kTopK + (1 + cb) * kTopK;
