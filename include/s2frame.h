@@ -22,7 +22,11 @@
  *  - "device" pointers are CUDA device memory (e.g. torch tensors); "host" pointers are
  *    ordinary host memory read before the call returns.
  *  - The library allocates no device memory: all of it (KV cache, per-stream state,
- *    scratch) lives in the caller's workspace.  It keeps only a small host-side object.
+ *    scratch) lives in the caller's workspace.  It keeps a small host-side object and, for
+ *    bf16 models, a private CUDA stream, the weights' tensor maps and one instantiated CUDA
+ *    graph per stream count decoded together (released by s2_frame_free).
+ *  - s2_stop_stream and s2_stream_progress are the exception to the ordering rule: they are
+ *    meant to run on a second, non-blocking stream while a decode call is in flight.
  *  - Return values are S2_* status codes; no C++ exception crosses this boundary.  A
  *    message for the last failure is available from s2_last_error().
  *  - Problems detected on the device (a grid barrier or pipeline wait that gave up) are
