@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--batched", default="serving", choices=["serving", "longctx", "none"],
                     help="also measure the aggregate of a batched workload (reported under 'batched')")
     ap.add_argument("--batched-steps", type=int, default=16)
+    ap.add_argument("--no-fp8", dest="fp8", action="store_false",
+                    help="skip the fp8 e4m3 weight-streaming measurements")
     ap.add_argument("--batched-streams", type=int, default=None,
                     help="profiling captures only: the first N streams of the batched workload")
     ap.add_argument("--slow-layers", type=int, default=None,
@@ -66,15 +68,18 @@ def frame_bytes(d, ctx_avg):
     per use (Fast-AR weights once per call), admissible tied-logit rows, embedding rows gathered,
     KV cache read over the context and the new slot written."""
     e = 2  # bf16
+    fp8 = bool(d.get("weight_fp8", 0))
+    # projection matrices: bf16, or e4m3 codes + one fp32 scale per row when streamed as fp8
+    mat = (lambda r, c: r * c + 4 * r) if fp8 else (lambda r, c: r * c * e)
     D, F, hd = d["dim"], d["ffn"], d["head_dim"]
-    lay = lambda D_, H, Hk, h, F_: ((H + 2 * Hk) * h * D_ + D_ * H * h + 3 * F_ * D_) * e
+    lay = lambda D_, H, Hk, h, F_: mat((H + 2 * Hk) * h, D_) + mat(D_, H * h) + 2 * mat(F_, D_) + mat(D_, F_)
     slow = d["n_layer"] * lay(D, d["n_head"], d["n_kv_head"], hd, F)
     logits = (d["codebook_size"] + 1) * D * e
     gathers = (1 + d["n_codebooks"]) * D * e + (d["n_codebooks"] - 1) * d["fast_dim"] * e
     fast = (d["n_codebooks"] - 1) * (d["fast_n_layer"] * lay(d["fast_dim"], d["fast_n_head"], d["fast_n_kv_head"],
                                                              d["fast_head_dim"], d["fast_ffn"])
-                                     + d["codebook_size"] * d["fast_dim"] * e)
-    proj = d["fast_dim"] * D * e
+                                     + mat(d["codebook_size"], d["fast_dim"]))
+    proj = mat(d["fast_dim"], D)
     kv_per_slot = d["n_layer"] * d["n_kv_head"] * hd * 2 * 2  # K and V, fp16
     kv = kv_per_slot * (ctx_avg + 1)  # read slots 0..pos, the new one written
     return slow + logits + gathers + fast + proj + kv, dict(slow=slow, logits=logits, fast=fast + proj, kv=kv)
@@ -215,13 +220,56 @@ def batched_measure(pkg, d, dev_w, cfg_name, steps, warmup, peak, local, n_strea
     step_bytes = w_bytes + sum(kv_slot * (c + 1) for c in ctx_avg)
     t = ms / 1000.0
     achieved = step_bytes * steps / t / 1e9
-    return {"workload": f"{cfg_name}: {n} streams, contexts {min(lengths)}..{kmax}, bf16 weights, fp16 KV "
+    wname = "fp8 e4m3 projections (per-row scales)" if d.get("weight_fp8") else "bf16 weights"
+    return {"workload": f"{cfg_name}: {n} streams, contexts {min(lengths)}..{kmax}, {wname}, fp16 KV "
                         f"(decode state imported, see docstring)",
             "streams": n, "frames_per_stream": steps, "warmup": warmup,
             "value": n * steps / t, "unit": "frames/s (aggregate)", "per_stream_fps": steps / t,
             "ms_per_step": ms / steps, "algorithmic_gb_per_step": step_bytes / 1e9,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak},
             "clocks": clk.summary()}
+
+
+def fp8_measure(pkg, d, dev_w, prompt, args, peak, local):
+    """The same two measurements with the projection matrices streamed as fp8 e4m3 (quantised by
+    the library at init): one stream (the frame workload, decoded by the batched engine) and the
+    batched workload."""
+    import torch
+    import synth
+    d8 = dict(d, weight_fp8=1)
+    K, W = args.steps, args.warmup
+    s = synth.sampling("frame", min_tokens_before_end=W + K + 1)
+    dec = pkg.Decoder(d8, dev_w, max_streams=1, kv_slots=PROMPT_LEN + W + K + 8)
+    dec.prefill([prompt])
+    expo_w = torch.from_numpy(synth.expo(100, 0, W)).cuda()[None]
+    dec.decode(W, s, expo_w)
+    torch.cuda.synchronize()
+    assert dec.sync_status() == pkg.S2_OK, pkg.s2_last_error(dec.ctx)
+    expo = torch.from_numpy(synth.expo(200, 0, K)).cuda()[None]
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        out = dec.decode(K, s, expo)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    assert dec.sync_status() == pkg.S2_OK, pkg.s2_last_error(dec.ctx)
+    assert int(out["n_out"][0]) == K
+    dec.close()
+    torch.cuda.empty_cache()
+    fb, parts = frame_bytes(d8, PROMPT_LEN + W + (K - 1) / 2.0)
+    achieved = fb * K / (ms / 1000.0) / 1e9
+    res = {"weights": "projections e4m3 + fp32 row scales; embeddings, norms and tied logits bf16",
+           "batch1": {"workload": "frame: 1 stream, context 512, batched engine", "value": K / (ms / 1000.0),
+                      "unit": "frames/s", "ms_per_step": ms / K, "algorithmic_gb_per_frame": fb / 1e9,
+                      "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                                   "frac": achieved / peak},
+                      "clocks": clk.summary()}}
+    if args.batched != "none":
+        res["batched"] = batched_measure(pkg, d8, dev_w, args.batched, args.batched_steps, W, peak, local,
+                                         args.batched_streams)
+    return res
 
 
 def cpu_oracle_sample(d, host_w, n_frames, s):
@@ -405,6 +453,10 @@ def main():
         torch.cuda.empty_cache()
         line["batched"] = batched_measure(pkg, d, dev_w, args.batched, args.batched_steps, args.warmup, pk, local,
                                           args.batched_streams)
+    if args.fp8 and args.slow_layers is None:
+        dec.close()
+        torch.cuda.empty_cache()
+        line["fp8"] = fp8_measure(pkg, d, dev_w, prompt, args, pk, local)
     if rank == 0 and not args.no_cpu_baseline and args.slow_layers is None:
         try:
             v, cores, sample = cpu_oracle_sample(d, host_w, args.cpu_frames, s)

@@ -21,7 +21,7 @@ STATUS_NAMES = {0: "S2_OK", 1: "S2_EINVAL", 2: "S2_ENOMEM", 3: "S2_ECAPACITY", 4
 EXPORTS = ("s2_weight_count", "s2_weight_info", "s2_frame_workspace_bytes", "s2_frame_init", "s2_prefill",
            "s2_decode_frames", "s2_fast_logits", "s2_sync_status", "s2_set_spin_limit", "s2_set_trace",
            "s2_phase_count", "s2_frame_free", "s2_last_error", "s2_fast_logits_static", "s2_stream_import",
-           "s2_stop_stream", "s2_stream_progress", "s2_codec_latent")
+           "s2_stop_stream", "s2_stream_progress", "s2_codec_latent", "s2_quantize_e4m3")
 
 
 class s2_dims(ctypes.Structure):
@@ -30,7 +30,7 @@ class s2_dims(ctypes.Structure):
                [(n, ctypes.c_float) for n in ("sem_scale", "norm_eps", "rope_base")] + \
                [(n, ctypes.c_int) for n in ("qk_norm", "rope_table_bf16", "fast_dim", "fast_n_layer", "fast_n_head",
                                             "fast_n_kv_head", "fast_head_dim", "fast_ffn", "fast_window",
-                                            "has_fast_project_in", "weight_dtype", "kv_dtype")]
+                                            "has_fast_project_in", "weight_dtype", "kv_dtype", "weight_fp8")]
 
 
 class s2_sampling(ctypes.Structure):
@@ -81,6 +81,7 @@ def load(path: str = LIB_PATH):
         "s2_stream_import": (i32, [vp, i32, i32, vp, vp, vp, vp]),
         "s2_stop_stream": (i32, [vp, i32, vp]),
         "s2_codec_latent": (i32, [i32, i32, i32, P(vp), i32, vp, vp, vp, vp]),
+        "s2_quantize_e4m3": (i32, [vp, ctypes.c_longlong, i32, vp, vp, vp]),
         "s2_stream_progress": (i32, [vp, i32, P(i32), vp, vp]),
     }
     for name, (res, args) in sig.items():
@@ -107,7 +108,7 @@ def _ints(seq):
 def make_dims(d: dict) -> s2_dims:
     s = s2_dims()
     for name, _ in s2_dims._fields_:
-        setattr(s, name, d[name])
+        setattr(s, name, d.get(name, 0) if name == "weight_fp8" else d[name])
     return s
 
 
@@ -161,6 +162,24 @@ def s2_codec_latent(n_codebooks: int, codebook_size: int, dim: int, quantizer_pt
     rc = load().s2_codec_latent(n_codebooks, codebook_size, dim, arr, n_frames, codes_ptr, latent_ptr, status_ptr,
                                 stream)
     return _check("s2_codec_latent", rc)
+
+
+def s2_quantize_e4m3(w_ptr: int, rows: int, cols: int, codes_ptr: int, scales_ptr: int, stream: int = 0):
+    """e4m3 codes + fp32 row scales of bf16 rows (device pointers; see s2frame.h)."""
+    return _check("s2_quantize_e4m3", load().s2_quantize_e4m3(w_ptr, rows, cols, codes_ptr, scales_ptr, stream))
+
+
+def quantize_e4m3(w):
+    """Device bf16 matrix (torch, [rows][cols]) -> (uint8 codes [rows][cols], fp32 scales [rows])."""
+    import torch
+    if w.dtype != torch.bfloat16 or w.dim() != 2 or not w.is_cuda:
+        raise ValueError("quantize_e4m3 takes a 2-D bf16 CUDA tensor")
+    w = w.contiguous()
+    codes = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+    scales = torch.empty(w.shape[0], dtype=torch.float32, device=w.device)
+    s2_quantize_e4m3(w.data_ptr(), w.shape[0], w.shape[1], codes.data_ptr(), scales.data_ptr(),
+                     torch.cuda.current_stream().cuda_stream)
+    return codes, scales
 
 
 def s2_decode_frames(ctx, stream_ids, n_frames: int, params, expo_ptr: int, forced_ptr: int | None, codes_ptr: int,

@@ -43,6 +43,9 @@ constexpr int kGemvThreads = 192;           // 4 epilogue warps, 1 TMA warp, 1 M
 constexpr int kMaxGemvStages = 8;
 constexpr int kGemvSmemBudget = 100 * 1024;  // two CTAs per SM
 constexpr int kGemvCtasPerSm = 2;
+// dynamic shared memory of a projection CTA is at least this much, so that no more than two of
+// them (each holding up to 256 TMEM columns of the SM's 512) are ever resident on one SM
+constexpr int kGemvSmemFloor = 80 * 1024;
 constexpr int kSamplerSplits = 4;             // split-K of projections summed by one CTA per stream
 constexpr int kPrefillCols = 128;             // prompt positions per projection launch (N = 256)
 constexpr int kPrepThreads = 1024;                // column preparation: one CTA per column
@@ -237,6 +240,217 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvCtasPerSm)
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tacc, ncols);
+}
+
+// =========================================================================================
+// fp8 projection: the same partials from e4m3 weights Q with one fp32 scale per row,
+// part[...] = scale[row0 + m]·Σ_{k in split} Q[row0 + m][k]·a_c[k].  A stage carries 128 K (one
+// 128-byte fp8 row per weight row, 128-byte swizzle) and the planes of those 128 K (two 64-K
+// boxes).  The four epilogue warps, idle until the accumulator is ready, expand every fp8 tile to
+// bf16 in registers (thread = tile row = TMEM lane) and store it into one of two tensor-memory A
+// buffers; the MMA reads A from tensor memory and B from shared memory, so the expanded tile never
+// goes through shared memory.
+// =========================================================================================
+
+constexpr int kAtom8 = 128;                // K elements per fp8 stage
+constexpr int kA8Bytes = kTileM * kAtom8;  // one fp8 weight tile (16 KB)
+
+struct Gemv8Bars {
+  uint64_t full[kMaxGemvStages], empty[kMaxGemvStages], afull[2], aempty[2], acc;
+  uint32_t taddr;
+};
+
+// accumulator columns [0, acc) and the two A buffers of 64 columns after them
+__host__ __device__ constexpr uint32_t gemv8_acc_cols(int N) { return N <= 128 ? 128u : 256u; }
+__host__ __device__ constexpr uint32_t gemv8_tmem_cols(int N) { return N <= 128 ? 256u : 512u; }
+
+__global__ void __launch_bounds__(kGemvThreads, kGemvCtasPerSm)
+    k_bgemv8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+             const __grid_constant__ CUtensorMap tmB, const float* scA, const float* scA2, int M, int row0, int N,
+             int NC, int atoms_total, int atoms_per, int nstages, float* part, Control* ctl) {
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  const int bbytes = N * 128;  // planes of 64 K
+  const int sbytes = kA8Bytes + 2 * bbytes;
+  Gemv8Bars& S = *reinterpret_cast<Gemv8Bars*>(sm + nstages * sbytes);
+  const int tile = blockIdx.x, split = blockIdx.y, z = blockIdx.z, splits = gridDim.y;
+  const int a0 = split * atoms_per, a1 = min(a0 + atoms_per, atoms_total);
+  const int na = a1 - a0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const CUtensorMap* tA = z == 0 ? &tmA : &tmA2;
+  const float* sc = z == 0 ? scA : scA2;
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < nstages; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 1 + 4);  // the MMA's commit and the four expanding warps
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.afull[b], 4);
+      mbar_init(&S.aempty[b], 1);
+    }
+    mbar_init(&S.acc, 1);
+    fence_barrier_init();
+  }
+  const uint32_t acc_cols = gemv8_acc_cols(N), ncols = gemv8_tmem_cols(N);
+  if (warp == 0) {
+    tmem_alloc(&S.taddr, ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tacc = S.taddr;
+  if (warp == 4) {
+    if (lane == 0) {
+      prefetch_tmap(tA);
+      prefetch_tmap(&tmB);
+      const uint64_t pol = policy_evict_first();
+      const int pre = min(nstages, na);
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&S.full[i], sbytes);
+        tma_load_2d(sm + i * sbytes, tA, (a0 + i) * kAtom8, row0 + tile * kTileM, &S.full[i], pol);
+      }
+      pdl_wait();
+      for (int i = 0; i < pre; ++i) {
+        unsigned char* Bs = sm + i * sbytes + kA8Bytes;
+        tma_load_2d(Bs, &tmB, (a0 + i) * kAtom8, 0, &S.full[i], pol);
+        tma_load_2d(Bs + bbytes, &tmB, (a0 + i) * kAtom8 + kAtom, 0, &S.full[i], pol);
+      }
+      for (int i = pre; i < na; ++i) {
+        const int s = i % nstages;
+        if (!wait_bar(&S.empty[s], ((i / nstages) & 1) ^ 1, ctl)) break;
+        unsigned char* A = sm + s * sbytes;
+        mbar_arrive_expect_tx(&S.full[s], sbytes);
+        tma_load_2d(A, tA, (a0 + i) * kAtom8, row0 + tile * kTileM, &S.full[s], pol);
+        tma_load_2d(A + kA8Bytes, &tmB, (a0 + i) * kAtom8, 0, &S.full[s], pol);
+        tma_load_2d(A + kA8Bytes + bbytes, &tmB, (a0 + i) * kAtom8 + kAtom, 0, &S.full[s], pol);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kTileM, N);
+      for (int i = 0; i < na; ++i) {
+        const int s = i % nstages, b = i & 1;
+        if (!wait_bar(&S.afull[b], (i >> 1) & 1, ctl)) break;
+        if (!wait_bar(&S.full[s], (i / nstages) & 1, ctl)) break;
+        tc_fence_after();
+        const uint32_t B = smem_u32(sm + s * sbytes + kA8Bytes);
+        const uint32_t abuf = tacc + acc_cols + static_cast<uint32_t>(b) * 64u;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_tmem_a(tacc, abuf + kk * 8, desc_sw128(B + (kk >> 2) * bbytes + (kk & 3) * 32), idesc,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&S.empty[s]);
+        tc_commit(&S.aempty[b]);
+      }
+      tc_commit(&S.acc);
+    }
+  } else {
+    const int r = warp * 32 + lane;  // tile row = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    for (int i = 0; i < na; ++i) {
+      const int s = i % nstages, b = i & 1;
+      if (!__all_sync(0xffffffffu, wait_bar(&S.full[s], (i / nstages) & 1, ctl))) break;
+      if (!__all_sync(0xffffffffu, wait_bar(&S.aempty[b], ((i >> 1) & 1) ^ 1, ctl))) break;
+      tc_fence_after();
+      const unsigned char* rowp = sm + s * sbytes + r * 128;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t o[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int chunk = h * 4 + c;  // K elements 16·chunk .. 16·chunk + 15
+          const uint4 w = *reinterpret_cast<const uint4*>(rowp + ((chunk ^ (r & 7)) << 4));
+          e4m3x4_to_bf16x4(w.x, o[c * 8 + 0], o[c * 8 + 1]);
+          e4m3x4_to_bf16x4(w.y, o[c * 8 + 2], o[c * 8 + 3]);
+          e4m3x4_to_bf16x4(w.z, o[c * 8 + 4], o[c * 8 + 5]);
+          e4m3x4_to_bf16x4(w.w, o[c * 8 + 6], o[c * 8 + 7]);
+        }
+        tmem_st32(tacc + lane_off + acc_cols + static_cast<uint32_t>(b) * 64u + h * 32, o);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&S.afull[b]);
+        mbar_arrive(&S.empty[s]);
+      }
+    }
+    const bool ok = __all_sync(0xffffffffu, wait_bar(&S.acc, 0, ctl));
+    pdl_wait();  // the partials buffer may still be read by the previous grid until it completes
+    if (ok) {
+      tc_fence_after();
+      const int row = tile * kTileM + r;
+      const float scale = row < M ? __ldg(sc + row0 + row) : 0.f;
+      float* out = part + (static_cast<size_t>(z) * splits + split) * NC * M;
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        float v[16];
+        tmem_ld16(tacc + lane_off + c0, v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int c = c0 / 2 + j;
+          if (c < NC && row < M) out[static_cast<size_t>(c) * M + row] = (v[2 * j] + v[2 * j + 1]) * scale;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tacc, ncols);
+}
+
+// e4m3 quantisation of bf16 rows: scale = max|w| / 448 (fp32 division), code = w / scale rounded
+// to the nearest e4m3 value, ties to even, saturating at ±448; an all-zero row gets scale 0 and
+// zero codes.  One CTA per row (grid-stride).
+constexpr int kQuantThreads = 256;
+
+__global__ void __launch_bounds__(kQuantThreads) k_quant_e4m3(const uint16_t* w, long long rows, int K, uint8_t* q,
+                                                              float* scales) {
+  __shared__ float red[kQuantThreads / 32];
+  for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
+    const uint16_t* wr = w + r * K;
+    float m = 0.f;
+    for (int k = threadIdx.x; k < K; k += kQuantThreads) m = fmaxf(m, fabsf(bf16_to_f(wr[k])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < kQuantThreads / 32; ++i) amax = fmaxf(amax, red[i]);
+    __syncthreads();
+    const float scale = __fdiv_rn(amax, 448.f);
+    if (threadIdx.x == 0) scales[r] = scale;
+    uint8_t* qr = q + r * K;
+    for (int k = threadIdx.x; k < K; k += kQuantThreads) {
+      uint8_t code = 0;
+      if (scale > 0.f) {
+        const float v = __fdiv_rn(bf16_to_f(wr[k]), scale);
+        uint16_t pair;  // v converted into both bytes
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(v), "f"(v));
+        code = static_cast<uint8_t>(pair & 0xFFu);
+      }
+      qr[k] = code;
+    }
+  }
+}
+
+// Check of the e4m3 -> bf16 expansion used by k_bgemv8 against the hardware e4m3 -> f16
+// conversion, over every finite code: bad[0] = number of codes that differ.
+__global__ void k_e4m3_selfcheck(int* bad) {
+  const uint32_t c = threadIdx.x;  // 256 threads, one code each
+  if ((c & 0x7Fu) == 0x7Fu) return;  // NaN codes are never produced
+  uint32_t lo, hi;
+  e4m3x4_to_bf16x4(c | (c << 8) | (c << 16) | (c << 24), lo, hi);
+  uint32_t h2;
+  const uint16_t in = static_cast<uint16_t>(c | (c << 8));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  const float ref = __half2float(__ushort_as_half(static_cast<uint16_t>(h2 & 0xFFFFu)));
+  const float got[4] = {bf16lo(lo), bf16hi(lo), bf16lo(hi), bf16hi(hi)};
+  bool ok = true;
+  for (int i = 0; i < 4; ++i)
+    ok = ok && __float_as_uint(got[i]) == __float_as_uint(ref);
+  if (!ok) atomicAdd(bad, 1);
 }
 
 // =========================================================================================
@@ -1320,12 +1534,12 @@ struct GemvPlan {
   int tiles, splits, per, atoms, nmat, M, K;
 };
 
-GemvPlan plan_gemv(int M, int K, int nmat, int sms, bool whole_k, int max_splits = 1 << 30) {
+GemvPlan plan_gemv(int M, int K, int nmat, int sms, bool whole_k, int max_splits = 1 << 30, int atom = kAtom) {
   GemvPlan g{};
   g.M = M;
   g.K = K;
   g.nmat = nmat;
-  g.atoms = K / kAtom;
+  g.atoms = K / atom;
   g.tiles = (M + kTileM - 1) / kTileM;
   int splits = whole_k ? 1 : std::max(1, std::min(std::min(g.atoms, max_splits), sms / std::max(1, g.tiles * nmat)));
   g.per = (g.atoms + splits - 1) / splits;
@@ -1359,12 +1573,40 @@ bool encode_map(CUtensorMap* m, const void* base, int inner, long long rows, int
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D fp8 (byte) tensor map over rows x K codes, box {128, 128}, 128-byte swizzle
+bool encode_map8(CUtensorMap* m, const void* base, int K, long long rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kAtom8), static_cast<cuuint32_t>(kTileM)};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// fp8 projection launch shape: stages that fit the shared-memory budget (two CTAs per SM up to
+// 128 MMA columns; wider tiles take one SM each, which also leaves their 512 TMEM columns alone)
+constexpr int kGemv8WideBudget = 200 * 1024;
+int gemv8_smem(int N, int* nst) {
+  const int sbytes = kA8Bytes + N * 256;
+  *nst = std::min(kMaxGemvStages, (N <= 128 ? kGemvSmemBudget : kGemv8WideBudget) / sbytes);
+  return std::max(kGemvSmemFloor, *nst * sbytes + 1024 + static_cast<int>(sizeof(Gemv8Bars)));
+}
+
 
 }  // namespace
+
+struct QEntry {
+  CUtensorMap map;  // fp8 codes
+  const float* s;   // row scales
+};
 
 struct Batch {
   BatchModel m;
   std::map<const void*, CUtensorMap> wmaps;
+  std::map<const void*, QEntry> qmaps;  // bf16 weight -> its e4m3 copy (fp8 weight streaming)
   std::map<std::tuple<const void*, int, int>, CUtensorMap> pmaps;
   BatchSizes sz{};
   std::vector<BStream> host_bs;
@@ -1389,6 +1631,9 @@ bool batch_supported(const Dims& d, int max_streams, std::string* why) {
     if (k % kAtom != 0) return no("projection lengths must be multiples of 64");
   if (d.D > kPrepMaxK || d.Df > kPrepMaxK) return no("model width above the column-preparation limit");
   if (d.Wf > 16) return no("Fast-AR window above 16");
+  if (d.fp8)
+    for (int k : ks)
+      if (k % kAtom8 != 0) return no("fp8 projection lengths must be multiples of 128");
   return true;
 }
 
@@ -1450,6 +1695,13 @@ Batch* batch_create(const BatchModel& m, std::string* err) {
     ok = add(w.wqkv, QKVf, d.Df) && add(w.wo, d.Df, d.Hqf * d.hdf) && add(w.w1, d.Ff, d.Df) &&
          add(w.w3, d.Ff, d.Df) && add(w.w2, d.Df, d.Ff);
   }
+  for (int i = 0; i < m.n_qw && ok; ++i) {
+    const QuantW& q = m.qw[i];
+    QEntry e{};
+    e.s = q.s;
+    ok = encode_map8(&e.map, q.q, q.cols, q.rows);
+    b->qmaps[q.w] = e;
+  }
   if (!ok) {
     *err = "encoding a weight tensor map failed";
     delete b;
@@ -1469,7 +1721,9 @@ Batch* batch_create(const BatchModel& m, std::string* err) {
     return nullptr;
   }
   const int gsmem = kGemvSmemBudget + 1024 + static_cast<int>(sizeof(GemvBars));
-  if (cudaFuncSetAttribute(k_bgemv, cudaFuncAttributeMaxDynamicSharedMemorySize, gsmem) != cudaSuccess) {
+  const int g8smem = kGemv8WideBudget + 1024 + static_cast<int>(sizeof(Gemv8Bars));
+  if (cudaFuncSetAttribute(k_bgemv, cudaFuncAttributeMaxDynamicSharedMemorySize, gsmem) != cudaSuccess ||
+      cudaFuncSetAttribute(k_bgemv8, cudaFuncAttributeMaxDynamicSharedMemorySize, g8smem) != cudaSuccess) {
     *err = "setting the projection kernel's shared memory failed";
     delete b;
     return nullptr;
@@ -1480,11 +1734,7 @@ Batch* batch_create(const BatchModel& m, std::string* err) {
 int batch_prefill_proj(Batch* b, const void* w0, const void* w1, int M, int K, const uint16_t* planes, int ld, int NC,
                        float* part, void* stream) {
   if (NC < 1 || NC > kPrefillCols || K % kAtom != 0) return -1;
-  const GemvPlan g = plan_gemv(M, K, w1 ? 2 : 1, kGemvCtasPerSm * b->m.sms, false);
   const int N = round16(2 * NC);
-  auto wa = b->wmaps.find(w0);
-  auto wb = b->wmaps.find(w1 ? w1 : w0);
-  if (wa == b->wmaps.end() || wb == b->wmaps.end()) return -1;
   auto key = std::make_tuple(static_cast<const void*>(planes), N, K);
   auto it = b->pmaps.find(key);
   if (it == b->pmaps.end()) {
@@ -1492,9 +1742,26 @@ int batch_prefill_proj(Batch* b, const void* w0, const void* w1, int M, int K, c
     if (!encode_map(&t, planes, K, N, ld, N)) return -1;
     it = b->pmaps.emplace(key, t).first;
   }
+  auto qa = b->qmaps.find(w0);
+  if (qa != b->qmaps.end()) {
+    auto qb = b->qmaps.find(w1 ? w1 : w0);
+    if (qb == b->qmaps.end() || K % kAtom8 != 0) return -1;
+    const GemvPlan g = plan_gemv(M, K, w1 ? 2 : 1, kGemvCtasPerSm * b->m.sms, false, 1 << 30, kAtom8);
+    int nst = 0;
+    const int smem = gemv8_smem(N, &nst);
+    dim3 grid(g.tiles, g.splits, g.nmat);
+    k_bgemv8<<<grid, kGemvThreads, smem, static_cast<cudaStream_t>(stream)>>>(
+        qa->second.map, qb->second.map, it->second, qa->second.s, qb->second.s, M, 0, N, NC, g.atoms, g.per, nst,
+        part, b->m.ctl);
+    return cudaGetLastError() == cudaSuccess ? g.splits : -1;
+  }
+  const GemvPlan g = plan_gemv(M, K, w1 ? 2 : 1, kGemvCtasPerSm * b->m.sms, false);
+  auto wa = b->wmaps.find(w0);
+  auto wb = b->wmaps.find(w1 ? w1 : w0);
+  if (wa == b->wmaps.end() || wb == b->wmaps.end()) return -1;
   const int sbytes = kABytes + N * 128;
   const int nst = std::min(kMaxGemvStages, kGemvSmemBudget / sbytes);
-  const int smem = nst * sbytes + 1024 + static_cast<int>(sizeof(GemvBars));
+  const int smem = std::max(kGemvSmemFloor, nst * sbytes + 1024 + static_cast<int>(sizeof(GemvBars)));
   dim3 grid(g.tiles, g.splits, g.nmat);
   k_bgemv<<<grid, kGemvThreads, smem, static_cast<cudaStream_t>(stream)>>>(
       wa->second, wb->second, it->second, M, 0, N, NC, g.atoms, g.per, nst, part, b->m.ctl);
@@ -1527,6 +1794,21 @@ size_t batch_prefill_part_floats(const Dims& d, int sms) {
   acc(d.F, d.D, 2);
   acc(d.D, d.F, 1);
   return mx;
+}
+
+int quantize_e4m3(const void* w, long long rows, int K, uint8_t* q, float* scales, void* stream) {
+  if (rows <= 0 || K <= 0) return 0;
+  const int grid = static_cast<int>(std::min<long long>(rows, 152LL * 8));
+  k_quant_e4m3<<<grid, kQuantThreads, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<const uint16_t*>(w), rows,
+                                                                             K, q, scales);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int e4m3_selfcheck(int* bad, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(bad, 0, sizeof(int), s) != cudaSuccess) return -1;
+  k_e4m3_selfcheck<<<1, 256, 0, s>>>(bad);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
 void batch_destroy(Batch* b) {
@@ -1575,6 +1857,20 @@ struct Frame {
   // projection of NC columns; returns the plan (partials layout)
   GemvPlan gemv(const void* w0, const void* w1, int M, int K, int row0, uint16_t* pl, int ld, int NC, bool whole_k,
                int max_splits = 1 << 30) {
+    auto q0 = b->qmaps.find(w0);
+    if (q0 != b->qmaps.end()) {
+      const QEntry& qa = q0->second;
+      const QEntry& qb = w1 ? b->qmaps.at(w1) : qa;
+      const GemvPlan g = plan_gemv(M, K, w1 ? 2 : 1, kGemvCtasPerSm * b->m.sms, whole_k, max_splits, kAtom8);
+      const int N = round16(2 * NC);
+      const CUtensorMap& tb = planes(pl, N, K, ld);
+      int nst = 0;
+      const int smem = gemv8_smem(N, &nst);
+      dim3 grid(g.tiles, g.splits, g.nmat);
+      launch(k_bgemv8, grid, kGemvThreads, smem, qa.map, qb.map, tb, qa.s, qb.s, M, row0, N, NC, g.atoms, g.per, nst,
+             e.part, e.ctl);
+      return g;
+    }
     const GemvPlan g = plan_gemv(M, K, w1 ? 2 : 1, kGemvCtasPerSm * b->m.sms, whole_k, max_splits);
     const int N = round16(2 * NC);
     const CUtensorMap& ta = b->wmaps.at(w0);
@@ -1582,7 +1878,7 @@ struct Frame {
     const CUtensorMap& tb = planes(pl, N, K, ld);
     const int sbytes = kABytes + N * 128;
     const int nst = std::min(kMaxGemvStages, kGemvSmemBudget / sbytes);
-    const int smem = nst * sbytes + 1024 + static_cast<int>(sizeof(GemvBars));
+    const int smem = std::max(kGemvSmemFloor, nst * sbytes + 1024 + static_cast<int>(sizeof(GemvBars)));
     dim3 grid(g.tiles, g.splits, g.nmat);
     launch(k_bgemv, grid, kGemvThreads, smem, ta, ta2, tb, M, row0, N, NC, g.atoms, g.per, nst, e.part, e.ctl);
     return g;

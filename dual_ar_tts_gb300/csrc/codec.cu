@@ -70,3 +70,10 @@ extern "C" int s2_codec_latent(int ncb, int cbs, int dim, const void* const* qua
                                                                                latent, status);
   return cudaGetLastError() == cudaSuccess ? S2_OK : S2_ECUDA;
 }
+
+extern "C" int s2_quantize_e4m3(const void* w, long long rows, int cols, uint8_t* codes, float* scales,
+                                CUstream_st* stream) {
+  if (!w || !codes || !scales || rows < 1 || cols < 1) return S2_EINVAL;
+  if (reinterpret_cast<uintptr_t>(w) % 2 != 0 || reinterpret_cast<uintptr_t>(scales) % 4 != 0) return S2_EINVAL;
+  return quantize_e4m3(w, rows, cols, codes, scales, stream) == 0 ? S2_OK : S2_ECUDA;
+}

@@ -53,6 +53,8 @@ struct s2_ctx {
   uint16_t* pf_planes = nullptr;   // prompt projections: planes [256][pf_ld]
   int pf_ld = 0;
   float* pf_part = nullptr;
+  std::vector<QuantW> qw;          // fp8 weight streaming: e4m3 copies of the projections
+  int* qbad = nullptr;             // expansion check result
 };
 
 namespace {
@@ -104,6 +106,7 @@ bool to_dims(const s2_dims* s, Dims& d, std::string& why) {
   d.qk_norm = s->qk_norm; d.rope_bf16 = s->rope_table_bf16; d.Df = s->fast_dim; d.Lf = s->fast_n_layer;
   d.Hqf = s->fast_n_head; d.Hkvf = s->fast_n_kv_head; d.hdf = s->fast_head_dim; d.Ff = s->fast_ffn;
   d.Wf = s->fast_window; d.has_proj = s->has_fast_project_in; d.wdt = s->weight_dtype; d.kvdt = s->kv_dtype;
+  d.fp8 = s->weight_fp8;
   d.esz = d.wdt == S2_BF16 ? 2 : 4;
   d.kvsz = d.kvdt == S2_F16 ? 2 : 4;
   d.A = d.cbs + 1;
@@ -111,6 +114,10 @@ bool to_dims(const s2_dims* s, Dims& d, std::string& why) {
   if (d.wdt != S2_BF16 && d.wdt != S2_F32) return bad("weight_dtype must be S2_BF16 or S2_F32");
   if (d.kvdt != S2_F16 && d.kvdt != S2_F32) return bad("kv_dtype must be S2_F16 or S2_F32");
   if ((d.wdt == S2_BF16) != (d.kvdt == S2_F16)) return bad("bf16 weights go with an S2_F16 KV cache, fp32 weights with S2_F32");
+  if (d.fp8 != 0 && d.fp8 != 1) return bad("weight_fp8 must be 0 or 1");
+  if (d.fp8 && d.wdt != S2_BF16) return bad("fp8 weight streaming needs bf16 weights");
+  if (d.fp8 && (d.D % 128 || d.Df % 128 || d.F % 128 || d.Ff % 128 || (d.Hq * d.hd) % 128 || (d.Hqf * d.hdf) % 128))
+    return bad("fp8 weight streaming needs projection lengths that are multiples of 128");
   const int al = d.wdt == S2_BF16 ? 8 : 4;
   if (d.D <= 0 || d.D % al || d.Df <= 0 || d.Df % al) return bad("dim/fast_dim must be positive multiples of 16 bytes");
   if (d.L < 0 || d.Lf <= 0) return bad("a fast decoder (fast_n_layer > 0) is required");
@@ -269,6 +276,34 @@ void carve(s2_ctx* c, Carver& cv) {
     c->pf_ld = std::max(std::max(d.D, d.Hq * d.hd), d.F);
     c->pf_planes = cv.take<uint16_t>(static_cast<size_t>(2 * kPrefillChunkTC) * c->pf_ld);
     c->pf_part = cv.take<float>(batch_prefill_part_floats(d, c->sms));
+  }
+  // fp8 weight streaming: e4m3 codes + row scales of every projection matrix
+  c->qw.clear();
+  if (d.fp8) {
+    auto addq = [&](const void* w, long long rows, int cols) {
+      QuantW q{};
+      q.w = w;
+      q.rows = rows;
+      q.cols = cols;
+      q.q = cv.take<uint8_t>(static_cast<size_t>(rows) * cols);
+      q.s = cv.take<float>(static_cast<size_t>(rows));
+      c->qw.push_back(q);
+    };
+    auto layers = [&](const std::vector<LayerW>& v, int n, int D, int qkv, int hq, int F) {
+      for (int l = 0; l < n; ++l) {
+        const bool have = l < static_cast<int>(v.size());
+        addq(have ? v[l].wqkv : nullptr, qkv, D);
+        addq(have ? v[l].wo : nullptr, D, hq);
+        addq(have ? v[l].w1 : nullptr, F, D);
+        addq(have ? v[l].w3 : nullptr, F, D);
+        addq(have ? v[l].w2 : nullptr, D, F);
+      }
+    };
+    layers(c->slow, d.L, d.D, QKV, d.Hq * d.hd, d.F);
+    layers(c->fast, d.Lf, d.Df, QKVf, d.Hqf * d.hdf, d.Ff);
+    if (d.has_proj) addq(c->P, d.Df, d.D);
+    addq(c->FO, d.cbs, d.Df);
+    c->qbad = cv.take<int>(1);
   }
 }
 
@@ -636,6 +671,12 @@ int s2_frame_init(const s2_dims* s, const void* const* weights, int n_weights, v
     delete c;
     return fail(nullptr, S2_ENOMEM, "workspace too small: need " + std::to_string(align_up(cv.off, 256)) + " bytes");
   }
+  if (d.fp8 && !c->batched) {
+    std::string why;
+    batch_supported(d, max_streams, &why);
+    delete c;
+    return fail(nullptr, S2_EINVAL, "fp8 weight streaming runs on the batched decode engine: " + why);
+  }
   Carver real{c->ws};
   carve(c, real);
   // control block, stream states, tables
@@ -659,9 +700,24 @@ int s2_frame_init(const s2_dims* s, const void* const* weights, int n_weights, v
   }
   c->host_pos.assign(max_streams, 0);
   c->host_prefilled.assign(max_streams, 0);
+  if (d.fp8) {
+    // quantise every projection once, and check the kernel's fp8 expansion on this device
+    int bad = -1;
+    bool ok = true;
+    for (const QuantW& q : c->qw) ok = ok && quantize_e4m3(q.w, q.rows, q.cols, q.q, q.s, nullptr) == 0;
+    ok = ok && e4m3_selfcheck(c->qbad, nullptr) == 0 &&
+         cudaMemcpy(&bad, c->qbad, sizeof(int), cudaMemcpyDeviceToHost) == cudaSuccess;
+    if (!ok || bad != 0) {
+      delete c;
+      return fail(nullptr, S2_ECUDA, !ok ? "quantising the projections to e4m3 failed"
+                                         : "the fp8 expansion differs from the hardware conversion on this device");
+    }
+  }
   if (c->batched) {
     BatchModel& m = c->bm;
     m.d = d;
+    m.qw = c->qw.data();
+    m.n_qw = static_cast<int>(c->qw.size());
     m.E = c->E;
     m.CE = c->CE;
     m.FE = c->FE;
@@ -801,7 +857,7 @@ int s2_decode_frames(s2_ctx* c, int n, const int* ids, int n_frames, const s2_sa
     for (int j = 0; j < k; ++j)
       if (ids[j] == sid) return fail(c, S2_EINVAL, "a stream appears twice");
   }
-  if (c->batch && n >= 2) {
+  if (c->batch && (n >= 2 || d.fp8)) {
     int max_ctx = 0;
     for (int k = 0; k < n; ++k) max_ctx = std::max(max_ctx, c->host_pos[ids[k]] + n_frames);
     std::string why;
@@ -886,6 +942,7 @@ int s2_fast_logits(s2_ctx* c, int n_frames, const float* hidden, const int32_t* 
   if (!c) return fail(nullptr, S2_EINVAL, "ctx is NULL");
   const Dims& d = c->d;
   if (n_frames <= 0 || !hidden || !prefix || !logits) return fail(c, S2_EINVAL, "bad fast_logits arguments");
+  if (d.fp8) return fail(c, S2_ESTATE, "the Fast-AR-alone path streams bf16 weights (fp8 contexts decode frames only)");
   CallParams cp = base_params(c);
   cp.n_frames = n_frames;
   cp.fast_only = 1;
@@ -1136,6 +1193,7 @@ extern "C" int s2_fast_logits_static(const s2_dims* s, const void* const* weight
   Dims d;
   std::string why;
   if (!s || !to_dims(s, d, why)) return static_fail(S2_EINVAL, "bad dims: " + why);
+  if (d.fp8) return static_fail(S2_EINVAL, "the static entry streams bf16 or fp32 weights (weight_fp8 must be 0)");
   if (!weights || n_weights != layer_count(d)) return static_fail(S2_EINVAL, "weight table size does not match the dims");
   if (n_frames <= 0 || n_frames > kStaticMaxFrames) return static_fail(S2_EINVAL, "n_frames must be in 1..1048576");
   if (!hidden || !prefix || !logits) return static_fail(S2_EINVAL, "hidden, prefix and logits are required");

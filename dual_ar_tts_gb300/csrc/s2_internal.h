@@ -61,6 +61,7 @@ struct Dims {
   int esz;       // weight element bytes
   int kvsz;      // KV element bytes
   int A;         // admissible logits = cbs + 1
+  int fp8;       // projection matrices streamed as e4m3 + per-row scales (quantised copies)
 };
 
 struct LayerW {
@@ -218,8 +219,19 @@ struct BatchSizes {
   size_t apart_floats;     // attention split partials
 };
 
+// e4m3 copy of one bf16 projection matrix (fp8 weight streaming)
+struct QuantW {
+  const void* w;      // the bf16 matrix it stands for
+  uint8_t* q;         // codes [rows][cols]
+  float* s;           // row scales [rows]
+  long long rows;
+  int cols;
+};
+
 struct BatchModel {
   Dims d;
+  const QuantW* qw;        // [n_qw]: projections streamed as fp8 (none: bf16)
+  int n_qw;
   const void *E, *CE, *FE, *P, *FO, *norm, *fnorm;
   const LayerW* slow;      // [L]
   const LayerW* fast;      // [Lf]
@@ -252,6 +264,11 @@ void batch_destroy(Batch* b);
 int batch_prefill_proj(Batch* b, const void* w0, const void* w1, int M, int K, const uint16_t* planes, int ld, int NC,
                        float* part, void* stream);
 size_t batch_prefill_part_floats(const Dims& d, int sms);
+// e4m3 codes and row scales of bf16 rows (rows x K): 0 or -1 (launch failed)
+int quantize_e4m3(const void* w, long long rows, int K, uint8_t* q, float* scales, void* stream);
+// the fp8 expansion of the projection kernel against the hardware conversion: *bad (device) =
+// number of codes that differ
+int e4m3_selfcheck(int* bad, void* stream);
 // Prompt attention of a chunk (positions pos0..pos0+Tc-1, causal) on the tensor cores; K/V of this
 // stream's layer [Hkv][slots][hd] fp16 already hold every slot up to pos0+Tc-1.  0 or -1.
 int batch_prefill_attn(const float* QKV, int Tc, int pos0, const Dims& d, const void* Kc, const void* Vc, int slots,

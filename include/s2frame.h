@@ -69,6 +69,12 @@ typedef struct s2_dims {
   int weight_dtype;     /* S2_F32 or S2_BF16: every weight tensor has this type */
   int kv_dtype;         /* Slow-AR KV cache element type: S2_F16 with bf16 weights, S2_F32 with fp32
                            weights (the supported pairs); head_dim == fast_head_dim, 64 or 128 */
+  int weight_fp8;       /* 1: stream the projection matrices (wqkv, wo, w1, w3, w2 of both transformers,
+                           fast_project_in, fast_output) as fp8 e4m3 with one fp32 scale per row
+                           (scale = max|row| / 448, round to nearest even, saturating), quantised by
+                           s2_frame_init into the workspace from the bf16 weights; embeddings, norms
+                           and the tied logits stay bf16.  bf16 weights only, projection lengths
+                           multiples of 128.  0: stream bf16. */
 } s2_dims;
 
 /* Sampler settings of one stream ([ch.06 §5.3, §6]; Mizuoto "Fish Speech" engine page:
@@ -255,6 +261,24 @@ int s2_fast_logits_static(const s2_dims* d, const void* const* weights, int n_we
  * pointers or alignment; S2_ECUDA launch failed. */
 int s2_codec_latent(int n_codebooks, int codebook_size, int dim, const void* const* quantizers, int n_frames,
                     const int32_t* codes, float* latent, int32_t* status, struct CUstream_st* stream);
+
+/* e4m3 quantisation of bf16 rows, the one s2_frame_init applies to the projection matrices when
+ * weight_fp8 = 1 (low-precision weight streaming; the precedent on the pages is s2.cpp's
+ * K-quantised GGUF tensors, s2.cpp analysis ch.02 §5 and ch.04 §4; the e4m3 format and the row
+ * scaling are this library's choice): per row r of w [rows][cols],
+ *   scales[r] = max_k |w[r][k]| / 448          (fp32 division, rounded to nearest)
+ *   codes[r][k] = e4m3(w[r][k] / scales[r])    (fp32 division; round to nearest, ties to even,
+ *                                               saturating at ±448; never a NaN code)
+ * and an all-zero row gets scale 0 and zero codes.  e4m3 = sign, 4 exponent bits (bias 7), 3
+ * mantissa bits, exponent field 0 = subnormals m·2^-9.  The decode then uses
+ * scales[r]·value(codes[r][k]) in place of w[r][k].
+ *   w       device bf16 [rows][cols], 2-byte aligned
+ *   codes   device uint8 [rows][cols]
+ *   scales  device fp32 [rows], 4-byte aligned
+ * Stateless; allocates nothing; asynchronous on `stream`.
+ * Errors (nothing launched): S2_EINVAL bad pointer, alignment or size; S2_ECUDA launch failed. */
+int s2_quantize_e4m3(const void* w, long long rows, int cols, uint8_t* codes, float* scales,
+                     struct CUstream_st* stream);
 
 #ifdef __cplusplus
 }

@@ -83,6 +83,10 @@ def _load():
                 "or_draw": (i32, [vp, vp, i32, f32, f32, i32, vp, vp]),
                 "or_kv_set_f16": (i32, [vp, i32, i32, vp, vp]),
                 "or_head": (i32, [vp, vp, vp, vp]),
+                "or_e4m3_value": (f64, [i32]),
+                "or_e4m3_encode": (i32, [f32]),
+                "or_quant_e4m3": (None, [vp, ctypes.c_longlong, i32, vp, vp]),
+                "or_bind_e4m3": (i32, [vp, i32, vp, vp, i32]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -147,10 +151,56 @@ def draw(logits, temperature, top_p, top_k, E, ids=None):
 
 # ---------------------------------------------------------------- the session
 
-class Session:
-    """One stream of the oracle: weights (host arrays, table order) + its own fp32 KV cache."""
+# ------------------------------------------------------------------ e4m3 weights
 
-    def __init__(self, d: dict, weights, slots: int):
+def e4m3_value(code: int) -> float:
+    """Value of an e4m3 code (OCP 8-bit float E4M3: bias 7, 3 mantissa bits, subnormals m*2^-9)."""
+    return _load().or_e4m3_value(int(code))
+
+
+def e4m3_encode(x: float) -> int:
+    """Nearest e4m3 code of a finite fp32 x (ties to even mantissa; magnitudes >= 448 -> 448)."""
+    return _load().or_e4m3_encode(float(x))
+
+
+def quant_e4m3(w_bf16):
+    """bf16 bit patterns [rows][cols] -> (uint8 codes [rows][cols], fp32 scales [rows]):
+    scale = max|row| / 448 in fp32, code = e4m3(w / scale) (fp32 division); zero rows -> 0, 0."""
+    w = np.ascontiguousarray(w_bf16, dtype=np.uint16)
+    rows, cols = (w.shape[0], int(np.prod(w.shape[1:]))) if w.ndim > 1 else (1, w.shape[0])
+    codes = np.empty((rows, cols), np.uint8)
+    scales = np.empty(rows, np.float32)
+    _load().or_quant_e4m3(w.ctypes.data, rows, cols, codes.ctypes.data, scales.ctypes.data)
+    return codes, scales
+
+
+def projection_indices(d: dict):
+    """Table indices of the projection matrices (wqkv, wo, w1, w3, w2 of every layer of both
+    transformers, fast_project_in when present, fast_output)."""
+    out = []
+    for l in range(d["n_layer"]):
+        out += [3 + 9 * l + f for f in (1, 4, 6, 7, 8)]
+    base = 3 + 9 * d["n_layer"]
+    if d["has_fast_project_in"]:
+        out.append(base)
+    out.append(base + 3)
+    for l in range(d["fast_n_layer"]):
+        out += [base + 4 + 9 * l + f for f in (1, 4, 6, 7, 8)]
+    return out
+
+
+def quantize_projections(d: dict, weights):
+    """{table index: (codes, scales)} for every projection of a bf16 weight table."""
+    return {i: quant_e4m3(weights[i]) for i in projection_indices(d)}
+
+
+class Session:
+    """One stream of the oracle: weights (host arrays, table order) + its own fp32 KV cache.
+
+    With ``quant`` ({table index: (codes, scales)}, see ``quantize_projections``) those entries
+    are read as scale[row] * e4m3_value(code) instead of the bf16 matrix."""
+
+    def __init__(self, d: dict, weights, slots: int, quant=None):
         lib = _load()
         self.d = d
         self._dims = dims_struct(d)
@@ -163,6 +213,10 @@ class Session:
         if not self._h:
             raise MemoryError("oracle session allocation failed")
         self.slots = slots
+        self._quant = quant
+        for i, (codes, scales) in (quant or {}).items():
+            if lib.or_bind_e4m3(self._h, int(i), codes.ctypes.data, scales.ctypes.data, int(codes.shape[-1])):
+                raise ValueError(f"binding e4m3 weights to table entry {i} failed")
 
     def close(self):
         if getattr(self, "_h", None):

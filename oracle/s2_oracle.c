@@ -39,6 +39,8 @@ typedef struct or_dims {
 typedef struct {
   const void* p;
   int bf16;
+  const float* rs; /* non-NULL: p holds e4m3 codes, one scale per row of `cols` codes */
+  int cols;
 } wref;
 
 static inline float bf16_bits_to_f32(uint16_t h) {
@@ -59,7 +61,60 @@ static inline float f32_to_bf16_value(float f) {
 
 static inline float f32_to_f16_value(float f) { return (float)(_Float16)f; }
 
+/* ------------------------------------------------------ e4m3 weights
+ * Low-precision weight streaming (the K-quantised GGUF tensors of s2.cpp are the pages'
+ * precedent, s2.cpp analysis ch.02 §5 and ch.04 §4; the format and the scaling below are the
+ * library's choice).  e4m3 as the OCP 8-bit float E4M3 defines it: sign bit, 4 exponent bits with
+ * bias 7, 3 mantissa bits, no infinities, S.1111.111 = NaN; exponent field 0 holds the
+ * subnormals m * 2^-9.  Largest finite value 1.75 * 2^8 = 448. */
+
+double or_e4m3_value(int code) {
+  const int e = (code >> 3) & 15, m = code & 7;
+  const double v = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+  return (code & 0x80) ? -v : v;
+}
+
+/* nearest e4m3 value of a finite x, ties to the even mantissa, magnitudes from 448 up -> 448 */
+int or_e4m3_encode(float x) {
+  const int sign = signbit(x) ? 0x80 : 0;
+  const double a = fabs((double)x);
+  if (a >= 448.0) return sign | 0x7E;
+  if (a < ldexp(1.0, -6)) /* subnormal steps of 2^-9; 8 steps is the smallest normal, code 0x08 */
+    return sign | (int)nearbyint(a * 512.0);
+  int e2;
+  frexp(a, &e2);
+  int E = e2 - 1; /* 2^E <= a < 2^(E+1), -6 <= E <= 8 */
+  double q = nearbyint(ldexp(a, 3 - E)); /* a / 2^(E-3) in [8, 16): 8 + mantissa */
+  if (q == 16.0) {
+    q = 8.0;
+    E += 1;
+  }
+  return sign | ((E + 7) << 3) | ((int)q - 8);
+}
+
+/* per row: scale = max|w| / 448 (fp32), code = e4m3(w / scale) (fp32 division); all-zero rows get
+ * scale 0 and zero codes */
+void or_quant_e4m3(const uint16_t* w, long long rows, int cols, uint8_t* codes, float* scales) {
+#pragma omp parallel for schedule(static)
+  for (long long r = 0; r < rows; ++r) {
+    const uint16_t* wr = w + r * cols;
+    float amax = 0.f;
+    for (int k = 0; k < cols; ++k) {
+      const float a = fabsf(bf16_bits_to_f32(wr[k]));
+      if (a > amax) amax = a;
+    }
+    const float scale = amax / 448.0f;
+    scales[r] = scale;
+    for (int k = 0; k < cols; ++k)
+      codes[r * cols + k] = scale > 0.f ? (uint8_t)or_e4m3_encode(bf16_bits_to_f32(wr[k]) / scale) : 0;
+  }
+}
+
+/* the 256 code values, filled by or_bind_e4m3 before any session reads codes */
+static double g_e4m3[256];
+
 static inline float wget(wref w, size_t i) {
+  if (w.rs) return (float)(g_e4m3[((const uint8_t*)w.p)[i]] * (double)w.rs[i / (size_t)w.cols]);
   return w.bf16 ? bf16_bits_to_f32(((const uint16_t*)w.p)[i]) : ((const float*)w.p)[i];
 }
 
@@ -590,4 +645,40 @@ int or_draw(const float* logits, const int32_t* ids, int n, float temperature, f
   }
   free(c);
   return tok;
+}
+
+/* weight table entry i of a session (the order of or_new's table) */
+static wref* table_ref(or_sess* s, int i) {
+  const or_dims* d = &s->d;
+  if (i < 0 || i >= or_weight_count(d)) return NULL;
+  if (i == 0) return &s->E;
+  if (i == 1) return &s->CE;
+  if (i == 2) return &s->norm;
+  i -= 3;
+  if (i < 9 * d->n_layer) {
+    or_layer* L = &s->slow[i / 9];
+    wref* f[9] = {&L->an, &L->wqkv, &L->qn, &L->kn, &L->wo, &L->fn, &L->w1, &L->w3, &L->w2};
+    return f[i % 9];
+  }
+  i -= 9 * d->n_layer;
+  if (i == 0) return &s->P;
+  if (i == 1) return &s->FE;
+  if (i == 2) return &s->fnorm;
+  if (i == 3) return &s->FO;
+  i -= 4;
+  or_layer* L = &s->fast[i / 9];
+  wref* f[9] = {&L->an, &L->wqkv, &L->qn, &L->kn, &L->wo, &L->fn, &L->w1, &L->w3, &L->w2};
+  return f[i % 9];
+}
+
+/* read table entry i from e4m3 codes [rows][cols] and row scales instead */
+int or_bind_e4m3(or_sess* s, int i, const uint8_t* codes, const float* scales, int cols) {
+  wref* w = table_ref(s, i);
+  if (!w || !codes || !scales || cols <= 0) return 1;
+  for (int c = 0; c < 256; ++c) g_e4m3[c] = or_e4m3_value(c);
+  w->p = codes;
+  w->bf16 = 0;
+  w->rs = scales;
+  w->cols = cols;
+  return 0;
 }

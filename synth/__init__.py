@@ -124,7 +124,7 @@ _S2PRO = dict(
     sem_scale=1.0 / math.sqrt(11.0), norm_eps=1e-6, rope_base=1e6, qk_norm=1, rope_table_bf16=1,
     fast_dim=2560, fast_n_layer=4, fast_n_head=32, fast_n_kv_head=8, fast_head_dim=128,
     fast_ffn=9728, fast_window=11, has_fast_project_in=1,
-    weight_dtype=BF16, kv_dtype=F16,
+    weight_dtype=BF16, kv_dtype=F16, weight_fp8=0,
 )
 
 _TINY = dict(
@@ -133,7 +133,7 @@ _TINY = dict(
     sem_scale=1.0 / math.sqrt(5.0), norm_eps=1e-6, rope_base=1e6, qk_norm=1, rope_table_bf16=1,
     fast_dim=256, fast_n_layer=2, fast_n_head=4, fast_n_kv_head=2, fast_head_dim=64,
     fast_ffn=768, fast_window=5, has_fast_project_in=1,
-    weight_dtype=F32, kv_dtype=F32,
+    weight_dtype=F32, kv_dtype=F32, weight_fp8=0,
 )
 
 _SAMPLING = dict(temperature=0.8, top_p=0.8, ras_temperature=1.0, ras_top_p=0.9, top_k=30, ras_window=10)

@@ -8,6 +8,7 @@ import subprocess
 
 import pytest
 
+import numpy as np
 import synth
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -25,7 +26,7 @@ def lib():
 def _declared():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(s2_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(s2_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declarations_are_exported(lib):
@@ -95,3 +96,32 @@ def test_codec_latent_rejects_bad_arguments_before_any_cuda_call():
     assert lib.s2_codec_latent(2, 64, 16, arr, 0, 16, 16, None, None) == pkg.S2_EINVAL   # no frame
     bad = (ctypes.c_void_p * 2)(16, 40)                                                  # unaligned quantizer
     assert lib.s2_codec_latent(2, 64, 16, bad, 4, 16, 16, None, None) == pkg.S2_EINVAL
+
+
+def test_quantize_e4m3_rejects_bad_arguments_before_any_cuda_call():
+    import dual_ar_tts_gb300 as pkg
+    lib = pkg.load()
+    assert lib.s2_quantize_e4m3(16, 0, 8, 32, 64, None) == pkg.S2_EINVAL    # no row
+    assert lib.s2_quantize_e4m3(16, 4, 0, 32, 64, None) == pkg.S2_EINVAL    # no column
+    assert lib.s2_quantize_e4m3(None, 4, 8, 32, 64, None) == pkg.S2_EINVAL  # no matrix
+    assert lib.s2_quantize_e4m3(17, 4, 8, 32, 64, None) == pkg.S2_EINVAL    # unaligned bf16 rows
+    assert lib.s2_quantize_e4m3(16, 4, 8, 32, 66, None) == pkg.S2_EINVAL    # unaligned scales
+
+
+def test_fp8_dims_are_checked():
+    import dual_ar_tts_gb300 as pkg
+    import synth
+    d = dict(synth.CONFIGS["tiny"]["dims"], weight_fp8=1)        # fp32 weights
+    assert pkg.s2_frame_workspace_bytes(pkg.make_dims(d), 1, 64) == 0
+    d = dict(synth.MINI, weight_fp8=1, ffn=576)                 # 576 is not a multiple of 128
+    assert pkg.s2_frame_workspace_bytes(pkg.make_dims(d), 1, 64) == 0
+    d = dict(synth.MINI, weight_fp8=2)
+    assert pkg.s2_frame_workspace_bytes(pkg.make_dims(d), 1, 64) == 0
+    d8 = dict(synth.MINI, weight_fp8=1)
+    a = pkg.s2_frame_workspace_bytes(pkg.make_dims(synth.MINI), 2, 64)
+    b = pkg.s2_frame_workspace_bytes(pkg.make_dims(d8), 2, 64)
+    # the e4m3 copies of the projections (1 byte per element + a 4-byte scale per row) are carved too
+    import oracle
+    host_shapes = [s for _, s, _ in synth.weight_specs(synth.MINI)]
+    q = sum(int(np.prod(host_shapes[i])) + 4 * host_shapes[i][0] for i in oracle.projection_indices(synth.MINI))
+    assert q <= b - a <= q + 256 * (2 * len(oracle.projection_indices(synth.MINI)) + 1)
