@@ -244,137 +244,150 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvCtasPerSm)
 
 // =========================================================================================
 // fp8 projection: the same partials from e4m3 weights Q with one fp32 scale per row,
-// part[...] = scale[row0 + m]·Σ_{k in split} Q[row0 + m][k]·a_c[k].  A stage carries 128 K (one
-// 128-byte fp8 row per weight row, 128-byte swizzle) and the planes of those 128 K (two 64-K
-// boxes).  The four epilogue warps, idle until the accumulator is ready, expand every fp8 tile to
-// bf16 in registers (thread = tile row = TMEM lane) and store it into one of two tensor-memory A
-// buffers; the MMA reads A from tensor memory and B from shared memory, so the expanded tile never
-// goes through shared memory.
+// part[...] = scale[row0 + m]·Σ_{k in split} Q[row0 + m][k]·a_c[k].  K advances 128 per step (one
+// 128-byte fp8 row per weight row, 128-byte swizzle).  Two rings: fp8 weight tiles, and the planes
+// of the same 128 K (two 64-K boxes).  Eight warps, idle until the accumulator is ready, expand
+// each fp8 tile to bf16 in registers (a thread owns one tile row = one TMEM lane, half of its 128
+// codes) and store it into one of the tensor-memory A buffers, from which the MMA reads A (B, the
+// planes, stays in shared memory).  A weight slot is refilled as soon as its tile has been read;
+// a planes slot and an A buffer once the MMAs that read them have completed.
 // =========================================================================================
 
-constexpr int kAtom8 = 128;                // K elements per fp8 stage
+constexpr int kAtom8 = 128;                // K elements per fp8 step
 constexpr int kA8Bytes = kTileM * kAtom8;  // one fp8 weight tile (16 KB)
+constexpr int kGemv8Threads = 320;         // 8 expanding / epilogue warps, a TMA warp, an MMA warp
+constexpr int kMaxTBufs = 4;               // tensor-memory A buffers at most
 
 struct Gemv8Bars {
-  uint64_t full[kMaxGemvStages], empty[kMaxGemvStages], afull[2], aempty[2], acc;
+  uint64_t wfull[kMaxGemvStages], wempty[kMaxGemvStages];  // fp8 weight tiles
+  uint64_t bfull[kMaxGemvStages], bempty[kMaxGemvStages];  // planes
+  uint64_t tfull[kMaxTBufs], tempty[kMaxTBufs];            // tensor-memory A buffers
+  uint64_t acc;
   uint32_t taddr;
 };
 
-// accumulator columns [0, acc) and the two A buffers of 64 columns after them
-__host__ __device__ constexpr uint32_t gemv8_acc_cols(int N) { return N <= 128 ? 128u : 256u; }
-__host__ __device__ constexpr uint32_t gemv8_tmem_cols(int N) { return N <= 128 ? 256u : 512u; }
+// tensor memory: accumulator columns [0, acc), then A buffers of 64 columns up to the allocation
+__host__ __device__ constexpr int gemv8_acc_cols(int N) { return N <= 64 ? 64 : (N <= 128 ? 128 : 256); }
+__host__ __device__ constexpr int gemv8_tmem_cols(int N) { return N <= 128 ? 256 : 512; }
+__host__ __device__ constexpr int gemv8_tbufs(int N) {
+  return (gemv8_tmem_cols(N) - gemv8_acc_cols(N)) / 64 < kMaxTBufs ? (gemv8_tmem_cols(N) - gemv8_acc_cols(N)) / 64
+                                                                    : kMaxTBufs;
+}
 
-__global__ void __launch_bounds__(kGemvThreads, kGemvCtasPerSm)
+__global__ void __launch_bounds__(kGemv8Threads, kGemvCtasPerSm)
     k_bgemv8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
              const __grid_constant__ CUtensorMap tmB, const float* scA, const float* scA2, int M, int row0, int N,
-             int NC, int atoms_total, int atoms_per, int nstages, float* part, Control* ctl) {
+             int NC, int atoms_total, int atoms_per, int nw, int nb, float* part, Control* ctl) {
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   const int bbytes = N * 128;  // planes of 64 K
-  const int sbytes = kA8Bytes + 2 * bbytes;
-  Gemv8Bars& S = *reinterpret_cast<Gemv8Bars*>(sm + nstages * sbytes);
+  unsigned char* smW = sm;
+  unsigned char* smB = sm + nw * kA8Bytes;
+  Gemv8Bars& S = *reinterpret_cast<Gemv8Bars*>(smB + nb * 2 * bbytes);
   const int tile = blockIdx.x, split = blockIdx.y, z = blockIdx.z, splits = gridDim.y;
   const int a0 = split * atoms_per, a1 = min(a0 + atoms_per, atoms_total);
   const int na = a1 - a0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const CUtensorMap* tA = z == 0 ? &tmA : &tmA2;
   const float* sc = z == 0 ? scA : scA2;
+  const int acc_cols = gemv8_acc_cols(N), ncols = gemv8_tmem_cols(N), nt = gemv8_tbufs(N);
   pdl_trigger();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < nstages; ++s) {
-      mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], 1 + 4);  // the MMA's commit and the four expanding warps
+    for (int s = 0; s < nw; ++s) {
+      mbar_init(&S.wfull[s], 1);
+      mbar_init(&S.wempty[s], 8);  // the eight expanding warps
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&S.afull[b], 4);
-      mbar_init(&S.aempty[b], 1);
+    for (int s = 0; s < nb; ++s) {
+      mbar_init(&S.bfull[s], 1);
+      mbar_init(&S.bempty[s], 1);  // the MMA's commit
+    }
+    for (int b = 0; b < nt; ++b) {
+      mbar_init(&S.tfull[b], 8);
+      mbar_init(&S.tempty[b], 1);
     }
     mbar_init(&S.acc, 1);
     fence_barrier_init();
   }
-  const uint32_t acc_cols = gemv8_acc_cols(N), ncols = gemv8_tmem_cols(N);
   if (warp == 0) {
-    tmem_alloc(&S.taddr, ncols);
+    tmem_alloc(&S.taddr, static_cast<uint32_t>(ncols));
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tacc = S.taddr;
-  if (warp == 4) {
+  if (warp == 8) {
     if (lane == 0) {
+      // weight tiles: independent of earlier kernels, requested without waiting for them
       prefetch_tmap(tA);
-      prefetch_tmap(&tmB);
       const uint64_t pol = policy_evict_first();
-      const int pre = min(nstages, na);
-      for (int i = 0; i < pre; ++i) {
-        mbar_arrive_expect_tx(&S.full[i], sbytes);
-        tma_load_2d(sm + i * sbytes, tA, (a0 + i) * kAtom8, row0 + tile * kTileM, &S.full[i], pol);
+      for (int i = 0; i < na; ++i) {
+        const int s = i % nw;
+        if (i >= nw && !wait_bar(&S.wempty[s], ((i / nw) & 1) ^ 1, ctl)) break;
+        mbar_arrive_expect_tx(&S.wfull[s], kA8Bytes);
+        tma_load_2d(smW + s * kA8Bytes, tA, (a0 + i) * kAtom8, row0 + tile * kTileM, &S.wfull[s], pol);
       }
+    } else if (lane == 1) {
+      // planes: produced by the previous kernel; shared by every row tile of this split
+      prefetch_tmap(&tmB);
+      const uint64_t pol = policy_evict_last();
       pdl_wait();
-      for (int i = 0; i < pre; ++i) {
-        unsigned char* Bs = sm + i * sbytes + kA8Bytes;
-        tma_load_2d(Bs, &tmB, (a0 + i) * kAtom8, 0, &S.full[i], pol);
-        tma_load_2d(Bs + bbytes, &tmB, (a0 + i) * kAtom8 + kAtom, 0, &S.full[i], pol);
-      }
-      for (int i = pre; i < na; ++i) {
-        const int s = i % nstages;
-        if (!wait_bar(&S.empty[s], ((i / nstages) & 1) ^ 1, ctl)) break;
-        unsigned char* A = sm + s * sbytes;
-        mbar_arrive_expect_tx(&S.full[s], sbytes);
-        tma_load_2d(A, tA, (a0 + i) * kAtom8, row0 + tile * kTileM, &S.full[s], pol);
-        tma_load_2d(A + kA8Bytes, &tmB, (a0 + i) * kAtom8, 0, &S.full[s], pol);
-        tma_load_2d(A + kA8Bytes + bbytes, &tmB, (a0 + i) * kAtom8 + kAtom, 0, &S.full[s], pol);
+      for (int i = 0; i < na; ++i) {
+        const int s = i % nb;
+        if (i >= nb && !wait_bar(&S.bempty[s], ((i / nb) & 1) ^ 1, ctl)) break;
+        unsigned char* Bs = smB + s * 2 * bbytes;
+        mbar_arrive_expect_tx(&S.bfull[s], 2 * bbytes);
+        tma_load_2d(Bs, &tmB, (a0 + i) * kAtom8, 0, &S.bfull[s], pol);
+        tma_load_2d(Bs + bbytes, &tmB, (a0 + i) * kAtom8 + kAtom, 0, &S.bfull[s], pol);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(kTileM, N);
       for (int i = 0; i < na; ++i) {
-        const int s = i % nstages, b = i & 1;
-        if (!wait_bar(&S.afull[b], (i >> 1) & 1, ctl)) break;
-        if (!wait_bar(&S.full[s], (i / nstages) & 1, ctl)) break;
+        const int s = i % nb, b = i % nt;
+        if (!wait_bar(&S.tfull[b], (i / nt) & 1, ctl)) break;
+        if (!wait_bar(&S.bfull[s], (i / nb) & 1, ctl)) break;
         tc_fence_after();
-        const uint32_t B = smem_u32(sm + s * sbytes + kA8Bytes);
-        const uint32_t abuf = tacc + acc_cols + static_cast<uint32_t>(b) * 64u;
+        const uint32_t B = smem_u32(smB + s * 2 * bbytes);
+        const uint32_t abuf = tacc + static_cast<uint32_t>(acc_cols + b * 64);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           tc_mma_tmem_a(tacc, abuf + kk * 8, desc_sw128(B + (kk >> 2) * bbytes + (kk & 3) * 32), idesc,
                         (i > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&S.empty[s]);
-        tc_commit(&S.aempty[b]);
+        tc_commit(&S.bempty[s]);
+        tc_commit(&S.tempty[b]);
       }
       tc_commit(&S.acc);
     }
   } else {
-    const int r = warp * 32 + lane;  // tile row = TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    // warps 0..7: warp w expands half h = w / 4 (codes 64h .. 64h + 63) of tile rows 32q .. 32q + 31,
+    // q = w % 4 (the TMEM lane quarter this warp may access)
+    const int q = warp & 3, h = warp >> 2;
+    const int r = q * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     for (int i = 0; i < na; ++i) {
-      const int s = i % nstages, b = i & 1;
-      if (!__all_sync(0xffffffffu, wait_bar(&S.full[s], (i / nstages) & 1, ctl))) break;
-      if (!__all_sync(0xffffffffu, wait_bar(&S.aempty[b], ((i >> 1) & 1) ^ 1, ctl))) break;
+      const int s = i % nw, b = i % nt;
+      if (!__all_sync(0xffffffffu, wait_bar(&S.wfull[s], (i / nw) & 1, ctl))) break;
+      if (!__all_sync(0xffffffffu, wait_bar(&S.tempty[b], ((i / nt) & 1) ^ 1, ctl))) break;
       tc_fence_after();
-      const unsigned char* rowp = sm + s * sbytes + r * 128;
+      const unsigned char* rowp = smW + s * kA8Bytes + r * 128;
+      uint32_t o[32];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t o[32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int chunk = h * 4 + c;  // K elements 16·chunk .. 16·chunk + 15
-          const uint4 w = *reinterpret_cast<const uint4*>(rowp + ((chunk ^ (r & 7)) << 4));
-          e4m3x4_to_bf16x4(w.x, o[c * 8 + 0], o[c * 8 + 1]);
-          e4m3x4_to_bf16x4(w.y, o[c * 8 + 2], o[c * 8 + 3]);
-          e4m3x4_to_bf16x4(w.z, o[c * 8 + 4], o[c * 8 + 5]);
-          e4m3x4_to_bf16x4(w.w, o[c * 8 + 6], o[c * 8 + 7]);
-        }
-        tmem_st32(tacc + lane_off + acc_cols + static_cast<uint32_t>(b) * 64u + h * 32, o);
+      for (int c = 0; c < 4; ++c) {
+        const int chunk = h * 4 + c;  // K elements 16·chunk .. 16·chunk + 15
+        const uint4 w = *reinterpret_cast<const uint4*>(rowp + ((chunk ^ (r & 7)) << 4));
+        e4m3x4_to_bf16x4(w.x, o[c * 8 + 0], o[c * 8 + 1]);
+        e4m3x4_to_bf16x4(w.y, o[c * 8 + 2], o[c * 8 + 3]);
+        e4m3x4_to_bf16x4(w.z, o[c * 8 + 4], o[c * 8 + 5]);
+        e4m3x4_to_bf16x4(w.w, o[c * 8 + 6], o[c * 8 + 7]);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.wempty[s]);  // the weight slot's codes are in registers
+      tmem_st32(tacc + lane_off + static_cast<uint32_t>(acc_cols + b * 64 + h * 32), o);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&S.afull[b]);
-        mbar_arrive(&S.empty[s]);
-      }
+      if (lane == 0) mbar_arrive(&S.tfull[b]);
     }
     const bool ok = __all_sync(0xffffffffu, wait_bar(&S.acc, 0, ctl));
     pdl_wait();  // the partials buffer may still be read by the previous grid until it completes
@@ -383,7 +396,7 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvCtasPerSm)
       const int row = tile * kTileM + r;
       const float scale = row < M ? __ldg(sc + row0 + row) : 0.f;
       float* out = part + (static_cast<size_t>(z) * splits + split) * NC * M;
-      for (int c0 = 0; c0 < N; c0 += 16) {
+      for (int c0 = h * 16; c0 < N; c0 += 32) {
         float v[16];
         tmem_ld16(tacc + lane_off + c0, v);
 #pragma unroll
@@ -396,9 +409,10 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvCtasPerSm)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tacc, ncols);
+  if (warp == 0) tmem_dealloc(tacc, static_cast<uint32_t>(ncols));
 }
 
+// =========================================================================================
 // e4m3 quantisation of bf16 rows: scale = max|w| / 448 (fp32 division), code = w / scale rounded
 // to the nearest e4m3 value, ties to even, saturating at ±448; an all-zero row gets scale 0 and
 // zero codes.  One CTA per row (grid-stride).
@@ -1589,10 +1603,14 @@ bool encode_map8(CUtensorMap* m, const void* base, int K, long long rows) {
 // fp8 projection launch shape: stages that fit the shared-memory budget (two CTAs per SM up to
 // 128 MMA columns; wider tiles take one SM each, which also leaves their 512 TMEM columns alone)
 constexpr int kGemv8WideBudget = 200 * 1024;
-int gemv8_smem(int N, int* nst) {
-  const int sbytes = kA8Bytes + N * 256;
-  *nst = std::min(kMaxGemvStages, (N <= 128 ? kGemvSmemBudget : kGemv8WideBudget) / sbytes);
-  return std::max(kGemvSmemFloor, *nst * sbytes + 1024 + static_cast<int>(sizeof(Gemv8Bars)));
+// weight-tile and planes stages that fit the budget (two CTAs per SM up to 128 MMA columns; wider
+// tiles take one SM each, which also leaves their 512 TMEM columns alone)
+int gemv8_smem(int N, int* nw, int* nb) {
+  const int bstage = N * 256;
+  const int budget = N <= 128 ? kGemvSmemBudget : kGemv8WideBudget;
+  *nb = bstage < 16 * 1024 ? 3 : 2;
+  *nw = std::min(kMaxGemvStages, (budget - *nb * bstage) / kA8Bytes);
+  return std::max(kGemvSmemFloor, *nw * kA8Bytes + *nb * bstage + 1024 + static_cast<int>(sizeof(Gemv8Bars)));
 }
 
 
@@ -1747,11 +1765,11 @@ int batch_prefill_proj(Batch* b, const void* w0, const void* w1, int M, int K, c
     auto qb = b->qmaps.find(w1 ? w1 : w0);
     if (qb == b->qmaps.end() || K % kAtom8 != 0) return -1;
     const GemvPlan g = plan_gemv(M, K, w1 ? 2 : 1, kGemvCtasPerSm * b->m.sms, false, 1 << 30, kAtom8);
-    int nst = 0;
-    const int smem = gemv8_smem(N, &nst);
+    int nw = 0, nb = 0;
+    const int smem = gemv8_smem(N, &nw, &nb);
     dim3 grid(g.tiles, g.splits, g.nmat);
-    k_bgemv8<<<grid, kGemvThreads, smem, static_cast<cudaStream_t>(stream)>>>(
-        qa->second.map, qb->second.map, it->second, qa->second.s, qb->second.s, M, 0, N, NC, g.atoms, g.per, nst,
+    k_bgemv8<<<grid, kGemv8Threads, smem, static_cast<cudaStream_t>(stream)>>>(
+        qa->second.map, qb->second.map, it->second, qa->second.s, qb->second.s, M, 0, N, NC, g.atoms, g.per, nw, nb,
         part, b->m.ctl);
     return cudaGetLastError() == cudaSuccess ? g.splits : -1;
   }
@@ -1864,10 +1882,10 @@ struct Frame {
       const GemvPlan g = plan_gemv(M, K, w1 ? 2 : 1, kGemvCtasPerSm * b->m.sms, whole_k, max_splits, kAtom8);
       const int N = round16(2 * NC);
       const CUtensorMap& tb = planes(pl, N, K, ld);
-      int nst = 0;
-      const int smem = gemv8_smem(N, &nst);
+      int nw = 0, nb = 0;
+      const int smem = gemv8_smem(N, &nw, &nb);
       dim3 grid(g.tiles, g.splits, g.nmat);
-      launch(k_bgemv8, grid, kGemvThreads, smem, qa.map, qb.map, tb, qa.s, qb.s, M, row0, N, NC, g.atoms, g.per, nst,
+      launch(k_bgemv8, grid, kGemv8Threads, smem, qa.map, qb.map, tb, qa.s, qb.s, M, row0, N, NC, g.atoms, g.per, nw, nb,
              e.part, e.ctl);
       return g;
     }
