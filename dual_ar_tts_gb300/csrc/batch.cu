@@ -243,12 +243,10 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvCtasPerSm)
 }
 
 // =========================================================================================
-// fp8 projection (W8A16): the same partials from e4m3 weights Q with one fp32 scale per row and
-// the activations rounded to bf16 (the hi planes alone),
-// part[...] = scale[row0 + m]·Σ_{k in split} Q[row0 + m][k]·bf16(a_c[k]).  The MMA's N is the
-// column count rounded up to 16 (planes rows beyond the columns read as zeros).  K advances 128
-// per step (one 128-byte fp8 row per weight row, 128-byte swizzle).  Two rings: fp8 weight tiles,
-// and the hi planes of the same 128 K (two 64-K boxes).  Eight warps, idle until the accumulator is ready, expand
+// fp8 projection: the same partials from e4m3 weights Q with one fp32 scale per row,
+// part[...] = scale[row0 + m]·Σ_{k in split} Q[row0 + m][k]·a_c[k].  K advances 128 per step (one
+// 128-byte fp8 row per weight row, 128-byte swizzle).  Two rings: fp8 weight tiles, and the planes
+// of the same 128 K (two 64-K boxes).  Eight warps, idle until the accumulator is ready, expand
 // each fp8 tile to bf16 in registers (a thread owns one tile row = one TMEM lane, half of its 128
 // codes) and store it into one of the tensor-memory A buffers, from which the MMA reads A (B, the
 // planes, stays in shared memory).  A weight slot is refilled as soon as its tile has been read;
@@ -402,9 +400,9 @@ __global__ void __launch_bounds__(kGemv8Threads, kGemvCtasPerSm)
         float v[16];
         tmem_ld16(tacc + lane_off + c0, v);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int c = c0 + j;
-          if (c < NC && row < M) out[static_cast<size_t>(c) * M + row] = v[j] * scale;
+        for (int j = 0; j < 8; ++j) {
+          const int c = c0 / 2 + j;
+          if (c < NC && row < M) out[static_cast<size_t>(c) * M + row] = (v[2 * j] + v[2 * j + 1]) * scale;
         }
       }
     }
@@ -1604,13 +1602,12 @@ bool encode_map8(CUtensorMap* m, const void* base, int K, long long rows) {
 
 // fp8 projection launch shape: stages that fit the shared-memory budget (two CTAs per SM up to
 // 128 MMA columns; wider tiles take one SM each, which also leaves their 512 TMEM columns alone)
-constexpr int kGemv8Budget = 108 * 1024;  // two CTAs per SM
 constexpr int kGemv8WideBudget = 200 * 1024;
 // weight-tile and planes stages that fit the budget (two CTAs per SM up to 128 MMA columns; wider
 // tiles take one SM each, which also leaves their 512 TMEM columns alone)
 int gemv8_smem(int N, int* nw, int* nb) {
   const int bstage = N * 256;
-  const int budget = N <= 128 ? kGemv8Budget : kGemv8WideBudget;
+  const int budget = N <= 128 ? kGemvSmemBudget : kGemv8WideBudget;
   *nb = bstage < 16 * 1024 ? 3 : 2;
   *nw = std::min(kMaxGemvStages, (budget - *nb * bstage) / kA8Bytes);
   return std::max(kGemvSmemFloor, *nw * kA8Bytes + *nb * bstage + 1024 + static_cast<int>(sizeof(Gemv8Bars)));
@@ -1628,7 +1625,6 @@ struct Batch {
   BatchModel m;
   std::map<const void*, CUtensorMap> wmaps;
   std::map<const void*, QEntry> qmaps;  // bf16 weight -> its e4m3 copy (fp8 weight streaming)
-  std::map<std::tuple<const void*, int, int>, CUtensorMap> hmaps;  // hi planes alone (fp8 projections)
   std::map<std::tuple<const void*, int, int>, CUtensorMap> pmaps;
   BatchSizes sz{};
   std::vector<BStream> host_bs;
@@ -1753,18 +1749,6 @@ Batch* batch_create(const BatchModel& m, std::string* err) {
   return b;
 }
 
-// planes map of the hi rows alone (rows 2c, c < NC; box of round16(NC) rows, the rest zeros), cached
-static const CUtensorMap* hi_planes_map(Batch* b, const void* planes, int NC, int K, int ld) {
-  auto key = std::make_tuple(planes, NC, K);
-  auto it = b->hmaps.find(key);
-  if (it == b->hmaps.end()) {
-    CUtensorMap t;
-    if (!encode_map(&t, planes, K, NC, 2 * ld, round16(NC))) return nullptr;
-    it = b->hmaps.emplace(key, t).first;
-  }
-  return &it->second;
-}
-
 int batch_prefill_proj(Batch* b, const void* w0, const void* w1, int M, int K, const uint16_t* planes, int ld, int NC,
                        float* part, void* stream) {
   if (NC < 1 || NC > kPrefillCols || K % kAtom != 0) return -1;
@@ -1781,14 +1765,11 @@ int batch_prefill_proj(Batch* b, const void* w0, const void* w1, int M, int K, c
     auto qb = b->qmaps.find(w1 ? w1 : w0);
     if (qb == b->qmaps.end() || K % kAtom8 != 0) return -1;
     const GemvPlan g = plan_gemv(M, K, w1 ? 2 : 1, kGemvCtasPerSm * b->m.sms, false, 1 << 30, kAtom8);
-    const int N8 = round16(NC);
-    const CUtensorMap* th = hi_planes_map(b, planes, NC, K, ld);
-    if (!th) return -1;
     int nw = 0, nb = 0;
-    const int smem = gemv8_smem(N8, &nw, &nb);
+    const int smem = gemv8_smem(N, &nw, &nb);
     dim3 grid(g.tiles, g.splits, g.nmat);
     k_bgemv8<<<grid, kGemv8Threads, smem, static_cast<cudaStream_t>(stream)>>>(
-        qa->second.map, qb->second.map, *th, qa->second.s, qb->second.s, M, 0, N8, NC, g.atoms, g.per, nw, nb,
+        qa->second.map, qb->second.map, it->second, qa->second.s, qb->second.s, M, 0, N, NC, g.atoms, g.per, nw, nb,
         part, b->m.ctl);
     return cudaGetLastError() == cudaSuccess ? g.splits : -1;
   }
@@ -1899,17 +1880,13 @@ struct Frame {
       const QEntry& qa = q0->second;
       const QEntry& qb = w1 ? b->qmaps.at(w1) : qa;
       const GemvPlan g = plan_gemv(M, K, w1 ? 2 : 1, kGemvCtasPerSm * b->m.sms, whole_k, max_splits, kAtom8);
-      const int N8 = round16(NC);
-      const CUtensorMap* th = hi_planes_map(b, pl, NC, K, ld);
-      if (!th) {
-        ok = false;
-        return g;
-      }
+      const int N = round16(2 * NC);
+      const CUtensorMap& tb = planes(pl, N, K, ld);
       int nw = 0, nb = 0;
-      const int smem = gemv8_smem(N8, &nw, &nb);
+      const int smem = gemv8_smem(N, &nw, &nb);
       dim3 grid(g.tiles, g.splits, g.nmat);
-      launch(k_bgemv8, grid, kGemv8Threads, smem, qa.map, qb.map, *th, qa.s, qb.s, M, row0, N8, NC, g.atoms, g.per, nw,
-             nb, e.part, e.ctl);
+      launch(k_bgemv8, grid, kGemv8Threads, smem, qa.map, qb.map, tb, qa.s, qb.s, M, row0, N, NC, g.atoms, g.per, nw, nb,
+             e.part, e.ctl);
       return g;
     }
     const GemvPlan g = plan_gemv(M, K, w1 ? 2 : 1, kGemvCtasPerSm * b->m.sms, whole_k, max_splits);

@@ -73,11 +73,8 @@ typedef struct s2_dims {
                            fast_project_in, fast_output) as fp8 e4m3 with one fp32 scale per row
                            (scale = max|row| / 448, round to nearest even, saturating), quantised by
                            s2_frame_init into the workspace from the bf16 weights; embeddings, norms
-                           and the tied logits stay bf16.  Such a projection multiplies the input
-                           rounded to bf16 (nearest even) by the e4m3 weights, fp32 sums (W8A16).
-                           bf16 weights only, projection lengths multiples of 128, shapes the
-                           batched decode supports (every decode, n = 1 included, runs there;
-                           s2_fast_logits is not available).  0: stream bf16. */
+                           and the tied logits stay bf16.  bf16 weights only, projection lengths
+                           multiples of 128.  0: stream bf16. */
 } s2_dims;
 
 /* Sampler settings of one stream ([ch.06 §5.3, §6]; Mizuoto "Fish Speech" engine page:
@@ -273,8 +270,8 @@ int s2_codec_latent(int n_codebooks, int codebook_size, int dim, const void* con
  *   codes[r][k] = e4m3(w[r][k] / scales[r])    (fp32 division; round to nearest, ties to even,
  *                                               saturating at ±448; never a NaN code)
  * and an all-zero row gets scale 0 and zero codes.  e4m3 = sign, 4 exponent bits (bias 7), 3
- * mantissa bits, exponent field 0 = subnormals m·2^-9.  The decode then computes
- * y[r] = scales[r]·Σ_k value(codes[r][k])·bf16(x[k]) in place of Σ_k w[r][k]·x[k].
+ * mantissa bits, exponent field 0 = subnormals m·2^-9.  The decode then uses
+ * scales[r]·value(codes[r][k]) in place of w[r][k].
  *   w       device bf16 [rows][cols], 2-byte aligned
  *   codes   device uint8 [rows][cols]
  *   scales  device fp32 [rows], 4-byte aligned

@@ -87,7 +87,6 @@ def _load():
                 "or_e4m3_encode": (i32, [f32]),
                 "or_quant_e4m3": (None, [vp, ctypes.c_longlong, i32, vp, vp]),
                 "or_bind_e4m3": (i32, [vp, i32, vp, vp, i32]),
-                "or_linear_e4m3": (None, [vp, vp, i32, i32, vp, i32, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -173,17 +172,6 @@ def quant_e4m3(w_bf16):
     scales = np.empty(rows, np.float32)
     _load().or_quant_e4m3(w.ctypes.data, rows, cols, codes.ctypes.data, scales.ctypes.data)
     return codes, scales
-
-
-def linear_e4m3(codes, scales, x):
-    """y[t] = (scale * e4m3(codes)) @ bf16(x[t]) for the rows x[t] of x (W8A16, fp32 sums)."""
-    c = np.ascontiguousarray(codes, np.uint8)
-    s = _f32(scales)
-    xv = _f32(x)
-    n = 1 if xv.ndim == 1 else xv.shape[0]
-    y = np.empty((n, c.shape[0]), np.float32)
-    _load().or_linear_e4m3(c.ctypes.data, s.ctypes.data, c.shape[0], c.shape[1], xv.ctypes.data, n, y.ctypes.data)
-    return y[0] if xv.ndim == 1 else y
 
 
 def projection_indices(d: dict):

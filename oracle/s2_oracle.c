@@ -219,21 +219,8 @@ void or_attention(const float* q, const float* K, const float* V, int Hq, int Hk
   free(map);
 }
 
-/* y[t][r] = Σ_k W[r][k]·x[t][k] for t < n, summed in k order (one GEMV per position).
- * An e4m3 matrix multiplies bf16 activations (W8A16): its input is rounded to bf16 first. */
-static void linear_in(wref W, int M, int K, const float* x, int n, float* y);
+/* y[t][r] = Σ_k W[r][k]·x[t][k] for t < n, summed in k order (one GEMV per position). */
 static void linear(wref W, int M, int K, const float* x, int n, float* y) {
-  if (!W.rs) {
-    linear_in(W, M, K, x, n, y);
-    return;
-  }
-  float* xb = (float*)malloc(sizeof(float) * (size_t)K * n);
-  for (size_t i = 0; i < (size_t)K * n; ++i) xb[i] = f32_to_bf16_value(x[i]);
-  linear_in(W, M, K, xb, n, y);
-  free(xb);
-}
-
-static void linear_in(wref W, int M, int K, const float* x, int n, float* y) {
   if (n == 1) {
 #pragma omp parallel for schedule(static)
     for (int r = 0; r < M; ++r) {
@@ -694,12 +681,4 @@ int or_bind_e4m3(or_sess* s, int i, const uint8_t* codes, const float* scales, i
   w->rs = scales;
   w->cols = cols;
   return 0;
-}
-
-/* y[t][r] = Σ_k scale[r]·e4m3(codes[r][k])·bf16(x[t][k]): one e4m3 projection as the sessions
- * apply it */
-void or_linear_e4m3(const uint8_t* codes, const float* scales, int M, int K, const float* x, int n, float* y) {
-  for (int c = 0; c < 256; ++c) g_e4m3[c] = or_e4m3_value(c);
-  wref w = {codes, 0, scales, K};
-  linear(w, M, K, x, n, y);
 }

@@ -11,11 +11,8 @@ nearest with ties to the even mantissa and saturates at 448, with one fp32 scale
   random values and on the exact midpoints between neighbours;
 * closed-form cases: ties at 1, in the subnormal range and at the top; saturation;
 * the quantiser's invariants (the largest element of a row maps to +-448 exactly, the error is
-  within half a step, zero rows);
-* an e4m3 projection multiplies bf16-rounded activations (W8A16) with fp32 sums: against numpy
-  fp64 with the rounding written out here as bit arithmetic;
-* the binding: a session reading e4m3 codes stays close to one given the dequantised fp32 matrices
-  (they differ by the input rounding alone) and far from the bf16 model.
+  within half a step, zero rows) and the binding: a session reading e4m3 codes gives the same
+  numbers as one given the dequantised fp32 matrices.
 """
 import numpy as np
 import pytest
@@ -121,33 +118,7 @@ def test_quantiser_invariants():
     assert codes[4, 17] == 0xFE and np.count_nonzero(codes[4]) == 1
 
 
-def _bf16_round(x):
-    """fp32 -> nearest bf16 value (ties to even), by bit arithmetic."""
-    u = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)
-    u = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
-    return u.astype(np.uint32).view(np.float32)
-
-
-def test_e4m3_projection_is_w8a16():
-    # y = (scale * e4m3(codes)) @ bf16(x), fp32 sums: against numpy fp64 on the rounded input
-    rng = np.random.default_rng(8)
-    M, K, n = 40, 384, 3
-    codes = rng.integers(0, 256, (M, K)).astype(np.uint8)
-    codes[(codes & 0x7F) == 0x7F] = 0x11  # no NaN codes
-    scales = rng.uniform(1e-4, 1e-2, M).astype(np.float32)
-    x = rng.normal(0, 1, (n, K)).astype(np.float32)
-    y = oracle.linear_e4m3(codes, scales, x)
-    table = np.array([oracle.e4m3_value(c) for c in range(256)])
-    deq = table[codes] * scales.astype(np.float64)[:, None]
-    ref = _bf16_round(x).astype(np.float64) @ deq.T
-    raw = x.astype(np.float64) @ deq.T
-    bound = (np.abs(_bf16_round(x)).astype(np.float64) @ np.abs(deq).T) * K * 2.0 ** -24
-    assert np.all(np.abs(y - ref) <= bound + 1e-30)
-    # the rounding of the input is in effect: the unrounded product is further away than that
-    assert np.max(np.abs(y - raw) - bound) > 0
-
-
-def test_session_binds_the_codes_of_every_projection():
+def test_session_reading_codes_equals_dequantised_fp32_weights():
     d = synth.MINI
     host = synth.make_weights(d, 3, norm_jitter=0.1)
     quant = oracle.quantize_projections(d, host)
@@ -164,16 +135,14 @@ def test_session_binds_the_codes_of_every_projection():
             deq.append((w.astype(np.uint32) << 16).view(np.float32))
     prompt = synth.make_prompt(d, 3, 0, 12, 4)
     a = oracle.Session(d, host, 32, quant=quant)
-    b = oracle.Session(dict(d, weight_dtype=synth.F32), deq, 32)   # same weights, fp32 inputs
-    c = oracle.Session(d, host, 32)                                 # the bf16 model
+    b = oracle.Session(dict(d, weight_dtype=synth.F32), deq, 32)
     la, ha = a.prefill(prompt)
     lb, hb = b.prefill(prompt)
+    assert np.array_equal(la, lb) and np.array_equal(ha, hb)
+    # and the e4m3 model is a different model from the bf16 one (the codes are in use)
+    c = oracle.Session(d, host, 32)
     lc, _ = c.prefill(prompt)
-    # a and b differ only by the bf16 rounding of the projection inputs: close, not equal
-    assert not np.array_equal(la, lb)
-    assert np.max(np.abs(la - lb)) < 2e-2 * np.max(np.abs(lb))
-    assert np.max(np.abs(ha - hb)) < 2e-2 * np.max(np.abs(hb))
-    # a code bound to the wrong entry, or left unbound, would move the logits by far more
-    assert np.max(np.abs(la - lc)) > 4 * np.max(np.abs(la - lb))
-    for sess in (a, b, c):
-        sess.close()
+    assert not np.array_equal(la, lc)
+    assert np.max(np.abs(la - lc)) < 0.1 * np.max(np.abs(lc))
+    for s in (a, b, c):
+        s.close()
