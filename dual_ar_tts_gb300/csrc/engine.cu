@@ -309,14 +309,6 @@ void carve(s2_ctx* c, Carver& cv) {
 
 // ------------------------------------------------------------ phase builders
 
-// the e4m3 copy of a bf16 projection matrix (fp8 weight streaming), or null
-const QuantW* find_quant(const s2_ctx* c, const void* w) {
-  if (!w) return nullptr;
-  for (const QuantW& q : c->qw)
-    if (q.w == w) return &q;
-  return nullptr;
-}
-
 struct Builder {
   s2_ctx* c;
   std::vector<Phase>* out;
@@ -333,16 +325,6 @@ struct Builder {
     p.epi = epi;
     p.w[0] = w0;
     p.w[1] = w1;
-    if (d.fp8) {
-      // projections stream their e4m3 copies
-      for (int m = 0; m < p.nmat; ++m) {
-        const QuantW* q = find_quant(c, p.w[m]);
-        if (!q && m == 1) err = "internal: a gate partner without its e4m3 copy";
-        if (!q) break;
-        p.w[m] = q->q;
-        p.wscale[m] = q->s;
-      }
-    }
     p.normw = normw;
     const int epc = 16 / d.esz;
     const int nchunk = K / epc;
@@ -875,7 +857,7 @@ int s2_decode_frames(s2_ctx* c, int n, const int* ids, int n_frames, const s2_sa
     for (int j = 0; j < k; ++j)
       if (ids[j] == sid) return fail(c, S2_EINVAL, "a stream appears twice");
   }
-  if (c->batch && n >= 2) {
+  if (c->batch && (n >= 2 || d.fp8)) {
     int max_ctx = 0;
     for (int k = 0; k < n; ++k) max_ctx = std::max(max_ctx, c->host_pos[ids[k]] + n_frames);
     std::string why;

@@ -23,7 +23,6 @@
 #include <type_traits>
 
 #include "ptx.cuh"
-#include "tc05.cuh"
 #include "s2_internal.h"
 #include "sampler.cuh"
 
@@ -214,13 +213,12 @@ __device__ __noinline__ void drain_copies(const CallParams& cp, uint64_t* bar, u
 // producer
 // =========================================================================
 
-// K split of an 8-row (or shorter) tile of bf16 (eb = 2) or e4m3 (eb = 1) weights: the fewest K
-// tiles such that `rows` padded row segments fit one stage (Kt a multiple of 16 dividing K).
-// Producer and consumers agree on it.
-__device__ __forceinline__ int tile_kt(int K, int rows, int eb = 2) {
+// K split of an 8-row (or shorter) bf16 tile: the fewest K tiles such that `rows` padded row
+// segments fit one stage (Kt a multiple of 16 dividing K).  Producer and consumers agree on it.
+__device__ __forceinline__ int tile_kt(int K, int rows) {
   for (int n = 1; n <= K / 16; ++n) {
     if (K % n != 0 || (K / n) % 16 != 0) continue;
-    if (rows * ((K / n) * eb + kTileRowPad) <= kStageBytes) return K / n;
+    if (rows * ((K / n) * 2 + kTileRowPad) <= kStageBytes) return K / n;
   }
   return 16;
 }
@@ -271,20 +269,17 @@ __device__ void producer(const CallParams& cp, Smem& S) {
           }
         }
         if constexpr (C::bf16) {
-          // bf16 (or e4m3 codes): tiles of <= 8 rows x Kt columns, row segments padded by 16 bytes,
-          // one lane per row
-          const int eb = ph.wscale[0] != nullptr ? 1 : 2;
-          const uint32_t wrow = static_cast<uint32_t>(ph.K) * eb;
+          // bf16: tiles of <= 8 rows x Kt columns, row segments padded by 16 bytes, one lane per row
           for (int b = 0; b < nr && !stop; b += kTileRows) {
             const int rows = min(kTileRows, nr - b);
-            const int Kt = tile_kt(ph.K, rows, eb), nkt = ph.K / Kt;
-            const uint32_t segb = static_cast<uint32_t>(Kt) * eb, pitch = segb + kTileRowPad;
+            const int Kt = tile_kt(ph.K, rows), nkt = ph.K / Kt;
+            const uint32_t segb = static_cast<uint32_t>(Kt) * 2u, pitch = segb + kTileRowPad;
             const int row = r0 + b + lane;
             for (int m = 0; m < ph.nmat && !stop; ++m) {
               const unsigned char* rsrc =
                   (ph.last_row != nullptr && row == ph.M - 1)
                       ? static_cast<const unsigned char*>(ph.last_row)
-                      : static_cast<const unsigned char*>(ph.w[m]) + static_cast<size_t>(row) * wrow;
+                      : static_cast<const unsigned char*>(ph.w[m]) + static_cast<size_t>(row) * rowb;
               for (int kt = 0; kt < nkt; ++kt) {
                 if (!producer_acquire(cp, S, pp, segb * rows)) {
                   stop = 1;
@@ -628,42 +623,6 @@ __device__ __forceinline__ void tile_steps(uint32_t tb, uint32_t b_off, uint32_t
   }
 }
 
-// e4m3 weights (fp8 streaming): the same k steps, with each B fragment (weight row g = lane / 4,
-// k = 2t, 2t+1 and 2t+8, 2t+9 of the step, t = lane % 4) expanded exactly to bf16 from two 16-bit
-// shared loads of its codes; `bb` addresses the lane's row at k = 2t of step 0.
-__device__ __forceinline__ uint32_t lds16(uint32_t a) {
-  uint16_t v;
-  asm("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
-  return v;
-}
-
-__device__ __forceinline__ void tile_steps8(uint32_t bb, uint32_t a_ld, uint32_t a_ld0, uint32_t ak, int warp,
-                                            int nsteps, bool a_live, float (&acc0)[4], float (&acc1)[4],
-                                            float (&acc2)[4], float (&acc3)[4]) {
-  int i = 0;
-#pragma unroll 2
-  for (int st = warp; st < nsteps; st += 2 * kConsumerWarps, ++i) {
-    const bool two = st + kConsumerWarps < nsteps;
-    const uint32_t p = bb + 16u * static_cast<uint32_t>(st);
-    uint32_t b0, b1, b2 = 0u, b3 = 0u, a0, a2, c0 = 0u, c2 = 0u;
-    e4m3x4_to_bf16x4(lds16(p) | (lds16(p + 8u) << 16), b0, b1);
-    if (two) {
-      e4m3x4_to_bf16x4(lds16(p + 128u) | (lds16(p + 136u) << 16), b2, b3);
-      ldmatrix_x4(a_ld + ak + 32u * st, a0, a2, c0, c2);
-    } else {
-      ldmatrix_x2(a_ld0 + ak + 32u * st, a0, a2);
-    }
-    if (!a_live) a0 = a2 = c0 = c2 = 0u;
-    if (i & 1) {
-      mma_bf16_16816(acc2, a0, 0u, a2, 0u, b0, b1);
-      if (two) mma_bf16_16816(acc3, c0, 0u, c2, 0u, b2, b3);
-    } else {
-      mma_bf16_16816(acc0, a0, 0u, a2, 0u, b0, b1);
-      if (two) mma_bf16_16816(acc1, c0, 0u, c2, 0u, b2, b3);
-    }
-  }
-}
-
 template <int NC>
 __device__ __noinline__ void gemv_tiles(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe, float yres);
 
@@ -847,14 +806,11 @@ __device__ __noinline__ void gemv_tiles(const CallParams& cp, const Phase& ph, S
   // a block of 8 rows has at most kIters iterations per warp; shorter blocks can have longer K
   // tiles, which the outer loop covers
   constexpr int kIters = ((kStageBytes / kTileRows - kTileRowPad) / 32 + 2 * kConsumerWarps - 1) / (2 * kConsumerWarps);
-  const bool w8 = ph.wscale[0] != nullptr;  // e4m3 codes with row scales
-  const int eb = w8 ? 1 : 2;
   for (int b = 0; b < nr; b += kTileRows) {
     const int rows = min(kTileRows, nr - b);
-    const int Kt = tile_kt(K, rows, eb), nkt = K / Kt;
-    const uint32_t pitch = static_cast<uint32_t>(Kt) * eb + kTileRowPad;
+    const int Kt = tile_kt(K, rows), nkt = K / Kt;
+    const uint32_t pitch = static_cast<uint32_t>(Kt) * 2u + kTileRowPad;
     const int nsteps = Kt / 16;
-    const uint32_t b8 = static_cast<uint32_t>(min(lane >> 2, rows - 1)) * pitch + 2u * static_cast<uint32_t>(lane & 3);
     // ldmatrix.x4 rows for B: matrices 0,1 = k step s (k, k+8), matrices 2,3 = k step s + 8; rows
     // past the block's last one repeat it (their outputs are discarded)
     const uint32_t b_off2 = static_cast<uint32_t>(min(lane & 7, rows - 1)) * pitch +
@@ -870,9 +826,7 @@ __device__ __noinline__ void gemv_tiles(const CallParams& cp, const Phase& ph, S
           const uint32_t tb = order_after(smem_u32(S.ring[pipe.stage]));
           const uint32_t ak = 2u * static_cast<uint32_t>(kt * Kt);
           // the K tiles of the S2-Pro projections (2560, 2432, 2048 columns) have fixed step counts
-          if (w8) {
-            tile_steps8(tb + b8, a_ld, a_ld0, ak, warp, nsteps, a_live, acc0, acc1, acc2, acc3);
-          } else if (nsteps == 160) {
+          if (nsteps == 160) {
             tile_steps<10, false>(tb, b_off, b_off2, a_ld, a_ld0, ak, warp, a_live, acc0, acc1, acc2, acc3);
           } else if (nsteps == 152) {
             tile_steps<9, true>(tb, b_off, b_off2, a_ld, a_ld0, ak, warp, a_live, acc0, acc1, acc2, acc3);
@@ -937,10 +891,6 @@ __device__ __noinline__ void gemv_tiles(const CallParams& cp, const Phase& ph, S
       for (int w = 0; w < kConsumerWarps; ++w) a += S.red[((rl * nmat + 0) * NC + c) * kConsumerWarps + w];
       if (nmat == 2)
         for (int w = 0; w < kConsumerWarps; ++w) bb += S.red[((rl * nmat + 1) * NC + c) * kConsumerWarps + w];
-      if (w8) {
-        a *= __ldg(ph.wscale[0] + r0 + rl);
-        if (nmat == 2) bb *= __ldg(ph.wscale[1] + r0 + rl);
-      }
       float v;
       if (ph.epi == EPI_STORE) {
         v = a;

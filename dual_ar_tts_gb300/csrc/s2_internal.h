@@ -108,7 +108,6 @@ struct alignas(16) Phase {
   int M, K, nmat, ncols, epi, rows_per_tile, Q;
   int Kt;                // bf16 weights: columns per tile (K = nkt * Kt)
   const void* w[2];   // row-major [M][K]; w[1] is the gate partner for EPI_SWIGLU
-  const float* wscale[2];  // non-null: w[m] holds e4m3 codes [M][K] with these row scales (fp8 streaming)
   const void* last_row;  // nullable: source of row M-1 (admissible logits: im_end row)
   const void* normw;     // nullable RMSNorm weight [K]
   float* hid_out;        // nullable: CTA 0 writes normalised column 0 here
