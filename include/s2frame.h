@@ -73,8 +73,10 @@ typedef struct s2_dims {
                            fast_project_in, fast_output) as fp8 e4m3 with one fp32 scale per row
                            (scale = max|row| / 448, round to nearest even, saturating), quantised by
                            s2_frame_init into the workspace from the bf16 weights; embeddings, norms
-                           and the tied logits stay bf16.  bf16 weights only, projection lengths
-                           multiples of 128.  0: stream bf16. */
+                           and the tied logits stay bf16; activations stay fp32-exact (bf16 hi + lo
+                           parts).  bf16 weights only, projection lengths multiples of 128, shapes
+                           the batched decode supports (every decode runs there, n = 1 included;
+                           s2_fast_logits is not available).  0: stream bf16. */
 } s2_dims;
 
 /* Sampler settings of one stream ([ch.06 §5.3, §6]; Mizuoto "Fish Speech" engine page:

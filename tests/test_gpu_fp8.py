@@ -8,6 +8,8 @@
 * a small bf16 model decoded with fp8 projections, three streams together and one stream alone,
   teacher-forced with the oracle's draws: the oracle reads the same e4m3 codes and scales
   (logits and hidden at max-abs-rel <= 2e-2, pinned draws and codes exactly);
+* S2-Pro, one stream: a 512-position prompt through the fp8 prompt projections and frames with a
+  batch of one, against the oracle;
 * the S2-Pro serving workload with fp8 projections: two sampled streams of the 32 against the
   oracle for their first frames, then free-running frames decoded twice with the same codes.
 """
@@ -157,3 +159,29 @@ def test_s2pro_fp8_serving_streams_match_oracle(s2pro):
     assert torch.equal(runs[0], runs[1])
     del kd, vd
     torch.cuda.empty_cache()
+
+
+def test_s2pro_fp8_single_stream_prefill_and_frames_match_oracle(s2pro):
+    # one stream: the 512-position prompt through the fp8 prompt projections (128-position chunks,
+    # 256 MMA columns), then frames on the batched engine with a batch of one, against the oracle
+    import dual_ar_tts_gb300 as pkg
+    d, host, dev, names = s2pro
+    cfg = synth.CONFIGS["frame"]
+    n_frames = 2
+    prompt = synth.prompt("frame")
+    s = synth.sampling("frame")
+    expo = synth.expo(cfg["input_seed"], 0, n_frames)
+    quant = oracle.quantize_projections(d, host)
+    sess = oracle.Session(d, host, len(prompt) + n_frames + 1, quant=quant)
+    ref = oracle.generate(sess, prompt, n_frames, s, expo)
+    sess.close()
+    forced = np.zeros((n_frames, 11), np.int32)
+    forced[:len(ref["draws"])] = np.asarray(ref["draws"], np.int32)
+    dec = pkg.Decoder(dict(d, weight_fp8=1), dev, max_streams=1, kv_slots=1024)
+    dec.prefill([prompt])
+    out = dec.decode(n_frames, s, torch.from_numpy(expo).cuda()[None], torch.from_numpy(forced).cuda()[None],
+                     taps=True)
+    assert dec.sync_status() == pkg.S2_OK, pkg.s2_last_error(dec.ctx)
+    st = compare_frames(ref, out, d, s, TOL)
+    print("fp8 single-stream parity:", st)
+    dec.close()
