@@ -453,7 +453,7 @@ def main():
         torch.cuda.empty_cache()
         line["batched"] = batched_measure(pkg, d, dev_w, args.batched, args.batched_steps, args.warmup, pk, local,
                                           args.batched_streams)
-    if args.fp8 and args.slow_layers is None:
+    if args.fp8:
         dec.close()
         torch.cuda.empty_cache()
         line["fp8"] = fp8_measure(pkg, d, dev_w, prompt, args, pk, local)
