@@ -270,8 +270,8 @@ struct Gemv8Bars {
 __host__ __device__ constexpr int gemv8_acc_cols(int N) { return N <= 64 ? 64 : (N <= 128 ? 128 : 256); }
 __host__ __device__ constexpr int gemv8_tmem_cols(int N) { return N <= 128 ? 256 : 512; }
 __host__ __device__ constexpr int gemv8_tbufs(int N) {
-  return (gemv8_tmem_cols(N) - gemv8_acc_cols(N)) / 64 < kMaxTBufs ? (gemv8_tmem_cols(N) - gemv8_acc_cols(N)) / 64
-                                                                    : kMaxTBufs;
+  const int n = (gemv8_tmem_cols(N) - gemv8_acc_cols(N)) / 64;
+  return n < kMaxTBufs ? n : kMaxTBufs;
 }
 
 __global__ void __launch_bounds__(kGemv8Threads, kGemvCtasPerSm)
