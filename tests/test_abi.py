@@ -125,3 +125,13 @@ def test_fp8_dims_are_checked():
     host_shapes = [s for _, s, _ in synth.weight_specs(synth.MINI)]
     q = sum(int(np.prod(host_shapes[i])) + 4 * host_shapes[i][0] for i in oracle.projection_indices(synth.MINI))
     assert q <= b - a <= q + 256 * (2 * len(oracle.projection_indices(synth.MINI)) + 1)
+
+
+def test_static_fast_logits_rejects_fp8_dims_before_any_cuda_call():
+    import dual_ar_tts_gb300 as pkg
+    import synth
+    d = dict(synth.MINI, weight_fp8=1)
+    n = pkg.s2_weight_count(pkg.make_dims(d))
+    with pytest.raises(pkg.S2Error) as e:
+        pkg.s2_fast_logits_static(pkg.make_dims(d), [16] * n, 1, 16, 16, 16)
+    assert e.value.code == pkg.S2_EINVAL

@@ -185,3 +185,16 @@ def test_s2pro_fp8_single_stream_prefill_and_frames_match_oracle(s2pro):
     st = compare_frames(ref, out, d, s, TOL)
     print("fp8 single-stream parity:", st)
     dec.close()
+
+
+def test_fp8_context_refuses_fast_alone():
+    import dual_ar_tts_gb300 as pkg
+    d = synth.MINI
+    dev = pkg.upload_weights(synth.make_weights(d, 7, norm_jitter=0.1))
+    dec = pkg.Decoder(dict(d, weight_fp8=1), dev, max_streams=1, kv_slots=64)
+    hidden = torch.zeros((1, d["dim"]), device="cuda")
+    prefix = torch.zeros((1, d["n_codebooks"] - 1), dtype=torch.int32, device="cuda")
+    with pytest.raises(pkg.S2Error) as e:
+        dec.fast_logits(hidden, prefix)
+    assert e.value.code == pkg.S2_ESTATE
+    dec.close()
