@@ -51,7 +51,6 @@ constexpr int kPrefillCols = 128;             // prompt positions per projection
 constexpr int kPrepThreads = 1024;                // column preparation: one CTA per column
 constexpr int kPrepPer = 3;                       // row elements per thread
 constexpr int kPrepMaxK = kPrepPer * kPrepThreads;  // longest row a column-preparation CTA holds
-constexpr int kAttnTile = 32;               // KV slots per staged tile (Slow-AR attention)
 constexpr int kAttnChunk = 1024;            // target slots per Slow-AR attention item
 constexpr int kAttnStages = 3;              // K/V slot groups in flight per warp
 constexpr int kMaxSplitsAttn = 32;          // items per (stream, KV head) at most
@@ -610,14 +609,10 @@ template <typename KT>
 __device__ __forceinline__ float kvf(KT x);
 template <>
 __device__ __forceinline__ float kvf<__half>(__half x) { return __half2float(x); }
-template <>
-__device__ __forceinline__ float kvf<float>(float x) { return x; }
 template <typename KT>
 __device__ __forceinline__ KT tokv(float x);
 template <>
 __device__ __forceinline__ __half tokv<__half>(float x) { return __float2half_rn(x); }
-template <>
-__device__ __forceinline__ float tokv<float>(float x) { return x; }
 
 // per-head RMSNorm (weight [hd]) then RoPE on adjacent pairs, in place on v[0..HD) by 128 threads
 // of one head group (helpers run by the whole CTA with head h = thread / (HD/2) pairs)
