@@ -146,3 +146,17 @@ def test_session_reading_codes_equals_dequantised_fp32_weights():
     assert np.max(np.abs(la - lc)) < 0.1 * np.max(np.abs(lc))
     for s in (a, b, c):
         s.close()
+
+
+@pytest.mark.parametrize("cfg", ["frame", "tiny"])
+def test_projection_indices_name_exactly_the_projection_matrices(cfg):
+    # the table indices the oracle reads as e4m3 are the projections, by the weight table's names
+    d = synth.CONFIGS[cfg]["dims"]
+    specs = synth.weight_specs(d)
+    idx = oracle.projection_indices(d)
+    want = {i for i, (name, shape, _) in enumerate(specs)
+            if name.split(".")[-1] in ("wqkv", "wo", "w1", "w3", "w2")
+            or (name == "fast_project_in" and d["has_fast_project_in"]) or name == "fast_output"}
+    assert sorted(idx) == sorted(want) and len(idx) == len(set(idx))
+    assert len(idx) == 5 * (d["n_layer"] + d["fast_n_layer"]) + 1 + int(bool(d["has_fast_project_in"]))
+    assert all(len(specs[i][1]) == 2 for i in idx)
