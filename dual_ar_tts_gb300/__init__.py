@@ -21,7 +21,7 @@ STATUS_NAMES = {0: "S2_OK", 1: "S2_EINVAL", 2: "S2_ENOMEM", 3: "S2_ECAPACITY", 4
 EXPORTS = ("s2_weight_count", "s2_weight_info", "s2_frame_workspace_bytes", "s2_frame_init", "s2_prefill",
            "s2_decode_frames", "s2_fast_logits", "s2_sync_status", "s2_set_spin_limit", "s2_set_trace",
            "s2_phase_count", "s2_frame_free", "s2_last_error", "s2_fast_logits_static", "s2_stream_import",
-           "s2_stop_stream", "s2_stream_progress", "s2_codec_latent", "s2_quantize_e4m3")
+           "s2_stop_stream", "s2_stream_progress", "s2_codec_latent", "s2_quantize_e4m3", "s2_set_barrier_base")
 
 
 class s2_dims(ctypes.Structure):
@@ -74,6 +74,7 @@ def load(path: str = LIB_PATH):
         "s2_sync_status": (i32, [vp, vp]),
         "s2_set_spin_limit": (i32, [vp, i64]),
         "s2_set_trace": (i32, [vp, vp, i32]),
+        "s2_set_barrier_base": (i32, [vp, ctypes.c_uint]),
         "s2_phase_count": (i32, [vp, i32]),
         "s2_frame_free": (i32, [vp]),
         "s2_last_error": (ctypes.c_char_p, [vp]),
@@ -202,6 +203,10 @@ def s2_sync_status(ctx, stream: int = 0) -> int:
 
 def s2_set_spin_limit(ctx, limit: int):
     return _check("s2_set_spin_limit", load().s2_set_spin_limit(ctx, limit), ctx)
+
+
+def s2_set_barrier_base(ctx, base: int):
+    return _check("s2_set_barrier_base", load().s2_set_barrier_base(ctx, base), ctx)
 
 
 def s2_set_trace(ctx, buf_ptr: int | None, capacity: int):

@@ -42,6 +42,7 @@ struct s2_ctx {
   int n_dec = 0, n_fast = 0, prefill_chunk = 0;
   unsigned long long* trace = nullptr;  // caller-owned device buffer (tracing hook)
   int trace_cap = 0;
+  unsigned gbar_base = 0;          // grid-barrier counter start (test hook)
   std::vector<int> host_pos;
   std::vector<char> host_prefilled;
   std::string err;
@@ -605,6 +606,7 @@ CallParams base_params(s2_ctx* c) {
   cp.kv_slots = c->kv_slots;
   cp.trace = c->trace;
   cp.trace_cap = c->trace_cap;
+  cp.gbar_base = c->gbar_base;
   return cp;
 }
 
@@ -941,7 +943,8 @@ int s2_fast_logits(s2_ctx* c, int n_frames, const float* hidden, const int32_t* 
                    CUstream_st* stream) {
   if (!c) return fail(nullptr, S2_EINVAL, "ctx is NULL");
   const Dims& d = c->d;
-  if (n_frames <= 0 || !hidden || !prefix || !logits) return fail(c, S2_EINVAL, "bad fast_logits arguments");
+  if (n_frames <= 0 || n_frames > kMaxFastFrames || !hidden || !prefix || !logits)
+    return fail(c, S2_EINVAL, "bad fast_logits arguments (n_frames must be in 1..1048576)");
   if (d.fp8) return fail(c, S2_ESTATE, "the Fast-AR-alone path streams bf16 weights (fp8 contexts decode frames only)");
   CallParams cp = base_params(c);
   cp.n_frames = n_frames;
@@ -985,6 +988,12 @@ int s2_set_spin_limit(s2_ctx* c, long long limit) {
   return S2_OK;
 }
 
+int s2_set_barrier_base(s2_ctx* c, unsigned base) {
+  if (!c) return fail(nullptr, S2_EINVAL, "ctx is NULL");
+  c->gbar_base = base;
+  return S2_OK;
+}
+
 int s2_set_trace(s2_ctx* c, unsigned long long* buf, int capacity) {
   if (!c) return fail(nullptr, S2_EINVAL, "ctx is NULL");
   if ((buf == nullptr) != (capacity == 0) || capacity < 0) return fail(c, S2_EINVAL, "bad trace buffer");
@@ -1020,7 +1029,7 @@ namespace {
 constexpr size_t kStaticScratchBytes = S2_STATIC_SCRATCH_BYTES;
 constexpr int kStaticMaxPhases = 1024;
 constexpr int kStaticMaxDevices = 64;
-constexpr int kStaticMaxFrames = 1 << 20;
+constexpr int kStaticMaxFrames = kMaxFastFrames;
 
 // In host code this name is only a stand-in for the symbol: the device address of each device's
 // copy comes from cudaGetSymbolAddress, made once per device with that device current.

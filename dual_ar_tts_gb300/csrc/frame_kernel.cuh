@@ -145,8 +145,10 @@ __device__ bool grid_sync(const CallParams& cp, Smem& S, unsigned& target) {
       const long long lim = cp.ctl->spin_limit;
       const long long t0 = clock_us();
       unsigned spins = 0;
-      // the clock every 8 polls, the global error word every 64
-      while (ld_acquire(&cp.ctl->gbar) < target) {
+      // the clock every 8 polls, the global error word every 64.  The counter may wrap around
+      // 2^32 within a long call: the signed difference orders it correctly (it is never more
+      // than one phase of arrivals away from the target)
+      while (static_cast<int>(ld_acquire(&cp.ctl->gbar) - target) < 0) {
         if ((++spins & 7u) == 0) {
           if ((spins & 63u) == 0 && ld_volatile_int(&cp.ctl->error) != 0) {
             ok = 0;
@@ -1492,7 +1494,7 @@ __device__ void fast_in(const CallParams& cp, int f) {
 template <class C>
 __device__ void consumers(const CallParams& cp, Smem& S) {
   Pipe pipe{0, 0, 0};
-  unsigned target = 0;
+  unsigned target = cp.gbar_base;  // the host starts the counter there
   const bool cta0 = blockIdx.x == 0;
   const int tid = threadIdx.x;
   constexpr int NQ = static_cast<int>(sizeof(Phase) / 16);

@@ -14,6 +14,8 @@ size_t frame_kernel_smem_bytes();
 
 namespace {
 
+__global__ void k_set_u32(unsigned* p, unsigned v) { *p = v; }
+
 // bf16 weights run with an fp16 KV cache, fp32 weights with an fp32 cache; the head_dim of the
 // Fast-AR transformer (equal to the Slow-AR one when there is a Slow-AR) selects the rest
 const void* kernel_for(const Dims& d) {
@@ -42,7 +44,13 @@ int frame_kernel_grid(int device, int* grid_out) {
 
 int launch_frames(const CallParams& cp, int grid, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(&cp.ctl->gbar, 0, sizeof(unsigned), s) != cudaSuccess) return S2_ECUDA;
+  // the grid-barrier counter starts at cp.gbar_base (0 unless a test moves it near 2^32)
+  if (cp.gbar_base == 0u) {
+    if (cudaMemsetAsync(&cp.ctl->gbar, 0, sizeof(unsigned), s) != cudaSuccess) return S2_ECUDA;
+  } else {
+    k_set_u32<<<1, 1, 0, s>>>(&cp.ctl->gbar, cp.gbar_base);
+    if (cudaGetLastError() != cudaSuccess) return S2_ECUDA;
+  }
   void* args[] = {const_cast<CallParams*>(&cp)};
   const cudaError_t e = cudaLaunchCooperativeKernel(kernel_for(cp.d), dim3(grid), dim3(kThreads), args,
                                                     frame_kernel_smem_bytes(), s);

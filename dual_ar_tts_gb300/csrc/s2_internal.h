@@ -16,6 +16,7 @@ constexpr int kDraws = 11;             // main, redraw, codebooks 1..9
 constexpr int kMaxCodebooks = 15;      // vals[] holds NCB+1 <= 16 ids
 constexpr int kMaxWindow = 16;         // RAS window capacity (ras_window <= 10 used)
 constexpr int kMaxFramesPerCall = 8192;
+constexpr int kMaxFastFrames = 1 << 20;        // Fast-AR-alone calls (teacher-forced frames)
 
 // persistent frame kernel geometry
 constexpr int kConsumerWarps = 8;
@@ -165,6 +166,7 @@ struct alignas(16) CallParams {
   const void* CE;
   const void* FE;
   int kv_slots;
+  unsigned gbar_base;     // grid-barrier counter value at launch (the launch sets it)
 };
 
 // host entry points between translation units

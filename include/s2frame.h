@@ -179,7 +179,8 @@ int s2_stream_progress(s2_ctx* ctx, int n, const int* stream_ids, int32_t* out, 
 
 /* Fast-AR alone, teacher-forced (ch.06 §1-§4): for each of n_frames frames, hidden device
  * [n_frames][dim] and prefix device [n_frames][n_codebooks-1] (code_0..code_{NCB-2}); writes
- * logits device [n_frames][n_codebooks-1][codebook_size], window w = 2..n_codebooks. */
+ * logits device [n_frames][n_codebooks-1][codebook_size], window w = 2..n_codebooks.
+ * n_frames is in 1..1048576 (S2_EINVAL otherwise). */
 int s2_fast_logits(s2_ctx* ctx, int n_frames, const float* hidden, const int32_t* prefix, float* logits,
                    struct CUstream_st* stream);
 
@@ -190,6 +191,11 @@ int s2_sync_status(s2_ctx* ctx, struct CUstream_st* stream);
 /* Testing hook: bound on device-side spin waits, in units of ~1 µs (0 restores the default of
  * about two seconds).  Lets a test make a wait give up without any fault. */
 int s2_set_spin_limit(s2_ctx* ctx, long long limit);
+
+/* Testing hook: value at which the device grid-barrier counter starts in later launches
+ * (default 0).  The counter grows by the grid size at every phase and wraps around 2^32 in long
+ * calls; a test starts it a few phases below 2^32 to exercise the wrap. */
+int s2_set_barrier_base(s2_ctx* ctx, unsigned base);
 
 /* Tracing hook: when buf (device, 2*capacity entries) is set, later decode / Fast-AR calls record,
  * for frame f and program phase p (index k = f*phase_count + p < capacity), the globaltimer (ns)
