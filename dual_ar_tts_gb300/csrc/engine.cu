@@ -37,7 +37,6 @@ struct s2_ctx {
   uint16_t *op = nullptr, *gp = nullptr, *fop = nullptr, *fgp = nullptr;
   float *flogits = nullptr, *part = nullptr, *pscratch = nullptr;
   int32_t* fcode = nullptr;
-  float* hidden_src = nullptr;     // builder: hidden buffer feeding Fast-AR position 0
   Phase* prog = nullptr;           // [max_streams][n_dec] then fast-only program
   int n_dec = 0, n_fast = 0, prefill_chunk = 0;
   unsigned long long* trace = nullptr;  // caller-owned device buffer (tracing hook)
@@ -202,6 +201,8 @@ int fast_call_phases(const Dims& d) {
   return n;
 }
 
+int fast_alone_phases(const Dims& d) { return 2 + fast_call_phases(d); }
+
 int attn_items_max(const Dims& d, int grid, int slots) {
   if (d.L == 0) return 1;
   return d.Hkv * (grid / d.Hkv + slots / kAttnMaxChunk + 2);
@@ -254,7 +255,7 @@ void carve(s2_ctx* c, Carver& cv) {
   c->prefill_chunk = 512;
   c->pscratch = d.L > 0 ? cv.take<float>(prefill_scratch_floats(d, c->prefill_chunk)) : nullptr;
   c->n_dec = d.L > 0 ? 1 + fast_call_phases(d) + 5 * d.L + 1 : 0;
-  c->n_fast = 2 + fast_call_phases(d);
+  c->n_fast = fast_alone_phases(d);
   c->prog = cv.take<Phase>(static_cast<size_t>(B) * c->n_dec + c->n_fast);
   if (c->batched) {
     const BatchSizes z = batch_sizes(d, B, c->sms);
@@ -310,13 +311,32 @@ void carve(s2_ctx* c, Carver& cv) {
 
 // ------------------------------------------------------------ phase builders
 
+// The buffers the Fast-AR phases read and write: a context's workspace regions or the static
+// array's (s2_fast_logits_static).
+struct FastBufs {
+  float* hidden_src;  // the hidden feeding Fast-AR position 0
+  float *fx, *fqkv, *fo, *fg, *fk, *fv, *flogits;
+  uint16_t *fop, *fgp;  // bf16 hi / lo rows of the attention and SwiGLU outputs (bf16 models)
+  int32_t* fcode;
+};
+
+// The Fast-AR weights (device pointers of the weight table)
+struct FastWts {
+  const LayerW* layers;  // [fast_n_layer]
+  const void *P, *FO, *fnorm;
+};
+
+// Appends phases to a caller-given array (no allocation); `n` counts every push, so a program
+// longer than `cap` is detected by the caller (n > cap) without writing past the array.
 struct Builder {
-  s2_ctx* c;
-  std::vector<Phase>* out;
+  Dims d;
+  int grid;
+  Phase* out;
+  int cap;
+  int n = 0;
   std::string err;
 
   Phase gemv(int M, int K, int ncols, const void* w0, const void* w1, const void* normw, int epi) {
-    const Dims& d = c->d;
     Phase p{};
     p.op = OP_GEMV;
     p.M = M;
@@ -347,8 +367,8 @@ struct Builder {
     }
     return p;
   }
-  void push(Phase p) {
-    const int g2 = c->grid - p.cta0;
+  void push(const Phase& p) {
+    const int g2 = grid - p.cta0;
     if (p.op == OP_GEMV && p.ncols == 2 && (p.col[0].src == SRC_PLANES) != (p.col[1].src == SRC_PLANES))
       err = "internal: a phase mixes planes and other activation sources";
     if (p.op == OP_GEMV && p.col[0].src == SRC_PLANES && p.normw != nullptr) err = "internal: normalised planes input";
@@ -358,32 +378,32 @@ struct Builder {
         err = "too many rows per CTA for the partial-sum buffer";
       if (p.last_row && p.nmat != 1) err = "last-row override needs one matrix";
     }
-    out->push_back(p);
+    if (n < cap) out[n] = p;
+    ++n;
   }
   static GemvCol buf(const float* p, float* wb = nullptr) { return GemvCol{SRC_BUF, 0, p, wb}; }
   static GemvCol planes(const uint16_t* p) { return GemvCol{SRC_PLANES, 0, p, nullptr}; }
   // bf16 models pass attention and SwiGLU outputs to the next projection as hi / lo planes
-  bool use_planes() const { return c->d.wdt == S2_BF16; }
-  bool split_down(int npos) const { return split_fast_down(c->d, npos); }
+  bool use_planes() const { return d.wdt == S2_BF16; }
 
-  // Fast-AR calls 1..NCB-1 (fast_only: without draws' side effects on the stream state)
-  void fast_calls() {
-    const Dims& d = c->d;
+  // Fast-AR calls 1..NCB-1, each followed by its draw (ch.06 §1-§4): positions 0 and 1 in the
+  // first call, then one new position per call over the within-frame K/V
+  void fast_calls(const FastBufs& b, const FastWts& w) {
     const int QKVf = (d.Hqf + 2 * d.Hkvf) * d.hdf;
     const size_t kvl = static_cast<size_t>(d.Wf) * d.Hkvf * d.hdf;
     const float scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d.hdf)));
     for (int cb = 1; cb < d.ncb; ++cb) {
       const int npos = cb == 1 ? 2 : 1, pos0 = cb == 1 ? 0 : cb;
       for (int l = 0; l < d.Lf; ++l) {
-        const LayerW& w = c->fast[l];
-        Phase q = gemv(QKVf, d.Df, npos, w.wqkv, nullptr, w.an, EPI_STORE);
+        const LayerW& lw = w.layers[l];
+        Phase q = gemv(QKVf, d.Df, npos, lw.wqkv, nullptr, lw.an, EPI_STORE);
         for (int j = 0; j < npos; ++j) {
           const int p = pos0 + j;
-          float* xp = c->fx + static_cast<size_t>(p) * d.Df;
-          if (l == 0 && p >= 1) q.col[j] = GemvCol{SRC_FEROW, 0, c->fcode + (p - 1), xp};
-          else if (l == 0 && p == 0 && !d.has_proj) q.col[j] = buf(c->hidden_src, xp);
+          float* xp = b.fx + static_cast<size_t>(p) * d.Df;
+          if (l == 0 && p >= 1) q.col[j] = GemvCol{SRC_FEROW, 0, b.fcode + (p - 1), xp};
+          else if (l == 0 && p == 0 && !d.has_proj) q.col[j] = buf(b.hidden_src, xp);
           else q.col[j] = buf(xp);
-          q.y[j] = c->fqkv + static_cast<size_t>(j) * QKVf;
+          q.y[j] = b.fqkv + static_cast<size_t>(j) * QKVf;
         }
         push(q);
         Phase a{};
@@ -391,57 +411,69 @@ struct Builder {
         a.layer = l;
         a.npos = npos;
         a.pos0 = pos0;
-        a.qkv = c->fqkv;
-        a.out = c->fo;
-        if (use_planes()) a.outp = c->fop;
-        a.kc = c->fk + l * kvl;
-        a.vc = c->fv + l * kvl;
-        a.qn = w.qn;
-        a.kn = w.kn;
+        a.qkv = b.fqkv;
+        a.out = b.fo;
+        if (use_planes()) a.outp = b.fop;
+        a.kc = b.fk + l * kvl;
+        a.vc = b.fv + l * kvl;
+        a.qn = lw.qn;
+        a.kn = lw.kn;
         a.scale = scale;
         push(a);
-        Phase o = gemv(d.Df, d.Hqf * d.hdf, npos, w.wo, nullptr, nullptr, EPI_ADD);
+        Phase o = gemv(d.Df, d.Hqf * d.hdf, npos, lw.wo, nullptr, nullptr, EPI_ADD);
         for (int j = 0; j < npos; ++j) {
-          o.col[j] = use_planes() ? planes(c->fop + static_cast<size_t>(j) * 2 * d.Hqf * d.hdf)
-                                  : buf(c->fo + static_cast<size_t>(j) * d.Hqf * d.hdf);
-          o.y[j] = c->fx + static_cast<size_t>(pos0 + j) * d.Df;
+          o.col[j] = use_planes() ? planes(b.fop + static_cast<size_t>(j) * 2 * d.Hqf * d.hdf)
+                                  : buf(b.fo + static_cast<size_t>(j) * d.Hqf * d.hdf);
+          o.y[j] = b.fx + static_cast<size_t>(pos0 + j) * d.Df;
         }
         push(o);
-        Phase u = gemv(d.Ff, d.Df, npos, w.w1, w.w3, w.fn, EPI_SWIGLU);
+        Phase u = gemv(d.Ff, d.Df, npos, lw.w1, lw.w3, lw.fn, EPI_SWIGLU);
         for (int j = 0; j < npos; ++j) {
-          u.col[j] = buf(c->fx + static_cast<size_t>(pos0 + j) * d.Df);
-          if (use_planes()) u.yp[j] = c->fgp + static_cast<size_t>(j) * 2 * d.Ff;
-          else u.y[j] = c->fg + static_cast<size_t>(j) * d.Ff;
+          u.col[j] = buf(b.fx + static_cast<size_t>(pos0 + j) * d.Df);
+          if (use_planes()) u.yp[j] = b.fgp + static_cast<size_t>(j) * 2 * d.Ff;
+          else u.y[j] = b.fg + static_cast<size_t>(j) * d.Ff;
         }
         push(u);
-        if (split_down(npos)) {
-          // two positions whose activations exceed the shared buffer: one phase per position
-          for (int j = 0; j < npos; ++j) {
-            Phase dn = gemv(d.Df, d.Ff, 1, w.w2, nullptr, nullptr, EPI_ADD);
-            dn.col[0] = use_planes() ? planes(c->fgp + static_cast<size_t>(j) * 2 * d.Ff)
-                                     : buf(c->fg + static_cast<size_t>(j) * d.Ff);
-            dn.y[0] = c->fx + static_cast<size_t>(pos0 + j) * d.Df;
-            push(dn);
-          }
-        } else {
-          Phase dn = gemv(d.Df, d.Ff, npos, w.w2, nullptr, nullptr, EPI_ADD);
-          for (int j = 0; j < npos; ++j) {
-            dn.col[j] = use_planes() ? planes(c->fgp + static_cast<size_t>(j) * 2 * d.Ff)
-                                     : buf(c->fg + static_cast<size_t>(j) * d.Ff);
-            dn.y[j] = c->fx + static_cast<size_t>(pos0 + j) * d.Df;
+        // two positions whose activations exceed the shared buffer: one down phase per position
+        const int ndown = split_fast_down(d, npos) ? npos : 1;
+        for (int t = 0; t < ndown; ++t) {
+          const int nc = ndown == 1 ? npos : 1;
+          Phase dn = gemv(d.Df, d.Ff, nc, lw.w2, nullptr, nullptr, EPI_ADD);
+          for (int j = 0; j < nc; ++j) {
+            const int jj = ndown == 1 ? j : t;
+            dn.col[j] = use_planes() ? planes(b.fgp + static_cast<size_t>(jj) * 2 * d.Ff)
+                                     : buf(b.fg + static_cast<size_t>(jj) * d.Ff);
+            dn.y[j] = b.fx + static_cast<size_t>(pos0 + jj) * d.Df;
           }
           push(dn);
         }
       }
-      Phase fo = gemv(d.cbs, d.Df, 1, c->FO, nullptr, c->fnorm, EPI_STORE);
-      fo.col[0] = buf(c->fx + static_cast<size_t>(cb) * d.Df);
-      fo.y[0] = c->flogits;
+      Phase fo = gemv(d.cbs, d.Df, 1, w.FO, nullptr, w.fnorm, EPI_STORE);
+      fo.col[0] = buf(b.fx + static_cast<size_t>(cb) * d.Df);
+      fo.y[0] = b.flogits;
       push(fo);
       Phase s{};
       s.op = OP_SAMPLE_FAST;
       s.cb = cb;
       push(s);
     }
+  }
+
+  // The Fast-AR-alone program (teacher-forced frames): the frame's hidden and first prefix code
+  // (CTA 0), its projection into position 0, then the calls
+  void fast_alone(const FastBufs& b, const FastWts& w) {
+    Phase fi{};
+    fi.op = OP_FAST_IN;
+    push(fi);
+    if (d.has_proj) {
+      Phase p = gemv(d.Df, d.D, 1, w.P, nullptr, nullptr, EPI_STORE);
+      p.col[0] = buf(b.hidden_src);
+      p.y[0] = b.fx;
+      push(p);
+    } else {
+      push(fi);  // a harmless repeat keeps the program length of every shape at 2 + the calls
+    }
+    fast_calls(b, w);
   }
 };
 
@@ -490,15 +522,32 @@ size_t s2_frame_workspace_bytes(const s2_dims* s, int max_streams, int kv_slots)
 
 namespace {
 
+FastBufs ctx_fast_bufs(s2_ctx* c, float* hidden_src) {
+  FastBufs b{};
+  b.hidden_src = hidden_src;
+  b.fx = c->fx;
+  b.fqkv = c->fqkv;
+  b.fo = c->fo;
+  b.fg = c->fg;
+  b.fk = c->fk;
+  b.fv = c->fv;
+  b.flogits = c->flogits;
+  b.fop = c->fop;
+  b.fgp = c->fgp;
+  b.fcode = c->fcode;
+  return b;
+}
+
 int build_programs(s2_ctx* c) {
   const Dims& d = c->d;
-  std::vector<Phase> all;
-  Builder b{c, &all, {}};
+  const size_t total = static_cast<size_t>(c->max_streams) * c->n_dec + c->n_fast;
+  std::vector<Phase> all(total);
+  Builder b{d, c->grid, all.data(), static_cast<int>(total)};
+  const FastWts fw{c->fast.data(), c->P, c->FO, c->fnorm};
   for (int sid = 0; sid < c->max_streams && d.L > 0; ++sid) {
-    const size_t before = all.size();
+    const int before = b.n;
     float* hid = c->hidden + static_cast<size_t>(sid) * d.D;
     float* lg = c->logits + static_cast<size_t>(sid) * logits_stride(d);
-    c->hidden_src = hid;
     // 1. main draw on CTA 0 while the other CTAs project the hidden state into Fast-AR position 0
     if (d.has_proj) {
       Phase p = b.gemv(d.Df, d.D, 1, c->P, nullptr, nullptr, EPI_STORE);
@@ -513,7 +562,7 @@ int build_programs(s2_ctx* c) {
       b.push(p);
     }
     // 2. nine Fast-AR calls with their draws
-    b.fast_calls();
+    b.fast_calls(ctx_fast_bufs(c, hid), fw);
     // 3. Slow-AR step on [token, code_0..code_{NCB-1}]
     const size_t kvl = static_cast<size_t>(c->max_streams) * d.Hkv * c->kv_slots * d.hd * d.kvsz;
     const size_t kvs = static_cast<size_t>(sid) * d.Hkv * c->kv_slots * d.hd * d.kvsz;
@@ -560,30 +609,16 @@ int build_programs(s2_ctx* c) {
     lo.y[0] = lg;
     lo.bump_pos = 1;
     b.push(lo);
-    if (static_cast<int>(all.size() - before) != c->n_dec) return fail(c, S2_EINVAL, "internal: decode program length");
+    if (b.n - before != c->n_dec) return fail(c, S2_EINVAL, "internal: decode program length");
   }
-  // Fast-AR-alone program
+  // Fast-AR-alone program (its own hidden and stream-state slots after the streams')
   {
-    const size_t before = all.size();
-    float* hid = c->hidden + static_cast<size_t>(c->max_streams) * d.D;
-    c->hidden_src = hid;
-    Phase fi{};
-    fi.op = OP_FAST_IN;
-    b.push(fi);
-    if (d.has_proj) {
-      Phase p = b.gemv(d.Df, d.D, 1, c->P, nullptr, nullptr, EPI_STORE);
-      p.col[0] = Builder::buf(hid);
-      p.y[0] = c->fx;
-      b.push(p);
-    } else {
-      Phase p{};
-      p.op = OP_FAST_IN;  // harmless repeat keeps the program length fixed
-      b.push(p);
-    }
-    b.fast_calls();
-    if (static_cast<int>(all.size() - before) != c->n_fast) return fail(c, S2_EINVAL, "internal: fast program length");
+    const int before = b.n;
+    b.fast_alone(ctx_fast_bufs(c, c->hidden + static_cast<size_t>(c->max_streams) * d.D), fw);
+    if (b.n - before != c->n_fast) return fail(c, S2_EINVAL, "internal: fast program length");
   }
   if (!b.err.empty()) return fail(c, S2_EINVAL, b.err);
+  if (static_cast<size_t>(b.n) != total) return fail(c, S2_EINVAL, "internal: program length");
   std::string why;
   if (!planes_inside(all.data(), all.size(), c->ws, c->ws_bytes, why)) return fail(c, S2_EINVAL, "internal: " + why);
   if (cudaMemcpy(c->prog, all.data(), all.size() * sizeof(Phase), cudaMemcpyHostToDevice) != cudaSuccess)
@@ -1019,10 +1054,11 @@ const char* s2_last_error(const s2_ctx* c) { return c ? c->err.c_str() : g_init_
 
 // ============================================ Fast-AR alone on static scratch (no allocation)
 //
-// s2_fast_logits_static serves callers that may not allocate device memory (a host application
-// whose pool already holds the device memory, or a latency-critical thread that must not block
-// in cudaMalloc/cudaFree).  Its scratch is a file-scope device array that is part of this
-// library; every call on a device shares it.
+// s2_fast_logits_static serves callers that may not allocate device memory: a host application
+// whose own memory pool has already reserved the device (a game engine, a DAW plug-in), or a
+// latency-critical thread (an audio callback) that must not block in cudaMalloc/cudaFree.  Its
+// scratch is a file-scope device array that is part of this library; every call on a device
+// shares it.
 
 namespace {
 
@@ -1030,166 +1066,73 @@ constexpr size_t kStaticScratchBytes = S2_STATIC_SCRATCH_BYTES;
 constexpr int kStaticMaxPhases = 1024;
 constexpr int kStaticMaxDevices = 64;
 constexpr int kStaticMaxFrames = kMaxFastFrames;
+constexpr int kStaticMaxWeights = 3 + 4 + 9 * 128;  // weight-table entries kept for the program key
 
 // In host code this name is only a stand-in for the symbol: the device address of each device's
-// copy comes from cudaGetSymbolAddress, made once per device with that device current.
+// copy comes from cudaGetSymbolAddress, made with that device current.
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 struct StaticDevice {
   unsigned char* scratch = nullptr;  // device address of g_static_scratch on this device
   int grid = 0;                      // frame kernel grid (one CTA per SM)
+  // the program and RoPE table in the array were built for this shape and weight table
+  bool have_prog = false;
+  Dims d{};
+  int n_weights = 0;
+  const void* w[kStaticMaxWeights] = {};
 };
 
 std::mutex g_static_mu;                       // serialises the host side of the calls
 StaticDevice g_static_dev[kStaticMaxDevices];
 Phase g_static_prog[kStaticMaxPhases];        // host copy of the program being uploaded
+LayerW g_static_layers[kStaticMaxPhases / 5]; // Fast-AR layers bound from the weight table
 
-struct StaticFastLayout {
+struct StaticLayout {
   Control* ctl;
   float2* rope_f;
   StreamState* st;
-  float *hidden, *fx, *fqkv, *fo, *fg, *fk, *fv, *flogits;
-  uint16_t *fop, *fgp;
-  int32_t* fcode;
+  FastBufs fb;
   Phase* prog;
 };
 
 // Scratch of the Fast-AR-alone program: the context's Fast-AR buffers, carved from the array.
-size_t carve_static_fast(const Dims& d, int n_phases, unsigned char* base, StaticFastLayout& s) {
+size_t carve_static(const Dims& d, int n_phases, unsigned char* base, StaticLayout& s) {
   Carver cv{base};
   const int QKVf = (d.Hqf + 2 * d.Hkvf) * d.hdf;
   s.ctl = cv.take<Control>(1);
   s.rope_f = cv.take<float2>(static_cast<size_t>(d.Wf) * (d.hdf / 2));
   s.st = cv.take<StreamState>(1);
-  s.hidden = cv.take<float>(d.D);
-  s.fx = cv.take<float>(static_cast<size_t>(d.Wf) * d.Df);
-  s.fqkv = cv.take<float>(2 * static_cast<size_t>(QKVf));
-  s.fo = cv.take<float>(2 * static_cast<size_t>(d.Hqf) * d.hdf);
-  s.fg = cv.take<float>(2 * static_cast<size_t>(d.Ff));
-  s.fk = cv.take<float>(static_cast<size_t>(d.Lf) * d.Wf * d.Hkvf * d.hdf);
-  s.fv = cv.take<float>(static_cast<size_t>(d.Lf) * d.Wf * d.Hkvf * d.hdf);
-  s.flogits = cv.take<float>(d.cbs);
-  s.fop = cv.take<uint16_t>(4 * static_cast<size_t>(d.Hqf) * d.hdf);
-  s.fgp = cv.take<uint16_t>(4 * static_cast<size_t>(d.Ff));
-  s.fcode = cv.take<int32_t>(16);
+  FastBufs& b = s.fb;
+  b.hidden_src = cv.take<float>(d.D);
+  b.fx = cv.take<float>(static_cast<size_t>(d.Wf) * d.Df);
+  b.fqkv = cv.take<float>(2 * static_cast<size_t>(QKVf));
+  b.fo = cv.take<float>(2 * static_cast<size_t>(d.Hqf) * d.hdf);
+  b.fg = cv.take<float>(2 * static_cast<size_t>(d.Ff));
+  b.fk = cv.take<float>(static_cast<size_t>(d.Lf) * d.Wf * d.Hkvf * d.hdf);
+  b.fv = cv.take<float>(static_cast<size_t>(d.Lf) * d.Wf * d.Hkvf * d.hdf);
+  b.flogits = cv.take<float>(d.cbs);
+  b.fop = cv.take<uint16_t>(4 * static_cast<size_t>(d.Hqf) * d.hdf);
+  b.fgp = cv.take<uint16_t>(4 * static_cast<size_t>(d.Ff));
+  b.fcode = cv.take<int32_t>(16);
   s.prog = cv.take<Phase>(static_cast<size_t>(n_phases));
   return align_up(cv.off, 256);
 }
 
-// The Fast-AR-alone program (the same phases as a context's) over the static layout, written to
-// `out` (host, kStaticMaxPhases entries).  wt is the s2_frame_init weight table.
-int build_static_fast_program(const Dims& d, int grid, const void* const* wt, const StaticFastLayout& s,
-                              Phase* out, int* n_out, std::string& why) {
-  s2_ctx shape;  // the phase helper reads only the shape
-  shape.d = d;
-  shape.grid = grid;
-  Builder b{&shape, nullptr, {}};
-  int n = 0;
-  auto push = [&](const Phase& p) {
-    if (p.op == OP_GEMV && p.ncols == 2 && (p.col[0].src == SRC_PLANES) != (p.col[1].src == SRC_PLANES))
-      b.err = "internal: a phase mixes planes and other activation sources";
-    if (p.op == OP_GEMV) {
-      const int g2 = grid - p.cta0;
-      const int rows = (p.M + g2 - 1) / g2;
-      if (static_cast<long long>(rows) * p.nmat * p.ncols * kConsumerWarps > kRedFloats)
-        b.err = "too many rows per CTA for the partial-sum buffer";
-    }
-    if (n < kStaticMaxPhases) out[n] = p;
-    ++n;
-  };
-  const int base = 3 + 9 * d.L;
-  const void* P = wt[base];
-  const void* fnorm = wt[base + 2];
-  const void* FO = wt[base + 3];
-  auto fw = [&](int l, int k) { return wt[base + 4 + 9 * l + k]; };  // an wqkv qn kn wo fn w1 w3 w2
-  Phase fi{};
-  fi.op = OP_FAST_IN;
-  push(fi);
-  if (d.has_proj) {
-    Phase p = b.gemv(d.Df, d.D, 1, P, nullptr, nullptr, EPI_STORE);
-    p.col[0] = Builder::buf(s.hidden);
-    p.y[0] = s.fx;
-    push(p);
-  } else {
-    push(fi);  // keeps the program length of a context's Fast-AR-alone program
-  }
-  const int QKVf = (d.Hqf + 2 * d.Hkvf) * d.hdf;
-  const size_t kvl = static_cast<size_t>(d.Wf) * d.Hkvf * d.hdf;
-  const float scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d.hdf)));
-  for (int cb = 1; cb < d.ncb; ++cb) {
-    const int npos = cb == 1 ? 2 : 1, pos0 = cb == 1 ? 0 : cb;
-    for (int l = 0; l < d.Lf; ++l) {
-      Phase q = b.gemv(QKVf, d.Df, npos, fw(l, 1), nullptr, fw(l, 0), EPI_STORE);
-      for (int j = 0; j < npos; ++j) {
-        const int p = pos0 + j;
-        float* xp = s.fx + static_cast<size_t>(p) * d.Df;
-        if (l == 0 && p >= 1) q.col[j] = GemvCol{SRC_FEROW, 0, s.fcode + (p - 1), xp};
-        else if (l == 0 && p == 0 && !d.has_proj) q.col[j] = Builder::buf(s.hidden, xp);
-        else q.col[j] = Builder::buf(xp);
-        q.y[j] = s.fqkv + static_cast<size_t>(j) * QKVf;
-      }
-      push(q);
-      Phase a{};
-      a.op = OP_ATTN_FAST;
-      a.layer = l;
-      a.npos = npos;
-      a.pos0 = pos0;
-      a.qkv = s.fqkv;
-      a.out = s.fo;
-      if (b.use_planes()) a.outp = s.fop;
-      a.kc = s.fk + l * kvl;
-      a.vc = s.fv + l * kvl;
-      a.qn = fw(l, 2);
-      a.kn = fw(l, 3);
-      a.scale = scale;
-      push(a);
-      Phase o = b.gemv(d.Df, d.Hqf * d.hdf, npos, fw(l, 4), nullptr, nullptr, EPI_ADD);
-      for (int j = 0; j < npos; ++j) {
-        o.col[j] = b.use_planes() ? Builder::planes(s.fop + static_cast<size_t>(j) * 2 * d.Hqf * d.hdf)
-                                  : Builder::buf(s.fo + static_cast<size_t>(j) * d.Hqf * d.hdf);
-        o.y[j] = s.fx + static_cast<size_t>(pos0 + j) * d.Df;
-      }
-      push(o);
-      Phase u = b.gemv(d.Ff, d.Df, npos, fw(l, 6), fw(l, 7), fw(l, 5), EPI_SWIGLU);
-      for (int j = 0; j < npos; ++j) {
-        u.col[j] = Builder::buf(s.fx + static_cast<size_t>(pos0 + j) * d.Df);
-        if (b.use_planes()) u.yp[j] = s.fgp + static_cast<size_t>(j) * 2 * d.Ff;
-        else u.y[j] = s.fg + static_cast<size_t>(j) * d.Ff;
-      }
-      push(u);
-      const int ndown = split_fast_down(d, npos) ? npos : 1;  // one phase per position when split
-      for (int t = 0; t < ndown; ++t) {
-        const int nc = ndown == 1 ? npos : 1;
-        Phase dn = b.gemv(d.Df, d.Ff, nc, fw(l, 8), nullptr, nullptr, EPI_ADD);
-        for (int j = 0; j < nc; ++j) {
-          const int jj = ndown == 1 ? j : t;
-          dn.col[j] = b.use_planes() ? Builder::planes(s.fgp + static_cast<size_t>(jj) * 2 * d.Ff)
-                                     : Builder::buf(s.fg + static_cast<size_t>(jj) * d.Ff);
-          dn.y[j] = s.fx + static_cast<size_t>(pos0 + jj) * d.Df;
-        }
-        push(dn);
-      }
-    }
-    Phase fo = b.gemv(d.cbs, d.Df, 1, FO, nullptr, fnorm, EPI_STORE);
-    fo.col[0] = Builder::buf(s.fx + static_cast<size_t>(cb) * d.Df);
-    fo.y[0] = s.flogits;
-    push(fo);
-    Phase sf{};
-    sf.op = OP_SAMPLE_FAST;
-    sf.cb = cb;
-    push(sf);
-  }
-  if (!b.err.empty()) {
-    why = b.err;
-    return S2_EINVAL;
-  }
-  if (n > kStaticMaxPhases) {
-    why = "the Fast-AR program has " + std::to_string(n) + " phases; the static path holds at most " +
-          std::to_string(kStaticMaxPhases);
-    return S2_ENOMEM;
-  }
-  *n_out = n;
-  return S2_OK;
+// control block and stream state of a call: zero, with the default wait bound
+__global__ void k_static_reset(Control* ctl, StreamState* st, long long spin_limit) {
+  const int n = static_cast<int>(sizeof(Control) / sizeof(int));
+  for (int i = threadIdx.x; i < n; i += blockDim.x) reinterpret_cast<int*>(ctl)[i] = 0;
+  for (int i = threadIdx.x; i < static_cast<int>(sizeof(StreamState) / sizeof(int)); i += blockDim.x)
+    reinterpret_cast<int*>(st)[i] = 0;
+  __syncthreads();
+  if (threadIdx.x == 0) ctl->spin_limit = spin_limit;
+}
+
+bool same_key(const StaticDevice& sd, const Dims& d, const void* const* w, int n) {
+  if (!sd.have_prog || sd.n_weights != n || std::memcmp(&sd.d, &d, sizeof(Dims)) != 0) return false;
+  for (int i = 0; i < n; ++i)
+    if (sd.w[i] != w[i]) return false;
+  return true;
 }
 
 int static_fail(int code, const std::string& msg) { return fail(nullptr, code, "s2_fast_logits_static: " + msg); }
@@ -1199,7 +1142,7 @@ int static_fail(int code, const std::string& msg) { return fail(nullptr, code, "
 extern "C" int s2_fast_logits_static(const s2_dims* s, const void* const* weights, int n_weights, int n_frames,
                                      const float* hidden, const int32_t* prefix, float* logits, int32_t* status,
                                      CUstream_st* stream) {
-  Dims d;
+  Dims d{};
   std::string why;
   if (!s || !to_dims(s, d, why)) return static_fail(S2_EINVAL, "bad dims: " + why);
   if (d.fp8) return static_fail(S2_EINVAL, "the static entry streams bf16 or fp32 weights (weight_fp8 must be 0)");
@@ -1212,50 +1155,68 @@ extern "C" int s2_fast_logits_static(const s2_dims* s, const void* const* weight
     if (!weights[i]) return static_fail(S2_EINVAL, "a Fast-AR weight is NULL");
     if (reinterpret_cast<uintptr_t>(weights[i]) & 15u) return static_fail(S2_EINVAL, "weights must be 16-byte aligned");
   }
-  const int n_phases = 2 + fast_call_phases(d);
-  StaticFastLayout probe{};
-  const size_t need = carve_static_fast(d, n_phases, nullptr, probe);
+  const int n_phases = fast_alone_phases(d);
+  if (n_phases > kStaticMaxPhases)
+    return static_fail(S2_ENOMEM, "the Fast-AR program has " + std::to_string(n_phases) +
+                                      " phases; the static path holds at most " + std::to_string(kStaticMaxPhases));
+  StaticLayout probe{};
+  const size_t need = carve_static(d, n_phases, nullptr, probe);
   if (need > kStaticScratchBytes)
     return static_fail(S2_ENOMEM, "this Fast-AR shape needs " + std::to_string(need) +
                                       " bytes of scratch; the static array holds " + std::to_string(kStaticScratchBytes));
+  const int n_fast_w = n_weights - base;
+  if (n_fast_w > kStaticMaxWeights) return static_fail(S2_ENOMEM, "too many Fast-AR weights for the static path");
   std::lock_guard<std::mutex> lock(g_static_mu);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return static_fail(S2_ECUDA, "no current CUDA device");
   if (dev < 0 || dev >= kStaticMaxDevices) return static_fail(S2_EINVAL, "device ordinal above 63");
   StaticDevice& sd = g_static_dev[dev];
-  if (sd.scratch == nullptr) {
-    // set-up, once per device (this device is current)
-    void* ptr = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
-    if (e != cudaSuccess) return static_fail(S2_ECUDA, std::string("cudaGetSymbolAddress failed: ") + cudaGetErrorString(e));
+  // the array's device address on this device, looked up on every call (this device is current):
+  // after a device reset the module, and with it the array, is loaded again at a new address
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+  if (e != cudaSuccess) return static_fail(S2_ECUDA, std::string("cudaGetSymbolAddress failed: ") + cudaGetErrorString(e));
+  if (sd.scratch != static_cast<unsigned char*>(ptr) || sd.grid == 0) {
     int grid = 0;
     if (frame_kernel_grid(dev, &grid) != S2_OK) return static_fail(S2_ECUDA, "the frame kernel cannot be resident on this device");
+    sd = StaticDevice{};
     sd.grid = grid;
     sd.scratch = static_cast<unsigned char*>(ptr);
   }
-  StaticFastLayout sl{};
-  carve_static_fast(d, n_phases, sd.scratch, sl);
-  int n_built = 0;
-  int rc = build_static_fast_program(d, sd.grid, weights, sl, g_static_prog, &n_built, why);
-  if (rc != S2_OK) return static_fail(rc, why);
-  if (n_built != n_phases) return static_fail(S2_EINVAL, "internal: Fast-AR program length");
-  if (!planes_inside(g_static_prog, static_cast<size_t>(n_built), sd.scratch, kStaticScratchBytes, why))
-    return static_fail(S2_EINVAL, "internal: " + why);
+  StaticLayout sl{};
+  carve_static(d, n_phases, sd.scratch, sl);
   cudaStream_t cs = stream;
-  // what must start from zero (the array keeps the previous call's contents): control block, stream state
-  Control ctl{};
-  ctl.spin_limit = 2000000;
-  if (cudaMemcpyAsync(sl.ctl, &ctl, sizeof(Control), cudaMemcpyHostToDevice, cs) != cudaSuccess ||
-      cudaMemsetAsync(sl.st, 0, sizeof(StreamState), cs) != cudaSuccess ||
-      cudaMemcpyAsync(sl.prog, g_static_prog, sizeof(Phase) * n_phases, cudaMemcpyHostToDevice, cs) != cudaSuccess)
-    return static_fail(S2_ECUDA, "initialising the static scratch failed");
-  if (build_rope_tables(nullptr, 0, d.hd, sl.rope_f, d.Wf, d.hdf, d.rope_base, d.rope_bf16, cs) != S2_OK)
-    return static_fail(S2_ECUDA, "building the RoPE table failed");
+  if (!same_key(sd, d, weights + base, n_fast_w)) {
+    // a new shape or weight table: build the program and the RoPE table into the array (the
+    // program is copied from this library's host memory, which waits for the stream's earlier work)
+    sd.have_prog = false;
+    for (int l = 0; l < d.Lf; ++l) {
+      const void* const* lw = weights + base + 4 + 9 * l;
+      g_static_layers[l] = LayerW{lw[0], lw[1], lw[2], lw[3], lw[4], lw[5], lw[6], lw[7], lw[8]};
+    }
+    Builder b{d, sd.grid, g_static_prog, kStaticMaxPhases};
+    b.fast_alone(sl.fb, FastWts{g_static_layers, weights[base], weights[base + 3], weights[base + 2]});
+    if (!b.err.empty()) return static_fail(S2_EINVAL, b.err);
+    if (b.n != n_phases) return static_fail(S2_EINVAL, "internal: Fast-AR program length");
+    if (!planes_inside(g_static_prog, static_cast<size_t>(b.n), sd.scratch, kStaticScratchBytes, why))
+      return static_fail(S2_EINVAL, "internal: " + why);
+    if (cudaMemcpyAsync(sl.prog, g_static_prog, sizeof(Phase) * n_phases, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+      return static_fail(S2_ECUDA, "copying the program failed");
+    if (build_rope_tables(nullptr, 0, d.hd, sl.rope_f, d.Wf, d.hdf, d.rope_base, d.rope_bf16, cs) != S2_OK)
+      return static_fail(S2_ECUDA, "building the RoPE table failed");
+    sd.have_prog = true;
+    sd.d = d;
+    sd.n_weights = n_fast_w;
+    for (int i = 0; i < n_fast_w; ++i) sd.w[i] = weights[base + i];
+  }
+  // what must start from zero (the array keeps the previous call's contents)
+  k_static_reset<<<1, 64, 0, cs>>>(sl.ctl, sl.st, 2000000);
+  if (cudaGetLastError() != cudaSuccess) return static_fail(S2_ECUDA, "initialising the static scratch failed");
   CallParams cp{};
   cp.d = d;
   cp.ctl = sl.ctl;
-  cp.fcode = sl.fcode;
-  cp.flogits = sl.flogits;
+  cp.fcode = sl.fb.fcode;
+  cp.flogits = sl.fb.flogits;
   cp.rope_f = sl.rope_f;
   cp.FE = weights[base + 1];
   cp.n_frames = n_frames;
@@ -1263,13 +1224,13 @@ extern "C" int s2_fast_logits_static(const s2_dims* s, const void* const* weight
   cp.n_phases = n_phases;
   cp.prog = sl.prog;
   cp.st = sl.st;
-  cp.hidden = sl.hidden;
+  cp.hidden = sl.fb.hidden_src;
   cp.fin_hidden = hidden;
   cp.fin_prefix = prefix;
   cp.fout = logits;
   cp.temperature = 1.f;
   cp.top_p = 1.f;
-  rc = launch_frames(cp, sd.grid, cs);
+  const int rc = launch_frames(cp, sd.grid, cs);
   if (rc != S2_OK) return static_fail(rc, std::string("frame kernel launch failed: ") + cudaGetErrorString(cudaGetLastError()));
   if (status && cudaMemcpyAsync(status, &sl.ctl->error, 2 * sizeof(int32_t), cudaMemcpyDeviceToDevice, cs) != cudaSuccess)
     return static_fail(S2_ECUDA, "copying the status failed");

@@ -240,13 +240,24 @@ const char* s2_last_error(const s2_ctx* ctx);
  * Limits: the shape's scratch must fit S2_STATIC_SCRATCH_BYTES and its program 1024 phases, else
  * S2_ENOMEM and nothing is launched; n_frames in 1..1048576 (frames run one after another in the
  * same scratch, so their number does not grow it).
- * Set-up: the first call on a device (the current one) looks up the array's device address and
- * configures the kernel on that device; make that first call before any stream capture.
+ * Set-up: the first call on a device (the current one) configures the kernel on that device; make
+ * that first call before any stream capture.  The array is committed on a device when the
+ * library's device code is loaded there: at this first call under lazy module loading (the CUDA
+ * default), or when the library is loaded with CUDA_MODULE_LOADING=EAGER.  A caller whose memory
+ * pool reserves the device should make its first call before the pool does.  Every call looks the
+ * array's address up again (cudaGetSymbolAddress, no allocation once loaded), so a device reset
+ * between calls only repeats the set-up.
+ * Program: the first call with a given shape and weight table on a device (and the first call
+ * after a call with another one) writes the phase program and the Fast-AR RoPE table into the
+ * array; the program is copied from this library's host memory, so that call waits until the
+ * stream's earlier work is done.  Later calls with the same shape and table launch only a small
+ * reset kernel (control block and state to zero), the frame kernel and, with status, one
+ * device-to-device copy, and never wait on the host.
  * Sharing: all calls on a device use the one array, which keeps the previous call's contents; each
- * call re-initialises what must start from zero (control block, state, program, RoPE table) before
- * its kernel.  Calls whose GPU work overlaps (different streams, or host threads without ordering)
- * race on the array and give undefined results: issue them on one stream or synchronise between them.
- * The host side of concurrent calls is serialised.
+ * call resets what must start from zero before its kernel.  Calls whose GPU work overlaps
+ * (different streams, or host threads without ordering) race on the array and give undefined
+ * results: issue them on one stream or synchronise between them.  The host side of concurrent
+ * calls is serialised.
  * Errors (nothing launched): S2_EINVAL bad shape, pointer, alignment, count or device ordinal (> 63);
  * S2_ENOMEM above the limits; S2_ECUDA set-up, copy or launch failed.  Message: s2_last_error(NULL). */
 #define S2_STATIC_SCRATCH_BYTES ((size_t)2 << 20)

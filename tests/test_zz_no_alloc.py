@@ -1,10 +1,15 @@
 """s2_fast_logits_static — Fast-AR alone on the library's static scratch (no allocation).
 
+It serves callers that cannot allocate device memory: an application whose memory pool already
+holds the device, or a latency-critical thread that must not block in cudaMalloc/cudaFree.
+
 The GPU test calls the static entry point through the C ABI twice in a row, with different inputs
 and frame counts, and compares each output with s2_fast_logits of a context on the same weights
-(same tolerances as the other parity tests: 1e-4 for fp32 weights, 2e-2 for bf16).  The file is
-named to be collected last, and passes alone in a fresh process as well as after the other tests.
-The CPU tests check the argument and size rejections, which return before any CUDA call.
+and with the oracle (same tolerances as the other parity tests: 1e-4 for fp32 weights, 2e-2 for
+bf16).  A second test checks that a repeated call changes neither the device's free memory nor
+the memory torch has allocated.  The file is named to be collected last, and passes alone in a
+fresh process as well as after the other tests.  The CPU tests check the argument and size
+rejections, which return before any CUDA call.
 """
 import ctypes
 
@@ -12,6 +17,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 from tests.parity import max_abs_rel
 
@@ -37,6 +43,7 @@ def test_static_matches_context_path_on_two_calls(pkg, case, tol):
     dev = pkg.upload_weights(host)
     dims = pkg.make_dims(d)
     dec = pkg.Decoder(d, dev, max_streams=1, kv_slots=8 if d["n_layer"] > 0 else 0)
+    sess = oracle.Session(d, host, 1)
     stream = torch.cuda.current_stream().cuda_stream
     ncb, cbs = d["n_codebooks"], d["codebook_size"]
     for seed, n in ((11, 8), (12, 5)):
@@ -54,7 +61,44 @@ def test_static_matches_context_path_on_two_calls(pkg, case, tol):
         assert np.isfinite(got).all()
         worst = max(max_abs_rel(got[f, c], want[f, c]) for f in range(n) for c in range(ncb - 1))
         assert worst <= tol, (case, seed, worst)
+        # the oracle recomputes each window from scratch (first and last frame, three windows)
+        for f in (0, n - 1):
+            for c in (1, (ncb - 1) // 2 + 1, ncb - 1):
+                e = max_abs_rel(got[f, c - 1], sess.fast_logits(hid[f], pre[f, :c]))
+                assert e <= tol, (case, seed, f, c, e)
     dec.close()
+
+
+@pytest.mark.gpu
+def test_static_repeat_call_allocates_no_device_memory(pkg):
+    d = synth.CONFIGS["tiny"]["dims"]
+    dev = pkg.upload_weights(synth.make_weights(d, 0, norm_jitter=0.1))
+    dims = pkg.make_dims(d)
+    stream = torch.cuda.current_stream().cuda_stream
+    ncb, cbs = d["n_codebooks"], d["codebook_size"]
+    n = 6
+    hid, pre = synth.fast_inputs(21, n, d)
+    h = torch.from_numpy(hid).cuda()
+    p = torch.from_numpy(pre).cuda()
+    out = torch.empty((n, ncb - 1, cbs), device="cuda")
+    status = torch.empty((2,), dtype=torch.int32, device="cuda")
+    # the first call with this weight table sets the array up
+    pkg.s2_fast_logits_static(dims, _ptrs(dev), n, h.data_ptr(), p.data_ptr(), out.data_ptr(), status.data_ptr(),
+                              stream)
+    torch.cuda.synchronize()
+    first = out.clone()
+    free0, _ = torch.cuda.mem_get_info()
+    alloc0 = torch.cuda.memory_allocated()
+    out.fill_(float("nan"))
+    torch.cuda.synchronize()
+    pkg.s2_fast_logits_static(dims, _ptrs(dev), n, h.data_ptr(), p.data_ptr(), out.data_ptr(), status.data_ptr(),
+                              stream)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, (free0, free1)
+    assert torch.cuda.memory_allocated() == alloc0
+    assert int(status[0].item()) == pkg.S2_OK
+    assert torch.equal(out, first)
 
 
 def test_static_rejects_bad_arguments_before_any_cuda_call(pkg):
@@ -74,11 +118,17 @@ def test_static_rejects_bad_arguments_before_any_cuda_call(pkg):
     assert "aligned" in pkg.s2_last_error(None)
 
 
-def test_static_rejects_shapes_beyond_its_scratch(pkg):
-    # a Fast-AR decoder deeper than the static array holds (16 layers of 5120 wide, 15 codebooks)
+@pytest.mark.parametrize("over,limit", [
+    # a Fast-AR decoder with more phases than the static program holds (16 layers, 15 codebooks)
+    (dict(fast_dim=5120, dim=5120, fast_ffn=5120, fast_n_layer=16, fast_n_head=40, fast_n_kv_head=10,
+          n_codebooks=15, fast_window=16), "1024"),
+    # one whose scratch exceeds the array (12 wide layers: within-frame K/V and SwiGLU buffers)
+    (dict(fast_dim=5120, dim=5120, fast_ffn=20480, fast_n_layer=12, fast_n_head=40, fast_n_kv_head=10),
+     str(2 << 20)),
+])
+def test_static_rejects_shapes_beyond_its_limits(pkg, over, limit):
     d = dict(synth.CONFIGS["fast"]["dims"])
-    d.update(fast_dim=5120, dim=5120, fast_ffn=5120, fast_n_layer=16, fast_n_head=40, fast_n_kv_head=10,
-             n_codebooks=15, fast_window=16)
+    d.update(over)
     dims = pkg.make_dims(d)
     lib = pkg.load()
     n_w = lib.s2_weight_count(ctypes.byref(dims))
@@ -87,4 +137,4 @@ def test_static_rejects_shapes_beyond_its_scratch(pkg):
     rc = lib.s2_fast_logits_static(ctypes.byref(dims), arr, n_w, 1, 16, 16, 16, None, None)
     assert rc == pkg.S2_ENOMEM
     msg = pkg.s2_last_error(None)
-    assert "static" in msg and str(2 << 20) in msg, msg
+    assert "static" in msg and limit in msg, msg
