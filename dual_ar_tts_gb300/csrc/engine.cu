@@ -362,6 +362,7 @@ struct Builder {
       while (nkt <= K / 16 && (K % nkt != 0 || (K / nkt) % 16 != 0)) ++nkt;
       if (nkt > K / 16) err = "no K tiling of a projection fits the pipeline stage";
       p.Kt = K / nkt;
+      p.nkt = nkt;
       if (2LL * ncols * (2LL * K + kTileRowPad) > kXsBytes) err = "projection input does not fit the shared activation buffer";
       if (K * d.esz > kStageBytes) err = "norm vector exceeds one pipeline stage";
     }

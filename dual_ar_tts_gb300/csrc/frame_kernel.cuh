@@ -215,16 +215,6 @@ __device__ __noinline__ void drain_copies(const CallParams& cp, uint64_t* bar, u
 // producer
 // =========================================================================
 
-// K split of an 8-row (or shorter) bf16 tile: the fewest K tiles such that `rows` padded row
-// segments fit one stage (Kt a multiple of 16 dividing K).  Producer and consumers agree on it.
-__device__ __forceinline__ int tile_kt(int K, int rows) {
-  for (int n = 1; n <= K / 16; ++n) {
-    if (K % n != 0 || (K / n) % 16 != 0) continue;
-    if (rows * ((K / n) * 2 + kTileRowPad) <= kStageBytes) return K / n;
-  }
-  return 16;
-}
-
 // Producer warp: walks the program ahead of the consumers and fills the ring with each GEMV
 // phase's weights (the RMSNorm vector first, then the row tiles).  Lane 0 waits for a free stage
 // and posts the byte count; the tile's row segments are then issued by separate lanes.
@@ -274,7 +264,9 @@ __device__ void producer(const CallParams& cp, Smem& S) {
           // bf16: tiles of <= 8 rows x Kt columns, row segments padded by 16 bytes, one lane per row
           for (int b = 0; b < nr && !stop; b += kTileRows) {
             const int rows = min(kTileRows, nr - b);
-            const int Kt = tile_kt(ph.K, rows), nkt = ph.K / Kt;
+            // every block, a short last one included, takes the phase's 8-row K tiling (no
+            // per-block division on the issue path)
+            const int Kt = ph.Kt, nkt = ph.nkt;
             const uint32_t segb = static_cast<uint32_t>(Kt) * 2u, pitch = segb + kTileRowPad;
             const int row = r0 + b + lane;
             for (int m = 0; m < ph.nmat && !stop; ++m) {
@@ -805,14 +797,14 @@ __device__ __noinline__ void gemv_tiles(const CallParams& cp, const Phase& ph, S
                          static_cast<uint32_t>((lane >> 3) & 1) * 16u;
   const uint32_t a_ld = a_ld0 + static_cast<uint32_t>((lane >> 4) & 1) * 256u;
   const uint32_t red = smem_u32(S.red);
-  // a block of 8 rows has at most kIters iterations per warp; shorter blocks can have longer K
-  // tiles, which the outer loop covers
+  // a K tile has at most kIters iterations per warp (the outer loop covers any longer one)
   constexpr int kIters = ((kStageBytes / kTileRows - kTileRowPad) / 32 + 2 * kConsumerWarps - 1) / (2 * kConsumerWarps);
   for (int b = 0; b < nr; b += kTileRows) {
     const int rows = min(kTileRows, nr - b);
-    const int Kt = tile_kt(K, rows), nkt = K / Kt;
+    // the phase's K tiling for every block (a short last block too): no division per block
+    const int Kt = ph.Kt, nkt = ph.nkt;
     const uint32_t pitch = static_cast<uint32_t>(Kt) * 2u + kTileRowPad;
-    const int nsteps = Kt / 16;
+    const int nsteps = Kt >> 4;
     // ldmatrix.x4 rows for B: matrices 0,1 = k step s (k, k+8), matrices 2,3 = k step s + 8; rows
     // past the block's last one repeat it (their outputs are discarded)
     const uint32_t b_off2 = static_cast<uint32_t>(min(lane & 7, rows - 1)) * pitch +

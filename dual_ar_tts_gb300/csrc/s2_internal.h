@@ -107,7 +107,8 @@ struct alignas(16) Phase {
   int merge_main;     // OP_GEMV: CTA 0 performs the main draw instead of GEMV rows
   int cta0;           // first CTA doing GEMV rows
   int M, K, nmat, ncols, epi, rows_per_tile, Q;
-  int Kt;                // bf16 weights: columns per tile (K = nkt * Kt)
+  int Kt;                // bf16 weights: columns per tile (K = nkt * Kt), for every 8-row block
+  int nkt;               //   and the count of K tiles
   const void* w[2];   // row-major [M][K]; w[1] is the gate partner for EPI_SWIGLU
   const void* last_row;  // nullable: source of row M-1 (admissible logits: im_end row)
   const void* normw;     // nullable RMSNorm weight [K]
