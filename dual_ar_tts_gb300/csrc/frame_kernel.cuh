@@ -180,10 +180,10 @@ __device__ __forceinline__ void unpack16(const uint4& u, float* f, float) {
 
 // v as bf16 hi (row 0, index i) and lo (row 1 at offset n): hi + lo = v to ~2^-17 relative
 __device__ __forceinline__ void store_planes(uint16_t* planes, int n, int i, float v) {
-  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-  const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-  planes[i] = __bfloat16_as_ushort(hi);
-  planes[n + i] = __bfloat16_as_ushort(lo);
+  const float hi = bf16lo(cvt_bf16x2(v, 0.f));
+  const uint32_t p = cvt_bf16x2(hi, v - hi);  // hi (exact) in the low half, lo in the high half
+  planes[i] = static_cast<uint16_t>(p & 0xffffu);
+  planes[n + i] = static_cast<uint16_t>(p >> 16);
 }
 
 // Split of the Slow-AR attention over n slots: ns splits of `chunk` slots per KV head, at most one
@@ -763,9 +763,10 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
       const int g = tid + kConsumers * j;
       if (g < ng) {
         const float4 v = xv[c][j];
-        const float h0 = round_bf16(v.x), h1 = round_bf16(v.y), h2 = round_bf16(v.z), h3 = round_bf16(v.w);
-        const uint32_t hi01 = pack_bf16x2(h0, h1), hi23 = pack_bf16x2(h2, h3);
-        const uint32_t lo01 = pack_bf16x2(v.x - h0, v.y - h1), lo23 = pack_bf16x2(v.z - h2, v.w - h3);
+        // packed conversions: hi = bf16(v), lo = bf16(v - hi)
+        const uint32_t hi01 = cvt_bf16x2(v.x, v.y), hi23 = cvt_bf16x2(v.z, v.w);
+        const float h0 = bf16lo(hi01), h1 = bf16hi(hi01), h2 = bf16lo(hi23), h3 = bf16hi(hi23);
+        const uint32_t lo01 = cvt_bf16x2(v.x - h0, v.y - h1), lo23 = cvt_bf16x2(v.z - h2, v.w - h3);
         const uint32_t ahi = xsb + static_cast<uint32_t>(2 * c) * xpitch + 8u * static_cast<uint32_t>(g);
         const uint32_t alo = ahi + xpitch;
         asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(ahi), "r"(hi01), "r"(hi23) : "memory");

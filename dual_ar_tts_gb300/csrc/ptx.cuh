@@ -158,6 +158,13 @@ __device__ __forceinline__ void hold(float (&d)[4]) {
   asm volatile("" : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3]));
 }
 
+// two floats rounded to bf16 (nearest even) in one conversion: lo in bits 0-15, hi in bits 16-31
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const uint32_t a = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo)));
   const uint32_t b = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi)));
