@@ -960,10 +960,26 @@ __device__ void gemv(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe)
 // per-head RMSNorm + RoPE of one head vector held by a warp (lane holds DPL contiguous values)
 // =========================================================================
 
+// the head's norm weights and RoPE row held by a lane (loaded before the head vector itself, so
+// that their loads overlap it)
 template <int DPL>
-__device__ __forceinline__ void head_norm_rope(float (&v)[DPL], const void* nw, int esz, float eps, int hd,
-                                               bool norm, const float2* rope_row) {
+struct NormRope {
+  float w[DPL];
+  float2 cs[DPL / 2];
+};
+
+template <int DPL>
+__device__ __forceinline__ void load_norm_rope(NormRope<DPL>& nr, const void* nw, int esz, bool norm,
+                                               const float2* rope_row) {
   const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) nr.w[j] = norm ? wload(nw, lane * DPL + j, esz) : 1.f;
+#pragma unroll
+  for (int j = 0; j < DPL; j += 2) nr.cs[j >> 1] = rope_row[(lane * DPL + j) >> 1];
+}
+
+template <int DPL>
+__device__ __forceinline__ void head_norm_rope(float (&v)[DPL], const NormRope<DPL>& nr, float eps, int hd, bool norm) {
   if (norm) {
     float s = 0.f;
 #pragma unroll
@@ -971,15 +987,24 @@ __device__ __forceinline__ void head_norm_rope(float (&v)[DPL], const void* nw, 
     s = warp_sum(s);
     const float r = 1.0f / sqrtf(s / static_cast<float>(hd) + eps);
 #pragma unroll
-    for (int j = 0; j < DPL; ++j) v[j] = (v[j] * r) * wload(nw, lane * DPL + j, esz);
+    for (int j = 0; j < DPL; ++j) v[j] = (v[j] * r) * nr.w[j];
   }
 #pragma unroll
   for (int j = 0; j < DPL; j += 2) {
-    const float2 cs = rope_row[(lane * DPL + j) >> 1];
+    const float2 cs = nr.cs[j >> 1];
     const float a = v[j], b = v[j + 1];
     v[j] = a * cs.x - b * cs.y;
     v[j + 1] = a * cs.y + b * cs.x;
   }
+}
+
+// per-head RMSNorm + RoPE of one head vector held by a warp (lane holds DPL contiguous values)
+template <int DPL>
+__device__ __forceinline__ void head_norm_rope(float (&v)[DPL], const void* nw, int esz, float eps, int hd,
+                                               bool norm, const float2* rope_row) {
+  NormRope<DPL> nr;
+  load_norm_rope<DPL>(nr, nw, esz, norm, rope_row);
+  head_norm_rope<DPL>(v, nr, eps, hd, norm);
 }
 
 template <typename KT>
@@ -1085,20 +1110,24 @@ __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, 
     // ---- q heads of this KV head; the new slot's k (normed, rotated) and v, stored in the cache
     if (warp < rep) {
       const int h = g * rep + warp;
+      NormRope<DPL> nr;
+      load_norm_rope<DPL>(nr, ph.qn, d.esz, d.qk_norm != 0, rope_row);
       float v[DPL];
 #pragma unroll
       for (int j = 0; j < DPL; ++j) v[j] = ldcg(ph.qkv + h * HD + lane * DPL + j);
-      head_norm_rope<DPL>(v, ph.qn, d.esz, d.eps, HD, d.qk_norm != 0, rope_row);
+      head_norm_rope<DPL>(v, nr, d.eps, HD, d.qk_norm != 0);
 #pragma unroll
       for (int j = 0; j < DPL; ++j) qs[warp * HD + lane * DPL + j] = v[j];
     } else if (warp == rep && has_new) {
+      NormRope<DPL> nr;
+      load_norm_rope<DPL>(nr, ph.kn, d.esz, d.qk_norm != 0, rope_row);
       float k[DPL], v[DPL];
 #pragma unroll
       for (int j = 0; j < DPL; ++j) {
         k[j] = ldcg(ph.qkv + (d.Hq + g) * HD + lane * DPL + j);
         v[j] = ldcg(ph.qkv + (d.Hq + d.Hkv + g) * HD + lane * DPL + j);
       }
-      head_norm_rope<DPL>(k, ph.kn, d.esz, d.eps, HD, d.qk_norm != 0, rope_row);
+      head_norm_rope<DPL>(k, nr, d.eps, HD, d.qk_norm != 0);
       KT* kd = const_cast<KT*>(Kc) + g * kvh + static_cast<size_t>(pos) * HD + lane * DPL;
       KT* vd = const_cast<KT*>(Vc) + g * kvh + static_cast<size_t>(pos) * HD + lane * DPL;
 #pragma unroll
