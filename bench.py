@@ -25,9 +25,9 @@ if ROOT not in sys.path:
 METRIC = "codec frames/sec per stream & aggregate (S2-Pro shapes); HBM GB/s vs 8 TB/s"
 # DRAM bytes (read + write) over algorithmic bytes for one frame_kernel launch, from an ncu capture
 # of the same kernel on a smaller case (S2-Pro widths, 4 Slow-AR layers, 2 frames: 16.621 GB
-# measured against 16.611 GB algorithmic).  Traffic grows with the weights and KV streamed, so the
-# full launch's traffic is this ratio times its algorithmic bytes.  Set to None when the kernel
-# changes until a new capture is taken.
+# measured against 16.611 GB algorithmic; profiles/frame_kernel_small_case_full.md).  Traffic grows
+# with the weights and KV streamed, so the full launch's traffic is this ratio times its
+# algorithmic bytes.  Set to None when the kernel changes until a new capture is taken.
 NCU_TRAFFIC_RATIO = 1.0006
 WORKLOAD = "full-frame Dual-AR decode, S2-Pro shapes (36+4 layers, dim 2560, vocab 155776), batch 1"
 PROMPT_LEN = 512
@@ -41,9 +41,12 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-frames", type=int, default=2, help="frames in the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--batched", default="serving", choices=["serving", "longctx", "none"],
-                    help="also measure the aggregate of a batched workload (reported under 'batched')")
-    ap.add_argument("--batched-steps", type=int, default=16)
+    ap.add_argument("--batched", default="serving,longctx",
+                    help="comma-separated batched workloads to measure as well (serving, longctx; 'none')")
+    ap.add_argument("--batched-steps", type=int, default=None,
+                    help="frames per stream of the batched workloads (default: the workload's own count)")
+    ap.add_argument("--no-extra", dest="extra", action="store_false",
+                    help="skip the tiny-model, Fast-AR-alone and long-prompt prefill measurements")
     ap.add_argument("--no-fp8", dest="fp8", action="store_false",
                     help="skip the fp8 e4m3 weight-streaming measurements")
     ap.add_argument("--batched-streams", type=int, default=None,
@@ -86,7 +89,7 @@ def frame_bytes(d, ctx_avg):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms while running."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -100,7 +103,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -180,6 +183,7 @@ def batched_measure(pkg, d, dev_w, cfg_name, steps, warmup, peak, local, n_strea
     import synth
     cfg = synth.CONFIGS[cfg_name]
     n, slots, seed = cfg["streams"], cfg["kv_slots"], cfg["input_seed"]
+    steps = steps or cfg["frames"]
     lengths = synth.prompt_lengths(cfg_name)
     if n_streams:
         n = min(n, n_streams)
@@ -266,28 +270,123 @@ def fp8_measure(pkg, d, dev_w, prompt, args, peak, local):
                       "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                                    "frac": achieved / peak},
                       "clocks": clk.summary()}}
-    if args.batched != "none":
-        res["batched"] = batched_measure(pkg, d8, dev_w, args.batched, args.batched_steps, W, peak, local,
+    work = batched_workloads(args)
+    if work:
+        res["batched"] = batched_measure(pkg, d8, dev_w, work[0], args.batched_steps, W, peak, local,
                                          args.batched_streams)
     return res
 
 
+def batched_workloads(args):
+    return [w for w in args.batched.split(",") if w and w != "none"]
+
+
+def tiny_measure(pkg, args):
+    """The tiny Dual-AR model (fp32, L2-resident weights): frames/s of its 16-frame decode."""
+    import torch
+    import synth
+    cfg = synth.CONFIGS["tiny"]
+    d = cfg["dims"]
+    dec = pkg.Decoder(d, pkg.upload_weights(synth.make_weights(d, 0)), max_streams=1, kv_slots=cfg["kv_slots"])
+    n = cfg["frames"]
+    s = synth.sampling("tiny")
+    best = None
+    for rep in range(4):
+        dec.prefill([synth.prompt("tiny")])
+        expo = torch.from_numpy(synth.expo(cfg["input_seed"], 0, n)).cuda()[None]
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record()
+        out = dec.decode(n, s, expo)
+        ev1.record()
+        torch.cuda.synchronize()
+        assert dec.sync_status() == pkg.S2_OK
+        ms = ev0.elapsed_time(ev1)
+        if rep > 0:  # the first call is a warm-up
+            best = ms if best is None else min(best, ms)
+    produced = int(out["n_out"][0])
+    dec.close()
+    return {"workload": "tiny Dual-AR (dim 256, 4+2 layers, fp32), 32-position prompt, one call of 16 frames",
+            "value": produced / (best / 1000.0), "unit": "frames/s", "ms_per_frame": best / produced,
+            "roofline": "n/a (weights L2-resident, latency-bound)"}
+
+
+def fast_measure(pkg, d_full, dev_w, peak, args):
+    """Fast-AR alone at S2-Pro shapes, batch 1: 1000 teacher-forced frames x 9 windows."""
+    import torch
+    import synth
+    cfg = synth.CONFIGS["fast"]
+    d = cfg["dims"]
+    by = dict(zip([nm for nm, _, _ in synth.weight_specs(d_full)], dev_w))
+    w = [None if nm in ("embeddings", "codebook_embeddings", "norm") else by[nm] for nm, _, _ in synth.weight_specs(d)]
+    dec = pkg.Decoder(d, w, max_streams=1, kv_slots=0)
+    n = cfg["frames"]
+    hid, pre = synth.fast_inputs(cfg["input_seed"], n, d)
+    h, p = torch.from_numpy(hid).cuda(), torch.from_numpy(pre).cuda()
+    dec.fast_logits(h[:8].contiguous(), p[:8].contiguous())
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    dec.fast_logits(h, p)
+    ev1.record()
+    torch.cuda.synchronize()
+    assert dec.sync_status() == pkg.S2_OK
+    ms = ev0.elapsed_time(ev1)
+    dec.close()
+    _, parts = frame_bytes(d_full, 0)
+    fb = parts["fast"]
+    achieved = fb * n / (ms / 1000.0) / 1e9
+    return {"workload": "Fast-AR alone, S2-Pro shapes (4 layers, dim 2560), batch 1, 1000 frames x 9 windows",
+            "value": n / (ms / 1000.0), "unit": "frames/s", "ms_per_frame": ms / n,
+            "algorithmic_gb_per_frame": fb / 1e9,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak}}
+
+
+def prefill_long_measure(pkg, d, dev_w):
+    """Prefill of the 30000-position long-context prompt (1000 text ids, 29000 reference positions)."""
+    import torch
+    import synth
+    prompt = synth.prompt("longctx", stream=0)
+    dec = pkg.Decoder(d, dev_w, max_streams=1, kv_slots=len(prompt) + 8)
+    dec.prefill([prompt[:512]])
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    dec.prefill([prompt])
+    ev1.record()
+    torch.cuda.synchronize()
+    assert dec.sync_status() == pkg.S2_OK
+    ms = ev0.elapsed_time(ev1)
+    dec.close()
+    return {"positions": len(prompt), "ms": ms, "positions_per_s": len(prompt) / (ms / 1000.0)}
+
+
 def cpu_oracle_sample(d, host_w, n_frames, s):
-    """Oracle (plain fp32 C + OpenMP) on the host cores: prefill of a short prompt (untimed), then
-    n_frames whole frames timed.  Returns (frames/s, cores, description)."""
+    """Oracle (plain fp32 C + OpenMP) on the host cores: n_frames whole frames timed from a decode
+    state of the bench's context (PROMPT_LEN positions).  The state is seeded synthetic fp16 K/V
+    and a last residual (the oracle's own prefill of the prompt takes minutes; the contents of the
+    cache do not change the work of a frame).  Returns (frames/s, cores, description)."""
     import oracle
     import synth
-    sess = oracle.Session(d, host_w, 64)
-    p = synth.prompt("frame")[:16]
-    logits, hidden = sess.prefill(p)
+    sess = oracle.Session(d, host_w, PROMPT_LEN + n_frames + 1)
+    k16, v16, x = synth.kv_state(9, 0, d, PROMPT_LEN)
+    logits, hidden = sess.import_state(k16, v16, x)
     expo = synth.expo(9, 0, n_frames)
     t = time.perf_counter()
     oracle.run_frames(sess, logits, hidden, n_frames, dict(s, min_tokens_before_end=n_frames), expo, trace=False)
     dt = time.perf_counter() - t
+    sess.close()
     cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count()))
-    return n_frames / dt, cores, (f"{n_frames} whole frames (main draw, 9 Fast-AR calls recomputed per window, "
-                                  f"Slow-AR step) after a 16-position prefill; S2-Pro shapes, bf16 weights widened "
-                                  f"to fp32")
+    return n_frames / dt, cores, (f"{n_frames} whole frames (main draw over the full vocabulary, 9 Fast-AR calls "
+                                  f"recomputed per window, Slow-AR step) at a {PROMPT_LEN}-position context "
+                                  f"(seeded fp16 K/V state); S2-Pro shapes, bf16 weights widened to fp32")
+
+
+def bench_config(world, K, fb=None):
+    c = {"workload": WORKLOAD, "global_batch": world, "seq_len": PROMPT_LEN,
+         "parallelism": f"replicas{world}" if world > 1 else "none", "frames_per_call": K}
+    c["l2"] = "inputs larger than L2 (about 14.8 GB of weights and KV streamed per frame)"
+    return c
 
 
 def run_reference(args):
@@ -309,8 +408,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "frames/s", "n_gpus": args.gpus,
             "steps": len(vals), "warmup": 0, "ms_per_step": 1000.0 / v, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": PROMPT_LEN, "parallelism": "none",
-                       "l2": "inputs larger than L2 (9.1 GB of weights)"},
+            "config": bench_config(args.gpus, args.steps),
             "cpu_baseline": {"kind": "oracle", "value": v, "unit": "frames/s", "cores": cores, "sample": sample},
             "e2e": {"value": v, "unit": "frames/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": time.perf_counter() - t0}
@@ -428,10 +526,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": t_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded random weights of the S2-Pro shape, synthetic prompt/variates)",
-        "config": {"workload": workload, "global_batch": world, "seq_len": PROMPT_LEN,
-                   "parallelism": f"replicas{world}" if world > 1 else "none",
-                   "frames_per_call": K,
-                   "l2": f"inputs larger than L2 ({fb / 1e9:.1f} GB of weights and KV streamed per frame)"},
+        "config": dict(bench_config(world, K), workload=workload),
         "per_stream_fps": K / (dev_ms / 1000.0),
         "hbm": {"algorithmic_gb_per_frame": fb / 1e9, "achieved_gbs": achieved, "frac_of_8tbs": achieved / 8000.0,
                 "frac_of_measured": achieved / pk, "parts_gb": {k: v / 1e9 for k, v in parts.items()}},
@@ -448,11 +543,22 @@ def main():
         "clocks": clk.summary(),
         "setup_s": setup_s,
     }
-    if args.batched != "none":
+    work = batched_workloads(args)
+    if work:
         dec.close()
         torch.cuda.empty_cache()
-        line["batched"] = batched_measure(pkg, d, dev_w, args.batched, args.batched_steps, args.warmup, pk, local,
+        line["batched"] = batched_measure(pkg, d, dev_w, work[0], args.batched_steps, args.warmup, pk, local,
                                           args.batched_streams)
+        for wname in work[1:]:
+            torch.cuda.empty_cache()
+            line[f"batched_{wname}"] = batched_measure(pkg, d, dev_w, wname, args.batched_steps, args.warmup, pk,
+                                                       local, args.batched_streams)
+    if args.extra and args.slow_layers is None:
+        dec.close()
+        torch.cuda.empty_cache()
+        line["tiny"] = tiny_measure(pkg, args)
+        line["fast_alone"] = fast_measure(pkg, d, dev_w, pk, args)
+        line["prefill_longctx"] = prefill_long_measure(pkg, d, dev_w)
     if args.fp8:
         dec.close()
         torch.cuda.empty_cache()
