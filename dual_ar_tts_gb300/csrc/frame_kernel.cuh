@@ -264,9 +264,13 @@ __device__ void producer(const CallParams& cp, Smem& S) {
           // bf16: tiles of <= 8 rows x Kt columns, row segments padded by 16 bytes, one lane per row
           for (int b = 0; b < nr && !stop; b += kTileRows) {
             const int rows = min(kTileRows, nr - b);
-            // every block, a short last one included, takes the phase's 8-row K tiling (no
-            // per-block division on the issue path)
-            const int Kt = ph.Kt, nkt = ph.nkt;
+            // the phase's 16-row K tiling (no per-block division on the issue path); a short last
+            // block whose rows fit one stage whole takes all of K in one tile
+            int Kt = ph.Kt, nkt = ph.nkt;
+            if (rows < kTileRows && rows * (2 * ph.K + kTileRowPad) <= kStageBytes) {
+              Kt = ph.K;
+              nkt = 1;
+            }
             const uint32_t segb = static_cast<uint32_t>(Kt) * 2u, pitch = segb + kTileRowPad;
             const int row = r0 + b + lane;
             for (int m = 0; m < ph.nmat && !stop; ++m) {
@@ -575,45 +579,28 @@ __device__ __noinline__ void gemv_t(const CallParams& cp, const Phase& ph, Smem&
 }
 
 // =========================================================================
-// GEMV phase, bf16 weights, on the tensor cores (mma.sync m16n8k16, fp32 accumulate), in
-// transposed form: D[16 x 8] += X^T[16 x 16] · W^T[16 x 8], where the 8 columns of W^T are 8
-// weight rows (an 8-row tile, ldmatrix from shared memory) and the rows of X^T are the
-// activation columns split into bf16 hi and lo parts (x = hi + lo to ~2^-17 relative), so each
-// output is Σ_k w·hi + Σ_k w·lo.  Each warp owns every 8th 16-wide k step of a tile; the eight
-// warps' partial sums are added in a fixed order.
+// GEMV phase, bf16 weights, on the tensor cores (mma.sync m16n8k16, fp32 accumulate):
+// D[16 x 8] += W[16 x 16] · X[16 x 8], where the 16 rows of W are 16 weight rows (a 16-row tile,
+// ldmatrix.x4 from shared memory) and the columns of X are the activation columns split into bf16
+// hi and lo parts (x = hi + lo to ~2^-17 relative; column 2c = hi, 2c + 1 = lo of activation c;
+// ldmatrix.x2 of those rows), so each output is Σ_k w·hi + Σ_k w·lo.  Each warp owns every 8th
+// 16-wide k step of a tile; the eight warps' partial sums are added in a fixed order.
 // =========================================================================
 
-// The k steps of one tile for a warp, with the step count fixed at compile time so that the loads
-// of later steps are issued ahead of the MMAs of earlier ones: Q iterations over the step pairs
-// (st, st + 8), st = warp + 16 i, then with TAIL one more single step st = warp + 16 Q.
-// (nsteps = 16 Q, or 16 Q + 8 with TAIL.)  Four accumulation chains.
-template <int Q, bool TAIL>
-__device__ __forceinline__ void tile_steps(uint32_t tb, uint32_t b_off, uint32_t b_off2, uint32_t a_ld, uint32_t a_ld0,
-                                           uint32_t ak, int warp, bool a_live, float (&acc0)[4], float (&acc1)[4],
-                                           float (&acc2)[4], float (&acc3)[4]) {
+// The k steps of one K tile for a warp, with the step count fixed at compile time so that the loads
+// of later steps are issued ahead of the MMAs of earlier ones: steps st = warp + 8 i for i < S,
+// with TAIL one more step st = warp + 8 S when it is below nsteps.  Four accumulation chains.
+template <int S, bool TAIL>
+__device__ __forceinline__ void tile_steps(uint32_t tb, uint32_t a_off, uint32_t b_ld, int warp, int nsteps,
+                                           float (&acc)[4][4]) {
 #pragma unroll
-  for (int i = 0; i < Q; ++i) {
-    const uint32_t st = static_cast<uint32_t>(warp + 2 * kConsumerWarps * i);
-    uint32_t b0, b1, b2, b3, a0, a2, c0, c2;
-    ldmatrix_x4(tb + b_off + 32u * st, b0, b1, b2, b3);
-    ldmatrix_x4(a_ld + ak + 32u * st, a0, a2, c0, c2);
-    if (!a_live) a0 = a2 = c0 = c2 = 0u;
-    if (i & 1) {
-      mma_bf16_16816(acc2, a0, 0u, a2, 0u, b0, b1);
-      mma_bf16_16816(acc3, c0, 0u, c2, 0u, b2, b3);
-    } else {
-      mma_bf16_16816(acc0, a0, 0u, a2, 0u, b0, b1);
-      mma_bf16_16816(acc1, c0, 0u, c2, 0u, b2, b3);
-    }
-  }
-  if constexpr (TAIL) {
-    const uint32_t st = static_cast<uint32_t>(warp + 2 * kConsumerWarps * Q);
-    uint32_t b0, b1, a0, a2;
-    ldmatrix_x2(tb + b_off2 + 32u * st, b0, b1);
-    ldmatrix_x2(a_ld0 + ak + 32u * st, a0, a2);
-    if (!a_live) a0 = a2 = 0u;
-    if (Q & 1) mma_bf16_16816(acc2, a0, 0u, a2, 0u, b0, b1);
-    else mma_bf16_16816(acc0, a0, 0u, a2, 0u, b0, b1);
+  for (int i = 0; i < S + (TAIL ? 1 : 0); ++i) {
+    const uint32_t st = static_cast<uint32_t>(warp + kConsumerWarps * i);
+    if (TAIL && i == S && static_cast<int>(st) >= nsteps) break;
+    uint32_t a0, a1, a2, a3, b0, b1;
+    ldmatrix_x4(tb + a_off + 32u * st, a0, a1, a2, a3);
+    ldmatrix_x2(b_ld + 32u * st, b0, b1);
+    mma_bf16_16816(acc[i & 3], a0, a1, a2, a3, b0, b1);
   }
 }
 
@@ -787,91 +774,79 @@ __device__ __noinline__ void gemv_tiles(const CallParams& cp, const Phase& ph, S
   rows_of(ph, blockIdx.x, gridDim.x, r0, nr);
   const uint32_t xsb = smem_u32(S.xs);
   const uint32_t xpitch = 2u * static_cast<uint32_t>(K) + kTileRowPad;
-  // ---- tiles: 8-row blocks, each matrix, each K tile; D accumulates over the K tiles.
-  // A (activations) and B (weights) both come from shared memory by ldmatrix: per iteration one
-  // x4 load of each covers k steps s and s + 8; four accumulation chains.
+  // ---- tiles: 16-row blocks, each matrix, each K tile; D accumulates over the K tiles.
   const int nmat = ph.nmat;
-  const bool a_live = lane < 8 * NC;
-  // ldmatrix row addresses for A: matrix row r is activation row r (rows >= 2·NC repeat live rows;
-  // their products land in D rows that are discarded); matrices: k 0-7 / 8-15 of step s, then s + 8
-  const uint32_t a_ld0 = order_after(xsb) + static_cast<uint32_t>((lane & 7) % (2 * NC)) * xpitch +
-                         static_cast<uint32_t>((lane >> 3) & 1) * 16u;
-  const uint32_t a_ld = a_ld0 + static_cast<uint32_t>((lane >> 4) & 1) * 256u;
+  // ldmatrix.x2 row addresses for B (lanes 0-15): column n = lane & 7 reads activation row n
+  // (2c = hi, 2c + 1 = lo of column c; columns >= 2·NC repeat live rows, their outputs are
+  // discarded); matrix 0 = k 0-7 of a step, matrix 1 = k 8-15
+  const uint32_t b_ld = order_after(xsb) + static_cast<uint32_t>((lane & 7) % (2 * NC)) * xpitch +
+                        static_cast<uint32_t>((lane >> 3) & 1) * 16u;
   const uint32_t red = smem_u32(S.red);
-  // a K tile has at most kIters iterations per warp (the outer loop covers any longer one)
-  constexpr int kIters = ((kStageBytes / kTileRows - kTileRowPad) / 32 + 2 * kConsumerWarps - 1) / (2 * kConsumerWarps);
+  const int g = lane >> 2, t = lane & 3;  // D fragment: rows g and g + 8, columns 2t and 2t + 1
   for (int b = 0; b < nr; b += kTileRows) {
     const int rows = min(kTileRows, nr - b);
-    // the phase's K tiling for every block (a short last block too): no division per block
-    const int Kt = ph.Kt, nkt = ph.nkt;
+    // the phase's K tiling (no division per block); a short last block whose rows fit one stage
+    // whole takes all of K in one tile (the producer makes the same choice)
+    int Kt = ph.Kt, nkt = ph.nkt;
+    if (rows < kTileRows && rows * (2 * K + kTileRowPad) <= kStageBytes) {
+      Kt = K;
+      nkt = 1;
+    }
     const uint32_t pitch = static_cast<uint32_t>(Kt) * 2u + kTileRowPad;
     const int nsteps = Kt >> 4;
-    // ldmatrix.x4 rows for B: matrices 0,1 = k step s (k, k+8), matrices 2,3 = k step s + 8; rows
-    // past the block's last one repeat it (their outputs are discarded)
-    const uint32_t b_off2 = static_cast<uint32_t>(min(lane & 7, rows - 1)) * pitch +
-                            static_cast<uint32_t>((lane >> 3) & 1) * 16u;
-    const uint32_t b_off = b_off2 + static_cast<uint32_t>((lane >> 4) & 1) * 256u;
+    // ldmatrix.x4 rows for A: matrices (rows 0-7, k 0-7), (rows 8-15, k 0-7), (rows 0-7, k 8-15),
+    // (rows 8-15, k 8-15); rows past the block's last one repeat it (their outputs are discarded)
+    const uint32_t a_off = static_cast<uint32_t>(min((lane & 7) + 8 * ((lane >> 3) & 1), rows - 1)) * pitch +
+                           static_cast<uint32_t>(lane >> 4) * 16u;
     for (int m = 0; m < nmat; ++m) {
-      float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-      float acc2[4] = {0.f, 0.f, 0.f, 0.f}, acc3[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc[4][4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[q][j] = 0.f;
       for (int kt = 0; kt < nkt; ++kt) {
         const bool ok = wait_bar(cp, S, &S.full[pipe.stage], pipe.round & 1u, 4, false);
         if (!ok) S.fail = 1;
         if (ok) {
           const uint32_t tb = order_after(smem_u32(S.ring[pipe.stage]));
-          const uint32_t ak = 2u * static_cast<uint32_t>(kt * Kt);
-          // the K tiles of the S2-Pro projections (2560, 2432, 2048 columns) have fixed step counts
-          if (nsteps == 160) {
-            tile_steps<10, false>(tb, b_off, b_off2, a_ld, a_ld0, ak, warp, a_live, acc0, acc1, acc2, acc3);
-          } else if (nsteps == 152) {
-            tile_steps<9, true>(tb, b_off, b_off2, a_ld, a_ld0, ak, warp, a_live, acc0, acc1, acc2, acc3);
-          } else if (nsteps == 128) {
-            tile_steps<8, false>(tb, b_off, b_off2, a_ld, a_ld0, ak, warp, a_live, acc0, acc1, acc2, acc3);
-          } else
-          for (int st0 = warp; st0 < nsteps; st0 += 2 * kConsumerWarps * kIters) {
+          const uint32_t bk = b_ld + 2u * static_cast<uint32_t>(kt * Kt);
+          // the K tiles of the S2-Pro projections (1280, 1216 and 1024 columns) have fixed step counts
+          if (nsteps == 80) {
+            tile_steps<10, false>(tb, a_off, bk, warp, nsteps, acc);
+          } else if (nsteps == 76) {
+            tile_steps<9, true>(tb, a_off, bk, warp, nsteps, acc);
+          } else if (nsteps == 64) {
+            tile_steps<8, false>(tb, a_off, bk, warp, nsteps, acc);
+          } else {
+#pragma unroll 1
+            for (int st0 = warp; st0 < nsteps; st0 += 4 * kConsumerWarps) {
 #pragma unroll
-            for (int i = 0; i < kIters; ++i) {
-              const int st = st0 + 2 * kConsumerWarps * i;
-              if (st < nsteps) {
-                uint32_t b0, b1, b2 = 0u, b3 = 0u, a0, a2, c0 = 0u, c2 = 0u;
-                const bool two = st + kConsumerWarps < nsteps;
-                if (two) {
-                  ldmatrix_x4(tb + b_off + 32u * st, b0, b1, b2, b3);
-                  ldmatrix_x4(a_ld + ak + 32u * st, a0, a2, c0, c2);
-                } else {
-                  ldmatrix_x2(tb + b_off2 + 32u * st, b0, b1);
-                  ldmatrix_x2(a_ld0 + ak + 32u * st, a0, a2);
-                }
-                if (!a_live) a0 = a2 = c0 = c2 = 0u;
-                if (i & 1) {
-                  mma_bf16_16816(acc2, a0, 0u, a2, 0u, b0, b1);
-                  if (two) mma_bf16_16816(acc3, c0, 0u, c2, 0u, b2, b3);
-                } else {
-                  mma_bf16_16816(acc0, a0, 0u, a2, 0u, b0, b1);
-                  if (two) mma_bf16_16816(acc1, c0, 0u, c2, 0u, b2, b3);
+              for (int q = 0; q < 4; ++q) {
+                const int st = st0 + q * kConsumerWarps;
+                if (st < nsteps) {
+                  uint32_t a0, a1, a2, a3, b0, b1;
+                  ldmatrix_x4(tb + a_off + 32u * st, a0, a1, a2, a3);
+                  ldmatrix_x2(bk + 32u * st, b0, b1);
+                  mma_bf16_16816(acc[q], a0, a1, a2, a3, b0, b1);
                 }
               }
             }
           }
         }
-        hold(acc0);
-        hold(acc1);
-        hold(acc2);
-        hold(acc3);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) hold(acc[q]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[pipe.stage]);
         pipe.advance();
       }
-      const float s0 = (acc0[0] + acc1[0]) + (acc2[0] + acc3[0]);
-      const float s1 = (acc0[1] + acc1[1]) + (acc2[1] + acc3[1]);
-      // rows 2c (hi) and 2c+1 (lo) of D: lanes 8c..8c+3 and 8c+4..8c+7, columns n = 2(lane&3), +1
-      const float o0 = __shfl_down_sync(0xffffffffu, s0, 4);
-      const float o1 = __shfl_down_sync(0xffffffffu, s1, 4);
-      if (a_live && (lane & 4) == 0) {
-        const int c = lane >> 3, n0 = 2 * (lane & 3);
-        if (n0 < rows) sts32f(red + 4u * ((((b + n0) * nmat + m) * NC + c) * kConsumerWarps + warp), s0 + o0);
-        if (n0 + 1 < rows)
-          sts32f(red + 4u * ((((b + n0 + 1) * nmat + m) * NC + c) * kConsumerWarps + warp), s1 + o1);
+      // column pair (2t, 2t + 1) = (hi, lo) of activation column t: rows g and g + 8
+      if (t < NC) {
+        const float v0 = ((acc[0][0] + acc[1][0]) + (acc[2][0] + acc[3][0])) +
+                         ((acc[0][1] + acc[1][1]) + (acc[2][1] + acc[3][1]));
+        const float v1 = ((acc[0][2] + acc[1][2]) + (acc[2][2] + acc[3][2])) +
+                         ((acc[0][3] + acc[1][3]) + (acc[2][3] + acc[3][3]));
+        if (g < rows) sts32f(red + 4u * ((((b + g) * nmat + m) * NC + t) * kConsumerWarps + warp), v0);
+        if (g + 8 < rows) sts32f(red + 4u * ((((b + g + 8) * nmat + m) * NC + t) * kConsumerWarps + warp), v1);
       }
     }
   }

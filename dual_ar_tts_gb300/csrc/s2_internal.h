@@ -23,8 +23,8 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumers + 32;      // + one producer warp
 constexpr int kStages = 4;                     // weight ring depth
-constexpr int kStageBytes = 41088;             // one tile: 8 row segments of <= 2560 bf16 (+16 B pad each)
-constexpr int kTileRows = 8;                   // rows per bf16 weight tile (the MMA n dimension)
+constexpr int kStageBytes = 41216;             // one tile: 16 row segments of <= 1280 bf16 (+16 B pad each)
+constexpr int kTileRows = 16;                  // rows per bf16 weight tile (the MMA m dimension)
 constexpr int kTileRowPad = 16;                // bytes added to each tile row (bank-conflict-free ldmatrix)
 constexpr int kXsBytes = 40960;                // shared activations: padded bf16 hi/lo rows of 1 column x <= 10232 (2 x <= 5112)
 constexpr int kRedFloats = 2048;               // per-CTA partial sums (GEMV row × K-slice)
