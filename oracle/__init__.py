@@ -78,6 +78,7 @@ def _load():
                 "or_embed": (None, [vp, vp, vp]),
                 "or_prefill": (i32, [vp, vp, i32, vp, vp]),
                 "or_step": (i32, [vp, vp, vp, vp]),
+                "or_extend": (i32, [vp, vp, i32, vp, vp]),
                 "or_fast_forward": (i32, [vp, vp, vp, i32, vp, vp]),
                 "or_kv_io": (i32, [vp, i32, i32, i32, vp, vp, i32]),
                 "or_draw": (i32, [vp, vp, i32, f32, f32, i32, vp, vp]),
@@ -246,6 +247,24 @@ class Session:
         rc = _load().or_prefill(self._h, t.ctypes.data, t.shape[0], logits.ctypes.data, hidden.ctypes.data)
         if rc:
             raise ValueError(f"oracle prefill failed ({rc})")
+        return logits, hidden
+
+    def extend(self, tokens):
+        """More prompt positions after those already in the cache (a prompt run in pieces)."""
+        t = _i32(tokens)
+        logits = np.empty(self.d["vocab"], np.float32)
+        hidden = np.empty(self.d["dim"], np.float32)
+        rc = _load().or_extend(self._h, t.ctypes.data, t.shape[0], logits.ctypes.data, hidden.ctypes.data)
+        if rc:
+            raise ValueError(f"oracle extend failed ({rc})")
+        return logits, hidden
+
+    def prefill_chunked(self, tokens, chunk=256):
+        """Prefill in pieces of `chunk` positions (the same result as one prefill)."""
+        t = _i32(tokens)
+        logits, hidden = self.prefill(t[:chunk])
+        for a in range(chunk, t.shape[0], chunk):
+            logits, hidden = self.extend(t[a:a + chunk])
         return logits, hidden
 
     def step(self, vals):

@@ -446,6 +446,14 @@ int or_prefill(or_sess* s, const int32_t* tokens, int T, float* logits, float* h
   return slow_forward(s, tokens, T, logits, hidden);
 }
 
+/* Further prompt positions after the ones already in the cache: a prompt run in consecutive
+ * pieces (causal attention over every earlier slot, [ch02] §3.1) gives what one prefill of the
+ * whole prompt gives, with a small working set per piece.  Logits and hidden of the last
+ * position come back. */
+int or_extend(or_sess* s, const int32_t* tokens, int n, float* logits, float* hidden) {
+  return slow_forward(s, tokens, n, logits, hidden);
+}
+
 /* One Slow-AR step on the 11 values [main_token, code_0..code_9] ([ch02] §3.4). */
 int or_step(or_sess* s, const int32_t* vals, float* logits, float* hidden) {
   return slow_forward(s, vals, 1, logits, hidden);

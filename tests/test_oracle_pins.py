@@ -456,6 +456,22 @@ def test_incremental_step_equals_longer_prefill():
     np.testing.assert_allclose(ka, kb, rtol=1e-5, atol=1e-6)
 
 
+def test_prompt_in_pieces_equals_one_prefill():
+    # causal attention over every earlier slot: running the prompt in pieces changes nothing
+    d = TINY
+    w = _tiny_weights(jitter=0.1)
+    p = synth.prompt("tiny")
+    a = oracle.Session(d, w, 40)
+    la, ha = a.prefill(p)
+    b = oracle.Session(d, w, 40)
+    lb, hb = b.prefill_chunked(p, chunk=7)
+    np.testing.assert_allclose(lb, la, rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(hb, ha, rtol=1e-5, atol=1e-6)
+    assert b.pos == a.pos == len(p)
+    for layer in (0, d["n_layer"] - 1):
+        np.testing.assert_allclose(b.kv(layer, 0, len(p))[0], a.kv(layer, 0, len(p))[0], rtol=1e-5, atol=1e-6)
+
+
 def test_fast_prefix_consistency():
     d = TINY
     w = _tiny_weights(jitter=0.1)
