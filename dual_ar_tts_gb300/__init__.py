@@ -367,7 +367,7 @@ def upload_weights(host_weights, device="cuda"):
     return out
 
 
-def serve(decoder, requests, slots, frames_per_call, sampling, expo_fn):
+def serve(decoder, requests, slots, frames_per_call, sampling, expo_fn, forced_fn=None):
     """Continuous batching over the decoder's stream slots.
 
     requests: list of (prompt [T][NCB+1] int32, n_frames).  A request holds a slot from its prefill
@@ -375,7 +375,9 @@ def serve(decoder, requests, slots, frames_per_call, sampling, expo_fn):
     request.  The active slots are decoded together (one weight read per step) in calls of at most
     frames_per_call frames, cut so that no request overshoots.  expo_fn(request, first_frame, n)
     returns that request's exponential variates [n][11][30] (float32), so a request sees the same
-    variates whatever the batch around it.  Returns, per request, its codes [NCB][frames] (int32).
+    variates whatever the batch around it.  forced_fn(request, first_frame, n), when given, returns
+    that request's forced draws [n][11] (int32; teacher forcing, as in s2_decode_frames).  Returns,
+    per request, its codes [NCB][frames] (int32).
     """
     import collections
     import numpy as np
@@ -393,7 +395,11 @@ def serve(decoder, requests, slots, frames_per_call, sampling, expo_fn):
         ids = sorted(active)
         n = min(frames_per_call, min(requests[active[k][0]][1] - active[k][1] for k in ids))
         expo = torch.from_numpy(np.stack([expo_fn(active[k][0], active[k][1], n) for k in ids])).cuda()
-        out = decoder.decode(n, sampling, expo, stream_ids=ids)
+        if forced_fn is not None:
+            forced = torch.from_numpy(np.stack([forced_fn(active[k][0], active[k][1], n) for k in ids])).cuda()
+            out = decoder.decode(n, sampling, expo, forced=forced, stream_ids=ids)
+        else:
+            out = decoder.decode(n, sampling, expo, stream_ids=ids)
         n_out = out["n_out"].cpu().numpy()
         codes = out["codes"].cpu().numpy()
         for j, k in enumerate(ids):

@@ -2,9 +2,10 @@
 
 * Fast-AR alone: 1000 teacher-forced frames x 9 windows on the GPU; the oracle recomputes each
   window from scratch (no prefix cache) on a sample of frames; logits max-abs-rel <= 2e-2.
-* Full frame, batch 1: the 512-position prompt, then frames teacher-forced with the oracle's own
-  draws; Slow-AR logits (admissible ids), hidden state and every Fast-AR logit vector compared at
-  max-abs-rel <= 2e-2, pinned draws and all emitted codes compared exactly.
+* Full frame, batch 1: the 512-position prompt, then 40 frames teacher-forced with the oracle's
+  own draws (past min_tokens_before_end = 32, where im_end becomes drawable); Slow-AR logits
+  (admissible ids), hidden state and every Fast-AR logit vector compared at max-abs-rel <= 2e-2,
+  pinned draws and all emitted codes compared exactly.
 * Full frame at its bench length (256 frames, free running): properties that hold at any size —
   every frame produced, codes in range, identical codes on a second run from the same state.
 """
@@ -54,7 +55,7 @@ def test_full_frame_prefill_and_frames_match_oracle(s2pro):
     import dual_ar_tts_gb300 as pkg
     d, host, dev, names = s2pro
     cfg = synth.CONFIGS["frame"]
-    n_frames = 3
+    n_frames = 40
     prompt = synth.prompt("frame")
     s = synth.sampling("frame")
     expo = synth.expo(cfg["input_seed"], 0, n_frames)
