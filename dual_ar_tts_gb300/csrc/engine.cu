@@ -42,6 +42,7 @@ struct s2_ctx {
   unsigned long long* trace = nullptr;  // caller-owned device buffer (tracing hook)
   int trace_cap = 0;
   unsigned gbar_base = 0;          // grid-barrier counter start (test hook)
+  unsigned tag_next = 1;           // tag counter of the tagged handoffs (per launch: take_tags)
   std::vector<int> host_pos;
   std::vector<char> host_prefilled;
   std::string err;
@@ -82,8 +83,9 @@ bool planes_inside(const Phase* prog, size_t n, const void* base, size_t bytes, 
     const Phase& p = prog[i];
     if (p.op == OP_GEMV) {
       for (int c = 0; c < p.ncols; ++c) {
-        if (p.col[c].src == SRC_PLANES && !in(p.col[c].p, 4ull * p.K)) return (why = "planes input outside the workspace", false);
-        if (p.yp[c] != nullptr && !in(p.yp[c], 4ull * p.M)) return (why = "planes output outside the workspace", false);
+        const size_t in_b = (p.col[c].tag_back > 0 ? 8ull : 4ull) * p.K, out_b = (p.tag_out ? 8ull : 4ull) * p.M;
+        if (p.col[c].src == SRC_PLANES && !in(p.col[c].p, in_b)) return (why = "planes input outside the workspace", false);
+        if (p.yp[c] != nullptr && !in(p.yp[c], out_b)) return (why = "planes output outside the workspace", false);
       }
     }
     if ((p.op == OP_ATTN_SLOW || p.op == OP_ATTN_FAST) && p.outp != nullptr &&
@@ -235,18 +237,18 @@ void carve(s2_ctx* c, Carver& cv) {
   c->kc = cv.take<unsigned char>(kv);
   c->vc = cv.take<unsigned char>(kv);
   c->stage = cv.take<int32_t>(static_cast<size_t>(B) * kMaxFramesPerCall * d.ncb);
-  c->x = cv.take<float>(d.D);
+  c->x = cv.take<float>(2 * static_cast<size_t>(d.D));  // tagged words (bf16 models)
   c->qkv = cv.take<float>(std::max(QKV, 1));
   c->o = cv.take<float>(std::max(d.Hq * d.hd, 1));
   c->g = cv.take<float>(std::max(d.F, 1));
-  c->fx = cv.take<float>(static_cast<size_t>(d.Wf) * d.Df);
+  c->fx = cv.take<float>(2 * static_cast<size_t>(d.Wf) * d.Df);
   c->fqkv = cv.take<float>(2 * static_cast<size_t>(QKVf));
   c->fo = cv.take<float>(2 * static_cast<size_t>(d.Hqf) * d.hdf);
   c->fg = cv.take<float>(2 * static_cast<size_t>(d.Ff));
   c->op = cv.take<uint16_t>(2 * static_cast<size_t>(std::max(d.Hq * d.hd, 1)));
-  c->gp = cv.take<uint16_t>(2 * static_cast<size_t>(std::max(d.F, 1)));
+  c->gp = cv.take<uint16_t>(4 * static_cast<size_t>(std::max(d.F, 1)));
   c->fop = cv.take<uint16_t>(4 * static_cast<size_t>(d.Hqf) * d.hdf);
-  c->fgp = cv.take<uint16_t>(4 * static_cast<size_t>(d.Ff));
+  c->fgp = cv.take<uint16_t>(8 * static_cast<size_t>(d.Ff));
   c->fk = cv.take<float>(static_cast<size_t>(d.Lf) * d.Wf * d.Hkvf * d.hdf);
   c->fv = cv.take<float>(static_cast<size_t>(d.Lf) * d.Wf * d.Hkvf * d.hdf);
   c->flogits = cv.take<float>(d.cbs);
@@ -311,6 +313,16 @@ void carve(s2_ctx* c, Carver& cv) {
 
 // ------------------------------------------------------------ phase builders
 
+// Base tag of a launch of `count` phases from a running counter: tags are never 0 (the value the
+// tagged buffers are cleared to), and a launch's tags do not wrap around 2^32.
+unsigned take_tags(unsigned& ctr, long long count) {
+  if (ctr == 0u || static_cast<unsigned long long>(ctr) + static_cast<unsigned long long>(count) + 1ull > 0xffffffffull)
+    ctr = 1u;
+  const unsigned t = ctr;
+  ctr += static_cast<unsigned>(count) + 1u;
+  return t;
+}
+
 // The buffers the Fast-AR phases read and write: a context's workspace regions or the static
 // array's (s2_fast_logits_static).
 struct FastBufs {
@@ -335,6 +347,67 @@ struct Builder {
   int cap;
   int n = 0;
   std::string err;
+  // tagged buffers (bf16 models: the residual rows and the SwiGLU planes) and the index of the
+  // phase that last wrote each of them in the program being built
+  std::vector<std::pair<const unsigned char*, size_t>> tagged_ranges;
+  std::vector<std::pair<const void*, int>> last_write;
+
+  bool tagged() const { return d.wdt == S2_BF16; }
+  int xw() const { return tagged() ? 2 : 1; }  // floats per residual element
+  int pw() const { return tagged() ? 4 : 2; }  // 16-bit units per planes element
+  void add_tagged(const void* p, size_t bytes) {
+    if (tagged()) tagged_ranges.emplace_back(static_cast<const unsigned char*>(p), bytes);
+  }
+  bool is_tagged(const void* p) const {
+    const unsigned char* q = static_cast<const unsigned char*>(p);
+    for (const auto& r : tagged_ranges)
+      if (q >= r.first && q < r.first + r.second) return true;
+    return false;
+  }
+  void new_program() { last_write.clear(); }
+  int* lw(const void* p) {
+    for (auto& e : last_write)
+      if (e.first == p) return &e.second;
+    return nullptr;
+  }
+  void wrote(const void* p) {
+    if (int* w = lw(p)) *w = n;
+    else last_write.emplace_back(p, n);
+  }
+  // tagged inputs take the distance to their writer; tagged outputs and write-backs are recorded;
+  // the residual-add and SwiGLU projections hand over without a grid barrier
+  void tag(Phase& p) {
+    if (!tagged() || p.op != OP_GEMV) return;
+    for (int c = 0; c < p.ncols; ++c) {
+      const GemvCol& col = p.col[c];
+      if ((col.src == SRC_BUF || col.src == SRC_PLANES) && is_tagged(col.p)) {
+        const int* w = lw(col.p);
+        if (!w) {
+          err = "internal: a tagged input is read before it is written";
+          continue;
+        }
+        p.col[c].tag_back = n - *w;
+      }
+    }
+    bool any_t = false, any_u = false;
+    for (int c = 0; c < p.ncols; ++c) {
+      for (const void* o : {static_cast<const void*>(p.y[c]), static_cast<const void*>(p.yp[c])}) {
+        if (!o) continue;
+        (is_tagged(o) ? any_t : any_u) = true;
+      }
+    }
+    if (any_t && any_u) err = "internal: a phase mixes tagged and plain outputs";
+    p.tag_out = any_t ? 1 : 0;
+    p.no_sync = (any_t && (p.epi == EPI_ADD || p.epi == EPI_SWIGLU)) ? 1 : 0;
+    for (int c = 0; c < p.ncols; ++c) {
+      if (p.y[c] && any_t) wrote(p.y[c]);
+      if (p.yp[c] && any_t) wrote(p.yp[c]);
+      if (p.col[c].wb) {
+        if (!is_tagged(p.col[c].wb)) err = "internal: a column write-back outside the tagged buffers";
+        wrote(p.col[c].wb);
+      }
+    }
+  }
 
   Phase gemv(int M, int K, int ncols, const void* w0, const void* w1, const void* normw, int epi) {
     Phase p{};
@@ -368,7 +441,8 @@ struct Builder {
     }
     return p;
   }
-  void push(const Phase& p) {
+  void push(Phase p) {
+    tag(p);
     const int g2 = grid - p.cta0;
     if (p.op == OP_GEMV && p.ncols == 2 && (p.col[0].src == SRC_PLANES) != (p.col[1].src == SRC_PLANES))
       err = "internal: a phase mixes planes and other activation sources";
@@ -400,7 +474,7 @@ struct Builder {
         Phase q = gemv(QKVf, d.Df, npos, lw.wqkv, nullptr, lw.an, EPI_STORE);
         for (int j = 0; j < npos; ++j) {
           const int p = pos0 + j;
-          float* xp = b.fx + static_cast<size_t>(p) * d.Df;
+          float* xp = b.fx + static_cast<size_t>(p) * d.Df * xw();
           if (l == 0 && p >= 1) q.col[j] = GemvCol{SRC_FEROW, 0, b.fcode + (p - 1), xp};
           else if (l == 0 && p == 0 && !d.has_proj) q.col[j] = buf(b.hidden_src, xp);
           else q.col[j] = buf(xp);
@@ -425,13 +499,13 @@ struct Builder {
         for (int j = 0; j < npos; ++j) {
           o.col[j] = use_planes() ? planes(b.fop + static_cast<size_t>(j) * 2 * d.Hqf * d.hdf)
                                   : buf(b.fo + static_cast<size_t>(j) * d.Hqf * d.hdf);
-          o.y[j] = b.fx + static_cast<size_t>(pos0 + j) * d.Df;
+          o.y[j] = b.fx + static_cast<size_t>(pos0 + j) * d.Df * xw();
         }
         push(o);
         Phase u = gemv(d.Ff, d.Df, npos, lw.w1, lw.w3, lw.fn, EPI_SWIGLU);
         for (int j = 0; j < npos; ++j) {
-          u.col[j] = buf(b.fx + static_cast<size_t>(pos0 + j) * d.Df);
-          if (use_planes()) u.yp[j] = b.fgp + static_cast<size_t>(j) * 2 * d.Ff;
+          u.col[j] = buf(b.fx + static_cast<size_t>(pos0 + j) * d.Df * xw());
+          if (use_planes()) u.yp[j] = b.fgp + static_cast<size_t>(j) * d.Ff * pw();
           else u.y[j] = b.fg + static_cast<size_t>(j) * d.Ff;
         }
         push(u);
@@ -442,15 +516,15 @@ struct Builder {
           Phase dn = gemv(d.Df, d.Ff, nc, lw.w2, nullptr, nullptr, EPI_ADD);
           for (int j = 0; j < nc; ++j) {
             const int jj = ndown == 1 ? j : t;
-            dn.col[j] = use_planes() ? planes(b.fgp + static_cast<size_t>(jj) * 2 * d.Ff)
+            dn.col[j] = use_planes() ? planes(b.fgp + static_cast<size_t>(jj) * d.Ff * pw())
                                      : buf(b.fg + static_cast<size_t>(jj) * d.Ff);
-            dn.y[j] = b.fx + static_cast<size_t>(pos0 + jj) * d.Df;
+            dn.y[j] = b.fx + static_cast<size_t>(pos0 + jj) * d.Df * xw();
           }
           push(dn);
         }
       }
       Phase fo = gemv(d.cbs, d.Df, 1, w.FO, nullptr, w.fnorm, EPI_STORE);
-      fo.col[0] = buf(b.fx + static_cast<size_t>(cb) * d.Df);
+      fo.col[0] = buf(b.fx + static_cast<size_t>(cb) * d.Df * xw());
       fo.y[0] = b.flogits;
       push(fo);
       Phase s{};
@@ -463,6 +537,7 @@ struct Builder {
   // The Fast-AR-alone program (teacher-forced frames): the frame's hidden and first prefix code
   // (CTA 0), its projection into position 0, then the calls
   void fast_alone(const FastBufs& b, const FastWts& w) {
+    new_program();
     Phase fi{};
     fi.op = OP_FAST_IN;
     push(fi);
@@ -544,9 +619,14 @@ int build_programs(s2_ctx* c) {
   const size_t total = static_cast<size_t>(c->max_streams) * c->n_dec + c->n_fast;
   std::vector<Phase> all(total);
   Builder b{d, c->grid, all.data(), static_cast<int>(total)};
+  b.add_tagged(c->x, 8ull * d.D);
+  b.add_tagged(c->fx, 8ull * d.Wf * d.Df);
+  b.add_tagged(c->gp, 8ull * std::max(d.F, 1));
+  b.add_tagged(c->fgp, 16ull * d.Ff);
   const FastWts fw{c->fast.data(), c->P, c->FO, c->fnorm};
   for (int sid = 0; sid < c->max_streams && d.L > 0; ++sid) {
     const int before = b.n;
+    b.new_program();
     float* hid = c->hidden + static_cast<size_t>(sid) * d.D;
     float* lg = c->logits + static_cast<size_t>(sid) * logits_stride(d);
     // 1. main draw on CTA 0 while the other CTAs project the hidden state into Fast-AR position 0
@@ -721,7 +801,10 @@ int s2_frame_init(const s2_dims* s, const void* const* weights, int n_weights, v
   Control ctl{};
   ctl.spin_limit = 2000000;
   if (cudaMemcpy(c->ctl, &ctl, sizeof(Control), cudaMemcpyHostToDevice) != cudaSuccess ||
-      cudaMemset(c->st, 0, sizeof(StreamState) * (max_streams + 1)) != cudaSuccess) {
+      cudaMemset(c->st, 0, sizeof(StreamState) * (max_streams + 1)) != cudaSuccess ||
+      // the tagged buffers start with tag 0, which no phase uses
+      cudaMemset(c->x, 0, 8ull * d.D) != cudaSuccess || cudaMemset(c->fx, 0, 8ull * d.Wf * d.Df) != cudaSuccess ||
+      cudaMemset(c->gp, 0, 8ull * std::max(d.F, 1)) != cudaSuccess || cudaMemset(c->fgp, 0, 16ull * d.Ff) != cudaSuccess) {
     delete c;
     return fail(nullptr, S2_ECUDA, "initialising the workspace failed");
   }
@@ -917,6 +1000,7 @@ int s2_decode_frames(s2_ctx* c, int n, const int* ids, int n_frames, const s2_sa
     cp.n_frames = n_frames;
     cp.fast_only = 0;
     cp.n_phases = c->n_dec;
+    cp.tag0 = take_tags(c->tag_next, static_cast<long long>(n_frames) * c->n_dec);
     cp.stream = sid;
     cp.prog = c->prog + static_cast<size_t>(sid) * c->n_dec;
     cp.st = c->st + sid;
@@ -986,6 +1070,7 @@ int s2_fast_logits(s2_ctx* c, int n_frames, const float* hidden, const int32_t* 
   cp.n_frames = n_frames;
   cp.fast_only = 1;
   cp.n_phases = c->n_fast;
+  cp.tag0 = take_tags(c->tag_next, static_cast<long long>(n_frames) * c->n_fast);
   cp.prog = c->prog + static_cast<size_t>(c->max_streams) * c->n_dec;
   cp.st = c->st + c->max_streams;
   cp.hidden = c->hidden + static_cast<size_t>(c->max_streams) * d.D;
@@ -1078,6 +1163,7 @@ struct StaticDevice {
   int grid = 0;                      // frame kernel grid (one CTA per SM)
   // the program and RoPE table in the array were built for this shape and weight table
   bool have_prog = false;
+  unsigned tag_next = 1;             // tag counter of the tagged handoffs on this device
   Dims d{};
   int n_weights = 0;
   const void* w[kStaticMaxWeights] = {};
@@ -1105,7 +1191,7 @@ size_t carve_static(const Dims& d, int n_phases, unsigned char* base, StaticLayo
   s.st = cv.take<StreamState>(1);
   FastBufs& b = s.fb;
   b.hidden_src = cv.take<float>(d.D);
-  b.fx = cv.take<float>(static_cast<size_t>(d.Wf) * d.Df);
+  b.fx = cv.take<float>(2 * static_cast<size_t>(d.Wf) * d.Df);
   b.fqkv = cv.take<float>(2 * static_cast<size_t>(QKVf));
   b.fo = cv.take<float>(2 * static_cast<size_t>(d.Hqf) * d.hdf);
   b.fg = cv.take<float>(2 * static_cast<size_t>(d.Ff));
@@ -1113,7 +1199,7 @@ size_t carve_static(const Dims& d, int n_phases, unsigned char* base, StaticLayo
   b.fv = cv.take<float>(static_cast<size_t>(d.Lf) * d.Wf * d.Hkvf * d.hdf);
   b.flogits = cv.take<float>(d.cbs);
   b.fop = cv.take<uint16_t>(4 * static_cast<size_t>(d.Hqf) * d.hdf);
-  b.fgp = cv.take<uint16_t>(4 * static_cast<size_t>(d.Ff));
+  b.fgp = cv.take<uint16_t>(8 * static_cast<size_t>(d.Ff));
   b.fcode = cv.take<int32_t>(16);
   s.prog = cv.take<Phase>(static_cast<size_t>(n_phases));
   return align_up(cv.off, 256);
@@ -1196,11 +1282,16 @@ extern "C" int s2_fast_logits_static(const s2_dims* s, const void* const* weight
       g_static_layers[l] = LayerW{lw[0], lw[1], lw[2], lw[3], lw[4], lw[5], lw[6], lw[7], lw[8]};
     }
     Builder b{d, sd.grid, g_static_prog, kStaticMaxPhases};
+    b.add_tagged(sl.fb.fx, 8ull * d.Wf * d.Df);
+    b.add_tagged(sl.fb.fgp, 16ull * d.Ff);
     b.fast_alone(sl.fb, FastWts{g_static_layers, weights[base], weights[base + 3], weights[base + 2]});
     if (!b.err.empty()) return static_fail(S2_EINVAL, b.err);
     if (b.n != n_phases) return static_fail(S2_EINVAL, "internal: Fast-AR program length");
     if (!planes_inside(g_static_prog, static_cast<size_t>(b.n), sd.scratch, kStaticScratchBytes, why))
       return static_fail(S2_EINVAL, "internal: " + why);
+    // the scratch starts from zero (the tagged buffers' tag 0 is used by no phase)
+    if (cudaMemsetAsync(sd.scratch, 0, need, cs) != cudaSuccess)
+      return static_fail(S2_ECUDA, "clearing the static scratch failed");
     if (cudaMemcpyAsync(sl.prog, g_static_prog, sizeof(Phase) * n_phases, cudaMemcpyHostToDevice, cs) != cudaSuccess)
       return static_fail(S2_ECUDA, "copying the program failed");
     if (build_rope_tables(nullptr, 0, d.hd, sl.rope_f, d.Wf, d.hdf, d.rope_base, d.rope_bf16, cs) != S2_OK)
@@ -1223,6 +1314,7 @@ extern "C" int s2_fast_logits_static(const s2_dims* s, const void* const* weight
   cp.n_frames = n_frames;
   cp.fast_only = 1;
   cp.n_phases = n_phases;
+  cp.tag0 = take_tags(sd.tag_next, static_cast<long long>(n_frames) * n_phases);
   cp.prog = sl.prog;
   cp.st = sl.st;
   cp.hidden = sl.fb.hidden_src;

@@ -76,6 +76,7 @@ struct Pipe {
   int stage;
   uint32_t round;
   uint32_t xs_uses;  // completed uses of the xs barrier (its phase parity)
+  uint32_t tag;      // tag of the phase being run (tagged handoffs, bf16 models)
   __device__ void advance() {
     if (++stage == kStages) {
       stage = 0;
@@ -211,6 +212,50 @@ __device__ __noinline__ void drain_copies(const CallParams& cp, uint64_t* bar, u
   }
 }
 
+// ---------------------------------------------------------------- tagged handoffs
+// A tagged word holds a 32-bit value and, above it, the tag of the phase that stored it.  An
+// aligned 8-byte store is single-copy atomic, so a reader that sees the tag it expects also sees
+// that phase's value; it polls the words (L2, bypassing L1) instead of waiting at a grid barrier.
+__device__ __forceinline__ unsigned long long tagw(uint32_t bits, uint32_t tag) {
+  return (static_cast<unsigned long long>(tag) << 32) | bits;
+}
+__device__ __forceinline__ ulonglong2 ldcg_u64x2(const unsigned long long* p) {
+  return __ldcg(reinterpret_cast<const ulonglong2*>(p));
+}
+__device__ __forceinline__ bool tags_are(const ulonglong2& a, uint32_t tag) {
+  return static_cast<uint32_t>(a.x >> 32) == tag && static_cast<uint32_t>(a.y >> 32) == tag;
+}
+__device__ __forceinline__ float tval(unsigned long long w) { return __uint_as_float(static_cast<uint32_t>(w)); }
+
+// Waits, bounded, until the pairs of tagged words at p[2i], p[2i + 1] (i in `miss`, a mask) carry
+// `tag`; returns their values in v.  A give-up records S2_ETIMEOUT (site 8) and the CTA's failure.
+template <int N>
+__device__ __noinline__ void wait_tagged(const CallParams& cp, Smem& S, const unsigned long long* const (&p)[N],
+                                         uint32_t tag, uint32_t miss, ulonglong2 (&v)[N]) {
+  const long long t0 = clock_us();
+  for (unsigned it = 1; miss != 0u; ++it) {
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if (miss & (1u << i)) {
+        v[i] = ldcg_u64x2(p[i]);
+        if (tags_are(v[i], tag)) miss &= ~(1u << i);
+      }
+    if (miss != 0u && (it & 15u) == 0u) {
+      if (ld_volatile_int(&cp.ctl->error) != 0 || *reinterpret_cast<volatile int*>(&S.fail) != 0) break;
+      if (clock_us() - t0 > cp.ctl->spin_limit) {
+        if (atomicCAS(&cp.ctl->error, 0, S2_ETIMEOUT) == 0) cp.ctl->error_where = 8;
+        break;
+      }
+    }
+  }
+  if (miss != 0u) S.fail = 1;
+}
+
+// an output row of the phase's column c (read back for a residual add): tagged word or float
+__device__ __forceinline__ float ld_out(const Phase& ph, int c, int row) {
+  return ph.tag_out ? tval(__ldcg(reinterpret_cast<const unsigned long long*>(ph.y[c]) + row)) : ldcg(ph.y[c] + row);
+}
+
 // =========================================================================
 // producer
 // =========================================================================
@@ -233,7 +278,7 @@ __device__ void producer(const CallParams& cp, Smem& S) {
   const int lane = threadIdx.x & 31;
   constexpr int NQ = static_cast<int>(sizeof(Phase) / 16);
   const uint64_t pol = policy_evict_first();
-  Pipe pp{0, 0, 0};
+  Pipe pp{0, 0, 0, 0u};
   unsigned long long issued = 0;  // stages filled so far (all lanes keep the same count)
   int stop = (ld_volatile_int(&cp.st->done) != 0 && !cp.fast_only) ? 1 : 0;
   if (lane < NQ) reinterpret_cast<uint4*>(&S.pph[0])[lane] = __ldg(reinterpret_cast<const uint4*>(cp.prog) + lane);
@@ -618,7 +663,7 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
   int r0, nr;
   rows_of(ph, blockIdx.x, gridDim.x, r0, nr);
   float yres = 0.f;
-  if (ph.epi == EPI_ADD && tid < nr * NC) yres = ldcg(ph.y[tid % NC] + r0 + tid / NC);
+  if (ph.epi == EPI_ADD && tid < nr * NC) yres = ld_out(ph, tid % NC, r0 + tid / NC);
 
   // ---- activation columns into registers: thread tid holds elements 4·(tid + 256 j) .. +3
   static_assert(GM * 4 * kConsumers * NC <= 10240, "activation registers");
@@ -629,7 +674,32 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
   for (int c = 0; c < NC; ++c) {
     const GemvCol col = ph.col[c];
     const int* vals = static_cast<const int*>(col.p);
-    if (col.src == SRC_BUF) {
+    if (col.src == SRC_BUF && col.tag_back > 0) {
+      // tagged words written `tag_back` phases ago: every load first, then the (rare) wait
+      const unsigned long long* src = static_cast<const unsigned long long*>(col.p);
+      const uint32_t want = pipe.tag - static_cast<uint32_t>(col.tag_back);
+      const unsigned long long* ptr[2 * GM];
+      ulonglong2 w[2 * GM];
+      uint32_t miss = 0u;
+#pragma unroll
+      for (int j = 0; j < GM; ++j) {
+        const int g = min(tid + kConsumers * j, ng - 1);
+        ptr[2 * j] = src + 4 * g;
+        ptr[2 * j + 1] = src + 4 * g + 2;
+        w[2 * j] = ldcg_u64x2(ptr[2 * j]);
+        w[2 * j + 1] = ldcg_u64x2(ptr[2 * j + 1]);
+      }
+#pragma unroll
+      for (int i = 0; i < 2 * GM; ++i)
+        if (!tags_are(w[i], want)) miss |= 1u << i;
+      if (miss != 0u) wait_tagged<2 * GM>(cp, S, ptr, want, miss, w);
+#pragma unroll
+      for (int j = 0; j < GM; ++j) {
+        const int g = tid + kConsumers * j;
+        xv[c][j] = g < ng ? make_float4(tval(w[2 * j].x), tval(w[2 * j].y), tval(w[2 * j + 1].x), tval(w[2 * j + 1].y))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    } else if (col.src == SRC_BUF) {
       const float* src = static_cast<const float*>(col.p);
 #pragma unroll
       for (int j = 0; j < GM; ++j) {
@@ -686,14 +756,21 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
     }
   }
   if (blockIdx.x == 0) {
+    // the raw column written back to its residual row (tagged words with this phase's tag)
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
-      float* wb = ph.col[c].wb;
+      unsigned long long* wb = reinterpret_cast<unsigned long long*>(ph.col[c].wb);
       if (wb == nullptr) continue;
 #pragma unroll
       for (int j = 0; j < GM; ++j) {
         const int g = tid + kConsumers * j;
-        if (g < ng) *reinterpret_cast<float4*>(wb + 4 * g) = xv[c][j];
+        if (g < ng) {
+          const float4 v = xv[c][j];
+          *reinterpret_cast<ulonglong2*>(wb + 4 * g) =
+              make_ulonglong2(tagw(__float_as_uint(v.x), pipe.tag), tagw(__float_as_uint(v.y), pipe.tag));
+          *reinterpret_cast<ulonglong2*>(wb + 4 * g + 2) =
+              make_ulonglong2(tagw(__float_as_uint(v.z), pipe.tag), tagw(__float_as_uint(v.w), pipe.tag));
+        }
       }
     }
   }
@@ -799,6 +876,43 @@ __device__ __noinline__ void gemv_tiles(const CallParams& cp, const Phase& ph, S
     const uint32_t a_off = static_cast<uint32_t>(min((lane & 7) + 8 * ((lane >> 3) & 1), rows - 1)) * pitch +
                            static_cast<uint32_t>(lane >> 4) * 16u;
     for (int m = 0; m < nmat; ++m) {
+      if (rows == 1 && nkt == 1) {
+        // a one-row last block (the rows of a CTA are 16·n + 1): CUDA-core dot products over the
+        // whole row (an MMA would use one of its 16 rows); each thread takes 8-element chunks
+        const bool ok = wait_bar(cp, S, &S.full[pipe.stage], pipe.round & 1u, 4, false);
+        if (!ok) S.fail = 1;
+        float dv[NC];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) dv[c] = 0.f;
+        if (ok) {
+          const uint32_t tb = order_after(smem_u32(S.ring[pipe.stage]));
+          const int nch = K >> 3;
+#pragma unroll 2
+          for (int ch = tid; ch < nch; ch += kConsumers) {
+            const uint4 w = lds128(tb + 16u * static_cast<uint32_t>(ch));
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+              const uint32_t xa = xsb + static_cast<uint32_t>(2 * c) * xpitch + 16u * static_cast<uint32_t>(ch);
+              const uint4 h = lds128(xa), l = lds128(xa + xpitch);
+              const uint32_t wq[4] = {w.x, w.y, w.z, w.w}, hq[4] = {h.x, h.y, h.z, h.w}, lq[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                dv[c] = fmaf(bf16lo(wq[q]), bf16lo(hq[q]) + bf16lo(lq[q]), dv[c]);
+                dv[c] = fmaf(bf16hi(wq[q]), bf16hi(hq[q]) + bf16hi(lq[q]), dv[c]);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[pipe.stage]);
+        pipe.advance();
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          const float v = warp_sum(dv[c]);
+          if (lane == 0) sts32f(red + 4u * ((((b * nmat + m) * NC + c) * kConsumerWarps) + warp), v);
+        }
+        continue;
+      }
       float acc[4][4];
 #pragma unroll
       for (int q = 0; q < 4; ++q)
@@ -865,12 +979,22 @@ __device__ __noinline__ void gemv_tiles(const CallParams& cp, const Phase& ph, S
       if (ph.epi == EPI_STORE) {
         v = a;
       } else if (ph.epi == EPI_ADD) {
-        v = (idx == tid ? yres : ldcg(ph.y[c] + r0 + rl)) + a;
+        v = (idx == tid ? yres : ld_out(ph, c, r0 + rl)) + a;
       } else {
         v = (a / (1.0f + expf(-a))) * bb;
       }
-      if (ph.y[c] != nullptr) ph.y[c][r0 + rl] = v;
-      if (ph.yp[c] != nullptr) store_planes(ph.yp[c], ph.M, r0 + rl, v);
+      if (ph.tag_out) {
+        // tagged words: the value, or the bf16 hi / lo pair of a planes output
+        if (ph.y[c] != nullptr)
+          reinterpret_cast<unsigned long long*>(ph.y[c])[r0 + rl] = tagw(__float_as_uint(v), pipe.tag);
+        if (ph.yp[c] != nullptr) {
+          const float hi = bf16lo(cvt_bf16x2(v, 0.f));
+          reinterpret_cast<unsigned long long*>(ph.yp[c])[r0 + rl] = tagw(cvt_bf16x2(hi, v - hi), pipe.tag);
+        }
+      } else {
+        if (ph.y[c] != nullptr) ph.y[c][r0 + rl] = v;
+        if (ph.yp[c] != nullptr) store_planes(ph.yp[c], ph.M, r0 + rl, v);
+      }
     }
   }
 }
@@ -884,8 +1008,49 @@ __device__ __noinline__ void gemv_planes(const CallParams& cp, const Phase& ph, 
   int r0, nr;
   rows_of(ph, blockIdx.x, gridDim.x, r0, nr);
   float yres = 0.f;
-  if (ph.epi == EPI_ADD && tid < nr * NC) yres = ldcg(ph.y[tid % NC] + r0 + tid / NC);
+  if (ph.epi == EPI_ADD && tid < nr * NC) yres = ld_out(ph, tid % NC, r0 + tid / NC);
   const uint32_t xpitch = 2u * static_cast<uint32_t>(K) + kTileRowPad;
+  if (ph.col[0].tag_back > 0) {
+    // tagged planes words (hi | lo << 16, then the tag), written tag_back phases ago: two rounds
+    // of loads per thread, unpacked into the hi and lo rows of xs
+    constexpr int B = 10;  // element pairs per thread and round
+    const uint32_t xsb = smem_u32(S.xs);
+    const int npairs = K / 2;
+#pragma unroll 1
+    for (int c = 0; c < NC; ++c) {
+      const unsigned long long* src = static_cast<const unsigned long long*>(ph.col[c].p);
+      const uint32_t want = pipe.tag - static_cast<uint32_t>(ph.col[c].tag_back);
+#pragma unroll 1
+      for (int base = tid; base < npairs; base += B * kConsumers) {
+        const unsigned long long* ptr[B];
+        ulonglong2 w[B];
+        uint32_t miss = 0u;
+#pragma unroll
+        for (int i = 0; i < B; ++i) {
+          ptr[i] = src + 2 * min(base + i * kConsumers, npairs - 1);
+          w[i] = ldcg_u64x2(ptr[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < B; ++i)
+          if (!tags_are(w[i], want)) miss |= 1u << i;
+        if (miss != 0u) wait_tagged<B>(cp, S, ptr, want, miss, w);
+#pragma unroll
+        for (int i = 0; i < B; ++i) {
+          const int q = base + i * kConsumers;
+          if (q < npairs) {
+            const uint32_t e0 = static_cast<uint32_t>(w[i].x), e1 = static_cast<uint32_t>(w[i].y);
+            const uint32_t hi2 = (e0 & 0xffffu) | (e1 << 16), lo2 = (e0 >> 16) | (e1 & 0xffff0000u);
+            const uint32_t a = xsb + static_cast<uint32_t>(2 * c) * xpitch + 4u * static_cast<uint32_t>(q);
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(hi2) : "memory");
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(a + xpitch), "r"(lo2) : "memory");
+          }
+        }
+      }
+    }
+    named_bar(1, kConsumers);
+    gemv_tiles<NC>(cp, ph, S, pipe, yres);
+    return;
+  }
   if (tid == 0) {
     // the previous users of xs (generic-proxy accesses, ordered before by the phase barrier) come
     // before these async-proxy writes
@@ -1490,7 +1655,7 @@ __device__ void fast_in(const CallParams& cp, int f) {
 
 template <class C>
 __device__ void consumers(const CallParams& cp, Smem& S) {
-  Pipe pipe{0, 0, 0};
+  Pipe pipe{0, 0, 0, 0u};
   unsigned target = cp.gbar_base;  // the host starts the counter there
   const bool cta0 = blockIdx.x == 0;
   const int tid = threadIdx.x;
@@ -1512,6 +1677,7 @@ __device__ void consumers(const CallParams& cp, Smem& S) {
       const bool has_next = (p + 1 < cp.n_phases) || (f + 1 < cp.n_frames);
       uint4 nx = make_uint4(0u, 0u, 0u, 0u);
       if (tid < NQ && has_next) nx = __ldg(reinterpret_cast<const uint4*>(cp.prog + np) + tid);
+      pipe.tag = cp.tag0 + static_cast<uint32_t>(k);
       switch (ph.op) {
         case OP_GEMV:
           if (ph.merge_main && cta0) sample_main(cp, S, f);
@@ -1539,7 +1705,13 @@ __device__ void consumers(const CallParams& cp, Smem& S) {
         cp.st->pos = cp.st->pos + 1;  // the Slow-AR step's last phase: its slot is now filled
       }
       if (tid < NQ && has_next) reinterpret_cast<uint4*>(&S.ph[(k + 1) & 1])[tid] = nx;
-      if (!grid_sync(cp, S, target)) return;
+      if (ph.no_sync) {
+        // the next phase polls this phase's tagged outputs: only this CTA's threads meet here
+        named_bar(1, kConsumers);
+        if (*reinterpret_cast<volatile int*>(&S.fail) != 0) return;
+      } else if (!grid_sync(cp, S, target)) {
+        return;
+      }
       if (cp.trace != nullptr && cta0 && tid == 0) {
         const int kk = f * cp.n_phases + p;
         if (kk < cp.trace_cap) cp.trace[kk] = globaltimer_ns();

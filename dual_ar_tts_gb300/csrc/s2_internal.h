@@ -97,7 +97,7 @@ struct Control {
 
 struct GemvCol {
   int src;            // Src
-  int pad;
+  int tag_back;       // 0: a plain buffer; n > 0: a tagged buffer written n phases earlier (see Phase)
   const void* p;      // SRC_BUF: float[K]; SRC_EMBED: int[NCB+1]; SRC_FEROW: int* code
   float* wb;          // nullable: CTA 0 writes the raw (pre-norm) column here
 };
@@ -107,8 +107,14 @@ struct alignas(16) Phase {
   int merge_main;     // OP_GEMV: CTA 0 performs the main draw instead of GEMV rows
   int cta0;           // first CTA doing GEMV rows
   int M, K, nmat, ncols, epi, rows_per_tile, Q;
-  int Kt;                // bf16 weights: columns per tile (K = nkt * Kt), for every 8-row block
+  int Kt;                // bf16 weights: columns per tile (K = nkt * Kt), for every 16-row block
   int nkt;               //   and the count of K tiles
+  // Tagged handoffs (bf16 models): the residual rows and the SwiGLU planes are written as 64-bit
+  // words (value bits, then the writing phase's tag: the launch's base tag + the phase's index).
+  // A reader of such a buffer polls for the tag of the phase that wrote it (GemvCol::tag_back)
+  // instead of waiting at a grid barrier after that phase.
+  int tag_out;           // y / yp / column write-backs of this phase are tagged words
+  int no_sync;           // no grid barrier after this phase: the next one polls its tagged inputs
   const void* w[2];   // row-major [M][K]; w[1] is the gate partner for EPI_SWIGLU
   const void* last_row;  // nullable: source of row M-1 (admissible logits: im_end row)
   const void* normw;     // nullable RMSNorm weight [K]
@@ -168,6 +174,7 @@ struct alignas(16) CallParams {
   const void* FE;
   int kv_slots;
   unsigned gbar_base;     // grid-barrier counter value at launch (the launch sets it)
+  unsigned tag0;          // tag of the launch's first phase (never 0; phase k: tag0 + k)
 };
 
 // host entry points between translation units
