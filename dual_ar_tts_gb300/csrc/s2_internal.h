@@ -31,7 +31,7 @@ constexpr int kRedFloats = 2048;               // per-CTA partial sums (GEMV row
 constexpr int kXRegFloats = 80;                // activation slice per lane held in registers
 constexpr int kGemvChunksPerLane = 5;          // 16-byte chunks per lane: K-slices of 1/8 of <= 10240 bf16
 constexpr int kAttnMaxChunk = 2048;            // workspace sizing of the split-K partials
-constexpr int kAttnItemSlots = 32;             // target slots per Slow-AR attention split
+constexpr int kAttnItemSlots = 64;             // target slots per Slow-AR attention split
 constexpr int kAttnMaxSplits = 32;             // splits per KV head at most
 
 enum Op : int {
