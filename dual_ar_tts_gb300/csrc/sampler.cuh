@@ -37,18 +37,21 @@ __device__ __forceinline__ float fval(uint32_t k) {
 }
 
 // Sampler scratch in shared memory (256 consumer threads; kSampPer logits per thread).
-constexpr int kSampHist = 4096;  // first-level histogram: the top 12 bits of a key
+constexpr int kSampHist = 4096;  // first-level histogram of the fallback selection: top 12 key bits
+constexpr int kSampCand = 64;    // candidates the threshold selection ranks directly
 struct SampScratch {
   int nvalid, cut, rem, nA, nB, result, pad[2];
+  uint32_t thr, pad2[3];
   int wsum[kConsumerWarps];
-  uint32_t aK[32];  // candidates above the boundary bin (fewer than 30)
+  uint32_t aK[32];  // fallback: candidates above the boundary bin (fewer than 30)
   int aI[32];
-  uint32_t bK[64];  // candidates in the boundary bin
-  int bI[64];
+  uint32_t bK[kSampCand];  // threshold selection: the candidates; fallback: the boundary bin
+  int bI[kSampCand];
   uint32_t cK[32];  // the final candidates in rank order
   int cI[32];
+  alignas(16) uint32_t mx[kConsumers];  // per-thread maximum keys
   int hist[kSampHist];
-  alignas(16) uint32_t keys[kSampPer * kConsumers];  // by entry index: the logits, then their keys
+  alignas(16) uint32_t keys[kSampPer * kConsumers];  // fallback: the keys by entry index
 };
 
 // bitonic sort of 32 (key, id) pairs across a warp, one per lane: best (larger key, then lower
@@ -71,55 +74,67 @@ __device__ __forceinline__ void warp_sort32(uint32_t& k, int& id) {
   }
 }
 
-// One draw: the top-30 candidates by (value desc, id asc), then, in rank order exactly as the
-// method states: softmax over them, keep rank r iff r == 0 or Σ_{s<r} π_s < top_p, winner =
-// argmax π_r / E_r (ties -> lower rank).  Returns the drawn id in every consumer thread; -1 if
-// nothing is drawable.
-// Selection: order-preserving 32-bit keys of z = logit / T (kSampPer per thread, in shared
-// memory so that the loops stay compact).  A 4096-bin histogram of the top 12 bits locates the
-// bin holding the 30th key; while that bin holds more than 64 keys it is refined by the next 10
-// bits (at most twice).  Keys above the boundary and the boundary bin's keys are then sorted by
-// two warps.
-__device__ __noinline__ int draw(const Dims& d, SampScratch& W, const float* logits, int n, bool main, bool mask_end,
-                                 float temperature, float top_p, const float* E) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // the rank-r variate, needed at the end, is requested first; the logits come into shared
-  // memory in one batch of 16-byte copies (n4 full chunks, then the remaining entries)
-  const float ev = (warp == 0 && lane < kTopK) ? ldcg(E + lane) : 1.f;
-  const int n4 = n / 4;
-#pragma unroll 1
-  for (int c = tid; c < n4; c += kConsumers) cp_async16(&W.keys[4 * c], logits + 4 * c);
-  if (tid < n - 4 * n4) W.keys[4 * n4 + tid] = __float_as_uint(ldcg(logits + 4 * n4 + tid));
-  cp_async_wait_all();
-  named_bar(1, kConsumers);
-  int nv = 0;
-#pragma unroll 1
-  for (int k = 0; k < kSampPer; ++k) {
-    const int i = tid + k * kConsumers;
-    uint32_t key = 0u;
-    if (i < n) {
-      const float l = __uint_as_float(W.keys[i]);
-      if (!(mask_end && main && entry_id(d, main, i) == d.im_end) && isfinite(l)) {
-        key = fkey(l / temperature);
-        ++nv;
+// The kk-th largest of the 256 per-thread maxima W.mx, by one warp: bitonic sort of the 256 keys,
+// 8 per lane (element e = 8·lane + j), largest first.  Strides 1-4 stay in a lane's registers,
+// strides 8-128 pair lanes (lane ^ stride/8).
+__device__ __forceinline__ uint32_t kth_of_maxima(const SampScratch& W, int kk) {
+  const int lane = threadIdx.x & 31;
+  uint32_t v[8];
+  {
+    const uint4 a = *reinterpret_cast<const uint4*>(&W.mx[8 * lane]);
+    const uint4 b = *reinterpret_cast<const uint4*>(&W.mx[8 * lane + 4]);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+#pragma unroll
+  for (int size = 2; size <= 256; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride < 8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (j & stride) continue;
+          // descending block iff bit `size` of the element index is 0
+          const bool desc = size < 8 ? (j & size) == 0 : ((8 * lane) & size) == 0;
+          const uint32_t a = v[j], b = v[j | stride];
+          const uint32_t hi = max(a, b), lo = min(a, b);
+          v[j] = desc ? hi : lo;
+          v[j | stride] = desc ? lo : hi;
+        }
+      } else {
+        const int ls = stride >> 3;
+        const bool lower = (lane & ls) == 0;
+        const bool desc = (lane & (size >> 3)) == 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t p = __shfl_xor_sync(0xffffffffu, v[j], ls);
+          v[j] = (lower == desc) ? max(v[j], p) : min(v[j], p);
+        }
       }
     }
-    W.keys[i] = key;
   }
+  const int e = kk - 1, jj = e & 7;
+  uint32_t r = v[0];
+#pragma unroll
+  for (int j = 1; j < 8; ++j)
+    if (j == jj) r = v[j];
+  return __shfl_sync(0xffffffffu, r, e >> 3);
+}
+
+// Fallback selection of the top kk (any tie pattern): the keys are in W.keys.  A 4096-bin histogram
+// of the top 12 bits locates the bin holding the kk-th key; while that bin holds more than 64
+// keys it is refined by the next 10 bits (at most twice).  Keys above the boundary and the boundary
+// bin's keys are then sorted by two warps; more than 64 equal keys at full resolution are taken in
+// id order one by one.  Writes W.cK / W.cI[0 .. kk) in rank order.
+__device__ __noinline__ void select_hist(const Dims& d, SampScratch& W, bool main, int kk) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 #pragma unroll 1
   for (int b = tid; b < kSampHist; b += kConsumers) W.hist[b] = 0;
-  nv = warp_sum_i(nv);
-  if (lane == 0) W.wsum[warp] = nv;
   if (tid == 0) {
     W.nA = 0;
     W.nB = 0;
   }
   named_bar(1, kConsumers);
-  int nvalid = 0;
-#pragma unroll 1
-  for (int w = 0; w < kConsumerWarps; ++w) nvalid += W.wsum[w];
-  if (nvalid == 0) return -1;  // uniform: every thread saw the same count
-  const int kk = min(kTopK, nvalid);
 
   // ---- locate the kk-th largest key: prefix `pre` of its top (32 - shift) bits, `need` of the
   // keys with that prefix belong to the top kk
@@ -273,6 +288,110 @@ __device__ __noinline__ int draw(const Dims& d, SampScratch& W, const float* log
     }
   }
   named_bar(1, kConsumers);
+}
+
+// One draw: the top-30 candidates by (value desc, id asc), then, in rank order exactly as the
+// method states: softmax over them, keep rank r iff r == 0 or Σ_{s<r} π_s < top_p, winner =
+// argmax π_r / E_r (ties -> lower rank).  Returns the drawn id in every consumer thread; -1 if
+// nothing is drawable.
+// Selection: order-preserving 32-bit keys of z = logit / T, kSampPer per thread in registers.  At
+// least kk of the 256 per-thread maxima are >= the kk-th largest of them (thr), so at least kk keys
+// are, and every key of the top kk is >= thr: the keys >= thr hold the top kk, ranked by the same
+// total order.  They are gathered (one shared-memory counter per warp) and, when at most 64, each
+// is ranked by counting the candidates ahead of it; more than 64 (heavy ties) take the histogram
+// selection above.
+__device__ __noinline__ int draw(const Dims& d, SampScratch& W, const float* logits, int n, bool main, bool mask_end,
+                                 float temperature, float top_p, const float* E) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the rank-r variate, needed at the end, and this thread's logits (entries tid + 256 k) are
+  // requested first, every load in flight together
+  const float ev = (warp == 0 && lane < kTopK) ? ldcg(E + lane) : 1.f;
+  uint32_t key[kSampPer];
+#pragma unroll
+  for (int k = 0; k < kSampPer; ++k) {
+    const int i = tid + k * kConsumers;
+    key[k] = i < n ? __float_as_uint(ldcg(logits + i)) : 0u;
+  }
+  uint32_t mx = 0u;
+  int nv = 0;
+#pragma unroll
+  for (int k = 0; k < kSampPer; ++k) {
+    const int i = tid + k * kConsumers;
+    const float l = __uint_as_float(key[k]);
+    uint32_t kv = 0u;
+    if (i < n && !(mask_end && main && entry_id(d, main, i) == d.im_end) && isfinite(l)) {
+      // + 0: -0 and +0 compare equal, so they share one key
+      kv = fkey(l / temperature + 0.0f);
+      ++nv;
+    }
+    key[k] = kv;
+    mx = max(mx, kv);
+  }
+  nv = warp_sum_i(nv);
+  if (lane == 0) W.wsum[warp] = nv;
+  W.mx[tid] = mx;
+  if (tid == 0) W.nB = 0;
+  named_bar(1, kConsumers);
+  int nvalid = 0;
+#pragma unroll
+  for (int w = 0; w < kConsumerWarps; ++w) nvalid += W.wsum[w];
+  if (nvalid == 0) {
+    named_bar(1, kConsumers);  // uniform: every thread saw the same count, and has read it
+    return -1;
+  }
+  const int kk = min(kTopK, nvalid);
+  if (warp == 0) {
+    const uint32_t t = kth_of_maxima(W, kk);
+    if (lane == 0) W.thr = t;
+  }
+  named_bar(1, kConsumers);
+  // ---- gather the keys >= thr (key 0 = not drawable): warp-local slots, one counter per warp
+  const uint32_t thr = max(W.thr, 1u);
+  int c = 0;
+#pragma unroll
+  for (int k = 0; k < kSampPer; ++k) c += key[k] >= thr ? 1 : 0;
+  int incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  int base = 0;
+  if (lane == 31 && incl > 0) base = atomicAdd(&W.nB, incl);
+  int slot = __shfl_sync(0xffffffffu, base, 31) + incl - c;
+#pragma unroll
+  for (int k = 0; k < kSampPer; ++k) {
+    if (key[k] >= thr) {
+      if (slot < kSampCand) {
+        W.bK[slot] = key[k];
+        W.bI[slot] = entry_id(d, main, tid + k * kConsumers);
+      }
+      ++slot;
+    }
+  }
+  named_bar(1, kConsumers);
+  const int nb = W.nB;  // >= kk
+  if (nb <= kSampCand) {
+    // rank of each candidate = the candidates ahead of it in (key desc, id asc); the top kk land
+    // at their ranks
+    if (tid < nb) {
+      const uint32_t mk = W.bK[tid];
+      const int mi = W.bI[tid];
+      int rank = 0;
+#pragma unroll 4
+      for (int j = 0; j < nb; ++j) rank += better_k(W.bK[j], W.bI[j], mk, mi) ? 1 : 0;
+      if (rank < kk) {
+        W.cK[rank] = mk;
+        W.cI[rank] = mi;
+      }
+    }
+    named_bar(1, kConsumers);
+  } else {
+#pragma unroll
+    for (int k = 0; k < kSampPer; ++k) W.keys[k * kConsumers + tid] = key[k];
+    named_bar(1, kConsumers);  // every thread has read W.nB before the selection resets it
+    select_hist(d, W, main, kk);
+  }
   // ---- warp 0: the draw over the kk candidates, rank r = lane.  The sums, whose rounding depends
   // on the order, are taken in rank order (every lane runs the same sequence over shuffled values)
   if (warp == 0) {
