@@ -21,7 +21,8 @@ STATUS_NAMES = {0: "S2_OK", 1: "S2_EINVAL", 2: "S2_ENOMEM", 3: "S2_ECAPACITY", 4
 EXPORTS = ("s2_weight_count", "s2_weight_info", "s2_frame_workspace_bytes", "s2_frame_init", "s2_prefill",
            "s2_decode_frames", "s2_fast_logits", "s2_sync_status", "s2_set_spin_limit", "s2_set_trace",
            "s2_phase_count", "s2_frame_free", "s2_last_error", "s2_fast_logits_static", "s2_stream_import",
-           "s2_stop_stream", "s2_stream_progress", "s2_codec_latent", "s2_quantize_e4m3", "s2_set_barrier_base")
+           "s2_stop_stream", "s2_stream_progress", "s2_codec_latent", "s2_quantize_e4m3", "s2_set_barrier_base",
+           "s2_draw")
 
 
 class s2_dims(ctypes.Structure):
@@ -84,6 +85,7 @@ def load(path: str = LIB_PATH):
         "s2_codec_latent": (i32, [i32, i32, i32, P(vp), i32, vp, vp, vp, vp]),
         "s2_quantize_e4m3": (i32, [vp, ctypes.c_longlong, i32, vp, vp, vp]),
         "s2_stream_progress": (i32, [vp, i32, P(i32), vp, vp]),
+        "s2_draw": (i32, [i32, vp, i32, i32, i32, i32, ctypes.c_float, ctypes.c_float, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -168,6 +170,29 @@ def s2_codec_latent(n_codebooks: int, codebook_size: int, dim: int, quantizer_pt
 def s2_quantize_e4m3(w_ptr: int, rows: int, cols: int, codes_ptr: int, scales_ptr: int, stream: int = 0):
     """e4m3 codes + fp32 row scales of bf16 rows (device pointers; see s2frame.h)."""
     return _check("s2_quantize_e4m3", load().s2_quantize_e4m3(w_ptr, rows, cols, codes_ptr, scales_ptr, stream))
+
+
+def s2_draw(rows: int, logits_ptr: int, n: int, sem_begin: int, im_end: int, block_end: bool, temperature: float,
+            top_p: float, expo_ptr: int, out_ptr: int, stream: int = 0):
+    """The S2 draw on device logits rows (see s2frame.h)."""
+    rc = load().s2_draw(rows, logits_ptr, n, sem_begin, im_end, 1 if block_end else 0, temperature, top_p, expo_ptr,
+                        out_ptr, stream)
+    return _check("s2_draw", rc)
+
+
+def draw(logits, expo, temperature: float, top_p: float, sem_begin: int = -1, im_end: int = 0,
+         block_end: bool = False):
+    """Device fp32 logits [rows][n] and variates [rows][30] (torch) -> drawn ids, int32 [rows]."""
+    import torch
+    if logits.dtype != torch.float32 or logits.dim() != 2 or not logits.is_cuda:
+        raise ValueError("draw takes 2-D fp32 CUDA logits")
+    if expo.dtype != torch.float32 or tuple(expo.shape) != (logits.shape[0], 30) or not expo.is_cuda:
+        raise ValueError("draw takes fp32 CUDA variates of shape [rows][30]")
+    logits, expo = logits.contiguous(), expo.contiguous()
+    out = torch.empty(logits.shape[0], dtype=torch.int32, device=logits.device)
+    s2_draw(logits.shape[0], logits.data_ptr(), logits.shape[1], sem_begin, im_end, block_end, temperature, top_p,
+            expo.data_ptr(), out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    return out
 
 
 def quantize_e4m3(w):

@@ -12,7 +12,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libs2frame.so")
 BUILD = os.path.join(HERE, "_build")
 SOURCES = ["fk_bf16_h128.cu", "fk_bf16_h64.cu", "fk_f32_h128.cu", "fk_f32_h64.cu", "frame_launch.cu", "prefill.cu",
-           "engine.cu", "batch.cu", "codec.cu"]
+           "engine.cu", "batch.cu", "codec.cu", "draw.cu"]
 HEADERS = ["s2_internal.h", "ptx.cuh", "frame_kernel.cuh", "sampler.cuh", "tc05.cuh", os.path.join("..", "..", "include", "s2frame.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

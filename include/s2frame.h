@@ -299,6 +299,27 @@ int s2_codec_latent(int n_codebooks, int codebook_size, int dim, const void* con
 int s2_quantize_e4m3(const void* w, long long rows, int cols, uint8_t* codes, float* scales,
                      struct CUstream_st* stream);
 
+/* The S2 draw on caller logits rows: the device routine both decode engines run (s2.cpp analysis
+ * ch.06 §5 for the draw and the min_tokens masking of im_end; the Mizuoto "Fish Speech" engine
+ * page for top-k fixed at 30 and winner = argmax(probs / -log u)).  For each row r:
+ *   z = logits / temperature (fp32 division); entries that are not finite, and the im_end entry
+ *   when block_end != 0, cannot be drawn;
+ *   the top 30 by (z desc, id asc), -0 equal to +0; π = softmax over them (fp32, max-subtracted,
+ *   summed in rank order); rank r is kept iff r == 0 or Σ_{s<r} π_s < top_p;
+ *   out[r] = the id of the kept rank maximising π_r / E_r (ties -> the lower rank), or -1 when
+ *   no entry of the row can be drawn.
+ * Ids: sem_begin < 0 -> the entry index (Fast-AR codes); sem_begin >= 0 -> the admissible main
+ * vocabulary of n = codebook_size + 1 entries: entry i < n - 1 is token sem_begin + i, entry
+ * n - 1 is im_end.
+ *   logits  device fp32 [rows][n], 4-byte aligned, n 1..4352
+ *   expo    device fp32 [rows][30]: E of each rank (-log u, u uniform in (0, 1])
+ *   out     device int32 [rows]
+ * Stateless; allocates nothing; asynchronous on `stream`.
+ * Errors (nothing launched): S2_EINVAL bad count, pointer or alignment, temperature not finite
+ * or <= 0, top_p not finite; S2_ECUDA launch failed. */
+int s2_draw(int rows, const float* logits, int n, int sem_begin, int im_end, int block_end, float temperature,
+            float top_p, const float* expo, int32_t* out, struct CUstream_st* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -108,6 +108,23 @@ def test_quantize_e4m3_rejects_bad_arguments_before_any_cuda_call():
     assert lib.s2_quantize_e4m3(16, 4, 8, 32, 66, None) == pkg.S2_EINVAL    # unaligned scales
 
 
+def test_draw_rejects_bad_arguments_before_any_cuda_call():
+    import dual_ar_tts_gb300 as pkg
+    lib = pkg.load()
+    assert lib.s2_draw(0, 16, 64, -1, 0, 0, 0.7, 0.8, 32, 48, None) == pkg.S2_EINVAL      # no row
+    assert lib.s2_draw(1, 16, 0, -1, 0, 0, 0.7, 0.8, 32, 48, None) == pkg.S2_EINVAL       # empty row
+    assert lib.s2_draw(1, 16, 4353, -1, 0, 0, 0.7, 0.8, 32, 48, None) == pkg.S2_EINVAL    # row too long
+    assert lib.s2_draw(1, 16, 1, 100, 7, 0, 0.7, 0.8, 32, 48, None) == pkg.S2_EINVAL      # main row without im_end
+    assert lib.s2_draw(1, None, 64, -1, 0, 0, 0.7, 0.8, 32, 48, None) == pkg.S2_EINVAL    # no logits
+    assert lib.s2_draw(1, 16, 64, -1, 0, 0, 0.7, 0.8, None, 48, None) == pkg.S2_EINVAL    # no variates
+    assert lib.s2_draw(1, 16, 64, -1, 0, 0, 0.7, 0.8, 32, None, None) == pkg.S2_EINVAL    # no output
+    assert lib.s2_draw(1, 18, 64, -1, 0, 0, 0.7, 0.8, 32, 48, None) == pkg.S2_EINVAL      # unaligned logits
+    assert lib.s2_draw(1, 16, 64, -1, 0, 0, 0.0, 0.8, 32, 48, None) == pkg.S2_EINVAL      # temperature 0
+    assert lib.s2_draw(1, 16, 64, -1, 0, 0, -1.0, 0.8, 32, 48, None) == pkg.S2_EINVAL     # negative temperature
+    assert lib.s2_draw(1, 16, 64, -1, 0, 0, float("nan"), 0.8, 32, 48, None) == pkg.S2_EINVAL
+    assert lib.s2_draw(1, 16, 64, -1, 0, 0, 0.7, float("inf"), 32, 48, None) == pkg.S2_EINVAL
+
+
 def test_fp8_dims_are_checked():
     import dual_ar_tts_gb300 as pkg
     import synth
