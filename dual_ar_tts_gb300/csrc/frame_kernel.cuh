@@ -230,7 +230,7 @@ __device__ __forceinline__ float tval(unsigned long long w) { return __uint_as_f
 // Waits, bounded, until the pairs of tagged words at p[2i], p[2i + 1] (i in `miss`, a mask) carry
 // `tag`; returns their values in v.  A give-up records S2_ETIMEOUT (site 8) and the CTA's failure.
 template <int N>
-__device__ __noinline__ void wait_tagged(const CallParams& cp, Smem& S, const unsigned long long* const (&p)[N],
+__device__ __forceinline__ void wait_tagged(const CallParams& cp, Smem& S, const unsigned long long* const (&p)[N],
                                          uint32_t tag, uint32_t miss, ulonglong2 (&v)[N]) {
   const long long t0 = clock_us();
   for (unsigned it = 1; miss != 0u; ++it) {
@@ -383,7 +383,7 @@ __device__ void producer(const CallParams& cp, Smem& S) {
 // =========================================================================
 
 template <typename WT, int NC>
-__device__ __noinline__ void gemv_t(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe) {
+__device__ __noinline__ Pipe gemv_t(const CallParams& cp, const Phase& ph, Smem& S, Pipe pipe) {
   constexpr int EPC = 16 / static_cast<int>(sizeof(WT));
   constexpr int NCH = kGemvChunksPerLane;  // every warp holds a 1/8 K-slice: <= 5 chunks per lane
   const Dims& d = cp.d;
@@ -621,6 +621,7 @@ __device__ __noinline__ void gemv_t(const CallParams& cp, const Phase& ph, Smem&
       }
     }
   }
+  return pipe;
 }
 
 // =========================================================================
@@ -650,12 +651,12 @@ __device__ __forceinline__ void tile_steps(uint32_t tb, uint32_t a_off, uint32_t
 }
 
 template <int NC>
-__device__ __noinline__ void gemv_tiles(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe, float yres);
+__device__ __noinline__ Pipe gemv_tiles(const CallParams& cp, const Phase& ph, Smem& S, Pipe pipe, float yres);
 
 // GEMV prologue for activations of at most GM·1024 elements per column: the columns into registers
 // (GM float4 groups per thread), RMSNorm, the bf16 hi/lo split into shared memory; then the tiles.
 template <int NC, int GM>
-__device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe) {
+__device__ __noinline__ Pipe gemv_mma(const CallParams& cp, const Phase& ph, Smem& S, Pipe pipe) {
   const Dims& d = cp.d;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int K = ph.K;
@@ -840,11 +841,11 @@ __device__ __noinline__ void gemv_mma(const CallParams& cp, const Phase& ph, Sme
   }
   named_bar(1, kConsumers);
 
-  gemv_tiles<NC>(cp, ph, S, pipe, yres);
+  return gemv_tiles<NC>(cp, ph, S, pipe, yres);
 }
 
 template <int NC>
-__device__ __noinline__ void gemv_tiles(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe, float yres) {
+__device__ __noinline__ Pipe gemv_tiles(const CallParams& cp, const Phase& ph, Smem& S, Pipe pipe, float yres) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int K = ph.K;
   int r0, nr;
@@ -997,12 +998,13 @@ __device__ __noinline__ void gemv_tiles(const CallParams& cp, const Phase& ph, S
       }
     }
   }
+  return pipe;
 }
 
 // The activation comes as bf16 hi / lo rows written by the producing phase: one bulk copy per row
 // into xs, then the tiles (no normalisation on this path).
 template <int NC>
-__device__ __noinline__ void gemv_planes(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe) {
+__device__ __noinline__ Pipe gemv_planes(const CallParams& cp, const Phase& ph, Smem& S, Pipe pipe) {
   const int tid = threadIdx.x;
   const int K = ph.K;
   int r0, nr;
@@ -1011,9 +1013,10 @@ __device__ __noinline__ void gemv_planes(const CallParams& cp, const Phase& ph, 
   if (ph.epi == EPI_ADD && tid < nr * NC) yres = ld_out(ph, tid % NC, r0 + tid / NC);
   const uint32_t xpitch = 2u * static_cast<uint32_t>(K) + kTileRowPad;
   if (ph.col[0].tag_back > 0) {
-    // tagged planes words (hi | lo << 16, then the tag), written tag_back phases ago: two rounds
-    // of loads per thread, unpacked into the hi and lo rows of xs
-    constexpr int B = 10;  // element pairs per thread and round
+    // tagged planes words (hi | lo << 16, then the tag), written tag_back phases ago: every load
+    // of a thread in flight at once (one round up to K = 9728), unpacked into the hi and lo rows
+    // of xs
+    constexpr int B = 19;  // element pairs per thread and round: K <= 9728 in one round
     const uint32_t xsb = smem_u32(S.xs);
     const int npairs = K / 2;
 #pragma unroll 1
@@ -1048,8 +1051,7 @@ __device__ __noinline__ void gemv_planes(const CallParams& cp, const Phase& ph, 
       }
     }
     named_bar(1, kConsumers);
-    gemv_tiles<NC>(cp, ph, S, pipe, yres);
-    return;
+    return gemv_tiles<NC>(cp, ph, S, pipe, yres);
   }
   if (tid == 0) {
     // the previous users of xs (generic-proxy accesses, ordered before by the phase barrier) come
@@ -1070,29 +1072,26 @@ __device__ __noinline__ void gemv_planes(const CallParams& cp, const Phase& ph, 
     if (tid == 0) drain_copies(cp, &S.xsbar, pipe.xs_uses & 1u, 7);  // this CTA's own copies
   }
   ++pipe.xs_uses;
-  gemv_tiles<NC>(cp, ph, S, pipe, yres);
+  return gemv_tiles<NC>(cp, ph, S, pipe, yres);
 }
 
 template <class C>
-__device__ void gemv(const CallParams& cp, const Phase& ph, Smem& S, Pipe& pipe) {
+__device__ __forceinline__ Pipe gemv(const CallParams& cp, const Phase& ph, Smem& S, Pipe pipe) {
   if constexpr (C::bf16) {
     if (ph.col[0].src == SRC_PLANES) {
-      if (ph.ncols == 1) gemv_planes<1>(cp, ph, S, pipe);
-      else gemv_planes<2>(cp, ph, S, pipe);
-      return;
+      return ph.ncols == 1 ? gemv_planes<1>(cp, ph, S, pipe) : gemv_planes<2>(cp, ph, S, pipe);
     }
     // the activation length selects how many float4 groups each thread holds (K <= GM·1024)
     if (ph.ncols == 1) {
-      if (ph.K <= 3072) gemv_mma<1, 3>(cp, ph, S, pipe);
-      else if (ph.K <= 4096) gemv_mma<1, 4>(cp, ph, S, pipe);
-      else gemv_mma<1, 10>(cp, ph, S, pipe);
+      if (ph.K <= 3072) return gemv_mma<1, 3>(cp, ph, S, pipe);
+      if (ph.K <= 4096) return gemv_mma<1, 4>(cp, ph, S, pipe);
+      return gemv_mma<1, 10>(cp, ph, S, pipe);
     } else {
-      if (ph.K <= 3072) gemv_mma<2, 3>(cp, ph, S, pipe);
-      else gemv_mma<2, 5>(cp, ph, S, pipe);
+      if (ph.K <= 3072) return gemv_mma<2, 3>(cp, ph, S, pipe);
+      return gemv_mma<2, 5>(cp, ph, S, pipe);
     }
   } else {
-    if (ph.ncols == 1) gemv_t<float, 1>(cp, ph, S, pipe);
-    else gemv_t<float, 2>(cp, ph, S, pipe);
+    return ph.ncols == 1 ? gemv_t<float, 1>(cp, ph, S, pipe) : gemv_t<float, 2>(cp, ph, S, pipe);
   }
 }
 
@@ -1407,19 +1406,34 @@ __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, 
         mls[2 * i + 1] = ml.y;
       }
       named_bar(1, kConsumers);
-#pragma unroll 1
-      for (int idx = tid; idx < rep * HD; idx += kConsumers) {
-        const int r = idx / HD, e = idx % HD;
+      // at most 4 heads x 128 elements: two outputs per thread, every split's partial of both
+      // requested at once (the sums keep split order)
+      static_assert(4 * HD <= 2 * kConsumers, "combine outputs per thread");
+      float pv[2][kAttnMaxSplits];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int idx = tid + q * kConsumers, r = idx / HD, e = idx % HD;
+#pragma unroll
+        for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
+          pv[q][s2] = (idx < rep * HD && s2 < ns)
+                          ? ldcg(cp.part + (static_cast<size_t>(g * ns + s2) * 4 + r) * HD + e) : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int idx = tid + q * kConsumers, r = idx / HD, e = idx % HD;
+        if (idx >= rep * HD) continue;
         const float* mr = mls + 2 * r * ns;
         float M = -INFINITY;
 #pragma unroll 1
         for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, mr[2 * s2]);
         float o = 0.f, l = 0.f;
-#pragma unroll 4
-        for (int s2 = 0; s2 < ns; ++s2) {
-          const float w = expf(mr[2 * s2] - M);
-          o += w * ldcg(cp.part + (static_cast<size_t>(g * ns + s2) * 4 + r) * HD + e);
-          l += w * mr[2 * s2 + 1];
+#pragma unroll
+        for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
+          if (s2 < ns) {
+            const float w = expf(mr[2 * s2] - M);
+            o += w * pv[q][s2];
+            l += w * mr[2 * s2 + 1];
+          }
         }
         ph.out[(g * rep + r) * HD + e] = o / l;
         if (ph.outp != nullptr) store_planes(ph.outp, d.Hq * HD, (g * rep + r) * HD + e, o / l);
@@ -1442,82 +1456,118 @@ __device__ void attn_slow(const CallParams& cp, const Phase& ph, Smem& S) {
 
 template <int HD>
 __device__ __noinline__ void attn_fast_t(const CallParams& cp, const Phase& ph, Smem& S) {
+  // One CTA per (position, query head); its eight warps split the window's slots (warp w: slots
+  // w and w + 8), so each warp issues its few key / value loads at once instead of walking the
+  // slots one dependent load after another.  Each warp keeps an online-softmax partial (max,
+  // sum, weighted values); warp 0 combines the eight in warp order.
   constexpr int DPL = HD / 32;
+  constexpr int kSlotsPerWarp = 2;  // window <= 16 positions
   const Dims& d = cp.d;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = d.Hqf, Hk = d.Hkvf, rep = H / Hk;
   const int QKV = (H + 2 * Hk) * HD;
   const int nitems = ph.npos * H;
-  const int G = gridDim.x;
   const float sc_mul = ph.scale;
   float* kc = static_cast<float*>(ph.kc);  // [Wf][Hk][HD]
   float* vc = static_cast<float*>(ph.vc);
-  for (int item = blockIdx.x + G * warp; item < nitems; item += G * kConsumerWarps) {
+  float* part = reinterpret_cast<float*>(S.xs);  // per warp: o[HD], max, sum
+  for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
     const int jn = item / H, h = item % H, g = h / rep;
     const int p = ph.pos0 + jn;
+    // every load first: the query, and the keys / values of this warp's slots (the frame's new
+    // positions from the projection output, earlier ones from the window cache)
+    NormRope<DPL> nq;
+    load_norm_rope<DPL>(nq, ph.qn, d.esz, d.qk_norm != 0, cp.rope_f + static_cast<size_t>(p) * (HD / 2));
     float q[DPL];
     const float* qrow = ph.qkv + static_cast<size_t>(jn) * QKV;
 #pragma unroll
     for (int j = 0; j < DPL; ++j) q[j] = ldcg(qrow + h * HD + lane * DPL + j);
-    head_norm_rope<DPL>(q, ph.qn, d.esz, d.eps, HD, d.qk_norm != 0, cp.rope_f + static_cast<size_t>(p) * (HD / 2));
-    float sc[16];
-    float kk[16][DPL];  // keys of slots 0..p (p <= 10)
-    float vv[16][DPL];
-    for (int s = 0; s <= p; ++s) {
+    float k[kSlotsPerWarp][DPL], v[kSlotsPerWarp][DPL];
+    NormRope<DPL> nk[kSlotsPerWarp];
+#pragma unroll
+    for (int t = 0; t < kSlotsPerWarp; ++t) {
+      const int s = warp + kConsumerWarps * t;
+      const bool fresh = s >= ph.pos0;
+      if (fresh && s <= p)
+        load_norm_rope<DPL>(nk[t], ph.kn, d.esz, d.qk_norm != 0, cp.rope_f + static_cast<size_t>(s) * (HD / 2));
+      const float* kr = fresh ? ph.qkv + static_cast<size_t>(s - ph.pos0) * QKV + (H + g) * HD
+                              : kc + (static_cast<size_t>(s) * Hk + g) * HD;
+      const float* vr = fresh ? ph.qkv + static_cast<size_t>(s - ph.pos0) * QKV + (H + Hk + g) * HD
+                              : vc + (static_cast<size_t>(s) * Hk + g) * HD;
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) {
+        k[t][j] = s <= p ? ldcg(kr + lane * DPL + j) : 0.f;
+        v[t][j] = s <= p ? ldcg(vr + lane * DPL + j) : 0.f;
+      }
+    }
+    head_norm_rope<DPL>(q, nq, d.eps, HD, d.qk_norm != 0);
+    float m = -INFINITY, sc[kSlotsPerWarp];
+#pragma unroll
+    for (int t = 0; t < kSlotsPerWarp; ++t) {
+      const int s = warp + kConsumerWarps * t;
+      sc[t] = -INFINITY;
+      if (s > p) continue;  // uniform across the warp
       if (s >= ph.pos0) {
-        const float* r = ph.qkv + static_cast<size_t>(s - ph.pos0) * QKV;
-        float k[DPL], v[DPL];
-#pragma unroll
-        for (int j = 0; j < DPL; ++j) {
-          k[j] = ldcg(r + (H + g) * HD + lane * DPL + j);
-          v[j] = ldcg(r + (H + Hk + g) * HD + lane * DPL + j);
-        }
-        head_norm_rope<DPL>(k, ph.kn, d.esz, d.eps, HD, d.qk_norm != 0, cp.rope_f + static_cast<size_t>(s) * (HD / 2));
-#pragma unroll
-        for (int j = 0; j < DPL; ++j) {
-          kk[s][j] = k[j];
-          vv[s][j] = v[j];
-        }
+        // a new position of this frame: its key is normalised and rotated here
+        head_norm_rope<DPL>(k[t], nk[t], d.eps, HD, d.qk_norm != 0);
         if (s == p && (h % rep) == 0) {
 #pragma unroll
           for (int j = 0; j < DPL; ++j) {
-            kc[(static_cast<size_t>(s) * Hk + g) * HD + lane * DPL + j] = k[j];
-            vc[(static_cast<size_t>(s) * Hk + g) * HD + lane * DPL + j] = v[j];
+            kc[(static_cast<size_t>(s) * Hk + g) * HD + lane * DPL + j] = k[t][j];
+            vc[(static_cast<size_t>(s) * Hk + g) * HD + lane * DPL + j] = v[t][j];
           }
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < DPL; ++j) {
-          kk[s][j] = ldcg(kc + (static_cast<size_t>(s) * Hk + g) * HD + lane * DPL + j);
-          vv[s][j] = ldcg(vc + (static_cast<size_t>(s) * Hk + g) * HD + lane * DPL + j);
         }
       }
       float dot = 0.f;
 #pragma unroll
-      for (int j = 0; j < DPL; ++j) dot += q[j] * kk[s][j];
-      sc[s] = warp_sum(dot) * sc_mul;
+      for (int j = 0; j < DPL; ++j) dot += q[j] * k[t][j];
+      sc[t] = warp_sum(dot) * sc_mul;
+      m = fmaxf(m, sc[t]);
     }
-    float m = -INFINITY;
-    for (int s = 0; s <= p; ++s) m = fmaxf(m, sc[s]);
-    float l = 0.f;
-    for (int s = 0; s <= p; ++s) {
-      sc[s] = expf(sc[s] - m);
-      l += sc[s];
-    }
-    float o[DPL];
+    float l = 0.f, o[DPL];
 #pragma unroll
     for (int j = 0; j < DPL; ++j) o[j] = 0.f;
-    for (int s = 0; s <= p; ++s) {
-      const float pr = sc[s] / l;
 #pragma unroll
-      for (int j = 0; j < DPL; ++j) o[j] += pr * vv[s][j];
+    for (int t = 0; t < kSlotsPerWarp; ++t) {
+      if (sc[t] == -INFINITY) continue;
+      const float e = expf(sc[t] - m);
+      l += e;
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) o[j] += e * v[t][j];
     }
+    float* pw = part + warp * (HD + 2);
 #pragma unroll
-    for (int j = 0; j < DPL; ++j) ph.out[static_cast<size_t>(jn) * (H * HD) + h * HD + lane * DPL + j] = o[j];
-    if (ph.outp != nullptr)
+    for (int j = 0; j < DPL; ++j) pw[lane * DPL + j] = o[j];
+    if (lane == 0) {
+      pw[HD] = m;
+      pw[HD + 1] = l;
+    }
+    named_bar(1, kConsumers);
+    if (warp == 0) {
+      float M = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < DPL; ++j)
-        store_planes(ph.outp + static_cast<size_t>(jn) * 2 * (H * HD), H * HD, h * HD + lane * DPL + j, o[j]);
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, part[w * (HD + 2) + HD]);
+      float L = 0.f, O[DPL];
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) O[j] = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float mw = part[w * (HD + 2) + HD];
+        if (mw == -INFINITY) continue;  // a warp without slots
+        const float f = expf(mw - M);
+        L += part[w * (HD + 2) + HD + 1] * f;
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) O[j] += part[w * (HD + 2) + lane * DPL + j] * f;
+      }
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) {
+        const float ov = O[j] / L;
+        ph.out[static_cast<size_t>(jn) * (H * HD) + h * HD + lane * DPL + j] = ov;
+        if (ph.outp != nullptr)
+          store_planes(ph.outp + static_cast<size_t>(jn) * 2 * (H * HD), H * HD, h * HD + lane * DPL + j, ov);
+      }
+    }
+    named_bar(1, kConsumers);  // the partials are read before the next item overwrites them
   }
 }
 
@@ -1681,7 +1731,7 @@ __device__ void consumers(const CallParams& cp, Smem& S) {
       switch (ph.op) {
         case OP_GEMV:
           if (ph.merge_main && cta0) sample_main(cp, S, f);
-          else gemv<C>(cp, ph, S, pipe);
+          else pipe = gemv<C>(cp, ph, S, pipe);
           break;
         case OP_ATTN_SLOW:
           attn_slow<C>(cp, ph, S);
