@@ -238,11 +238,11 @@ void carve(s2_ctx* c, Carver& cv) {
   c->vc = cv.take<unsigned char>(kv);
   c->stage = cv.take<int32_t>(static_cast<size_t>(B) * kMaxFramesPerCall * d.ncb);
   c->x = cv.take<float>(2 * static_cast<size_t>(d.D));  // tagged words (bf16 models)
-  c->qkv = cv.take<float>(std::max(QKV, 1));
+  c->qkv = cv.take<float>(2 * static_cast<size_t>(std::max(QKV, 1)));  // tagged words (bf16 models)
   c->o = cv.take<float>(std::max(d.Hq * d.hd, 1));
   c->g = cv.take<float>(std::max(d.F, 1));
   c->fx = cv.take<float>(2 * static_cast<size_t>(d.Wf) * d.Df);
-  c->fqkv = cv.take<float>(2 * static_cast<size_t>(QKVf));
+  c->fqkv = cv.take<float>(4 * static_cast<size_t>(QKVf));  // two positions of tagged words
   c->fo = cv.take<float>(2 * static_cast<size_t>(d.Hqf) * d.hdf);
   c->fg = cv.take<float>(2 * static_cast<size_t>(d.Ff));
   c->op = cv.take<uint16_t>(2 * static_cast<size_t>(std::max(d.Hq * d.hd, 1)));
@@ -375,9 +375,19 @@ struct Builder {
     else last_write.emplace_back(p, n);
   }
   // tagged inputs take the distance to their writer; tagged outputs and write-backs are recorded;
-  // the residual-add and SwiGLU projections hand over without a grid barrier
-  void tag(Phase& p) {
-    if (!tagged() || p.op != OP_GEMV) return;
+  // the residual-add and SwiGLU projections, and a projection whose output only the next
+  // (attention) phase reads (`polled`), hand over without a grid barrier
+  void tag(Phase& p, bool polled) {
+    if (!tagged()) return;
+    if (p.op == OP_ATTN_SLOW || p.op == OP_ATTN_FAST) {
+      if (is_tagged(p.qkv)) {
+        const int* w = lw(p.qkv);
+        if (!w) err = "internal: a tagged attention input is read before it is written";
+        else p.qkv_tag_back = n - *w;
+      }
+      return;
+    }
+    if (p.op != OP_GEMV) return;
     for (int c = 0; c < p.ncols; ++c) {
       const GemvCol& col = p.col[c];
       if ((col.src == SRC_BUF || col.src == SRC_PLANES) && is_tagged(col.p)) {
@@ -398,7 +408,7 @@ struct Builder {
     }
     if (any_t && any_u) err = "internal: a phase mixes tagged and plain outputs";
     p.tag_out = any_t ? 1 : 0;
-    p.no_sync = (any_t && (p.epi == EPI_ADD || p.epi == EPI_SWIGLU)) ? 1 : 0;
+    p.no_sync = (any_t && (p.epi == EPI_ADD || p.epi == EPI_SWIGLU || polled)) ? 1 : 0;
     for (int c = 0; c < p.ncols; ++c) {
       if (p.y[c] && any_t) wrote(p.y[c]);
       if (p.yp[c] && any_t) wrote(p.yp[c]);
@@ -441,8 +451,8 @@ struct Builder {
     }
     return p;
   }
-  void push(Phase p) {
-    tag(p);
+  void push(Phase p, bool polled = false) {
+    tag(p, polled);
     const int g2 = grid - p.cta0;
     if (p.op == OP_GEMV && p.ncols == 2 && (p.col[0].src == SRC_PLANES) != (p.col[1].src == SRC_PLANES))
       err = "internal: a phase mixes planes and other activation sources";
@@ -478,9 +488,9 @@ struct Builder {
           if (l == 0 && p >= 1) q.col[j] = GemvCol{SRC_FEROW, 0, b.fcode + (p - 1), xp};
           else if (l == 0 && p == 0 && !d.has_proj) q.col[j] = buf(b.hidden_src, xp);
           else q.col[j] = buf(xp);
-          q.y[j] = b.fqkv + static_cast<size_t>(j) * QKVf;
+          q.y[j] = b.fqkv + static_cast<size_t>(j) * QKVf * xw();
         }
-        push(q);
+        push(q, true);  // read only by the attention phase that follows, which polls its words
         Phase a{};
         a.op = OP_ATTN_FAST;
         a.layer = l;
@@ -623,6 +633,8 @@ int build_programs(s2_ctx* c) {
   b.add_tagged(c->fx, 8ull * d.Wf * d.Df);
   b.add_tagged(c->gp, 8ull * std::max(d.F, 1));
   b.add_tagged(c->fgp, 16ull * d.Ff);
+  b.add_tagged(c->qkv, 8ull * std::max((d.Hq + 2 * d.Hkv) * d.hd, 1));
+  b.add_tagged(c->fqkv, 16ull * (d.Hqf + 2 * d.Hkvf) * d.hdf);
   const FastWts fw{c->fast.data(), c->P, c->FO, c->fnorm};
   for (int sid = 0; sid < c->max_streams && d.L > 0; ++sid) {
     const int before = b.n;
@@ -654,7 +666,7 @@ int build_programs(s2_ctx* c) {
       Phase q = b.gemv(QKV, d.D, 1, w.wqkv, nullptr, w.an, EPI_STORE);
       q.col[0] = l == 0 ? GemvCol{SRC_EMBED, 0, c->st[sid].vals, c->x} : Builder::buf(c->x);
       q.y[0] = c->qkv;
-      b.push(q);
+      b.push(q, true);  // read only by the attention phase that follows, which polls its words
       Phase a{};
       a.op = OP_ATTN_SLOW;
       a.layer = l;
@@ -804,7 +816,9 @@ int s2_frame_init(const s2_dims* s, const void* const* weights, int n_weights, v
       cudaMemset(c->st, 0, sizeof(StreamState) * (max_streams + 1)) != cudaSuccess ||
       // the tagged buffers start with tag 0, which no phase uses
       cudaMemset(c->x, 0, 8ull * d.D) != cudaSuccess || cudaMemset(c->fx, 0, 8ull * d.Wf * d.Df) != cudaSuccess ||
-      cudaMemset(c->gp, 0, 8ull * std::max(d.F, 1)) != cudaSuccess || cudaMemset(c->fgp, 0, 16ull * d.Ff) != cudaSuccess) {
+      cudaMemset(c->gp, 0, 8ull * std::max(d.F, 1)) != cudaSuccess || cudaMemset(c->fgp, 0, 16ull * d.Ff) != cudaSuccess ||
+      cudaMemset(c->qkv, 0, 8ull * std::max((d.Hq + 2 * d.Hkv) * d.hd, 1)) != cudaSuccess ||
+      cudaMemset(c->fqkv, 0, 16ull * (d.Hqf + 2 * d.Hkvf) * d.hdf) != cudaSuccess) {
     delete c;
     return fail(nullptr, S2_ECUDA, "initialising the workspace failed");
   }
@@ -1192,7 +1206,7 @@ size_t carve_static(const Dims& d, int n_phases, unsigned char* base, StaticLayo
   FastBufs& b = s.fb;
   b.hidden_src = cv.take<float>(d.D);
   b.fx = cv.take<float>(2 * static_cast<size_t>(d.Wf) * d.Df);
-  b.fqkv = cv.take<float>(2 * static_cast<size_t>(QKVf));
+  b.fqkv = cv.take<float>(4 * static_cast<size_t>(QKVf));
   b.fo = cv.take<float>(2 * static_cast<size_t>(d.Hqf) * d.hdf);
   b.fg = cv.take<float>(2 * static_cast<size_t>(d.Ff));
   b.fk = cv.take<float>(static_cast<size_t>(d.Lf) * d.Wf * d.Hkvf * d.hdf);
@@ -1284,6 +1298,7 @@ extern "C" int s2_fast_logits_static(const s2_dims* s, const void* const* weight
     Builder b{d, sd.grid, g_static_prog, kStaticMaxPhases};
     b.add_tagged(sl.fb.fx, 8ull * d.Wf * d.Df);
     b.add_tagged(sl.fb.fgp, 16ull * d.Ff);
+    b.add_tagged(sl.fb.fqkv, 16ull * (d.Hqf + 2 * d.Hkvf) * d.hdf);
     b.fast_alone(sl.fb, FastWts{g_static_layers, weights[base], weights[base + 3], weights[base + 2]});
     if (!b.err.empty()) return static_fail(S2_EINVAL, b.err);
     if (b.n != n_phases) return static_fail(S2_EINVAL, "internal: Fast-AR program length");

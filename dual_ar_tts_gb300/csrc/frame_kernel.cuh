@@ -250,6 +250,69 @@ __device__ __forceinline__ void wait_tagged(const CallParams& cp, Smem& S, const
   }
   if (miss != 0u) S.fail = 1;
 }
+// the same wait out of line (call sites whose registers are scarce: the attention phases)
+template <int N>
+__device__ __noinline__ void wait_tagged_nl(const CallParams& cp, Smem& S, const unsigned long long* const (&p)[N],
+                                         uint32_t tag, uint32_t miss, ulonglong2 (&v)[N]) {
+  const long long t0 = clock_us();
+  for (unsigned it = 1; miss != 0u; ++it) {
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if (miss & (1u << i)) {
+        v[i] = ldcg_u64x2(p[i]);
+        if (tags_are(v[i], tag)) miss &= ~(1u << i);
+      }
+    if (miss != 0u && (it & 15u) == 0u) {
+      if (ld_volatile_int(&cp.ctl->error) != 0 || *reinterpret_cast<volatile int*>(&S.fail) != 0) break;
+      if (clock_us() - t0 > cp.ctl->spin_limit) {
+        if (atomicCAS(&cp.ctl->error, 0, S2_ETIMEOUT) == 0) cp.ctl->error_where = 8;
+        break;
+      }
+    }
+  }
+  if (miss != 0u) S.fail = 1;
+}
+
+// DPL consecutive values of an attention phase's projection input (element e of ph.qkv): plain
+// floats, or tagged words of the projection phase (ph.qkv_tag_back > 0).  qkv_issue requests
+// them; qkv_ready waits for any word not yet stored and unpacks the values.
+template <int DPL>
+struct QkvWords {
+  ulonglong2 w[DPL / 2];
+  const unsigned long long* p;
+};
+template <int DPL>
+__device__ __forceinline__ void qkv_issue(const Phase& ph, size_t e, QkvWords<DPL>& t, float (&v)[DPL]) {
+  if (ph.qkv_tag_back > 0) {
+    t.p = reinterpret_cast<const unsigned long long*>(ph.qkv) + e;
+#pragma unroll
+    for (int i = 0; i < DPL / 2; ++i) t.w[i] = ldcg_u64x2(t.p + 2 * i);
+  } else {
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) v[j] = ldcg(ph.qkv + e + j);
+  }
+}
+template <int DPL>
+__device__ __forceinline__ void qkv_ready(const CallParams& cp, Smem& S, const Phase& ph, uint32_t tag,
+                                          QkvWords<DPL>& t, float (&v)[DPL]) {
+  if (ph.qkv_tag_back <= 0) return;
+  const uint32_t want = tag - static_cast<uint32_t>(ph.qkv_tag_back);
+  uint32_t miss = 0u;
+#pragma unroll
+  for (int i = 0; i < DPL / 2; ++i)
+    if (!tags_are(t.w[i], want)) miss |= 1u << i;
+  if (miss != 0u) {
+    const unsigned long long* ptr[DPL / 2];
+#pragma unroll
+    for (int i = 0; i < DPL / 2; ++i) ptr[i] = t.p + 2 * i;
+    wait_tagged_nl<DPL / 2>(cp, S, ptr, want, miss, t.w);
+  }
+#pragma unroll
+  for (int i = 0; i < DPL / 2; ++i) {
+    v[2 * i] = tval(t.w[i].x);
+    v[2 * i + 1] = tval(t.w[i].y);
+  }
+}
 
 // an output row of the phase's column c (read back for a residual add): tagged word or float
 __device__ __forceinline__ float ld_out(const Phase& ph, int c, int row) {
@@ -277,6 +340,7 @@ template <class C>
 __device__ void producer(const CallParams& cp, Smem& S) {
   const int lane = threadIdx.x & 31;
   constexpr int NQ = static_cast<int>(sizeof(Phase) / 16);
+  static_assert(NQ <= 32, "one 16-byte piece of a phase descriptor per producer lane");
   const uint64_t pol = policy_evict_first();
   Pipe pp{0, 0, 0, 0u};
   unsigned long long issued = 0;  // stages filled so far (all lanes keep the same count)
@@ -1189,7 +1253,7 @@ __device__ __forceinline__ void unpack_kv(const uint4& u, float (&f)[16 / sizeof
 // =========================================================================
 
 template <typename KT, int HD>
-__device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, Smem& S) {
+__device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, Smem& S, uint32_t tag) {
   constexpr int RB = HD * static_cast<int>(sizeof(KT));  // bytes per K/V row
   constexpr int RS = kXsStageBytes / RB;                 // slots per round (16, 32 or 64)
   constexpr int TPS = kConsumers / RS;                   // threads per slot in the scores
@@ -1252,8 +1316,9 @@ __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, 
       NormRope<DPL> nr;
       load_norm_rope<DPL>(nr, ph.qn, d.esz, d.qk_norm != 0, rope_row);
       float v[DPL];
-#pragma unroll
-      for (int j = 0; j < DPL; ++j) v[j] = ldcg(ph.qkv + h * HD + lane * DPL + j);
+      QkvWords<DPL> tq;
+      qkv_issue<DPL>(ph, static_cast<size_t>(h) * HD + lane * DPL, tq, v);
+      qkv_ready<DPL>(cp, S, ph, tag, tq, v);
       head_norm_rope<DPL>(v, nr, d.eps, HD, d.qk_norm != 0);
 #pragma unroll
       for (int j = 0; j < DPL; ++j) qs[warp * HD + lane * DPL + j] = v[j];
@@ -1261,11 +1326,11 @@ __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, 
       NormRope<DPL> nr;
       load_norm_rope<DPL>(nr, ph.kn, d.esz, d.qk_norm != 0, rope_row);
       float k[DPL], v[DPL];
-#pragma unroll
-      for (int j = 0; j < DPL; ++j) {
-        k[j] = ldcg(ph.qkv + (d.Hq + g) * HD + lane * DPL + j);
-        v[j] = ldcg(ph.qkv + (d.Hq + d.Hkv + g) * HD + lane * DPL + j);
-      }
+      QkvWords<DPL> tk, tv;
+      qkv_issue<DPL>(ph, static_cast<size_t>(d.Hq + g) * HD + lane * DPL, tk, k);
+      qkv_issue<DPL>(ph, static_cast<size_t>(d.Hq + d.Hkv + g) * HD + lane * DPL, tv, v);
+      qkv_ready<DPL>(cp, S, ph, tag, tk, k);
+      qkv_ready<DPL>(cp, S, ph, tag, tv, v);
       head_norm_rope<DPL>(k, nr, d.eps, HD, d.qk_norm != 0);
       KT* kd = const_cast<KT*>(Kc) + g * kvh + static_cast<size_t>(pos) * HD + lane * DPL;
       KT* vd = const_cast<KT*>(Vc) + g * kvh + static_cast<size_t>(pos) * HD + lane * DPL;
@@ -1444,8 +1509,8 @@ __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, 
 }
 
 template <class C>
-__device__ void attn_slow(const CallParams& cp, const Phase& ph, Smem& S) {
-  attn_slow_t<typename C::KT, C::hd>(cp, ph, S);
+__device__ void attn_slow(const CallParams& cp, const Phase& ph, Smem& S, uint32_t tag) {
+  attn_slow_t<typename C::KT, C::hd>(cp, ph, S, tag);
 }
 
 // =========================================================================
@@ -1455,7 +1520,7 @@ __device__ void attn_slow(const CallParams& cp, const Phase& ph, Smem& S) {
 // =========================================================================
 
 template <int HD>
-__device__ __noinline__ void attn_fast_t(const CallParams& cp, const Phase& ph, Smem& S) {
+__device__ __noinline__ void attn_fast_t(const CallParams& cp, const Phase& ph, Smem& S, uint32_t tag) {
   // One CTA per (position, query head); its eight warps split the window's slots (warp w: slots
   // w and w + 8), so each warp issues its few key / value loads at once instead of walking the
   // slots one dependent load after another.  Each warp keeps an online-softmax partial (max,
@@ -1479,27 +1544,29 @@ __device__ __noinline__ void attn_fast_t(const CallParams& cp, const Phase& ph, 
     NormRope<DPL> nq;
     load_norm_rope<DPL>(nq, ph.qn, d.esz, d.qk_norm != 0, cp.rope_f + static_cast<size_t>(p) * (HD / 2));
     float q[DPL];
-    const float* qrow = ph.qkv + static_cast<size_t>(jn) * QKV;
-#pragma unroll
-    for (int j = 0; j < DPL; ++j) q[j] = ldcg(qrow + h * HD + lane * DPL + j);
+    QkvWords<DPL> tq, tk[kSlotsPerWarp], tv[kSlotsPerWarp];
+    qkv_issue<DPL>(ph, static_cast<size_t>(jn) * QKV + h * HD + lane * DPL, tq, q);
     float k[kSlotsPerWarp][DPL], v[kSlotsPerWarp][DPL];
     NormRope<DPL> nk[kSlotsPerWarp];
 #pragma unroll
     for (int t = 0; t < kSlotsPerWarp; ++t) {
       const int s = warp + kConsumerWarps * t;
-      const bool fresh = s >= ph.pos0;
-      if (fresh && s <= p)
+      if (s > p) continue;  // uniform across the warp
+      if (s >= ph.pos0) {
         load_norm_rope<DPL>(nk[t], ph.kn, d.esz, d.qk_norm != 0, cp.rope_f + static_cast<size_t>(s) * (HD / 2));
-      const float* kr = fresh ? ph.qkv + static_cast<size_t>(s - ph.pos0) * QKV + (H + g) * HD
-                              : kc + (static_cast<size_t>(s) * Hk + g) * HD;
-      const float* vr = fresh ? ph.qkv + static_cast<size_t>(s - ph.pos0) * QKV + (H + Hk + g) * HD
-                              : vc + (static_cast<size_t>(s) * Hk + g) * HD;
+        const size_t row = static_cast<size_t>(s - ph.pos0) * QKV;
+        qkv_issue<DPL>(ph, row + (H + g) * HD + lane * DPL, tk[t], k[t]);
+        qkv_issue<DPL>(ph, row + (H + Hk + g) * HD + lane * DPL, tv[t], v[t]);
+      } else {
+        const size_t off = (static_cast<size_t>(s) * Hk + g) * HD + lane * DPL;
 #pragma unroll
-      for (int j = 0; j < DPL; ++j) {
-        k[t][j] = s <= p ? ldcg(kr + lane * DPL + j) : 0.f;
-        v[t][j] = s <= p ? ldcg(vr + lane * DPL + j) : 0.f;
+        for (int j = 0; j < DPL; ++j) {
+          k[t][j] = ldcg(kc + off + j);
+          v[t][j] = ldcg(vc + off + j);
+        }
       }
     }
+    qkv_ready<DPL>(cp, S, ph, tag, tq, q);
     head_norm_rope<DPL>(q, nq, d.eps, HD, d.qk_norm != 0);
     float m = -INFINITY, sc[kSlotsPerWarp];
 #pragma unroll
@@ -1509,6 +1576,8 @@ __device__ __noinline__ void attn_fast_t(const CallParams& cp, const Phase& ph, 
       if (s > p) continue;  // uniform across the warp
       if (s >= ph.pos0) {
         // a new position of this frame: its key is normalised and rotated here
+        qkv_ready<DPL>(cp, S, ph, tag, tk[t], k[t]);
+        qkv_ready<DPL>(cp, S, ph, tag, tv[t], v[t]);
         head_norm_rope<DPL>(k[t], nk[t], d.eps, HD, d.qk_norm != 0);
         if (s == p && (h % rep) == 0) {
 #pragma unroll
@@ -1572,8 +1641,8 @@ __device__ __noinline__ void attn_fast_t(const CallParams& cp, const Phase& ph, 
 }
 
 template <class C>
-__device__ void attn_fast(const CallParams& cp, const Phase& ph, Smem& S) {
-  attn_fast_t<C::hd>(cp, ph, S);
+__device__ void attn_fast(const CallParams& cp, const Phase& ph, Smem& S, uint32_t tag) {
+  attn_fast_t<C::hd>(cp, ph, S, tag);
 }
 
 // caller-supplied ids (forced draws, Fast-AR-alone prefixes) are checked before any use as an index
@@ -1734,10 +1803,10 @@ __device__ void consumers(const CallParams& cp, Smem& S) {
           else pipe = gemv<C>(cp, ph, S, pipe);
           break;
         case OP_ATTN_SLOW:
-          attn_slow<C>(cp, ph, S);
+          attn_slow<C>(cp, ph, S, pipe.tag);
           break;
         case OP_ATTN_FAST:
-          attn_fast<C>(cp, ph, S);
+          attn_fast<C>(cp, ph, S, pipe.tag);
           break;
         case OP_SAMPLE_FAST:
           if (cta0) sample_fast(cp, S, f, ph.cb);

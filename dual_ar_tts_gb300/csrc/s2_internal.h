@@ -125,6 +125,7 @@ struct alignas(16) Phase {
   // attention
   int layer, npos, pos0, cb;
   int bump_pos;          // CTA 0 advances the stream position after this phase
+  int qkv_tag_back;      // attention: 0 = qkv holds floats; n > 0 = tagged words stored n phases earlier
   float scale;           // attention: 1/sqrt(head_dim)
   const float* qkv;      // [npos][QKV]
   float* out;            // [npos][Hq*hd]
