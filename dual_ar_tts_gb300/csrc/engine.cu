@@ -1102,14 +1102,19 @@ int s2_sync_status(s2_ctx* c, CUstream_st* stream) {
   if (!c) return fail(nullptr, S2_EINVAL, "ctx is NULL");
   if (cudaStreamSynchronize(stream) != cudaSuccess)
     return fail(c, S2_ECUDA, std::string("stream synchronisation failed: ") + cudaGetErrorString(cudaGetLastError()));
-  int e[2] = {0, 0};
-  if (cudaMemcpy(e, &c->ctl->error, sizeof(e), cudaMemcpyDeviceToHost) != cudaSuccess)
+  Control h;
+  if (cudaMemcpy(&h, c->ctl, sizeof(Control), cudaMemcpyDeviceToHost) != cudaSuccess)
     return fail(c, S2_ECUDA, "reading the device status failed");
-  if (e[0] != 0) {
-    const int z[2] = {0, 0};
+  if (h.error != 0) {
+    const int z[3] = {0, 0, 0};
     cudaMemcpy(&c->ctl->error, z, sizeof(z), cudaMemcpyHostToDevice);
-    return fail(c, e[0], e[0] == S2_ETIMEOUT ? "a device-side wait gave up (site " + std::to_string(e[1]) + ")"
-                                             : "an input id was out of range");
+    if (h.error != S2_ETIMEOUT) return fail(c, h.error, "an input id was out of range");
+    std::string msg = "a device-side wait gave up (site " + std::to_string(h.error_where);
+    if (h.error_where != 10) {
+      msg += ", CTA " + std::to_string(h.error_cta);
+      if (h.error_phase >= 0) msg += ", phase " + std::to_string(h.error_phase) + " of the launch";
+    }
+    return fail(c, h.error, msg + ")");
   }
   return S2_OK;
 }

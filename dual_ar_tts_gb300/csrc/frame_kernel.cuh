@@ -50,6 +50,7 @@ struct Smem {
   int fail;         // a consumer wait gave up: leave at the next phase boundary
   int sync_ok;
   int flag;
+  int phase_k;      // the consumers' current phase index in the launch (failure reports)
   Phase ph[2];      // consumers: the current phase descriptor and the prefetched next one
   Phase pph[2];     // producer: the same, walked ahead of the consumers
   alignas(16) CallParams cp;         // the launch's parameters (shared, so that callees taking them by
@@ -99,6 +100,15 @@ __device__ __forceinline__ void rows_of(const Phase& ph, int cta, int G, int& r0
   nr = base + (i < rem ? 1 : 0);
 }
 
+// The first wait of a launch to give up records its site, CTA and the consumers' phase index.
+__device__ __forceinline__ void record_timeout(const CallParams& cp, int phase, int where) {
+  if (atomicCAS(&cp.ctl->error, 0, S2_ETIMEOUT) == 0) {
+    cp.ctl->error_where = where;
+    cp.ctl->error_cta = static_cast<int>(blockIdx.x);
+    cp.ctl->error_phase = phase;
+  }
+}
+
 // Bounded wait on an mbarrier phase; on give-up records the failure and returns false.
 // try_wait suspends in hardware until the phase completes or a short time limit passes; the
 // abort/failure flags (shared memory) are polled every 16 tries, the global error word and the
@@ -117,7 +127,7 @@ __device__ __noinline__ bool wait_bar_slow(const CallParams& cp, Smem& S, uint64
         const long long t = clock_us();
         if (t0 < 0) t0 = t;
         else if (t - t0 > cp.ctl->spin_limit) {
-          if (atomicCAS(&cp.ctl->error, 0, S2_ETIMEOUT) == 0) cp.ctl->error_where = where;
+          record_timeout(cp, *reinterpret_cast<volatile int*>(&S.phase_k), where);
           return false;
         }
       }
@@ -156,7 +166,7 @@ __device__ bool grid_sync(const CallParams& cp, Smem& S, unsigned& target) {
             break;
           }
           if (clock_us() - t0 > lim) {
-            if (atomicCAS(&cp.ctl->error, 0, S2_ETIMEOUT) == 0) cp.ctl->error_where = 1;
+            record_timeout(cp, S.phase_k, 1);
             ok = 0;
             break;
           }
@@ -206,7 +216,7 @@ __device__ __noinline__ void drain_copies(const CallParams& cp, uint64_t* bar, u
   const long long t0 = clock_us();
   while (!mbar_test(bar, parity)) {
     if (clock_us() - t0 > kDrainLimitUs) {
-      if (atomicCAS(&cp.ctl->error, 0, S2_ETIMEOUT) == 0) cp.ctl->error_where = where;
+      record_timeout(cp, -1, where);
       break;
     }
   }
@@ -243,7 +253,7 @@ __device__ __forceinline__ void wait_tagged(const CallParams& cp, Smem& S, const
     if (miss != 0u && (it & 15u) == 0u) {
       if (ld_volatile_int(&cp.ctl->error) != 0 || *reinterpret_cast<volatile int*>(&S.fail) != 0) break;
       if (clock_us() - t0 > cp.ctl->spin_limit) {
-        if (atomicCAS(&cp.ctl->error, 0, S2_ETIMEOUT) == 0) cp.ctl->error_where = 8;
+        record_timeout(cp, S.phase_k, 8);
         break;
       }
     }
@@ -265,7 +275,7 @@ __device__ __noinline__ void wait_tagged_nl(const CallParams& cp, Smem& S, const
     if (miss != 0u && (it & 15u) == 0u) {
       if (ld_volatile_int(&cp.ctl->error) != 0 || *reinterpret_cast<volatile int*>(&S.fail) != 0) break;
       if (clock_us() - t0 > cp.ctl->spin_limit) {
-        if (atomicCAS(&cp.ctl->error, 0, S2_ETIMEOUT) == 0) cp.ctl->error_where = 8;
+        record_timeout(cp, S.phase_k, 8);
         break;
       }
     }
@@ -924,6 +934,7 @@ __device__ __noinline__ Pipe gemv_tiles(const CallParams& cp, const Phase& ph, S
   const uint32_t b_ld = order_after(xsb) + static_cast<uint32_t>((lane & 7) % (2 * NC)) * xpitch +
                         static_cast<uint32_t>((lane >> 3) & 1) * 16u;
   const uint32_t red = smem_u32(S.red);
+  const int P = nr * ph.nmat * NC;  // partials per warp: [warp][row, matrix, column], conflict-free sums
   const int g = lane >> 2, t = lane & 3;  // D fragment: rows g and g + 8, columns 2t and 2t + 1
   for (int b = 0; b < nr; b += kTileRows) {
     const int rows = min(kTileRows, nr - b);
@@ -974,7 +985,7 @@ __device__ __noinline__ Pipe gemv_tiles(const CallParams& cp, const Phase& ph, S
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
           const float v = warp_sum(dv[c]);
-          if (lane == 0) sts32f(red + 4u * ((((b * nmat + m) * NC + c) * kConsumerWarps) + warp), v);
+          if (lane == 0) sts32f(red + 4u * (warp * P + (b * nmat + m) * NC + c), v);
         }
         continue;
       }
@@ -1024,8 +1035,8 @@ __device__ __noinline__ Pipe gemv_tiles(const CallParams& cp, const Phase& ph, S
                          ((acc[0][1] + acc[1][1]) + (acc[2][1] + acc[3][1]));
         const float v1 = ((acc[0][2] + acc[1][2]) + (acc[2][2] + acc[3][2])) +
                          ((acc[0][3] + acc[1][3]) + (acc[2][3] + acc[3][3]));
-        if (g < rows) sts32f(red + 4u * ((((b + g) * nmat + m) * NC + t) * kConsumerWarps + warp), v0);
-        if (g + 8 < rows) sts32f(red + 4u * ((((b + g + 8) * nmat + m) * NC + t) * kConsumerWarps + warp), v1);
+        if (g < rows) sts32f(red + 4u * (warp * P + ((b + g) * nmat + m) * NC + t), v0);
+        if (g + 8 < rows) sts32f(red + 4u * (warp * P + ((b + g + 8) * nmat + m) * NC + t), v1);
       }
     }
   }
@@ -1037,9 +1048,11 @@ __device__ __noinline__ Pipe gemv_tiles(const CallParams& cp, const Phase& ph, S
     for (int idx = tid; idx < nout; idx += kConsumers) {
       const int rl = idx / NC, c = idx % NC;
       float a = 0.f, bb = 0.f;
-      for (int w = 0; w < kConsumerWarps; ++w) a += S.red[((rl * nmat + 0) * NC + c) * kConsumerWarps + w];
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) a += S.red[w * P + (rl * nmat + 0) * NC + c];
       if (nmat == 2)
-        for (int w = 0; w < kConsumerWarps; ++w) bb += S.red[((rl * nmat + 1) * NC + c) * kConsumerWarps + w];
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) bb += S.red[w * P + (rl * nmat + 1) * NC + c];
       float v;
       if (ph.epi == EPI_STORE) {
         v = a;
@@ -1794,9 +1807,12 @@ __device__ void consumers(const CallParams& cp, Smem& S) {
       int np = p + 1;
       if (np == cp.n_phases) np = 0;
       const bool has_next = (p + 1 < cp.n_phases) || (f + 1 < cp.n_frames);
-      uint4 nx = make_uint4(0u, 0u, 0u, 0u);
-      if (tid < NQ && has_next) nx = __ldg(reinterpret_cast<const uint4*>(cp.prog + np) + tid);
+      // the next descriptor travels into the other slot while this phase runs (an async copy, so
+      // that no register holds it and its load is not deferred to the end of the phase)
+      if (tid < NQ && has_next)
+        cp_async16(reinterpret_cast<uint4*>(&S.ph[(k + 1) & 1]) + tid, reinterpret_cast<const uint4*>(cp.prog + np) + tid);
       pipe.tag = cp.tag0 + static_cast<uint32_t>(k);
+      if (tid == 0) S.phase_k = k;
       switch (ph.op) {
         case OP_GEMV:
           if (ph.merge_main && cta0) sample_main(cp, S, f);
@@ -1823,7 +1839,7 @@ __device__ void consumers(const CallParams& cp, Smem& S) {
       if (ph.bump_pos && cta0 && tid == 0) {
         cp.st->pos = cp.st->pos + 1;  // the Slow-AR step's last phase: its slot is now filled
       }
-      if (tid < NQ && has_next) reinterpret_cast<uint4*>(&S.ph[(k + 1) & 1])[tid] = nx;
+      if (tid < NQ) cp_async_wait_all();
       if (ph.no_sync) {
         // the next phase polls this phase's tagged outputs: only this CTA's threads meet here
         named_bar(1, kConsumers);
@@ -1858,6 +1874,7 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constan
     S.fail = 0;
     S.sync_ok = 1;
     S.flag = 0;
+    S.phase_k = -1;
     fence_barrier_init();
   }
   __syncthreads();

@@ -88,8 +88,10 @@ struct Control {
   unsigned gbar;            // grid barrier counter (reset before each launch)
   int error;                // device-detected failure (S2_ETIMEOUT) of any launch
   int error_where;          // which wait gave up
-  int pad;
+  int error_cta;            // the CTA (frame kernel) whose wait gave up first
   long long spin_limit;     // wait bound in ~1 µs units
+  int error_phase;          // that CTA's phase index within its launch (frame kernel; -1 unknown)
+  int pad;
   unsigned tickets[64];     // split-K attention: arrivals per KV head
 };
 

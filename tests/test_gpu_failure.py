@@ -24,7 +24,15 @@ def test_wait_bound_gives_timeout_status_and_the_context_recovers():
     pkg.s2_set_spin_limit(dec.ctx, 1)  # about 1 us: a grid barrier or pipeline wait gives up
     dec.decode(n, s, expo)
     assert dec.sync_status() == pkg.S2_ETIMEOUT
-    assert "gave up" in pkg.s2_last_error(dec.ctx)
+    msg = pkg.s2_last_error(dec.ctx)
+    assert "gave up" in msg
+    # the report names the wait, the CTA and (for the consumers' waits) the phase of the launch
+    import re
+    m = re.search(r"site (\d+), CTA (\d+)(, phase (\d+) of the launch)?\)", msg)
+    assert m, msg
+    assert 0 <= int(m.group(2)) < 1024
+    if m.group(4) is not None:
+        assert 0 <= int(m.group(4)) < n * pkg.s2_phase_count(dec.ctx)
 
     pkg.s2_set_spin_limit(dec.ctx, 0)  # the default bound again
     dec.prefill([prompt])
