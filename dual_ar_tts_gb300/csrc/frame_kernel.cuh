@@ -229,8 +229,13 @@ __device__ __noinline__ void drain_copies(const CallParams& cp, uint64_t* bar, u
 __device__ __forceinline__ unsigned long long tagw(uint32_t bits, uint32_t tag) {
   return (static_cast<unsigned long long>(tag) << 32) | bits;
 }
+// Polled words are read with relaxed loads at GPU scope (morally strong): a weak load in a polling
+// loop has no visibility guarantee, and on this two-die part it was seen to keep returning a stale
+// copy of a word for a second after the word had been stored.
 __device__ __forceinline__ ulonglong2 ldcg_u64x2(const unsigned long long* p) {
-  return __ldcg(reinterpret_cast<const ulonglong2*>(p));
+  ulonglong2 v;
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p));
+  return v;
 }
 __device__ __forceinline__ bool tags_are(const ulonglong2& a, uint32_t tag) {
   return static_cast<uint32_t>(a.x >> 32) == tag && static_cast<uint32_t>(a.y >> 32) == tag;
@@ -725,7 +730,8 @@ __device__ __forceinline__ void tile_steps(uint32_t tb, uint32_t a_off, uint32_t
 }
 
 template <int NC>
-__device__ __noinline__ Pipe gemv_tiles(const CallParams& cp, const Phase& ph, Smem& S, Pipe pipe, float yres);
+__device__ __noinline__ Pipe gemv_tiles(const CallParams& cp, const Phase& ph, Smem& S, Pipe pipe, float yres,
+                                         float rs0 = 1.f, float rs1 = 1.f);
 
 // GEMV prologue for activations of at most GM·1024 elements per column: the columns into registers
 // (GM float4 groups per thread), RMSNorm, the bf16 hi/lo split into shared memory; then the tiles.
@@ -849,47 +855,36 @@ __device__ __noinline__ Pipe gemv_mma(const CallParams& cp, const Phase& ph, Sme
       }
     }
   }
-  // ---- RMSNorm in fp32 (block reduction of the sum of squares)
+  // ---- RMSNorm in fp32, with the scale applied after the projection: the activation is multiplied
+  // by the norm weight and split at once, the sum of squares is reduced meanwhile, and
+  // W·(x·r·w) = r·(W·(x·w)) takes r = 1/sqrt(mean(x²) + eps) in the epilogue
   if (has_norm) {
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
       const float t = warp_sum(ss[c]);
       if (lane == 0) S.misc[kMiscSS + warp * NC + c] = t;
     }
-  }
-  named_bar(1, kConsumers);
-  if (has_norm) {
     const bool ok = wait_bar(cp, S, &S.full[pipe.stage], pipe.round & 1u, 5, false);
     if (!ok) S.fail = 1;
     const uint32_t nws = smem_u32(S.ring[pipe.stage]);
 #pragma unroll
-    for (int c = 0; c < NC; ++c) {
-      float tot = 0.f;
-      for (int w = 0; w < kConsumerWarps; ++w) tot += S.misc[kMiscSS + w * NC + c];
-      const float r = 1.0f / sqrtf(tot / static_cast<float>(K) + d.eps);
+    for (int j = 0; j < GM; ++j) {
+      const int g = tid + kConsumers * j;
+      if (g < ng) {
+        const uint32_t w01 = lds32(nws + 8u * g), w23 = lds32(nws + 8u * g + 4u);
 #pragma unroll
-      for (int j = 0; j < GM; ++j) {
-        const int g = tid + kConsumers * j;
-        if (g < ng) {
-          const uint32_t w01 = lds32(nws + 8u * g), w23 = lds32(nws + 8u * g + 4u);
+        for (int c = 0; c < NC; ++c) {
           float4& v = xv[c][j];
-          v.x = (v.x * r) * bf16lo(w01);
-          v.y = (v.y * r) * bf16hi(w01);
-          v.z = (v.z * r) * bf16lo(w23);
-          v.w = (v.w * r) * bf16hi(w23);
+          v.x *= bf16lo(w01);
+          v.y *= bf16hi(w01);
+          v.z *= bf16lo(w23);
+          v.w *= bf16hi(w23);
         }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.empty[pipe.stage]);
     pipe.advance();
-    if (blockIdx.x == 0 && ph.hid_out != nullptr) {
-#pragma unroll
-      for (int j = 0; j < GM; ++j) {
-        const int g = tid + kConsumers * j;
-        if (g < ng) *reinterpret_cast<float4*>(ph.hid_out + 4 * g) = xv[0][j];
-      }
-    }
   }
   // ---- split into bf16 hi and lo rows: xs row 2c = hi, row 2c+1 = lo (rows padded by 16 bytes so
   // the rows of one ldmatrix sit in different banks)
@@ -914,12 +909,33 @@ __device__ __noinline__ Pipe gemv_mma(const CallParams& cp, const Phase& ph, Sme
     }
   }
   named_bar(1, kConsumers);
+  float rs[2] = {1.f, 1.f};
+  if (has_norm) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) tot += S.misc[kMiscSS + w * NC + c];
+      rs[c] = 1.0f / sqrtf(tot / static_cast<float>(K) + d.eps);
+    }
+    if (blockIdx.x == 0 && ph.hid_out != nullptr) {
+#pragma unroll
+      for (int j = 0; j < GM; ++j) {
+        const int g = tid + kConsumers * j;
+        if (g < ng) {
+          const float4 v = xv[0][j];
+          *reinterpret_cast<float4*>(ph.hid_out + 4 * g) = make_float4(v.x * rs[0], v.y * rs[0], v.z * rs[0], v.w * rs[0]);
+        }
+      }
+    }
+  }
 
-  return gemv_tiles<NC>(cp, ph, S, pipe, yres);
+  return gemv_tiles<NC>(cp, ph, S, pipe, yres, rs[0], rs[1]);
 }
 
 template <int NC>
-__device__ __noinline__ Pipe gemv_tiles(const CallParams& cp, const Phase& ph, Smem& S, Pipe pipe, float yres) {
+__device__ __noinline__ Pipe gemv_tiles(const CallParams& cp, const Phase& ph, Smem& S, Pipe pipe, float yres,
+                                         float rs0, float rs1) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int K = ph.K;
   int r0, nr;
@@ -1053,6 +1069,10 @@ __device__ __noinline__ Pipe gemv_tiles(const CallParams& cp, const Phase& ph, S
       if (nmat == 2)
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) bb += S.red[w * P + (rl * nmat + 1) * NC + c];
+      // the norm scale of the column (1 without a norm)
+      const float rsc = c == 0 ? rs0 : rs1;
+      a *= rsc;
+      bb *= rsc;
       float v;
       if (ph.epi == EPI_STORE) {
         v = a;
