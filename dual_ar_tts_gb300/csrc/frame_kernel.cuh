@@ -51,6 +51,7 @@ struct Smem {
   int sync_ok;
   int flag;
   int phase_k;      // the consumers' current phase index in the launch (failure reports)
+  int pos_frame;    // the Slow-AR slot of the current frame (the stream position at the launch + f)
   Phase ph[2];      // consumers: the current phase descriptor and the prefetched next one
   Phase pph[2];     // producer: the same, walked ahead of the consumers
   alignas(16) CallParams cp;         // the launch's parameters (shared, so that callees taking them by
@@ -1298,7 +1299,7 @@ __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, 
   const Dims& d = cp.d;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rep = d.Hq / d.Hkv;
-  const int pos = ldcgi(&cp.st->pos);
+  const int pos = S.pos_frame;
   const int n = pos + 1;
   const int G = gridDim.x;
   int ns, chunk;
@@ -1482,16 +1483,13 @@ __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, 
     }
     // ---- the last split of this KV head to arrive combines all of them:
     //   o = Σ_s e^{m_s - M} o_s / Σ_s e^{m_s - M} l_s
-    __threadfence();
+    // The CTA's partials are ordered before thread 0's ticket by the barrier; the ticket is a
+    // release (publishing them) and an acquire (the last arriver sees every split's partials).
     named_bar(1, kConsumers);
     if (tid == 0) {
-      __threadfence();
-      const unsigned t = atomicAdd(&cp.ctl->tickets[g], 1u);
+      const unsigned t = atom_add_acq_rel_gpu(&cp.ctl->tickets[g], 1u);
       S.flag = (t == static_cast<unsigned>(ns - 1)) ? 1 : 0;
-      if (S.flag) {
-        __threadfence();
-        cp.ctl->tickets[g] = 0u;
-      }
+      if (S.flag) cp.ctl->tickets[g] = 0u;  // every split of this item has arrived
     }
     named_bar(1, kConsumers);
     if (S.flag) {
@@ -1819,9 +1817,13 @@ __device__ void consumers(const CallParams& cp, Smem& S) {
   if (cta0 && tid == 0) cp.st->n_out = 0;
   // phase descriptors live in shared memory; the next one is fetched while the current one runs
   if (tid < NQ) reinterpret_cast<uint4*>(&S.ph[0])[tid] = __ldg(reinterpret_cast<const uint4*>(cp.prog) + tid);
+  // the stream position advances by one per frame (the last phase of a frame bumps it), so the
+  // slot of frame f is the position at the launch + f: read once here, not in every layer
+  const int pos_launch = cp.fast_only ? 0 : ldcgi(&cp.st->pos);
   named_bar(1, kConsumers);
   int k = 0;
   for (int f = 0; f < cp.n_frames; ++f) {
+    if (tid == 0) S.pos_frame = pos_launch + f;
     for (int p = 0; p < cp.n_phases; ++p, ++k) {
       const Phase& ph = S.ph[k & 1];
       int np = p + 1;
