@@ -52,6 +52,8 @@ struct Smem {
   int flag;
   int phase_k;      // the consumers' current phase index in the launch (failure reports)
   int pos_frame;    // the Slow-AR slot of the current frame (the stream position at the launch + f)
+  int attn_ns, attn_chunk, attn_g, attn_s, attn_rep;  // the frame's Slow-AR attention plan (this CTA's item)
+  const float* attn_pml;
   Phase ph[2];      // consumers: the current phase descriptor and the prefetched next one
   Phase pph[2];     // producer: the same, walked ahead of the consumers
   alignas(16) CallParams cp;         // the launch's parameters (shared, so that callees taking them by
@@ -1286,6 +1288,45 @@ __device__ __forceinline__ void unpack_kv(const uint4& u, float (&f)[16 / sizeof
 // each a 32-byte part of the row; P·V: each thread owns fixed (head, element) outputs.
 // =========================================================================
 
+// The combine of the Slow-AR split partials of KV head g (the last split to arrive): for each of
+// its rep heads h and elements e, o = Σ_s e^{m_s - M} o_s / Σ_s e^{m_s - M} l_s over the ns splits
+// in split order; (m_s, l_s) of head h at mls[2 (h ns + s)].  NSM bounds ns (the unrolled length).
+template <int NSM, int HD>
+__device__ __forceinline__ void combine_splits(const CallParams& cp, const Phase& ph, const float* mls, int g, int ns,
+                                               int rep) {
+  static_assert(4 * HD <= 2 * kConsumers, "combine outputs per thread");
+  const int tid = threadIdx.x;
+  float pv[2][NSM];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int idx = tid + q * kConsumers, r = idx / HD, e = idx % HD;
+#pragma unroll
+    for (int s2 = 0; s2 < NSM; ++s2)
+      pv[q][s2] = (idx < rep * HD && s2 < ns) ? ldcg(cp.part + (static_cast<size_t>(g * ns + s2) * 4 + r) * HD + e) : 0.f;
+  }
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int idx = tid + q * kConsumers, r = idx / HD, e = idx % HD;
+    if (idx >= rep * HD) continue;
+    const float* mr = mls + 2 * r * ns;
+    float M = -INFINITY;
+#pragma unroll
+    for (int s2 = 0; s2 < NSM; ++s2)
+      if (s2 < ns) M = fmaxf(M, mr[2 * s2]);
+    float o = 0.f, l = 0.f;
+#pragma unroll
+    for (int s2 = 0; s2 < NSM; ++s2) {
+      if (s2 < ns) {
+        const float w = expf(mr[2 * s2] - M);
+        o += w * pv[q][s2];
+        l += w * mr[2 * s2 + 1];
+      }
+    }
+    ph.out[(g * rep + r) * HD + e] = o / l;
+    if (ph.outp != nullptr) store_planes(ph.outp, cp.d.Hq * HD, (g * rep + r) * HD + e, o / l);
+  }
+}
+
 template <typename KT, int HD>
 __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, Smem& S, uint32_t tag) {
   constexpr int RB = HD * static_cast<int>(sizeof(KT));  // bytes per K/V row
@@ -1298,12 +1339,11 @@ __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, 
   static_assert(RS <= 64 && EPS * static_cast<int>(sizeof(KT)) == 32, "attention round layout");
   const Dims& d = cp.d;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int rep = d.Hq / d.Hkv;
+  const int rep = S.attn_rep;
   const int pos = S.pos_frame;
   const int n = pos + 1;
   const int G = gridDim.x;
-  int ns, chunk;
-  attn_split(n, G, d.Hkv, ns, chunk);
+  const int ns = S.attn_ns, chunk = S.attn_chunk;
   const int nitems = d.Hkv * ns;
   const float sc_mul = ph.scale;  // 1/sqrt(head_dim)
   const size_t kvh = static_cast<size_t>(cp.kv_slots) * HD;  // elements per KV head
@@ -1318,12 +1358,13 @@ __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, 
   float* vnew = xsf + kXsKV + 128;
   float* ps = xsf + kXsSc;
   float* stat = xsf + kXsStat;
-  float* pml = const_cast<float*>(attn_part_ml(cp, G));
+  float* pml = const_cast<float*>(S.attn_pml);
   const int ss = tid / TPS, sp = tid % TPS;  // scores: slot, part
   const int oe = tid % HD, oh = tid / HD;    // P·V: element, first head (then + kConsumers / HD)
 
   for (int item = blockIdx.x; item < nitems; item += G) {
-    const int g = item / ns, s = item % ns;
+    const bool own = item == static_cast<int>(blockIdx.x);  // the item planned at the frame start
+    const int g = own ? S.attn_g : item / ns, s = own ? S.attn_s : item % ns;
     const int j0 = s * chunk, j1 = min(n, j0 + chunk);
     const bool has_new = (j1 == n);
     const int nrounds = (j1 - j0 + RS - 1) / RS;
@@ -1503,37 +1544,10 @@ __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, 
       }
       named_bar(1, kConsumers);
       // at most 4 heads x 128 elements: two outputs per thread, every split's partial of both
-      // requested at once (the sums keep split order)
-      static_assert(4 * HD <= 2 * kConsumers, "combine outputs per thread");
-      float pv[2][kAttnMaxSplits];
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int idx = tid + q * kConsumers, r = idx / HD, e = idx % HD;
-#pragma unroll
-        for (int s2 = 0; s2 < kAttnMaxSplits; ++s2)
-          pv[q][s2] = (idx < rep * HD && s2 < ns)
-                          ? ldcg(cp.part + (static_cast<size_t>(g * ns + s2) * 4 + r) * HD + e) : 0.f;
-      }
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int idx = tid + q * kConsumers, r = idx / HD, e = idx % HD;
-        if (idx >= rep * HD) continue;
-        const float* mr = mls + 2 * r * ns;
-        float M = -INFINITY;
-#pragma unroll 1
-        for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, mr[2 * s2]);
-        float o = 0.f, l = 0.f;
-#pragma unroll
-        for (int s2 = 0; s2 < kAttnMaxSplits; ++s2) {
-          if (s2 < ns) {
-            const float w = expf(mr[2 * s2] - M);
-            o += w * pv[q][s2];
-            l += w * mr[2 * s2 + 1];
-          }
-        }
-        ph.out[(g * rep + r) * HD + e] = o / l;
-        if (ph.outp != nullptr) store_planes(ph.outp, d.Hq * HD, (g * rep + r) * HD + e, o / l);
-      }
+      // requested at once (the sums keep split order); the unrolled length follows ns
+      if (ns <= 8) combine_splits<8, HD>(cp, ph, mls, g, ns, rep);
+      else if (ns <= 16) combine_splits<16, HD>(cp, ph, mls, g, ns, rep);
+      else combine_splits<kAttnMaxSplits, HD>(cp, ph, mls, g, ns, rep);
     }
     named_bar(1, kConsumers);
   }
@@ -1823,7 +1837,21 @@ __device__ void consumers(const CallParams& cp, Smem& S) {
   named_bar(1, kConsumers);
   int k = 0;
   for (int f = 0; f < cp.n_frames; ++f) {
-    if (tid == 0) S.pos_frame = pos_launch + f;
+    if (tid == 0) {
+      // the Slow-AR attention plan depends on the frame's slot only: its integer divisions are
+      // taken once per frame, not in every layer
+      S.pos_frame = pos_launch + f;
+      if (!cp.fast_only && cp.d.L > 0) {
+        int ns, chunk;
+        attn_split(pos_launch + f + 1, static_cast<int>(gridDim.x), cp.d.Hkv, ns, chunk);
+        S.attn_ns = ns;
+        S.attn_chunk = chunk;
+        S.attn_g = static_cast<int>(blockIdx.x) / ns;
+        S.attn_s = static_cast<int>(blockIdx.x) % ns;
+        S.attn_rep = cp.d.Hq / cp.d.Hkv;
+        S.attn_pml = attn_part_ml(cp, static_cast<int>(gridDim.x));
+      }
+    }
     for (int p = 0; p < cp.n_phases; ++p, ++k) {
       const Phase& ph = S.ph[k & 1];
       int np = p + 1;
