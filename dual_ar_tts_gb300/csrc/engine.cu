@@ -454,6 +454,11 @@ struct Builder {
   void push(Phase p, bool polled = false) {
     tag(p, polled);
     const int g2 = grid - p.cta0;
+    if (g2 > 0) {
+      // the device splits the rows without dividing (rows_of)
+      p.rows_base = p.M / g2;
+      p.rows_rem = p.M % g2;
+    }
     if (p.op == OP_GEMV && p.ncols == 2 && (p.col[0].src == SRC_PLANES) != (p.col[1].src == SRC_PLANES))
       err = "internal: a phase mixes planes and other activation sources";
     if (p.op == OP_GEMV && p.col[0].src == SRC_PLANES && p.normw != nullptr) err = "internal: normalised planes input";

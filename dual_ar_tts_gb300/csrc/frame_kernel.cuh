@@ -54,6 +54,7 @@ struct Smem {
   int pos_frame;    // the Slow-AR slot of the current frame (the stream position at the launch + f)
   int attn_ns, attn_chunk, attn_g, attn_s, attn_rep;  // the frame's Slow-AR attention plan (this CTA's item)
   const float* attn_pml;
+  int fa_j, fa_h, fa_g, fa_rep;  // Fast-AR attention: this CTA's (position, head, KV head) item
   Phase ph[2];      // consumers: the current phase descriptor and the prefetched next one
   Phase pph[2];     // producer: the same, walked ahead of the consumers
   alignas(16) CallParams cp;         // the launch's parameters (shared, so that callees taking them by
@@ -98,7 +99,7 @@ __device__ __forceinline__ void rows_of(const Phase& ph, int cta, int G, int& r0
     nr = 0;
     return;
   }
-  const int base = ph.M / g2, rem = ph.M % g2;
+  const int base = ph.rows_base, rem = ph.rows_rem;  // M / (G - cta0), M % (G - cta0), from the host
   r0 = i * base + (i < rem ? i : rem);
   nr = base + (i < rem ? 1 : 0);
 }
@@ -1574,7 +1575,7 @@ __device__ __noinline__ void attn_fast_t(const CallParams& cp, const Phase& ph, 
   constexpr int kSlotsPerWarp = 2;  // window <= 16 positions
   const Dims& d = cp.d;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int H = d.Hqf, Hk = d.Hkvf, rep = H / Hk;
+  const int H = d.Hqf, Hk = d.Hkvf, rep = S.fa_rep;
   const int QKV = (H + 2 * Hk) * HD;
   const int nitems = ph.npos * H;
   const float sc_mul = ph.scale;
@@ -1582,7 +1583,8 @@ __device__ __noinline__ void attn_fast_t(const CallParams& cp, const Phase& ph, 
   float* vc = static_cast<float*>(ph.vc);
   float* part = reinterpret_cast<float*>(S.xs);  // per warp: o[HD], max, sum
   for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
-    const int jn = item / H, h = item % H, g = h / rep;
+    const bool own = item == static_cast<int>(blockIdx.x);  // the item planned at the launch start
+    const int jn = own ? S.fa_j : item / H, h = own ? S.fa_h : item % H, g = own ? S.fa_g : h / rep;
     const int p = ph.pos0 + jn;
     // every load first: the query, and the keys / values of this warp's slots (the frame's new
     // positions from the projection output, earlier ones from the window cache)
@@ -1834,6 +1836,13 @@ __device__ void consumers(const CallParams& cp, Smem& S) {
   // the stream position advances by one per frame (the last phase of a frame bumps it), so the
   // slot of frame f is the position at the launch + f: read once here, not in every layer
   const int pos_launch = cp.fast_only ? 0 : ldcgi(&cp.st->pos);
+  if (tid == 0) {
+    // the Fast-AR attention item of this CTA, fixed for the launch (no division per phase)
+    S.fa_rep = cp.d.Hqf / cp.d.Hkvf;
+    S.fa_j = static_cast<int>(blockIdx.x) / cp.d.Hqf;
+    S.fa_h = static_cast<int>(blockIdx.x) % cp.d.Hqf;
+    S.fa_g = S.fa_h / S.fa_rep;
+  }
   named_bar(1, kConsumers);
   int k = 0;
   for (int f = 0; f < cp.n_frames; ++f) {

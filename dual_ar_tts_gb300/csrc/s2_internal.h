@@ -128,6 +128,7 @@ struct alignas(16) Phase {
   int layer, npos, pos0, cb;
   int bump_pos;          // CTA 0 advances the stream position after this phase
   int qkv_tag_back;      // attention: 0 = qkv holds floats; n > 0 = tagged words stored n phases earlier
+  int rows_base, rows_rem;  // GEMV rows per CTA: the first rows_rem CTAs (after cta0) take rows_base + 1
   float scale;           // attention: 1/sqrt(head_dim)
   const float* qkv;      // [npos][QKV]
   float* out;            // [npos][Hq*hd]
