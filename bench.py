@@ -28,7 +28,7 @@ METRIC = "codec frames/sec per stream & aggregate (S2-Pro shapes); HBM GB/s vs 8
 # measured against 16.611 GB algorithmic; the capture's summary is committed with the profiles).  Traffic grows
 # with the weights and KV streamed, so the full launch's traffic is this ratio times its
 # algorithmic bytes.  Set to None when the kernel changes until a new capture is taken.
-NCU_TRAFFIC_RATIO = 1.0020
+NCU_TRAFFIC_RATIO = None
 WORKLOAD = "full-frame Dual-AR decode, S2-Pro shapes (36+4 layers, dim 2560, vocab 155776), batch 1"
 PROMPT_LEN = 512
 

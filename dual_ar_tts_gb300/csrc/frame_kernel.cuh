@@ -1260,22 +1260,23 @@ __device__ __forceinline__ __half f_to_kv<__half>(float x) { return __float2half
 template <>
 __device__ __forceinline__ float f_to_kv<float>(float x) { return x; }
 
-// one 16-byte chunk of a K/V row to fp32
+// four consecutive elements of a K/V row in shared memory (8- or 16-byte aligned) to fp32
 template <typename KT>
-__device__ __forceinline__ void unpack_kv(const uint4& u, float (&f)[16 / sizeof(KT)]) {
+__device__ __forceinline__ void load4_kv(const KT* p, float (&f)[4]) {
   if constexpr (sizeof(KT) == 2) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&w[t]));
-      f[2 * t] = f2.x;
-      f[2 * t + 1] = f2.y;
-    }
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    f[0] = a.x;
+    f[1] = a.y;
+    f[2] = b.x;
+    f[3] = b.y;
   } else {
-    f[0] = __uint_as_float(u.x);
-    f[1] = __uint_as_float(u.y);
-    f[2] = __uint_as_float(u.z);
-    f[3] = __uint_as_float(u.w);
+    const float4 u = *reinterpret_cast<const float4*>(p);
+    f[0] = u.x;
+    f[1] = u.y;
+    f[2] = u.z;
+    f[3] = u.w;
   }
 }
 
@@ -1286,7 +1287,10 @@ __device__ __forceinline__ void unpack_kv(const uint4& u, float (&f)[16 / sizeof
 // max and denominator, and the last split of a KV head to finish combines them.
 // Rounds of RS slots: the K and V rows of the next round are copied into shared memory
 // (cp.async, double-buffered) while the current one is processed.  Scores: TPS threads per slot,
-// each a 32-byte part of the row; P·V: each thread owns fixed (head, element) outputs.
+// thread sp taking the 4-element chunks sp, sp + TPS, ... of the row, so that at each step the
+// threads of a slot read one contiguous span of q (a broadcast across the warp's slots, free of
+// bank conflicts); P·V: each thread owns fixed (head, element) outputs and reads the
+// probabilities of 4 slots at once.
 // =========================================================================
 
 // The combine of the Slow-AR split partials of KV head g (the last split to arrive): for each of
@@ -1337,7 +1341,7 @@ __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, 
   constexpr int CPS = RB / 16;                           // 16-byte chunks per row
   constexpr int OPT = 4 * HD / kConsumers;               // outputs per thread in P·V
   constexpr int DPL = HD / 32;
-  static_assert(RS <= 64 && EPS * static_cast<int>(sizeof(KT)) == 32, "attention round layout");
+  static_assert(RS <= 64 && EPS * static_cast<int>(sizeof(KT)) == 32 && EPS % 4 == 0, "attention round layout");
   const Dims& d = cp.d;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rep = S.attn_rep;
@@ -1440,19 +1444,24 @@ __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, 
         vst[so] = f_to_kv<KT>(vnew[tid]);
       }
       named_bar(1, kConsumers);
-      // ---- scores: slot ss, elements sp·EPS .. +EPS of each of the rep q heads
+      // ---- scores: slot ss, chunks sp + c·TPS (4 elements each) of each of the rep q heads
       {
-        float kf[EPS];
-        const uint4* kr = reinterpret_cast<const uint4*>(kst + (static_cast<size_t>(buf) * RS + ss) * HD + sp * EPS);
-        unpack_kv<KT>(kr[0], *reinterpret_cast<float(*)[16 / sizeof(KT)]>(&kf[0]));
-        unpack_kv<KT>(kr[1], *reinterpret_cast<float(*)[16 / sizeof(KT)]>(&kf[16 / sizeof(KT)]));
+        const KT* kr = kst + (static_cast<size_t>(buf) * RS + ss) * HD;
         float dot[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          if (h < rep) {
-            const float* q = qs + h * HD + sp * EPS;
+        for (int c = 0; c < EPS / 4; ++c) {
+          const int e0 = (c * TPS + sp) * 4;
+          float kf[4];
+          load4_kv<KT>(kr + e0, kf);
 #pragma unroll
-            for (int e = 0; e < EPS; ++e) dot[h] = fmaf(q[e], kf[e], dot[h]);
+          for (int h = 0; h < 4; ++h) {
+            if (h < rep) {
+              const float4 q = *reinterpret_cast<const float4*>(qs + h * HD + e0);
+              dot[h] = fmaf(q.x, kf[0], dot[h]);
+              dot[h] = fmaf(q.y, kf[1], dot[h]);
+              dot[h] = fmaf(q.z, kf[2], dot[h]);
+              dot[h] = fmaf(q.w, kf[3], dot[h]);
+            }
           }
         }
 #pragma unroll
@@ -1487,8 +1496,25 @@ __device__ __noinline__ void attn_slow_t(const CallParams& cp, const Phase& ph, 
         acc[j] *= h < rep ? stat[h] : 0.f;
       }
       const KT* vr = vst + static_cast<size_t>(buf) * RS * HD + oe;
-#pragma unroll 4
-      for (int sl = 0; sl < L; ++sl) {
+      const int L4 = L & ~3;
+#pragma unroll 2
+      for (int sl = 0; sl < L4; sl += 4) {
+        float v[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) v[t] = kv_to_f<KT>(vr[static_cast<size_t>(sl + t) * HD]);
+#pragma unroll
+        for (int j = 0; j < OPT; ++j) {
+          const int h = oh + j * (kConsumers / HD);
+          if (h < rep) {
+            const float4 p = *reinterpret_cast<const float4*>(ps + h * 64 + sl);
+            acc[j] = fmaf(p.x, v[0], acc[j]);
+            acc[j] = fmaf(p.y, v[1], acc[j]);
+            acc[j] = fmaf(p.z, v[2], acc[j]);
+            acc[j] = fmaf(p.w, v[3], acc[j]);
+          }
+        }
+      }
+      for (int sl = L4; sl < L; ++sl) {
         const float v = kv_to_f<KT>(vr[static_cast<size_t>(sl) * HD]);
 #pragma unroll
         for (int j = 0; j < OPT; ++j) {
