@@ -24,11 +24,11 @@ if ROOT not in sys.path:
 
 METRIC = "codec frames/sec per stream & aggregate (S2-Pro shapes); HBM GB/s vs 8 TB/s"
 # DRAM bytes (read + write) over algorithmic bytes for one frame_kernel launch, from an ncu capture
-# of the same kernel on a smaller case (S2-Pro widths, 4 Slow-AR layers, 2 frames: 16.645 GB
+# of the same kernel on a smaller case (S2-Pro widths, 4 Slow-AR layers, 2 frames: 16.649 GB
 # measured against 16.611 GB algorithmic; the capture's summary is committed with the profiles).  Traffic grows
 # with the weights and KV streamed, so the full launch's traffic is this ratio times its
 # algorithmic bytes.  Set to None when the kernel changes until a new capture is taken.
-NCU_TRAFFIC_RATIO = None
+NCU_TRAFFIC_RATIO = 1.0023
 WORKLOAD = "full-frame Dual-AR decode, S2-Pro shapes (36+4 layers, dim 2560, vocab 155776), batch 1"
 PROMPT_LEN = 512
 
