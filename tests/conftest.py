@@ -13,6 +13,27 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "slow: long-running (full-size workloads)")
 
 
+def pytest_terminal_summary(terminalreporter):
+    """The parity statistics of the run (tests.parity.REPORT): per compared stream, the largest
+    max-abs-rel of the main logits, hidden state and Fast-AR logits against the oracle, the
+    tolerance, and the draws compared (pinned ones must be equal, the rest are teacher-forced).
+    With S2_PARITY_REPORT set, also written there as JSON."""
+    from tests import parity
+    if not parity.REPORT:
+        return
+    tr = terminalreporter
+    tr.write_sep("-", "parity with the oracle (max-abs-rel; draws pinned / compared)")
+    for r in parity.REPORT:
+        tr.write_line(f"{r['test']} [stream {r['stream']}]: logits {r['logit_err']:.2e}  hidden {r['hidden_err']:.2e}  "
+                      f"fast {r['fast_err']:.2e}  (tol {r['tol']:.0e}); frames {r['frames']}, "
+                      f"draws {r['pinned']} / {r['draws']}")
+    path = os.environ.get("S2_PARITY_REPORT")
+    if path:
+        import json
+        with open(path, "w") as f:
+            json.dump(parity.REPORT, f, indent=1)
+
+
 def pytest_collection_modifyitems(config, items):
     try:
         import torch

@@ -1,5 +1,14 @@
-"""Comparison helpers for CUDA-path vs oracle parity (test support, no arithmetic of the method)."""
+"""Comparison helpers for CUDA-path vs oracle parity (test support, no arithmetic of the method).
+
+Every ``compare_frames`` call records its statistics in ``REPORT`` (with the test that made it);
+``tests/conftest.py`` prints them at the end of the run, so the measured errors of each
+configuration stay visible while they are within tolerance, and a drift shows before it fails.
+"""
+import os
+
 import numpy as np
+
+REPORT = []  # one dict per compare_frames call: test, stream and the statistics it returned
 
 
 def max_abs_rel(g, r):
@@ -67,4 +76,5 @@ def compare_frames(ref, out, d, s, tol, stream=0, check_draws=True):
                 assert int(dr[f, k]) == int(gd), f"frame {f} draw {k}: GPU {dr[f, k]} vs oracle {gd} (pinned)"
             else:
                 stats["unpinned"] += 1
+    REPORT.append(dict(test=os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0], stream=stream, tol=tol, **stats))
     return stats
