@@ -23,15 +23,18 @@ def pytest_terminal_summary(terminalreporter):
         return
     tr = terminalreporter
     tr.write_sep("-", "parity with the oracle (max-abs-rel; draws pinned / compared)")
-    for r in parity.REPORT:
-        tr.write_line(f"{r['test']} [stream {r['stream']}]: logits {r['logit_err']:.2e}  hidden {r['hidden_err']:.2e}  "
-                      f"fast {r['fast_err']:.2e}  (tol {r['tol']:.0e}); frames {r['frames']}, "
-                      f"draws {r['pinned']} / {r['draws']}")
-    path = os.environ.get("S2_PARITY_REPORT")
-    if path:
-        import json
-        with open(path, "w") as f:
-            json.dump(parity.REPORT, f, indent=1)
+    try:
+        for r in parity.REPORT:
+            tr.write_line(f"{r['test']} [stream {r['stream']}]: logits {r['logit_err']:.2e}  "
+                          f"hidden {r['hidden_err']:.2e}  fast {r['fast_err']:.2e}  (tol {r['tol']:.0e}); "
+                          f"frames {r['frames']}, draws {r['pinned']} / {r['draws']}")
+        path = os.environ.get("S2_PARITY_REPORT")
+        if path:
+            import json
+            with open(path, "w") as f:
+                json.dump(parity.REPORT, f, indent=1)
+    except Exception as e:  # a report problem must not change the run's outcome
+        tr.write_line(f"(parity report incomplete: {e!r})")
 
 
 def pytest_collection_modifyitems(config, items):
