@@ -236,7 +236,7 @@ __device__ __forceinline__ unsigned long long tagw(uint32_t bits, uint32_t tag) 
 // Polled words are read with relaxed loads at GPU scope (morally strong): a weak load in a polling
 // loop has no visibility guarantee, and on this two-die part it was seen to keep returning a stale
 // copy of a word for a second after the word had been stored.
-__device__ __forceinline__ ulonglong2 ldcg_u64x2(const unsigned long long* p) {
+__device__ __forceinline__ ulonglong2 ld_relaxed_u64x2(const unsigned long long* p) {
   ulonglong2 v;
   asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p));
   return v;
@@ -256,7 +256,7 @@ __device__ __forceinline__ void wait_tagged(const CallParams& cp, Smem& S, const
 #pragma unroll
     for (int i = 0; i < N; ++i)
       if (miss & (1u << i)) {
-        v[i] = ldcg_u64x2(p[i]);
+        v[i] = ld_relaxed_u64x2(p[i]);
         if (tags_are(v[i], tag)) miss &= ~(1u << i);
       }
     if (miss != 0u && (it & 15u) == 0u) {
@@ -278,7 +278,7 @@ __device__ __noinline__ void wait_tagged_nl(const CallParams& cp, Smem& S, const
 #pragma unroll
     for (int i = 0; i < N; ++i)
       if (miss & (1u << i)) {
-        v[i] = ldcg_u64x2(p[i]);
+        v[i] = ld_relaxed_u64x2(p[i]);
         if (tags_are(v[i], tag)) miss &= ~(1u << i);
       }
     if (miss != 0u && (it & 15u) == 0u) {
@@ -305,7 +305,7 @@ __device__ __forceinline__ void qkv_issue(const Phase& ph, size_t e, QkvWords<DP
   if (ph.qkv_tag_back > 0) {
     t.p = reinterpret_cast<const unsigned long long*>(ph.qkv) + e;
 #pragma unroll
-    for (int i = 0; i < DPL / 2; ++i) t.w[i] = ldcg_u64x2(t.p + 2 * i);
+    for (int i = 0; i < DPL / 2; ++i) t.w[i] = ld_relaxed_u64x2(t.p + 2 * i);
   } else {
 #pragma unroll
     for (int j = 0; j < DPL; ++j) v[j] = ldcg(ph.qkv + e + j);
@@ -771,8 +771,8 @@ __device__ __noinline__ Pipe gemv_mma(const CallParams& cp, const Phase& ph, Sme
         const int g = min(tid + kConsumers * j, ng - 1);
         ptr[2 * j] = src + 4 * g;
         ptr[2 * j + 1] = src + 4 * g + 2;
-        w[2 * j] = ldcg_u64x2(ptr[2 * j]);
-        w[2 * j + 1] = ldcg_u64x2(ptr[2 * j + 1]);
+        w[2 * j] = ld_relaxed_u64x2(ptr[2 * j]);
+        w[2 * j + 1] = ld_relaxed_u64x2(ptr[2 * j + 1]);
       }
 #pragma unroll
       for (int i = 0; i < 2 * GM; ++i)
@@ -1132,7 +1132,7 @@ __device__ __noinline__ Pipe gemv_planes(const CallParams& cp, const Phase& ph, 
 #pragma unroll
         for (int i = 0; i < B; ++i) {
           ptr[i] = src + 2 * min(base + i * kConsumers, npairs - 1);
-          w[i] = ldcg_u64x2(ptr[i]);
+          w[i] = ld_relaxed_u64x2(ptr[i]);
         }
 #pragma unroll
         for (int i = 0; i < B; ++i)
