@@ -185,7 +185,12 @@ int s2_fast_logits(s2_ctx* ctx, int n_frames, const float* hidden, const int32_t
                    struct CUstream_st* stream);
 
 /* Synchronise `stream` and report device-side failures of earlier calls (S2_ETIMEOUT) or
- * S2_OK; clears the recorded failure. */
+ * S2_OK; clears the recorded failure.  After S2_ETIMEOUT, s2_last_error names the wait that gave
+ * up first: its site, the CTA and the index of the phase in the launch's program.  Sites of the
+ * persistent kernel: 1 grid barrier; 2 weight loader waiting for a free ring stage; 3 weight
+ * loader draining its copies at exit; 4, 5 a projection waiting for its weight stage; 6 the bulk
+ * copy of a projection input; 7 draining those copies; 8 a poll of tagged words.  Site 10: a wait
+ * of the batched engine's kernels (no CTA or phase reported). */
 int s2_sync_status(s2_ctx* ctx, struct CUstream_st* stream);
 
 /* Testing hook: bound on device-side spin waits, in units of ~1 µs (0 restores the default of
